@@ -1,0 +1,409 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here touches a GPU.  Each test checks the oracle against something
+other than itself: a value the pages print (fixtures in tests/golden/, each
+with its citation), a closed form, an invariant, a library routine
+(torch scaled_dot_product_attention / logsumexp / float8 casts in fp64), or
+brute force on tiny inputs.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ maps
+
+
+def test_zigzag_cp4_16_tokens_matches_page():
+    g = golden("zigzag_cp4_16tokens.json")
+    plan = oracle.zigzag_plan(g["new_len"], g["prefix_len"], g["C"])
+    assert [sorted(o) for o in plan["order"]] == g["rank_tokens"]
+    for b, e in oracle.zigzag_block_bounds(16, 4):
+        assert e - b == g["tokens_per_block"]
+
+
+def test_interleave_cp4_16_tokens_matches_page():
+    g = golden("interleave_cp4_16tokens.json")
+    plan = oracle.interleave_plan(g["new_len"], g["prefix_len"], g["C"])
+    assert plan["order"] == g["rank_tokens"]
+
+
+def test_interleave_batch_5_3_matches_page():
+    g = golden("interleave_batch_5_3.json")
+    plan = oracle.interleave_plan(g["new_len"], g["prefix_len"], g["C"])
+    p = g["printed"]
+    assert plan["order"][0] == p["rank0"]
+    assert plan["order"][1] == p["rank1"]
+    i5 = plan["order"][1].index(5)
+    assert plan["req"][1][i5] == p["index5_request"]
+    assert plan["pos"][1][i5] == p["index5_offset_in_request"]
+    # the index does not reset at the request boundary
+    assert plan["order"][2] == [2, 6] and plan["order"][3] == [3, 7]
+    # positions keep their original values within each request
+    assert plan["pos"][2] == [2, 1] and plan["req"][2] == [0, 1]
+
+
+def test_consecutive_split_pairs_match_page():
+    g = golden("consecutive_split_pairs_16tokens_4gpus.json")
+    pairs = oracle.consecutive_split_pairs(g["n"], g["C"])
+    assert pairs[0] == g["gpu0_pairs"] and pairs[-1] == g["gpu3_pairs"]
+    assert pairs == [10, 26, 42, 58]
+    # the long-prompt limit of last/first is 2C-1
+    big = oracle.consecutive_split_pairs(4 * 4096, 4)
+    assert abs(big[-1] / big[0] - g["ratio_formula_long_prompt"]) < 0.01
+
+
+def brute_pairs(owner_of_token, C):
+    """Pairs per rank by brute force: count (q, k) with k <= q."""
+    out = [0] * C
+    for qpos, r in enumerate(owner_of_token):
+        for k in range(qpos + 1):
+            out[r] += 1
+    return out
+
+
+def test_pair_counts_16_tokens_cp4_brute_force():
+    zz = oracle.zigzag_plan([16], [0], 4)
+    il = oracle.interleave_plan([16], [0], 4)
+    for plan in (zz, il):
+        owner = [None] * 16
+        for r in range(4):
+            for f in plan["order"][r]:
+                owner[f] = r
+        assert oracle.pairs_per_rank(plan) == brute_pairs(owner, 4)
+    # zigzag balances exactly, interleave nearly
+    assert oracle.pairs_per_rank(zz) == [34, 34, 34, 34]
+    assert oracle.pairs_per_rank(il) == [28, 32, 36, 40]
+
+
+def test_zigzag_block_units_equal_2C():
+    # block b reads the b blocks before it plus half of itself: b + 1/2 units;
+    # in units of (block queries x block keys) the exact pair count of block b
+    # with blocks of size s is s*s*b + s*(s+1)/2.
+    g = golden("long_prompt_counts.json")
+    for C in (2, 4, 8):
+        s = 1024
+        plan = oracle.zigzag_plan([2 * C * s], [0], C)
+        pairs = oracle.pairs_per_rank(plan)
+        assert len(set(pairs)) == 1
+        units = pairs[0] / (s * s)
+        assert abs(units - 2 * C) < 2.0 / s
+    assert g["zigzag_units_C4"] == 2 * 4
+
+
+def test_long_prompt_closed_forms():
+    g = golden("long_prompt_counts.json")
+    n = g["n"]
+    # about N^2/2 pairs for the whole prompt
+    total = n * (n + 1) // 2
+    assert round(total / 1e9, 1) == g["pairs_billion_rounded"]
+    il = oracle.interleave_plan_np([n], [0], g["interleave_C"])
+    pairs = [int((p + 1).sum()) for p in il["pos"]]
+    assert sum(pairs) == total
+    excess = (max(pairs) - total / g["interleave_C"]) / (total / g["interleave_C"]) * 100
+    assert 0.005 < excess < 0.02  # "about 0.01%"
+
+
+def test_maps_are_partitions_with_prefix_and_ragged_batch():
+    rng = np.random.default_rng(0)
+    for C in (1, 2, 3, 4, 8):
+        new = [int(x) for x in rng.integers(0, 40, size=5)]
+        pre = [int(x) for x in rng.integers(0, 30, size=5)]
+        T = sum(new)
+        for plan in (oracle.zigzag_plan(new, pre, C), oracle.interleave_plan(new, pre, C)):
+            allf = sorted(f for r in range(C) for f in plan["order"][r])
+            assert allf == list(range(T))
+            # every query's position is prefix + its offset in its request
+            starts = np.concatenate([[0], np.cumsum(new)[:-1]])
+            for r in range(C):
+                for f, j, p in zip(plan["order"][r], plan["req"][r], plan["pos"][r]):
+                    assert starts[j] <= f < starts[j] + new[j]
+                    assert p == pre[j] + (f - starts[j])
+
+
+def test_zigzag_remainder_and_kv_lengths():
+    # 19 tokens, C=4: 8 blocks of 2, the first 3 blocks get one more
+    b = oracle.zigzag_block_bounds(19, 4)
+    assert [e - s for s, e in b] == [3, 3, 3, 2, 2, 2, 2, 2]
+    plan = oracle.zigzag_plan([19], [7], 4)
+    for (r, j, which, blk, qs, ql, kvl) in plan["blocks"]:
+        assert blk == (r if which == 0 else 7 - r)
+        assert (qs, qs + ql) == b[blk]
+        assert kvl == 7 + b[blk][1]  # reads end where the block ends, prefix included
+    # fewer tokens than blocks: some blocks are empty
+    b = oracle.zigzag_block_bounds(3, 4)
+    assert [e - s for s, e in b] == [1, 1, 1, 0, 0, 0, 0, 0]
+
+
+def test_interleave_np_matches_loop():
+    rng = np.random.default_rng(1)
+    for C in (1, 3, 8):
+        new = [int(x) for x in rng.integers(1, 50, size=6)]
+        pre = [int(x) for x in rng.integers(0, 20, size=6)]
+        a = oracle.interleave_plan(new, pre, C)
+        b = oracle.interleave_plan_np(new, pre, C)
+        for r in range(C):
+            assert list(a["order"][r]) == list(b["order"][r])
+            assert list(a["req"][r]) == list(b["req"][r])
+            assert list(a["pos"][r]) == list(b["pos"][r])
+
+
+def test_decode_slot_map_matches_page():
+    g = golden("decode_slot9_4gpus.json")
+    shard, row = oracle.decode_shard_map(g["slot"] + 1, g["C"])
+    assert shard[g["slot"]] == g["gpu"] and row[g["slot"]] == g["row"]
+    # shards partition the tokens; shard r holds ceil((L - r)/C) rows
+    for L in (0, 1, 5, 257):
+        for C in (1, 4, 8):
+            shard, row = oracle.decode_shard_map(L, C)
+            for r in range(C):
+                rows = [row[p] for p in range(L) if shard[p] == r]
+                assert rows == list(range(len(rows)))
+                assert len(rows) == max(0, -(-(L - r) // C))
+
+
+# ------------------------------------------------------------------ fp8
+
+
+def test_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = oracle.e4m3_decode(np.arange(256))
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(ref[~nan], ours[~nan])
+    assert oracle.e4m3_to_float(0x7E) == 448.0
+    assert oracle.e4m3_to_float(0x01) == 2.0 ** -9
+
+
+# ------------------------------------------------------------------ attention
+
+
+def sdpa_causal_ref(q, k, v, pos, scale):
+    """torch SDPA in fp64 with a boolean mask: key j readable iff j <= pos."""
+    n, Hq, D = q.shape
+    L, Hkv, _ = k.shape
+    g = Hq // Hkv
+    qt = torch.from_numpy(q).permute(1, 0, 2)  # [Hq, n, D]
+    kt = torch.from_numpy(k).repeat_interleave(g, dim=1).permute(1, 0, 2)
+    vt = torch.from_numpy(v).repeat_interleave(g, dim=1).permute(1, 0, 2)
+    mask = torch.arange(L)[None, :] <= torch.from_numpy(np.asarray(pos))[:, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+    s = (qt @ kt.transpose(1, 2)) * scale
+    s = s.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy()
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,n,pre", [(4, 1, 8, 13, 0), (8, 2, 16, 11, 5), (6, 3, 4, 1, 0)])
+def test_causal_rows_vs_torch_sdpa(Hq, Hkv, D, n, pre):
+    rng = np.random.default_rng(Hq * 100 + n)
+    L = pre + n
+    q = rng.standard_normal((n, Hq, D))
+    k = rng.standard_normal((L, Hkv, D))
+    v = rng.standard_normal((L, Hkv, D))
+    pos = np.arange(pre, pre + n)
+    scale = 1 / math.sqrt(D)
+    o, lse = oracle.causal_rows(q, k, v, pos, scale)
+    o_ref, lse_ref = sdpa_causal_ref(q, k, v, pos, scale)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_causal_rows_brute_force_python():
+    """Pure-Python probability table on a tiny case (no numpy algebra)."""
+    rng = np.random.default_rng(7)
+    n, Hq, Hkv, D = 5, 2, 1, 3
+    q = rng.standard_normal((n, Hq, D))
+    k = rng.standard_normal((n, Hkv, D))
+    v = rng.standard_normal((n, Hkv, D))
+    o, lse = oracle.causal_rows(q, k, v, np.arange(n), 0.7)
+    for i in range(n):
+        for h in range(Hq):
+            w = [math.exp(0.7 * sum(q[i, h, d] * k[j, 0, d] for d in range(D))) for j in range(i + 1)]
+            Z = sum(w)
+            for d in range(D):
+                assert abs(o[i, h, d] - sum(w[j] * v[j, 0, d] for j in range(i + 1)) / Z) < 1e-12
+            assert abs(lse[i, h] - math.log(Z)) < 1e-12
+
+
+def test_single_key_and_identical_keys():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 2, 4))
+    k = rng.standard_normal((1, 1, 4))
+    v = rng.standard_normal((1, 1, 4))
+    o, lse = oracle.causal_rows(q, k, v, [0], 0.5)
+    for h in range(2):
+        np.testing.assert_allclose(o[0, h], v[0, 0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[0, h], 0.5 * q[0, h] @ k[0, 0], rtol=0, atol=1e-14)
+    # n identical keys: O = mean(v), LSE = s + ln n
+    n = 9
+    k = np.repeat(k, n, axis=0)
+    v = rng.standard_normal((n, 1, 4))
+    o, lse = oracle.decode_attention(q[0], k, v, 0.5)
+    for h in range(2):
+        np.testing.assert_allclose(o[h], v[:, 0].mean(axis=0), atol=1e-14)
+        np.testing.assert_allclose(lse[h], 0.5 * q[0, h] @ k[0, 0] + math.log(n), atol=1e-13)
+
+
+def test_decode_attention_vs_torch_and_gqa_mapping():
+    rng = np.random.default_rng(11)
+    H, Hkv, D, L = 8, 2, 6, 37
+    q = rng.standard_normal((H, D))
+    k = rng.standard_normal((L, Hkv, D))
+    v = rng.standard_normal((L, Hkv, D + 2))
+    o, lse = oracle.decode_attention(q, k, v, 0.3)
+    for h in range(H):
+        kh = h // (H // Hkv)  # consecutive grouping
+        s = torch.from_numpy(0.3 * (k[:, kh] @ q[h]))
+        ref_lse = torch.logsumexp(s, 0).item()
+        ref_o = (torch.softmax(s, 0) @ torch.from_numpy(v[:, kh])).numpy()
+        assert abs(lse[h] - ref_lse) < 1e-12
+        np.testing.assert_allclose(o[h], ref_o, atol=1e-12)
+    # empty key set
+    o, lse = oracle.decode_attention(q, k[:0], v[:0], 0.3)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def test_mla_cache_split():
+    rng = np.random.default_rng(5)
+    lat = rng.standard_normal((7, 576))
+    sc = rng.random(7) + 0.5
+    K, V = oracle.mla_cache_to_kv(lat, sc)
+    assert K.shape == (7, 1, 576) and V.shape == (7, 1, 512)
+    np.testing.assert_array_equal(K[:, 0, :512], V[:, 0])
+    np.testing.assert_allclose(K[:, 0, 575], lat[:, 575] * sc)
+
+
+# ------------------------------------------------------------------ merge
+
+
+def test_figure8_merge_values():
+    g = golden("figure8_merge.json")
+    e = np.array(g["exp_scores"], dtype=np.float64)
+    s = np.log(e)[None, :]  # scores whose exponentials are 4, 2, 1, 1
+    v = np.eye(4)  # value j = unit vector j, so O = probabilities
+    o, lse = oracle.softmax_attention(s, v)
+    np.testing.assert_allclose(o[0], g["global_probs"], atol=1e-15)
+    parts_o, parts_lse = [], []
+    for toks, lp, ls in zip(g["gpu_tokens"], g["local_probs"], g["local_sums"]):
+        op, lsep = oracle.softmax_attention(s[:, toks], v[toks])
+        np.testing.assert_allclose(op[0][toks], lp, atol=1e-15)
+        assert abs(lsep[0] - math.log(ls)) < 1e-15
+        parts_o.append(op)
+        parts_lse.append(lsep)
+    o_m, lse_m = oracle.lse_merge(np.stack(parts_o), np.stack(parts_lse))
+    np.testing.assert_allclose(o_m[0], g["global_probs"], atol=1e-15)
+    assert abs(lse_m[0] - math.log(8)) < 1e-15
+    # the scale of each GPU is exp(LSE_p - global LSE)
+    for lsep, sc in zip(parts_lse, g["scales"]):
+        assert abs(math.exp(lsep[0] - lse_m[0]) - sc) < 1e-15
+
+
+def test_merge_over_every_two_way_partition_equals_unsharded():
+    rng = np.random.default_rng(21)
+    n, H, Dv = 10, 3, 5
+    q = rng.standard_normal((H, 4)) * 2
+    k = rng.standard_normal((n, 1, 4))
+    v = rng.standard_normal((n, 1, Dv))
+    o_full, lse_full = oracle.decode_attention(q, k, v, 1.0)
+    for bits in itertools.product([0, 1], repeat=n):
+        sel = np.array(bits, dtype=bool)
+        parts = [oracle.decode_attention(q, k, v, 1.0, keys=np.nonzero(sel == b)[0]) for b in (0, 1)]
+        o, lse = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(o, o_full, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_full, atol=1e-13)
+
+
+def test_merge_random_multiway_partitions_and_shards():
+    rng = np.random.default_rng(22)
+    for trial in range(20):
+        L = int(rng.integers(1, 60))
+        P = int(rng.integers(1, 9))
+        q = rng.standard_normal((4, 8)) * 3
+        k = rng.standard_normal((L, 2, 8))
+        v = rng.standard_normal((L, 2, 7))
+        o_full, lse_full = oracle.decode_attention(q, k, v, 0.5)
+        owner = rng.integers(0, P, size=L)
+        parts = [oracle.decode_attention(q, k, v, 0.5, keys=np.nonzero(owner == p)[0]) for p in range(P)]
+        o, lse = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+        np.testing.assert_allclose(o, o_full, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_full, atol=1e-12)
+        # the token-sharded partials (p mod C) merge to the same result
+        po, pl = oracle.decode_shard_partials(q, k, v, P, 0.5)
+        o2, l2 = oracle.lse_merge(po, pl)
+        np.testing.assert_allclose(o2, o_full, atol=1e-12)
+        np.testing.assert_allclose(l2, lse_full, atol=1e-12)
+
+
+def test_merge_all_empty_and_vs_torch_logsumexp():
+    o, lse = oracle.lse_merge(np.zeros((3, 2, 4)), np.full((3, 2), -np.inf))
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+    rng = np.random.default_rng(2)
+    lp = rng.standard_normal((5, 6)) * 10
+    lp[2, 3] = -np.inf
+    op = rng.standard_normal((5, 6, 3))
+    o, lse = oracle.lse_merge(op, lp)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.from_numpy(lp), dim=0).numpy(), atol=1e-12)
+
+
+# ------------------------------------------------------------------ planted mistakes
+
+
+def test_planted_mistakes_are_caught(monkeypatch):
+    """Plant plausible mistakes in copies of oracle steps and check that the
+    pins above would catch each of them."""
+    g = golden("zigzag_cp4_16tokens.json")
+
+    def wrong_pairing(new_len, prefix_len, C):  # rank r takes r and 2C-2-r
+        out = [[] for _ in range(C)]
+        bounds = oracle.zigzag_block_bounds(new_len[0], C)
+        for r in range(C):
+            for b in (r, (2 * C - 2 - r) % (2 * C)):
+                out[r] += list(range(*bounds[b]))
+        return out
+
+    assert [sorted(o) for o in wrong_pairing([16], [0], 4)] != g["rank_tokens"]
+
+    # a merge that drops the max shift overflows / a merge without weights is wrong
+    f8 = golden("figure8_merge.json")
+    s = np.log(np.array(f8["exp_scores"], float))[None, :]
+    v = np.eye(4)
+    parts = [oracle.softmax_attention(s[:, t], v[t]) for t in f8["gpu_tokens"]]
+    naive = sum(p[0] for p in parts)  # "just add the results"
+    assert not np.allclose(naive[0], f8["global_probs"])
+    # a transposed operand in the scores is caught by the SDPA pin
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((6, 2, 6))
+    k = rng.standard_normal((6, 1, 6))
+    vv = rng.standard_normal((6, 1, 6))
+    o_ref, _ = sdpa_causal_ref(q, k, vv, np.arange(6), 0.5)
+    qT = np.ascontiguousarray(np.transpose(q, (2, 1, 0)))
+    o_bad, _ = oracle.causal_rows(qT, k, vv, np.arange(6), 0.5)
+    assert not np.allclose(o_bad, o_ref)
+    # an off-by-one causal extent (reading keys < pos only) is caught
+    with monkeypatch.context() as m:
+        orig = oracle.causal_rows
+
+        def shifted(q, k, v, pos, sc):
+            return orig(q, k, v, np.maximum(np.asarray(pos) - 1, 0), sc)
+
+        m.setattr(oracle, "causal_rows", shifted)
+        o_bad, _ = oracle.causal_rows(q, k, vv, np.arange(6), 0.5)
+        assert not np.allclose(o_bad, o_ref)
