@@ -1,0 +1,64 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn.h"
+
+namespace cpattn {
+
+constexpr int kHeaderWords = (int)(sizeof(cp_plan_header) / 4);
+constexpr int kSegWords = (int)(sizeof(cp_seg_desc) / 4);
+constexpr int kPairWords = (int)(sizeof(cp_pair_desc) / 4);
+constexpr int kWorkWords = (int)(sizeof(cp_work_desc) / 4);
+constexpr int kPrefillTileRows = 128;  // queries per prefill tile (MMA M)
+constexpr int kDecodeTileRows = 128;   // KV rows per decode scheduling tile (MMA M)
+
+// Device status word layout (written by kernels, read by cp_device_error_check).
+//   [0] non-zero once any bounded wait gave up
+//   [1] kernel id   [2] wait site   [3] block index
+enum KernelId : unsigned { kKernPrefillTc = 1, kKernDecodeMlaTc = 2 };
+
+struct ShardPtrs {
+  const void* p[CP_MAX_SHARDS];
+};
+struct ScalePtrs {
+  const float* p[CP_MAX_SHARDS];
+};
+struct MutShardPtrs {
+  void* p[CP_MAX_SHARDS];
+};
+struct MutScalePtrs {
+  float* p[CP_MAX_SHARDS];
+};
+
+// Returns the device address of this device's status words (set up once per device).
+unsigned* device_status_ptr();
+
+// ---- plan / pack / merge kernels (plan_kernels.cu)
+cudaError_t launch_plan_maps(const int32_t* dev_plan, int n_seg, int off_seg, int off_idx,
+                             int off_qpos, int off_qreq, cudaStream_t s);
+cudaError_t launch_kv_pack(const int32_t* dev_plan, const cp_plan_header& h, int elem_bytes,
+                           const void* kv, const float* kv_scale, int row_elems,
+                           const MutShardPtrs& dst, const MutScalePtrs& dst_scale, bool has_scale,
+                           cudaStream_t s);
+cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
+                             const float* lse_part, void* o, bool o_bf16, float* lse,
+                             cudaStream_t s);
+cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h, int H, int Dv,
+                                const float* ws_o, const float* ws_lse, float* o_part,
+                                float* lse_part, cudaStream_t s);
+
+// ---- CUDA-core attention (simt_attn.cu)
+cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h, int rank,
+                                int row_begin, int n_rows, bool bf16, const void* q,
+                                const void* k, const void* v, int Hq, int Hkv, int D,
+                                float sm_scale, void* o, float* lse, cudaStream_t s);
+cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h, bool mla,
+                               cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
+                               const ShardPtrs& v, const ScalePtrs& sc, int Hq, int Hkv, int Dqk,
+                               int Dv, float sm_scale, float* o_part, float* lse_part,
+                               float* ws_o, float* ws_lse, cudaStream_t s);
+
+}  // namespace cpattn

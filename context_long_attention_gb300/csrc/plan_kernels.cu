@@ -1,0 +1,176 @@
+// Index maps, token-shard packing and the exact log-sum-exp merge.
+//
+// * plan_map_kernel: per-query arrays of a prefill plan (flattened index,
+//   position, request) from its segments — zigzag blocks or interleave runs
+//   ("How GPUs Share a Long Context During LLM Inference", §2.3-2.4).
+// * kv_pack_kernel: token p of a request -> shard p mod C, row p / C (§3.1).
+// * lse_merge_kernel / decode_fixup_kernel: O = sum_p w_p O_p / sum_p w_p
+//   with w_p = exp(LSE_p - max LSE) (§3.3; "DeepSeek-V4 Attention Inference
+//   Systems" §5), one warp per (row, head), 128-bit loads.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace cpattn {
+namespace {
+
+__global__ void plan_map_kernel(int32_t* __restrict__ plan, int off_seg, int off_idx, int off_qpos,
+                                int off_qreq) {
+  const cp_seg_desc s = reinterpret_cast<const cp_seg_desc*>(plan + off_seg)[blockIdx.x];
+  int32_t* idx = plan + off_idx;
+  int32_t* qpos = plan + off_qpos;
+  int32_t* qreq = plan + off_qreq;
+  for (int i = threadIdx.x; i < s.count; i += blockDim.x) {
+    const int row = s.local_start + i;
+    idx[row] = s.first_f + i * s.stride;
+    qpos[row] = s.first_pos + i * s.stride;
+    qreq[row] = s.req;
+  }
+}
+
+// One warp per token row.  The request of token t is the last b with
+// first_token[b] <= t (requests of length 0 share their start with the next).
+__global__ void kv_pack_kernel(const int32_t* __restrict__ plan, int C, int B, int T,
+                               int off_pair, int off_req, const uint4* __restrict__ kv,
+                               const float* __restrict__ kv_scale, int row_vec,
+                               MutShardPtrs dst, MutScalePtrs dst_scale, int has_scale) {
+  const int warps = blockDim.x >> 5;
+  const long long t = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int32_t* req = plan + off_req;  // [B][2] {ctx_len, first token}
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (req[2 * mid + 1] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int p = (int)(t - req[2 * b + 1]);
+  const int r = p % C;
+  const cp_pair_desc* pair = reinterpret_cast<const cp_pair_desc*>(plan + off_pair);
+  const long long row = (long long)pair[r * B + b].row_off + p / C;
+  const uint4* src = kv + t * row_vec;
+  uint4* out = static_cast<uint4*>(dst.p[r]) + row * row_vec;
+  for (int c = lane; c < row_vec; c += 32) out[c] = src[c];
+  if (has_scale && lane == 0) dst_scale.p[r][row] = kv_scale[t];
+}
+
+// Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride.
+__device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, long long ostride,
+                                          const float* __restrict__ l, long long lstride, int Dv,
+                                          float* out_f32, __nv_bfloat16* out_bf16, float* out_lse) {
+  const int lane = threadIdx.x & 31;
+  float l0 = lane < P ? l[lane * lstride] : -INFINITY;
+  float l1 = lane + 32 < P ? l[(lane + 32) * lstride] : -INFINITY;
+  float g = fmaxf(l0, l1);
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, d));
+  const bool any = g != -INFINITY;
+  const float w0 = (any && l0 != -INFINITY) ? expf(l0 - g) : 0.f;
+  const float w1 = (any && l1 != -INFINITY) ? expf(l1 - g) : 0.f;
+  float z = w0 + w1;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
+  const float inv = any ? 1.f / z : 0.f;
+  for (int c = lane; c < Dv / 4; c += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < P; ++p) {
+      const float w = __shfl_sync(0xffffffffu, p < 32 ? w0 : w1, p & 31);
+      if (w != 0.f) {
+        const float4 x = reinterpret_cast<const float4*>(o + p * ostride)[c];
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+      }
+    }
+    acc.x *= inv;
+    acc.y *= inv;
+    acc.z *= inv;
+    acc.w *= inv;
+    if (out_f32) {
+      reinterpret_cast<float4*>(out_f32)[c] = acc;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 u;
+      u.x = *reinterpret_cast<unsigned*>(&a);
+      u.y = *reinterpret_cast<unsigned*>(&b);
+      reinterpret_cast<uint2*>(out_bf16)[c] = u;
+    }
+  }
+  if (out_lse && lane == 0) *out_lse = any ? g + logf(z) : -INFINITY;
+}
+
+__global__ void lse_merge_kernel(int P, long long NH, int Dv, const float* __restrict__ o_part,
+                                 const float* __restrict__ lse_part, void* __restrict__ o,
+                                 int o_bf16, float* __restrict__ lse) {
+  const long long i = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= NH) return;
+  float* of = o_bf16 ? nullptr : static_cast<float*>(o) + i * Dv;
+  __nv_bfloat16* ob = o_bf16 ? static_cast<__nv_bfloat16*>(o) + i * Dv : nullptr;
+  merge_row(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, of, ob, lse ? lse + i : nullptr);
+}
+
+__global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
+                                    int off_split, int n_split, int H, int Dv,
+                                    const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                    float* __restrict__ o_part, float* __restrict__ lse_part) {
+  const long long i = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= (long long)n_split * H) return;
+  const int s = (int)(i / H), h = (int)(i % H);
+  const int pair = plan[off_split + s];
+  const cp_pair_desc d = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[pair];
+  const long long ob = (long long)pair * H + h;
+  merge_row(d.n_parts, ws_o + ((long long)d.first_part * H + h) * Dv, (long long)H * Dv,
+            ws_lse + (long long)d.first_part * H + h, H, Dv, o_part + ob * Dv, nullptr,
+            lse_part + ob);
+}
+
+}  // namespace
+
+cudaError_t launch_plan_maps(const int32_t* dev_plan, int n_seg, int off_seg, int off_idx,
+                             int off_qpos, int off_qreq, cudaStream_t s) {
+  if (n_seg == 0) return cudaSuccess;
+  plan_map_kernel<<<n_seg, 256, 0, s>>>(const_cast<int32_t*>(dev_plan), off_seg, off_idx, off_qpos,
+                                        off_qreq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_pack(const int32_t* dev_plan, const cp_plan_header& h, int elem_bytes,
+                           const void* kv, const float* kv_scale, int row_elems,
+                           const MutShardPtrs& dst, const MutScalePtrs& dst_scale, bool has_scale,
+                           cudaStream_t s) {
+  const int row_vec = row_elems * elem_bytes / 16;
+  const int warps = 8;
+  const long long blocks = ((long long)h.T + warps - 1) / warps;
+  kv_pack_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(dev_plan, h.C, h.R, h.T, h.off_rank,
+                                                         h.off_tiles, static_cast<const uint4*>(kv),
+                                                         kv_scale, row_vec, dst, dst_scale,
+                                                         has_scale ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
+                             const float* lse_part, void* o, bool o_bf16, float* lse,
+                             cudaStream_t s) {
+  const long long NH = (long long)N * H;
+  const int warps = 8;
+  const long long blocks = (NH + warps - 1) / warps;
+  lse_merge_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(P, NH, Dv, o_part, lse_part, o,
+                                                           o_bf16 ? 1 : 0, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h, int H, int Dv,
+                                const float* ws_o, const float* ws_lse, float* o_part,
+                                float* lse_part, cudaStream_t s) {
+  const long long n = (long long)h.n_split * H;
+  if (n == 0) return cudaSuccess;
+  const int warps = 8;
+  decode_fixup_kernel<<<(unsigned)((n + warps - 1) / warps), warps * 32, 0, s>>>(
+      dev_plan, h.R, h.off_rank, h.off_rtile, h.n_split, H, Dv, ws_o, ws_lse, o_part, lse_part);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

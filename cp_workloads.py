@@ -174,3 +174,16 @@ def mla_decode_inputs(ctx, H=64, Dqk=576, seed=0, device="cpu", q_std=1.0, kv_st
         out["kv_fp8"] = codes
         out["kv_scale"] = scale
     return out
+
+
+def tiny_inputs(device="cpu", seed=SEEDS["tiny"]):
+    """The tiny workload: prefill Q/K/V of a 256-token prompt (fp32), then the
+    decode step of token 256, whose cache holds the 256 prompt entries plus
+    its own key and value (257 entries, token order)."""
+    w = WORKLOADS["tiny"]
+    q, k, v = prefill_inputs(w["new_len"], w["prefix_len"], w["Hq"], w["Hkv"], w["D"], w["dtype"],
+                             seed=seed, device=device)
+    dq, dk, dv = gqa_decode_inputs(1, [1], w["Hq"], w["Hkv"], w["D"], w["dtype"], seed=seed + 1,
+                                   device=device)
+    return {"q": q, "k": k, "v": v, "dec_q": dq, "dec_k": torch.cat([k, dk]),
+            "dec_v": torch.cat([v, dv]), "ctx": [w["decode_ctx"]]}

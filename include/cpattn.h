@@ -1,0 +1,303 @@
+/*
+ * cpattn.h — context-parallel attention on one GPU (sm_103a), C ABI.
+ *
+ * The library computes the data-parallel hot path of context parallelism for
+ * long-context LLM inference, with C *virtual* shards executed as
+ * independent partitions on one GPU:
+ *
+ *   cp_shard_plan      prompt-token shard maps (zigzag, interleave)
+ *   cp_decode_plan     decode KV-cache token shards + split-KV schedule
+ *   cp_prefill_attn    causal GQA prefill per shard, emitting (O, LSE)
+ *   cp_kv_shard_pack   gather a token-ordered cache into token shards
+ *   cp_decode_attn     one decode query per request against each shard,
+ *                      emitting per-shard partial (O, LSE)
+ *   cp_lse_merge       exact log-sum-exp combine of partial results
+ *
+ * Sources (page title, section):
+ *   [CTX] "How GPUs Share a Long Context During LLM Inference"
+ *   [SGL] SGLang documentation, "Prefill context parallelism"
+ *   [V4]  "DeepSeek-V4 Attention Inference Systems", §5
+ *   [GLM] vLLM blog "GLM-5.3 Part 2: PCP, DCP and Hybrid HiSparse on 16 H200"
+ *   [DCP] vLLM blog on Decode Context Parallelism, §4.1 and §5.3
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Ownership: the caller allocates every host and device buffer; the
+ *   library never allocates memory and never synchronises the device, except
+ *   cp_device_error_check(), which reads a device status word.
+ * - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *   default stream).  All device work is enqueued on it, in order.
+ * - Errors: every entry point validates its arguments on the host and returns
+ *   a cp_status before launching anything; on error nothing is enqueued and
+ *   cp_last_error() returns a message for the calling thread.
+ * - LSE is the natural logarithm of the sum of exponentiated (scaled)
+ *   scores ([CTX] §3.3).  An empty key set has O = 0 and LSE = -inf.
+ * - Tensors are dense, row-major, with the innermost dimension last.
+ *   Device pointers must be 16-byte aligned.
+ * - Kernels never wait without a bound: an mbarrier wait that runs past its
+ *   iteration limit sets a device status word and the kernel returns;
+ *   cp_device_error_check() then reports CP_ERR_DEVICE_TIMEOUT.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CPATTN_VERSION 1
+#define CP_PLAN_MAGIC 0x4c504350 /* 'CPPL' */
+#define CP_MAX_SHARDS 64         /* C limit: per-shard pointers travel as kernel arguments */
+
+typedef enum {
+  CP_OK = 0,
+  CP_ERR_INVALID_ARG = -1,    /* a null pointer, a bad size, a misaligned pointer */
+  CP_ERR_UNSUPPORTED = -2,    /* a valid combination this build does not implement */
+  CP_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed (message has details) */
+  CP_ERR_DEVICE_TIMEOUT = -4, /* a kernel gave up a bounded wait (see cp_device_error_check) */
+  CP_ERR_WORKSPACE = -5       /* the workspace passed is too small */
+} cp_status;
+
+typedef enum { CP_ZIGZAG = 0, CP_INTERLEAVE = 1 } cp_strategy;
+typedef enum { CP_BF16 = 0, CP_FP32 = 1, CP_FP8_E4M3 = 2 } cp_dtype;
+typedef enum { CP_DECODE_GQA = 0, CP_DECODE_MLA = 1 } cp_decode_mode;
+
+/* ---------------------------------------------------------------------------
+ * Plan layout.  A plan is an array of int32 words: a cp_plan_header, then
+ * tables at the word offsets the header gives.  The host part (header and
+ * tables) is written by the host into `host_plan` and copied, in stream
+ * order, to the front of `dev_plan`; per-token arrays exist only in
+ * `dev_plan` and are written there by a device kernel.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  int32_t magic;      /* CP_PLAN_MAGIC */
+  int32_t kind;       /* 0 zigzag prefill, 1 interleave prefill, 2 decode */
+  int32_t C;          /* number of virtual shards (ranks) */
+  int32_t R;          /* number of requests */
+  int32_t T;          /* prefill: total new tokens; decode: total cached tokens */
+  int32_t KV;         /* prefill: total K/V rows = sum(prefix + new); decode: 0 */
+  int32_t n_seg;      /* prefill: number of segments; decode: number of work items */
+  int32_t n_tiles;    /* prefill: number of 128-query tiles; decode: number of workers */
+  int32_t off_rank;   /* prefill: int32 rank_off[C+1]; decode: cp_pair_desc[C*R] */
+  int32_t off_req;    /* prefill: cp_req_desc[R]; decode: int32 worker_off[n_workers+1] */
+  int32_t off_seg;    /* prefill: cp_seg_desc[n_seg]; decode: cp_work_desc[n_seg] */
+  int32_t off_tiles;  /* prefill: cp_tile_desc[n_tiles], all ranks, longest first */
+  int32_t off_rtile;  /* prefill: int32 rank_tile_off[C+1] + cp_tile_desc[n_tiles] by rank */
+  int32_t off_idx;    /* prefill, device only: int32 idx[T]  (flattened new-token index) */
+  int32_t off_qpos;   /* prefill, device only: int32 qpos[T] (position incl. prefix) */
+  int32_t off_qreq;   /* prefill, device only: int32 qreq[T] (request of the query) */
+  int32_t host_words; /* words in the host part */
+  int32_t dev_words;  /* words in the device plan */
+  int32_t n_parts;    /* decode: partial slots in the workspace (split pairs) */
+  int32_t tile_rows;  /* decode: KV rows per scheduling tile (work boundaries) */
+  int32_t n_split;    /* decode: pairs covered by more than one work item */
+  int32_t reserved[3];
+} cp_plan_header;
+/* Decode plans reuse the table offsets: off_tiles -> int32 [R][2]
+ * {ctx_len, first token of the request in the token-ordered cache};
+ * off_rtile -> int32 split_pairs[n_split]. */
+
+/* One request of a prefill batch. */
+typedef struct {
+  int32_t new_len;    /* newly extended tokens (queries) */
+  int32_t prefix_len; /* cached prefix read by every query of the request */
+  int32_t q_base;     /* flattened index of the request's first new token */
+  int32_t kv_base;    /* first K/V row of the request (prefix, then new tokens) */
+} cp_req_desc;
+
+/* A run of one rank's queries inside one request: a zigzag block, or the
+ * C-strided interleave run.  Segments are ordered by (rank, local_start). */
+typedef struct {
+  int32_t rank;        /* owning virtual shard */
+  int32_t req;         /* request index */
+  int32_t block;       /* zigzag: block 0..2C-1; interleave: -1 */
+  int32_t which;       /* zigzag: 0 early block, 1 late block; interleave: 0 */
+  int32_t local_start; /* first row of the segment in the rank-major output */
+  int32_t count;       /* queries in the segment (q_len) */
+  int32_t first_f;     /* flattened new-token index of its first query */
+  int32_t stride;      /* flattened-index step between its queries: 1 or C */
+  int32_t q_start;     /* offset of its first query within the request's new tokens */
+  int32_t first_pos;   /* position of its first query, prefix included */
+  int32_t kv_len;      /* keys read by its last query (zigzag: prefix + block end);
+                          0 for an empty interleave run */
+  int32_t kv_base;     /* first K/V row of the request */
+} cp_seg_desc;
+
+/* A tile of up to 128 consecutive queries of one segment. */
+typedef struct {
+  int32_t seg;   /* segment index */
+  int32_t q_off; /* offset of the tile's first query within the segment */
+} cp_tile_desc;
+
+/* Decode: one (shard r, request b) pair; pair index = r * R + b. */
+typedef struct {
+  int32_t rows;       /* tokens of request b stored on shard r = ceil((L_b - r) / C) */
+  int32_t row_off;    /* first row of request b in shard r's cache */
+  int32_t ctx_len;    /* L_b, the request's cached tokens */
+  int32_t n_parts;    /* work items that cover this pair (>1: merged from the workspace) */
+  int32_t first_part; /* first workspace slot of this pair when n_parts > 1, else -1 */
+  int32_t reserved[3];
+} cp_pair_desc;
+
+/* Decode: a contiguous row range of one pair, processed by one worker. */
+typedef struct {
+  int32_t pair;      /* pair index */
+  int32_t row_begin; /* first row within the pair */
+  int32_t row_end;   /* one past the last row within the pair */
+  int32_t part;      /* workspace slot, or -1 when the item covers the whole pair */
+} cp_work_desc;
+
+/* ---------------------------------------------------------------------------
+ * Library state
+ * ------------------------------------------------------------------------- */
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* cp_last_error(void);
+
+/* CPATTN_VERSION of the loaded library. */
+int cp_version(void);
+
+/* Reads (and clears) the device status word that bounded waits set.  Blocks
+ * until `stream` has drained.  CP_OK, or CP_ERR_DEVICE_TIMEOUT with the
+ * failing kernel and wait site in cp_last_error(). */
+cp_status cp_device_error_check(void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_shard_plan — prompt-token shard maps.
+ *
+ * Zigzag ([CTX] §2.3 "Zigzag"; [SGL] "Zigzag strategy"): each request's
+ * new_len[j] new tokens are cut into 2C contiguous blocks; block sizes are
+ * floor(n/2C), plus one for the first n mod 2C blocks (early blocks receive
+ * the remainder); rank r takes blocks r and 2C-1-r; the split restarts for
+ * every request.  A block's queries read the cached prefix and every new
+ * token up to themselves, so its kv length is prefix_len[j] + block end.
+ *
+ * Interleave ([CTX] §2.4 "Interleave"; [SGL] "Interleave strategy"): the new
+ * tokens of all requests are flattened (f = 0..T-1, no reset at request
+ * boundaries) and rank r owns f = r, r+C, r+2C, ...; a query keeps its
+ * position in its request, prefix included, and reads keys 0..position.
+ *
+ * Local order: rank-major.  Rank r's queries occupy rows
+ * [rank_off[r], rank_off[r+1]) of every per-rank output; within a rank,
+ * zigzag orders request by request, early block then late block, and
+ * interleave orders by ascending f.
+ *
+ * cp_plan_size: host and device plan sizes in bytes for this batch.
+ * cp_shard_plan: writes the host part into host_plan (host_bytes), copies it
+ *   to dev_plan (dev_bytes, device memory) on `stream` and launches the
+ *   kernel that fills idx/qpos/qreq.  If host_plan is pinned memory the copy
+ *   is asynchronous: keep host_plan unchanged until the stream passes it.
+ * Arguments: strategy; C in [1, CP_MAX_SHARDS]; R >= 1 requests;
+ *   new_len[R] >= 0, prefix_len[R] >= 0 (host arrays); totals < 2^31.
+ * ------------------------------------------------------------------------- */
+cp_status cp_plan_size(cp_strategy strategy, int C, int R, const int32_t* new_len,
+                       const int32_t* prefix_len, size_t* host_bytes, size_t* dev_bytes);
+cp_status cp_shard_plan(cp_strategy strategy, int C, int R, const int32_t* new_len,
+                        const int32_t* prefix_len, void* host_plan, size_t host_bytes,
+                        void* dev_plan, size_t dev_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_prefill_attn — causal GQA prefill for every query a rank owns.
+ *
+ * For each owned query at position p of request j and each q head h, with
+ * kv head g = h / (Hq / Hkv) (consecutive grouping):
+ *   s_t = sm_scale * <q_h, k_{t,g}> for t = 0..p  (keys up to and including
+ *   itself, [CTX] §1.1; the prefix and the request's new tokens);
+ *   LSE = ln sum_t exp(s_t);  O = sum_t exp(s_t - LSE) v_{t,g}.
+ * With virtual shards the KV all-gather of [CTX] §2.1 is the identity: every
+ * rank reads the same global K/V buffers.
+ *
+ * q   [T, Hq, D]    flattened new-token order, dtype `dtype`
+ * k,v [KV, Hkv, D]  per request: prefix rows then new-token rows
+ * o   [rows, Hq, D] same dtype as q; rows = T (rank = -1, rank-major order)
+ *                   or rank r's count (rank = r, its local order)
+ * lse [rows, Hq]    fp32
+ * dtype: CP_BF16 (tensor-core path, D in {64, 128}) or CP_FP32 (CUDA-core
+ *   path, D <= 128, D % 32 == 0).  Hq % Hkv == 0.  host_plan and dev_plan
+ *   come from cp_shard_plan (the host part is read for the launch shape).
+ * ------------------------------------------------------------------------- */
+cp_status cp_prefill_attn(const void* host_plan, const void* dev_plan, int rank, cp_dtype dtype,
+                          const void* q, const void* k, const void* v, int Hq, int Hkv, int D,
+                          float sm_scale, void* o, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_decode_plan — decode KV-cache token shards and split-KV schedule.
+ *
+ * Token p of request b lives on shard p mod C at row p / C ([CTX] §3.1
+ * "Storing each token once": gpu = slot % C, row = slot // C; [V4] §5
+ * owner(j) = j mod P).  Shard r holds rows_{r,b} = ceil((L_b - r)/C) rows of
+ * request b, requests back to back (row_off).  The work of all (r, b) pairs
+ * is cut into contiguous row ranges balanced over `n_workers` CTAs
+ * (0 = twice the SM count of the current device); a pair split over several
+ * workers gets workspace slots that cp_decode_attn merges exactly.
+ *
+ * Arguments: C in [1, CP_MAX_SHARDS]; B >= 1; ctx_len[B] >= 0 host array.
+ * ------------------------------------------------------------------------- */
+cp_status cp_decode_plan_size(int C, int B, const int32_t* ctx_len, int n_workers,
+                              size_t* host_bytes, size_t* dev_bytes);
+cp_status cp_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers, void* host_plan,
+                         size_t host_bytes, void* dev_plan, size_t dev_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_kv_shard_pack — copy a token-ordered cache into its token shards
+ * (the decode side's store of [CTX] §5 case C: each decode GPU keeps only the
+ * tokens it owns).
+ *
+ * kv        [sum_b L_b, row_elems] device, requests back to back, dtype `dtype`
+ * kv_scale  [sum_b L_b] fp32 per-token scales, or NULL (copied when non-NULL)
+ * shard_kv  host array of C device pointers; shard r: [sum_b rows_{r,b}, row_elems]
+ * shard_scale host array of C device pointers (fp32 [sum_b rows_{r,b}]) or NULL
+ * Row bytes (row_elems * element size) must be a multiple of 16.
+ * ------------------------------------------------------------------------- */
+cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype dtype,
+                           const void* kv, const float* kv_scale, int row_elems,
+                           void* const* shard_kv, float* const* shard_scale, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_decode_attn — one decode query per request against every shard.
+ *
+ * For shard r and request b, the same attention as cp_prefill_attn restricted
+ * to the tokens stored on shard r ([CTX] §3.2, §3.4 step 3), giving a partial
+ * (O_r, LSE_r); merging the C partials with cp_lse_merge gives the
+ * attention over the whole cache ([CTX] §3.3; [V4] §5).
+ *
+ * mode CP_DECODE_MLA: one latent KV head shared by all H query heads
+ *   ([CTX] §1.3; [DCP] §5.3).  Dqk = 576, Dv = 512: keys are the whole
+ *   576-dim entry, values its first 512 dims ([GLM] footnote 1).
+ *   q [B, H, 576] bf16; shard_k[r] [rows_r, 576] as kv_dtype CP_BF16, or
+ *   CP_FP8_E4M3 codes with shard_scale[r] [rows_r] fp32 (value = code *
+ *   scale); shard_v must be NULL.
+ * mode CP_DECODE_GQA: q [B, Hq, D] and shard_k[r], shard_v[r]
+ *   [rows_r, Hkv, D], all of kv_dtype CP_BF16 or CP_FP32; Dqk = Dv = D,
+ *   D % 32 == 0, D <= 256; shard_scale must be NULL.
+ * o_part [C, B, H, Dv] fp32 and lse_part [C, B, H] fp32 (normalised partial
+ *   outputs; an empty shard gives O = 0, LSE = -inf).
+ * ws: workspace of cp_decode_workspace_size() bytes (NULL if that is 0).
+ * ------------------------------------------------------------------------- */
+cp_status cp_decode_workspace_size(const void* host_plan, int H, int Dv, size_t* bytes);
+cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                         cp_dtype kv_dtype, const void* q, const void* const* shard_k,
+                         const void* const* shard_v, const float* const* shard_scale, int Hq,
+                         int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * cp_lse_merge — exact combine of P partial results ([CTX] §3.3; [V4] §5).
+ *
+ * Per (n, h): g = max_p LSE_p; w_p = exp(LSE_p - g) (0 for LSE_p = -inf);
+ * O = sum_p w_p O_p / sum_p w_p; LSE = g + ln sum_p w_p.  If every part is
+ * empty, O = 0 and LSE = -inf.
+ * o_part [P, N, H, Dv] fp32; lse_part [P, N, H] fp32;
+ * o [N, H, Dv] of o_dtype CP_BF16 or CP_FP32; lse [N, H] fp32 or NULL.
+ * P in [1, CP_MAX_SHARDS]; Dv % 4 == 0.
+ * ------------------------------------------------------------------------- */
+cp_status cp_lse_merge(int P, int N, int H, int Dv, const float* o_part, const float* lse_part,
+                       void* o, cp_dtype o_dtype, float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPATTN_H */

@@ -1,0 +1,340 @@
+"""GPU parity: the CUDA library through its C ABI against the fp64 oracle.
+
+Tolerances (written here, applied to every floating-point comparison):
+  bf16 inputs, O:      max abs error <= 2e-2 and relative Frobenius <= 5e-3
+  fp32 inputs (tiny):  held to the bf16 bound
+  FP8-E4M3 cache, O:   max abs error <= 6e-2
+  LSE:                 max abs error <= 1e-3
+Shard maps, packing and plans: bit-exact.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import cp_workloads as W
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+TOL_BF16 = dict(max_abs=2e-2, rel_fro=5e-3)
+TOL_FP8 = dict(max_abs=6e-2, rel_fro=None)
+TOL_LSE = 1e-3
+
+
+@pytest.fixture(scope="module")
+def cp():
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a GPU")
+    from context_long_attention_gb300 import _build
+    import os
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    import context_long_attention_gb300 as cp
+    return cp
+
+
+def check_o(got, ref, max_abs, rel_fro, what="O"):
+    g = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    d = g - ref
+    err = np.abs(d).max() if d.size else 0.0
+    assert err <= max_abs, f"{what}: max abs err {err:.3e} > {max_abs}"
+    if rel_fro is not None and d.size:
+        nr = np.linalg.norm(ref)
+        rf = np.linalg.norm(d) / nr if nr > 0 else np.linalg.norm(d)
+        assert rf <= rel_fro, f"{what}: rel Frobenius err {rf:.3e} > {rel_fro}"
+
+
+def check_lse(got, ref, tol=TOL_LSE):
+    g = got.double().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    assert np.array_equal(np.isneginf(g), np.isneginf(ref)), "LSE -inf pattern differs"
+    fin = np.isfinite(ref)
+    if fin.any():
+        err = np.abs(g[fin] - ref[fin]).max()
+        assert err <= tol, f"LSE max abs err {err:.3e} > {tol}"
+
+
+def np64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+# ---------------------------------------------------------------- plans
+
+PLAN_BATCHES = [([16], [0], 4), ([5, 3], [0, 0], 4), ([19], [7], 4), ([3], [2], 4),
+                ([0, 9, 1, 33], [4, 0, 11, 2], 3), ([100, 1, 0, 57, 256], [0, 13, 5, 0, 1000], 8),
+                ([1000], [0], 1), ([7, 7, 7], [0, 0, 0], 64)]
+
+
+@pytest.mark.parametrize("new_len,prefix_len,C", PLAN_BATCHES)
+def test_device_maps_bit_exact(cp, new_len, prefix_len, C):
+    for strategy, ofn in ((cp.CP_ZIGZAG, oracle.zigzag_plan), (cp.CP_INTERLEAVE, oracle.interleave_plan)):
+        plan = cp.cp_shard_plan(strategy, C, new_len, prefix_len, device=DEV)
+        idx, qpos, qreq = (t.cpu().numpy() for t in plan.device_maps())
+        ref = ofn(new_len, prefix_len, C)
+        ro = plan.rank_off
+        for r in range(C):
+            sl = slice(ro[r], ro[r + 1])
+            assert list(idx[sl]) == list(ref["order"][r])
+            assert list(qpos[sl]) == list(ref["pos"][r])
+            assert list(qreq[sl]) == list(ref["req"][r])
+        # the device copy of the host part is identical
+        hw = plan.host_words
+        assert np.array_equal(plan.dev[:hw].cpu().numpy(), plan.host[:hw])
+
+
+def test_device_maps_full_size(cp):
+    z = W.WORKLOADS["zigzag"]
+    lens = W.interleave_lengths()
+    for strategy, nl, pl, C, ofn in (
+            (cp.CP_ZIGZAG, z["new_len"], z["prefix_len"], z["C"], oracle.zigzag_plan),
+            (cp.CP_INTERLEAVE, lens, [0] * len(lens), 8, oracle.interleave_plan_np)):
+        plan = cp.cp_shard_plan(strategy, C, nl, pl, device=DEV)
+        idx, qpos, qreq = (t.cpu().numpy() for t in plan.device_maps())
+        ref = ofn(nl, pl, C)
+        ro = plan.rank_off
+        for r in range(C):
+            sl = slice(ro[r], ro[r + 1])
+            assert np.array_equal(idx[sl], np.asarray(ref["order"][r]))
+            assert np.array_equal(qpos[sl], np.asarray(ref["pos"][r]))
+            assert np.array_equal(qreq[sl], np.asarray(ref["req"][r]))
+
+
+# ---------------------------------------------------------------- prefill
+
+
+def prefill_vs_oracle(cp, strategy, new_len, prefix_len, C, Hq, Hkv, D, dtype, seed, rows=None,
+                      tol=TOL_BF16, std=None, check_ranks=False):
+    q, k, v = W.prefill_inputs(new_len, prefix_len, Hq, Hkv, D, dtype, seed=seed, device=DEV, std=std)
+    plan = cp.cp_shard_plan(strategy, C, new_len, prefix_len, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = cp.cp_prefill_attn(plan, q, k, v, scale)
+    cp.cp_device_error_check()
+    ofn = oracle.zigzag_plan if strategy == cp.CP_ZIGZAG else oracle.interleave_plan_np
+    ref_plan = ofn(new_len, prefix_len, C)
+    ref = oracle.prefill_reference(ref_plan, new_len, prefix_len, np64(q), np64(k), np64(v), scale,
+                                   rows=rows)
+    ro = plan.rank_off
+    for r in range(C):
+        local, o_ref, l_ref = ref[r]
+        rows_g = ro[r] + local
+        check_o(o[rows_g], o_ref, what=f"rank {r} O", **tol)
+        check_lse(lse[rows_g], l_ref)
+    if check_ranks:  # a single rank's call gives that rank's rows, in local order
+        for r in range(C):
+            o_r, l_r = cp.cp_prefill_attn(plan, q, k, v, scale, rank=r)
+            assert torch.equal(o_r, o[ro[r]:ro[r + 1]])
+            assert torch.equal(l_r, lse[ro[r]:ro[r + 1]])
+    return plan
+
+
+def test_prefill_tiny_fp32(cp):
+    w = W.WORKLOADS["tiny"]
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, w["new_len"], w["prefix_len"], w["C"], w["Hq"], w["Hkv"],
+                      w["D"], "fp32", W.SEEDS["tiny"], check_ranks=True)
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_bf16_ragged_batch(cp, strategy, D):
+    prefill_vs_oracle(cp, strategy, [300, 1000, 77, 5], [0, 500, 13, 0], 4, 8, 2, D, "bf16",
+                      seed=7 + D + strategy, check_ranks=True)
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_prefill_bf16_sharp_scores(cp, strategy):
+    # larger inputs give peaked softmax rows (scores of order 10)
+    prefill_vs_oracle(cp, strategy, [700, 333], [129, 0], 8, 16, 4, 128, "bf16", seed=99,
+                      std=0.35)
+
+
+def test_prefill_edge_cases(cp):
+    # C=1 (textbook causal attention); fewer tokens than blocks; a single token
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, [200], [0], 1, 4, 4, 64, "bf16", seed=3)
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, [3, 1], [5, 0], 4, 4, 1, 64, "bf16", seed=4)
+    prefill_vs_oracle(cp, cp.CP_INTERLEAVE, [1], [0], 8, 2, 2, 128, "fp32", seed=5)
+
+
+def sample_rows(plan, per_rank=48, seed=0):
+    """Each segment's first and last row, plus random rows, per rank."""
+    rng = np.random.default_rng(seed)
+    ro = plan.rank_off
+    out = []
+    for r in range(plan.C):
+        n = int(ro[r + 1] - ro[r])
+        pick = set()
+        for s in plan.segments:
+            if s[0] == r and s[5] > 0:
+                pick.add(int(s[4] - ro[r]))
+                pick.add(int(s[4] + s[5] - 1 - ro[r]))
+        pick.update(int(x) for x in rng.integers(0, n, size=per_rank)) if n else None
+        out.append(np.array(sorted(pick), dtype=np.int64))
+    return out
+
+
+def test_prefill_zigzag_full_size_sampled(cp):
+    z = W.WORKLOADS["zigzag"]
+    plan = cp.cp_shard_plan(cp.CP_ZIGZAG, z["C"], z["new_len"], z["prefix_len"], device=None)
+    rows = sample_rows(plan, per_rank=24)
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, z["new_len"], z["prefix_len"], z["C"], z["Hq"], z["Hkv"],
+                      z["D"], "bf16", W.SEEDS["zigzag"], rows=rows)
+
+
+# ---------------------------------------------------------------- merge
+
+
+@pytest.mark.parametrize("P", [1, 3, 8, 64])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_lse_merge(cp, P, out_dtype):
+    g = torch.Generator(device="cpu").manual_seed(P)
+    N, H, Dv = 5, 4, 96
+    o_part = torch.randn((P, N, H, Dv), generator=g)
+    lse_part = torch.randn((P, N, H), generator=g) * 5
+    if P > 1:
+        lse_part[1, 0, :] = -math.inf  # an empty part
+    lse_part[:, 2, 1] = -math.inf      # every part empty
+    o_part[:, 2, 1] = 0
+    o, lse = cp.cp_lse_merge(o_part.to(DEV), lse_part.to(DEV), out_dtype=out_dtype)
+    o_ref, l_ref = oracle.lse_merge(o_part.double().numpy(), lse_part.double().numpy())
+    tol = dict(max_abs=1e-5, rel_fro=1e-6) if out_dtype == torch.float32 else TOL_BF16
+    check_o(o, o_ref, **tol)
+    check_lse(lse, l_ref, 1e-5)
+
+
+# ---------------------------------------------------------------- decode
+
+
+def test_kv_shard_pack_bit_exact(cp):
+    ctx = [0, 1, 5, 1000, 3, 257]
+    C = 4
+    data = W.mla_decode_inputs(ctx, H=2, seed=11, device=DEV)
+    plan = cp.cp_decode_plan(C, ctx, n_workers=5, device=DEV)
+    for kv, sc in ((data["kv_bf16"], None), (data["kv_fp8"], data["kv_scale"])):
+        shards, scales = cp.cp_kv_shard_pack(plan, kv, sc)
+        kvc = kv.cpu()
+        base = np.concatenate([[0], np.cumsum(ctx)])
+        for r in range(C):
+            sh = shards[r].cpu()
+            row = 0
+            for b, L in enumerate(ctx):
+                shard, rowmap = oracle.decode_shard_map(L, C)
+                toks = [p for p in range(L) if shard[p] == r]
+                assert [rowmap[p] for p in toks] == list(range(len(toks)))
+                idx = torch.tensor([base[b] + p for p in toks], dtype=torch.long)
+                got = sh[row:row + len(toks)]
+                assert torch.equal(got.view(torch.uint8), kvc[idx].view(torch.uint8))
+                if sc is not None:
+                    assert torch.equal(scales[r].cpu()[row:row + len(toks)], sc.cpu()[idx])
+                row += len(toks)
+            assert row == sh.shape[0]
+
+
+def gqa_decode_case(cp, q, kc, vc, ctx, C, scale, n_workers, dtype_tol=TOL_BF16):
+    plan = cp.cp_decode_plan(C, ctx, n_workers=n_workers, device=DEV)
+    sk, _ = cp.cp_kv_shard_pack(plan, kc)
+    sv, _ = cp.cp_kv_shard_pack(plan, vc)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, sk, sv, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    qn, kn, vn = np64(q), np64(kc), np64(vc)
+    for b, L in enumerate(ctx):
+        kb, vb = kn[base[b]:base[b] + L], vn[base[b]:base[b] + L]
+        po, pl = oracle.decode_shard_partials(qn[b], kb, vb, C, scale)
+        for r in range(C):
+            check_o(o_part[r, b], po[r], what=f"partial r{r} b{b}", **dtype_tol)
+            check_lse(lse_part[r, b], pl[r])
+        fo, fl = oracle.decode_attention(qn[b], kb, vb, scale)
+        check_o(o[b], fo, what=f"merged b{b}", **dtype_tol)
+        check_lse(lse[b], fl)
+
+
+def test_decode_gqa_tiny(cp):
+    t = W.tiny_inputs(device=DEV)
+    w = W.WORKLOADS["tiny"]
+    for nw in (0, 3, 64):
+        gqa_decode_case(cp, t["dec_q"], t["dec_k"], t["dec_v"], t["ctx"], w["C"],
+                        1.0 / math.sqrt(w["D"]), nw)
+
+
+def test_decode_gqa_bf16_ragged(cp):
+    ctx = [0, 2, 300, 4100]
+    q, k, v = W.gqa_decode_inputs(len(ctx), ctx, 16, 4, 128, "bf16", seed=12, device=DEV, std=0.3)
+    gqa_decode_case(cp, q, k, v, ctx, 8, 1.0 / math.sqrt(128), 6)
+
+
+def mla_decode_case(cp, data, C, fp8, n_workers, check_reqs=None, H=64):
+    ctx = data["ctx"]
+    scale = 1.0 / math.sqrt(576)
+    plan = cp.cp_decode_plan(C, ctx, n_workers=n_workers, device=DEV)
+    if fp8:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_fp8"], data["kv_scale"])
+    else:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_bf16"])
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_MLA, data["q"], shards,
+                                         shard_scale=scales, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.bfloat16)
+    cp.cp_device_error_check()
+    tol = TOL_FP8 if fp8 else TOL_BF16
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    qn = np64(data["q"])
+    reqs = range(len(ctx)) if check_reqs is None else check_reqs
+    for b in reqs:
+        L = ctx[b]
+        if fp8:
+            codes = data["kv_fp8"][base[b]:base[b] + L].cpu().numpy()
+            lat = oracle.e4m3_decode(codes)
+            sc = data["kv_scale"][base[b]:base[b] + L].double().cpu().numpy()
+            K, V = oracle.mla_cache_to_kv(lat, sc)
+        else:
+            K, V = oracle.mla_cache_to_kv(np64(data["kv_bf16"][base[b]:base[b] + L]))
+        po, pl = oracle.decode_shard_partials(qn[b], K, V, C, scale)
+        for r in range(C):
+            check_o(o_part[r, b], po[r], what=f"partial r{r} b{b}", **tol)
+            check_lse(lse_part[r, b], pl[r])
+        fo, fl = oracle.decode_attention(qn[b], K, V, scale)
+        check_o(o[b], fo, what=f"merged b{b}", **tol)
+        check_lse(lse[b], fl)
+    return o_part, lse_part
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("C,nw", [(8, 5), (1, 3), (4, 0)])
+def test_decode_mla_ragged(cp, fp8, C, nw):
+    ctx = [0, 1, 3, 129, 1000, 4097]
+    data = W.mla_decode_inputs(ctx, H=64, seed=21 + C, device=DEV)
+    mla_decode_case(cp, data, C, fp8, nw)
+
+
+def test_decode_mla_sharp_scores(cp):
+    ctx = [517, 2048]
+    data = W.mla_decode_inputs(ctx, H=64, seed=31, device=DEV, q_std=3.0)
+    for fp8 in (False, True):
+        mla_decode_case(cp, data, 8, fp8, 4)
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_decode_mla_full_size_sampled(cp, fp8):
+    w = W.WORKLOADS["mla"]
+    data = W.mla_decode_inputs([w["ctx"]] * w["B"], H=w["H"], seed=W.SEEDS["mla"], device=DEV,
+                               fp8=fp8, bf16=not fp8)
+    mla_decode_case(cp, data, w["C"], fp8, 0, check_reqs=[0, 37, 63])
+    del data
+    torch.cuda.empty_cache()
+
+
+def test_misaligned_pointer_rejected(cp):
+    t = W.tiny_inputs(device=DEV)
+    plan = cp.cp_shard_plan(cp.CP_ZIGZAG, 4, [256], [0], device=DEV)
+    q = t["q"]
+    bad = q.view(-1)[1:].view(-1)[: q.numel() - 1]
+    o = torch.empty_like(q)
+    lse = torch.empty((256, 8), device=DEV)
+    import ctypes
+    st = cp.lib.cp_prefill_attn(plan.host.ctypes.data_as(ctypes.c_void_p), ctypes.c_void_p(plan.dev.data_ptr()),
+                                -1, cp.CP_FP32, ctypes.c_void_p(bad.data_ptr()), ctypes.c_void_p(t["k"].data_ptr()),
+                                ctypes.c_void_p(t["v"].data_ptr()), 8, 2, 64, 0.125, ctypes.c_void_p(o.data_ptr()),
+                                ctypes.c_void_p(lse.data_ptr()), None)
+    assert st == cp.CpError(-1, "").status and b"aligned" in cp.lib.cp_last_error()

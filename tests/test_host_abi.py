@@ -1,0 +1,198 @@
+"""CPU tests of the C ABI: the library loads, exports every declared entry
+point, validates arguments, and its host-side planning matches the oracle's
+enumerated shard maps bit for bit (no GPU needed: plans are built host-only)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cp():
+    from context_long_attention_gb300 import _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    import context_long_attention_gb300 as cp
+    return cp
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "cpattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cp_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(cp):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(cp.lib, n), n
+    assert cp.lib.cp_version() == 1
+
+
+def expand_segments(plan):
+    """(f, pos, req) of every rank-major row, from the host segment table."""
+    T = plan.T
+    f = np.full(T, -1, np.int64)
+    pos = np.full(T, -1, np.int64)
+    req = np.full(T, -1, np.int64)
+    for s in plan.segments:
+        d = dict(zip(cp_fields(), s))
+        for i in range(d["count"]):
+            row = d["local_start"] + i
+            f[row] = d["first_f"] + i * d["stride"]
+            pos[row] = d["first_pos"] + i * d["stride"]
+            req[row] = d["req"]
+    return f, pos, req
+
+
+def cp_fields():
+    from context_long_attention_gb300._binding import SEG_FIELDS
+    return SEG_FIELDS
+
+
+BATCHES = [
+    ([16], [0], 4),
+    ([5, 3], [0, 0], 4),
+    ([19], [7], 4),
+    ([3], [2], 4),
+    ([0, 9, 1, 33], [4, 0, 11, 2], 3),
+    ([100, 1, 0, 57, 256], [0, 13, 5, 0, 1000], 8),
+    ([1000], [0], 1),
+    ([7, 7, 7], [0, 0, 0], 64),
+]
+
+
+@pytest.mark.parametrize("new_len,prefix_len,C", BATCHES)
+def test_host_plan_matches_oracle(cp, new_len, prefix_len, C):
+    for strategy, ofn in ((cp.CP_ZIGZAG, oracle.zigzag_plan), (cp.CP_INTERLEAVE, oracle.interleave_plan)):
+        plan = cp.cp_shard_plan(strategy, C, new_len, prefix_len, device=None)
+        ref = ofn(new_len, prefix_len, C)
+        f, pos, req = expand_segments(plan)
+        ro = plan.rank_off
+        for r in range(C):
+            sl = slice(ro[r], ro[r + 1])
+            assert list(f[sl]) == list(ref["order"][r])
+            assert list(pos[sl]) == list(ref["pos"][r])
+            assert list(req[sl]) == list(ref["req"][r])
+        if strategy == cp.CP_ZIGZAG:
+            got = []
+            for s in plan.segments:
+                d = dict(zip(cp_fields(), s))
+                got.append((d["rank"], d["req"], d["which"], d["block"], d["q_start"], d["count"], d["kv_len"]))
+            assert sorted(got) == sorted(ref["blocks"])
+        # tiles cover every query exactly once, in both orders
+        for tiles in (plan.tiles, plan.tiles_by_rank):
+            seen = np.zeros(plan.T, np.int64)
+            for seg, off in tiles:
+                d = dict(zip(cp_fields(), plan.segments[seg]))
+                n = min(128, d["count"] - off)
+                seen[d["local_start"] + off:d["local_start"] + off + n] += 1
+            assert np.all(seen == 1)
+
+
+def test_host_plan_full_size_workloads(cp):
+    import cp_workloads as W
+    z = W.WORKLOADS["zigzag"]
+    plan = cp.cp_shard_plan(cp.CP_ZIGZAG, z["C"], z["new_len"], z["prefix_len"])
+    ref = oracle.zigzag_plan(z["new_len"], z["prefix_len"], z["C"])
+    got = sorted((int(s[0]), int(s[1]), int(s[3]), int(s[2]), int(s[8]), int(s[5]), int(s[10])) for s in plan.segments)
+    assert got == sorted(ref["blocks"])
+    # rank r: early kv_len = 4096 + 2048 (r+1), late = 4096 + 2048 (16 - r)
+    for s in plan.segments:
+        r, which, count, kvl = int(s[0]), int(s[3]), int(s[5]), int(s[10])
+        assert count == 2048
+        assert kvl == 4096 + 2048 * ((r + 1) if which == 0 else (16 - r))
+    lens = W.interleave_lengths()
+    plan = cp.cp_shard_plan(cp.CP_INTERLEAVE, 8, lens, [0] * len(lens))
+    ref = oracle.interleave_plan_np(lens, [0] * len(lens), 8)
+    f, pos, req = expand_segments_fast(plan)
+    ro = plan.rank_off
+    for r in range(8):
+        sl = slice(ro[r], ro[r + 1])
+        assert np.array_equal(f[sl], ref["order"][r])
+        assert np.array_equal(pos[sl], ref["pos"][r])
+        assert np.array_equal(req[sl], ref["req"][r])
+
+
+def expand_segments_fast(plan):
+    T = plan.T
+    f = np.empty(T, np.int64)
+    pos = np.empty(T, np.int64)
+    req = np.empty(T, np.int64)
+    for s in plan.segments:
+        d = dict(zip(cp_fields(), (int(x) for x in s)))
+        i = np.arange(d["count"])
+        rows = d["local_start"] + i
+        f[rows] = d["first_f"] + i * d["stride"]
+        pos[rows] = d["first_pos"] + i * d["stride"]
+        req[rows] = d["req"]
+    return f, pos, req
+
+
+@pytest.mark.parametrize("ctx,C,G", [([257], 4, 3), ([0, 1, 5, 1000, 3], 4, 7), ([131072] * 4, 8, 148),
+                                     ([2, 2], 8, 4), ([300000, 1024, 70000], 8, 16)])
+def test_decode_plan_matches_shard_map_and_covers_rows(cp, ctx, C, G):
+    plan = cp.cp_decode_plan(C, ctx, n_workers=G, device=None)
+    B = len(ctx)
+    pairs = plan.pairs
+    for r in range(C):
+        off = 0
+        for b in range(B):
+            shard, row = oracle.decode_shard_map(ctx[b], C)
+            rows = sum(1 for s in shard if s == r)
+            p = pairs[r * B + b]
+            assert p[0] == rows and p[1] == off and p[2] == ctx[b]
+            off += rows
+    covered = [np.zeros(int(p[0]), np.int64) for p in pairs]
+    parts = {}
+    for pair, rb, re_, part in plan.work:
+        covered[pair][rb:re_] += 1
+        parts.setdefault(int(pair), []).append(int(part))
+        assert rb % 128 == 0
+    for i, c in enumerate(covered):
+        assert np.all(c == 1)
+        ps = parts[i]
+        if len(ps) == 1:
+            assert ps == [-1] and pairs[i][3] == 1
+        else:
+            first = int(pairs[i][4])
+            assert sorted(ps) == list(range(first, first + len(ps)))
+    # balance: each worker holds floor or ceil of NT/G tiles
+    tiles = [0] * G
+    wo = plan.worker_off
+    for w in range(G):
+        for pair, rb, re_, part in plan.work[wo[w]:wo[w + 1]]:
+            tiles[w] += (re_ - rb + 127) // 128
+    NT = sum((int(p[0]) + 127) // 128 for p in pairs)
+    assert sum(tiles) == NT and max(tiles) - min(tiles) <= 1
+
+
+def test_argument_validation(cp):
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):
+        cp.cp_shard_plan(cp.CP_ZIGZAG, 0, [4], [0])
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):
+        cp.cp_shard_plan(cp.CP_ZIGZAG, 65, [4], [0])
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):
+        cp.cp_shard_plan(cp.CP_INTERLEAVE, 2, [4, -1], [0, 0])
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):
+        cp.cp_shard_plan(7, 2, [4], [0])
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):
+        cp.cp_decode_plan(4, [10, -2], n_workers=4)
+    lib = cp.lib
+    # null pointers and bad plans are rejected before any launch
+    assert lib.cp_prefill_attn(None, None, -1, 0, None, None, None, 8, 2, 64, 0.1, None, None, None) == -1
+    bogus = np.zeros(64, np.int32)
+    st = lib.cp_decode_attn(bogus.ctypes.data_as(ctypes.c_void_p), None, 1, 0, None, None, None, None,
+                            64, 1, 576, 512, 0.1, None, None, None, 0, None)
+    assert st == -1 and b"magic" in lib.cp_last_error()
+    assert lib.cp_lse_merge(0, 1, 1, 4, None, None, None, 0, None, None) == -1
+    assert lib.cp_lse_merge(2, 1, 1, 6, None, None, None, 0, None, None) == -1
