@@ -29,10 +29,8 @@ TOL_LSE = 1e-3
 def cp():
     if not torch.cuda.is_available():
         pytest.fail("a GPU test ran without a GPU")
-    from context_long_attention_gb300 import _build
-    import os
-    if not os.path.exists(_build.LIB):
-        _build.build()
+    import __graft_entry__
+    __graft_entry__.ensure_built()
     import context_long_attention_gb300 as cp
     return cp
 

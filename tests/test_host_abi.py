@@ -16,9 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def cp():
-    from context_long_attention_gb300 import _build
-    if not os.path.exists(_build.LIB):
-        _build.build()
+    import __graft_entry__
+    __graft_entry__.ensure_built()
     import context_long_attention_gb300 as cp
     return cp
 
