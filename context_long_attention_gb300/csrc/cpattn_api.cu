@@ -7,6 +7,7 @@
 // the device (plan_kernels.cu); everything else here is O(requests x shards).
 #include <algorithm>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -473,8 +474,18 @@ cp_status cp_prefill_attn(const void* host_plan, const void* dev_plan, int rank,
   const int n_rows = rank < 0 ? h.T : W[h.off_rank + rank + 1] - W[h.off_rank + rank];
   if (n_rows == 0) return ok();
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_prefill_simt((const int32_t*)dev_plan, h, rank, row_begin, n_rows,
-                                      dtype == CP_BF16, q, k, v, Hq, Hkv, D, sm_scale, o, lse, s);
+  cudaError_t e;
+  if (dtype == CP_BF16) {
+    if (D != 64 && D != 128) return fail(CP_ERR_UNSUPPORTED, "bf16 prefill needs D in {64, 128}, got %d", D);
+    // Test hook for failure detection: with CPATTN_TEST_STALL=1 one bounded
+    // wait in the kernel waits for a barrier nothing arrives at.
+    const char* stall = getenv("CPATTN_TEST_STALL");
+    e = launch_prefill_tc((const int32_t*)dev_plan, W, h, rank, q, k, v, Hq, Hkv, D, sm_scale, o,
+                          lse, stall && stall[0] == '1', s);
+  } else {
+    e = launch_prefill_simt((const int32_t*)dev_plan, h, rank, row_begin, n_rows, false, q, k, v,
+                            Hq, Hkv, D, sm_scale, o, lse, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "prefill kernel");
   return ok();
 }

@@ -12,7 +12,7 @@ constexpr int kHeaderWords = (int)(sizeof(cp_plan_header) / 4);
 constexpr int kSegWords = (int)(sizeof(cp_seg_desc) / 4);
 constexpr int kPairWords = (int)(sizeof(cp_pair_desc) / 4);
 constexpr int kWorkWords = (int)(sizeof(cp_work_desc) / 4);
-constexpr int kPrefillTileRows = 128;  // queries per prefill tile (MMA M)
+constexpr int kPrefillTileRows = 256;  // queries per prefill tile (two 128-row MMA tiles)
 constexpr int kDecodeTileRows = 128;   // KV rows per decode scheduling tile (MMA M)
 
 // Device status word layout (written by kernels, read by cp_device_error_check).
@@ -49,6 +49,12 @@ cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
 cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h, int H, int Dv,
                                 const float* ws_o, const float* ws_lse, float* o_part,
                                 float* lse_part, cudaStream_t s);
+
+// ---- tensor-core prefill (prefill_tc.cu)
+cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
+                              const cp_plan_header& h, int rank, const void* q, const void* k,
+                              const void* v, int Hq, int Hkv, int D, float sm_scale, void* o,
+                              float* lse, bool stall_test, cudaStream_t s);
 
 // ---- CUDA-core attention (simt_attn.cu)
 cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h, int rank,

@@ -72,11 +72,15 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
   const float inv = any ? 1.f / z : 0.f;
-  for (int c = lane; c < Dv / 4; c += 32) {
+  // Every lane runs every iteration (the weights travel by warp shuffles);
+  // lanes past the row's end only skip their loads and stores.
+  for (int c0 = 0; c0 < Dv / 4; c0 += 32) {
+    const int c = c0 + lane;
+    const bool active = c < Dv / 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p = 0; p < P; ++p) {
       const float w = __shfl_sync(0xffffffffu, p < 32 ? w0 : w1, p & 31);
-      if (w != 0.f) {
+      if (active && w != 0.f) {
         const float4 x = reinterpret_cast<const float4*>(o + p * ostride)[c];
         acc.x += w * x.x;
         acc.y += w * x.y;
@@ -88,6 +92,7 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
+    if (!active) continue;
     if (out_f32) {
       reinterpret_cast<float4*>(out_f32)[c] = acc;
     } else {

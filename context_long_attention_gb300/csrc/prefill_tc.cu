@@ -1,0 +1,492 @@
+// Causal GQA prefill on the tcgen05 tensor cores (bf16 in, fp32 accumulate).
+//
+// What it computes is the attention of "How GPUs Share a Long Context During
+// LLM Inference" §1.1 for every query a virtual shard owns (§2.3 zigzag
+// blocks, §2.4 interleave runs): each query at position p reads the keys at
+// positions 0..p of its request, and the kernel emits O and the natural-log
+// LSE of the scaled scores (§3.3).
+//
+// One CTA = one plan tile (up to 256 consecutive queries of one segment) x
+// one query head, as two 128-row M tiles that share every K/V tile:
+//   warps 0-3  softmax of M tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax of M tile 1
+//   warp 8     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring
+//   warp 9     MMA issuer (one thread) and TMEM owner
+// TMEM (512 columns): tile t holds S_t = Q_t K_j^T in columns [256t, 256t+128)
+// and its output accumulator O_t in [256t+128, 256t+128+D).  The softmax
+// writes P_t (bf16) over the first 64 columns of S_t, and O_t += P_t V_j
+// reads P from TMEM.  The MMA thread alternates the two M tiles so that one
+// tile's softmax overlaps the other tile's matrix products.  The running max
+// used in the exponentials only moves when a row's max grows by more than
+// 2^8, so O is rarely rescaled; the result is exact either way because
+// O = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m) holds for any m.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace cpattn {
+namespace {
+using namespace tc;
+
+constexpr int BM = 128;        // query rows per M tile
+constexpr int BN = 128;        // keys per K/V tile
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;  // move the running max when it grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;                   // 128-byte column chunks per row
+  static constexpr int kQBytes = BM * D * 2;               // one Q tile
+  static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
+  static constexpr int kSlots = D == 128 ? 4 : 8;          // ring of K/V tiles
+  static constexpr int kSmem = 2 * kQBytes + kSlots * kSlotBytes + 1024;
+};
+
+struct Params {
+  const int32_t* plan;
+  int off_seg;
+  int tile_list;  // word offset of this launch's cp_tile_desc list
+  int n_tiles;
+  int row_sub;    // subtracted from rank-major rows (per-rank output)
+  const __nv_bfloat16* q;
+  __nv_bfloat16* o;
+  float* lse;
+  int Hq, group;
+  float sm_scale, scale_log2;
+  unsigned* status;
+  unsigned long long wait_ns;
+  int stall_test;  // test hook: the MMA thread waits on a barrier nobody arrives at
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
+  *abort = 1;
+  if (atomicCAS(status, 0u, 1u) == 0u) {
+    status[1] = kKernPrefillTc;
+    status[2] = site;
+    status[3] = blockIdx.x;
+    __threadfence();
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;                    // two Q tiles
+  uint8_t* sKV = smem + 2 * C::kQBytes;  // K/V slot ring
+  __shared__ __align__(8) uint64_t bar_full[C::kSlots], bar_empty[C::kSlots];
+  __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_never, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_i = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
+  const cp_tile_desc td = reinterpret_cast<const cp_tile_desc*>(p.plan + p.tile_list)[tile_i];
+  const cp_seg_desc sg = reinterpret_cast<const cp_seg_desc*>(p.plan + p.off_seg)[td.seg];
+  const int g = h / p.group;
+
+  // Rows and K/V tile counts of the two M tiles.
+  int rows[2], nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    rows[t] = min(BM, max(0, sg.count - td.q_off - t * BM));
+    const int last_pos = sg.first_pos + (td.q_off + t * BM + rows[t] - 1) * sg.stride;
+    nkv[t] = rows[t] > 0 ? (last_pos + BN) / BN : 0;
+  }
+  const int nK = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), 1);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bar_q[t]), 128);
+      mbar_init(smem_u32(&bar_s[t]), 1);
+      mbar_init(smem_u32(&bar_p[t]), 128);
+      mbar_init(smem_u32(&bar_o[t]), 1);
+    }
+    mbar_init(smem_u32(&bar_never), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    zero_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 512);
+  if (warp == kWarpTma && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;
+    const int i = (warp & 3) * 32 + lane;  // row within the M tile = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t colS = t * 256, colO = t * 256 + 128;
+    const bool valid = i < rows[t];
+    // Q row -> shared memory in the 128-byte-swizzled K-major layout.
+    {
+      const long long f = (long long)sg.first_f + (long long)(td.q_off + t * BM + i) * sg.stride;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + (f * p.Hq + h) * D);
+      uint8_t* dst = sQ + t * C::kQBytes + i * 128;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (valid) val = __ldg(src + c);
+        const int a = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(dst + a * (BM * 128) + ((cc ^ (i & 7)) << 4)) = val;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bar_q[t]));
+    }
+    const int n_t = nkv[t];
+    if (n_t > 0) {
+      const int my_row = valid ? i : rows[t] - 1;
+      const int pos = sg.first_pos + (td.q_off + t * BM + my_row) * sg.stride;
+      const float sl2 = p.scale_log2;
+      const float thr = kRescaleLog2 / sl2;  // threshold in raw score units
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_t && ok; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns, &abort_flag))) {
+          report_timeout(p.status, 1, &abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kbase = j * BN;
+        const bool mask = kbase + BN - 1 > pos;
+        // pass 1: row max of this tile
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_addr + colS + c * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float s = __uint_as_float(r[e]);
+            if (mask && kbase + c * 32 + e > pos) s = -INFINITY;
+            mx = fmaxf(mx, s);
+          }
+        }
+        // tcgen05.ld/st are warp-collective: the warp rescales together, rows
+        // whose max did not move use a factor of 1.
+        const bool need = mx > m_used + thr;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2((m_used - mx) * sl2) : 1.f;
+          if (need) {
+            l *= alpha;
+            m_used = mx;
+          }
+          if (j > 0) {  // rescale O_t once its previous P V product has landed
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
+                                                   &abort_flag))) {
+              report_timeout(p.status, 2, &abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(lane_addr + colO + c * 32, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(lane_addr + colO + c * 32, r);
+            }
+          }
+        }
+        // pass 2: P = 2^(s*c - m*c) in bf16 over the first 64 columns of S
+        const float neg = -m_used * sl2;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_addr + colS + c * 32, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+            float p0 = ex2(fmaf(s0, sl2, neg)), p1 = ex2(fmaf(s1, sl2, neg));
+            if (mask) {
+              if (kbase + c * 32 + 2 * e > pos) p0 = 0.f;
+              if (kbase + c * 32 + 2 * e + 1 > pos) p1 = 0.f;
+            }
+            lsum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(lane_addr + colS + c * 16, pk);
+        }
+        l += lsum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p[t]));
+      }
+      // epilogue: O / l and LSE
+      const bool landed =
+          __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_o[t]), (n_t - 1) & 1, p.wait_ns,
+                                                  &abort_flag));
+      if (landed) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        const long long out_row =
+            (long long)sg.local_start + td.q_off + t * BM + i - p.row_sub;
+        __nv_bfloat16* dst = p.o + (out_row * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(lane_addr + colO + c * 32, r);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
+              reinterpret_cast<uint4*>(dst + c * 32)[v4] = w;
+            }
+          }
+        }
+        if (valid) p.lse[out_row * p.Hq + h] = m_used * p.sm_scale + logf(l);
+      } else if (ok) {
+        report_timeout(p.status, 3, &abort_flag);
+      }
+    }
+  } else if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_round[C::kSlots];
+#pragma unroll
+      for (int s = 0; s < C::kSlots; ++s) last_round[s] = -1;
+      for (int u = 0; u < 2 * nK; ++u) {
+        const int j = u >> 1, slot = u % C::kSlots, round = u / C::kSlots;
+        if (!mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1, p.wait_ns, &abort_flag)) {
+          report_timeout(p.status, 4, &abort_flag);
+          break;
+        }
+        const uint32_t full = smem_u32(&bar_full[slot]);
+        mbar_expect_tx(full, C::kSlotBytes);
+        const uint32_t dst = smem_u32(sKV + slot * C::kSlotBytes);
+        const CUtensorMap* map = (u & 1) ? &vmap : &kmap;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(dst + c * (BN * 128), map, c * 64, g, sg.kv_base + j * BN, full);
+        last_round[slot] = round;
+      }
+      // Never leave with a copy in flight: wait for the last load of every slot.
+      for (int s = 0; s < C::kSlots; ++s)
+        if (last_round[s] >= 0)
+          mbar_wait(smem_u32(&bar_full[s]), last_round[s] & 1, 1000000000ull, &zero_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
+      const uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
+      auto fail = [&](unsigned site) { report_timeout(p.status, site, &abort_flag); };
+      auto wait_full = [&](int u) -> bool {
+        return mbar_wait(smem_u32(&bar_full[u % C::kSlots]), (u / C::kSlots) & 1, p.wait_ns,
+                         &abort_flag);
+      };
+      auto issue_s = [&](int t, int u) {
+        const uint32_t kb = smem_u32(sKV + (u % C::kSlots) * C::kSlotBytes);
+        const uint32_t qb = smem_u32(sQ + t * C::kQBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
+          mma_ss(tmem + t * 256, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
+                 idS, kk > 0);
+        }
+        mma_commit(smem_u32(&bar_s[t]));
+      };
+      auto issue_pv = [&](int t, int u, bool acc) {
+        const uint32_t vb = smem_u32(sKV + (u % C::kSlots) * C::kSlotBytes);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
+                 smem_desc(vb + kk * 16 * 128, BN * 128, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bar_o[t]));
+      };
+      bool ok = true;
+      if (p.stall_test && !mbar_wait(smem_u32(&bar_never), 0, p.wait_ns, &abort_flag)) {
+        fail(10);
+        ok = false;
+      }
+      for (int t = 0; t < 2 && ok; ++t)
+        if (nkv[t] > 0 && !mbar_wait(smem_u32(&bar_q[t]), 0, p.wait_ns, &abort_flag)) {
+          fail(11);
+          ok = false;
+        }
+      if (ok && nK > 0) {
+        if (!wait_full(0)) {
+          fail(12);
+          ok = false;
+        } else {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (nkv[t] > 0) issue_s(t, 0);
+          mma_commit(smem_u32(&bar_empty[0]));
+        }
+      }
+      for (int j = 0; j < nK && ok; ++j) {
+        const int uV = 2 * j + 1, uK = 2 * j + 2;
+        if (!wait_full(uV)) {
+          fail(13);
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (j >= nkv[t]) continue;
+          if (!mbar_wait(smem_u32(&bar_p[t]), j & 1, p.wait_ns, &abort_flag)) {
+            fail(14 + t);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, uV, j > 0);
+          if (j + 1 < nkv[t]) {
+            if (!wait_full(uK)) {
+              fail(16);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, uK);
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bar_empty[uV % C::kSlots]));
+        if (j + 1 < nK) mma_commit(smem_u32(&bar_empty[uK % C::kSlots]));
+      }
+      // Never free TMEM under a running MMA: wait for everything issued.
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [rows, H, D] bf16 viewed as 3-D (D, H, rows); box (64, 1, 128), 128-byte swizzle.
+bool make_kv_map(CUtensorMap* m, const void* base, int rows, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)BN};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* s = getenv("CPATTN_WAIT_LIMIT_MS");
+    const long long ms = s ? atoll(s) : 4000;
+    return (unsigned long long)(ms > 0 ? ms : 4000) * 1000000ull;
+  }();
+  return v;
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params& p,
+                     cudaStream_t s) {
+  const int smem = Cfg<D>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const long long blocks = (long long)p.n_tiles * p.Hq;
+  prefill_tc_kernel<D><<<(unsigned)blocks, kThreads, smem, s>>>(km, vm, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
+                              const cp_plan_header& h, int rank, const void* q, const void* k,
+                              const void* v, int Hq, int Hkv, int D, float sm_scale, void* o,
+                              float* lse, bool stall_test, cudaStream_t s) {
+  Params p;
+  p.plan = dev_plan;
+  p.off_seg = h.off_seg;
+  if (rank < 0) {
+    p.tile_list = h.off_tiles;
+    p.n_tiles = h.n_tiles;
+    p.row_sub = 0;
+  } else {
+    const int32_t* rto = host_plan + h.off_rtile;
+    p.tile_list = h.off_rtile + h.C + 1 + 2 * rto[rank];
+    p.n_tiles = rto[rank + 1] - rto[rank];
+    p.row_sub = host_plan[h.off_rank + rank];
+  }
+  if (p.n_tiles == 0) return cudaSuccess;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.Hq = Hq;
+  p.group = Hq / Hkv;
+  p.sm_scale = sm_scale;
+  p.scale_log2 = sm_scale * kLog2e;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevice;
+  p.wait_ns = stall_test ? 50000000ull : wait_limit_ns();
+  p.stall_test = stall_test ? 1 : 0;
+  CUtensorMap km, vm;
+  if (!make_kv_map(&km, k, h.KV, Hkv, D) || !make_kv_map(&vm, v, h.KV, Hkv, D))
+    return cudaErrorInvalidValue;
+  return D == 128 ? launch_d<128>(km, vm, p, s) : launch_d<64>(km, vm, p, s);
+}
+
+}  // namespace cpattn

@@ -80,7 +80,7 @@ typedef struct {
   int32_t T;          /* prefill: total new tokens; decode: total cached tokens */
   int32_t KV;         /* prefill: total K/V rows = sum(prefix + new); decode: 0 */
   int32_t n_seg;      /* prefill: number of segments; decode: number of work items */
-  int32_t n_tiles;    /* prefill: number of 128-query tiles; decode: number of workers */
+  int32_t n_tiles;    /* prefill: number of 256-query tiles; decode: number of workers */
   int32_t off_rank;   /* prefill: int32 rank_off[C+1]; decode: cp_pair_desc[C*R] */
   int32_t off_req;    /* prefill: cp_req_desc[R]; decode: int32 worker_off[n_workers+1] */
   int32_t off_seg;    /* prefill: cp_seg_desc[n_seg]; decode: cp_work_desc[n_seg] */
@@ -126,7 +126,7 @@ typedef struct {
   int32_t kv_base;     /* first K/V row of the request */
 } cp_seg_desc;
 
-/* A tile of up to 128 consecutive queries of one segment. */
+/* A tile of up to 256 consecutive queries of one segment. */
 typedef struct {
   int32_t seg;   /* segment index */
   int32_t q_off; /* offset of the tile's first query within the segment */

@@ -93,7 +93,7 @@ def test_host_plan_matches_oracle(cp, new_len, prefix_len, C):
             seen = np.zeros(plan.T, np.int64)
             for seg, off in tiles:
                 d = dict(zip(cp_fields(), plan.segments[seg]))
-                n = min(128, d["count"] - off)
+                n = min(256, d["count"] - off)
                 seen[d["local_start"] + off:d["local_start"] + off + n] += 1
             assert np.all(seen == 1)
 
