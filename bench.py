@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Benchmark of context-parallel attention on GB300, one JSON line.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  prefill  zigzag shard plan + causal GQA prefill over 8 virtual shards of a
+           32,768-token prompt after a 4,096-token cached prefix (32 q / 8 kv
+           heads, head dim 128, bf16) — the primary metric, TFLOP/s;
+  decode   decode shard plan + split-KV MLA decode of 64 requests x 131,072
+           cached tokens over 8 token shards (FP8-E4M3 latent cache with a
+           per-token scale) + exact LSE merge — reported as KV HBM GB/s.
+The token-shard packing of the decode cache happens once, before timing
+(the prefill-to-decode hand-off).  Inputs are larger than L2 (129 MB), so no
+flush is needed between steps.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+prefill workload on the host cores (there is no other implementation to run:
+the pages describe serving systems, not a library).
+Multi-GPU (torchrun): replicas only — every rank runs its own copy of the
+step; the value is the work of all ranks over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import cp_workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+WORKLOAD = ("zigzag prefill: 1 request, 32768 new tokens + 4096-token cached prefix, GQA 32q/8kv, "
+            "D 128, bf16, CP=8 virtual shards; plus MLA decode: 64 x 131072 ctx, 64 heads, 576/512 "
+            "FP8-E4M3 latent, DCP=8, LSE merge")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(new_len, prefix_len, Hq, D):
+    """4 * D * Hq per causal (query, key) pair; pairs = sum of query extents.
+    Masked halves of diagonal tiles are not credited."""
+    pairs = 0
+    for n, p in zip(new_len, prefix_len):
+        pairs += n * p + n * (n + 1) // 2
+    return 4 * D * Hq * pairs, pairs
+
+
+def decode_bytes(ctx, H, fp8=True):
+    """KV rows read once (576 B + 4 B scale per token for FP8, 1,152 B for
+    bf16), the bf16 query and the bf16 merged output."""
+    per_tok = 580 if fp8 else 1152
+    B = len(ctx)
+    return sum(ctx) * per_tok + B * H * 576 * 2 + B * H * 512 * 2
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+
+def oracle_prefill_sample(rows_per_call=64, seed=0, budget_s=15.0):
+    """The fp64 oracle on a bounded sample of the zigzag prefill workload:
+    rows of rank 0's late block (the longest extents) for all heads.
+    Returns (TFLOP/s, seconds, rows, cores)."""
+    import oracle
+    z = W.WORKLOADS["zigzag"]
+    q, k, v = W.prefill_inputs(z["new_len"], z["prefix_len"], z["Hq"], z["Hkv"], z["D"], "bf16",
+                               seed=W.SEEDS["zigzag"], device="cpu")
+    plan = oracle.zigzag_plan(z["new_len"], z["prefix_len"], z["C"])
+    n_late = len(plan["order"][0]) // 2
+    rng = np.random.default_rng(seed)
+    L = z["new_len"][0] + z["prefix_len"][0]
+    k64 = k.double().numpy()
+    v64 = v.double().numpy()
+    done_flops = 0
+    done_rows = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done_rows < 4 * rows_per_call:
+        li = n_late + rng.choice(n_late, size=rows_per_call, replace=False)
+        f = np.asarray(plan["order"][0])[li]
+        pos = np.asarray(plan["pos"][0])[li]
+        oracle.causal_rows(q[f].double().numpy(), k64[:L], v64[:L], pos, 1.0 / math.sqrt(z["D"]))
+        done_flops += 4 * z["D"] * z["Hq"] * int((pos + 1).sum())
+        done_rows += rows_per_call
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return done_flops / dt / 1e12, dt, done_rows, cores
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    steps = []
+    for i in range(args.warmup + args.steps):
+        tf, dt, rows, cores = oracle_prefill_sample(rows_per_call=16, seed=i, budget_s=2.0)
+        if i >= args.warmup:
+            steps.append((tf, dt, rows))
+    value = statistics.median(s[0] for s in steps)
+    z = W.WORKLOADS["zigzag"]
+    line = {
+        "impl": "reference", "metric": "prefill causal-attn TFLOP/s", "value": value,
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * statistics.median(s[1] for s in steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "timed": "prefill (oracle sample)",
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{steps[0][2]} query rows x {z['Hq']} heads per step "
+                                   "(rank 0's late zigzag block)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+
+def run_ours(args, world, rank, local):
+    import context_long_attention_gb300 as cp
+
+    dev = torch.device("cuda", local if world > 1 else 0)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_kind = load_peaks()
+    do_pre = args.only in ("all", "prefill")
+    do_dec = args.only in ("all", "decode")
+
+    # ---- prefill inputs (zigzag)
+    z = W.WORKLOADS["zigzag"]
+    nl, pl, C, Hq, Hkv, D = z["new_len"], z["prefix_len"], z["C"], z["Hq"], z["Hkv"], z["D"]
+    scale = 1.0 / math.sqrt(D)
+    p_flops, _ = prefill_flops(nl, pl, Hq, D)
+    if do_pre:
+        q, k, v = W.prefill_inputs(nl, pl, Hq, Hkv, D, "bf16", seed=W.SEEDS["zigzag"] + rank,
+                                   device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((q.shape[0], Hq), dtype=torch.float32, device=dev)
+
+    # ---- decode inputs (MLA, FP8 cache, packed into token shards once)
+    m = W.WORKLOADS["mla"]
+    ctx = [m["ctx"]] * m["B"]
+    d_bytes = decode_bytes(ctx, m["H"], fp8=True)
+    dscale = 1.0 / math.sqrt(m["Dqk"])
+    n_dec_kernels = 0
+    if do_dec:
+        data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev, bf16=False)
+        dplan = cp.cp_decode_plan(m["C"], ctx, device=dev)
+        shards, scales = cp.cp_kv_shard_pack(dplan, data["kv_fp8"], data["kv_scale"])
+        del data["kv_fp8"], data["kv_scale"]
+        dq = data["q"]
+        o_part = torch.empty((m["C"], m["B"], m["H"], m["Dv"]), dtype=torch.float32, device=dev)
+        lse_part = torch.empty((m["C"], m["B"], m["H"]), dtype=torch.float32, device=dev)
+        o_dec = torch.empty((m["B"], m["H"], m["Dv"]), dtype=torch.bfloat16, device=dev)
+        lse_dec = torch.empty((m["B"], m["H"]), dtype=torch.float32, device=dev)
+        ws_bytes = cp.cp_decode_workspace_size(dplan, m["H"], m["Dv"])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        n_dec_kernels = 2 + (1 if dplan.n_split > 0 else 0)  # decode (+ split merge) + LSE merge
+    torch.cuda.synchronize(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(rec):
+        e0, e1, e2, e3, e4 = rec
+        e0.record(stream)
+        if do_pre:
+            plan = cp.cp_shard_plan(cp.CP_ZIGZAG, C, nl, pl, device=dev)
+        e1.record(stream)
+        if do_pre:
+            cp.cp_prefill_attn(plan, q, k, v, scale, out=o, lse=lse)
+        e2.record(stream)
+        if do_dec:
+            dp = cp.cp_decode_plan(m["C"], ctx, device=dev)
+            cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
+                              sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
+        e3.record(stream)
+        if do_dec:
+            cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
+        e4.record(stream)
+
+    for _ in range(args.warmup):
+        step([ev() for _ in range(5)])
+    cp.cp_device_error_check(dev)
+    torch.cuda.synchronize(dev)
+
+    recs = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start, t_end = ev(), ev()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(recs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clock_info = clocks.stop()
+    cp.cp_device_error_check(dev)
+
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    plan_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    pre_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    dec_ms = [r[2].elapsed_time(r[3]) for r in recs]
+    mrg_ms = [r[3].elapsed_time(r[4]) for r in recs]
+    # whole job: the work of all ranks over the slowest rank's time
+    pre_total = max_over_ranks(sum(plan_ms) + sum(pre_ms), world)
+    dec_total = max_over_ranks(sum(dec_ms) + sum(mrg_ms), world)
+    value = world * p_flops * args.steps / (pre_total / 1e3) / 1e12 if do_pre else None
+    dec_gbs = world * d_bytes * args.steps / (dec_total / 1e3) / 1e9 if do_dec else None
+
+    # ---- end to end through the public API with host buffers (prefill)
+    e2e = None
+    if do_pre:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            plan = cp.cp_shard_plan(cp.CP_ZIGZAG, C, nl, pl, device=dev)
+            cp.cp_prefill_attn(plan, qd, kd, vd, scale, out=o, lse=lse)
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+        e2e = {"value": world * p_flops * args.steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
+               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4}
+
+    if rank != 0:
+        return
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    roof = dec = None
+    if do_pre:
+        pre_avg = statistics.mean(pre_ms)
+        achieved = p_flops / (pre_avg / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind + " burst",
+                "kernel": "prefill_tc_kernel<128>"}
+    if do_dec:
+        dec_avg = statistics.mean(dec_ms)
+        dec_ach = d_bytes / (dec_avg / 1e3) / 1e9
+        dec = {"metric": "decode KV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
+               "ms_decode": dec_avg, "ms_merge": statistics.mean(mrg_ms),
+               "merge_share": statistics.mean(mrg_ms) / (dec_avg + statistics.mean(mrg_ms)),
+               "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
+                            "frac": dec_ach / hbm, "traffic": None, "peak_kind": peak_kind}}
+    cpu = None
+    if not args.no_cpu:
+        cpu_tf, cpu_s, cpu_rows, cores = oracle_prefill_sample(rows_per_call=32, budget_s=12.0)
+        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{cpu_rows} query rows x 32 heads of rank 0's late zigzag block, "
+                         f"fp64 numpy, {cpu_s:.1f} s"}
+    line = {
+        "metric": "prefill causal-attn TFLOP/s",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "timed": args.only,
+            "prefill_flops_per_step": p_flops,
+            "decode_bytes_per_step": d_bytes,
+            "l2": "inputs larger than L2 (K/V 151 MB, Q 268 MB, FP8 cache 4.9 GB); no flush",
+            "parallelism": "virtual CP=8 on each GPU; replicas across GPUs",
+        },
+        "decode": dec,
+        "ms_breakdown": {"plan": statistics.mean(plan_ms), "prefill": statistics.mean(pre_ms),
+                         "decode": statistics.mean(dec_ms), "merge": statistics.mean(mrg_ms)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * ((2 if do_pre else 0) + n_dec_kernels),
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="time one half of the step (for profiler captures)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
