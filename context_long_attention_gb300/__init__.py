@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     DecodePlan,
     PrefillPlan,
     cp_decode_attn,
+    cp_decode_attn_noalloc,
     cp_decode_plan,
     cp_decode_workspace_size,
     cp_device_error_check,

@@ -53,7 +53,10 @@ _SIGS = {
     "cp_decode_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp,
                             _vp, _sz, _vp]),
     "cp_lse_merge": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
+    "cp_decode_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
+                                    _vp, _vp]),
 }
+NOALLOC_SCRATCH_BYTES = 16 << 20
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.restype = _res
@@ -303,6 +306,34 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
                               _ptr_array(shard_scale) if shard_scale is not None else None,
                               H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part), _ptr(lse_part),
                               _ptr(ws), ws_bytes, _stream(q.device)))
+    return o_part, lse_part
+
+
+def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None,
+                           shard_scale=None, sm_scale=None, o_part=None, lse_part=None):
+    """cp_decode_attn without a workspace argument: the split-KV scratch is a
+    fixed library-owned device array (NOALLOC_SCRATCH_BYTES).  Calls must not
+    overlap on the GPU."""
+    B, H, Dqk = q.shape
+    _need_cuda(q, *[t for t in shard_k if t is not None])
+    sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in shard_k]
+    kv_dtype = _dtype_code(sk[0]) if sk else CP_BF16
+    if mode == CP_DECODE_MLA:
+        Hkv, Dv = 1, 512
+    else:
+        Hkv, Dv = sk[0].shape[1], Dqk
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(Dqk)
+    C = plan.C
+    if o_part is None:
+        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+    _check(lib.cp_decode_attn_noalloc(
+        _np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q), _ptr_array(sk),
+        _ptr_array(shard_v) if shard_v is not None else None,
+        _ptr_array(shard_scale) if shard_scale is not None else None, H, Hkv, Dqk, Dv,
+        float(sm_scale), _ptr(o_part), _ptr(lse_part), _stream(q.device)))
     return o_part, lse_part
 
 

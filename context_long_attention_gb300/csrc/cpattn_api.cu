@@ -390,6 +390,16 @@ size_t elem_size(cp_dtype d) { return d == CP_FP32 ? 4 : d == CP_BF16 ? 2 : 1; }
 }  // namespace
 
 namespace cpattn {
+cp_status report_error(cp_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
 unsigned* device_status_ptr() {
   static unsigned* ptrs[256] = {nullptr};
   int dev = 0;

@@ -36,6 +36,9 @@ struct MutScalePtrs {
 // Returns the device address of this device's status words (set up once per device).
 unsigned* device_status_ptr();
 
+// Records a message for cp_last_error() on this thread and returns `st`.
+cp_status report_error(cp_status st, const char* fmt, ...);
+
 // ---- plan / pack / merge kernels (plan_kernels.cu)
 cudaError_t launch_plan_maps(const int32_t* dev_plan, int n_seg, int off_seg, int off_idx,
                              int off_qpos, int off_qreq, cudaStream_t s);

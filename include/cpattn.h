@@ -297,6 +297,37 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
 cp_status cp_lse_merge(int P, int N, int H, int Dv, const float* o_part, const float* lse_part,
                        void* o, cp_dtype o_dtype, float* lse, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * cp_decode_attn_noalloc — cp_decode_attn for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is an interface convenience.  Some
+ * callers cannot allocate device memory where they call the decode: code
+ * inside a CUDA-graph capture that must not grow the memory pool, serving
+ * loops with a fixed memory budget, plugins reached through a C interface
+ * without an allocator.  This entry point takes the same arguments as
+ * cp_decode_attn minus the workspace, and keeps the split-KV partial results
+ * in a library-owned static device array of CP_NOALLOC_SCRATCH_BYTES.
+ *
+ * - Memory: the array is part of the loaded library; every GPU that loads it
+ *   holds the array until the process exits.  Nothing is allocated per call.
+ * - Limit: a plan that needs more scratch than the array
+ *   (cp_decode_workspace_size > CP_NOALLOC_SCRATCH_BYTES) is rejected with
+ *   CP_ERR_WORKSPACE and a message; nothing is launched.
+ * - Sharing: all calls use the same array and it keeps the last call's
+ *   contents; nothing in it needs to start at zero (each slot is fully written
+ *   before it is read within one call).  Calls that overlap on the GPU race
+ *   on the array: serialise them on one stream.
+ * - Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, that device current); make that first call before
+ *   any stream capture begins.
+ * ------------------------------------------------------------------------- */
+#define CP_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per device */
+cp_status cp_decode_attn_noalloc(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                                 cp_dtype kv_dtype, const void* q, const void* const* shard_k,
+                                 const void* const* shard_v, const float* const* shard_scale,
+                                 int Hq, int Hkv, int Dqk, int Dv, float sm_scale, float* o_part,
+                                 float* lse_part, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
