@@ -237,14 +237,21 @@ def run_ours(args, world, rank, local):
     # ---- decode inputs (MLA, FP8 cache, packed into token shards once)
     m = W.WORKLOADS["mla"]
     ctx = [m["ctx"]] * m["B"]
-    d_bytes = decode_bytes(ctx, m["H"], fp8=True)
+    fp8 = args.decode_kv == "fp8"
+    d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
     dscale = 1.0 / math.sqrt(m["Dqk"])
     n_dec_kernels = 0
     if do_dec:
-        data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev, bf16=False)
+        data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev,
+                                   bf16=not fp8, fp8=fp8)
         dplan = cp.cp_decode_plan(m["C"], ctx, device=dev)
-        shards, scales = cp.cp_kv_shard_pack(dplan, data["kv_fp8"], data["kv_scale"])
-        del data["kv_fp8"], data["kv_scale"]
+        if fp8:
+            shards, scales = cp.cp_kv_shard_pack(dplan, data["kv_fp8"], data["kv_scale"])
+            del data["kv_fp8"], data["kv_scale"]
+        else:
+            shards, _ = cp.cp_kv_shard_pack(dplan, data["kv_bf16"])
+            scales = None
+            del data["kv_bf16"]
         dq = data["q"]
         o_part = torch.empty((m["C"], m["B"], m["H"], m["Dv"]), dtype=torch.float32, device=dev)
         lse_part = torch.empty((m["C"], m["B"], m["H"]), dtype=torch.float32, device=dev)
@@ -355,6 +362,7 @@ def run_ours(args, world, rank, local):
         dec_avg = statistics.mean(dec_ms)
         dec_ach = d_bytes / (dec_avg / 1e3) / 1e9
         dec = {"metric": "decode KV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
+               "kv": args.decode_kv,
                "ms_decode": dec_avg, "ms_merge": statistics.mean(mrg_ms),
                "merge_share": statistics.mean(mrg_ms) / (dec_avg + statistics.mean(mrg_ms)),
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
@@ -407,6 +415,8 @@ def main():
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time one half of the step (for profiler captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--decode-kv", choices=["fp8", "bf16"], default="fp8",
+                    help="decode cache type (the MLA workload has both)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

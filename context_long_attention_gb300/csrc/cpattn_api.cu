@@ -582,7 +582,7 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   if (mode != CP_DECODE_MLA && mode != CP_DECODE_GQA) return fail(CP_ERR_INVALID_ARG, "bad mode");
   if (mla) {
     if (Dqk != 576 || Dv != 512 || Hkv != 1) return fail(CP_ERR_UNSUPPORTED, "MLA needs Dqk=576, Dv=512, Hkv=1");
-    if (Hq < 1 || Hq > 128) return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d outside [1, 128]", Hq);
+    if (Hq < 1 || Hq > 64) return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d outside [1, 64]", Hq);
     if (kv_dtype != CP_BF16 && kv_dtype != CP_FP8_E4M3) return fail(CP_ERR_UNSUPPORTED, "MLA cache must be bf16 or fp8");
     if (shard_v) return fail(CP_ERR_INVALID_ARG, "MLA takes values from the latent: shard_v must be NULL");
     if ((kv_dtype == CP_FP8_E4M3) != (shard_scale != nullptr))
@@ -619,8 +619,11 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   float* ws_o = (float*)ws;
   float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hq * Dv : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_decode_simt((const int32_t*)dev_plan, h, mla, kv_dtype, q, K, V, S, Hq,
-                                     Hkv, Dqk, Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
+  cudaError_t e =
+      mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, kv_dtype == CP_FP8_E4M3, q, K, S, Hq,
+                                 sm_scale, o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+          : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, Hq, Hkv, Dqk,
+                               Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
   if (h.n_split) {
     e = launch_decode_fixup((const int32_t*)dev_plan, h, Hq, Dv, ws_o, ws_lse, o_part, lse_part, s);

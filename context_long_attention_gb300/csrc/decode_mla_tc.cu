@@ -1,0 +1,489 @@
+// MLA split-KV decode on the tcgen05 tensor cores.
+//
+// One decode query per request (64 heads x 576 dims) against the rows a
+// virtual shard stores ("How GPUs Share a Long Context During LLM Inference"
+// §3.1-3.4): every head reads the same 576-dim latent entry of each token
+// (§1.3); keys are the whole entry and values its first 512 dims (vLLM blog
+// "GLM-5.3 Part 2", footnote 1).  Each work item (a row range of one
+// (shard, request) pair, from the decode plan) yields a partial O and the
+// natural-log LSE over its rows, merged later exactly (§3.3).
+//
+// The products are transposed so that the MMA M dimension is 128 KV rows:
+//   S^T [128 rows x 64 heads]  = K_tile [128 x 576] . Q^T          (K = 576)
+//   O^T [512 dims x 64 heads] += V_tile^T [512 x 128] . P^T        (K = 128)
+// V_tile^T is the same shared-memory tile as K_tile read as an MN-major
+// operand (V is the first 512 latent dims), so one bf16 tile serves both
+// products.  P^T (bf16) goes over the tile's last 64-dim chunk, which only
+// the first product reads.  An FP8 cache is expanded to bf16 exactly: the
+// E4M3 bits move into a bf16 whose value is 2^-120 times the code's value
+// (exponent bias 127 instead of 7), and the 2^120 and the per-token scale are
+// applied to the scores and folded into P^T.
+//
+// Warp roles (288 threads): warps 0-3 softmax, thread = KV row of the tile
+// (TMEM lane) and, in the epilogue, dim row of O^T; warps 4-7 fill the tile
+// from global memory (row = thread, 16-byte loads) and prefetch the next
+// tiles into L2; warp 8 owns TMEM and issues the MMAs.
+// Softmax down the KV axis needs per-head maxima over the 128 rows of a tile.
+// The running maximum M_h used in the exponentials only moves when some score
+// exceeds it by more than 2^8 (checked per tile with one block-wide vote);
+// then a column max is reduced with redux.sync and O^T and the per-thread
+// partial sums are rescaled.  Any M_h gives the exact result; this one keeps
+// every exponential <= 2^8.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace cpattn {
+namespace {
+using namespace tc;
+
+constexpr int kRows = 128;      // KV rows per tile (MMA M)
+constexpr int kHeads = 64;      // MMA N (query heads, zero-padded)
+constexpr int kDqk = 576, kDv = 512;
+constexpr int kChunks = kDqk / 64;          // 9 chunks of 64 dims (128 B bf16 rows)
+constexpr int kChunkBytes = kRows * 128;    // one chunk of the tile: 16 KB
+constexpr int kTileBytes = kChunks * kChunkBytes;  // 147,456 B
+constexpr int kQChunkBytes = kHeads * 128;  // one chunk of Q: 8 KB
+constexpr int kQBytes = kChunks * kQChunkBytes;    // 73,728 B
+constexpr int kSmem = kTileBytes + kQBytes + 1024;
+constexpr int kThreads = 288;
+constexpr int kWarpMma = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kTwo120 = 1.329227995784916e36f;  // 2^120
+
+struct Params {
+  const int32_t* plan;
+  int B, off_pair, off_worker, off_work;
+  const __nv_bfloat16* q;
+  ShardPtrs k;
+  ScalePtrs sc;
+  int H;
+  float scale_log2;  // sm_scale * log2(e)
+  float* o_part;
+  float* lse_part;
+  float* ws_o;
+  float* ws_lse;
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ int ordered(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float unordered(int b) {
+  return __int_as_float(b >= 0 ? b : b ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
+  *abort = 1;
+  if (atomicCAS(status, 0u, 1u) == 0u) {
+    status[1] = kKernDecodeMlaTc;
+    status[2] = site;
+    status[3] = blockIdx.x;
+    __threadfence();
+  }
+}
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Four E4M3 codes -> four bf16 whose values are 2^-120 x the codes' values.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4_scaled(uint32_t w) {
+  const uint32_t lo = __byte_perm(w, 0u, 0x4140);  // bytes 0,1 -> bits [0,8) and [16,24)
+  const uint32_t hi = __byte_perm(w, 0u, 0x4342);  // bytes 2,3
+  uint2 r;
+  r.x = ((lo & 0x00800080u) << 8) | ((lo & 0x007F007Fu) << 4);
+  r.y = ((hi & 0x00800080u) << 8) | ((hi & 0x007F007Fu) << 4);
+  return r;
+}
+
+template <bool FP8>
+__global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sTile = smem;                  // [9 chunks][128 rows x 128 B]
+  uint8_t* sQ = smem + kTileBytes;        // [9 chunks][64 heads x 128 B]
+  uint8_t* sP = sTile + 8 * kChunkBytes;  // P^T over the last chunk: [128 rows][64 heads]
+  __shared__ __align__(8) uint64_t bar_fill, bar_s, bar_p, bar_pv, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int zero_flag;
+  __shared__ float sM[kHeads];     // running max per head (log2 units)
+  __shared__ float sAlpha[kHeads];
+  __shared__ float sDelta[kHeads];
+  __shared__ int sRed[4][kHeads];  // cross-warp column maxima
+  __shared__ float sL[4][kHeads];  // cross-warp column sums
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar_fill), 128);
+    mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_p), 128);
+    mbar_init(smem_u32(&bar_pv), 1);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    zero_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;  // S^T: cols [0,64); O^T block mb: [64 + 64 mb, 128 + 64 mb)
+
+  const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair);
+  const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work);
+  const int w0 = p.plan[p.off_worker + blockIdx.x], w1 = p.plan[p.off_worker + blockIdx.x + 1];
+  constexpr int kRowBytes = FP8 ? kDqk : 2 * kDqk;
+  // Every barrier completes exactly once per tile, so the parity of the phase
+  // to wait for is that of the tile's index g over all items of this CTA.
+  int g0 = 0;
+  bool ok = true;
+
+  for (int wi = w0; wi < w1 && ok; ++wi) {
+    const cp_work_desc wd = work[wi];
+    const int r = wd.pair / p.B, b = wd.pair % p.B;
+    const cp_pair_desc pd = pairs[wd.pair];
+    const int nrows = wd.row_end - wd.row_begin;
+    const int ntiles = (nrows + kRows - 1) / kRows;
+    const long long row0 = (long long)pd.row_off + wd.row_begin;  // first shard row
+    float* out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
+                               : p.ws_o + (long long)wd.part * p.H * kDv;
+    float* out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
+                               : p.ws_lse + (long long)wd.part * p.H;
+    if (ntiles == 0) {  // empty shard: O = 0, LSE = -inf
+      for (int i = threadIdx.x; i < p.H * kDv; i += kThreads) out_o[i] = 0.f;
+      for (int i = threadIdx.x; i < p.H; i += kThreads) out_l[i] = -INFINITY;
+      continue;
+    }
+    const uint8_t* kbase = static_cast<const uint8_t*>(p.k.p[r]) + row0 * kRowBytes;
+    const float* sbase = FP8 ? p.sc.p[r] + row0 : nullptr;
+
+    // ---- the query of request b -> sQ (K-major, 128-byte swizzle); heads >= H are zero.
+    // The previous item's MMAs have completed: its softmax waited for its last P.V.
+    for (int i = threadIdx.x; i < kHeads * (kDqk / 8); i += kThreads) {
+      const int h = i / (kDqk / 8), piece = i % (kDqk / 8);
+      const int c = piece >> 3, cc = piece & 7;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (h < p.H)
+        v = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.H + h) * kDqk) + piece);
+      *reinterpret_cast<uint4*>(sQ + c * kQChunkBytes + h * 128 + ((cc ^ (h & 7)) << 4)) = v;
+    }
+    if (threadIdx.x < kHeads) sM[threadIdx.x] = 0.f;  // set from the first tile's maxima
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    if (warp >= 4 && warp < 8) {
+      // ------------------------------------------------------------ tile fill
+      const int t = threadIdx.x - 128;  // tile row
+      for (int j = 0; j < ntiles; ++j) {
+        const int g = g0 + j;
+        if (t == 0) {  // keep the next two tiles on their way into L2
+          for (int a = 1; a <= 2; ++a) {
+            const int jj = j + a;
+            if (jj < ntiles) {
+              const int rows = min(kRows, nrows - jj * kRows);
+              prefetch_l2(kbase + (long long)jj * kRows * kRowBytes, (uint32_t)rows * kRowBytes);
+            }
+          }
+        }
+        if (j > 0) {  // the tile is free once the previous P.V has read it
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g - 1) & 1, p.wait_ns, &abort_flag))) {
+            report_timeout(p.status, 1, &abort_flag);
+            ok = false;
+            break;
+          }
+        }
+        const int row = j * kRows + t;
+        const bool valid = row < nrows;
+        uint8_t* dst = sTile + t * 128;
+        if (FP8) {
+          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk);
+#pragma unroll
+          for (int grp = 0; grp < 3; ++grp) {  // 3 x 12 loads of 16 codes
+            uint4 v[12];
+#pragma unroll
+            for (int e = 0; e < 12; ++e)
+              v[e] = valid ? __ldg(src + grp * 12 + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < 12; ++e) {
+              const int piece16 = grp * 12 + e;  // 16 codes = 32 B of bf16
+              const int c = piece16 >> 2;        // 64-dim chunk
+              const int cc0 = (piece16 & 3) * 2; // first of two 16-byte pieces in the row
+              const uint2 a0 = e4m3x4_to_bf16x4_scaled(v[e].x), a1 = e4m3x4_to_bf16x4_scaled(v[e].y);
+              const uint2 a2 = e4m3x4_to_bf16x4_scaled(v[e].z), a3 = e4m3x4_to_bf16x4_scaled(v[e].w);
+              uint8_t* base = dst + c * kChunkBytes;
+              *reinterpret_cast<uint4*>(base + ((cc0 ^ (t & 7)) << 4)) =
+                  make_uint4(a0.x, a0.y, a1.x, a1.y);
+              *reinterpret_cast<uint4*>(base + (((cc0 + 1) ^ (t & 7)) << 4)) =
+                  make_uint4(a2.x, a2.y, a3.x, a3.y);
+            }
+          }
+        } else {
+          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * 2 * kDqk);
+#pragma unroll
+          for (int grp = 0; grp < 6; ++grp) {  // 6 x 12 loads of 8 bf16
+            uint4 v[12];
+#pragma unroll
+            for (int e = 0; e < 12; ++e)
+              v[e] = valid ? __ldg(src + grp * 12 + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int e = 0; e < 12; ++e) {
+              const int piece = grp * 12 + e;
+              const int c = piece >> 3, cc = piece & 7;
+              *reinterpret_cast<uint4*>(dst + c * kChunkBytes + ((cc ^ (t & 7)) << 4)) = v[e];
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bar_fill));
+      }
+    } else if (warp == kWarpMma) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
+        const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
+        const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
+        for (int j = 0; j < ntiles; ++j) {
+          const int g = g0 + j;
+          if (!mbar_wait(smem_u32(&bar_fill), g & 1, p.wait_ns, &abort_flag)) {
+            report_timeout(p.status, 3, &abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 4
+          for (int kk = 0; kk < kDqk / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem, smem_desc(tile + off, 16, 1024), smem_desc(qb + qoff, 16, 1024), idS,
+                   kk > 0);
+          }
+          mma_commit(smem_u32(&bar_s));
+          if (!mbar_wait(smem_u32(&bar_p), g & 1, p.wait_ns, &abort_flag)) {
+            report_timeout(p.status, 4, &abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int mb = 0; mb < kDv / 128; ++mb)
+#pragma unroll
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_ss(tmem + 64 + 64 * mb,
+                     smem_desc(tile + 2 * mb * kChunkBytes + kk * 2048, kChunkBytes, 1024),
+                     smem_desc(pb + kk * 2048, 16, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_pv));
+        }
+      }
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ softmax (warps 0-3)
+      const int t = threadIdx.x;  // tile row = TMEM lane
+      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+      float l[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
+      for (int j = 0; j < ntiles; ++j) {
+        const int g = g0 + j;
+        const bool valid = j * kRows + t < nrows;
+        // scores in log2 units; the FP8 tile holds 2^-120 x the codes
+        float cj = p.scale_log2, vscale = 1.f;
+        if (FP8) {
+          vscale = valid ? __ldg(sbase + j * kRows + t) : 0.f;
+          cj = p.scale_log2 * vscale * kTwo120;
+        }
+        // The four softmax warps leave together: a warp that gave up still
+        // meets the others at the named barrier of this vote.
+        const bool got =
+            __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s), g & 1, p.wait_ns, &abort_flag));
+        if (bar_red_or(1, 128, !got)) {
+          if (!got) report_timeout(p.status, 6, &abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // u = score - running max (log2 units); invalid rows read nothing
+        float u[kHeads];
+        float over = -INFINITY;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t a[32];
+          tmem_ld32(lane_addr + 32 * half, a);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const int hh = 32 * half + h;
+            u[hh] = valid ? fmaf(__uint_as_float(a[h]), cj, -sM[hh]) : -INFINITY;
+            over = fmaxf(over, u[hh]);
+          }
+        }
+        // Block-wide vote: does any score pass its running max by more than 2^8?
+        if (bar_red_or(1, 128, j == 0 || over > kRescaleLog2)) {
+          // column maxima of this tile (relative to the old running max)
+#pragma unroll
+          for (int h = 0; h < kHeads; ++h) {
+            const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
+            if (lane == 0) sRed[warp][h] = m;
+          }
+          named_bar_sync(1, 128);
+          if (t < kHeads) {
+            const float cm = fmaxf(fmaxf(unordered(sRed[0][t]), unordered(sRed[1][t])),
+                                   fmaxf(unordered(sRed[2][t]), unordered(sRed[3][t])));
+            // move the running max to this tile's max on the first tile, or when it
+            // grew by more than 2^8; earlier sums and O^T shrink by 2^-delta
+            const float delta = (j == 0 || cm > kRescaleLog2) ? cm : 0.f;
+            sAlpha[t] = j == 0 ? 0.f : ex2(-delta);
+            sDelta[t] = delta;
+            sM[t] += delta;
+          }
+          named_bar_sync(1, 128);
+#pragma unroll
+          for (int h = 0; h < kHeads; ++h) {
+            l[h] *= sAlpha[h];
+            u[h] -= sDelta[h];
+          }
+          if (j > 0) {  // O^T holds earlier tiles (their P.V completed before this S)
+            // 16 columns at a time: u and l stay in registers meanwhile
+#pragma unroll 1
+            for (int c = 0; c < 4 * kHeads / 16; ++c) {
+              uint32_t a[16];
+              tmem_ld16(lane_addr + 64 + 16 * c, a);
+              tmem_ld_wait();
+              const float* al = sAlpha + ((16 * c) & (kHeads - 1));
+#pragma unroll
+              for (int h = 0; h < 16; ++h) a[h] = __float_as_uint(__uint_as_float(a[h]) * al[h]);
+              tmem_st16(lane_addr + 64 + 16 * c, a);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P^T row t: p = 2^u; the value weights carry the token's scale.
+        // MN-major B operand: row t = 64 heads x 2 B = one 128-byte swizzled row.
+        uint8_t* prow = sP + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int h = 8 * c + 2 * e;
+            const float p0 = ex2(u[h]), p1 = ex2(u[h + 1]);
+            l[h] += p0;
+            l[h + 1] += p1;
+            pk[e] = pack_bf16x2(p0 * vscale, p1 * vscale);
+          }
+          *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p));
+      }
+      // ---- epilogue: column sums of l, O^T / l, LSE
+      const bool landed =
+          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g0 + ntiles - 1) & 1,
+                                                  p.wait_ns, &abort_flag));
+      if (bar_red_or(1, 128, !landed)) {
+        if (ok && !landed) report_timeout(p.status, 7, &abort_flag);
+        ok = false;
+      }
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < kHeads; ++h) {
+          float v = l[h];
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+          if (lane == 0) sL[warp][h] = v;
+        }
+        named_bar_sync(1, 128);
+        const float oscale = FP8 ? kTwo120 : 1.f;
+#pragma unroll 1
+        for (int mb = 0; mb < kDv / 128; ++mb) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32];
+            tmem_ld32(lane_addr + 64 + 64 * mb + 32 * half, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              const int hh = 32 * half + h;
+              if (hh < p.H) {
+                const float tot = sL[0][hh] + sL[1][hh] + sL[2][hh] + sL[3][hh];
+                out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * oscale / tot;
+              }
+            }
+          }
+        }
+        if (t < p.H) {
+          const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
+          out_l[t] = (sM[t] + lg2(tot)) * kLn2;
+        }
+      }
+    }
+    g0 += ntiles;
+    // every role learns whether one gave up; shared state is free for the next item
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    ok = ok && !abort_flag;
+  }
+  // Never free TMEM under a running MMA.
+  if (warp == kWarpMma && lane == 0) {
+    mma_commit(smem_u32(&bar_drain));
+    mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
+                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc, int H,
+                                 float sm_scale, float* o_part, float* lse_part, float* ws_o,
+                                 float* ws_lse, unsigned long long wait_ns, cudaStream_t s) {
+  Params p;
+  p.plan = dev_plan;
+  p.B = h.R;
+  p.off_pair = h.off_rank;
+  p.off_worker = h.off_req;
+  p.off_work = h.off_seg;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = k;
+  p.sc = sc;
+  p.H = H;
+  p.scale_log2 = sm_scale * kLog2e;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevice;
+  p.wait_ns = wait_ns;
+  auto kern = fp8 ? decode_mla_tc_kernel<true> : decode_mla_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<h.n_tiles, kThreads, kSmem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -59,12 +59,19 @@ cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
                               const void* v, int Hq, int Hkv, int D, float sm_scale, void* o,
                               float* lse, bool stall_test, cudaStream_t s);
 
+// ---- tensor-core MLA decode (decode_mla_tc.cu)
+cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
+                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc, int H,
+                                 float sm_scale, float* o_part, float* lse_part, float* ws_o,
+                                 float* ws_lse, unsigned long long wait_ns, cudaStream_t s);
+unsigned long long wait_limit_ns();
+
 // ---- CUDA-core attention (simt_attn.cu)
 cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h, int rank,
                                 int row_begin, int n_rows, bool bf16, const void* q,
                                 const void* k, const void* v, int Hq, int Hkv, int D,
                                 float sm_scale, void* o, float* lse, cudaStream_t s);
-cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h, bool mla,
+cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
                                const ShardPtrs& v, const ScalePtrs& sc, int Hq, int Hkv, int Dqk,
                                int Dv, float sm_scale, float* o_part, float* lse_part,

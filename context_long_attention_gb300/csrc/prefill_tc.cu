@@ -431,15 +431,6 @@ bool make_kv_map(CUtensorMap* m, const void* base, int rows, int H, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-unsigned long long wait_limit_ns() {
-  static unsigned long long v = [] {
-    const char* s = getenv("CPATTN_WAIT_LIMIT_MS");
-    const long long ms = s ? atoll(s) : 4000;
-    return (unsigned long long)(ms > 0 ? ms : 4000) * 1000000ull;
-  }();
-  return v;
-}
-
 template <int D>
 cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params& p,
                      cudaStream_t s) {
@@ -453,6 +444,17 @@ cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params&
 }
 
 }  // namespace
+
+// Limit of every bounded device wait: CPATTN_WAIT_LIMIT_MS (default 4000 ms),
+// read once per process.
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* s = getenv("CPATTN_WAIT_LIMIT_MS");
+    const long long ms = s ? atoll(s) : 4000;
+    return (unsigned long long)(ms > 0 ? ms : 4000) * 1000000ull;
+  }();
+  return v;
+}
 
 cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
                               const cp_plan_header& h, int rank, const void* q, const void* k,

@@ -1,4 +1,4 @@
-// CUDA-core attention kernels: the fp32 prefill path and the split-KV decode.
+// CUDA-core attention kernels: the fp32 prefill path and the GQA split-KV decode.
 //
 // Both compute the attention definition of "How GPUs Share a Long Context
 // During LLM Inference" §1.1 (a query reads every key up to and including
@@ -7,7 +7,6 @@
 // One warp owns one (query row, head); lane l holds dims l, l+32, ... so that
 // every key/value row is read with coalesced loads.
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
 
 #include "internal.h"
 
@@ -17,10 +16,6 @@ namespace {
 __device__ __forceinline__ float ld_elem(const float* p, long long i) { return p[i]; }
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
-}
-__device__ __forceinline__ float ld_elem(const uint8_t* p, long long i) {
-  __half_raw h = __nv_cvt_fp8_to_halfraw(p[i], __NV_E4M3);
-  return __half2float(__half(h));
 }
 __device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) {
@@ -92,20 +87,21 @@ __global__ void prefill_simt_kernel(const int32_t* __restrict__ plan, int off_re
 
 // ------------------------------------------------------------------ decode
 
-// NQ: key dims per lane (Dqk / 32); NV: value dims per lane (Dv / 32).
-// MLA: keys are whole latent rows, values their first Dv dims (same row).
-template <typename KT, typename QT, int NQ, int NV, bool MLA>
-__global__ void decode_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
-                                   int off_worker, int off_work, const QT* __restrict__ q,
-                                   ShardPtrs kp, ShardPtrs vp, ScalePtrs sp, int Hq, int Hkv,
-                                   float sm_scale, float* __restrict__ o_part,
-                                   float* __restrict__ lse_part, float* __restrict__ ws_o,
-                                   float* __restrict__ ws_lse) {
-  constexpr int Dqk = NQ * 32, Dv = NV * 32;
+// GQA split-KV decode: a warp owns one (query head, work item) and walks the
+// item's shard rows; ND dims per lane (D / 32).  It is HBM-bound at a few
+// FLOP per byte (Hq/Hkv heads reuse each K/V row), so it runs on the CUDA
+// cores with coalesced loads.
+template <typename T, int ND>
+__global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
+                                       int off_worker, int off_work, const T* __restrict__ q,
+                                       ShardPtrs kp, ShardPtrs vp, int Hq, int Hkv, float sm_scale,
+                                       float* __restrict__ o_part, float* __restrict__ lse_part,
+                                       float* __restrict__ ws_o, float* __restrict__ ws_lse) {
+  constexpr int D = ND * 32;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (h >= Hq) return;
-  const int g = MLA ? 0 : h / (Hq / Hkv);
+  const int g = h / (Hq / Hkv);
   const int w0 = plan[off_worker + blockIdx.x], w1 = plan[off_worker + blockIdx.x + 1];
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(plan + off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(plan + off_work);
@@ -113,38 +109,35 @@ __global__ void decode_simt_kernel(const int32_t* __restrict__ plan, int B, int 
     const cp_work_desc wd = work[wi];
     const int r = wd.pair / B, b = wd.pair % B;
     const cp_pair_desc pd = pairs[wd.pair];
-    float qv[NQ];
+    float qv[ND];
 #pragma unroll
-    for (int e = 0; e < NQ; ++e) qv[e] = ld_elem(q, ((long long)b * Hq + h) * Dqk + lane + 32 * e);
-    const KT* kb = static_cast<const KT*>(kp.p[r]);
-    const KT* vb = static_cast<const KT*>(vp.p[r]);
-    const float* sb = sp.p[r];
-    RowState<NV> st;
+    for (int e = 0; e < ND; ++e) qv[e] = ld_elem(q, ((long long)b * Hq + h) * D + lane + 32 * e);
+    const T* kb = static_cast<const T*>(kp.p[r]);
+    const T* vb = static_cast<const T*>(vp.p[r]);
+    RowState<ND> st;
     for (int row = wd.row_begin; row < wd.row_end; ++row) {
-      const long long srow = (long long)pd.row_off + row;
-      const long long kr = MLA ? srow * Dqk : (srow * Hkv + g) * Dqk;
-      const float sc = sb ? sb[srow] : 1.f;
-      float part = 0.f, vv[NV];
+      const long long kr = (((long long)pd.row_off + row) * Hkv + g) * D + lane;
+      float part = 0.f, vv[ND];
 #pragma unroll
-      for (int e = 0; e < NQ; ++e) part += qv[e] * ld_elem(kb, kr + lane + 32 * e);
-#pragma unroll
-      for (int e = 0; e < NV; ++e)
-        vv[e] = sc * (MLA ? ld_elem(kb, kr + lane + 32 * e) : ld_elem(vb, kr + lane + 32 * e));
-      st.add(sm_scale * sc * warp_sum(part), vv);
+      for (int e = 0; e < ND; ++e) {
+        part += qv[e] * ld_elem(kb, kr + 32 * e);
+        vv[e] = ld_elem(vb, kr + 32 * e);
+      }
+      st.add(sm_scale * warp_sum(part), vv);
     }
     float* ob;
     float* lb;
     if (wd.part < 0) {
-      ob = o_part + ((long long)wd.pair * Hq + h) * Dv;
+      ob = o_part + ((long long)wd.pair * Hq + h) * D;
       lb = lse_part + (long long)wd.pair * Hq + h;
     } else {
-      ob = ws_o + ((long long)wd.part * Hq + h) * Dv;
+      ob = ws_o + ((long long)wd.part * Hq + h) * D;
       lb = ws_lse + (long long)wd.part * Hq + h;
     }
     const bool empty = st.l == 0.f;
     const float inv = empty ? 0.f : 1.f / st.l;
 #pragma unroll
-    for (int e = 0; e < NV; ++e) ob[lane + 32 * e] = st.acc[e] * inv;
+    for (int e = 0; e < ND; ++e) ob[lane + 32 * e] = st.acc[e] * inv;
     if (lane == 0) *lb = empty ? -INFINITY : st.m + logf(st.l);
   }
 }
@@ -162,15 +155,15 @@ cudaError_t prefill_simt_t(const int32_t* plan, const cp_plan_header& h, int ran
   return cudaGetLastError();
 }
 
-template <typename KT, typename QT, int NQ, int NV, bool MLA>
-cudaError_t decode_simt_t(const int32_t* plan, const cp_plan_header& h, const void* q,
-                          const ShardPtrs& k, const ShardPtrs& v, const ScalePtrs& sc, int Hq,
-                          int Hkv, float sm_scale, float* o_part, float* lse_part, float* ws_o,
-                          float* ws_lse, cudaStream_t s) {
+template <typename T, int ND>
+cudaError_t decode_gqa_t(const int32_t* plan, const cp_plan_header& h, const void* q,
+                         const ShardPtrs& k, const ShardPtrs& v, int Hq, int Hkv, float sm_scale,
+                         float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                         cudaStream_t s) {
   const int warps = 4;
   dim3 grid(h.n_tiles, (Hq + warps - 1) / warps);
-  decode_simt_kernel<KT, QT, NQ, NV, MLA><<<grid, warps * 32, 0, s>>>(
-      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const QT*>(q), k, v, sc, Hq, Hkv,
+  decode_gqa_simt_kernel<T, ND><<<grid, warps * 32, 0, s>>>(
+      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, Hq, Hkv,
       sm_scale, o_part, lse_part, ws_o, ws_lse);
   return cudaGetLastError();
 }
@@ -198,27 +191,20 @@ cudaError_t launch_prefill_simt(const int32_t* plan, const cp_plan_header& h, in
 #undef CP_PREFILL_CASE
 }
 
-cudaError_t launch_decode_simt(const int32_t* plan, const cp_plan_header& h, bool mla,
+cudaError_t launch_decode_simt(const int32_t* plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
                                const ShardPtrs& v, const ScalePtrs& sc, int Hq, int Hkv, int Dqk,
                                int Dv, float sm_scale, float* o_part, float* lse_part,
                                float* ws_o, float* ws_lse, cudaStream_t s) {
-  if (mla) {
-    if (kv_dtype == CP_FP8_E4M3)
-      return decode_simt_t<uint8_t, __nv_bfloat16, 18, 16, true>(plan, h, q, k, v, sc, Hq, 1,
-                                                                 sm_scale, o_part, lse_part, ws_o,
-                                                                 ws_lse, s);
-    return decode_simt_t<__nv_bfloat16, __nv_bfloat16, 18, 16, true>(
-        plan, h, q, k, v, sc, Hq, 1, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
-  }
-#define CP_GQA_CASE(ND)                                                                          \
-  case ND:                                                                                       \
-    return kv_dtype == CP_BF16                                                                   \
-               ? decode_simt_t<__nv_bfloat16, __nv_bfloat16, ND, ND, false>(                     \
-                     plan, h, q, k, v, sc, Hq, Hkv, sm_scale, o_part, lse_part, ws_o, ws_lse, s) \
-               : decode_simt_t<float, float, ND, ND, false>(plan, h, q, k, v, sc, Hq, Hkv,       \
-                                                            sm_scale, o_part, lse_part, ws_o,    \
-                                                            ws_lse, s);
+  (void)sc;
+  (void)Dv;
+#define CP_GQA_CASE(ND)                                                                         \
+  case ND:                                                                                      \
+    return kv_dtype == CP_BF16                                                                  \
+               ? decode_gqa_t<__nv_bfloat16, ND>(plan, h, q, k, v, Hq, Hkv, sm_scale, o_part,   \
+                                                 lse_part, ws_o, ws_lse, s)                     \
+               : decode_gqa_t<float, ND>(plan, h, q, k, v, Hq, Hkv, sm_scale, o_part, lse_part, \
+                                         ws_o, ws_lse, s);
   switch (Dqk / 32) {
     CP_GQA_CASE(1)
     CP_GQA_CASE(2)

@@ -264,8 +264,9 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  * (O_r, LSE_r); merging the C partials with cp_lse_merge gives the
  * attention over the whole cache ([CTX] §3.3; [V4] §5).
  *
- * mode CP_DECODE_MLA: one latent KV head shared by all H query heads
- *   ([CTX] §1.3; [DCP] §5.3).  Dqk = 576, Dv = 512: keys are the whole
+ * mode CP_DECODE_MLA: one latent KV head shared by all H <= 64 query heads
+ *   ([CTX] §1.3; [DCP] §5.3), on the tensor cores.  Dqk = 576, Dv = 512,
+ *   Hkv = 1: keys are the whole
  *   576-dim entry, values its first 512 dims ([GLM] footnote 1).
  *   q [B, H, 576] bf16; shard_k[r] [rows_r, 576] as kv_dtype CP_BF16, or
  *   CP_FP8_E4M3 codes with shard_scale[r] [rows_r] fp32 (value = code *
