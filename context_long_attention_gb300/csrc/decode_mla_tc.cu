@@ -19,10 +19,10 @@
 // (exponent bias 127 instead of 7), and the 2^120 and the per-token scale are
 // applied to the scores and folded into P^T.
 //
-// Warp roles (288 threads): warps 0-3 softmax, thread = KV row of the tile
-// (TMEM lane) and, in the epilogue, dim row of O^T; warps 4-7 fill the tile
-// from global memory (row = thread, 16-byte loads) and prefetch the next
-// tiles into L2; warp 8 owns TMEM and issues the MMAs.
+// Warp roles (256 threads): warps 0-3 softmax, thread = KV row of the tile
+// (TMEM lane) and, in the epilogue, dim row of O^T; thread 0 also owns TMEM
+// and issues the MMAs; warps 4-7 fill the tile from global memory (row =
+// thread, 16-byte loads) and prefetch the next tiles into L2.
 // Softmax down the KV axis needs per-head maxima over the 128 rows of a tile.
 // The running maximum M_h used in the exponentials only moves when some score
 // exceeds it by more than 2^8 (checked per tile with one block-wide vote);
@@ -50,8 +50,7 @@ constexpr int kTileBytes = kChunks * kChunkBytes;  // 147,456 B
 constexpr int kQChunkBytes = kHeads * 128;  // one chunk of Q: 8 KB
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 73,728 B
 constexpr int kSmem = kTileBytes + kQBytes + 1024;
-constexpr int kThreads = 288;
-constexpr int kWarpMma = 8;
+constexpr int kThreads = 256;  // 8 warps: 2 per SM sub-partition, up to 255 registers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -114,14 +113,14 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4_scaled(uint32_t w) {
 }
 
 template <bool FP8>
-__global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sTile = smem;                  // [9 chunks][128 rows x 128 B]
   uint8_t* sQ = smem + kTileBytes;        // [9 chunks][64 heads x 128 B]
   uint8_t* sP = sTile + 8 * kChunkBytes;  // P^T over the last chunk: [128 rows][64 heads]
-  __shared__ __align__(8) uint64_t bar_fill, bar_s, bar_p, bar_pv, bar_drain;
+  __shared__ __align__(8) uint64_t bar_fill, bar_s, bar_pv, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;
@@ -135,14 +134,13 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bar_fill), 128);
     mbar_init(smem_u32(&bar_s), 1);
-    mbar_init(smem_u32(&bar_p), 128);
     mbar_init(smem_u32(&bar_pv), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_flag = 0;
     zero_flag = 0;
     mbar_init_fence();
   }
-  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 512);
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -255,45 +253,6 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&bar_fill));
       }
-    } else if (warp == kWarpMma) {
-      // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
-        const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
-        const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
-        for (int j = 0; j < ntiles; ++j) {
-          const int g = g0 + j;
-          if (!mbar_wait(smem_u32(&bar_fill), g & 1, p.wait_ns, &abort_flag)) {
-            report_timeout(p.status, 3, &abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll 4
-          for (int kk = 0; kk < kDqk / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem, smem_desc(tile + off, 16, 1024), smem_desc(qb + qoff, 16, 1024), idS,
-                   kk > 0);
-          }
-          mma_commit(smem_u32(&bar_s));
-          if (!mbar_wait(smem_u32(&bar_p), g & 1, p.wait_ns, &abort_flag)) {
-            report_timeout(p.status, 4, &abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int mb = 0; mb < kDv / 128; ++mb)
-#pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-              mma_ss(tmem + 64 + 64 * mb,
-                     smem_desc(tile + 2 * mb * kChunkBytes + kk * 2048, kChunkBytes, 1024),
-                     smem_desc(pb + kk * 2048, 16, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bar_pv));
-        }
-      }
-      __syncwarp();
     } else {
       // ------------------------------------------------------------ softmax (warps 0-3)
       const int t = threadIdx.x;  // tile row = TMEM lane
@@ -301,8 +260,26 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
       float l[kHeads];
 #pragma unroll
       for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
+      const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
+      const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
+      const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
       for (int j = 0; j < ntiles; ++j) {
         const int g = g0 + j;
+        bool issued = true;
+        if (t == 0) {  // S^T = K_tile Q^T once the tile is filled
+          issued = mbar_wait(smem_u32(&bar_fill), g & 1, p.wait_ns, &abort_flag);
+          if (issued) {
+            tc_fence_after();
+#pragma unroll 4
+            for (int kk = 0; kk < kDqk / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+              const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
+              mma_ss(tmem, smem_desc(tile + off, 16, 1024), smem_desc(qb + qoff, 16, 1024), idS,
+                     kk > 0);
+            }
+            mma_commit(smem_u32(&bar_s));
+          }
+        }
         const bool valid = j * kRows + t < nrows;
         // scores in log2 units; the FP8 tile holds 2^-120 x the codes
         float cj = p.scale_log2, vscale = 1.f;
@@ -312,8 +289,8 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
         }
         // The four softmax warps leave together: a warp that gave up still
         // meets the others at the named barrier of this vote.
-        const bool got =
-            __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s), g & 1, p.wait_ns, &abort_flag));
+        const bool got = __all_sync(
+            0xffffffffu, issued && mbar_wait(smem_u32(&bar_s), g & 1, p.wait_ns, &abort_flag));
         if (bar_red_or(1, 128, !got)) {
           if (!got) report_timeout(p.status, 6, &abort_flag);
           ok = false;
@@ -393,7 +370,18 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p));
+        named_bar_sync(1, 128);  // every row of P^T is written
+        if (t == 0) {            // O^T += V_tile^T P^T
+          tc_fence_after();
+#pragma unroll
+          for (int mb = 0; mb < kDv / 128; ++mb)
+#pragma unroll
+            for (int kk = 0; kk < kRows / 16; ++kk)
+              mma_ss(tmem + 64 + 64 * mb,
+                     smem_desc(tile + 2 * mb * kChunkBytes + kk * 2048, kChunkBytes, 1024),
+                     smem_desc(pb + kk * 2048, 16, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_pv));
+        }
       }
       // ---- epilogue: column sums of l, O^T / l, LSE
       const bool landed =
@@ -445,14 +433,14 @@ __global__ void __maxnreg__(224) decode_mla_tc_kernel(const Params p) {
     ok = ok && !abort_flag;
   }
   // Never free TMEM under a running MMA.
-  if (warp == kWarpMma && lane == 0) {
+  if (threadIdx.x == 0) {
     mma_commit(smem_u32(&bar_drain));
     mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace

@@ -72,6 +72,25 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Packed pairs of fp32 (one instruction for two lanes of work).
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 __device__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
   *abort = 1;
@@ -105,15 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const cp_seg_desc sg = reinterpret_cast<const cp_seg_desc*>(p.plan + p.off_seg)[td.seg];
   const int g = h / p.group;
 
-  // Rows and K/V tile counts of the two M tiles.
-  int rows[2], nkv[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    rows[t] = min(BM, max(0, sg.count - td.q_off - t * BM));
-    const int last_pos = sg.first_pos + (td.q_off + t * BM + rows[t] - 1) * sg.stride;
-    nkv[t] = rows[t] > 0 ? (last_pos + BN) / BN : 0;
-  }
-  const int nK = max(nkv[0], nkv[1]);
+  // Rows and K/V tile counts of the two M tiles (scalars: no local-memory arrays).
+  const int rows0 = min(BM, max(0, sg.count - td.q_off));
+  const int rows1 = min(BM, max(0, sg.count - td.q_off - BM));
+  const int nkv0 = rows0 > 0 ? (sg.first_pos + (td.q_off + rows0 - 1) * sg.stride + BN) / BN : 0;
+  const int nkv1 = rows1 > 0 ? (sg.first_pos + (td.q_off + BM + rows1 - 1) * sg.stride + BN) / BN : 0;
+  const int nK = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kSlots; ++s) {
@@ -148,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = (warp & 3) * 32 + lane;  // row within the M tile = TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t colS = t * 256, colO = t * 256 + 128;
-    const bool valid = i < rows[t];
+    const int rows_t = t ? rows1 : rows0;
+    const bool valid = i < rows_t;
     // Q row -> shared memory in the 128-byte-swizzled K-major layout.
     {
       const long long f = (long long)sg.first_f + (long long)(td.q_off + t * BM + i) * sg.stride;
@@ -164,9 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bar_q[t]));
     }
-    const int n_t = nkv[t];
+    const int n_t = t ? nkv1 : nkv0;
     if (n_t > 0) {
-      const int my_row = valid ? i : rows[t] - 1;
+      const int my_row = valid ? i : rows_t - 1;
       const int pos = sg.first_pos + (td.q_off + t * BM + my_row) * sg.stride;
       const float sl2 = p.scale_log2;
       const float thr = kRescaleLog2 / sl2;  // threshold in raw score units
@@ -181,69 +198,95 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int kbase = j * BN;
         const bool mask = kbase + BN - 1 > pos;
-        // pass 1: row max of this tile
+        // One pass over S with the current running max m_used: P (bf16 pairs)
+        // stays in registers until the whole tile is done, so S is intact in
+        // TMEM if a second pass is needed.  That happens on the first tile and
+        // when a row's max grows by more than 2^8 (tcgen05.ld/st are
+        // warp-collective: the warp redoes the pass together; rows whose max
+        // did not move recompute the same values).
+        uint32_t pk[BN / 2];
+        float lsum = 0.f;
         float mx = -INFINITY;
+        if (j == 0) {  // no running max yet: find this tile's max first
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_addr + colS + c * 32, r);
-          tmem_ld_wait();
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + colS + c * 16, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float s = __uint_as_float(r[e]);
-            if (mask && kbase + c * 32 + e > pos) s = -INFINITY;
-            mx = fmaxf(mx, s);
+            for (int e = 0; e < 8; ++e) {
+              float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+              if (mask) {
+                if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
+                if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
+              }
+              mx = fmax3(mx, s0, s1);
+            }
           }
+          m_used = mx;
         }
-        // tcgen05.ld/st are warp-collective: the warp rescales together, rows
-        // whose max did not move use a factor of 1.
-        const bool need = mx > m_used + thr;
-        if (__any_sync(0xffffffffu, need)) {
+        // pass 0 exponentiates with the running max; pass 1 only runs when a
+        // row's max grew by more than 2^8 (after the rescale below)
+#pragma unroll 1
+        for (int pass = 0; pass < 2; ++pass) {
+          const float neg = -m_used * sl2;
+          float s0sum = 0.f, s1sum = 0.f;
+          const bool track = pass == 0 && j > 0;
+#pragma unroll
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + colS + c * 16, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+              if (mask) {
+                if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
+                if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
+              }
+              if (track) mx = fmax3(mx, s0, s1);
+              float u0, u1;
+              fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
+              const float p0 = ex2(u0), p1 = ex2(u1);
+              add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
+              pk[8 * c + e] = pack_bf16x2(p0, p1);
+            }
+          }
+          lsum = s0sum + s1sum;
+          if (!track) break;
+          const bool need = mx > m_used + thr;
+          if (!__any_sync(0xffffffffu, need)) break;
           const float alpha = need ? ex2((m_used - mx) * sl2) : 1.f;
           if (need) {
             l *= alpha;
             m_used = mx;
           }
-          if (j > 0) {  // rescale O_t once its previous P V product has landed
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
-                                                   &abort_flag))) {
-              report_timeout(p.status, 2, &abort_flag);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+          // rescale O_t once its previous P V product has landed
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
+                                                 &abort_flag))) {
+            report_timeout(p.status, 2, &abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + colO + c * 16, r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_addr + colO + c * 32, r);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(lane_addr + colO + c * 32, r);
-            }
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st16(lane_addr + colO + c * 16, r);
           }
         }
-        // pass 2: P = 2^(s*c - m*c) in bf16 over the first 64 columns of S
-        const float neg = -m_used * sl2;
-        float lsum = 0.f;
+        if (!ok) break;
+        // P over the first 64 columns of S
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(lane_addr + colS + c * 32, r);
-          tmem_ld_wait();
-          uint32_t pk[16];
+          uint32_t q16[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
-            float p0 = ex2(fmaf(s0, sl2, neg)), p1 = ex2(fmaf(s1, sl2, neg));
-            if (mask) {
-              if (kbase + c * 32 + 2 * e > pos) p0 = 0.f;
-              if (kbase + c * 32 + 2 * e + 1 > pos) p1 = 0.f;
-            }
-            lsum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(lane_addr + colS + c * 16, pk);
+          for (int e = 0; e < 16; ++e) q16[e] = pk[16 * c + e];
+          tmem_st16(lane_addr + colS + c * 16, q16);
         }
         l += lsum;
         tmem_st_wait();
@@ -343,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
       }
       for (int t = 0; t < 2 && ok; ++t)
-        if (nkv[t] > 0 && !mbar_wait(smem_u32(&bar_q[t]), 0, p.wait_ns, &abort_flag)) {
+        if ((t ? nkv1 : nkv0) > 0 && !mbar_wait(smem_u32(&bar_q[t]), 0, p.wait_ns, &abort_flag)) {
           fail(11);
           ok = false;
         }
@@ -353,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         } else {
           tc_fence_after();
-          for (int t = 0; t < 2; ++t)
-            if (nkv[t] > 0) issue_s(t, 0);
+          if (nkv0 > 0) issue_s(0, 0);
+          if (nkv1 > 0) issue_s(1, 0);
           mma_commit(smem_u32(&bar_empty[0]));
         }
       }
@@ -366,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         for (int t = 0; t < 2 && ok; ++t) {
-          if (j >= nkv[t]) continue;
+          const int nt = t ? nkv1 : nkv0;
+          if (j >= nt) continue;
           if (!mbar_wait(smem_u32(&bar_p[t]), j & 1, p.wait_ns, &abort_flag)) {
             fail(14 + t);
             ok = false;
@@ -374,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           issue_pv(t, uV, j > 0);
-          if (j + 1 < nkv[t]) {
+          if (j + 1 < nt) {
             if (!wait_full(uK)) {
               fail(16);
               ok = false;
