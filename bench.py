@@ -236,7 +236,7 @@ def run_ours(args, world, rank, local):
 
     # ---- decode inputs (MLA, FP8 cache, packed into token shards once)
     m = W.WORKLOADS["mla"]
-    ctx = [m["ctx"]] * m["B"]
+    ctx = [m["ctx"]] * (args.decode_batch or m["B"])
     fp8 = args.decode_kv == "fp8"
     d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
     dscale = 1.0 / math.sqrt(m["Dqk"])
@@ -253,10 +253,11 @@ def run_ours(args, world, rank, local):
             scales = None
             del data["kv_bf16"]
         dq = data["q"]
-        o_part = torch.empty((m["C"], m["B"], m["H"], m["Dv"]), dtype=torch.float32, device=dev)
-        lse_part = torch.empty((m["C"], m["B"], m["H"]), dtype=torch.float32, device=dev)
-        o_dec = torch.empty((m["B"], m["H"], m["Dv"]), dtype=torch.bfloat16, device=dev)
-        lse_dec = torch.empty((m["B"], m["H"]), dtype=torch.float32, device=dev)
+        B = len(ctx)
+        o_part = torch.empty((m["C"], B, m["H"], m["Dv"]), dtype=torch.float32, device=dev)
+        lse_part = torch.empty((m["C"], B, m["H"]), dtype=torch.float32, device=dev)
+        o_dec = torch.empty((B, m["H"], m["Dv"]), dtype=torch.bfloat16, device=dev)
+        lse_dec = torch.empty((B, m["H"]), dtype=torch.float32, device=dev)
         ws_bytes = cp.cp_decode_workspace_size(dplan, m["H"], m["Dv"])
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         n_dec_kernels = 2 + (1 if dplan.n_split > 0 else 0)  # decode (+ split merge) + LSE merge
@@ -417,6 +418,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--decode-kv", choices=["fp8", "bf16"], default="fp8",
                     help="decode cache type (the MLA workload has both)")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

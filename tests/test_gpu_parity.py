@@ -336,3 +336,56 @@ def test_misaligned_pointer_rejected(cp):
                                 ctypes.c_void_p(t["v"].data_ptr()), 8, 2, 64, 0.125, ctypes.c_void_p(o.data_ptr()),
                                 ctypes.c_void_p(lse.data_ptr()), None)
     assert st == cp.CpError(-1, "").status and b"aligned" in cp.lib.cp_last_error()
+
+
+def test_prefill_interleave_full_size_sampled(cp):
+    """The ragged interleave workload at full size (16 requests, 2^20 tokens,
+    64 q / 8 kv heads); the oracle checks sampled rows of three requests
+    (shortest, middle, longest): every rank's first and last query of the
+    request plus one at random."""
+    w = W.WORKLOADS["interleave"]
+    lens = W.interleave_lengths()
+    pre = [0] * len(lens)
+    C, Hq, Hkv, D = w["C"], w["Hq"], w["Hkv"], w["D"]
+    q, k, v = W.prefill_inputs(lens, pre, Hq, Hkv, D, "bf16", seed=W.SEEDS["interleave"], device=DEV)
+    plan = cp.cp_shard_plan(cp.CP_INTERLEAVE, C, lens, pre, device=DEV)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = cp.cp_prefill_attn(plan, q, k, v, scale)
+    cp.cp_device_error_check()
+    ref_plan = oracle.interleave_plan_np(lens, pre, C)
+    order = np.argsort(lens)
+    picks = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    base = np.concatenate([[0], np.cumsum(lens)])
+    rng = np.random.default_rng(3)
+    ro = plan.rank_off
+    for j in picks:
+        L = lens[j]
+        kj = np64(k[base[j]:base[j] + L])
+        vj = np64(v[base[j]:base[j] + L])
+        for r in range(C):
+            local = np.nonzero(np.asarray(ref_plan["req"][r]) == j)[0]
+            if len(local) == 0:
+                continue
+            sel = np.unique([local[0], local[-1], local[rng.integers(0, len(local))]])
+            f = np.asarray(ref_plan["order"][r])[sel]
+            pos = np.asarray(ref_plan["pos"][r])[sel]
+            o_ref, l_ref = oracle.causal_rows(np64(q[torch.as_tensor(f, device=DEV)]), kj, vj, pos, scale)
+            rows_g = torch.as_tensor(ro[r] + sel, device=DEV)
+            check_o(o[rows_g], o_ref, what=f"req {j} rank {r}", **TOL_BF16)
+            check_lse(lse[rows_g], l_ref)
+        del kj, vj
+
+
+def test_decode_mla_mixed_full_size_sampled(cp):
+    """The mixed-length FP8 MLA workload at full size (128 requests, 1k..1M
+    contexts, 8 shards); the oracle checks the shortest, the median and a
+    ~200k-token request in full (all shards' partials and the merge)."""
+    w = W.WORKLOADS["mla_mixed"]
+    ctx = W.mixed_context_lengths()
+    data = W.mla_decode_inputs(ctx, H=w["H"], seed=W.SEEDS["mla_mixed"], device=DEV, bf16=False)
+    srt = np.argsort(ctx)
+    near200k = int(np.argmin(np.abs(np.asarray(ctx) - 200000)))
+    mla_decode_case(cp, data, w["C"], True, 0,
+                    check_reqs=[int(srt[0]), int(srt[len(srt) // 2]), near200k])
+    del data
+    torch.cuda.empty_cache()
