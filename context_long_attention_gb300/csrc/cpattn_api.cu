@@ -602,9 +602,11 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   memset(&V, 0, sizeof(V));
   memset(&S, 0, sizeof(S));
   const int32_t* W = (const int32_t*)host_plan;
+  long long shard_rows[CP_MAX_SHARDS] = {0};
   for (int r = 0; r < h.C; ++r) {
     long long rows_r = 0;
     for (int b = 0; b < h.R; ++b) rows_r += W[h.off_rank + kPairWords * (r * h.R + b)];
+    shard_rows[r] = rows_r;
     K.p[r] = shard_k[r];
     if (rows_r > 0 && (!shard_k[r] || !aligned16(shard_k[r]))) return fail(CP_ERR_INVALID_ARG, "shard_k[%d] NULL or misaligned", r);
     if (shard_v) {
@@ -620,8 +622,9 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hq * Dv : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e =
-      mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, kv_dtype == CP_FP8_E4M3, q, K, S, Hq,
-                                 sm_scale, o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+      mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, kv_dtype == CP_FP8_E4M3, q, K, S,
+                                 shard_rows, Hq, sm_scale, o_part, lse_part, ws_o, ws_lse,
+                                 wait_limit_ns(), s)
           : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, Hq, Hkv, Dqk,
                                Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");

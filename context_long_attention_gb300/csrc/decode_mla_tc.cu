@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdlib>
+#include <cstring>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -70,6 +71,11 @@ struct Params {
   float* ws_lse;
   unsigned* status;
   unsigned long long wait_ns;
+};
+
+// Tensor maps of the shards' bf16 caches ([rows, 576], box 64 x 128, 128-byte swizzle).
+struct ShardMaps {
+  CUtensorMap m[CP_MAX_SHARDS];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -112,15 +118,24 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4_scaled(uint32_t w) {
   return r;
 }
 
+// Chunk groups of a tile: q = 0..3 hold dims [128q, 128q + 128) (chunks 2q,
+// 2q+1, also the M-block q of V^T); q = 4 holds the rope dims [512, 576),
+// overwritten by P^T once S^T is computed.
+__device__ __forceinline__ int group_chunks(int q) { return q < 4 ? 2 : 1; }
+
 template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_mla_tc_kernel(const __grid_constant__ ShardMaps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sTile = smem;                  // [9 chunks][128 rows x 128 B]
   uint8_t* sQ = smem + kTileBytes;        // [9 chunks][64 heads x 128 B]
   uint8_t* sP = sTile + 8 * kChunkBytes;  // P^T over the last chunk: [128 rows][64 heads]
-  __shared__ __align__(8) uint64_t bar_fill, bar_s, bar_pv, bar_drain;
+  // fill[q]: chunk group q of the tile holds the current tile.
+  // mb[q]: the P.V product of M-block q (dims of group q) has completed; mb[3]
+  //        also means the whole P.V (and every read of P^T) has completed.
+  __shared__ __align__(8) uint64_t bar_fill[5], bar_mb[4], bar_s, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;
@@ -132,9 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar_fill), 128);
+    for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_fill[q]), FP8 ? 128 : 1);
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bar_mb[q]), 1);
     mbar_init(smem_u32(&bar_s), 1);
-    mbar_init(smem_u32(&bar_pv), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_flag = 0;
     zero_flag = 0;
@@ -188,97 +203,107 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params
     fence_proxy_async_smem();
     __syncthreads();
 
-    if (warp >= 4 && warp < 8) {
+    if (warp >= 4) {
       // ------------------------------------------------------------ tile fill
       const int t = threadIdx.x - 128;  // tile row
-      for (int j = 0; j < ntiles; ++j) {
-        const int g = g0 + j;
-        if (t == 0) {  // keep the next two tiles on their way into L2
-          for (int a = 1; a <= 2; ++a) {
-            const int jj = j + a;
-            if (jj < ntiles) {
-              const int rows = min(kRows, nrows - jj * kRows);
-              prefetch_l2(kbase + (long long)jj * kRows * kRowBytes, (uint32_t)rows * kRowBytes);
-            }
-          }
+      if (t == 0) {  // the first tiles on their way into L2
+        for (int jj = 0; jj < min(ntiles, 3); ++jj)
+          prefetch_l2(kbase + (long long)jj * kRows * kRowBytes,
+                      (uint32_t)min(kRows, nrows - jj * kRows) * kRowBytes);
+      }
+      uint4 R[FP8 ? kDqk / 16 : 1];  // FP8: the thread's whole row of the next tile
+      auto load_row = [&](int j) {
+        if (FP8) {
+          const int row = j * kRows + t;
+          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk);
+          const bool valid = row < nrows;
+#pragma unroll
+          for (int e = 0; e < kDqk / 16; ++e) R[e] = valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
         }
-        if (j > 0) {  // the tile is free once the previous P.V has read it
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g - 1) & 1, p.wait_ns, &abort_flag))) {
+      };
+      load_row(0);
+      int issued_tiles = 0;  // bf16: tiles whose copies were issued (for the drain)
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int g = g0 + j;
+        if (t == 0 && j + 3 < ntiles)
+          prefetch_l2(kbase + (long long)(j + 3) * kRows * kRowBytes,
+                      (uint32_t)min(kRows, nrows - (j + 3) * kRows) * kRowBytes);
+#pragma unroll
+        for (int q = 0; q < 5; ++q) {
+          // group q is free once the previous tile's P.V M-block q (or, for the
+          // rope group that holds P^T, the whole P.V) has read it
+          if (ok && j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]),
+                                                                (g - 1) & 1, p.wait_ns, &abort_flag))) {
             report_timeout(p.status, 1, &abort_flag);
             ok = false;
-            break;
           }
-        }
-        const int row = j * kRows + t;
-        const bool valid = row < nrows;
-        uint8_t* dst = sTile + t * 128;
-        if (FP8) {
-          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk);
+          if (!ok) continue;
+          if (FP8) {
 #pragma unroll
-          for (int grp = 0; grp < 3; ++grp) {  // 3 x 12 loads of 16 codes
-            uint4 v[12];
+            for (int cc = 0; cc < 2; ++cc) {
+              if (cc < group_chunks(q)) {
+                const int c = 2 * q + cc;
+                uint8_t* base = sTile + c * kChunkBytes + t * 128;
 #pragma unroll
-            for (int e = 0; e < 12; ++e)
-              v[e] = valid ? __ldg(src + grp * 12 + e) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int e = 0; e < 12; ++e) {
-              const int piece16 = grp * 12 + e;  // 16 codes = 32 B of bf16
-              const int c = piece16 >> 2;        // 64-dim chunk
-              const int cc0 = (piece16 & 3) * 2; // first of two 16-byte pieces in the row
-              const uint2 a0 = e4m3x4_to_bf16x4_scaled(v[e].x), a1 = e4m3x4_to_bf16x4_scaled(v[e].y);
-              const uint2 a2 = e4m3x4_to_bf16x4_scaled(v[e].z), a3 = e4m3x4_to_bf16x4_scaled(v[e].w);
-              uint8_t* base = dst + c * kChunkBytes;
-              *reinterpret_cast<uint4*>(base + ((cc0 ^ (t & 7)) << 4)) =
-                  make_uint4(a0.x, a0.y, a1.x, a1.y);
-              *reinterpret_cast<uint4*>(base + (((cc0 + 1) ^ (t & 7)) << 4)) =
-                  make_uint4(a2.x, a2.y, a3.x, a3.y);
+                for (int e = 0; e < 4; ++e) {  // 4 x 16 codes = 64 dims
+                  const uint4 v = R[4 * c + e];
+                  const uint2 a0 = e4m3x4_to_bf16x4_scaled(v.x), a1 = e4m3x4_to_bf16x4_scaled(v.y);
+                  const uint2 a2 = e4m3x4_to_bf16x4_scaled(v.z), a3 = e4m3x4_to_bf16x4_scaled(v.w);
+                  *reinterpret_cast<uint4*>(base + (((2 * e) ^ (t & 7)) << 4)) =
+                      make_uint4(a0.x, a0.y, a1.x, a1.y);
+                  *reinterpret_cast<uint4*>(base + (((2 * e + 1) ^ (t & 7)) << 4)) =
+                      make_uint4(a2.x, a2.y, a3.x, a3.y);
+                }
+              }
             }
-          }
-        } else {
-          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * 2 * kDqk);
-#pragma unroll
-          for (int grp = 0; grp < 6; ++grp) {  // 6 x 12 loads of 8 bf16
-            uint4 v[12];
-#pragma unroll
-            for (int e = 0; e < 12; ++e)
-              v[e] = valid ? __ldg(src + grp * 12 + e) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int e = 0; e < 12; ++e) {
-              const int piece = grp * 12 + e;
-              const int c = piece >> 3, cc = piece & 7;
-              *reinterpret_cast<uint4*>(dst + c * kChunkBytes + ((cc ^ (t & 7)) << 4)) = v[e];
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&bar_fill[q]));
+          } else if (t == 0) {
+            const uint32_t full = smem_u32(&bar_fill[q]);
+            mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
+            for (int cc = 0; cc < group_chunks(q); ++cc) {
+              const int c = 2 * q + cc;
+              tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
+                          (int)(row0 + (long long)j * kRows), full);
             }
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bar_fill));
+        if (!ok) break;
+        issued_tiles = j + 1;
+        if (j + 1 < ntiles) load_row(j + 1);  // in flight while this tile computes
+      }
+      if (!FP8 && t == 0 && !ok && issued_tiles > 0) {
+        // never leave with a copy in flight: the last issued tile's groups
+        for (int q = 0; q < 5; ++q)
+          mbar_wait(smem_u32(&bar_fill[q]), (g0 + issued_tiles - 1) & 1, 1000000000ull, &zero_flag);
       }
     } else {
       // ------------------------------------------------------------ softmax (warps 0-3)
       const int t = threadIdx.x;  // tile row = TMEM lane
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      float l[kHeads];
-#pragma unroll
-      for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
       const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
       const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
       const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
+      float l[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
       for (int j = 0; j < ntiles; ++j) {
         const int g = g0 + j;
         bool issued = true;
-        if (t == 0) {  // S^T = K_tile Q^T once the tile is filled
-          issued = mbar_wait(smem_u32(&bar_fill), g & 1, p.wait_ns, &abort_flag);
-          if (issued) {
+        if (t == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
+          for (int q = 0; q < 5 && issued; ++q) {
+            issued = mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns, &abort_flag);
+            if (!issued) break;
             tc_fence_after();
-#pragma unroll 4
-            for (int kk = 0; kk < kDqk / 16; ++kk) {
+            for (int ks = 0; ks < 4 * group_chunks(q); ++ks) {
+              const int kk = 8 * q + ks;
               const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
               const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
               mma_ss(tmem, smem_desc(tile + off, 16, 1024), smem_desc(qb + qoff, 16, 1024), idS,
                      kk > 0);
             }
-            mma_commit(smem_u32(&bar_s));
           }
+          if (issued) mma_commit(smem_u32(&bar_s));
         }
         const bool valid = j * kRows + t < nrows;
         // scores in log2 units; the FP8 tile holds 2^-120 x the codes
@@ -371,21 +396,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(1, 128);  // every row of P^T is written
-        if (t == 0) {            // O^T += V_tile^T P^T
+        if (t == 0) {            // O^T += V_tile^T P^T, one M-block (128 dims) at a time
           tc_fence_after();
 #pragma unroll
-          for (int mb = 0; mb < kDv / 128; ++mb)
+          for (int mb = 0; mb < kDv / 128; ++mb) {
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk)
               mma_ss(tmem + 64 + 64 * mb,
                      smem_desc(tile + 2 * mb * kChunkBytes + kk * 2048, kChunkBytes, 1024),
                      smem_desc(pb + kk * 2048, 16, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bar_pv));
+            mma_commit(smem_u32(&bar_mb[mb]));
+          }
         }
       }
       // ---- epilogue: column sums of l, O^T / l, LSE
       const bool landed =
-          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g0 + ntiles - 1) & 1,
+          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[3]), (g0 + ntiles - 1) & 1,
                                                   p.wait_ns, &abort_flag));
       if (bar_red_or(1, 128, !landed)) {
         if (ok && !landed) report_timeout(p.status, 7, &abort_flag);
@@ -446,9 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mla_tc_kernel(const Params
 }  // namespace
 
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
-                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc, int H,
-                                 float sm_scale, float* o_part, float* lse_part, float* ws_o,
-                                 float* ws_lse, unsigned long long wait_ns, cudaStream_t s) {
+                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc,
+                                 const long long* shard_rows, int H, float sm_scale,
+                                 float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                                 unsigned long long wait_ns, cudaStream_t s) {
   Params p;
   p.plan = dev_plan;
   p.B = h.R;
@@ -467,10 +494,22 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.status = device_status_ptr();
   if (!p.status) return cudaErrorInvalidDevice;
   p.wait_ns = wait_ns;
+  ShardMaps local;
+  memset(&local, 0, sizeof(local));
+  if (!fp8) {
+    for (int r = 0; r < h.C; ++r) {
+      if (shard_rows[r] == 0) continue;
+      const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)shard_rows[r]};
+      const uint64_t strides[1] = {(uint64_t)kDqk * 2};
+      const uint32_t box[2] = {64, (uint32_t)kRows};
+      if (!encode_tensor_map_bf16(&local.m[r], k.p[r], 2, dims, strides, box))
+        return cudaErrorInvalidValue;
+    }
+  }
   auto kern = fp8 ? decode_mla_tc_kernel<true> : decode_mla_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<h.n_tiles, kThreads, kSmem, s>>>(p);
+  kern<<<h.n_tiles, kThreads, kSmem, s>>>(local, p);
   return cudaGetLastError();
 }
 

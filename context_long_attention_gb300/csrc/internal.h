@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,11 +60,17 @@ cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
                               const void* v, int Hq, int Hkv, int D, float sm_scale, void* o,
                               float* lse, bool stall_test, cudaStream_t s);
 
+// bf16 tensor map with a 128-byte swizzle (rank 2 or 3; strides in bytes for
+// dims 1..rank-1).  False if the driver entry point is missing or rejects it.
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box);
+
 // ---- tensor-core MLA decode (decode_mla_tc.cu)
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
-                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc, int H,
-                                 float sm_scale, float* o_part, float* lse_part, float* ws_o,
-                                 float* ws_lse, unsigned long long wait_ns, cudaStream_t s);
+                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc,
+                                 const long long* shard_rows, int H, float sm_scale,
+                                 float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                                 unsigned long long wait_ns, cudaStream_t s);
 unsigned long long wait_limit_ns();
 
 // ---- CUDA-core attention (simt_attn.cu)

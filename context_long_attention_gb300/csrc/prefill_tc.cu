@@ -464,15 +464,10 @@ EncodeTiledFn encode_fn() {
 
 // [rows, H, D] bf16 viewed as 3-D (D, H, rows); box (64, 1, 128), 128-byte swizzle.
 bool make_kv_map(CUtensorMap* m, const void* base, int rows, int H, int D) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)BN};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint64_t dims[3] = {(uint64_t)D, (uint64_t)H, (uint64_t)rows};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)H * D * 2};
+  const uint32_t box[3] = {64, 1, (uint32_t)BN};
+  return encode_tensor_map_bf16(m, base, 3, dims, strides, box);
 }
 
 template <int D>
@@ -488,6 +483,22 @@ cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params&
 }
 
 }  // namespace
+
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Limit of every bounded device wait: CPATTN_WAIT_LIMIT_MS (default 4000 ms),
 // read once per process.
