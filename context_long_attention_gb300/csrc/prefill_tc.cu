@@ -207,21 +207,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[BN / 2];
         float lsum = 0.f;
         float mx = -INFINITY;
+        // S is read 16 columns at a time with the next load in flight while a
+        // chunk is processed (tcgen05.wait::ld waits for every load issued).
         if (j == 0) {  // no running max yet: find this tile's max first
+          uint32_t ra[16], rb[16];
+          tmem_ld16(lane_addr + colS, ra);
+          tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < BN / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(lane_addr + colS + c * 16, r);
-            tmem_ld_wait();
+            uint32_t(&cur)[16] = (c & 1) ? rb : ra;
+            uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
+            if (c + 1 < BN / 16) tmem_ld16(lane_addr + colS + (c + 1) * 16, nxt);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
               if (mask) {
                 if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
                 if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
               }
               mx = fmax3(mx, s0, s1);
             }
+            if (c + 1 < BN / 16) tmem_ld_wait();
           }
           m_used = mx;
         }
@@ -232,14 +238,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float neg = -m_used * sl2;
           float s0sum = 0.f, s1sum = 0.f;
           const bool track = pass == 0 && j > 0;
+          uint32_t ra[16], rb[16];
+          tmem_ld16(lane_addr + colS, ra);
+          tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < BN / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(lane_addr + colS + c * 16, r);
-            tmem_ld_wait();
+            uint32_t(&cur)[16] = (c & 1) ? rb : ra;
+            uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
+            if (c + 1 < BN / 16) tmem_ld16(lane_addr + colS + (c + 1) * 16, nxt);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              float s0 = __uint_as_float(r[2 * e]), s1 = __uint_as_float(r[2 * e + 1]);
+              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
               if (mask) {
                 if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
                 if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
@@ -251,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
               pk[8 * c + e] = pack_bf16x2(p0, p1);
             }
+            if (c + 1 < BN / 16) tmem_ld_wait();
           }
           lsum = s0sum + s1sum;
           if (!track) break;
