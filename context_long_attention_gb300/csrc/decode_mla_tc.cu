@@ -56,6 +56,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kTwo120 = 1.329227995784916e36f;  // 2^120
+#ifndef CP_DECODE_PREFETCH_TILES
+#define CP_DECODE_PREFETCH_TILES 8
+#endif
+#ifndef CP_DECODE_PREFETCH_PIECE
+#define CP_DECODE_PREFETCH_PIECE 4096
+#endif
+constexpr int kPrefetchTiles = CP_DECODE_PREFETCH_TILES;  // tiles kept on their way into L2
+constexpr int kPrefetchPiece = CP_DECODE_PREFETCH_PIECE;  // bytes per bulk prefetch
 
 struct Params {
   const int32_t* plan;
@@ -206,11 +214,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 4) {
       // ------------------------------------------------------------ tile fill
       const int t = threadIdx.x - 128;  // tile row
-      if (t == 0) {  // the first tiles on their way into L2
-        for (int jj = 0; jj < min(ntiles, 3); ++jj)
-          prefetch_l2(kbase + (long long)jj * kRows * kRowBytes,
-                      (uint32_t)min(kRows, nrows - jj * kRows) * kRowBytes);
-      }
+      // L2 prefetch of the tiles ahead: warp 4 spreads pieces of a tile over its lanes
+      auto prefetch_tile = [&](int jj) {
+        const uint8_t* base = kbase + (long long)jj * kRows * kRowBytes;
+        const uint32_t bytes = (uint32_t)min(kRows, nrows - jj * kRows) * kRowBytes;
+        for (uint32_t o = (uint32_t)t * kPrefetchPiece; o < bytes; o += 32u * kPrefetchPiece)
+          prefetch_l2(base + o, min((uint32_t)kPrefetchPiece, bytes - o));
+      };
+      if (t < 32)
+        for (int jj = 0; jj < min(ntiles, kPrefetchTiles); ++jj) prefetch_tile(jj);
       uint4 R[FP8 ? kDqk / 16 : 1];  // FP8: the thread's whole row of the next tile
       auto load_row = [&](int j) {
         if (FP8) {
@@ -225,9 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued_tiles = 0;  // bf16: tiles whose copies were issued (for the drain)
       for (int j = 0; j < ntiles && ok; ++j) {
         const int g = g0 + j;
-        if (t == 0 && j + 3 < ntiles)
-          prefetch_l2(kbase + (long long)(j + 3) * kRows * kRowBytes,
-                      (uint32_t)min(kRows, nrows - (j + 3) * kRows) * kRowBytes);
+        if (t < 32 && j + kPrefetchTiles < ntiles) prefetch_tile(j + kPrefetchTiles);
 #pragma unroll
         for (int q = 0; q < 5; ++q) {
           // group q is free once the previous tile's P.V M-block q (or, for the
