@@ -21,8 +21,9 @@
 //
 // Warp roles (256 threads): warps 0-3 softmax, thread = KV row of the tile
 // (TMEM lane) and, in the epilogue, dim row of O^T; thread 0 also owns TMEM
-// and issues the MMAs; warps 4-7 fill the tile from global memory (row =
-// thread, 16-byte loads) and prefetch the next tiles into L2.
+// and issues the MMAs; warps 4-7 fill the tile chunk group by chunk group as
+// the previous tile's P.V releases it (FP8: from the next tile's codes, held in
+// the fill warps' registers; bf16: by TMA).
 // Softmax down the KV axis needs per-head maxima over the 128 rows of a tile.
 // The running maximum M_h used in the exponentials only moves when some score
 // exceeds it by more than 2^8 (checked per tile with one block-wide vote);
@@ -56,14 +57,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kTwo120 = 1.329227995784916e36f;  // 2^120
-#ifndef CP_DECODE_PREFETCH_TILES
-#define CP_DECODE_PREFETCH_TILES 8
-#endif
-#ifndef CP_DECODE_PREFETCH_PIECE
-#define CP_DECODE_PREFETCH_PIECE 4096
-#endif
-constexpr int kPrefetchTiles = CP_DECODE_PREFETCH_TILES;  // tiles kept on their way into L2
-constexpr int kPrefetchPiece = CP_DECODE_PREFETCH_PIECE;  // bytes per bulk prefetch
 
 struct Params {
   const int32_t* plan;
@@ -111,9 +104,6 @@ __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, 
     status[3] = blockIdx.x;
     __threadfence();
   }
-}
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Four E4M3 codes -> four bf16 whose values are 2^-120 x the codes' values.
@@ -213,31 +203,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= 4) {
       // ------------------------------------------------------------ tile fill
-      const int t = threadIdx.x - 128;  // tile row
-      // L2 prefetch of the tiles ahead: warp 4 spreads pieces of a tile over its lanes
-      auto prefetch_tile = [&](int jj) {
-        const uint8_t* base = kbase + (long long)jj * kRows * kRowBytes;
-        const uint32_t bytes = (uint32_t)min(kRows, nrows - jj * kRows) * kRowBytes;
-        for (uint32_t o = (uint32_t)t * kPrefetchPiece; o < bytes; o += 32u * kPrefetchPiece)
-          prefetch_l2(base + o, min((uint32_t)kPrefetchPiece, bytes - o));
-      };
-      if (t < 32)
-        for (int jj = 0; jj < min(ntiles, kPrefetchTiles); ++jj) prefetch_tile(jj);
-      uint4 R[FP8 ? kDqk / 16 : 1];  // FP8: the thread's whole row of the next tile
+      const int t = threadIdx.x - 128;  // tile row (bf16 copies are issued by t == 0)
+      // FP8: the next tile is loaded into registers while this one computes.
+      // A warp covers 32 rows; one load instruction reads 8 rows x 64 bytes
+      // (one chunk of each): lane l takes row 8 sb + l / 4 of the warp's rows,
+      // 16 codes at piece l % 4 of chunk c, kept in R[4 c + sb].
+      const int lw = warp - 4, sr = lane >> 2, pc = lane & 3;
+      uint4 R[FP8 ? kDqk / 16 : 1];
       auto load_row = [&](int j) {
         if (FP8) {
-          const int row = j * kRows + t;
-          const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk);
-          const bool valid = row < nrows;
 #pragma unroll
-          for (int e = 0; e < kDqk / 16; ++e) R[e] = valid ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+          for (int sb = 0; sb < 4; ++sb) {
+            const int row = j * kRows + 32 * lw + 8 * sb + sr;
+            const bool valid = row < nrows;
+            const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk) + pc;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+              R[4 * c + sb] = valid ? __ldg(src + 4 * c) : make_uint4(0, 0, 0, 0);
+          }
         }
       };
       load_row(0);
       int issued_tiles = 0;  // bf16: tiles whose copies were issued (for the drain)
       for (int j = 0; j < ntiles && ok; ++j) {
         const int g = g0 + j;
-        if (t < 32 && j + kPrefetchTiles < ntiles) prefetch_tile(j + kPrefetchTiles);
 #pragma unroll
         for (int q = 0; q < 5; ++q) {
           // group q is free once the previous tile's P.V M-block q (or, for the
@@ -253,15 +242,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int cc = 0; cc < 2; ++cc) {
               if (cc < group_chunks(q)) {
                 const int c = 2 * q + cc;
-                uint8_t* base = sTile + c * kChunkBytes + t * 128;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {  // 4 x 16 codes = 64 dims
-                  const uint4 v = R[4 * c + e];
+                for (int sb = 0; sb < 4; ++sb) {
+                  const int tr = 32 * lw + 8 * sb + sr;  // tile row; tr & 7 == sr
+                  uint8_t* base = sTile + c * kChunkBytes + tr * 128;
+                  const uint4 v = R[4 * c + sb];
                   const uint2 a0 = e4m3x4_to_bf16x4_scaled(v.x), a1 = e4m3x4_to_bf16x4_scaled(v.y);
                   const uint2 a2 = e4m3x4_to_bf16x4_scaled(v.z), a3 = e4m3x4_to_bf16x4_scaled(v.w);
-                  *reinterpret_cast<uint4*>(base + (((2 * e) ^ (t & 7)) << 4)) =
+                  *reinterpret_cast<uint4*>(base + (((2 * pc) ^ sr) << 4)) =
                       make_uint4(a0.x, a0.y, a1.x, a1.y);
-                  *reinterpret_cast<uint4*>(base + (((2 * e + 1) ^ (t & 7)) << 4)) =
+                  *reinterpret_cast<uint4*>(base + (((2 * pc + 1) ^ sr) << 4)) =
                       make_uint4(a2.x, a2.y, a3.x, a3.y);
                 }
               }
