@@ -52,6 +52,7 @@ constexpr int kTileBytes = kChunks * kChunkBytes;  // 147,456 B
 constexpr int kQChunkBytes = kHeads * 128;  // one chunk of Q: 8 KB
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 73,728 B
 constexpr int kSmem = kTileBytes + kQBytes + 1024;
+constexpr int kStageCol = 320;  // TMEM columns [320, 464): parked FP8 codes of the next tile
 constexpr int kThreads = 256;  // 8 warps: 2 per SM sub-partition, up to 255 registers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -157,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;  // S^T: cols [0,64); O^T block mb: [64 + 64 mb, 128 + 64 mb)
+  // TMEM: S^T cols [0,64); O^T block mb: [64 + 64 mb, 128 + 64 mb); FP8 staging [320, 464)
+  const uint32_t tmem = tmem_slot;
 
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work);
@@ -223,7 +225,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       };
+      // FP8: the codes of the tile after next are in flight in R while those of
+      // the next tile wait in TMEM columns [kStageCol, kStageCol + 144) of the
+      // thread's own lane, so two tiles are always on their way from memory.
+      const uint32_t stage_addr = tmem + ((uint32_t)(32 * lw) << 16) + kStageCol;
+      auto park = [&]() {
+        if (FP8) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            uint32_t w[32];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              w[4 * e] = R[8 * m + e].x;
+              w[4 * e + 1] = R[8 * m + e].y;
+              w[4 * e + 2] = R[8 * m + e].z;
+              w[4 * e + 3] = R[8 * m + e].w;
+            }
+            tmem_st32(stage_addr + 32 * m, w);
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            w[4 * e] = R[32 + e].x;
+            w[4 * e + 1] = R[32 + e].y;
+            w[4 * e + 2] = R[32 + e].z;
+            w[4 * e + 3] = R[32 + e].w;
+          }
+          tmem_st16(stage_addr + 128, w);
+          tmem_st_wait();
+        }
+      };
       load_row(0);
+      if (FP8) {
+        park();
+        if (ntiles > 1) load_row(1);
+      }
       int issued_tiles = 0;  // bf16: tiles whose copies were issued (for the drain)
       for (int j = 0; j < ntiles && ok; ++j) {
         const int g = g0 + j;
@@ -238,6 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) continue;
           if (FP8) {
+            uint32_t G[32];  // this group's parked codes: piece 4 cc + sb at G[4 (4 cc + sb)]
+            if (q < 4) {
+              tmem_ld32(stage_addr + 32 * q, G);
+            } else {
+              uint32_t G16[16];
+              tmem_ld16(stage_addr + 128, G16);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) G[e] = G16[e];
+            }
+            tmem_ld_wait();
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               if (cc < group_chunks(q)) {
@@ -246,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int sb = 0; sb < 4; ++sb) {
                   const int tr = 32 * lw + 8 * sb + sr;  // tile row; tr & 7 == sr
                   uint8_t* base = sTile + c * kChunkBytes + tr * 128;
-                  const uint4 v = R[4 * c + sb];
+                  const int k4 = 4 * (4 * cc + sb);
+                  const uint4 v = make_uint4(G[k4], G[k4 + 1], G[k4 + 2], G[k4 + 3]);
                   const uint2 a0 = e4m3x4_to_bf16x4_scaled(v.x), a1 = e4m3x4_to_bf16x4_scaled(v.y);
                   const uint2 a2 = e4m3x4_to_bf16x4_scaled(v.z), a3 = e4m3x4_to_bf16x4_scaled(v.w);
                   *reinterpret_cast<uint4*>(base + (((2 * pc) ^ sr) << 4)) =
@@ -270,7 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         issued_tiles = j + 1;
-        if (j + 1 < ntiles) load_row(j + 1);  // in flight while this tile computes
+        if (FP8 && j + 1 < ntiles) {  // tile j's codes are consumed: park tile j + 1's
+          park();
+          if (j + 2 < ntiles) load_row(j + 2);
+        }
       }
       if (!FP8 && t == 0 && !ok && issued_tiles > 0) {
         // never leave with a copy in flight: the last issued tile's groups
