@@ -198,105 +198,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int kbase = j * BN;
         const bool mask = kbase + BN - 1 > pos;
-        // One pass over S with the current running max m_used: P (bf16 pairs)
-        // stays in registers until the whole tile is done, so S is intact in
-        // TMEM if a second pass is needed.  That happens on the first tile and
-        // when a row's max grows by more than 2^8 (tcgen05.ld/st are
-        // warp-collective: the warp redoes the pass together; rows whose max
-        // did not move recompute the same values).
-        uint32_t pk[BN / 2];
-        float lsum = 0.f;
+        // The whole S row goes to registers with four loads and one wait (TMEM
+        // load latency is paid once per tile), so P can overwrite S's columns
+        // right away.  One pass exponentiates with the running max m_used; a
+        // second pass, from the registers, only runs on the first tile and when
+        // a row's max grows by more than 2^8 (tcgen05.ld/st are warp-collective:
+        // the warp redoes it together; rows whose max did not move recompute
+        // the same values).
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(lane_addr + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        tmem_ld_wait();
+        if (mask) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e)
+            if (kbase + e > pos) sr[e] = __float_as_uint(-INFINITY);
+        }
         float mx = -INFINITY;
-        // S is read 16 columns at a time with the next load in flight while a
-        // chunk is processed (tcgen05.wait::ld waits for every load issued).
-        if (j == 0) {  // no running max yet: find this tile's max first
-          uint32_t ra[16], rb[16];
-          tmem_ld16(lane_addr + colS, ra);
-          tmem_ld_wait();
+        if (j == 0) {  // no running max yet: this tile's max first
 #pragma unroll
-          for (int c = 0; c < BN / 16; ++c) {
-            uint32_t(&cur)[16] = (c & 1) ? rb : ra;
-            uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
-            if (c + 1 < BN / 16) tmem_ld16(lane_addr + colS + (c + 1) * 16, nxt);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
-              if (mask) {
-                if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
-                if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
-              }
-              mx = fmax3(mx, s0, s1);
-            }
-            if (c + 1 < BN / 16) tmem_ld_wait();
-          }
+          for (int e = 0; e < BN / 2; ++e)
+            mx = fmax3(mx, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
           m_used = mx;
         }
-        // pass 0 exponentiates with the running max; pass 1 only runs when a
-        // row's max grew by more than 2^8 (after the rescale below)
-#pragma unroll 1
-        for (int pass = 0; pass < 2; ++pass) {
+        // P = 2^(s c - m c) as bf16 pairs over the first 64 columns of S; returns the row sum
+        auto exp_pass = [&](bool track) -> float {
           const float neg = -m_used * sl2;
           float s0sum = 0.f, s1sum = 0.f;
-          const bool track = pass == 0 && j > 0;
-          uint32_t ra[16], rb[16];
-          tmem_ld16(lane_addr + colS, ra);
-          tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < BN / 16; ++c) {
-            uint32_t(&cur)[16] = (c & 1) ? rb : ra;
-            uint32_t(&nxt)[16] = (c & 1) ? ra : rb;
-            if (c + 1 < BN / 16) tmem_ld16(lane_addr + colS + (c + 1) * 16, nxt);
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t q16[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float s0 = __uint_as_float(cur[2 * e]), s1 = __uint_as_float(cur[2 * e + 1]);
-              if (mask) {
-                if (kbase + c * 16 + 2 * e > pos) s0 = -INFINITY;
-                if (kbase + c * 16 + 2 * e + 1 > pos) s1 = -INFINITY;
-              }
+            for (int e = 0; e < 16; ++e) {
+              const float s0 = __uint_as_float(sr[32 * c + 2 * e]);
+              const float s1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
               if (track) mx = fmax3(mx, s0, s1);
               float u0, u1;
               fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
               const float p0 = ex2(u0), p1 = ex2(u1);
               add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
-              pk[8 * c + e] = pack_bf16x2(p0, p1);
+              q16[e] = pack_bf16x2(p0, p1);
             }
-            if (c + 1 < BN / 16) tmem_ld_wait();
+            tmem_st16(lane_addr + colS + c * 16, q16);
           }
-          lsum = s0sum + s1sum;
-          if (!track) break;
+          return s0sum + s1sum;
+        };
+        float lsum = exp_pass(j > 0);
+        if (j > 0) {
           const bool need = mx > m_used + thr;
-          if (!__any_sync(0xffffffffu, need)) break;
-          const float alpha = need ? ex2((m_used - mx) * sl2) : 1.f;
-          if (need) {
-            l *= alpha;
-            m_used = mx;
-          }
-          // rescale O_t once its previous P V product has landed
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
-                                                 &abort_flag))) {
-            report_timeout(p.status, 2, &abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2((m_used - mx) * sl2) : 1.f;
+            if (need) {
+              l *= alpha;
+              m_used = mx;
+            }
+            // rescale O_t once its previous P V product has landed
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
+                                                   &abort_flag))) {
+              report_timeout(p.status, 2, &abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t r[16];
-            tmem_ld16(lane_addr + colO + c * 16, r);
-            tmem_ld_wait();
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t r[16];
+              tmem_ld16(lane_addr + colO + c * 16, r);
+              tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st16(lane_addr + colO + c * 16, r);
+              for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st16(lane_addr + colO + c * 16, r);
+            }
+            lsum = exp_pass(false);
           }
-        }
-        if (!ok) break;
-        // P over the first 64 columns of S
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t q16[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) q16[e] = pk[16 * c + e];
-          tmem_st16(lane_addr + colS + c * 16, q16);
         }
         l += lsum;
         tmem_st_wait();
