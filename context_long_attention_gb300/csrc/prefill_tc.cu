@@ -47,7 +47,7 @@ struct Cfg {
   static constexpr int kChunks = D / 64;                   // 128-byte column chunks per row
   static constexpr int kQBytes = BM * D * 2;               // one Q tile
   static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
-  static constexpr int kSlots = D == 128 ? 4 : 8;          // ring of K/V tiles
+  static constexpr int kSlots = D == 128 ? 5 : 10;         // ring of K/V tiles (5 x 32 KB fits beside Q)
   static constexpr int kSmem = 2 * kQBytes + kSlots * kSlotBytes + 1024;
 };
 
