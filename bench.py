@@ -74,7 +74,7 @@ def decode_bytes(ctx, H, fp8=True):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active," \
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown," \
@@ -90,7 +90,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -173,7 +173,7 @@ def oracle_prefill_sample(rows_per_call=64, seed=0, budget_s=15.0):
     done_flops = 0
     done_rows = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and done_rows < 4 * rows_per_call:
+    while time.perf_counter() - t0 < budget_s and done_rows < 64 * rows_per_call:
         li = n_late + rng.choice(n_late, size=rows_per_call, replace=False)
         f = np.asarray(plan["order"][0])[li]
         pos = np.asarray(plan["pos"][0])[li]
@@ -410,7 +410,7 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
