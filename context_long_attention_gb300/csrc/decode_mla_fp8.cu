@@ -1,0 +1,677 @@
+// MLA split-KV decode over an FP8-E4M3 cache, on FP8 tensor-core products.
+//
+// The work is that of the bf16 MLA decode: one decode query per request (64
+// heads x 576 dims) against the rows one virtual shard stores ("How GPUs Share
+// a Long Context During LLM Inference" §3.1-3.4); keys are the whole 576-dim
+// latent entry and values its first 512 dims (vLLM blog "GLM-5.3 Part 2",
+// footnote 1); each work item (a row range of one (shard, request) pair of
+// the decode plan) yields a partial O and the natural-log LSE over its rows,
+// merged later exactly (§3.3).  A cache entry is 576 E4M3 codes and one fp32
+// scale per token (value = code x scale).
+//
+// The codes go from HBM to shared memory by TMA as stored and feed
+// kind::f8f6f4 products directly: nothing is expanded to 16 bits.  The bf16
+// query and the softmax weights are not E4M3 numbers, so each is carried as
+// a pair hi + lo of E4M3 numbers (hi = x rounded to E4M3, lo = x - hi rounded
+// to E4M3), which keeps 8 significant bits (relative error <= 2^-8) for
+// |x| >= 2^-2 and an absolute error <= 2^-10 below that:
+//   query:   x = q 2^e_q, with e_q per request so that max |x| is in [128, 256)
+//   weights: x = 2^(s - M_h) scale_row 2^g, with M_h the running max of head h
+//            and g per work item so that scale_row 2^g < 32; the running max
+//            moves when a score passes it by more than 2^3, so x < 256
+// The products (transposed so that M = 128 KV rows):
+//   S^T [128 rows x 128] = K_codes [128 x 576] . [Q_hi | Q_lo]^T   (N = 128)
+//     score(row, h) = (S^T[row][h] + S^T[row][64 + h]) scale_row 2^-e_q
+//   O^T [512 x 64]      += V_codes^T [512 x 128] . (P_hi^T + P_lo^T) (K = 2 x 128)
+// V_codes^T is the tile's first four 128-dim chunks read as an MN-major
+// operand; P_hi^T goes over the tile's rope chunk once S^T is computed.
+//
+// Roles (320 threads): warps 0-7 softmax (thread = KV row of the tile = TMEM
+// lane, warps w and w + 4 taking heads 0-31 and 32-63 of the same rows; in
+// the epilogue, a dim row of O^T); warp 8 TMA producer; warp 9 MMA issuer and
+// TMEM owner.  Two tile stages in shared memory, each refilled chunk by chunk
+// as P.V's M-blocks release it, and two S^T buffers in TMEM let the next
+// tile's QK^T run while this tile's softmax works.  The issuer puts QK^T
+// first: P.V goes one M-block at a time, so a late tile waits for one block.
+// TMEM: S^T buffer b at columns [128 b, 128 b + 128); O^T M-block mb at
+// [256 + 64 mb, 320 + 64 mb).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace cpattn {
+namespace {
+using namespace tc;
+
+constexpr int kRows = 128;   // KV rows per tile (MMA M)
+constexpr int kHeads = 64;   // query heads (zero-padded)
+constexpr int kDqk = 576, kDv = 512;
+constexpr int kChunkBytes = kRows * 128;           // dims [128c, 128c + 128) of 128 rows: 16 KB
+constexpr int kRopeOff = 4 * kChunkBytes;          // dims [512, 576): 128 rows x 64 B
+constexpr int kStageBytes = kRopeOff + kRows * 64; // 73,728 B
+constexpr int kQOff = 2 * kStageBytes;             // [Q_hi | Q_lo]: 128 operand rows x 576 B
+constexpr int kPloOff = kQOff + kStageBytes;       // P_lo^T: 128 rows x 64 heads
+constexpr int kSmem = kPloOff + kRows * 64 + 1024;
+constexpr int kThreads = 320;
+constexpr int kSoftmax = 256;  // warps 0-7: a row's 64 heads in two halves of 32
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kPrefetchAhead = 2;  // tiles between the L2 prefetch and the shared-memory copy
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 3.0f;  // the running max moves when a score passes it by > 2^3
+constexpr int kWeightTop = 5;         // scale_row 2^g < 2^5, so a weight 2^(s - M) scale_row 2^g < 2^8
+
+struct Params {
+  const int32_t* plan;
+  int B, off_pair, off_worker, off_work;
+  const __nv_bfloat16* q;
+  ShardPtrs k;  // code arrays (for the L2 prefetch; the tiles come through the tensor maps)
+  ScalePtrs sc;
+  int H;
+  float scale_log2;  // sm_scale * log2(e)
+  float* o_part;
+  float* lse_part;
+  float* ws_o;
+  float* ws_lse;
+  unsigned* status;
+  unsigned long long wait_ns;
+};
+
+// Tensor maps of the shards' code arrays ([rows, 576] bytes): dims [0, 512)
+// in 128-byte boxes with a 128-byte swizzle, dims [512, 576) with a 64-byte one.
+struct CodeMaps {
+  CUtensorMap body[CP_MAX_SHARDS];
+  CUtensorMap rope[CP_MAX_SHARDS];
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ int ordered(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float unordered(int b) {
+  return __int_as_float(b >= 0 ? b : b ^ 0x7FFFFFFF);
+}
+// 2^e for integer e in [-126, 127], exactly.
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Byte offset of (row, byte) in a 128-byte-swizzled [rows][128 B] block and
+// in a 64-byte-swizzled [rows][64 B] block (the TMA and MMA layouts).
+__device__ __forceinline__ int sw128(int row, int byte) {
+  return row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15);
+}
+__device__ __forceinline__ int sw64(int row, int byte) {
+  return row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3))) << 4) + (byte & 15);
+}
+
+// Two values -> E4M3 pairs (hi, lo) with hi + lo ~ (x0, x1); byte 0 holds x0's code.
+// The fp32 -> f16 step uses single conversions (the paired form slows the
+// tensor-core products of the CTA); the E4M3 steps work on f16x2.
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint16_t a, b, h, l;
+  uint32_t xh, back, rem;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(a) : "f"(x0));
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(b) : "f"(x1));
+  asm("mov.b32 %0, {%1, %2};" : "=r"(xh) : "h"(a), "h"(b));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(xh));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rem) : "r"(xh), "r"(back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(rem));
+  hi = h;
+  lo = l;
+}
+
+// Exponent e with |x| < 2^e for the largest |x| of a set (x > 0 normal);
+// the scaling exponent that maps it into [2^(top-1), 2^top) is top - e.
+__device__ __forceinline__ int scale_exponent(float maxabs, int top, int fallback) {
+  if (!(maxabs > 0.f)) return fallback;
+  const int E = (__float_as_int(maxabs) >> 23) & 0xFF;
+  const int e = E == 0 ? -126 : E - 126;
+  return max(-120, min(120, top - e));
+}
+
+__device__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
+  *abort = 1;
+  if (atomicCAS(status, 0u, 1u) == 0u) {
+    status[1] = kKernDecodeMlaFp8;
+    status[2] = site;
+    status[3] = blockIdx.x;
+    __threadfence();
+  }
+}
+
+// One work item of this CTA as every role sees it.
+struct Item {
+  int r, b, nrows, ntiles;
+  long long row0;  // first shard row
+  float* out_o;
+  float* out_l;
+};
+__device__ __forceinline__ Item read_item(const Params& p, int wi) {
+  const cp_work_desc wd = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work)[wi];
+  const cp_pair_desc pd = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair)[wd.pair];
+  Item it;
+  it.r = wd.pair / p.B;
+  it.b = wd.pair % p.B;
+  it.nrows = wd.row_end - wd.row_begin;
+  it.ntiles = (it.nrows + kRows - 1) / kRows;
+  it.row0 = (long long)pd.row_off + wd.row_begin;
+  it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
+                         : p.ws_o + (long long)wd.part * p.H * kDv;
+  it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
+                         : p.ws_lse + (long long)wd.part * p.H;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_mla_fp8_kernel(const __grid_constant__ CodeMaps maps, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  // bar_full[s][q]: chunk group q of stage s (q < 4: dims [128q, 128q + 128);
+  //   q = 4: the rope dims) holds its tile.
+  // bar_done[s]: the P.V of the tile in stage s has completed, and with it
+  //   every product that read the stage (one commit per tile: a commit holds
+  //   the issuing thread until the products before it finish, so the stage
+  //   is released whole rather than chunk by chunk).
+  // bar_s[b]: S^T buffer b holds its tile's products.  bar_p: this tile's
+  // P^T is written.  bar_q: the work item's query is in shared memory.
+  __shared__ __align__(8) uint64_t bar_full[2][5], bar_done[2], bar_s[2];
+  __shared__ __align__(8) uint64_t bar_p, bar_q, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
+  __shared__ __align__(16) float sM[kHeads];  // running max per head (log2 units)
+  __shared__ float sDelta[kHeads];            // its last move; in the epilogue 1 / column sum
+  __shared__ int sRed[4][kHeads];             // per row-quarter column maxima, then column sums
+  __shared__ uint32_t sRed1[8];               // per-warp max of |q| or of the token scales
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_full[s][q]), 1);
+      mbar_init(smem_u32(&bar_done[s]), 1);
+      mbar_init(smem_u32(&bar_s[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_p), kSoftmax);
+    mbar_init(smem_u32(&bar_q), kSoftmax);
+    mbar_init(smem_u32(&bar_drain), 1);
+    abort_flag = 0;
+    zero_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t sbase = smem_u32(smem);
+  const int w0 = p.plan[p.off_worker + blockIdx.x], w1 = p.plan[p.off_worker + blockIdx.x + 1];
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_g[2] = {-1, -1}, last_n[2] = {0, 0};  // last tile per stage, groups issued for it
+      bool ok = true;
+      int g = 0;
+      for (int wi = w0; wi < w1 && ok; ++wi) {
+        const Item it = read_item(p, wi);
+        const uint8_t* codes = static_cast<const uint8_t*>(p.k.p[it.r]);
+        auto prefetch = [&](int jt) {  // tile jt of the item into L2 (rows are contiguous)
+          const int rows = min(kRows, it.nrows - jt * kRows);
+          prefetch_l2_bulk(codes + (it.row0 + (long long)jt * kRows) * kDqk, (uint32_t)rows * kDqk);
+        };
+        for (int jt = 0; jt < kPrefetchAhead && jt < it.ntiles; ++jt) prefetch(jt);
+        for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
+          const int s = g & 1;
+          const uint32_t stage = sbase + s * kStageBytes;
+          const int y = (int)(it.row0 + (long long)j * kRows);
+          if (j + kPrefetchAhead < it.ntiles) prefetch(j + kPrefetchAhead);
+          // the stage is free once the P.V of its previous tile (g - 2) has completed
+          if (g >= 2 && !mbar_wait(smem_u32(&bar_done[s]), ((g >> 1) & 1) ^ 1, p.wait_ns,
+                                   &abort_flag)) {
+            report_timeout(p.status, 1, &abort_flag);
+            ok = false;
+            break;
+          }
+          for (int q = 0; q < 5; ++q) {
+            const uint32_t full = smem_u32(&bar_full[s][q]);
+            if (q < 4) {
+              mbar_expect_tx(full, kChunkBytes);
+              tma_load_2d(stage + q * kChunkBytes, &maps.body[it.r], 128 * q, y, full);
+            } else {
+              mbar_expect_tx(full, kRows * 64);
+              tma_load_2d(stage + kRopeOff, &maps.rope[it.r], 4 * 128, y, full);
+            }
+            last_g[s] = g;
+            last_n[s] = q + 1;
+          }
+        }
+      }
+      // Never leave with a copy in flight.
+      for (int s = 0; s < 2; ++s)
+        for (int q = 0; q < last_n[s]; ++q)
+          mbar_wait(smem_u32(&bar_full[s][q]), (last_g[s] >> 1) & 1, 1000000000ull, &zero_flag);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idQK = idesc_e4m3_f32(kRows, 2 * kHeads, 0, 0);
+      const uint32_t idPV = idesc_e4m3_f32(kRows, kHeads, 1, 1);
+      // Descriptors are built once; an MMA adds its byte offset / 16 to the
+      // start-address field (shared addresses stay below 2^18, so it never carries).
+      const uint32_t st0 = sbase, st1 = sbase + kStageBytes;
+      const uint64_t dK[2] = {smem_desc(st0, 16, 1024, 2), smem_desc(st1, 16, 1024, 2)};
+      const uint64_t dKr[2] = {smem_desc(st0 + kRopeOff, 16, 512, 4),
+                               smem_desc(st1 + kRopeOff, 16, 512, 4)};
+      const uint64_t dV[2] = {smem_desc(st0, kChunkBytes, 1024, 2),
+                              smem_desc(st1, kChunkBytes, 1024, 2)};
+      const uint64_t dQ = smem_desc(sbase + kQOff, 16, 1024, 2);
+      const uint64_t dQr = smem_desc(sbase + kQOff + kRopeOff, 16, 512, 4);
+      const uint64_t dPlo = smem_desc(sbase + kPloOff, 16, 512, 4);
+      auto full_bar = [&](int gq, int q) { return smem_u32(&bar_full[gq & 1][q]); };
+      // S^T(gq) += K_codes . [Q_hi | Q_lo]^T over chunk group q
+      auto qk_group = [&](int gq, int q) {
+        const int s = gq & 1;
+        const uint32_t d = tmem + 128 * s;
+        tc_fence_after();
+        if (q < 4) {
+          const uint64_t a = (s ? dK[1] : dK[0]) + (uint64_t)((q * kChunkBytes) >> 4);
+          const uint64_t b = dQ + (uint64_t)((q * kChunkBytes) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss_f8(d, a + 2 * ks, b + 2 * ks, idQK, (q | ks) != 0 ? 1u : 0u);
+        } else {
+          const uint64_t a = s ? dKr[1] : dKr[0];
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) mma_ss_f8(d, a + 2 * ks, dQr + 2 * ks, idQK, 1u);
+          mma_commit(smem_u32(&bar_s[s]));
+        }
+      };
+      // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T); the last block's
+      // commit releases the stage and P_lo^T's buffer.
+      auto pv_block = [&](int gp, int mb, bool first) {
+        const int s = gp & 1;
+        const uint64_t av = (s ? dV[1] : dV[0]) + (uint64_t)((mb * kChunkBytes) >> 4);
+        const uint64_t bh = s ? dKr[1] : dKr[0];  // P_hi^T over the rope chunk
+        const uint32_t d = tmem + 256 + 64 * mb;
+#pragma unroll
+        for (int kk = 0; kk < kRows / 32; ++kk) {
+          const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
+          mma_ss_f8(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || !first) ? 1u : 0u);
+          mma_ss_f8(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
+        }
+        if (mb == 3) mma_commit(smem_u32(&bar_done[s]));
+      };
+      bool ok = true;
+      int g = 0, nq = 0;  // tiles and non-empty items so far
+      for (int wi = w0; wi < w1 && ok; ++wi) {
+        const Item it = read_item(p, wi);
+        if (it.ntiles == 0) continue;
+        // the item's query is in place (written after every earlier product completed)
+        if (!mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag)) {
+          report_timeout(p.status, 2, &abort_flag);
+          break;
+        }
+        ++nq;
+        int done = 0;  // chunk groups of QK^T(g) already issued
+        for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
+          for (; done < 5; ++done) {
+            if (!mbar_wait(full_bar(g, done), (g >> 1) & 1, p.wait_ns, &abort_flag)) {
+              report_timeout(p.status, 3, &abort_flag);
+              ok = false;
+              break;
+            }
+            qk_group(g, done);
+          }
+          if (!ok) break;
+          // Next tile's QK^T groups go first, as their codes land (its S^T buffer
+          // was read before P(g - 1) arrived); P.V(g) M-block by M-block once P(g)
+          // is written, so a late QK^T waits behind one block at most.
+          const bool more = j + 1 < it.ntiles;
+          int next = 0, mb = 0;
+          bool p_ready = false;
+          const uint64_t t0 = global_timer_ns();
+          for (uint32_t spin = 1; mb < 4; ++spin) {
+            if (more && next < 5 && mbar_test(full_bar(g + 1, next), ((g + 1) >> 1) & 1)) {
+              qk_group(g + 1, next++);
+              continue;
+            }
+            if (!p_ready && mbar_test(smem_u32(&bar_p), g & 1)) {
+              p_ready = true;
+              tc_fence_after();
+            }
+            if (p_ready) {
+              pv_block(g, mb, j == 0);
+              ++mb;
+              continue;
+            }
+            if ((spin & 255u) == 0 && (abort_flag || global_timer_ns() - t0 > p.wait_ns)) break;
+          }
+          if (mb < 4) {
+            report_timeout(p.status, 4, &abort_flag);
+            ok = false;
+            break;
+          }
+          done = next;
+        }
+      }
+      // Never free TMEM under a running MMA.
+      mma_commit(smem_u32(&bar_drain));
+      mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int quarter = warp & 3;          // TMEM lane quarter: tile rows [32 quarter, +32)
+    const int hb = (warp >> 2) * 32;       // this warp's heads [hb, hb + 32)
+    const int t = quarter * 32 + lane;     // tile row = TMEM lane; in the epilogue a dim row
+    const int tid = threadIdx.x;           // 0 .. 255
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* sQ = smem + kQOff;
+    uint8_t* sPlo = smem + kPloOff;
+    bool ok = true;
+    int g = 0;
+    for (int wi = w0; wi < w1 && ok; ++wi) {
+      const Item it = read_item(p, wi);
+      if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
+        for (int i = tid; i < p.H * kDv; i += kSoftmax) it.out_o[i] = 0.f;
+        for (int i = tid; i < p.H; i += kSoftmax) it.out_l[i] = -INFINITY;
+        continue;
+      }
+      // ---- [Q_hi | Q_lo] of request b: x = q 2^eq with max |x| in [128, 256).
+      // Every product of the previous item has completed (its epilogue waited
+      // for the last P.V), so the operand can be overwritten.
+      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
+      constexpr int kPieces = kDqk / 8;  // 16-byte pieces per head
+      uint32_t qmax = 0;                 // largest |q| as bf16 magnitude bits
+      for (int i = tid; i < p.H * kPieces; i += kSoftmax) {
+        const uint4 v = __ldg(qsrc + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+      }
+      qmax = __reduce_max_sync(0xffffffffu, qmax);
+      if (lane == 0) sRed1[warp] = qmax;
+      named_bar_sync(1, kSoftmax);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) qmax = max(qmax, sRed1[w]);
+      const int eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
+      const float qs = pow2i(eq);
+      for (int i = tid; i < kHeads * kPieces; i += kSoftmax) {
+        const int h = i / kPieces, d0 = (i % kPieces) * 8;
+        uint2 hw = make_uint2(0, 0), lw = make_uint2(0, 0);
+        if (h < p.H) {
+          const uint4 v = __ldg(qsrc + i);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t hs[4], ls[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
+                         hs[e], ls[e]);
+          hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
+          lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+        }
+        int oh, ol;
+        if (d0 < 4 * 128) {
+          const int base = (d0 >> 7) * kChunkBytes;
+          oh = base + sw128(h, d0 & 127);
+          ol = base + sw128(kHeads + h, d0 & 127);
+        } else {
+          oh = kRopeOff + sw64(h, d0 - 512);
+          ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+        }
+        *reinterpret_cast<uint2*>(sQ + oh) = hw;
+        *reinterpret_cast<uint2*>(sQ + ol) = lw;
+      }
+      if (tid < kHeads) sM[tid] = 0.f;  // set from the item's first tile
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bar_q));
+
+      const float* srow = p.sc.p[it.r] + it.row0;
+      const float cq = p.scale_log2 * pow2i(-eq);
+      int gs = 0;  // weights carry scale_row 2^gs (set on the item's first tile, only decreases)
+      float l[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) l[h] = 0.f;
+      for (int j = 0; j < it.ntiles; ++j, ++g) {
+        const int row = j * kRows + t;
+        const bool valid = row < it.nrows;
+        const float scale = valid ? __ldg(srow + row) : 0.f;
+        const int b = g & 1;
+        // The eight warps leave together: one that gave up meets the others at this vote.
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait(smem_u32(&bar_s[b]), (g >> 1) & 1, p.wait_ns, &abort_flag));
+        if (bar_red_or(1, kSoftmax, !got)) {
+          if (!got) report_timeout(p.status, 5, &abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // u = score - running max (log2 units); rows past the item read nothing
+        const float c = scale * cq;
+        float u[32];
+        float over = -INFINITY;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {  // 16 heads at a time keeps registers low
+          uint32_t a[16], z[16];
+          tmem_ld16(lane_addr + 128 * b + hb + 16 * half, a);
+          tmem_ld16(lane_addr + 128 * b + kHeads + hb + 16 * half, z);
+          tmem_ld_wait();
+#pragma unroll
+          for (int h4 = 0; h4 < 4; ++h4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 16 * half + 4 * h4]);
+            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = 16 * half + 4 * h4 + e;
+              u[h] = valid ? fmaf(__uint_as_float(a[4 * h4 + e]) + __uint_as_float(z[4 * h4 + e]), c, -mm[e])
+                           : -INFINITY;
+              over = fmaxf(over, u[h]);
+            }
+          }
+        }
+        // Block-wide vote: the item's first tile, a score past its running max by
+        // more than 2^3, or a token scale that would take a weight to 2^8 or more.
+        const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
+        if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2 || big)) {
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
+            if (lane == 0) sRed[quarter][hb + h] = m;
+          }
+          const uint32_t smx = __reduce_max_sync(0xffffffffu, __float_as_uint(scale));
+          if (lane == 0) sRed1[warp] = smx;
+          named_bar_sync(1, kSoftmax);
+          uint32_t smb = 0;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) smb = max(smb, sRed1[w]);
+          const float smax = __uint_as_float(smb);
+          const int gs_new = j == 0 ? scale_exponent(smax, kWeightTop, 0)
+                                    : min(gs, scale_exponent(smax, kWeightTop, gs));
+          if (tid < kHeads) {
+            const float cm = fmaxf(fmaxf(unordered(sRed[0][tid]), unordered(sRed[1][tid])),
+                                   fmaxf(unordered(sRed[2][tid]), unordered(sRed[3][tid])));
+            const float delta = (j == 0 || cm > kRescaleLog2) ? cm : 0.f;
+            sDelta[tid] = delta;
+            sM[tid] += delta;
+          }
+          named_bar_sync(1, kSoftmax);
+          const float gf = pow2i(max(gs_new - gs, -126));
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const float dl = sDelta[hb + h];
+            u[h] -= dl;
+            l[h] *= ex2(-dl);
+          }
+          if (j > 0) {
+            // O^T holds the earlier tiles: once the last P.V has landed, scale its columns
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1,
+                                                                  p.wait_ns, &abort_flag));
+            if (bar_red_or(1, kSoftmax, !landed)) {
+              if (!landed) report_timeout(p.status, 6, &abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            // column h of O^T becomes O^T 2^-delta_h 2^(gs_new - gs)
+#pragma unroll 1
+            for (int c = 0; c < 2 * (kDv / 128); ++c) {
+              const int mb = c >> 1, h0 = 16 * (c & 1);
+              uint32_t a[16];
+              tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                a[e] = __float_as_uint(__uint_as_float(a[e]) * (ex2(-sDelta[hb + h0 + e]) * gf));
+              tmem_st16(lane_addr + 256 + 64 * mb + hb + h0, a);
+            }
+            tmem_st_wait();
+          }
+          gs = gs_new;
+        }
+        // P^T row t, heads [hb, hb + 32): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
+        const float gr = scale * pow2i(gs);
+        uint32_t hw[8], lw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pk[e] = ex2(u[4 * k + e]);
+            l[4 * k + e] += pk[e];
+          }
+          uint32_t h0, l0, h1, l1;
+          split_e4m3x2(pk[0] * gr, pk[1] * gr, h0, l0);
+          split_e4m3x2(pk[2] * gr, pk[3] * gr, h1, l1);
+          hw[k] = h0 | (h1 << 16);
+          lw[k] = l0 | (l1 << 16);
+        }
+        // P_lo^T has one buffer: the previous tile's P.V must have read it
+        if (g > 0) {
+          const bool freed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1,
+                                                               p.wait_ns, &abort_flag));
+          if (bar_red_or(1, kSoftmax, !freed)) {
+            if (!freed) report_timeout(p.status, 7, &abort_flag);
+            ok = false;
+            break;
+          }
+        }
+        // MN-major operands [128 rows][64 heads], 64-byte swizzle; P_hi^T over the
+        // rope chunk of this tile's stage (QK^T(g) has read it)
+        uint8_t* phi = smem + b * kStageBytes + kRopeOff;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          *reinterpret_cast<uint4*>(phi + sw64(t, hb + 16 * k)) =
+              make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+          *reinterpret_cast<uint4*>(sPlo + sw64(t, hb + 16 * k)) =
+              make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_p));
+      }
+      if (!ok) break;
+      // ---- epilogue: column sums of l, O^T 2^-gs / l, LSE
+      const bool landed = __all_sync(
+          0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, p.wait_ns, &abort_flag));
+      if (bar_red_or(1, kSoftmax, !landed)) {
+        if (!landed) report_timeout(p.status, 8, &abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        float v = l[h];
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+        if (lane == 0) sRed[quarter][hb + h] = __float_as_int(v);
+      }
+      named_bar_sync(1, kSoftmax);
+      if (tid < kHeads) {
+        const float tot = __int_as_float(sRed[0][tid]) + __int_as_float(sRed[1][tid]) +
+                          __int_as_float(sRed[2][tid]) + __int_as_float(sRed[3][tid]);
+        sDelta[tid] = 1.f / tot;
+        if (tid < p.H) it.out_l[tid] = (sM[tid] + lg2(tot)) * kLn2;
+      }
+      named_bar_sync(1, kSoftmax);
+      const float og = pow2i(-gs);
+#pragma unroll 1
+      for (int mb = 0; mb < kDv / 128; ++mb) {
+        uint32_t a[32];
+        tmem_ld32(lane_addr + 256 + 64 * mb + hb, a);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const int hh = hb + h;
+          if (hh < p.H)
+            it.out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * og * sDelta[hh];
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, kSoftmax);  // shared state is free for the next item
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
+                                  const ShardPtrs& k, const ScalePtrs& sc,
+                                  const long long* shard_rows, int H, float sm_scale,
+                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                                  unsigned long long wait_ns, cudaStream_t s) {
+  Params p;
+  p.plan = dev_plan;
+  p.B = h.R;
+  p.off_pair = h.off_rank;
+  p.off_worker = h.off_req;
+  p.off_work = h.off_seg;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = k;
+  p.sc = sc;
+  p.H = H;
+  p.scale_log2 = sm_scale * kLog2e;
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
+  p.status = device_status_ptr();
+  if (!p.status) return cudaErrorInvalidDevice;
+  p.wait_ns = wait_ns;
+  CodeMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int r = 0; r < h.C; ++r) {
+    if (shard_rows[r] == 0) continue;
+    const uint64_t rows = (uint64_t)shard_rows[r];
+    if (!encode_tensor_map_u8_2d(&maps.body[r], k.p[r], kDqk, rows, kDqk, 128, kRows, true) ||
+        !encode_tensor_map_u8_2d(&maps.rope[r], k.p[r], kDqk, rows, kDqk, 64, kRows, false))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(decode_mla_fp8_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  decode_mla_fp8_kernel<<<h.n_tiles, kThreads, kSmem, s>>>(maps, p);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

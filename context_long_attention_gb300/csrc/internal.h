@@ -19,7 +19,7 @@ constexpr int kDecodeTileRows = 128;   // KV rows per decode scheduling tile (MM
 // Device status word layout (written by kernels, read by cp_device_error_check).
 //   [0] non-zero once any bounded wait gave up
 //   [1] kernel id   [2] wait site   [3] block index
-enum KernelId : unsigned { kKernPrefillTc = 1, kKernDecodeMlaTc = 2 };
+enum KernelId : unsigned { kKernPrefillTc = 1, kKernDecodeMlaTc = 2, kKernDecodeMlaFp8 = 3 };
 
 struct ShardPtrs {
   const void* p[CP_MAX_SHARDS];
@@ -64,6 +64,19 @@ cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
 // dims 1..rank-1).  False if the driver entry point is missing or rejects it.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides, const uint32_t* box);
+
+// [rows, cols] byte tensor (row stride row_bytes), box [box_rows, box_cols],
+// 128-byte swizzle if swizzle_128 else 64-byte.
+bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                             uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
+                             bool swizzle_128);
+
+// ---- MLA decode over an FP8 cache on FP8 tensor-core products (decode_mla_fp8.cu)
+cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
+                                  const ShardPtrs& k, const ScalePtrs& sc,
+                                  const long long* shard_rows, int H, float sm_scale,
+                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                                  unsigned long long wait_ns, cudaStream_t s);
 
 // ---- tensor-core MLA decode (decode_mla_tc.cu)
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,

@@ -485,6 +485,19 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const ui
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                             uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
+                             bool swizzle_128) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t d[2] = {cols, rows}, st[1] = {row_bytes};
+  const cuuint32_t b[2] = {box_cols, box_rows}, es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), d, st, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle_128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Limit of every bounded device wait: CPATTN_WAIT_LIMIT_MS (default 4000 ms),
 // read once per process.
 unsigned long long wait_limit_ns() {

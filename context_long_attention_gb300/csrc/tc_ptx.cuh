@@ -46,6 +46,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with `parity` to complete, for at most `limit_ns`
 // (measured on %globaltimer), or until *abort becomes non-zero.  Returns
 // false if it gave up.
@@ -80,6 +92,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes % 16 == 0); no completion.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -109,7 +125,8 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
-// offsets (16-byte units), descriptor version 1, swizzle mode (2 = 128 B).
+// offsets (16-byte units), descriptor version 1, swizzle mode (2 = 128 B,
+// 4 = 64 B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint32_t swizzle = 2) {
   uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
@@ -125,6 +142,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A/B (format code 0) and fp32
+// accumulation; K = 32 per instruction.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc], 8-bit operands.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc]
@@ -198,9 +231,17 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Two fp32 -> one bf16x2 word (round to nearest even; `lo` in the low half).
+// Two single conversions: on sm_103a the paired fp32 -> 16-bit conversion,
+// issued by the softmax warps at full rate, slows the CTA's tensor-core
+// products several fold, the single form barely at all (measured).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint16_t a, b;
+  uint32_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(a) : "f"(lo));
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(b) : "f"(hi));
+  asm("mov.b32 %0, {%1, %2};" : "=r"(r) : "h"(a), "h"(b));
+  return r;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -313,6 +313,23 @@ def test_decode_mla_sharp_scores(cp):
         mla_decode_case(cp, data, 8, fp8, 4)
 
 
+def test_decode_mla_fp8_scale_spread(cp):
+    """FP8 cache whose per-token scales grow along each request by up to 2^6
+    (so later tiles hold tokens with far larger scales than the first), with
+    the same values: the latent is re-quantised with the larger scales, so its
+    codes use less of the E4M3 range.  40 of the 64 head slots in use."""
+    ctx = [3000, 700, 129]
+    data = W.mla_decode_inputs(ctx, H=40, seed=41, device=DEV)
+    g = torch.Generator().manual_seed(43)
+    k = torch.cat([torch.clamp(torch.arange(L) * 7 // L + torch.randint(0, 2, (L,), generator=g), max=6)
+                   for L in ctx]).to(torch.float32)
+    scale = (data["kv_scale"].cpu() * torch.pow(2.0, k)).to(DEV)
+    data["kv_fp8"] = (data["kv_bf16"].float() / scale[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    data["kv_scale"] = scale
+    for C, nw in [(8, 3), (2, 0)]:
+        mla_decode_case(cp, data, C, True, nw, H=40)
+
+
 @pytest.mark.parametrize("fp8", [True, False])
 def test_decode_mla_full_size_sampled(cp, fp8):
     w = W.WORKLOADS["mla"]
