@@ -40,28 +40,42 @@ import torch  # noqa: E402
 import cp_workloads as W  # noqa: E402
 
 # DRAM bytes (read + write) per launch from the ncu captures summarised in
-# profiles/; a figure is reported only while the kernel source it was measured
-# on is unchanged (SHA-1 of the file).  The decode capture ran 8 of the 64
-# requests; its traffic scales with the tokens read.
+# profiles/; a figure is reported only while the kernel sources it was
+# measured on are unchanged (SHA-1 of the kernel file and the shared PTX
+# header).  The decode captures ran 8 of the 64 requests; their traffic scales
+# with the tokens read.
 PROFILED_TRAFFIC = {
-    "prefill": {"src": "context_long_attention_gb300/csrc/prefill_tc.cu",
-                "sha1": "f521201615d55e09efc998fc7d4198e9a3bf7def", "bytes": 2.370061e9 + 0.275298e9},
-    "decode_fp8": {"src": "context_long_attention_gb300/csrc/decode_mla_tc.cu",
-                   "sha1": "3c3f6dc8de660deb6fb6b37ca056248565998a8c", "bytes_per_token": (0.609499e9 + 0.010073e9) / (8 * 131072)},
-    "decode_bf16": {"src": "context_long_attention_gb300/csrc/decode_mla_tc.cu",
-                    "sha1": "3c3f6dc8de660deb6fb6b37ca056248565998a8c", "bytes_per_token": (1.209220e9 + 0.011080e9) / (8 * 131072)},
+    "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
+                        "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                "sha1": "0a9433007cd0c563b1e7a7f2166799f3dd34b052", "bytes": 2.370106e9 + 0.275549e9},
+    "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
+                           "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                   "sha1": "4cb3f309e8898b78becf5e13458cf1bb1f606503",
+                   "bytes_per_token": (0.637946e9 + 0.010263e9) / (8 * 131072)},
+    "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
+                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                    "sha1": "64f172d890a190d8e5237dc0d2192ddb2d638975",
+                    "bytes_per_token": (1.209230e9 + 0.011201e9) / (8 * 131072)},
 }
 
 
-def profiled_traffic(key, tokens=None):
+def sources_sha1(paths):
     import hashlib
+    h = hashlib.sha1()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(key, tokens=None):
+    """DRAM bytes per launch from the committed ncu capture of this kernel,
+    or None once the kernel's sources differ from the captured ones."""
     rec = PROFILED_TRAFFIC[key]
-    path = os.path.join(ROOT, rec["src"])
-    if not os.path.exists(path):
+    if rec["sha1"] is None or any(not os.path.exists(os.path.join(ROOT, r)) for r in rec["src"]):
         return None
-    with open(path, "rb") as f:
-        if hashlib.sha1(f.read()).hexdigest() != rec["sha1"]:
-            return None
+    if sources_sha1(rec["src"]) != rec["sha1"]:
+        return None
     return rec["bytes"] if "bytes" in rec else rec["bytes_per_token"] * tokens
 
 
@@ -168,6 +182,12 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def whole_job_rate(units_per_rank, total_ms, world):
+    """Units processed by all ranks (every replica runs the same workload) per
+    second of the slowest rank's time."""
+    return world * units_per_rank / (total_ms / 1e3)
 
 
 def max_over_ranks(x, world):
@@ -337,8 +357,8 @@ def run_ours(args, world, rank, local):
     # whole job: the work of all ranks over the slowest rank's time
     pre_total = max_over_ranks(sum(plan_ms) + sum(pre_ms), world)
     dec_total = max_over_ranks(sum(dec_ms) + sum(mrg_ms), world)
-    value = world * p_flops * args.steps / (pre_total / 1e3) / 1e12 if do_pre else None
-    dec_gbs = world * d_bytes * args.steps / (dec_total / 1e3) / 1e9 if do_dec else None
+    value = whole_job_rate(p_flops * args.steps, pre_total, world) / 1e12 if do_pre else None
+    dec_gbs = whole_job_rate(d_bytes * args.steps, dec_total, world) / 1e9 if do_dec else None
 
     # ---- end to end through the public API with host buffers (prefill)
     e2e = None
@@ -370,7 +390,7 @@ def run_ours(args, world, rank, local):
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world)
-        e2e = {"value": world * p_flops * args.steps / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_rate(p_flops * args.steps, e2e_ms, world) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4}
 

@@ -625,8 +625,8 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
       mla && kv_dtype == CP_FP8_E4M3
           ? launch_decode_mla_fp8((const int32_t*)dev_plan, h, q, K, S, shard_rows, Hq, sm_scale,
                                   o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
-      : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, false, q, K, S, shard_rows, Hq,
-                                   sm_scale, o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+      : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, q, K, shard_rows, Hq, sm_scale,
+                                   o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
           : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, Hq, Hkv, Dqk,
                                Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");

@@ -1,4 +1,4 @@
-// MLA split-KV decode on the tcgen05 tensor cores.
+// MLA split-KV decode over a bf16 cache on the tcgen05 tensor cores.
 //
 // One decode query per request (64 heads x 576 dims) against the rows a
 // virtual shard stores ("How GPUs Share a Long Context During LLM Inference"
@@ -6,7 +6,8 @@
 // (§1.3); keys are the whole entry and values its first 512 dims (vLLM blog
 // "GLM-5.3 Part 2", footnote 1).  Each work item (a row range of one
 // (shard, request) pair, from the decode plan) yields a partial O and the
-// natural-log LSE over its rows, merged later exactly (§3.3).
+// natural-log LSE over its rows, merged later exactly (§3.3).  (An FP8 cache
+// takes the FP8 tensor-core kernel instead.)
 //
 // The products are transposed so that the MMA M dimension is 128 KV rows:
 //   S^T [128 rows x 64 heads]  = K_tile [128 x 576] . Q^T          (K = 576)
@@ -14,16 +15,12 @@
 // V_tile^T is the same shared-memory tile as K_tile read as an MN-major
 // operand (V is the first 512 latent dims), so one bf16 tile serves both
 // products.  P^T (bf16) goes over the tile's last 64-dim chunk, which only
-// the first product reads.  An FP8 cache is expanded to bf16 exactly: the
-// E4M3 bits move into a bf16 whose value is 2^-120 times the code's value
-// (exponent bias 127 instead of 7), and the 2^120 and the per-token scale are
-// applied to the scores and folded into P^T.
+// the first product reads.
 //
 // Warp roles (256 threads): warps 0-3 softmax, thread = KV row of the tile
 // (TMEM lane) and, in the epilogue, dim row of O^T; thread 0 also owns TMEM
-// and issues the MMAs; warps 4-7 fill the tile chunk group by chunk group as
-// the previous tile's P.V releases it (FP8: from the next tile's codes, held in
-// the fill warps' registers; bf16: by TMA).
+// and issues the MMAs; one thread of warp 4 refills the tile by TMA chunk
+// group by chunk group as the previous tile's P.V releases it.
 // Softmax down the KV axis needs per-head maxima over the 128 rows of a tile.
 // The running maximum M_h used in the exponentials only moves when some score
 // exceeds it by more than 2^8 (checked per tile with one block-wide vote);
@@ -52,19 +49,16 @@ constexpr int kTileBytes = kChunks * kChunkBytes;  // 147,456 B
 constexpr int kQChunkBytes = kHeads * 128;  // one chunk of Q: 8 KB
 constexpr int kQBytes = kChunks * kQChunkBytes;    // 73,728 B
 constexpr int kSmem = kTileBytes + kQBytes + 1024;
-constexpr int kStageCol = 320;  // TMEM columns [320, 464): parked FP8 codes of the next tile
 constexpr int kThreads = 256;  // 8 warps: 2 per SM sub-partition, up to 255 registers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr float kTwo120 = 1.329227995784916e36f;  // 2^120
 
 struct Params {
   const int32_t* plan;
   int B, off_pair, off_worker, off_work;
   const __nv_bfloat16* q;
   ShardPtrs k;
-  ScalePtrs sc;
   int H;
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
@@ -107,22 +101,11 @@ __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, 
   }
 }
 
-// Four E4M3 codes -> four bf16 whose values are 2^-120 x the codes' values.
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4_scaled(uint32_t w) {
-  const uint32_t lo = __byte_perm(w, 0u, 0x4140);  // bytes 0,1 -> bits [0,8) and [16,24)
-  const uint32_t hi = __byte_perm(w, 0u, 0x4342);  // bytes 2,3
-  uint2 r;
-  r.x = ((lo & 0x00800080u) << 8) | ((lo & 0x007F007Fu) << 4);
-  r.y = ((hi & 0x00800080u) << 8) | ((hi & 0x007F007Fu) << 4);
-  return r;
-}
-
 // Chunk groups of a tile: q = 0..3 hold dims [128q, 128q + 128) (chunks 2q,
 // 2q+1, also the M-block q of V^T); q = 4 holds the rope dims [512, 576),
 // overwritten by P^T once S^T is computed.
 __device__ __forceinline__ int group_chunks(int q) { return q < 4 ? 2 : 1; }
 
-template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mla_tc_kernel(const __grid_constant__ ShardMaps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -146,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_fill[q]), FP8 ? 128 : 1);
+    for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_fill[q]), 1);
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bar_mb[q]), 1);
     mbar_init(smem_u32(&bar_s), 1);
     mbar_init(smem_u32(&bar_drain), 1);
@@ -158,13 +141,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM: S^T cols [0,64); O^T block mb: [64 + 64 mb, 128 + 64 mb); FP8 staging [320, 464)
+  // TMEM: S^T cols [0,64); O^T block mb: [64 + 64 mb, 128 + 64 mb)
   const uint32_t tmem = tmem_slot;
 
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work);
   const int w0 = p.plan[p.off_worker + blockIdx.x], w1 = p.plan[p.off_worker + blockIdx.x + 1];
-  constexpr int kRowBytes = FP8 ? kDqk : 2 * kDqk;
   // Every barrier completes exactly once per tile, so the parity of the phase
   // to wait for is that of the tile's index g over all items of this CTA.
   int g0 = 0;
@@ -186,8 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = threadIdx.x; i < p.H; i += kThreads) out_l[i] = -INFINITY;
       continue;
     }
-    const uint8_t* kbase = static_cast<const uint8_t*>(p.k.p[r]) + row0 * kRowBytes;
-    const float* sbase = FP8 ? p.sc.p[r] + row0 : nullptr;
 
     // ---- the query of request b -> sQ (K-major, 128-byte swizzle); heads >= H are zero.
     // The previous item's MMAs have completed: its softmax waited for its last P.V.
@@ -204,108 +184,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     if (warp >= 4) {
-      // ------------------------------------------------------------ tile fill
-      const int t = threadIdx.x - 128;  // tile row (bf16 copies are issued by t == 0)
-      // FP8: the next tile is loaded into registers while this one computes.
-      // A warp covers 32 rows; one load instruction reads 8 rows x 64 bytes
-      // (one chunk of each): lane l takes row 8 sb + l / 4 of the warp's rows,
-      // 16 codes at piece l % 4 of chunk c, kept in R[4 c + sb].
-      const int lw = warp - 4, sr = lane >> 2, pc = lane & 3;
-      uint4 R[FP8 ? kDqk / 16 : 1];
-      auto load_row = [&](int j) {
-        if (FP8) {
+      // ------------------------------------------------------------ tile fill (TMA, one thread)
+      if (threadIdx.x == 128) {
+        int issued_tiles = 0;  // tiles whose copies were issued (for the drain)
+        for (int j = 0; j < ntiles && ok; ++j) {
+          const int g = g0 + j;
 #pragma unroll
-          for (int sb = 0; sb < 4; ++sb) {
-            const int row = j * kRows + 32 * lw + 8 * sb + sr;
-            const bool valid = row < nrows;
-            const uint4* src = reinterpret_cast<const uint4*>(kbase + (long long)row * kDqk) + pc;
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-              R[4 * c + sb] = valid ? __ldg(src + 4 * c) : make_uint4(0, 0, 0, 0);
-          }
-        }
-      };
-      // FP8: the codes of the tile after next are in flight in R while those of
-      // the next tile wait in TMEM columns [kStageCol, kStageCol + 144) of the
-      // thread's own lane, so two tiles are always on their way from memory.
-      const uint32_t stage_addr = tmem + ((uint32_t)(32 * lw) << 16) + kStageCol;
-      auto park = [&]() {
-        if (FP8) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            uint32_t w[32];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              w[4 * e] = R[8 * m + e].x;
-              w[4 * e + 1] = R[8 * m + e].y;
-              w[4 * e + 2] = R[8 * m + e].z;
-              w[4 * e + 3] = R[8 * m + e].w;
+          for (int q = 0; q < 5; ++q) {
+            // group q is free once the previous tile's P.V M-block q (or, for the
+            // rope group that holds P^T, the whole P.V) has read it
+            if (ok && j > 0 && !mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]), (g - 1) & 1, p.wait_ns,
+                                          &abort_flag)) {
+              report_timeout(p.status, 1, &abort_flag);
+              ok = false;
             }
-            tmem_st32(stage_addr + 32 * m, w);
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            w[4 * e] = R[32 + e].x;
-            w[4 * e + 1] = R[32 + e].y;
-            w[4 * e + 2] = R[32 + e].z;
-            w[4 * e + 3] = R[32 + e].w;
-          }
-          tmem_st16(stage_addr + 128, w);
-          tmem_st_wait();
-        }
-      };
-      load_row(0);
-      if (FP8) {
-        park();
-        if (ntiles > 1) load_row(1);
-      }
-      int issued_tiles = 0;  // bf16: tiles whose copies were issued (for the drain)
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int g = g0 + j;
-#pragma unroll
-        for (int q = 0; q < 5; ++q) {
-          // group q is free once the previous tile's P.V M-block q (or, for the
-          // rope group that holds P^T, the whole P.V) has read it
-          if (ok && j > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]),
-                                                                (g - 1) & 1, p.wait_ns, &abort_flag))) {
-            report_timeout(p.status, 1, &abort_flag);
-            ok = false;
-          }
-          if (!ok) continue;
-          if (FP8) {
-            uint32_t G[32];  // this group's parked codes: piece 4 cc + sb at G[4 (4 cc + sb)]
-            if (q < 4) {
-              tmem_ld32(stage_addr + 32 * q, G);
-            } else {
-              uint32_t G16[16];
-              tmem_ld16(stage_addr + 128, G16);
-#pragma unroll
-              for (int e = 0; e < 16; ++e) G[e] = G16[e];
-            }
-            tmem_ld_wait();
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              if (cc < group_chunks(q)) {
-                const int c = 2 * q + cc;
-#pragma unroll
-                for (int sb = 0; sb < 4; ++sb) {
-                  const int tr = 32 * lw + 8 * sb + sr;  // tile row; tr & 7 == sr
-                  uint8_t* base = sTile + c * kChunkBytes + tr * 128;
-                  const int k4 = 4 * (4 * cc + sb);
-                  const uint4 v = make_uint4(G[k4], G[k4 + 1], G[k4 + 2], G[k4 + 3]);
-                  const uint2 a0 = e4m3x4_to_bf16x4_scaled(v.x), a1 = e4m3x4_to_bf16x4_scaled(v.y);
-                  const uint2 a2 = e4m3x4_to_bf16x4_scaled(v.z), a3 = e4m3x4_to_bf16x4_scaled(v.w);
-                  *reinterpret_cast<uint4*>(base + (((2 * pc) ^ sr) << 4)) =
-                      make_uint4(a0.x, a0.y, a1.x, a1.y);
-                  *reinterpret_cast<uint4*>(base + (((2 * pc + 1) ^ sr) << 4)) =
-                      make_uint4(a2.x, a2.y, a3.x, a3.y);
-                }
-              }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bar_fill[q]));
-          } else if (t == 0) {
+            if (!ok) continue;
             const uint32_t full = smem_u32(&bar_fill[q]);
             mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
             for (int cc = 0; cc < group_chunks(q); ++cc) {
@@ -314,18 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (int)(row0 + (long long)j * kRows), full);
             }
           }
+          if (!ok) break;
+          issued_tiles = j + 1;
         }
-        if (!ok) break;
-        issued_tiles = j + 1;
-        if (FP8 && j + 1 < ntiles) {  // tile j's codes are consumed: park tile j + 1's
-          park();
-          if (j + 2 < ntiles) load_row(j + 2);
+        if (!ok && issued_tiles > 0) {
+          // never leave with a copy in flight: the last issued tile's groups
+          for (int q = 0; q < 5; ++q)
+            mbar_wait(smem_u32(&bar_fill[q]), (g0 + issued_tiles - 1) & 1, 1000000000ull, &zero_flag);
         }
-      }
-      if (!FP8 && t == 0 && !ok && issued_tiles > 0) {
-        // never leave with a copy in flight: the last issued tile's groups
-        for (int q = 0; q < 5; ++q)
-          mbar_wait(smem_u32(&bar_fill[q]), (g0 + issued_tiles - 1) & 1, 1000000000ull, &zero_flag);
       }
     } else {
       // ------------------------------------------------------------ softmax (warps 0-3)
@@ -356,12 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (issued) mma_commit(smem_u32(&bar_s));
         }
         const bool valid = j * kRows + t < nrows;
-        // scores in log2 units; the FP8 tile holds 2^-120 x the codes
-        float cj = p.scale_log2, vscale = 1.f;
-        if (FP8) {
-          vscale = valid ? __ldg(sbase + j * kRows + t) : 0.f;
-          cj = p.scale_log2 * vscale * kTwo120;
-        }
+        const float cj = p.scale_log2;  // scores in log2 units
         // The four softmax warps leave together: a warp that gave up still
         // meets the others at the named barrier of this vote.
         const bool got = __all_sync(
@@ -427,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        // P^T row t: p = 2^u; the value weights carry the token's scale.
+        // P^T row t: p = 2^u.
         // MN-major B operand: row t = 64 heads x 2 B = one 128-byte swizzled row.
         uint8_t* prow = sP + t * 128;
 #pragma unroll
@@ -439,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2(u[h]), p1 = ex2(u[h + 1]);
             l[h] += p0;
             l[h + 1] += p1;
-            pk[e] = pack_bf16x2(p0 * vscale, p1 * vscale);
+            pk[e] = pack_bf16x2(p0, p1);
           }
           *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
@@ -477,7 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) sL[warp][h] = v;
         }
         named_bar_sync(1, 128);
-        const float oscale = FP8 ? kTwo120 : 1.f;
 #pragma unroll 1
         for (int mb = 0; mb < kDv / 128; ++mb) {
 #pragma unroll
@@ -490,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int hh = 32 * half + h;
               if (hh < p.H) {
                 const float tot = sL[0][hh] + sL[1][hh] + sL[2][hh] + sL[3][hh];
-                out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * oscale / tot;
+                out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) / tot;
               }
             }
           }
@@ -521,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
-                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc,
+cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,
+                                 const void* q, const ShardPtrs& k,
                                  const long long* shard_rows, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  unsigned long long wait_ns, cudaStream_t s) {
@@ -534,7 +417,6 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.off_work = h.off_seg;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = k;
-  p.sc = sc;
   p.H = H;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
@@ -546,17 +428,15 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.wait_ns = wait_ns;
   ShardMaps local;
   memset(&local, 0, sizeof(local));
-  if (!fp8) {
-    for (int r = 0; r < h.C; ++r) {
-      if (shard_rows[r] == 0) continue;
-      const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)shard_rows[r]};
-      const uint64_t strides[1] = {(uint64_t)kDqk * 2};
-      const uint32_t box[2] = {64, (uint32_t)kRows};
-      if (!encode_tensor_map_bf16(&local.m[r], k.p[r], 2, dims, strides, box))
-        return cudaErrorInvalidValue;
-    }
+  for (int r = 0; r < h.C; ++r) {
+    if (shard_rows[r] == 0) continue;
+    const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)shard_rows[r]};
+    const uint64_t strides[1] = {(uint64_t)kDqk * 2};
+    const uint32_t box[2] = {64, (uint32_t)kRows};
+    if (!encode_tensor_map_bf16(&local.m[r], k.p[r], 2, dims, strides, box))
+      return cudaErrorInvalidValue;
   }
-  auto kern = fp8 ? decode_mla_tc_kernel<true> : decode_mla_tc_kernel<false>;
+  auto kern = decode_mla_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   kern<<<h.n_tiles, kThreads, kSmem, s>>>(local, p);

@@ -78,9 +78,9 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                   unsigned long long wait_ns, cudaStream_t s);
 
-// ---- tensor-core MLA decode (decode_mla_tc.cu)
-cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h, bool fp8,
-                                 const void* q, const ShardPtrs& k, const ScalePtrs& sc,
+// ---- tensor-core MLA decode over a bf16 cache (decode_mla_tc.cu)
+cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,
+                                 const void* q, const ShardPtrs& k,
                                  const long long* shard_rows, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  unsigned long long wait_ns, cudaStream_t s);

@@ -270,7 +270,11 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  *   576-dim entry, values its first 512 dims ([GLM] footnote 1).
  *   q [B, H, 576] bf16; shard_k[r] [rows_r, 576] as kv_dtype CP_BF16, or
  *   CP_FP8_E4M3 codes with shard_scale[r] [rows_r] fp32 (value = code *
- *   scale); shard_v must be NULL.
+ *   scale); shard_v must be NULL.  FP8 codes must be finite (0x7F and 0xFF
+ *   are NaN in E4M3 and propagate), scales finite and >= 0.  The FP8 path
+ *   multiplies the codes on the tensor cores as they are stored; the bf16
+ *   query and the softmax weights enter those products as pairs of E4M3
+ *   numbers whose sum keeps 8 significant bits (see the kernel's notes).
  * mode CP_DECODE_GQA: q [B, Hq, D] and shard_k[r], shard_v[r]
  *   [rows_r, Hkv, D], all of kv_dtype CP_BF16 or CP_FP32; Dqk = Dv = D,
  *   D % 32 == 0, D <= 256; shard_scale must be NULL.
