@@ -291,13 +291,25 @@ def run_ours(args, world, rank, local):
         data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev,
                                    bf16=not fp8, fp8=fp8)
         dplan = cp.cp_decode_plan(m["C"], ctx, device=dev)
-        if fp8:
-            shards, scales = cp.cp_kv_shard_pack(dplan, data["kv_fp8"], data["kv_scale"])
-            del data["kv_fp8"], data["kv_scale"]
+        kv, kv_scale = (data["kv_fp8"], data["kv_scale"]) if fp8 else (data["kv_bf16"], None)
+        pages = None
+        if args.decode_paged:
+            # every (shard, request) pair's rows in pages of a shared pool, placed at random
+            ps = args.decode_paged
+            need = [-(-int(n) // ps) for n in dplan.pairs[:, 0]]
+            ids = np.random.default_rng(W.SEEDS["mla"] + rank).permutation(sum(need))
+            table = np.full((len(need), max(need)), -1, np.int32)
+            k0 = 0
+            for pr, n in enumerate(need):
+                table[pr, :n] = ids[k0:k0 + n]
+                k0 += n
+            pages = cp.PageTable(table, ps, sum(need), device=dev)
+            shards, scales = cp.cp_kv_shard_pack_paged(dplan, pages, kv, kv_scale)
         else:
-            shards, _ = cp.cp_kv_shard_pack(dplan, data["kv_bf16"])
-            scales = None
-            del data["kv_bf16"]
+            shards, scales = cp.cp_kv_shard_pack(dplan, kv, kv_scale)
+        del kv, kv_scale, data["kv_fp8" if fp8 else "kv_bf16"]
+        if fp8:
+            del data["kv_scale"]
         dq = data["q"]
         B = len(ctx)
         o_part = torch.empty((m["C"], B, m["H"], m["Dv"]), dtype=torch.float32, device=dev)
@@ -322,8 +334,12 @@ def run_ours(args, world, rank, local):
         e2.record(stream)
         if do_dec:
             dp = cp.cp_decode_plan(m["C"], ctx, device=dev)
-            cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
-                              sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
+            if pages is not None:
+                cp.cp_decode_attn_paged(dp, pages, cp.CP_DECODE_MLA, dq, shards, scale_pool=scales,
+                                        sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
+            else:
+                cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
+                                  sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
         e3.record(stream)
         if do_dec:
             cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
@@ -411,11 +427,14 @@ def run_ours(args, world, rank, local):
         dec_ach = d_bytes / (dec_avg / 1e3) / 1e9
         dec = {"metric": "decode KV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
                "kv": args.decode_kv,
+               "cache": (f"paged, {args.decode_paged}-row pages placed at random"
+                         if args.decode_paged else "one contiguous buffer per shard"),
                "ms_decode": dec_avg, "ms_merge": statistics.mean(mrg_ms),
                "merge_share": statistics.mean(mrg_ms) / (dec_avg + statistics.mean(mrg_ms)),
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
                             "frac": dec_ach / hbm,
-                            "traffic": profiled_traffic("decode_" + args.decode_kv, sum(ctx)),
+                            "traffic": (None if args.decode_paged else
+                                        profiled_traffic("decode_" + args.decode_kv, sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
     if not args.no_cpu:
@@ -467,6 +486,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--decode-kv", choices=["fp8", "bf16"], default="fp8",
                     help="decode cache type (the MLA workload has both)")
+    ap.add_argument("--decode-paged", type=int, default=0, metavar="PAGE_ROWS",
+                    help="decode from a paged pool with pages of this many rows (multiple of 64), "
+                         "placed at random; 0 = one contiguous buffer per shard")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()

@@ -22,13 +22,16 @@ from ._binding import (  # noqa: F401
     CP_ZIGZAG,
     CpError,
     DecodePlan,
+    PageTable,
     PrefillPlan,
     cp_decode_attn,
     cp_decode_attn_noalloc,
+    cp_decode_attn_paged,
     cp_decode_plan,
     cp_decode_workspace_size,
     cp_device_error_check,
     cp_kv_shard_pack,
+    cp_kv_shard_pack_paged,
     cp_lse_merge,
     cp_plan_size,
     cp_prefill_attn,

@@ -55,6 +55,10 @@ _SIGS = {
     "cp_lse_merge": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
     "cp_decode_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
                                     _vp, _vp]),
+    "cp_kv_shard_pack_paged": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
+                                    _vp]),
+    "cp_decode_attn_paged": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                  _i, _i, _i, _f, _vp, _vp, _vp, _sz, _vp]),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
 for _name, (_res, _args) in _SIGS.items():
@@ -268,6 +272,75 @@ def cp_kv_shard_pack(plan: DecodePlan, kv, kv_scale=None, shards=None, shard_sca
     _check(lib.cp_kv_shard_pack(_np_ptr(plan.host), _ptr(plan.dev), _dtype_code(kv), _ptr(kv),
                                 _ptr(kv_scale), row_elems, sarr, scarr, _stream(kv.device)))
     return shards, (shard_scales if kv_scale is not None else None)
+
+
+class PageTable:
+    """A paged decode cache's page table: int32 [C * R][max_pages] page ids
+    (row i of pair (shard r, request b) is row i % page_size of page
+    table[r * R + b][i // page_size]), kept as a host array and a device copy."""
+
+    def __init__(self, table, page_size: int, num_pages: int, device=None):
+        self.host = np.ascontiguousarray(np.asarray(table, dtype=np.int32))
+        assert self.host.ndim == 2
+        self.max_pages = int(self.host.shape[1])
+        self.page_size = int(page_size)
+        self.num_pages = int(num_pages)
+        self.dev = torch.from_numpy(self.host).to(device) if device is not None else None
+
+    @property
+    def pool_rows(self) -> int:
+        return self.num_pages * self.page_size
+
+
+def cp_kv_shard_pack_paged(plan: DecodePlan, pages: PageTable, kv, kv_scale=None, pool=None,
+                           scale_pool=None):
+    """Gathers a token-ordered cache kv [T, ...] into a paged pool
+    [pool_rows, ...].  Returns (pool, scale_pool)."""
+    _need_cuda(kv, kv_scale)
+    if kv.dtype == torch.float8_e4m3fn:
+        kv = kv.view(torch.uint8)
+    row_elems = int(np.prod(kv.shape[1:]))
+    if pool is None:
+        pool = torch.empty((pages.pool_rows, *kv.shape[1:]), dtype=kv.dtype, device=kv.device)
+    if kv_scale is not None and scale_pool is None:
+        scale_pool = torch.empty((pages.pool_rows,), dtype=torch.float32, device=kv.device)
+    _check(lib.cp_kv_shard_pack_paged(_np_ptr(plan.host), _ptr(plan.dev), _dtype_code(kv), _ptr(kv),
+                                      _ptr(kv_scale), row_elems, _ptr(pool),
+                                      _ptr(scale_pool) if kv_scale is not None else None,
+                                      _np_ptr(pages.host), _ptr(pages.dev), pages.max_pages,
+                                      pages.page_size, pages.num_pages, _stream(kv.device)))
+    return pool, (scale_pool if kv_scale is not None else None)
+
+
+def cp_decode_attn_paged(plan: DecodePlan, pages: PageTable, mode: int, q, k_pool, v_pool=None,
+                         scale_pool=None, sm_scale=None, o_part=None, lse_part=None, ws=None):
+    """cp_decode_attn over a paged pool (k_pool [pool_rows, 576] for MLA, or
+    k_pool / v_pool [pool_rows, Hkv, D] for GQA)."""
+    B, H, Dqk = q.shape
+    _need_cuda(q, k_pool)
+    kp = k_pool.view(torch.uint8) if k_pool.dtype == torch.float8_e4m3fn else k_pool
+    kv_dtype = _dtype_code(kp)
+    if mode == CP_DECODE_MLA:
+        Hkv, Dv = 1, 512
+    else:
+        Hkv, Dv = kp.shape[1], Dqk
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(Dqk)
+    C = plan.C
+    if o_part is None:
+        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+    need = cp_decode_workspace_size(plan, H, Dv)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.cp_decode_attn_paged(_np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q),
+                                    _ptr(kp), _ptr(v_pool), _ptr(scale_pool), _np_ptr(pages.host),
+                                    _ptr(pages.dev), pages.max_pages, pages.page_size,
+                                    pages.num_pages, H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part),
+                                    _ptr(lse_part), _ptr(ws), ws_bytes, _stream(q.device)))
+    return o_part, lse_part
 
 
 def cp_decode_workspace_size(plan: DecodePlan, H: int, Dv: int) -> int:

@@ -413,6 +413,102 @@ unsigned* device_status_ptr() {
 }
 }  // namespace cpattn
 
+// ====================================================================== decode helpers
+
+namespace {
+
+long long pair_rows_of_shard(const cp_plan_header& h, const int32_t* W, int r) {
+  long long rows = 0;
+  for (int b = 0; b < h.R; ++b) rows += W[h.off_rank + kPairWords * (r * h.R + b)];
+  return rows;
+}
+
+// Page table checks on its host copy: page size, pages per pair, page ids
+// in range and, when the call writes the pool, no page used twice.
+cp_status check_pages(const cp_plan_header& h, const int32_t* W, const int32_t* host_table,
+                      int max_pages, int page_size, int num_pages, bool distinct, RowMap* rm,
+                      const int32_t* dev_table) {
+  if (!host_table || !dev_table) return fail(CP_ERR_INVALID_ARG, "page table (host and device copies) is NULL");
+  if (!aligned16(dev_table)) return fail(CP_ERR_INVALID_ARG, "device page table is not 16-byte aligned");
+  if (page_size < 64 || page_size % 64) return fail(CP_ERR_UNSUPPORTED, "page_size=%d is not a positive multiple of 64", page_size);
+  if (max_pages < 1 || num_pages < 1) return fail(CP_ERR_INVALID_ARG, "max_pages=%d, num_pages=%d must be >= 1", max_pages, num_pages);
+  const long long pool_rows = (long long)num_pages * page_size;
+  if (pool_rows > 0x7FFFFF00LL) return fail(CP_ERR_UNSUPPORTED, "pool of %lld rows is too large", pool_rows);
+  std::vector<uint8_t> used(distinct ? (size_t)num_pages : 0, 0);
+  for (int pr = 0; pr < h.C * h.R; ++pr) {
+    const int rows = W[h.off_rank + kPairWords * pr];
+    const int need = (rows + page_size - 1) / page_size;
+    if (need > max_pages)
+      return fail(CP_ERR_INVALID_ARG, "pair %d needs %d pages > max_pages=%d", pr, need, max_pages);
+    for (int i = 0; i < need; ++i) {
+      const int pg = host_table[(size_t)pr * max_pages + i];
+      if (pg < 0 || pg >= num_pages)
+        return fail(CP_ERR_INVALID_ARG, "pair %d page %d: id %d outside [0, %d)", pr, i, pg, num_pages);
+      if (distinct) {
+        if (used[pg]) return fail(CP_ERR_INVALID_ARG, "page %d is used twice", pg);
+        used[pg] = 1;
+      }
+    }
+  }
+  rm->table = dev_table;
+  rm->max_pages = max_pages;
+  rm->page_size = page_size;
+  rm->pool_rows = pool_rows;
+  return ok();
+}
+
+cp_status check_decode_shapes(cp_decode_mode mode, cp_dtype kv_dtype, bool has_v, bool has_scale,
+                              int Hq, int Hkv, int Dqk, int Dv, float sm_scale) {
+  if (!(sm_scale > 0.f)) return fail(CP_ERR_INVALID_ARG, "sm_scale must be > 0");
+  if (mode != CP_DECODE_MLA && mode != CP_DECODE_GQA) return fail(CP_ERR_INVALID_ARG, "bad mode");
+  if (mode == CP_DECODE_MLA) {
+    if (Dqk != 576 || Dv != 512 || Hkv != 1) return fail(CP_ERR_UNSUPPORTED, "MLA needs Dqk=576, Dv=512, Hkv=1");
+    if (Hq < 1 || Hq > 64) return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d outside [1, 64]", Hq);
+    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP8_E4M3) return fail(CP_ERR_UNSUPPORTED, "MLA cache must be bf16 or fp8");
+    if (has_v) return fail(CP_ERR_INVALID_ARG, "MLA takes values from the latent: shard_v must be NULL");
+    if ((kv_dtype == CP_FP8_E4M3) != has_scale)
+      return fail(CP_ERR_INVALID_ARG, "shard_scale is required for fp8 and only for fp8");
+  } else {
+    if (Dqk != Dv || Dqk % 32 || Dqk < 32 || Dqk > 256) return fail(CP_ERR_UNSUPPORTED, "GQA needs Dqk == Dv, a multiple of 32 up to 256");
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(CP_ERR_INVALID_ARG, "Hq=%d must be a multiple of Hkv=%d", Hq, Hkv);
+    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP32) return fail(CP_ERR_UNSUPPORTED, "GQA cache must be bf16 or fp32");
+    if (!has_v || has_scale) return fail(CP_ERR_INVALID_ARG, "GQA needs shard_v and no shard_scale");
+  }
+  return ok();
+}
+
+// Workspace check, kernel dispatch and the split-pair merge shared by the
+// contiguous and the paged decode.
+cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mode mode,
+                     cp_dtype kv_dtype, const void* q, const ShardPtrs& K, const ShardPtrs& V,
+                     const ScalePtrs& S, const long long* shard_rows, const RowMap& rm, int Hq,
+                     int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
+                     void* ws, size_t ws_bytes, void* stream) {
+  size_t need = (size_t)h.n_parts * Hq * (Dv + 1) * sizeof(float);
+  if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (need && !aligned16(ws)) return fail(CP_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  float* ws_o = (float*)ws;
+  float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hq * Dv : nullptr;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool mla = mode == CP_DECODE_MLA;
+  cudaError_t e =
+      mla && kv_dtype == CP_FP8_E4M3
+          ? launch_decode_mla_fp8((const int32_t*)dev_plan, h, q, K, S, shard_rows, rm, Hq, sm_scale,
+                                  o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+      : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, q, K, shard_rows, rm, Hq, sm_scale,
+                                   o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+            : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk,
+                                 Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+  if (h.n_split) {
+    e = launch_decode_fixup((const int32_t*)dev_plan, h, Hq, Dv, ws_o, ws_lse, o_part, lse_part, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode split merge kernel");
+  }
+  return ok();
+}
+
+}  // namespace
+
 // ====================================================================== C ABI
 
 extern "C" {
@@ -551,8 +647,10 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
     }
   }
   if (h.T == 0) return ok();
+  RowMap rm;
+  memset(&rm, 0, sizeof(rm));
   cudaError_t e = launch_kv_pack((const int32_t*)dev_plan, h, (int)elem_size(dtype), kv, kv_scale,
-                                 row_elems, dst, dsc, kv_scale != nullptr, (cudaStream_t)stream);
+                                 row_elems, dst, dsc, kv_scale != nullptr, rm, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv pack kernel");
   return ok();
 }
@@ -577,25 +675,9 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   if (!dev_plan || !q || !shard_k || !o_part || !lse_part) return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
   if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o_part) || !aligned16(lse_part))
     return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
-  if (!(sm_scale > 0.f)) return fail(CP_ERR_INVALID_ARG, "sm_scale must be > 0");
-  const bool mla = mode == CP_DECODE_MLA;
-  if (mode != CP_DECODE_MLA && mode != CP_DECODE_GQA) return fail(CP_ERR_INVALID_ARG, "bad mode");
-  if (mla) {
-    if (Dqk != 576 || Dv != 512 || Hkv != 1) return fail(CP_ERR_UNSUPPORTED, "MLA needs Dqk=576, Dv=512, Hkv=1");
-    if (Hq < 1 || Hq > 64) return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d outside [1, 64]", Hq);
-    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP8_E4M3) return fail(CP_ERR_UNSUPPORTED, "MLA cache must be bf16 or fp8");
-    if (shard_v) return fail(CP_ERR_INVALID_ARG, "MLA takes values from the latent: shard_v must be NULL");
-    if ((kv_dtype == CP_FP8_E4M3) != (shard_scale != nullptr))
-      return fail(CP_ERR_INVALID_ARG, "shard_scale is required for fp8 and only for fp8");
-  } else {
-    if (Dqk != Dv || Dqk % 32 || Dqk < 32 || Dqk > 256) return fail(CP_ERR_UNSUPPORTED, "GQA needs Dqk == Dv, a multiple of 32 up to 256");
-    if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(CP_ERR_INVALID_ARG, "Hq=%d must be a multiple of Hkv=%d", Hq, Hkv);
-    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP32) return fail(CP_ERR_UNSUPPORTED, "GQA cache must be bf16 or fp32");
-    if (!shard_v || shard_scale) return fail(CP_ERR_INVALID_ARG, "GQA needs shard_v and no shard_scale");
-  }
-  size_t need = (size_t)h.n_parts * Hq * (Dv + 1) * sizeof(float);
-  if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
-  if (need && !aligned16(ws)) return fail(CP_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  st = check_decode_shapes(mode, kv_dtype, shard_v != nullptr, shard_scale != nullptr, Hq, Hkv, Dqk,
+                           Dv, sm_scale);
+  if (st != CP_OK) return st;
   ShardPtrs K, V;
   ScalePtrs S;
   memset(&K, 0, sizeof(K));
@@ -604,8 +686,7 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   const int32_t* W = (const int32_t*)host_plan;
   long long shard_rows[CP_MAX_SHARDS] = {0};
   for (int r = 0; r < h.C; ++r) {
-    long long rows_r = 0;
-    for (int b = 0; b < h.R; ++b) rows_r += W[h.off_rank + kPairWords * (r * h.R + b)];
+    const long long rows_r = pair_rows_of_shard(h, W, r);
     shard_rows[r] = rows_r;
     K.p[r] = shard_k[r];
     if (rows_r > 0 && (!shard_k[r] || !aligned16(shard_k[r]))) return fail(CP_ERR_INVALID_ARG, "shard_k[%d] NULL or misaligned", r);
@@ -618,22 +699,81 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
       if (rows_r > 0 && !shard_scale[r]) return fail(CP_ERR_INVALID_ARG, "shard_scale[%d] is NULL", r);
     }
   }
-  float* ws_o = (float*)ws;
-  float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hq * Dv : nullptr;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e =
-      mla && kv_dtype == CP_FP8_E4M3
-          ? launch_decode_mla_fp8((const int32_t*)dev_plan, h, q, K, S, shard_rows, Hq, sm_scale,
-                                  o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
-      : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, q, K, shard_rows, Hq, sm_scale,
-                                   o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
-          : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, Hq, Hkv, Dqk,
-                               Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
-  if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-  if (h.n_split) {
-    e = launch_decode_fixup((const int32_t*)dev_plan, h, Hq, Dv, ws_o, ws_lse, o_part, lse_part, s);
-    if (e != cudaSuccess) return cuda_fail(e, "decode split merge kernel");
+  RowMap rm;
+  memset(&rm, 0, sizeof(rm));
+  return run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv,
+                    sm_scale, o_part, lse_part, ws, ws_bytes, stream);
+}
+
+cp_status cp_decode_attn_paged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                               cp_dtype kv_dtype, const void* q, const void* k_pool,
+                               const void* v_pool, const float* scale_pool,
+                               const int32_t* host_page_table, const int32_t* dev_page_table,
+                               int max_pages, int page_size, int num_pages, int Hq, int Hkv,
+                               int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
+                               void* ws, size_t ws_bytes, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (!dev_plan || !q || !k_pool || !o_part || !lse_part) return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o_part) || !aligned16(lse_part) ||
+      !aligned16(k_pool) || (v_pool && !aligned16(v_pool)))
+    return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
+  st = check_decode_shapes(mode, kv_dtype, v_pool != nullptr, scale_pool != nullptr, Hq, Hkv, Dqk,
+                           Dv, sm_scale);
+  if (st != CP_OK) return st;
+  RowMap rm;
+  st = check_pages(h, (const int32_t*)host_plan, host_page_table, max_pages, page_size, num_pages,
+                   false, &rm, dev_page_table);
+  if (st != CP_OK) return st;
+  ShardPtrs K, V;
+  ScalePtrs S;
+  long long shard_rows[CP_MAX_SHARDS] = {0};
+  for (int r = 0; r < CP_MAX_SHARDS; ++r) {  // every shard reads the one pool
+    K.p[r] = k_pool;
+    V.p[r] = v_pool;
+    S.p[r] = scale_pool;
+    if (r < h.C) shard_rows[r] = pair_rows_of_shard(h, (const int32_t*)host_plan, r);
   }
+  return run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv,
+                    sm_scale, o_part, lse_part, ws, ws_bytes, stream);
+}
+
+cp_status cp_kv_shard_pack_paged(const void* host_plan, const void* dev_plan, cp_dtype dtype,
+                                 const void* kv, const float* kv_scale, int row_elems, void* pool,
+                                 float* scale_pool, const int32_t* host_page_table,
+                                 const int32_t* dev_page_table, int max_pages, int page_size,
+                                 int num_pages, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (!dev_plan || !kv || !pool) return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (dtype != CP_BF16 && dtype != CP_FP32 && dtype != CP_FP8_E4M3) return fail(CP_ERR_INVALID_ARG, "bad dtype");
+  if (row_elems < 1) return fail(CP_ERR_INVALID_ARG, "row_elems=%d < 1", row_elems);
+  const size_t rb = (size_t)row_elems * elem_size(dtype);
+  if (rb % 16) return fail(CP_ERR_UNSUPPORTED, "row bytes %zu not a multiple of 16", rb);
+  if ((kv_scale == nullptr) != (scale_pool == nullptr))
+    return fail(CP_ERR_INVALID_ARG, "kv_scale and scale_pool must both be given or both NULL");
+  if (!aligned16(kv) || !aligned16(dev_plan) || !aligned16(pool))
+    return fail(CP_ERR_INVALID_ARG, "kv/pool/dev_plan not 16-byte aligned");
+  RowMap rm;
+  st = check_pages(h, (const int32_t*)host_plan, host_page_table, max_pages, page_size, num_pages,
+                   true, &rm, dev_page_table);
+  if (st != CP_OK) return st;
+  MutShardPtrs dst;
+  MutScalePtrs dsc;
+  for (int r = 0; r < CP_MAX_SHARDS; ++r) {
+    dst.p[r] = pool;
+    dsc.p[r] = scale_pool;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (h.T > 0) {
+    cudaError_t e = launch_kv_pack((const int32_t*)dev_plan, h, (int)elem_size(dtype), kv, kv_scale,
+                                   row_elems, dst, dsc, kv_scale != nullptr, rm, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kv pack kernel");
+  }
+  cudaError_t e = launch_page_tail_zero((const int32_t*)dev_plan, h, rb, pool, scale_pool, rm, s);
+  if (e != cudaSuccess) return cuda_fail(e, "page tail kernel");
   return ok();
 }
 

@@ -73,6 +73,7 @@ struct Params {
   const __nv_bfloat16* q;
   ShardPtrs k;  // code arrays (for the L2 prefetch; the tiles come through the tensor maps)
   ScalePtrs sc;
+  RowMap rm;    // paged cache: 64-row boxes of a pool, rows through the page table
   int H;
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
@@ -84,7 +85,8 @@ struct Params {
 };
 
 // Tensor maps of the shards' code arrays ([rows, 576] bytes): dims [0, 512)
-// in 128-byte boxes with a 128-byte swizzle, dims [512, 576) with a 64-byte one.
+// in 128-byte boxes with a 128-byte swizzle, dims [512, 576) with a 64-byte
+// one; 128 rows a box, or for a paged cache one pool map with 64-row boxes.
 struct CodeMaps {
   CUtensorMap body[CP_MAX_SHARDS];
   CUtensorMap rope[CP_MAX_SHARDS];
@@ -158,7 +160,8 @@ __device__ void report_timeout(unsigned* status, unsigned site, volatile int* ab
 // One work item of this CTA as every role sees it.
 struct Item {
   int r, b, nrows, ntiles;
-  long long row0;  // first shard row
+  int pair, row_begin, pair_rows;  // the pair, the item's first row in it, the pair's rows
+  long long row0;  // first shard row (contiguous caches)
   float* out_o;
   float* out_l;
 };
@@ -171,6 +174,9 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   it.nrows = wd.row_end - wd.row_begin;
   it.ntiles = (it.nrows + kRows - 1) / kRows;
   it.row0 = (long long)pd.row_off + wd.row_begin;
+  it.pair = wd.pair;
+  it.row_begin = wd.row_begin;
+  it.pair_rows = pd.rows;
   it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
                          : p.ws_o + (long long)wd.part * p.H * kDv;
   it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
@@ -232,9 +238,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int wi = w0; wi < w1 && ok; ++wi) {
         const Item it = read_item(p, wi);
         const uint8_t* codes = static_cast<const uint8_t*>(p.k.p[it.r]);
-        auto prefetch = [&](int jt) {  // tile jt of the item into L2 (rows are contiguous)
-          const int rows = min(kRows, it.nrows - jt * kRows);
-          prefetch_l2_bulk(codes + (it.row0 + (long long)jt * kRows) * kDqk, (uint32_t)rows * kDqk);
+        // Cache row of the item's row i; past the pair's rows, a row past the
+        // pool, where the copy reads zeros.
+        auto cache_row = [&](int i) -> long long {
+          const int ip = it.row_begin + i;
+          if (!p.rm.table) return it.row0 + i;
+          return ip < it.pair_rows ? map_row(p.rm, it.pair, 0, ip) : p.rm.pool_rows;
+        };
+        auto prefetch = [&](int jt) {  // tile jt of the item into L2, 64 contiguous rows at a time
+          for (int hh = 0; hh < 2; ++hh) {
+            const int i = jt * kRows + 64 * hh;
+            const int rows = min(64, it.nrows - i);
+            if (rows > 0)
+              prefetch_l2_bulk(codes + cache_row(i) * kDqk, (uint32_t)rows * kDqk);
+          }
         };
         for (int jt = 0; jt < kPrefetchAhead && jt < it.ntiles; ++jt) prefetch(jt);
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
@@ -242,6 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t stage = sbase + s * kStageBytes;
           const int y = (int)(it.row0 + (long long)j * kRows);
           if (j + kPrefetchAhead < it.ntiles) prefetch(j + kPrefetchAhead);
+          // paged: the pool rows of the tile's two 64-row halves, looked up once
+          const long long yh[2] = {p.rm.table ? cache_row(j * kRows) : 0,
+                                   p.rm.table ? cache_row(j * kRows + 64) : 0};
           // the stage is free once the P.V of its previous tile (g - 2) has completed
           if (g >= 2 && !mbar_wait(smem_u32(&bar_done[s]), ((g >> 1) & 1) ^ 1, p.wait_ns,
                                    &abort_flag)) {
@@ -251,12 +271,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int q = 0; q < 5; ++q) {
             const uint32_t full = smem_u32(&bar_full[s][q]);
-            if (q < 4) {
-              mbar_expect_tx(full, kChunkBytes);
-              tma_load_2d(stage + q * kChunkBytes, &maps.body[it.r], 128 * q, y, full);
-            } else {
-              mbar_expect_tx(full, kRows * 64);
-              tma_load_2d(stage + kRopeOff, &maps.rope[it.r], 4 * 128, y, full);
+            const uint32_t dst = stage + (q < 4 ? q * kChunkBytes : kRopeOff);
+            const int x = 128 * q, row_bytes = q < 4 ? 128 : 64;
+            const CUtensorMap* map = q < 4 ? &maps.body[it.r] : &maps.rope[it.r];
+            mbar_expect_tx(full, kRows * row_bytes);
+            if (!p.rm.table) {
+              tma_load_2d(dst, map, x, y, full);
+            } else {  // two 64-row halves, each inside one page
+              for (int hh = 0; hh < 2; ++hh)
+                tma_load_2d(dst + hh * 64 * row_bytes, &(q < 4 ? maps.body : maps.rope)[0], x,
+                            (int)yh[hh], full);
             }
             last_g[s] = g;
             last_n[s] = q + 1;
@@ -451,7 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < it.ntiles; ++j, ++g) {
         const int row = j * kRows + t;
         const bool valid = row < it.nrows;
-        const float scale = valid ? __ldg(srow + row) : 0.f;
+        const float scale =
+            !valid ? 0.f
+                   : p.rm.table ? __ldg(p.sc.p[0] + map_row(p.rm, it.pair, 0, it.row_begin + row))
+                                : __ldg(srow + row);
         const int b = g & 1;
         // The eight warps leave together: one that gave up meets the others at this vote.
         const bool got = __all_sync(
@@ -637,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                   const ShardPtrs& k, const ScalePtrs& sc,
-                                  const long long* shard_rows, int H, float sm_scale,
+                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                   unsigned long long wait_ns, cudaStream_t s) {
   Params p;
@@ -649,6 +676,7 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = k;
   p.sc = sc;
+  p.rm = rm;
   p.H = H;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
@@ -660,12 +688,19 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
   p.wait_ns = wait_ns;
   CodeMaps maps;
   memset(&maps, 0, sizeof(maps));
-  for (int r = 0; r < h.C; ++r) {
-    if (shard_rows[r] == 0) continue;
-    const uint64_t rows = (uint64_t)shard_rows[r];
-    if (!encode_tensor_map_u8_2d(&maps.body[r], k.p[r], kDqk, rows, kDqk, 128, kRows, true) ||
-        !encode_tensor_map_u8_2d(&maps.rope[r], k.p[r], kDqk, rows, kDqk, 64, kRows, false))
+  if (rm.table) {
+    const uint64_t rows = (uint64_t)rm.pool_rows;
+    if (!encode_tensor_map_u8_2d(&maps.body[0], k.p[0], kDqk, rows, kDqk, 128, 64, true) ||
+        !encode_tensor_map_u8_2d(&maps.rope[0], k.p[0], kDqk, rows, kDqk, 64, 64, false))
       return cudaErrorInvalidValue;
+  } else {
+    for (int r = 0; r < h.C; ++r) {
+      if (shard_rows[r] == 0) continue;
+      const uint64_t rows = (uint64_t)shard_rows[r];
+      if (!encode_tensor_map_u8_2d(&maps.body[r], k.p[r], kDqk, rows, kDqk, 128, kRows, true) ||
+          !encode_tensor_map_u8_2d(&maps.rope[r], k.p[r], kDqk, rows, kDqk, 64, kRows, false))
+        return cudaErrorInvalidValue;
+    }
   }
   cudaError_t e = cudaFuncSetAttribute(decode_mla_fp8_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

@@ -59,6 +59,7 @@ struct Params {
   int B, off_pair, off_worker, off_work;
   const __nv_bfloat16* q;
   ShardPtrs k;
+  RowMap rm;  // paged cache: 64-row boxes of a pool, rows through the page table
   int H;
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
@@ -69,7 +70,8 @@ struct Params {
   unsigned long long wait_ns;
 };
 
-// Tensor maps of the shards' bf16 caches ([rows, 576], box 64 x 128, 128-byte swizzle).
+// Tensor maps of the shards' bf16 caches ([rows, 576], box 64 dims x 128 rows,
+// 128-byte swizzle); a paged cache has one map of the pool with 64-row boxes.
 struct ShardMaps {
   CUtensorMap m[CP_MAX_SHARDS];
 };
@@ -189,6 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued_tiles = 0;  // tiles whose copies were issued (for the drain)
         for (int j = 0; j < ntiles && ok; ++j) {
           const int g = g0 + j;
+          // paged: the pool rows of the tile's two 64-row halves (each inside one page);
+          // past the pair's rows the coordinate is past the pool and the copy reads zeros
+          long long yh[2] = {0, 0};
+          if (p.rm.table) {
+            for (int hh = 0; hh < 2; ++hh) {
+              const int i0 = wd.row_begin + j * kRows + 64 * hh;
+              yh[hh] = i0 < pd.rows ? map_row(p.rm, wd.pair, 0, i0) : p.rm.pool_rows;
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 5; ++q) {
             // group q is free once the previous tile's P.V M-block q (or, for the
@@ -203,8 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
             for (int cc = 0; cc < group_chunks(q); ++cc) {
               const int c = 2 * q + cc;
-              tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
-                          (int)(row0 + (long long)j * kRows), full);
+              if (!p.rm.table) {
+                tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
+                            (int)(row0 + (long long)j * kRows), full);
+              } else {
+                for (int hh = 0; hh < 2; ++hh)
+                  tma_load_2d(smem_u32(sTile + c * kChunkBytes + hh * 64 * 128), &maps.m[0],
+                              c * 64, (int)yh[hh], full);
+              }
             }
           }
           if (!ok) break;
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,
                                  const void* q, const ShardPtrs& k,
-                                 const long long* shard_rows, int H, float sm_scale,
+                                 const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  unsigned long long wait_ns, cudaStream_t s) {
   Params p;
@@ -417,6 +434,7 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.off_work = h.off_seg;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = k;
+  p.rm = rm;
   p.H = H;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
@@ -428,13 +446,21 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.wait_ns = wait_ns;
   ShardMaps local;
   memset(&local, 0, sizeof(local));
-  for (int r = 0; r < h.C; ++r) {
-    if (shard_rows[r] == 0) continue;
-    const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)shard_rows[r]};
+  if (rm.table) {
+    const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)rm.pool_rows};
     const uint64_t strides[1] = {(uint64_t)kDqk * 2};
-    const uint32_t box[2] = {64, (uint32_t)kRows};
-    if (!encode_tensor_map_bf16(&local.m[r], k.p[r], 2, dims, strides, box))
+    const uint32_t box[2] = {64, 64};
+    if (!encode_tensor_map_bf16(&local.m[0], k.p[0], 2, dims, strides, box))
       return cudaErrorInvalidValue;
+  } else {
+    for (int r = 0; r < h.C; ++r) {
+      if (shard_rows[r] == 0) continue;
+      const uint64_t dims[2] = {(uint64_t)kDqk, (uint64_t)shard_rows[r]};
+      const uint64_t strides[1] = {(uint64_t)kDqk * 2};
+      const uint32_t box[2] = {64, (uint32_t)kRows};
+      if (!encode_tensor_map_bf16(&local.m[r], k.p[r], 2, dims, strides, box))
+        return cudaErrorInvalidValue;
+    }
   }
   auto kern = decode_mla_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

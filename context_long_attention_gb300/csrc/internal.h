@@ -34,6 +34,25 @@ struct MutScalePtrs {
   float* p[CP_MAX_SHARDS];
 };
 
+// Where the rows of a (shard r, request b) decode pair live.  Contiguous:
+// rows [row_off, row_off + rows) of shard r's own buffer.  Paged: row i is
+// row i % page_size of page table[pair][i / page_size] of one pool shared by
+// all shards (every shard pointer is then the pool).  page_size is a multiple
+// of 64, so a 64-row half of a 128-row decode tile never crosses a page.
+struct RowMap {
+  const int32_t* table;  // device [C * B][max_pages] page ids, or nullptr
+  int max_pages;
+  int page_size;
+  long long pool_rows;   // num_pages * page_size (paged)
+};
+#ifdef __CUDACC__
+__device__ __forceinline__ long long map_row(const RowMap& m, int pair, long long row_off, int i) {
+  if (!m.table) return row_off + i;
+  const int page = __ldg(m.table + (long long)pair * m.max_pages + i / m.page_size);
+  return (long long)page * m.page_size + i % m.page_size;
+}
+#endif
+
 // Returns the device address of this device's status words (set up once per device).
 unsigned* device_status_ptr();
 
@@ -46,7 +65,12 @@ cudaError_t launch_plan_maps(const int32_t* dev_plan, int n_seg, int off_seg, in
 cudaError_t launch_kv_pack(const int32_t* dev_plan, const cp_plan_header& h, int elem_bytes,
                            const void* kv, const float* kv_scale, int row_elems,
                            const MutShardPtrs& dst, const MutScalePtrs& dst_scale, bool has_scale,
-                           cudaStream_t s);
+                           const RowMap& rm, cudaStream_t s);
+// Paged caches: zero the rows past each pair's last row on its last page (they
+// enter the decode products with zero weight, and must hold finite values).
+cudaError_t launch_page_tail_zero(const int32_t* dev_plan, const cp_plan_header& h,
+                                  size_t row_bytes, void* pool, float* scale_pool,
+                                  const RowMap& rm, cudaStream_t s);
 cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
                              const float* lse_part, void* o, bool o_bf16, float* lse,
                              cudaStream_t s);
@@ -74,14 +98,14 @@ bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, ui
 // ---- MLA decode over an FP8 cache on FP8 tensor-core products (decode_mla_fp8.cu)
 cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                   const ShardPtrs& k, const ScalePtrs& sc,
-                                  const long long* shard_rows, int H, float sm_scale,
+                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                   unsigned long long wait_ns, cudaStream_t s);
 
 // ---- tensor-core MLA decode over a bf16 cache (decode_mla_tc.cu)
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,
                                  const void* q, const ShardPtrs& k,
-                                 const long long* shard_rows, int H, float sm_scale,
+                                 const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  unsigned long long wait_ns, cudaStream_t s);
 unsigned long long wait_limit_ns();
@@ -93,7 +117,8 @@ cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h
                                 float sm_scale, void* o, float* lse, cudaStream_t s);
 cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
-                               const ShardPtrs& v, const ScalePtrs& sc, int Hq, int Hkv, int Dqk,
+                               const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,
+                               int Hkv, int Dqk,
                                int Dv, float sm_scale, float* o_part, float* lse_part,
                                float* ws_o, float* ws_lse, cudaStream_t s);
 

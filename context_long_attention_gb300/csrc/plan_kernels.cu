@@ -3,7 +3,8 @@
 // * plan_map_kernel: per-query arrays of a prefill plan (flattened index,
 //   position, request) from its segments — zigzag blocks or interleave runs
 //   ("How GPUs Share a Long Context During LLM Inference", §2.3-2.4).
-// * kv_pack_kernel: token p of a request -> shard p mod C, row p / C (§3.1).
+// * kv_pack_kernel: token p of a request -> shard p mod C, row p / C (§3.1),
+//   into the shard's buffer or, paged, into the pool row its page table gives.
 // * lse_merge_kernel / decode_fixup_kernel: O = sum_p w_p O_p / sum_p w_p
 //   with w_p = exp(LSE_p - max LSE) (§3.3; "DeepSeek-V4 Attention Inference
 //   Systems" §5), one warp per (row, head), 128-bit loads.
@@ -33,7 +34,8 @@ __global__ void plan_map_kernel(int32_t* __restrict__ plan, int off_seg, int off
 __global__ void kv_pack_kernel(const int32_t* __restrict__ plan, int C, int B, int T,
                                int off_pair, int off_req, const uint4* __restrict__ kv,
                                const float* __restrict__ kv_scale, int row_vec,
-                               MutShardPtrs dst, MutScalePtrs dst_scale, int has_scale) {
+                               MutShardPtrs dst, MutScalePtrs dst_scale, int has_scale,
+                               RowMap rm) {
   const int warps = blockDim.x >> 5;
   const long long t = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -48,11 +50,26 @@ __global__ void kv_pack_kernel(const int32_t* __restrict__ plan, int C, int B, i
   const int p = (int)(t - req[2 * b + 1]);
   const int r = p % C;
   const cp_pair_desc* pair = reinterpret_cast<const cp_pair_desc*>(plan + off_pair);
-  const long long row = (long long)pair[r * B + b].row_off + p / C;
+  const long long row = map_row(rm, r * B + b, pair[r * B + b].row_off, p / C);
   const uint4* src = kv + t * row_vec;
   uint4* out = static_cast<uint4*>(dst.p[r]) + row * row_vec;
   for (int c = lane; c < row_vec; c += 32) out[c] = src[c];
   if (has_scale && lane == 0) dst_scale.p[r][row] = kv_scale[t];
+}
+
+// Paged caches: one block per pair zeroes rows [rows, pages x page_size) of
+// the pair's last page (and their scales).
+__global__ void page_tail_zero_kernel(const int32_t* __restrict__ plan, int off_pair,
+                                      int row_vec, uint4* __restrict__ pool,
+                                      float* __restrict__ scale_pool, RowMap rm) {
+  const cp_pair_desc pd = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[blockIdx.x];
+  if (pd.rows == 0) return;
+  const int end = (pd.rows + rm.page_size - 1) / rm.page_size * rm.page_size;
+  for (int i = pd.rows + threadIdx.y; i < end; i += blockDim.y) {
+    const long long row = map_row(rm, blockIdx.x, 0, i);
+    for (int c = threadIdx.x; c < row_vec; c += blockDim.x) pool[row * row_vec + c] = make_uint4(0, 0, 0, 0);
+    if (scale_pool && threadIdx.x == 0) scale_pool[row] = 0.f;
+  }
 }
 
 // Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride.
@@ -145,14 +162,24 @@ cudaError_t launch_plan_maps(const int32_t* dev_plan, int n_seg, int off_seg, in
 cudaError_t launch_kv_pack(const int32_t* dev_plan, const cp_plan_header& h, int elem_bytes,
                            const void* kv, const float* kv_scale, int row_elems,
                            const MutShardPtrs& dst, const MutScalePtrs& dst_scale, bool has_scale,
-                           cudaStream_t s) {
+                           const RowMap& rm, cudaStream_t s) {
   const int row_vec = row_elems * elem_bytes / 16;
   const int warps = 8;
   const long long blocks = ((long long)h.T + warps - 1) / warps;
   kv_pack_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(dev_plan, h.C, h.R, h.T, h.off_rank,
                                                          h.off_tiles, static_cast<const uint4*>(kv),
                                                          kv_scale, row_vec, dst, dst_scale,
-                                                         has_scale ? 1 : 0);
+                                                         has_scale ? 1 : 0, rm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_page_tail_zero(const int32_t* dev_plan, const cp_plan_header& h,
+                                  size_t row_bytes, void* pool, float* scale_pool,
+                                  const RowMap& rm, cudaStream_t s) {
+  const int pairs = h.C * h.R;
+  if (pairs == 0) return cudaSuccess;
+  page_tail_zero_kernel<<<pairs, dim3(32, 8), 0, s>>>(dev_plan, h.off_rank, (int)(row_bytes / 16),
+                                                     static_cast<uint4*>(pool), scale_pool, rm);
   return cudaGetLastError();
 }
 

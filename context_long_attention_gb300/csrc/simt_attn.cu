@@ -94,7 +94,8 @@ __global__ void prefill_simt_kernel(const int32_t* __restrict__ plan, int off_re
 template <typename T, int ND>
 __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                                        int off_worker, int off_work, const T* __restrict__ q,
-                                       ShardPtrs kp, ShardPtrs vp, int Hq, int Hkv, float sm_scale,
+                                       ShardPtrs kp, ShardPtrs vp, RowMap rm, int Hq, int Hkv,
+                                       float sm_scale,
                                        float* __restrict__ o_part, float* __restrict__ lse_part,
                                        float* __restrict__ ws_o, float* __restrict__ ws_lse) {
   constexpr int D = ND * 32;
@@ -116,7 +117,7 @@ __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, 
     const T* vb = static_cast<const T*>(vp.p[r]);
     RowState<ND> st;
     for (int row = wd.row_begin; row < wd.row_end; ++row) {
-      const long long kr = (((long long)pd.row_off + row) * Hkv + g) * D + lane;
+      const long long kr = (map_row(rm, wd.pair, pd.row_off, row) * Hkv + g) * D + lane;
       float part = 0.f, vv[ND];
 #pragma unroll
       for (int e = 0; e < ND; ++e) {
@@ -157,13 +158,14 @@ cudaError_t prefill_simt_t(const int32_t* plan, const cp_plan_header& h, int ran
 
 template <typename T, int ND>
 cudaError_t decode_gqa_t(const int32_t* plan, const cp_plan_header& h, const void* q,
-                         const ShardPtrs& k, const ShardPtrs& v, int Hq, int Hkv, float sm_scale,
+                         const ShardPtrs& k, const ShardPtrs& v, const RowMap& rm, int Hq, int Hkv,
+                         float sm_scale,
                          float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                          cudaStream_t s) {
   const int warps = 4;
   dim3 grid(h.n_tiles, (Hq + warps - 1) / warps);
   decode_gqa_simt_kernel<T, ND><<<grid, warps * 32, 0, s>>>(
-      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, Hq, Hkv,
+      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, rm, Hq, Hkv,
       sm_scale, o_part, lse_part, ws_o, ws_lse);
   return cudaGetLastError();
 }
@@ -193,18 +195,18 @@ cudaError_t launch_prefill_simt(const int32_t* plan, const cp_plan_header& h, in
 
 cudaError_t launch_decode_simt(const int32_t* plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
-                               const ShardPtrs& v, const ScalePtrs& sc, int Hq, int Hkv, int Dqk,
-                               int Dv, float sm_scale, float* o_part, float* lse_part,
+                               const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,
+                               int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
                                float* ws_o, float* ws_lse, cudaStream_t s) {
   (void)sc;
   (void)Dv;
 #define CP_GQA_CASE(ND)                                                                         \
   case ND:                                                                                      \
     return kv_dtype == CP_BF16                                                                  \
-               ? decode_gqa_t<__nv_bfloat16, ND>(plan, h, q, k, v, Hq, Hkv, sm_scale, o_part,   \
-                                                 lse_part, ws_o, ws_lse, s)                     \
-               : decode_gqa_t<float, ND>(plan, h, q, k, v, Hq, Hkv, sm_scale, o_part, lse_part, \
-                                         ws_o, ws_lse, s);
+               ? decode_gqa_t<__nv_bfloat16, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale,       \
+                                                 o_part, lse_part, ws_o, ws_lse, s)             \
+               : decode_gqa_t<float, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale, o_part,       \
+                                         lse_part, ws_o, ws_lse, s);
   switch (Dqk / 32) {
     CP_GQA_CASE(1)
     CP_GQA_CASE(2)

@@ -290,6 +290,48 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
                          void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Paged token-sharded decode cache ("How GPUs Share a Long Context During LLM
+ * Inference" §3.1: a slot maps to (GPU, row); serving caches keep those rows
+ * in fixed-size pages, "DeepSeek-V4 Attention Inference Systems" §9.2).
+ *
+ * The rows of pair (shard r, request b) = pair index r * R + b of a decode
+ * plan are the shard's rows of that request in order (row i = token
+ * p = i * C + r).  Row i lives at row i % page_size of page
+ * page_table[pair][i / page_size] of one pool shared by all shards:
+ *   pool row = page_id * page_size + i % page_size,
+ *   pool: [num_pages * page_size, row] with row = 576 (MLA) or Hkv x D (GQA).
+ * page_table: int32 [C * R][max_pages], a host copy (validated: page ids in
+ *   [0, num_pages), ceil(rows / page_size) <= max_pages) and a device copy
+ *   (read by the kernels; must hold the same ids).  page_size is a multiple
+ *   of 64.  Entries past a pair's pages are ignored.
+ * Rows past a pair's last row on its last page enter the decode products
+ * with zero weight and must hold finite values; cp_kv_shard_pack_paged
+ * zeroes them.
+ * ------------------------------------------------------------------------- */
+
+/* cp_kv_shard_pack_paged — cp_kv_shard_pack into a paged pool: token p of
+ * request b goes to shard p mod C, row p / C, at the pool row its page table
+ * gives; then the tail rows of every pair's last page are zeroed.  No page
+ * may be used by two pairs.  pool / scale_pool (FP8: one fp32 scale per pool
+ * row, or NULL with kv_scale NULL) are caller-owned device buffers. */
+cp_status cp_kv_shard_pack_paged(const void* host_plan, const void* dev_plan, cp_dtype dtype,
+                                 const void* kv, const float* kv_scale, int row_elems, void* pool,
+                                 float* scale_pool, const int32_t* host_page_table,
+                                 const int32_t* dev_page_table, int max_pages, int page_size,
+                                 int num_pages, void* stream);
+
+/* cp_decode_attn_paged — cp_decode_attn over a paged pool: the same partials
+ * (O_r, LSE_r), with shard_k / shard_v / shard_scale replaced by k_pool,
+ * v_pool (GQA; NULL for MLA) and scale_pool (FP8; NULL otherwise). */
+cp_status cp_decode_attn_paged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                               cp_dtype kv_dtype, const void* q, const void* k_pool,
+                               const void* v_pool, const float* scale_pool,
+                               const int32_t* host_page_table, const int32_t* dev_page_table,
+                               int max_pages, int page_size, int num_pages, int Hq, int Hkv,
+                               int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * cp_lse_merge — exact combine of P partial results ([CTX] §3.3; [V4] §5).
  *
  * Per (n, h): g = max_p LSE_p; w_p = exp(LSE_p - g) (0 for LSE_p = -inf);

@@ -189,6 +189,28 @@ def decode_shard_map(ctx_len: int, C: int) -> tuple[list[int], list[int]]:
     return shard, row
 
 
+def paged_token_rows(ctx_len, C: int, page_table, page_size: int) -> list[tuple[int, int, int]]:
+    """Pool row of every cached token when the shards' rows are kept in pages.
+
+    [CTX] §3.1: token p of a request lives on shard p mod C at row p // C;
+    serving caches keep a shard's rows in fixed-size pages ([V4] §9.2).  Here
+    row i of the pair (shard r, request b) — pair index r * B + b — sits at
+    row i mod page_size of page page_table[pair][i // page_size], so its
+    pool row is page * page_size + i mod page_size.
+    Returns (request, token position, pool row) for every token.
+    """
+    B = len(ctx_len)
+    out = []
+    for b, L in enumerate(ctx_len):
+        shard, row = decode_shard_map(int(L), C)
+        for p in range(int(L)):
+            pair = shard[p] * B + b
+            i = row[p]
+            page = int(page_table[pair][i // page_size])
+            out.append((b, p, page * page_size + i % page_size))
+    return out
+
+
 # --------------------------------------------------------------------------
 # FP8 E4M3 decoding, bit by bit from the OCP 8-bit floating point format.
 # --------------------------------------------------------------------------

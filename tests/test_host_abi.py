@@ -195,3 +195,33 @@ def test_argument_validation(cp):
     assert st == -1 and b"magic" in lib.cp_last_error()
     assert lib.cp_lse_merge(0, 1, 1, 4, None, None, None, 0, None, None) == -1
     assert lib.cp_lse_merge(2, 1, 1, 6, None, None, None, 0, None, None) == -1
+
+
+def test_paged_argument_validation(cp):
+    """Page tables are checked on their host copy before any launch."""
+    plan = cp.cp_decode_plan(2, [5, 0, 130], n_workers=3)  # shard rows [3, 0, 65] and [2, 0, 65]
+    lib = cp.lib
+    fake = ctypes.c_void_p(256)  # never dereferenced: every case fails before a launch
+    good = np.array([[0, -1], [-1, -1], [1, 2], [3, -1], [-1, -1], [4, 5]], np.int32)
+
+    def pack(table, max_pages, page_size, num_pages):
+        t = np.ascontiguousarray(table, dtype=np.int32)
+        return lib.cp_kv_shard_pack_paged(plan.host.ctypes.data_as(ctypes.c_void_p), fake, cp.CP_BF16, fake,
+                                          None, 576, fake, None, t.ctypes.data_as(ctypes.c_void_p), fake,
+                                          max_pages, page_size, num_pages, None)
+
+    def decode(table, max_pages, page_size, num_pages):
+        t = np.ascontiguousarray(table, dtype=np.int32)
+        return lib.cp_decode_attn_paged(plan.host.ctypes.data_as(ctypes.c_void_p), fake, cp.CP_DECODE_MLA,
+                                        cp.CP_BF16, fake, fake, None, None, t.ctypes.data_as(ctypes.c_void_p),
+                                        fake, max_pages, page_size, num_pages, 64, 1, 576, 512, 0.04, fake,
+                                        fake, None, 0, None)
+
+    assert pack(good, 2, 96, 6) == -2 and b"multiple of 64" in lib.cp_last_error()
+    bad = good.copy(); bad[5, 1] = 6
+    assert pack(bad, 2, 64, 6) == -1 and b"outside [0, 6)" in lib.cp_last_error()
+    assert decode(bad, 2, 64, 6) == -1 and b"outside [0, 6)" in lib.cp_last_error()
+    assert pack(good[:, :1], 1, 64, 6) == -1 and b"needs 2 pages" in lib.cp_last_error()
+    dup = good.copy(); dup[3, 0] = 1
+    assert pack(dup, 2, 64, 6) == -1 and b"used twice" in lib.cp_last_error()
+    assert decode(good, 2, 64, 0) == -1 and b"num_pages=0" in lib.cp_last_error()

@@ -407,3 +407,49 @@ def test_planted_mistakes_are_caught(monkeypatch):
         m.setattr(oracle, "causal_rows", shifted)
         o_bad, _ = oracle.causal_rows(q, k, vv, np.arange(6), 0.5)
         assert not np.allclose(o_bad, o_ref)
+
+
+# ---------------------------------------------------------------- paged shard rows
+
+def test_paged_rows_hand_example():
+    """C = 2, one request of 5 tokens, pages of 2 rows.  Shard 0 holds tokens
+    0, 2, 4 (rows 0, 1, 2) on pages [3, 1]; shard 1 holds tokens 1, 3 (rows
+    0, 1) on page [0].  Pool row = page * 2 + row % 2:
+    token 0 -> page 3 row 0 = 6, token 2 -> page 3 row 1 = 7,
+    token 4 -> page 1 row 0 = 2, token 1 -> page 0 row 0 = 0,
+    token 3 -> page 0 row 1 = 1."""
+    got = oracle.paged_token_rows([5], 2, [[3, 1], [0, 0]], 2)
+    assert got == [(0, 0, 6), (0, 1, 0), (0, 2, 7), (0, 3, 1), (0, 4, 2)]
+
+
+def test_paged_rows_partition_and_contiguous_limit():
+    rng = np.random.default_rng(5)
+    ctx, C, ps = [0, 1, 77, 300, 129], 4, 8
+    B = len(ctx)
+    need = [[-(-len(range(r, L, C)) // ps) for L in ctx] for r in range(C)]
+    maxp = max(max(n) for n in need)
+    ids = rng.permutation(sum(sum(n) for n in need))
+    table = np.full((C * B, maxp), -1)
+    k = 0
+    for r in range(C):
+        for b in range(B):
+            for i in range(need[r][b]):
+                table[r * B + b, i] = ids[k]
+                k += 1
+    rows = oracle.paged_token_rows(ctx, C, table, ps)
+    assert sorted((b, p) for b, p, _ in rows) == [(b, p) for b, L in enumerate(ctx) for p in range(L)]
+    assert len({x for _, _, x in rows}) == len(rows)  # distinct pages -> distinct pool rows
+    # one shard, one page as large as the request, page 0: the pool row is the token
+    assert [x for _, _, x in oracle.paged_token_rows([40], 1, [[0]], 64)] == list(range(40))
+
+
+def test_paged_rows_pin_catches_swapped_row_and_shard():
+    """A planted mistake (shard p // C, row p mod C) moves tokens."""
+    def wrong(ctx_len, C, table, ps):
+        out = []
+        for b, L in enumerate(ctx_len):
+            for p in range(L):
+                pair, i = (p // C) * len(ctx_len) + b, p % C
+                out.append((b, p, int(table[pair][i // ps]) * ps + i % ps))
+        return out
+    assert wrong([5], 2, [[3, 1], [0, 0], [2, 2]], 2) != [(0, 0, 6), (0, 1, 0), (0, 2, 7), (0, 3, 1), (0, 4, 2)]
