@@ -8,17 +8,20 @@
 //
 // One CTA = one plan tile (up to 256 consecutive queries of one segment) x
 // one query head, as two 128-row M tiles that share every K/V tile:
-//   warps 0-3  softmax of M tile 0 (thread = query row = TMEM lane)
-//   warps 4-7  softmax of M tile 1
-//   warp 8     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring
-//   warp 9     MMA issuer (one thread) and TMEM owner
+//   warps 0-15  softmax: warp w takes rows [32 (w % 4), +32) of M tile
+//               (w / 4) % 2, columns [64 h, 64 h + 64) of S and dims
+//               [D/2 h, D/2 h + D/2) of O with h = w / 8 (four softmax warps
+//               per SM sub-partition hide each other's latency)
+//   warp 16     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring
+//   warp 17     MMA issuer (one thread) and TMEM owner
 // TMEM (512 columns): tile t holds S_t = Q_t K_j^T in columns [256t, 256t+128)
-// and its output accumulator O_t in [256t+128, 256t+128+D).  The softmax
-// writes P_t (bf16) over the first 64 columns of S_t, and O_t += P_t V_j
-// reads P from TMEM.  The MMA thread alternates the two M tiles so that one
-// tile's softmax overlaps the other tile's matrix products.  The running max
-// used in the exponentials only moves when a row's max grows by more than
-// 2^8, so O is rarely rescaled; the result is exact either way because
+// and its output accumulator O_t in [256t+128, 256t+128+D).  Each half of a
+// row writes its P (bf16 pairs) over the first 32 of its own 64 S columns,
+// and O_t += P_t V_j reads P from TMEM there.  The MMA thread alternates the
+// two M tiles so that one tile's softmax overlaps the other tile's matrix
+// products.  The running max used in the exponentials only moves when a
+// row's max grows by more than 2^8 (the two halves of the row exchange their
+// maxima then, and O is rescaled); the result is exact either way because
 // O = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m) holds for any m.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,9 +39,13 @@ using namespace tc;
 
 constexpr int BM = 128;        // query rows per M tile
 constexpr int BN = 128;        // keys per K/V tile
-constexpr int kThreads = 320;  // 10 warps
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
+constexpr int kSoftmaxWarps = 16;                 // two per row quarter of each M tile
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);  // + TMA warp + MMA warp
+constexpr int kWarpTma = kSoftmaxWarps;
+constexpr int kWarpMma = kSoftmaxWarps + 1;
+// Registers are capped as for five warps per SM sub-partition (warps 16, 17
+// share sub-partitions 0 and 1 with four softmax warps each).
+constexpr int kLaunchBoundThreads = 640;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max when it grows by > 2^8
 
@@ -47,7 +54,7 @@ struct Cfg {
   static constexpr int kChunks = D / 64;                   // 128-byte column chunks per row
   static constexpr int kQBytes = BM * D * 2;               // one Q tile
   static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
-  static constexpr int kSlots = D == 128 ? 5 : 10;         // ring of K/V tiles (5 x 32 KB fits beside Q)
+  static constexpr int kSlots = D == 128 ? 4 : 10;         // ring of K/V tiles (4 x 32 KB fits beside Q)
   static constexpr int kSmem = 2 * kQBytes + kSlots * kSlotBytes + 1024;
 };
 
@@ -103,7 +110,7 @@ __device__ void report_timeout(unsigned* status, unsigned site, volatile int* ab
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const Params p) {
   using C = Cfg<D>;
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
+  __shared__ float sXch[2][2][BM];    // row maxima / sums exchanged by the two halves of a row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_i = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
@@ -137,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
-      mbar_init(smem_u32(&bar_q[t]), 128);
+      mbar_init(smem_u32(&bar_q[t]), 2 * BM);
       mbar_init(smem_u32(&bar_s[t]), 1);
-      mbar_init(smem_u32(&bar_p[t]), 128);
+      mbar_init(smem_u32(&bar_p[t]), 2 * BM);
       mbar_init(smem_u32(&bar_o[t]), 1);
     }
     mbar_init(smem_u32(&bar_never), 1);
@@ -158,21 +166,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp < 8) {
+  if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
-    const int t = warp >> 2;
-    const int i = (warp & 3) * 32 + lane;  // row within the M tile = TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t colS = t * 256, colO = t * 256 + 128;
+    // Warps w and w + 8 take the same 32 rows of M tile t, columns
+    // [64 half, 64 half + 64) of each S row and dims [D/2 half, D/2 half + D/2)
+    // of each O row; they agree on the row's running max through sXch.
+    const int quarter = warp & 3;
+    const int t = (warp >> 2) & 1;
+    const int half = warp >> 3;
+    const int i = quarter * 32 + lane;  // row within the M tile = TMEM lane
+    const int pbar = 2 + t * 4 + quarter;  // named barrier of the two warps of these rows
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t colS = t * 256 + 64 * half, colO = t * 256 + 128 + (D / 2) * half;
     const int rows_t = t ? rows1 : rows0;
     const bool valid = i < rows_t;
-    // Q row -> shared memory in the 128-byte-swizzled K-major layout.
+    // Q row -> shared memory in the 128-byte-swizzled K-major layout (half of its pieces).
     {
       const long long f = (long long)sg.first_f + (long long)(td.q_off + t * BM + i) * sg.stride;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + (f * p.Hq + h) * D);
       uint8_t* dst = sQ + t * C::kQBytes + i * 128;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
+      for (int c = half * (D / 16); c < (half + 1) * (D / 16); ++c) {
         uint4 val = make_uint4(0, 0, 0, 0);
         if (valid) val = __ldg(src + c);
         const int a = c >> 3, cc = c & 7;
@@ -190,79 +204,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n_t && ok; ++j) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns, &abort_flag))) {
-          report_timeout(p.status, 1, &abort_flag);
+        const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns,
+                                                           &abort_flag));
+        // Both warps of these rows leave together: one that gave up meets the
+        // other at this vote.
+        if (bar_red_or(pbar, 64, !got)) {
+          if (!got) report_timeout(p.status, 1, &abort_flag);
           ok = false;
           break;
         }
         tc_fence_after();
-        const int kbase = j * BN;
-        const bool mask = kbase + BN - 1 > pos;
-        // The whole S row goes to registers with four loads and one wait (TMEM
-        // load latency is paid once per tile), so P can overwrite S's columns
-        // right away.  One pass exponentiates with the running max m_used; a
-        // second pass, from the registers, only runs on the first tile and when
-        // a row's max grows by more than 2^8 (tcgen05.ld/st are warp-collective:
-        // the warp redoes it together; rows whose max did not move recompute
-        // the same values).
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-          tmem_ld32(lane_addr + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+        // This half of the S row to registers (one wait); P overwrites only
+        // these columns, so the two halves never touch each other's S.
+        const int kbase = j * BN + 64 * half;
+        uint32_t sr[64];
+        tmem_ld32(lane_addr + colS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(lane_addr + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
-        if (mask) {
+        if (kbase + 63 > pos) {
 #pragma unroll
-          for (int e = 0; e < BN; ++e)
+          for (int e = 0; e < 64; ++e)
             if (kbase + e > pos) sr[e] = __float_as_uint(-INFINITY);
         }
         float mx = -INFINITY;
-        if (j == 0) {  // no running max yet: this tile's max first
 #pragma unroll
-          for (int e = 0; e < BN / 2; ++e)
-            mx = fmax3(mx, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
-          m_used = mx;
-        }
-        // P = 2^(s c - m c) as bf16 pairs over the first 64 columns of S; returns the row sum
-        auto exp_pass = [&](bool track) -> float {
-          const float neg = -m_used * sl2;
-          float s0sum = 0.f, s1sum = 0.f;
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t q16[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float s0 = __uint_as_float(sr[32 * c + 2 * e]);
-              const float s1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
-              if (track) mx = fmax3(mx, s0, s1);
-              float u0, u1;
-              fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
-              const float p0 = ex2(u0), p1 = ex2(u1);
-              add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
-              q16[e] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16(lane_addr + colS + c * 16, q16);
-          }
-          return s0sum + s1sum;
-        };
-        float lsum = exp_pass(j > 0);
-        if (j > 0) {
-          const bool need = mx > m_used + thr;
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2((m_used - mx) * sl2) : 1.f;
+        for (int e = 0; e < 32; ++e)
+          mx = fmax3(mx, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+        // The running max moves on the first tile and when a row's max grows by
+        // more than 2^8: the halves exchange maxima so both move it together.
+        if (bar_red_or(pbar, 64, j == 0 || mx > m_used + thr)) {
+          sXch[t][half][i] = mx;
+          named_bar_sync(pbar, 64);
+          const float mrow = fmaxf(mx, sXch[t][half ^ 1][i]);
+          if (j == 0) {
+            m_used = mrow;
+          } else {
+            const bool need = mrow > m_used + thr;
+            const float alpha = need ? ex2((m_used - mrow) * sl2) : 1.f;
             if (need) {
               l *= alpha;
-              m_used = mx;
+              m_used = mrow;
             }
-            // rescale O_t once its previous P V product has landed
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1, p.wait_ns,
-                                                   &abort_flag))) {
-              report_timeout(p.status, 2, &abort_flag);
+            // rescale this half of O_t once its previous P V product has landed
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1,
+                                                                  p.wait_ns, &abort_flag));
+            if (bar_red_or(pbar, 64, !landed)) {
+              if (!landed) report_timeout(p.status, 2, &abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < D / 16; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
               uint32_t r[16];
               tmem_ld16(lane_addr + colO + c * 16, r);
               tmem_ld_wait();
@@ -270,26 +263,46 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
               tmem_st16(lane_addr + colO + c * 16, r);
             }
-            lsum = exp_pass(false);
           }
         }
-        l += lsum;
+        // P = 2^(s c - m c) as bf16 pairs over this half's first 32 columns of S
+        const float neg = -m_used * sl2;
+        float s0sum = 0.f, s1sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t q16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float s0 = __uint_as_float(sr[32 * c + 2 * e]);
+            const float s1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
+            float u0, u1;
+            fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
+            const float p0 = ex2(u0), p1 = ex2(u1);
+            add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
+            q16[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(lane_addr + colS + c * 16, q16);
+        }
+        l += s0sum + s1sum;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p[t]));
       }
-      // epilogue: O / l and LSE
+      // epilogue: O / l and LSE (l summed over the two halves)
       const bool landed =
-          __all_sync(0xffffffffu, ok && mbar_wait(smem_u32(&bar_o[t]), (n_t - 1) & 1, p.wait_ns,
+          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (n_t - 1) & 1, p.wait_ns,
                                                   &abort_flag));
-      if (landed) {
+      if (!bar_red_or(pbar, 64, !landed)) {
         tc_fence_after();
-        const float inv = 1.f / l;
+        sXch[t][half][i] = l;
+        named_bar_sync(pbar, 64);
+        const float lt = l + sXch[t][half ^ 1][i];
+        const float inv = 1.f / lt;
         const long long out_row =
             (long long)sg.local_start + td.q_off + t * BM + i - p.row_sub;
-        __nv_bfloat16* dst = p.o + (out_row * p.Hq + h) * D;
+        __nv_bfloat16* dst = p.o + (out_row * p.Hq + h) * D + (D / 2) * half;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t r[32];
           tmem_ld32(lane_addr + colO + c * 32, r);
           tmem_ld_wait();
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (valid) p.lse[out_row * p.Hq + h] = m_used * p.sm_scale + logf(l);
+        if (valid && half == 0) p.lse[out_row * p.Hq + h] = m_used * p.sm_scale + logf(lt);
       } else if (ok) {
         report_timeout(p.status, 3, &abort_flag);
       }
@@ -346,23 +359,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         return mbar_wait(smem_u32(&bar_full[u % C::kSlots]), (u / C::kSlots) & 1, p.wait_ns,
                          &abort_flag);
       };
+      // Descriptors are built once; an MMA adds its byte offset / 16 to the
+      // start-address field (shared addresses stay below 2^18, so it never
+      // carries).  The issuing thread shares its SM sub-partition with four
+      // softmax warps: few instructions per MMA keep the tensor pipe fed.
+      const uint64_t dQ0 = smem_desc(smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024);
+      const uint64_t dV0 = smem_desc(smem_u32(sKV), BN * 128, 1024);
       auto issue_s = [&](int t, int u) {
-        const uint32_t kb = smem_u32(sKV + (u % C::kSlots) * C::kSlotBytes);
-        const uint32_t qb = smem_u32(sQ + t * C::kQBytes);
+        const uint64_t a0 = dQ0 + (uint64_t)((t * C::kQBytes) >> 4);
+        const uint64_t b0 = dK0 + (uint64_t)(((u % C::kSlots) * C::kSlotBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BM * 128) + (kk & 3) * 32;
-          mma_ss(tmem + t * 256, smem_desc(qb + off, 16, 1024), smem_desc(kb + off, 16, 1024),
-                 idS, kk > 0);
+          const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + t * 256, a0 + off, b0 + off, idS, kk > 0);
         }
         mma_commit(smem_u32(&bar_s[t]));
       };
       auto issue_pv = [&](int t, int u, bool acc) {
-        const uint32_t vb = smem_u32(sKV + (u % C::kSlots) * C::kSlotBytes);
+        const uint64_t v0 = dV0 + (uint64_t)(((u % C::kSlots) * C::kSlotBytes) >> 4);
+        const uint32_t pa = tmem + t * 256, d = tmem + t * 256 + 128;
+        // P of keys [64 h, 64 h + 64) sits over the first 32 of S's columns [64 h, 64 h + 64)
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + t * 256 + 128, tmem + t * 256 + kk * 8,
-                 smem_desc(vb + kk * 16 * 128, BN * 128, 1024), idPV, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, pa + (kk >> 2) * 64 + (kk & 3) * 8, v0 + (uint64_t)((kk * 16 * 128) >> 4), idPV,
+                 (acc || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&bar_o[t]));
       };
       bool ok = true;
