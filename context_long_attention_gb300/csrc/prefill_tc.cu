@@ -54,7 +54,7 @@ struct Cfg {
   static constexpr int kChunks = D / 64;                   // 128-byte column chunks per row
   static constexpr int kQBytes = BM * D * 2;               // one Q tile
   static constexpr int kSlotBytes = BN * D * 2;            // one K or V tile
-  static constexpr int kSlots = D == 128 ? 4 : 10;         // ring of K/V tiles (4 x 32 KB fits beside Q)
+  static constexpr int kSlots = D == 128 ? 5 : 10;         // ring of K/V tiles (5 x 32 KB fits beside Q)
   static constexpr int kSmem = 2 * kQBytes + kSlots * kSlotBytes + 1024;
 };
 
@@ -124,7 +124,6 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
-  __shared__ float sXch[2][2][BM];    // row maxima / sums exchanged by the two halves of a row
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_i = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
@@ -168,9 +167,11 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
 
   if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax
-    // Warps w and w + 8 take the same 32 rows of M tile t, columns
-    // [64 half, 64 half + 64) of each S row and dims [D/2 half, D/2 half + D/2)
-    // of each O row; they agree on the row's running max through sXch.
+    // Warps w and w + 8 take the same 32 rows (TMEM lanes) of M tile t,
+    // columns [64 half, 64 half + 64) of each S row and dims [D/2 half,
+    // D/2 half + D/2) of each O row.  They exchange row maxima and sums
+    // through column 63 of each half's S columns, which P never covers and
+    // which S no longer needs once a tile's values are in registers.
     const int quarter = warp & 3;
     const int t = (warp >> 2) & 1;
     const int half = warp >> 3;
@@ -180,6 +181,17 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     const uint32_t colS = t * 256 + 64 * half, colO = t * 256 + 128 + (D / 2) * half;
     const int rows_t = t ? rows1 : rows0;
     const bool valid = i < rows_t;
+    // value of the other half of this row
+    auto exchange = [&](float v) -> float {
+      tmem_st1(lane_addr + t * 256 + 64 * half + 63, __float_as_uint(v));
+      tmem_st_wait();
+      tc_fence_before();
+      named_bar_sync(pbar, 64);
+      tc_fence_after();
+      const uint32_t o = tmem_ld1(lane_addr + t * 256 + 64 * (half ^ 1) + 63);
+      tmem_ld_wait();
+      return __uint_as_float(o);
+    };
     // Q row -> shared memory in the 128-byte-swizzled K-major layout (half of its pieces).
     {
       const long long f = (long long)sg.first_f + (long long)(td.q_off + t * BM + i) * sg.stride;
@@ -233,9 +245,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
         // The running max moves on the first tile and when a row's max grows by
         // more than 2^8: the halves exchange maxima so both move it together.
         if (bar_red_or(pbar, 64, j == 0 || mx > m_used + thr)) {
-          sXch[t][half][i] = mx;
-          named_bar_sync(pbar, 64);
-          const float mrow = fmaxf(mx, sXch[t][half ^ 1][i]);
+          const float mrow = fmaxf(mx, exchange(mx));
           if (j == 0) {
             m_used = mrow;
           } else {
@@ -294,9 +304,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
                                                   &abort_flag));
       if (!bar_red_or(pbar, 64, !landed)) {
         tc_fence_after();
-        sXch[t][half][i] = l;
-        named_bar_sync(pbar, 64);
-        const float lt = l + sXch[t][half ^ 1][i];
+        const float lt = l + exchange(l);
         const float inv = 1.f / lt;
         const long long out_row =
             (long long)sg.local_start + td.q_off + t * BM + i - p.row_sub;
