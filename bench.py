@@ -47,15 +47,15 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "0a9433007cd0c563b1e7a7f2166799f3dd34b052", "bytes": 2.370106e9 + 0.275549e9},
+                "sha1": "b7e2d65e16aa3b45f81ef50e7b206f806cb4ada6", "bytes": 2.376624e9 + 0.273960e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "4cb3f309e8898b78becf5e13458cf1bb1f606503",
-                   "bytes_per_token": (0.637946e9 + 0.010263e9) / (8 * 131072)},
+                   "sha1": "6877ca2dd8c43b740d8df26608437b85500dc60f",
+                   "bytes_per_token": (0.637617e9 + 0.011065e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "64f172d890a190d8e5237dc0d2192ddb2d638975",
-                    "bytes_per_token": (1.209230e9 + 0.011201e9) / (8 * 131072)},
+                    "sha1": "2899e683da4b57101d20237f8e1458e96cfa6227",
+                    "bytes_per_token": (1.209231e9 + 0.011313e9) / (8 * 131072)},
 }
 
 

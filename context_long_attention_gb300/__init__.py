@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     cp_device_error_check,
     cp_kv_shard_pack,
     cp_kv_shard_pack_paged,
+    cp_lse_fold,
     cp_lse_merge,
     cp_plan_size,
     cp_prefill_attn,

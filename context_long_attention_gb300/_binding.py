@@ -53,6 +53,7 @@ _SIGS = {
     "cp_decode_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp,
                             _vp, _sz, _vp]),
     "cp_lse_merge": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
+    "cp_lse_fold": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "cp_decode_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
                                     _vp, _vp]),
     "cp_kv_shard_pack_paged": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
@@ -422,6 +423,19 @@ def cp_lse_merge(o_part, lse_part, out_dtype=torch.bfloat16, out=None, lse=None)
     _check(lib.cp_lse_merge(P, N, H, Dv, _ptr(o_part), _ptr(lse_part), _ptr(out),
                             _dtype_code(out), _ptr(lse), _stream(o_part.device)))
     return out, lse
+
+
+def cp_lse_fold(o, lse, o_add, lse_add):
+    """(o, lse) <- exact combine of (o, lse) and (o_add, lse_add), in place;
+    o, o_add [N, H, Dv] fp32 contiguous, lse, lse_add [N, H] fp32."""
+    _need_cuda(o, lse, o_add, lse_add)
+    for t in (o, lse, o_add, lse_add):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("cp_lse_fold takes contiguous fp32 tensors")
+    N, H, Dv = o.shape
+    _check(lib.cp_lse_fold(N, H, Dv, _ptr(o), _ptr(lse), _ptr(o_add), _ptr(lse_add),
+                           _stream(o.device)))
+    return o, lse
 
 
 def cp_device_error_check(device=None):

@@ -791,4 +791,14 @@ cp_status cp_lse_merge(int P, int N, int H, int Dv, const float* o_part, const f
   return ok();
 }
 
+cp_status cp_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o_add,
+                      const float* lse_add, void* stream) {
+  if (N < 0 || H < 1 || Dv < 1) return fail(CP_ERR_INVALID_ARG, "bad shape N=%d H=%d Dv=%d", N, H, Dv);
+  if (!o || !lse || !o_add || !lse_add) return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (N == 0) return ok();
+  cudaError_t e = launch_lse_fold(N, H, Dv, o, lse, o_add, lse_add, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fold kernel");
+  return ok();
+}
+
 }  // extern "C"

@@ -74,6 +74,8 @@ cudaError_t launch_page_tail_zero(const int32_t* dev_plan, const cp_plan_header&
 cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
                              const float* lse_part, void* o, bool o_bf16, float* lse,
                              cudaStream_t s);
+cudaError_t launch_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o_add,
+                            const float* lse_add, cudaStream_t s);
 cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h, int H, int Dv,
                                 const float* ws_o, const float* ws_lse, float* o_part,
                                 float* lse_part, cudaStream_t s);

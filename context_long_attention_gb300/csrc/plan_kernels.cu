@@ -5,7 +5,7 @@
 //   ("How GPUs Share a Long Context During LLM Inference", §2.3-2.4).
 // * kv_pack_kernel: token p of a request -> shard p mod C, row p / C (§3.1),
 //   into the shard's buffer or, paged, into the pool row its page table gives.
-// * lse_merge_kernel / decode_fixup_kernel: O = sum_p w_p O_p / sum_p w_p
+// * lse_merge_kernel / decode_fixup_kernel / lse_fold_kernel: O = sum_p w_p O_p / sum_p w_p
 //   with w_p = exp(LSE_p - max LSE) (§3.3; "DeepSeek-V4 Attention Inference
 //   Systems" §5), one warp per (row, head), 128-bit loads.
 #include <cuda_bf16.h>
@@ -134,6 +134,31 @@ __global__ void lse_merge_kernel(int P, long long NH, int Dv, const float* __res
   merge_row(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, of, ob, lse ? lse + i : nullptr);
 }
 
+// (O, LSE) <- the exact combine of (O, LSE) and (O', LSE'), in place; one warp
+// per (row, head).  Two empty partials stay O = 0, LSE = -inf.
+__global__ void lse_fold_kernel(long long NH, int Dv, float* __restrict__ o, float* __restrict__ lse,
+                                const float* __restrict__ o_add, const float* __restrict__ lse_add) {
+  const long long i = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= NH) return;
+  const int lane = threadIdx.x & 31;
+  const float l0 = lse[i], l1 = lse_add[i];
+  const float g = fmaxf(l0, l1);
+  float a0 = 0.f, a1 = 0.f, lg = -INFINITY;
+  if (g != -INFINITY) {
+    const float w0 = l0 == -INFINITY ? 0.f : expf(l0 - g);
+    const float w1 = l1 == -INFINITY ? 0.f : expf(l1 - g);
+    const float z = w0 + w1;
+    a0 = w0 / z;
+    a1 = w1 / z;
+    lg = g + logf(z);
+  }
+  float* od = o + i * Dv;
+  const float* oa = o_add + i * Dv;
+  for (int c = lane; c < Dv; c += 32) od[c] = a0 * od[c] + a1 * oa[c];
+  __syncwarp();
+  if (lane == 0) lse[i] = lg;
+}
+
 __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                                     int off_split, int n_split, int H, int Dv,
                                     const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
@@ -191,6 +216,15 @@ cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
   const long long blocks = (NH + warps - 1) / warps;
   lse_merge_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(P, NH, Dv, o_part, lse_part, o,
                                                            o_bf16 ? 1 : 0, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o_add,
+                            const float* lse_add, cudaStream_t s) {
+  const long long NH = (long long)N * H;
+  const int warps = 8;
+  const long long blocks = (NH + warps - 1) / warps;
+  lse_fold_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(NH, Dv, o, lse, o_add, lse_add);
   return cudaGetLastError();
 }
 

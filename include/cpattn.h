@@ -345,6 +345,18 @@ cp_status cp_lse_merge(int P, int N, int H, int Dv, const float* o_part, const f
                        void* o, cp_dtype o_dtype, float* lse, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * cp_lse_fold — exact combine of one partial into another, in place:
+ * (O, LSE) <- combine((O, LSE), (O_add, LSE_add)) with the weights of
+ * cp_lse_merge ([V4] §5).  The designated-rank rule of [V4] §5.3: a window
+ * (or sink) cache that every shard holds a copy of is attended once, as its
+ * own partial, and folded into exactly one shard's partial, so its
+ * probability mass is counted once when the shards are merged.
+ * o, o_add [N, H, Dv] fp32; lse, lse_add [N, H] fp32 (may alias nothing else).
+ * ------------------------------------------------------------------------- */
+cp_status cp_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o_add,
+                      const float* lse_add, void* stream);
+
+/* ---------------------------------------------------------------------------
  * cp_decode_attn_noalloc — cp_decode_attn for callers that cannot allocate.
  *
  * The pages have no counterpart: this is an interface convenience.  Some

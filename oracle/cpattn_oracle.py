@@ -428,3 +428,33 @@ def decode_shard_partials(q: np.ndarray, kcache: np.ndarray, vcache: np.ndarray,
         outs.append(o)
         lses.append(lse)
     return np.stack(outs), np.stack(lses)
+
+
+def designated_partials(q: np.ndarray, kmain: np.ndarray, vmain: np.ndarray, kwin: np.ndarray,
+                        vwin: np.ndarray, C: int, designated: int,
+                        sm_scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """Per-shard partials when a local window is replicated on every shard.
+
+    [V4] §5.1, §5.3: each rank attends to the main-cache entries it owns
+    (token p on shard p mod C); the small local window is held by every rank,
+    but only the designated rank includes it in its partial softmax, so its
+    probability mass is counted once in the exact combine.  Shard r's key set
+    is {main tokens p : p mod C = r}, plus every window row when r is the
+    designated rank.  Returns O [C, H, Dv], LSE [C, H] (empty: 0, -inf).
+    """
+    L = kmain.shape[0]
+    shard, _ = decode_shard_map(L, C)
+    shard = np.asarray(shard)
+    outs, lses = [], []
+    for r in range(C):
+        keys = [kmain[shard == r]]
+        vals = [vmain[shard == r]]
+        if r == designated:
+            keys.append(kwin)
+            vals.append(vwin)
+        o, lse = decode_attention(q, np.concatenate(keys, axis=0), np.concatenate(vals, axis=0),
+                                  sm_scale)
+        outs.append(o)
+        lses.append(lse)
+    return np.stack(outs), np.stack(lses)
+

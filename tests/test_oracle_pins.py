@@ -453,3 +453,50 @@ def test_paged_rows_pin_catches_swapped_row_and_shard():
                 out.append((b, p, int(table[pair][i // ps]) * ps + i % ps))
         return out
     assert wrong([5], 2, [[3, 1], [0, 0], [2, 2]], 2) != [(0, 0, 6), (0, 1, 0), (0, 2, 7), (0, 3, 1), (0, 4, 2)]
+
+
+# ---------------------------------------------------------------- replicated window, designated rank
+
+def _window_case(L=37, W=9, H=4, Hkv=2, D=16, seed=11):
+    rng = np.random.default_rng(seed)
+    q = rng.normal(size=(H, D))
+    km, vm = rng.normal(size=(L, Hkv, D)), rng.normal(size=(L, Hkv, D))
+    kw, vw = rng.normal(size=(W, Hkv, D)), rng.normal(size=(W, Hkv, D))
+    return q, km, vm, kw, vw
+
+
+def test_designated_window_counted_once():
+    """[V4] §5.3: the window's mass is counted once, so the exact combine of
+    the shards' partials is the attention over main cache + window."""
+    q, km, vm, kw, vw = _window_case()
+    scale = 0.3
+    for C, d in [(1, 0), (4, 0), (4, 3), (5, 2)]:
+        po, pl = oracle.designated_partials(q, km, vm, kw, vw, C, d, scale)
+        o, lse = oracle.lse_merge(po, pl)
+        fo, fl = oracle.decode_attention(q, np.concatenate([km, kw]), np.concatenate([vm, vw]), scale)
+        assert np.allclose(o, fo, atol=1e-12) and np.allclose(lse, fl, atol=1e-12)
+        # the other shards hold main-cache tokens only
+        so, sl = oracle.decode_shard_partials(q, km, vm, C, scale)
+        for r in range(C):
+            if r != d:
+                assert np.allclose(po[r], so[r]) and np.allclose(pl[r], sl[r])
+
+
+def test_designated_window_pin_catches_double_count():
+    """A planted mistake: every shard counts its copy of the window."""
+    q, km, vm, kw, vw = _window_case()
+    C, scale = 4, 0.3
+    parts = [oracle.designated_partials(q, km, vm, kw, vw, C, r, scale) for r in range(C)]
+    wrong_o = np.stack([parts[r][0][r] for r in range(C)])
+    wrong_l = np.stack([parts[r][1][r] for r in range(C)])
+    o, lse = oracle.lse_merge(wrong_o, wrong_l)
+    fo, fl = oracle.decode_attention(q, np.concatenate([km, kw]), np.concatenate([vm, vw]), scale)
+    assert not np.allclose(lse, fl, atol=1e-6)
+
+
+def test_designated_window_empty_main_cache():
+    q, km, vm, kw, vw = _window_case(L=0)
+    po, pl = oracle.designated_partials(q, km, vm, kw, vw, 3, 1, 0.5)
+    wo, wl = oracle.decode_attention(q, kw, vw, 0.5)
+    assert np.allclose(po[1], wo) and np.allclose(pl[1], wl)
+    assert np.isneginf(pl[0]).all() and np.isneginf(pl[2]).all() and not po[0].any()
