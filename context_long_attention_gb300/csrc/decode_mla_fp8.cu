@@ -294,7 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop, so that descriptors and loop state stay
+    // warp-uniform; one elected lane (lane 0, the same one every time, which
+    // also commits) issues the products.  Barrier results are made uniform by
+    // a vote before they steer the loop.
+    {
+      constexpr unsigned kAll = 0xffffffffu;
       const uint32_t idQK = idesc_e4m3_f32(kRows, 2 * kHeads, 0, 0);
       const uint32_t idPV = idesc_e4m3_f32(kRows, kHeads, 1, 1);
       // Descriptors are built once; an MMA adds its byte offset / 16 to the
@@ -309,6 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dQr = smem_desc(sbase + kQOff + kRopeOff, 16, 512, 4);
       const uint64_t dPlo = smem_desc(sbase + kPloOff, 16, 512, 4);
       auto full_bar = [&](int gq, int q) { return smem_u32(&bar_full[gq & 1][q]); };
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(kAll, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
+      };
+      auto test_any = [&](uint32_t bar, uint32_t parity) {
+        return __any_sync(kAll, mbar_test(bar, parity));
+      };
       // S^T(gq) += K_codes . [Q_hi | Q_lo]^T over chunk group q
       auto qk_group = [&](int gq, int q) {
         const int s = gq & 1;
@@ -317,15 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q < 4) {
           const uint64_t a = (s ? dK[1] : dK[0]) + (uint64_t)((q * kChunkBytes) >> 4);
           const uint64_t b = dQ + (uint64_t)((q * kChunkBytes) >> 4);
+          if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss_f8(d, a + 2 * ks, b + 2 * ks, idQK, (q | ks) != 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss_f8(d, a + 2 * ks, b + 2 * ks, idQK, (q | ks) != 0 ? 1u : 0u);
+          }
         } else {
           const uint64_t a = s ? dKr[1] : dKr[0];
+          if (elect_one()) {
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) mma_ss_f8(d, a + 2 * ks, dQr + 2 * ks, idQK, 1u);
-          mma_commit(smem_u32(&bar_s[s]));
+            for (int ks = 0; ks < 2; ++ks) mma_ss_f8(d, a + 2 * ks, dQr + 2 * ks, idQK, 1u);
+            mma_commit(smem_u32(&bar_s[s]));
+          }
         }
+        __syncwarp();
       };
       // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T); the last block's
       // commit releases the stage and P_lo^T's buffer.
@@ -334,13 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t av = (s ? dV[1] : dV[0]) + (uint64_t)((mb * kChunkBytes) >> 4);
         const uint64_t bh = s ? dKr[1] : dKr[0];  // P_hi^T over the rope chunk
         const uint32_t d = tmem + 256 + 64 * mb;
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kRows / 32; ++kk) {
-          const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
-          mma_ss_f8(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || !first) ? 1u : 0u);
-          mma_ss_f8(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
+          for (int kk = 0; kk < kRows / 32; ++kk) {
+            const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
+            mma_ss_f8(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || !first) ? 1u : 0u);
+            mma_ss_f8(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
+          }
+          if (mb == 3) mma_commit(smem_u32(&bar_done[s]));
         }
-        if (mb == 3) mma_commit(smem_u32(&bar_done[s]));
+        __syncwarp();
       };
       bool ok = true;
       int g = 0, nq = 0;  // tiles and non-empty items so far
@@ -348,16 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = read_item(p, wi);
         if (it.ntiles == 0) continue;
         // the item's query is in place (written after every earlier product completed)
-        if (!mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag)) {
-          report_timeout(p.status, 2, &abort_flag);
+        if (!wait_all(smem_u32(&bar_q), nq & 1)) {
+          if (lane == 0) report_timeout(p.status, 2, &abort_flag);
           break;
         }
         ++nq;
         int done = 0;  // chunk groups of QK^T(g) already issued
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
           for (; done < 5; ++done) {
-            if (!mbar_wait(full_bar(g, done), (g >> 1) & 1, p.wait_ns, &abort_flag)) {
-              report_timeout(p.status, 3, &abort_flag);
+            if (!wait_all(full_bar(g, done), (g >> 1) & 1)) {
+              if (lane == 0) report_timeout(p.status, 3, &abort_flag);
               ok = false;
               break;
             }
@@ -372,11 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool p_ready = false;
           const uint64_t t0 = global_timer_ns();
           for (uint32_t spin = 1; mb < 4; ++spin) {
-            if (more && next < 5 && mbar_test(full_bar(g + 1, next), ((g + 1) >> 1) & 1)) {
+            if (more && next < 5 && test_any(full_bar(g + 1, next), ((g + 1) >> 1) & 1)) {
               qk_group(g + 1, next++);
               continue;
             }
-            if (!p_ready && mbar_test(smem_u32(&bar_p), g & 1)) {
+            if (!p_ready && test_any(smem_u32(&bar_p), g & 1)) {
               p_ready = true;
               tc_fence_after();
             }
@@ -385,10 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               ++mb;
               continue;
             }
-            if ((spin & 255u) == 0 && (abort_flag || global_timer_ns() - t0 > p.wait_ns)) break;
+            if ((spin & 255u) == 0 &&
+                __any_sync(kAll, abort_flag || global_timer_ns() - t0 > p.wait_ns))
+              break;
           }
           if (mb < 4) {
-            report_timeout(p.status, 4, &abort_flag);
+            if (lane == 0) report_timeout(p.status, 4, &abort_flag);
             ok = false;
             break;
           }
@@ -396,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Never free TMEM under a running MMA.
-      mma_commit(smem_u32(&bar_drain));
+      if (elect_one()) mma_commit(smem_u32(&bar_drain));
+      __syncwarp();
       mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
     }
   } else {

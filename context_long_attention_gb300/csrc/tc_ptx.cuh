@@ -46,6 +46,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One lane of a converged warp (the lowest active one, the same lane on every
+// call) gets true.  Code that issues tensor-core work runs on the whole warp,
+// so that descriptors and loop state stay warp-uniform, and only the elected
+// lane issues the instruction.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b32 l;\n elect.sync l|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Non-blocking test of the same condition (never suspends the thread).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
