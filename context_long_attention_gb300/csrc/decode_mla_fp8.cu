@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // Warp-wide like the issuer: one elected lane issues the copies.
+    {
       int last_g[2] = {-1, -1}, last_n[2] = {0, 0};  // last tile per stage, groups issued for it
       bool ok = true;
       int g = 0;
@@ -249,8 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hh = 0; hh < 2; ++hh) {
             const int i = jt * kRows + 64 * hh;
             const int rows = min(64, it.nrows - i);
-            if (rows > 0)
-              prefetch_l2_bulk(codes + cache_row(i) * kDqk, (uint32_t)rows * kDqk);
+            const long long row = rows > 0 ? cache_row(i) : 0;
+            if (rows > 0 && elect_one()) prefetch_l2_bulk(codes + row * kDqk, (uint32_t)rows * kDqk);
+            __syncwarp();
           }
         };
         for (int jt = 0; jt < kPrefetchAhead && jt < it.ntiles; ++jt) prefetch(jt);
@@ -263,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const long long yh[2] = {p.rm.table ? cache_row(j * kRows) : 0,
                                    p.rm.table ? cache_row(j * kRows + 64) : 0};
           // the stage is free once the P.V of its previous tile (g - 2) has completed
-          if (g >= 2 && !mbar_wait(smem_u32(&bar_done[s]), ((g >> 1) & 1) ^ 1, p.wait_ns,
-                                   &abort_flag)) {
-            report_timeout(p.status, 1, &abort_flag);
+          if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[s]), ((g >> 1) & 1) ^ 1,
+                                                           p.wait_ns, &abort_flag))) {
+            if (lane == 0) report_timeout(p.status, 1, &abort_flag);
             ok = false;
             break;
           }
@@ -274,14 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = stage + (q < 4 ? q * kChunkBytes : kRopeOff);
             const int x = 128 * q, row_bytes = q < 4 ? 128 : 64;
             const CUtensorMap* map = q < 4 ? &maps.body[it.r] : &maps.rope[it.r];
-            mbar_expect_tx(full, kRows * row_bytes);
-            if (!p.rm.table) {
-              tma_load_2d(dst, map, x, y, full);
-            } else {  // two 64-row halves, each inside one page
-              for (int hh = 0; hh < 2; ++hh)
-                tma_load_2d(dst + hh * 64 * row_bytes, &(q < 4 ? maps.body : maps.rope)[0], x,
-                            (int)yh[hh], full);
+            if (elect_one()) {
+              mbar_expect_tx(full, kRows * row_bytes);
+              if (!p.rm.table) {
+                tma_load_2d(dst, map, x, y, full);
+              } else {  // two 64-row halves, each inside one page
+                for (int hh = 0; hh < 2; ++hh)
+                  tma_load_2d(dst + hh * 64 * row_bytes, &(q < 4 ? maps.body : maps.rope)[0], x,
+                              (int)yh[hh], full);
+              }
             }
+            __syncwarp();
             last_g[s] = g;
             last_n[s] = q + 1;
           }

@@ -18,9 +18,10 @@
 // the first product reads.
 //
 // Warp roles (256 threads): warps 0-3 softmax, thread = KV row of the tile
-// (TMEM lane) and, in the epilogue, dim row of O^T; thread 0 also owns TMEM
-// and issues the MMAs; one thread of warp 4 refills the tile by TMA chunk
-// group by chunk group as the previous tile's P.V releases it.
+// (TMEM lane) and, in the epilogue, dim row of O^T; warp 0 also owns TMEM
+// and issues the MMAs (one elected lane, the loop run warp-wide); warp 4
+// refills the tile by TMA chunk group by chunk group as the previous tile's
+// P.V releases it.
 // Softmax down the KV axis needs per-head maxima over the 128 rows of a tile.
 // The running maximum M_h used in the exponentials only moves when some score
 // exceeds it by more than 2^8 (checked per tile with one block-wide vote);
@@ -186,8 +187,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     if (warp >= 4) {
-      // ------------------------------------------------------------ tile fill (TMA, one thread)
-      if (threadIdx.x == 128) {
+      // ------------------------------------------------------------ tile fill (TMA, warp 4;
+      // the warp runs the loop, one elected lane issues the copies)
+      if (warp == 4) {
         int issued_tiles = 0;  // tiles whose copies were issued (for the drain)
         for (int j = 0; j < ntiles && ok; ++j) {
           const int g = g0 + j;
@@ -204,25 +206,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 5; ++q) {
             // group q is free once the previous tile's P.V M-block q (or, for the
             // rope group that holds P^T, the whole P.V) has read it
-            if (ok && j > 0 && !mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]), (g - 1) & 1, p.wait_ns,
-                                          &abort_flag)) {
-              report_timeout(p.status, 1, &abort_flag);
+            if (ok && j > 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]), (g - 1) & 1,
+                                                   p.wait_ns, &abort_flag))) {
+              if (lane == 0) report_timeout(p.status, 1, &abort_flag);
               ok = false;
             }
             if (!ok) continue;
             const uint32_t full = smem_u32(&bar_fill[q]);
-            mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
-            for (int cc = 0; cc < group_chunks(q); ++cc) {
-              const int c = 2 * q + cc;
-              if (!p.rm.table) {
-                tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
-                            (int)(row0 + (long long)j * kRows), full);
-              } else {
-                for (int hh = 0; hh < 2; ++hh)
-                  tma_load_2d(smem_u32(sTile + c * kChunkBytes + hh * 64 * 128), &maps.m[0],
-                              c * 64, (int)yh[hh], full);
+            if (elect_one()) {
+              mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
+              for (int cc = 0; cc < group_chunks(q); ++cc) {
+                const int c = 2 * q + cc;
+                if (!p.rm.table) {
+                  tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
+                              (int)(row0 + (long long)j * kRows), full);
+                } else {
+                  for (int hh = 0; hh < 2; ++hh)
+                    tma_load_2d(smem_u32(sTile + c * kChunkBytes + hh * 64 * 128), &maps.m[0],
+                                c * 64, (int)yh[hh], full);
+                }
               }
             }
+            __syncwarp();
           }
           if (!ok) break;
           issued_tiles = j + 1;
@@ -231,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // never leave with a copy in flight: the last issued tile's groups
           for (int q = 0; q < 5; ++q)
             mbar_wait(smem_u32(&bar_fill[q]), (g0 + issued_tiles - 1) & 1, 1000000000ull, &zero_flag);
+          __syncwarp();
         }
       }
     } else {
@@ -240,26 +247,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
       const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
       const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
+      // Warp 0 issues the products warp-wide (one elected lane); descriptors are
+      // built once and an MMA adds its byte offset / 16 to the address field.
+      const uint64_t dK = smem_desc(tile, 16, 1024), dQ = smem_desc(qb, 16, 1024);
+      const uint64_t dV = smem_desc(tile, kChunkBytes, 1024), dP = smem_desc(pb, 16, 1024);
       float l[kHeads];
 #pragma unroll
       for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
       for (int j = 0; j < ntiles; ++j) {
         const int g = g0 + j;
         bool issued = true;
-        if (t == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
+        if (warp == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
           for (int q = 0; q < 5 && issued; ++q) {
-            issued = mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns, &abort_flag);
+            issued = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns,
+                                                       &abort_flag));
             if (!issued) break;
             tc_fence_after();
-            for (int ks = 0; ks < 4 * group_chunks(q); ++ks) {
-              const int kk = 8 * q + ks;
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
-              mma_ss(tmem, smem_desc(tile + off, 16, 1024), smem_desc(qb + qoff, 16, 1024), idS,
-                     kk > 0);
+            if (elect_one()) {
+              for (int ks = 0; ks < 4 * group_chunks(q); ++ks) {
+                const int kk = 8 * q + ks;
+                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
+                mma_ss(tmem, dK + (off >> 4), dQ + (qoff >> 4), idS, kk > 0);
+              }
             }
+            __syncwarp();
           }
-          if (issued) mma_commit(smem_u32(&bar_s));
+          if (issued && elect_one()) mma_commit(smem_u32(&bar_s));
+          __syncwarp();
         }
         const bool valid = j * kRows + t < nrows;
         const float cj = p.scale_log2;  // scores in log2 units
@@ -347,17 +362,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(1, 128);  // every row of P^T is written
-        if (t == 0) {            // O^T += V_tile^T P^T, one M-block (128 dims) at a time
+        if (warp == 0) {         // O^T += V_tile^T P^T, one M-block (128 dims) at a time
           tc_fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int mb = 0; mb < kDv / 128; ++mb) {
+            for (int mb = 0; mb < kDv / 128; ++mb) {
 #pragma unroll
-            for (int kk = 0; kk < kRows / 16; ++kk)
-              mma_ss(tmem + 64 + 64 * mb,
-                     smem_desc(tile + 2 * mb * kChunkBytes + kk * 2048, kChunkBytes, 1024),
-                     smem_desc(pb + kk * 2048, 16, 1024), idPV, (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&bar_mb[mb]));
+              for (int kk = 0; kk < kRows / 16; ++kk)
+                mma_ss(tmem + 64 + 64 * mb, dV + ((2 * mb * kChunkBytes + kk * 2048) >> 4),
+                       dP + ((kk * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(smem_u32(&bar_mb[mb]));
+            }
           }
+          __syncwarp();
         }
       }
       // ---- epilogue: column sums of l, O^T / l, LSE
@@ -409,8 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = ok && !abort_flag;
   }
   // Never free TMEM under a running MMA.
-  if (threadIdx.x == 0) {
-    mma_commit(smem_u32(&bar_drain));
+  if (warp == 0) {
+    if (elect_one()) mma_commit(smem_u32(&bar_drain));
+    __syncwarp();
     mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
   }
   tc_fence_before();

@@ -13,7 +13,8 @@
 //               [D/2 h, D/2 h + D/2) of O with h = w / 8 (four softmax warps
 //               per SM sub-partition hide each other's latency)
 //   warp 16     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring
-//   warp 17     MMA issuer (one thread) and TMEM owner
+//   warp 17     MMA issuer (one elected lane; the warp runs the loop) and
+//               TMEM owner
 // TMEM (512 columns): tile t holds S_t = Q_t K_j^T in columns [256t, 256t+128)
 // and its output accumulator O_t in [256t+128, 256t+128+D).  Each half of a
 // row writes its P (bf16 pairs) over the first 32 of its own 64 S columns,
@@ -333,39 +334,56 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     }
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The warp runs the loop; one elected lane issues the copies.
+    {
       int last_round[C::kSlots];
 #pragma unroll
       for (int s = 0; s < C::kSlots; ++s) last_round[s] = -1;
       for (int u = 0; u < 2 * nK; ++u) {
         const int j = u >> 1, slot = u % C::kSlots, round = u / C::kSlots;
-        if (!mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1, p.wait_ns, &abort_flag)) {
-          report_timeout(p.status, 4, &abort_flag);
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1,
+                                               p.wait_ns, &abort_flag))) {
+          if (lane == 0) report_timeout(p.status, 4, &abort_flag);
           break;
         }
         const uint32_t full = smem_u32(&bar_full[slot]);
-        mbar_expect_tx(full, C::kSlotBytes);
         const uint32_t dst = smem_u32(sKV + slot * C::kSlotBytes);
         const CUtensorMap* map = (u & 1) ? &vmap : &kmap;
+        if (elect_one()) {
+          mbar_expect_tx(full, C::kSlotBytes);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(dst + c * (BN * 128), map, c * 64, g, sg.kv_base + j * BN, full);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(dst + c * (BN * 128), map, c * 64, g, sg.kv_base + j * BN, full);
+        }
+        __syncwarp();
         last_round[slot] = round;
       }
       // Never leave with a copy in flight: wait for the last load of every slot.
       for (int s = 0; s < C::kSlots; ++s)
         if (last_round[s] >= 0)
           mbar_wait(smem_u32(&bar_full[s]), last_round[s] & 1, 1000000000ull, &zero_flag);
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The warp runs the loop so that descriptors stay warp-uniform; one elected
+    // lane (the same one every time, which also commits) issues the products.
+    {
+      constexpr unsigned kAll = 0xffffffffu;
       const uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
       const uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
-      auto fail = [&](unsigned site) { report_timeout(p.status, site, &abort_flag); };
+      auto fail = [&](unsigned site) {
+        if (lane == 0) report_timeout(p.status, site, &abort_flag);
+      };
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(kAll, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
+      };
       auto wait_full = [&](int u) -> bool {
-        return mbar_wait(smem_u32(&bar_full[u % C::kSlots]), (u / C::kSlots) & 1, p.wait_ns,
-                         &abort_flag);
+        return wait_all(smem_u32(&bar_full[u % C::kSlots]), (u / C::kSlots) & 1);
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (elect_one()) mma_commit(smem_u32(bar));
+        __syncwarp();
       };
       // Descriptors are built once; an MMA adds its byte offset / 16 to the
       // start-address field (shared addresses stay below 2^18, so it never
@@ -377,30 +395,36 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
       auto issue_s = [&](int t, int u) {
         const uint64_t a0 = dQ0 + (uint64_t)((t * C::kQBytes) >> 4);
         const uint64_t b0 = dK0 + (uint64_t)(((u % C::kSlots) * C::kSlotBytes) >> 4);
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + t * 256, a0 + off, b0 + off, idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + t * 256, a0 + off, b0 + off, idS, kk > 0);
+          }
+          mma_commit(smem_u32(&bar_s[t]));
         }
-        mma_commit(smem_u32(&bar_s[t]));
+        __syncwarp();
       };
       auto issue_pv = [&](int t, int u, bool acc) {
         const uint64_t v0 = dV0 + (uint64_t)(((u % C::kSlots) * C::kSlotBytes) >> 4);
         const uint32_t pa = tmem + t * 256, d = tmem + t * 256 + 128;
         // P of keys [64 h, 64 h + 64) sits over the first 32 of S's columns [64 h, 64 h + 64)
+        if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(d, pa + (kk >> 2) * 64 + (kk & 3) * 8, v0 + (uint64_t)((kk * 16 * 128) >> 4), idPV,
-                 (acc || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bar_o[t]));
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(d, pa + (kk >> 2) * 64 + (kk & 3) * 8, v0 + (uint64_t)((kk * 16 * 128) >> 4),
+                   idPV, (acc || kk > 0) ? 1u : 0u);
+          mma_commit(smem_u32(&bar_o[t]));
+        }
+        __syncwarp();
       };
       bool ok = true;
-      if (p.stall_test && !mbar_wait(smem_u32(&bar_never), 0, p.wait_ns, &abort_flag)) {
+      if (p.stall_test && !wait_all(smem_u32(&bar_never), 0)) {
         fail(10);
         ok = false;
       }
       for (int t = 0; t < 2 && ok; ++t)
-        if ((t ? nkv1 : nkv0) > 0 && !mbar_wait(smem_u32(&bar_q[t]), 0, p.wait_ns, &abort_flag)) {
+        if ((t ? nkv1 : nkv0) > 0 && !wait_all(smem_u32(&bar_q[t]), 0)) {
           fail(11);
           ok = false;
         }
@@ -412,7 +436,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           tc_fence_after();
           if (nkv0 > 0) issue_s(0, 0);
           if (nkv1 > 0) issue_s(1, 0);
-          mma_commit(smem_u32(&bar_empty[0]));
+          commit(&bar_empty[0]);
         }
       }
       for (int j = 0; j < nK && ok; ++j) {
@@ -425,7 +449,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t ? nkv1 : nkv0;
           if (j >= nt) continue;
-          if (!mbar_wait(smem_u32(&bar_p[t]), j & 1, p.wait_ns, &abort_flag)) {
+          if (!wait_all(smem_u32(&bar_p[t]), j & 1)) {
             fail(14 + t);
             ok = false;
             break;
@@ -443,11 +467,11 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&bar_empty[uV % C::kSlots]));
-        if (j + 1 < nK) mma_commit(smem_u32(&bar_empty[uK % C::kSlots]));
+        commit(&bar_empty[uV % C::kSlots]);
+        if (j + 1 < nK) commit(&bar_empty[uK % C::kSlots]);
       }
       // Never free TMEM under a running MMA: wait for everything issued.
-      mma_commit(smem_u32(&bar_drain));
+      commit(&bar_drain);
       mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
     }
   }
