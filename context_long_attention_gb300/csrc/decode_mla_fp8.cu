@@ -191,13 +191,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   // bar_full[s][q]: chunk group q of stage s (q < 4: dims [128q, 128q + 128);
   //   q = 4: the rope dims) holds its tile.
-  // bar_done[s]: the P.V of the tile in stage s has completed, and with it
-  //   every product that read the stage (one commit per tile: a commit holds
-  //   the issuing thread until the products before it finish, so the stage
-  //   is released whole rather than chunk by chunk).
+  // bar_done[s][mb]: P.V M-block mb of the tile in stage s has completed
+  //   (and every product issued before it), so chunk mb of the stage may be
+  //   refilled; mb = 3 also frees the rope chunk (it holds P_hi^T) and the
+  //   P_lo^T buffer.
   // bar_s[b]: S^T buffer b holds its tile's products.  bar_p: this tile's
   // P^T is written.  bar_q: the work item's query is in shared memory.
-  __shared__ __align__(8) uint64_t bar_full[2][5], bar_done[2], bar_s[2];
+  __shared__ __align__(8) uint64_t bar_full[2][5], bar_done[2][4], bar_s[2];
   __shared__ __align__(8) uint64_t bar_p, bar_q, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_full[s][q]), 1);
-      mbar_init(smem_u32(&bar_done[s]), 1);
+      for (int mb = 0; mb < 4; ++mb) mbar_init(smem_u32(&bar_done[s][mb]), 1);
       mbar_init(smem_u32(&bar_s[s]), 1);
     }
     mbar_init(smem_u32(&bar_p), kSoftmax);
@@ -264,14 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // paged: the pool rows of the tile's two 64-row halves, looked up once
           const long long yh[2] = {p.rm.table ? cache_row(j * kRows) : 0,
                                    p.rm.table ? cache_row(j * kRows + 64) : 0};
-          // the stage is free once the P.V of its previous tile (g - 2) has completed
-          if (g >= 2 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[s]), ((g >> 1) & 1) ^ 1,
-                                                           p.wait_ns, &abort_flag))) {
-            if (lane == 0) report_timeout(p.status, 1, &abort_flag);
-            ok = false;
-            break;
-          }
-          for (int q = 0; q < 5; ++q) {
+          for (int q = 0; q < 5 && ok; ++q) {
+            // chunk q < 4 of the stage is free once P.V M-block q of its previous
+            // tile (g - 2) has completed; the rope chunk once the whole P.V has
+            if (g >= 2 && q < 4 &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[s][q]), ((g >> 1) & 1) ^ 1,
+                                                   p.wait_ns, &abort_flag))) {
+              if (lane == 0) report_timeout(p.status, 1, &abort_flag);
+              ok = false;
+              break;
+            }
             const uint32_t full = smem_u32(&bar_full[s][q]);
             const uint32_t dst = stage + (q < 4 ? q * kChunkBytes : kRopeOff);
             const int x = 128 * q, row_bytes = q < 4 ? 128 : 64;
@@ -348,8 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T); the last block's
-      // commit releases the stage and P_lo^T's buffer.
+      // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T); each block's commit
+      // releases its chunk of the stage (block 3's also the rope chunk and
+      // P_lo^T's buffer).
       auto pv_block = [&](int gp, int mb, bool first) {
         const int s = gp & 1;
         const uint64_t av = (s ? dV[1] : dV[0]) + (uint64_t)((mb * kChunkBytes) >> 4);
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_f8(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || !first) ? 1u : 0u);
             mma_ss_f8(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
           }
-          if (mb == 3) mma_commit(smem_u32(&bar_done[s]));
+          mma_commit(smem_u32(&bar_done[s][mb]));
         }
         __syncwarp();
       };
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (j > 0) {
             // O^T holds the earlier tiles: once the last P.V has landed, scale its columns
-            const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1,
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1,
                                                                   p.wait_ns, &abort_flag));
             if (bar_red_or(1, kSoftmax, !landed)) {
               if (!landed) report_timeout(p.status, 6, &abort_flag);
@@ -617,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P_lo^T has one buffer: the previous tile's P.V must have read it
         if (g > 0) {
-          const bool freed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1,
+          const bool freed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1,
                                                                p.wait_ns, &abort_flag));
           if (bar_red_or(1, kSoftmax, !freed)) {
             if (!freed) report_timeout(p.status, 7, &abort_flag);
@@ -642,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- epilogue: column sums of l, O^T 2^-gs / l, LSE
       const bool landed = __all_sync(
-          0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, p.wait_ns, &abort_flag));
+          0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1, p.wait_ns, &abort_flag));
       if (bar_red_or(1, kSoftmax, !landed)) {
         if (!landed) report_timeout(p.status, 8, &abort_flag);
         ok = false;
