@@ -5,8 +5,9 @@ It only marshals arguments: PyTorch provides device memory and the current
 stream, and every step of the computation runs in the library's CUDA kernels.
 The functions keep the C names:
 
-    cp_shard_plan, cp_prefill_attn, cp_decode_plan, cp_kv_shard_pack,
-    cp_decode_attn, cp_lse_merge, cp_device_error_check
+    cp_shard_plan, cp_prefill_attn, cp_decode_plan, cp_decode_plan_ex,
+    cp_kv_shard_pack, cp_decode_attn, cp_lse_merge, cp_lse_fold,
+    cp_device_error_check
 
 There is no CPU fallback: importing the package loads the library, and
 raises if it has not been built (``__graft_entry__.build()``).
@@ -14,6 +15,8 @@ raises if it has not been built (``__graft_entry__.build()``).
 
 from ._binding import (  # noqa: F401
     CP_BF16,
+    CP_DCP_CONTIGUOUS,
+    CP_DCP_ROUND_ROBIN,
     CP_DECODE_GQA,
     CP_DECODE_MLA,
     CP_FP8_E4M3,
@@ -28,6 +31,7 @@ from ._binding import (  # noqa: F401
     cp_decode_attn_noalloc,
     cp_decode_attn_paged,
     cp_decode_plan,
+    cp_decode_plan_ex,
     cp_decode_workspace_size,
     cp_device_error_check,
     cp_kv_shard_pack,

@@ -15,6 +15,7 @@ lib_path = os.path.join(_HERE, "_lib", "libcpattn.so")
 CP_ZIGZAG, CP_INTERLEAVE = 0, 1
 CP_BF16, CP_FP32, CP_FP8_E4M3 = 0, 1, 2
 CP_DECODE_GQA, CP_DECODE_MLA = 0, 1
+CP_DCP_ROUND_ROBIN, CP_DCP_CONTIGUOUS = 0, 1
 _STATUS = {0: "CP_OK", -1: "CP_ERR_INVALID_ARG", -2: "CP_ERR_UNSUPPORTED", -3: "CP_ERR_CUDA",
            -4: "CP_ERR_DEVICE_TIMEOUT", -5: "CP_ERR_WORKSPACE"}
 MAX_SHARDS = 64
@@ -22,7 +23,7 @@ HEADER_WORDS = 24
 SEG_WORDS, PAIR_WORDS, WORK_WORDS = 12, 8, 4
 HEADER_FIELDS = ["magic", "kind", "C", "R", "T", "KV", "n_seg", "n_tiles", "off_rank", "off_req",
                  "off_seg", "off_tiles", "off_rtile", "off_idx", "off_qpos", "off_qreq",
-                 "host_words", "dev_words", "n_parts", "tile_rows", "n_split"]
+                 "host_words", "dev_words", "n_parts", "tile_rows", "n_split", "layout", "s_q"]
 SEG_FIELDS = ["rank", "req", "block", "which", "local_start", "count", "first_f", "stride",
               "q_start", "first_pos", "kv_len", "kv_base"]
 
@@ -48,6 +49,8 @@ _SIGS = {
     "cp_prefill_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp]),
     "cp_decode_plan_size": (_i, [_i, _i, _vp, _i, _szp, _szp]),
     "cp_decode_plan": (_i, [_i, _i, _vp, _i, _vp, _sz, _vp, _sz, _vp]),
+    "cp_decode_plan_ex_size": (_i, [_i, _i, _vp, _i, _i, _i, _szp, _szp]),
+    "cp_decode_plan_ex": (_i, [_i, _i, _vp, _i, _i, _i, _vp, _sz, _vp, _sz, _vp]),
     "cp_kv_shard_pack": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp]),
     "cp_decode_workspace_size": (_i, [_vp, _i, _i, _szp]),
     "cp_decode_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp,
@@ -189,6 +192,11 @@ class DecodePlan(_Plan):
         p = self.pairs
         return [int(p[r * self.R:(r + 1) * self.R, 0].sum()) for r in range(self.C)]
 
+    @property
+    def query_rows(self):
+        """Query rows per request (s_q; 1 unless planned for MTP)."""
+        return max(1, self.header.get("s_q", 1))
+
 
 def cp_plan_size(strategy: int, C: int, new_len, prefix_len):
     nl, pl = _i32(new_len), _i32(prefix_len)
@@ -246,6 +254,36 @@ def cp_decode_plan(C: int, ctx_len, n_workers: int = 0, device=None) -> DecodePl
     _check(lib.cp_decode_plan(C, len(cl), _np_ptr(cl), n_workers, _np_ptr(host), hb.value,
                               _ptr(dev), db.value, _stream(dev.device) if dev is not None else None))
     return DecodePlan(host, dev)
+
+
+def cp_decode_plan_ex(C: int, ctx_len, layout: int = 0, s_q: int = 1, n_workers: int = 0,
+                      device=None) -> DecodePlan:
+    """cp_decode_plan with a shard layout (CP_DCP_ROUND_ROBIN or
+    CP_DCP_CONTIGUOUS) and s_q query rows per request."""
+    cl = _i32(ctx_len)
+    hb, db = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib.cp_decode_plan_ex_size(C, len(cl), _np_ptr(cl), layout, s_q, n_workers,
+                                      ctypes.byref(hb), ctypes.byref(db)))
+    host = np.zeros(hb.value // 4, dtype=np.int32)
+    dev = None
+    if device is not None:
+        dev = torch.empty(db.value // 4, dtype=torch.int32, device=device)
+    _check(lib.cp_decode_plan_ex(C, len(cl), _np_ptr(cl), layout, s_q, n_workers, _np_ptr(host),
+                                 hb.value, _ptr(dev), db.value,
+                                 _stream(dev.device) if dev is not None else None))
+    return DecodePlan(host, dev)
+
+
+def _decode_shapes(plan, q):
+    """(lead, H, Dqk) of a decode query: lead = (B,) or (B, s_q) for MTP plans."""
+    s_q = plan.query_rows
+    if s_q > 1:
+        B, sq, H, Dqk = q.shape
+        if sq != s_q:
+            raise ValueError(f"q has {sq} query rows, the plan {s_q}")
+        return (B, s_q), H, Dqk
+    B, H, Dqk = q.shape
+    return (B,), H, Dqk
 
 
 def _ptr_array(ts):
@@ -317,7 +355,7 @@ def cp_decode_attn_paged(plan: DecodePlan, pages: PageTable, mode: int, q, k_poo
                          scale_pool=None, sm_scale=None, o_part=None, lse_part=None, ws=None):
     """cp_decode_attn over a paged pool (k_pool [pool_rows, 576] for MLA, or
     k_pool / v_pool [pool_rows, Hkv, D] for GQA)."""
-    B, H, Dqk = q.shape
+    lead, H, Dqk = _decode_shapes(plan, q)
     _need_cuda(q, k_pool)
     kp = k_pool.view(torch.uint8) if k_pool.dtype == torch.float8_e4m3fn else k_pool
     kv_dtype = _dtype_code(kp)
@@ -329,9 +367,9 @@ def cp_decode_attn_paged(plan: DecodePlan, pages: PageTable, mode: int, q, k_poo
         sm_scale = 1.0 / math.sqrt(Dqk)
     C = plan.C
     if o_part is None:
-        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+        o_part = torch.empty((C, *lead, H, Dv), dtype=torch.float32, device=q.device)
     if lse_part is None:
-        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+        lse_part = torch.empty((C, *lead, H), dtype=torch.float32, device=q.device)
     need = cp_decode_workspace_size(plan, H, Dv)
     if ws is None and need:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -355,8 +393,9 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
     """Per-shard partial decode attention.  MLA: q [B, H, 576] bf16,
     shard_k[r] [rows_r, 576] bf16 or fp8 codes (+ shard_scale[r]).
     GQA: q [B, Hq, D], shard_k[r]/shard_v[r] [rows_r, Hkv, D].
-    Returns (o_part [C, B, H, Dv] fp32, lse_part [C, B, H] fp32)."""
-    B, H, Dqk = q.shape
+    Returns (o_part [C, B, H, Dv] fp32, lse_part [C, B, H] fp32).  With an
+    MTP plan (s_q > 1) q is [B, s_q, H, Dqk] and the outputs [C, B, s_q, ...]."""
+    lead, H, Dqk = _decode_shapes(plan, q)
     _need_cuda(q, *[t for t in shard_k if t is not None])
     sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in shard_k]
     kv_dtype = _dtype_code(sk[0]) if sk else CP_BF16
@@ -368,9 +407,9 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
         sm_scale = 1.0 / math.sqrt(Dqk)
     C = plan.C
     if o_part is None:
-        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+        o_part = torch.empty((C, *lead, H, Dv), dtype=torch.float32, device=q.device)
     if lse_part is None:
-        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+        lse_part = torch.empty((C, *lead, H), dtype=torch.float32, device=q.device)
     need = cp_decode_workspace_size(plan, H, Dv)
     if ws is None and need:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -388,7 +427,7 @@ def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None
     """cp_decode_attn without a workspace argument: the split-KV scratch is a
     fixed library-owned device array (NOALLOC_SCRATCH_BYTES).  Calls must not
     overlap on the GPU."""
-    B, H, Dqk = q.shape
+    lead, H, Dqk = _decode_shapes(plan, q)
     _need_cuda(q, *[t for t in shard_k if t is not None])
     sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in shard_k]
     kv_dtype = _dtype_code(sk[0]) if sk else CP_BF16
@@ -400,9 +439,9 @@ def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None
         sm_scale = 1.0 / math.sqrt(Dqk)
     C = plan.C
     if o_part is None:
-        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+        o_part = torch.empty((C, *lead, H, Dv), dtype=torch.float32, device=q.device)
     if lse_part is None:
-        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+        lse_part = torch.empty((C, *lead, H), dtype=torch.float32, device=q.device)
     _check(lib.cp_decode_attn_noalloc(
         _np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q), _ptr_array(sk),
         _ptr_array(shard_v) if shard_v is not None else None,

@@ -238,15 +238,20 @@ cp_status sm_count(int* n) {
   return CP_OK;
 }
 
-cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers,
-                            DecodeBuild* out) {
+cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, int s_q,
+                            int n_workers, DecodeBuild* out) {
   if (C < 1 || C > CP_MAX_SHARDS) return fail(CP_ERR_INVALID_ARG, "C=%d outside [1, %d]", C, CP_MAX_SHARDS);
   if (B < 1) return fail(CP_ERR_INVALID_ARG, "B=%d must be >= 1", B);
   if (!ctx_len) return fail(CP_ERR_INVALID_ARG, "ctx_len is NULL");
   if (n_workers < 0) return fail(CP_ERR_INVALID_ARG, "n_workers=%d < 0", n_workers);
+  if (layout != CP_DCP_ROUND_ROBIN && layout != CP_DCP_CONTIGUOUS)
+    return fail(CP_ERR_INVALID_ARG, "layout=%d is not a cp_dcp_layout", layout);
+  if (s_q < 1 || s_q > 64) return fail(CP_ERR_INVALID_ARG, "s_q=%d outside [1, 64]", s_q);
   long long total = 0;
   for (int b = 0; b < B; ++b) {
     if (ctx_len[b] < 0) return fail(CP_ERR_INVALID_ARG, "ctx_len[%d] < 0", b);
+    if (s_q > 1 && ctx_len[b] < s_q)
+      return fail(CP_ERR_INVALID_ARG, "ctx_len[%d]=%d < s_q=%d query rows", b, ctx_len[b], s_q);
     total += ctx_len[b];
   }
   if (total >= (1LL << 31) - 1) return fail(CP_ERR_INVALID_ARG, "total tokens %lld >= 2^31", total);
@@ -262,13 +267,25 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers,
     int off = 0;
     for (int b = 0; b < B; ++b) {
       const int L = ctx_len[b];
-      const int rows = L > r ? (L - r + C - 1) / C : 0;  // tokens p = r, r+C, ...
+      int rows, tok0, step;
+      if (layout == CP_DCP_ROUND_ROBIN) {  // tokens p = r, r + C, ...
+        rows = L > r ? (L - r + C - 1) / C : 0;
+        tok0 = r;
+        step = C;
+      } else {  // one chunk; the first L mod C chunks one token longer
+        const int q = L / C, m = L % C;
+        rows = q + (r < m ? 1 : 0);
+        tok0 = r * q + std::min(r, m);
+        step = 1;
+      }
       cp_pair_desc& d = pair[r * B + b];
       memset(&d, 0, sizeof(d));
       d.rows = rows;
       d.row_off = off;
       d.ctx_len = L;
       d.first_part = -1;
+      d.tok0 = tok0;
+      d.tok_step = step;
       off += rows;
     }
   }
@@ -333,6 +350,8 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers,
   h.n_parts = n_parts;
   h.n_split = (int)split.size();
   h.tile_rows = TR;
+  h.layout = layout;
+  h.s_q = s_q;
   int w = align4(kHeaderWords);
   h.off_rank = w;
   w = align4(w + kPairWords * P);
@@ -458,12 +477,13 @@ cp_status check_pages(const cp_plan_header& h, const int32_t* W, const int32_t* 
 }
 
 cp_status check_decode_shapes(cp_decode_mode mode, cp_dtype kv_dtype, bool has_v, bool has_scale,
-                              int Hq, int Hkv, int Dqk, int Dv, float sm_scale) {
+                              int Hq, int Hkv, int Dqk, int Dv, float sm_scale, int s_q) {
   if (!(sm_scale > 0.f)) return fail(CP_ERR_INVALID_ARG, "sm_scale must be > 0");
   if (mode != CP_DECODE_MLA && mode != CP_DECODE_GQA) return fail(CP_ERR_INVALID_ARG, "bad mode");
   if (mode == CP_DECODE_MLA) {
     if (Dqk != 576 || Dv != 512 || Hkv != 1) return fail(CP_ERR_UNSUPPORTED, "MLA needs Dqk=576, Dv=512, Hkv=1");
-    if (Hq < 1 || Hq > 64) return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d outside [1, 64]", Hq);
+    if (Hq < 1 || Hq * s_q > 64)
+      return fail(CP_ERR_UNSUPPORTED, "MLA Hq=%d x s_q=%d query rows outside [1, 64]", Hq, s_q);
     if (kv_dtype != CP_BF16 && kv_dtype != CP_FP8_E4M3) return fail(CP_ERR_UNSUPPORTED, "MLA cache must be bf16 or fp8");
     if (has_v) return fail(CP_ERR_INVALID_ARG, "MLA takes values from the latent: shard_v must be NULL");
     if ((kv_dtype == CP_FP8_E4M3) != has_scale)
@@ -484,11 +504,12 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
                      const ScalePtrs& S, const long long* shard_rows, const RowMap& rm, int Hq,
                      int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
                      void* ws, size_t ws_bytes, void* stream) {
-  size_t need = (size_t)h.n_parts * Hq * (Dv + 1) * sizeof(float);
+  const int Hc = Hq * plan_s_q(h);  // query rows x heads: the kernels' head columns
+  size_t need = (size_t)h.n_parts * Hc * (Dv + 1) * sizeof(float);
   if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   if (need && !aligned16(ws)) return fail(CP_ERR_INVALID_ARG, "ws is not 16-byte aligned");
   float* ws_o = (float*)ws;
-  float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hq * Dv : nullptr;
+  float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hc * Dv : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   const bool mla = mode == CP_DECODE_MLA;
   cudaError_t e =
@@ -501,7 +522,7 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
                                  Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
   if (h.n_split) {
-    e = launch_decode_fixup((const int32_t*)dev_plan, h, Hq, Dv, ws_o, ws_lse, o_part, lse_part, s);
+    e = launch_decode_fixup((const int32_t*)dev_plan, h, Hc, Dv, ws_o, ws_lse, o_part, lse_part, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split merge kernel");
   }
   return ok();
@@ -600,16 +621,37 @@ cp_status cp_decode_plan_size(int C, int B, const int32_t* ctx_len, int n_worker
                               size_t* host_bytes, size_t* dev_bytes) {
   if (!host_bytes || !dev_bytes) return fail(CP_ERR_INVALID_ARG, "size outputs are NULL");
   DecodeBuild b;
-  cp_status st = build_decode_plan(C, B, ctx_len, n_workers, &b);
+  cp_status st = build_decode_plan(C, B, ctx_len, CP_DCP_ROUND_ROBIN, 1, n_workers, &b);
   if (st != CP_OK) return st;
   *host_bytes = *dev_bytes = b.words.size() * 4;
   return ok();
 }
 
+cp_status cp_decode_plan_ex_size(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
+                                 int n_workers, size_t* host_bytes, size_t* dev_bytes) {
+  if (!host_bytes || !dev_bytes) return fail(CP_ERR_INVALID_ARG, "size outputs are NULL");
+  DecodeBuild b;
+  cp_status st = build_decode_plan(C, B, ctx_len, (int)layout, s_q, n_workers, &b);
+  if (st != CP_OK) return st;
+  *host_bytes = *dev_bytes = b.words.size() * 4;
+  return ok();
+}
+
+cp_status cp_decode_plan_ex(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
+                            int n_workers, void* host_plan, size_t host_bytes, void* dev_plan,
+                            size_t dev_bytes, void* stream) {
+  DecodeBuild b;
+  cp_status st = build_decode_plan(C, B, ctx_len, (int)layout, s_q, n_workers, &b);
+  if (st != CP_OK) return st;
+  st = copy_plan(b.words, host_plan, host_bytes, dev_plan, dev_bytes, b.words.size() * 4,
+                 (cudaStream_t)stream);
+  return st == CP_OK ? ok() : st;
+}
+
 cp_status cp_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers, void* host_plan,
                          size_t host_bytes, void* dev_plan, size_t dev_bytes, void* stream) {
   DecodeBuild b;
-  cp_status st = build_decode_plan(C, B, ctx_len, n_workers, &b);
+  cp_status st = build_decode_plan(C, B, ctx_len, CP_DCP_ROUND_ROBIN, 1, n_workers, &b);
   if (st != CP_OK) return st;
   st = copy_plan(b.words, host_plan, host_bytes, dev_plan, dev_bytes, b.words.size() * 4,
                  (cudaStream_t)stream);
@@ -660,7 +702,7 @@ cp_status cp_decode_workspace_size(const void* host_plan, int H, int Dv, size_t*
   cp_status st = read_header(host_plan, 2, &h);
   if (st != CP_OK) return st;
   if (!bytes || H < 1 || Dv < 1) return fail(CP_ERR_INVALID_ARG, "bad arguments");
-  *bytes = (size_t)h.n_parts * H * (Dv + 1) * sizeof(float);
+  *bytes = (size_t)h.n_parts * H * plan_s_q(h) * (Dv + 1) * sizeof(float);
   return ok();
 }
 
@@ -676,7 +718,7 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
   if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o_part) || !aligned16(lse_part))
     return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
   st = check_decode_shapes(mode, kv_dtype, shard_v != nullptr, shard_scale != nullptr, Hq, Hkv, Dqk,
-                           Dv, sm_scale);
+                           Dv, sm_scale, plan_s_q(h));
   if (st != CP_OK) return st;
   ShardPtrs K, V;
   ScalePtrs S;
@@ -720,7 +762,7 @@ cp_status cp_decode_attn_paged(const void* host_plan, const void* dev_plan, cp_d
       !aligned16(k_pool) || (v_pool && !aligned16(v_pool)))
     return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
   st = check_decode_shapes(mode, kv_dtype, v_pool != nullptr, scale_pool != nullptr, Hq, Hkv, Dqk,
-                           Dv, sm_scale);
+                           Dv, sm_scale, plan_s_q(h));
   if (st != CP_OK) return st;
   RowMap rm;
   st = check_pages(h, (const int32_t*)host_plan, host_page_table, max_pages, page_size, num_pages,

@@ -74,7 +74,8 @@ struct Params {
   ShardPtrs k;  // code arrays (for the L2 prefetch; the tiles come through the tensor maps)
   ScalePtrs sc;
   RowMap rm;    // paged cache: 64-row boxes of a pool, rows through the page table
-  int H;
+  int H;        // columns = s_q query rows x Hrow heads (<= 64)
+  int Hrow, s_q;
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
   float* lse_part;
@@ -161,6 +162,7 @@ __device__ void report_timeout(unsigned* status, unsigned site, volatile int* ab
 struct Item {
   int r, b, nrows, ntiles;
   int pair, row_begin, pair_rows;  // the pair, the item's first row in it, the pair's rows
+  int tok0, tok_step, ctx_len;     // token of the pair's row i = tok0 + i tok_step; L
   long long row0;  // first shard row (contiguous caches)
   float* out_o;
   float* out_l;
@@ -177,6 +179,9 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   it.pair = wd.pair;
   it.row_begin = wd.row_begin;
   it.pair_rows = pd.rows;
+  it.tok0 = pd.tok0;
+  it.tok_step = pd.tok_step;
+  it.ctx_len = pd.ctx_len;
   it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
                          : p.ws_o + (long long)wd.part * p.H * kDv;
   it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
@@ -505,6 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < it.ntiles; ++j, ++g) {
         const int row = j * kRows + t;
         const bool valid = row < it.nrows;
+        // Several query rows (s_q > 1): query row qi reads tokens up to
+        // L - s_q + qi, so this cache row is masked for columns [0, mcols).
+        const int tok = it.tok0 + (it.row_begin + row) * it.tok_step;
+        const int mcols = min(kHeads, max(0, tok - (it.ctx_len - p.s_q)) * p.Hrow);
         const float scale =
             !valid ? 0.f
                    : p.rm.table ? __ldg(p.sc.p[0] + map_row(p.rm, it.pair, 0, it.row_begin + row))
@@ -536,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int h = 16 * half + 4 * h4 + e;
-              u[h] = valid ? fmaf(__uint_as_float(a[4 * h4 + e]) + __uint_as_float(z[4 * h4 + e]), c, -mm[e])
+              u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[4 * h4 + e]) + __uint_as_float(z[4 * h4 + e]), c, -mm[e])
                            : -INFINITY;
               over = fmaxf(over, u[h]);
             }
@@ -563,7 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tid < kHeads) {
             const float cm = fmaxf(fmaxf(unordered(sRed[0][tid]), unordered(sRed[1][tid])),
                                    fmaxf(unordered(sRed[2][tid]), unordered(sRed[3][tid])));
-            const float delta = (j == 0 || cm > kRescaleLog2) ? cm : 0.f;
+            // (a column with no unmasked row in the item's first tile has none
+            // in the item: rows go up in token order; it keeps max 0, weight 0)
+            const float delta = j == 0 ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
             sDelta[tid] = delta;
             sM[tid] += delta;
           }
@@ -663,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < kHeads) {
         const float tot = __int_as_float(sRed[0][tid]) + __int_as_float(sRed[1][tid]) +
                           __int_as_float(sRed[2][tid]) + __int_as_float(sRed[3][tid]);
-        sDelta[tid] = 1.f / tot;
-        if (tid < p.H) it.out_l[tid] = (sM[tid] + lg2(tot)) * kLn2;
+        sDelta[tid] = tot > 0.f ? 1.f / tot : 0.f;
+        if (tid < p.H) it.out_l[tid] = tot > 0.f ? (sM[tid] + lg2(tot)) * kLn2 : -INFINITY;
       }
       named_bar_sync(1, kSoftmax);
       const float og = pow2i(-gs);
@@ -707,7 +718,9 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
   p.k = k;
   p.sc = sc;
   p.rm = rm;
-  p.H = H;
+  p.s_q = plan_s_q(h);
+  p.Hrow = H;
+  p.H = H * p.s_q;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
   p.lse_part = lse_part;

@@ -61,7 +61,8 @@ struct Params {
   const __nv_bfloat16* q;
   ShardPtrs k;
   RowMap rm;  // paged cache: 64-row boxes of a pool, rows through the page table
-  int H;
+  int H;             // columns = s_q query rows x Hrow heads (<= 64)
+  int Hrow, s_q;
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
   float* lse_part;
@@ -277,6 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         const bool valid = j * kRows + t < nrows;
+        // Several query rows (s_q > 1): row qi of the request reads tokens up
+        // to L - s_q + qi, so this cache row is masked for the columns of the
+        // query rows qi < tok - (L - s_q), columns [0, mcols).
+        const int tok = pd.tok0 + (wd.row_begin + j * kRows + t) * pd.tok_step;
+        const int mcols = min(kHeads, max(0, tok - (pd.ctx_len - p.s_q)) * p.Hrow);
         const float cj = p.scale_log2;  // scores in log2 units
         // The four softmax warps leave together: a warp that gave up still
         // meets the others at the named barrier of this vote.
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
             const int hh = 32 * half + h;
-            u[hh] = valid ? fmaf(__uint_as_float(a[h]), cj, -sM[hh]) : -INFINITY;
+            u[hh] = valid && hh >= mcols ? fmaf(__uint_as_float(a[h]), cj, -sM[hh]) : -INFINITY;
             over = fmaxf(over, u[hh]);
           }
         }
@@ -317,7 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    fmaxf(unordered(sRed[2][t]), unordered(sRed[3][t])));
             // move the running max to this tile's max on the first tile, or when it
             // grew by more than 2^8; earlier sums and O^T shrink by 2^-delta
-            const float delta = (j == 0 || cm > kRescaleLog2) ? cm : 0.f;
+            // (a column with no unmasked row in the item's first tile has none in
+            // the item: rows go up in token order; it keeps max 0 and weight 0)
+            const float delta = j == 0 ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
             sAlpha[t] = j == 0 ? 0.f : ex2(-delta);
             sDelta[t] = delta;
             sM[t] += delta;
@@ -407,14 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int hh = 32 * half + h;
               if (hh < p.H) {
                 const float tot = sL[0][hh] + sL[1][hh] + sL[2][hh] + sL[3][hh];
-                out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) / tot;
+                out_o[(long long)hh * kDv + 128 * mb + t] = tot > 0.f ? __uint_as_float(a[h]) / tot : 0.f;
               }
             }
           }
         }
         if (t < p.H) {
           const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
-          out_l[t] = (sM[t] + lg2(tot)) * kLn2;
+          out_l[t] = tot > 0.f ? (sM[t] + lg2(tot)) * kLn2 : -INFINITY;
         }
       }
     }
@@ -453,7 +461,9 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = k;
   p.rm = rm;
-  p.H = H;
+  p.s_q = plan_s_q(h);
+  p.Hrow = H;
+  p.H = H * p.s_q;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
   p.lse_part = lse_part;

@@ -16,6 +16,9 @@ constexpr int kWorkWords = (int)(sizeof(cp_work_desc) / 4);
 constexpr int kPrefillTileRows = 256;  // queries per prefill tile (two 128-row MMA tiles)
 constexpr int kDecodeTileRows = 128;   // KV rows per decode scheduling tile (MMA M)
 
+// Query rows per request of a decode plan (plans without the field have one).
+inline int plan_s_q(const cp_plan_header& h) { return h.s_q > 0 ? h.s_q : 1; }
+
 // Device status word layout (written by kernels, read by cp_device_error_check).
 //   [0] non-zero once any bounded wait gave up
 //   [1] kernel id   [2] wait site   [3] block index

@@ -35,7 +35,7 @@ __global__ void kv_pack_kernel(const int32_t* __restrict__ plan, int C, int B, i
                                int off_pair, int off_req, const uint4* __restrict__ kv,
                                const float* __restrict__ kv_scale, int row_vec,
                                MutShardPtrs dst, MutScalePtrs dst_scale, int has_scale,
-                               RowMap rm) {
+                               RowMap rm, int layout) {
   const int warps = blockDim.x >> 5;
   const long long t = (long long)blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -48,9 +48,17 @@ __global__ void kv_pack_kernel(const int32_t* __restrict__ plan, int C, int B, i
   }
   const int b = lo;
   const int p = (int)(t - req[2 * b + 1]);
-  const int r = p % C;
+  int r, i;  // shard and shard row of token p
+  if (layout == CP_DCP_ROUND_ROBIN) {
+    r = p % C;
+    i = p / C;
+  } else {  // chunks of q + 1 tokens for shards r < m, then of q tokens
+    const int L = req[2 * b], q = L / C, m = L % C, big = m * (q + 1);
+    r = p < big ? p / (q + 1) : m + (p - big) / q;
+    i = p < big ? p % (q + 1) : (p - big) % q;
+  }
   const cp_pair_desc* pair = reinterpret_cast<const cp_pair_desc*>(plan + off_pair);
-  const long long row = map_row(rm, r * B + b, pair[r * B + b].row_off, p / C);
+  const long long row = map_row(rm, r * B + b, pair[r * B + b].row_off, i);
   const uint4* src = kv + t * row_vec;
   uint4* out = static_cast<uint4*>(dst.p[r]) + row * row_vec;
   for (int c = lane; c < row_vec; c += 32) out[c] = src[c];
@@ -194,7 +202,7 @@ cudaError_t launch_kv_pack(const int32_t* dev_plan, const cp_plan_header& h, int
   kv_pack_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(dev_plan, h.C, h.R, h.T, h.off_rank,
                                                          h.off_tiles, static_cast<const uint4*>(kv),
                                                          kv_scale, row_vec, dst, dst_scale,
-                                                         has_scale ? 1 : 0, rm);
+                                                         has_scale ? 1 : 0, rm, h.layout);
   return cudaGetLastError();
 }
 

@@ -95,14 +95,17 @@ template <typename T, int ND>
 __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                                        int off_worker, int off_work, const T* __restrict__ q,
                                        ShardPtrs kp, ShardPtrs vp, RowMap rm, int Hq, int Hkv,
-                                       float sm_scale,
+                                       int s_q, float sm_scale,
                                        float* __restrict__ o_part, float* __restrict__ lse_part,
                                        float* __restrict__ ws_o, float* __restrict__ ws_lse) {
   constexpr int D = ND * 32;
   const int lane = threadIdx.x & 31;
+  // Column h = query row qi x Hq + head: a request's s_q query rows side by side.
+  const int Hc = Hq * s_q;
   const int h = blockIdx.y * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (h >= Hq) return;
-  const int g = h / (Hq / Hkv);
+  if (h >= Hc) return;
+  const int qi = h / Hq;
+  const int g = (h % Hq) / (Hq / Hkv);
   const int w0 = plan[off_worker + blockIdx.x], w1 = plan[off_worker + blockIdx.x + 1];
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(plan + off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(plan + off_work);
@@ -112,11 +115,16 @@ __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, 
     const cp_pair_desc pd = pairs[wd.pair];
     float qv[ND];
 #pragma unroll
-    for (int e = 0; e < ND; ++e) qv[e] = ld_elem(q, ((long long)b * Hq + h) * D + lane + 32 * e);
+    for (int e = 0; e < ND; ++e) qv[e] = ld_elem(q, ((long long)b * Hc + h) * D + lane + 32 * e);
+    // Query row qi reads the tokens up to position L - s_q + qi: the pair's
+    // rows hold tokens tok0 + i tok_step in increasing order, so a prefix.
+    const int lim = pd.ctx_len - s_q + qi;
+    const int n_valid = lim < pd.tok0 ? 0 : min(pd.rows, (lim - pd.tok0) / pd.tok_step + 1);
+    const int row_end = min(wd.row_end, n_valid);
     const T* kb = static_cast<const T*>(kp.p[r]);
     const T* vb = static_cast<const T*>(vp.p[r]);
     RowState<ND> st;
-    for (int row = wd.row_begin; row < wd.row_end; ++row) {
+    for (int row = wd.row_begin; row < row_end; ++row) {
       const long long kr = (map_row(rm, wd.pair, pd.row_off, row) * Hkv + g) * D + lane;
       float part = 0.f, vv[ND];
 #pragma unroll
@@ -129,11 +137,11 @@ __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, 
     float* ob;
     float* lb;
     if (wd.part < 0) {
-      ob = o_part + ((long long)wd.pair * Hq + h) * D;
-      lb = lse_part + (long long)wd.pair * Hq + h;
+      ob = o_part + ((long long)wd.pair * Hc + h) * D;
+      lb = lse_part + (long long)wd.pair * Hc + h;
     } else {
-      ob = ws_o + ((long long)wd.part * Hq + h) * D;
-      lb = ws_lse + (long long)wd.part * Hq + h;
+      ob = ws_o + ((long long)wd.part * Hc + h) * D;
+      lb = ws_lse + (long long)wd.part * Hc + h;
     }
     const bool empty = st.l == 0.f;
     const float inv = empty ? 0.f : 1.f / st.l;
@@ -163,10 +171,11 @@ cudaError_t decode_gqa_t(const int32_t* plan, const cp_plan_header& h, const voi
                          float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                          cudaStream_t s) {
   const int warps = 4;
-  dim3 grid(h.n_tiles, (Hq + warps - 1) / warps);
+  const int s_q = plan_s_q(h);
+  dim3 grid(h.n_tiles, (Hq * s_q + warps - 1) / warps);
   decode_gqa_simt_kernel<T, ND><<<grid, warps * 32, 0, s>>>(
       plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, rm, Hq, Hkv,
-      sm_scale, o_part, lse_part, ws_o, ws_lse);
+      s_q, sm_scale, o_part, lse_part, ws_o, ws_lse);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,11 @@ typedef enum {
 typedef enum { CP_ZIGZAG = 0, CP_INTERLEAVE = 1 } cp_strategy;
 typedef enum { CP_BF16 = 0, CP_FP32 = 1, CP_FP8_E4M3 = 2 } cp_dtype;
 typedef enum { CP_DECODE_GQA = 0, CP_DECODE_MLA = 1 } cp_decode_mode;
+/* Which decode shard holds token p of a request of L cached tokens. */
+typedef enum {
+  CP_DCP_ROUND_ROBIN = 0, /* shard p mod C, row p / C ([CTX] §3.1; [V4] §5) */
+  CP_DCP_CONTIGUOUS = 1   /* C consecutive chunks, the first L mod C one token longer ([DCP] §4) */
+} cp_dcp_layout;
 
 /* ---------------------------------------------------------------------------
  * Plan layout.  A plan is an array of int32 words: a cp_plan_header, then
@@ -94,7 +99,9 @@ typedef struct {
   int32_t n_parts;    /* decode: partial slots in the workspace (split pairs) */
   int32_t tile_rows;  /* decode: KV rows per scheduling tile (work boundaries) */
   int32_t n_split;    /* decode: pairs covered by more than one work item */
-  int32_t reserved[3];
+  int32_t layout;     /* decode: cp_dcp_layout of the token shards */
+  int32_t s_q;        /* decode: query rows per request (1, or more for MTP) */
+  int32_t reserved;
 } cp_plan_header;
 /* Decode plans reuse the table offsets: off_tiles -> int32 [R][2]
  * {ctx_len, first token of the request in the token-ordered cache};
@@ -134,12 +141,14 @@ typedef struct {
 
 /* Decode: one (shard r, request b) pair; pair index = r * R + b. */
 typedef struct {
-  int32_t rows;       /* tokens of request b stored on shard r = ceil((L_b - r) / C) */
+  int32_t rows;       /* tokens of request b stored on shard r (round robin: ceil((L_b - r) / C)) */
   int32_t row_off;    /* first row of request b in shard r's cache */
   int32_t ctx_len;    /* L_b, the request's cached tokens */
   int32_t n_parts;    /* work items that cover this pair (>1: merged from the workspace) */
   int32_t first_part; /* first workspace slot of this pair when n_parts > 1, else -1 */
-  int32_t reserved[3];
+  int32_t tok0;       /* token (position in the request) of the pair's row 0 */
+  int32_t tok_step;   /* token distance between consecutive rows: C or 1 */
+  int32_t reserved;
 } cp_pair_desc;
 
 /* Decode: a contiguous row range of one pair, processed by one worker. */
@@ -242,6 +251,38 @@ cp_status cp_decode_plan(int C, int B, const int32_t* ctx_len, int n_workers, vo
                          size_t host_bytes, void* dev_plan, size_t dev_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * cp_decode_plan_ex — cp_decode_plan with a choice of shard layout and
+ * several query rows per request.
+ *
+ * layout CP_DCP_ROUND_ROBIN is cp_decode_plan's map.  CP_DCP_CONTIGUOUS
+ *   gives shard r one chunk of consecutive tokens (the example of [DCP] §4:
+ *   four GPUs holding tokens 0-50K, 50K-100K, ... of one request): with
+ *   L = C q + m, shards r < m hold
+ *   q + 1 tokens and the others q, in token order, so token p of shard r sits
+ *   at row p - (r q + min(r, m)).  The merged result is the same for both
+ *   layouts (the exact combine does not depend on the partition).
+ * s_q >= 1 query rows per request ([V4] §2.2: MTP or speculative decode
+ *   raises the query rows per request above one).  Query row i of request b
+ *   stands at position L_b - s_q + i and reads the cached tokens 0 ..
+ *   L_b - s_q + i (the s_q new tokens are already in the cache, the last
+ *   one read by the last row only); every request then needs L_b >= s_q.
+ *   cp_decode_attn takes q [B, s_q, H, Dqk] and writes o_part
+ *   [C, B, s_q, H, Dv], lse_part [C, B, s_q, H]; the MLA kernels treat the
+ *   s_q H query rows as their columns (s_q H <= 64) and read each cache row
+ *   once for all of them.
+ * Shard sizes per pair, the split-KV schedule and the pack map follow the
+ *   layout; cp_kv_shard_pack(_paged) and the paged entry points accept
+ *   these plans unchanged.
+ * Errors: CP_ERR_INVALID_ARG for a layout outside the enum, s_q < 1 or
+ *   s_q > 64, or a request with L_b < s_q when s_q > 1.
+ * ------------------------------------------------------------------------- */
+cp_status cp_decode_plan_ex_size(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
+                                 int n_workers, size_t* host_bytes, size_t* dev_bytes);
+cp_status cp_decode_plan_ex(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
+                            int n_workers, void* host_plan, size_t host_bytes, void* dev_plan,
+                            size_t dev_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * cp_kv_shard_pack — copy a token-ordered cache into its token shards
  * (the decode side's store of [CTX] §5 case C: each decode GPU keeps only the
  * tokens it owns).
@@ -264,7 +305,11 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  * (O_r, LSE_r); merging the C partials with cp_lse_merge gives the
  * attention over the whole cache ([CTX] §3.3; [V4] §5).
  *
+ * With a plan of s_q > 1 query rows (cp_decode_plan_ex) q is [B, s_q, H, Dqk]
+ * and the outputs [C, B, s_q, H, ...]: below, read B as B s_q rows.
+ *
  * mode CP_DECODE_MLA: one latent KV head shared by all H <= 64 query heads
+ *   (s_q H <= 64)
  *   ([CTX] §1.3; [DCP] §5.3), on the tensor cores.  Dqk = 576, Dv = 512,
  *   Hkv = 1: keys are the whole
  *   576-dim entry, values its first 512 dims ([GLM] footnote 1).

@@ -189,6 +189,29 @@ def decode_shard_map(ctx_len: int, C: int) -> tuple[list[int], list[int]]:
     return shard, row
 
 
+def decode_shard_map_contiguous(ctx_len: int, C: int) -> tuple[list[int], list[int]]:
+    """Owner shard and row of every cached token when each shard holds one
+    chunk of consecutive positions.
+
+    vLLM's Decode Context Parallelism post, §4 "What is DCP?": each GPU keeps
+    the cache of a contiguous range of token positions (its example puts a
+    200K-token request on four GPUs, 50K positions each).  Where L is not a
+    multiple of C the reading taken is that the first L mod C chunks hold one
+    token more.  Enumerated: walk the tokens in order and fill chunk r to its
+    size before starting chunk r + 1.
+    """
+    sizes = [ctx_len // C + (1 if r < ctx_len % C else 0) for r in range(C)]
+    shard, row = [], []
+    r, i = 0, 0
+    for _ in range(ctx_len):
+        while i == sizes[r]:
+            r, i = r + 1, 0
+        shard.append(r)
+        row.append(i)
+        i += 1
+    return shard, row
+
+
 def paged_token_rows(ctx_len, C: int, page_table, page_size: int) -> list[tuple[int, int, int]]:
     """Pool row of every cached token when the shards' rows are kept in pages.
 
@@ -428,6 +451,34 @@ def decode_shard_partials(q: np.ndarray, kcache: np.ndarray, vcache: np.ndarray,
         outs.append(o)
         lses.append(lse)
     return np.stack(outs), np.stack(lses)
+
+
+def query_rows_partials(q_rows: np.ndarray, kcache: np.ndarray, vcache: np.ndarray, C: int,
+                        sm_scale: float, contiguous: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Per-shard partials of one request with several query rows.
+
+    [V4] §2.2: multi-token prediction or speculative decoding gives a decode
+    step a small number s_q of query rows per request instead of one.  The
+    reading taken: the rows are the request's last s_q positions, so row i
+    stands at position L - s_q + i and reads the tokens 0 .. L - s_q + i
+    (causal among themselves, as in prefill).  Shard r's key set for row i is
+    its own tokens (round robin, or contiguous chunks) up to that position.
+
+    q_rows [s_q, H, Dqk]; caches as decode_attention.
+    Returns O [C, s_q, H, Dv], LSE [C, s_q, H].
+    """
+    L, s_q = kcache.shape[0], q_rows.shape[0]
+    shard, _ = (decode_shard_map_contiguous if contiguous else decode_shard_map)(L, C)
+    shard = np.asarray(shard)
+    outs = np.empty((C, s_q, q_rows.shape[1], vcache.shape[2]))
+    lses = np.empty((C, s_q, q_rows.shape[1]))
+    for r in range(C):
+        for i in range(s_q):
+            last = L - s_q + i  # the row's own position
+            keys = [p for p in range(L) if shard[p] == r and p <= last]
+            outs[r, i], lses[r, i] = decode_attention(q_rows[i], kcache, vcache, sm_scale,
+                                                      keys=np.asarray(keys, dtype=np.int64))
+    return outs, lses
 
 
 def designated_partials(q: np.ndarray, kmain: np.ndarray, vmain: np.ndarray, kwin: np.ndarray,

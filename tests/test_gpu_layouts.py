@@ -1,0 +1,162 @@
+"""GPU parity of the contiguous-chunk decode layout (vLLM DCP post §4) and
+of decode steps with several query rows per request ("DeepSeek-V4 Attention
+Inference Systems" §2.2, MTP / speculative decode), against the oracle:
+the pack bit-exact, every shard's partial (O, LSE) and the merged result."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import cp_workloads as W
+import oracle
+from test_gpu_paged import make_pages
+from test_gpu_parity import DEV, TOL_BF16, TOL_FP8, check_lse, check_o, cp, np64  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+
+def token_map(L, C, contiguous):
+    return (oracle.decode_shard_map_contiguous if contiguous else oracle.decode_shard_map)(L, C)
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+def test_pack_bit_exact(cp, contiguous):
+    ctx = [0, 1, 7, 129, 1000, 4099]
+    C = 8
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    T = sum(ctx)
+    kv = torch.randint(0, 255, (T, 576), dtype=torch.uint8, device=DEV, generator=g)
+    sc = torch.rand(T, device=DEV, generator=g)
+    shards, scales = cp.cp_kv_shard_pack(plan, kv, sc)
+    kvh, sch = kv.cpu().numpy(), sc.cpu().numpy()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    off = [0] * C
+    for b, L in enumerate(ctx):
+        shard, row = token_map(L, C, contiguous)
+        for r in range(C):
+            toks = [p for p in range(L) if shard[p] == r]
+            assert [row[p] for p in toks] == list(range(len(toks)))
+            got = shards[r][off[r]:off[r] + len(toks)].cpu().numpy()
+            assert np.array_equal(got, kvh[base[b] + np.asarray(toks, dtype=np.int64)])
+            assert np.array_equal(scales[r][off[r]:off[r] + len(toks)].cpu().numpy(),
+                                  sch[base[b] + np.asarray(toks, dtype=np.int64)])
+            off[r] += len(toks)
+    assert [s.shape[0] for s in shards] == off
+
+
+def run_mla(cp, data, ctx, C, s_q, H, fp8, contiguous, n_workers=0):
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=n_workers, device=DEV)
+    B = len(ctx)
+    q = data["q"].reshape(B, s_q, H, 576) if s_q > 1 else data["q"]
+    if fp8:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_fp8"], data["kv_scale"])
+    else:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_bf16"])
+    scale = 1.0 / math.sqrt(576)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_MLA, q, shards, shard_scale=scales,
+                                         sm_scale=scale)
+    N = B * s_q
+    o, lse = cp.cp_lse_merge(o_part.reshape(C, N, H, 512), lse_part.reshape(C, N, H),
+                             out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    return plan, o_part.reshape(C, B, s_q, H, 512), lse_part.reshape(C, B, s_q, H), \
+        o.reshape(B, s_q, H, 512), lse.reshape(B, s_q, H)
+
+
+def check_mla(data, ctx, C, s_q, H, fp8, contiguous, o_part, lse_part, o, lse, reqs=None):
+    tol = TOL_FP8 if fp8 else TOL_BF16
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    B = len(ctx)
+    qn = np64(data["q"]).reshape(B, s_q, H, 576)
+    scale = 1.0 / math.sqrt(576)
+    for b in (range(B) if reqs is None else reqs):
+        L = ctx[b]
+        if fp8:
+            lat = oracle.e4m3_decode(data["kv_fp8"][base[b]:base[b] + L].cpu().numpy())
+            K, V = oracle.mla_cache_to_kv(lat, data["kv_scale"][base[b]:base[b] + L].double().cpu().numpy())
+        else:
+            K, V = oracle.mla_cache_to_kv(np64(data["kv_bf16"][base[b]:base[b] + L]))
+        po, pl = oracle.query_rows_partials(qn[b], K, V, C, scale, contiguous=contiguous)
+        for r in range(C):
+            for i in range(s_q):
+                check_o(o_part[r, b, i], po[r, i], what=f"partial r{r} b{b} row{i}", **tol)
+                check_lse(lse_part[r, b, i], pl[r, i])
+        for i in range(s_q):
+            fo, fl = oracle.decode_attention(qn[b, i], K[:L - s_q + i + 1], V[:L - s_q + i + 1], scale)
+            check_o(o[b, i], fo, what=f"merged b{b} row{i}", **tol)
+            check_lse(lse[b, i], fl)
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("s_q,H", [(1, 64), (2, 32), (4, 16), (3, 20)])
+def test_mla_layout_and_query_rows(cp, fp8, contiguous, s_q, H):
+    ctx = [max(s_q, 1), 5, 130, 1031, 4100]
+    data = W.mla_decode_inputs(ctx, H=s_q * H, seed=41 + s_q, device=DEV)
+    C = 8
+    _, o_part, lse_part, o, lse = run_mla(cp, data, ctx, C, s_q, H, fp8, contiguous, n_workers=7)
+    check_mla(data, ctx, C, s_q, H, fp8, contiguous, o_part, lse_part, o, lse)
+
+
+def test_mla_query_rows_tiny_requests(cp):
+    """Requests of exactly s_q tokens and shards that hold only tokens past a
+    row's position (that row's partial there is empty)."""
+    s_q, H, C = 4, 16, 8
+    ctx = [4, 5, 6, 9, 12]
+    for fp8 in (True, False):
+        data = W.mla_decode_inputs(ctx, H=s_q * H, seed=77, device=DEV)
+        for contiguous in (False, True):
+            _, o_part, lse_part, o, lse = run_mla(cp, data, ctx, C, s_q, H, fp8, contiguous)
+            check_mla(data, ctx, C, s_q, H, fp8, contiguous, o_part, lse_part, o, lse)
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("s_q", [1, 3])
+def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
+    ctx = [s_q, 40, 300, 4100]
+    B, Hq, Hkv, D, C = len(ctx), 8, 2, 128, 4
+    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=60 + s_q, device=DEV, std=0.3)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=5, device=DEV)
+    qq = q.reshape(B, s_q, Hq, D) if s_q > 1 else q
+    sk, _ = cp.cp_kv_shard_pack(plan, k)
+    sv, _ = cp.cp_kv_shard_pack(plan, v)
+    scale = 1.0 / math.sqrt(D)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, qq, sk, sv, sm_scale=scale)
+    o_part = o_part.reshape(C, B, s_q, Hq, D)
+    lse_part = lse_part.reshape(C, B, s_q, Hq)
+    o, lse = cp.cp_lse_merge(o_part.reshape(C, B * s_q, Hq, D), lse_part.reshape(C, B * s_q, Hq),
+                             out_dtype=torch.float32)
+    o, lse = o.reshape(B, s_q, Hq, D), lse.reshape(B, s_q, Hq)
+    cp.cp_device_error_check()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    qn, kn, vn = np64(q).reshape(B, s_q, Hq, D), np64(k), np64(v)
+    for b, L in enumerate(ctx):
+        K, V = kn[base[b]:base[b] + L], vn[base[b]:base[b] + L]
+        po, pl = oracle.query_rows_partials(qn[b], K, V, C, scale, contiguous=contiguous)
+        for r in range(C):
+            for i in range(s_q):
+                check_o(o_part[r, b, i], po[r, i], what=f"GQA partial r{r} b{b} row{i}", **TOL_BF16)
+                check_lse(lse_part[r, b, i], pl[r, i])
+        for i in range(s_q):
+            fo, fl = oracle.decode_attention(qn[b, i], K[:L - s_q + i + 1], V[:L - s_q + i + 1], scale)
+            check_o(o[b, i], fo, what=f"GQA merged b{b} row{i}", **TOL_BF16)
+            check_lse(lse[b, i], fl)
+
+
+def test_paged_contiguous_query_rows_match_unpaged(cp):
+    """The paged pool with a contiguous-layout MTP plan gives bit-identical
+    partials to the per-shard buffers."""
+    s_q, H, C, page = 2, 32, 4, 64
+    ctx = [2, 200, 1500]
+    data = W.mla_decode_inputs(ctx, H=s_q * H, seed=91, device=DEV)
+    plan, o_ref, l_ref, _, _ = run_mla(cp, data, ctx, C, s_q, H, True, True, n_workers=6)
+    pages = make_pages(cp, plan, page, seed=5)
+    pool, spool = cp.cp_kv_shard_pack_paged(plan, pages, data["kv_fp8"], data["kv_scale"])
+    q = data["q"].reshape(len(ctx), s_q, H, 576)
+    o_p, l_p = cp.cp_decode_attn_paged(plan, pages, cp.CP_DECODE_MLA, q, pool, scale_pool=spool,
+                                       sm_scale=1.0 / math.sqrt(576))
+    cp.cp_device_error_check()
+    assert torch.equal(o_p.reshape(o_ref.shape), o_ref) and torch.equal(l_p.reshape(l_ref.shape), l_ref)

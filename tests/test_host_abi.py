@@ -225,3 +225,48 @@ def test_paged_argument_validation(cp):
     dup = good.copy(); dup[3, 0] = 1
     assert pack(dup, 2, 64, 6) == -1 and b"used twice" in lib.cp_last_error()
     assert decode(good, 2, 64, 0) == -1 and b"num_pages=0" in lib.cp_last_error()
+
+
+@pytest.mark.parametrize("ctx,C", [([0, 1, 10, 129, 4100], 4), ([3, 8, 1000], 8), ([5], 1)])
+def test_contiguous_decode_plan_matches_oracle_map(cp, ctx, C):
+    """Pair rows and the row -> token map of a contiguous-layout plan against
+    the oracle's enumeration of the chunks."""
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=cp.CP_DCP_CONTIGUOUS, n_workers=7, device=None)
+    assert plan.layout == 1 and plan.query_rows == 1
+    B = len(ctx)
+    for r in range(C):
+        off = 0
+        for b in range(B):
+            shard, row = oracle.decode_shard_map_contiguous(ctx[b], C)
+            toks = [p for p in range(ctx[b]) if shard[p] == r]
+            rows, row_off, L, _, _, tok0, step, _ = plan.pairs[r * B + b]
+            assert rows == len(toks) and row_off == off and L == ctx[b]
+            # row i holds token tok0 + i * step
+            assert [tok0 + i * step for i in range(rows)] == toks
+            off += rows
+    covered = [np.zeros(int(p[0]), np.int64) for p in plan.pairs]
+    for pair, rb, re_, _ in plan.work:
+        covered[pair][rb:re_] += 1
+    assert all(np.all(c == 1) for c in covered)
+
+
+def test_round_robin_pairs_record_token_map(cp):
+    ctx, C = [0, 7, 300], 4
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=cp.CP_DCP_ROUND_ROBIN, n_workers=5, device=None)
+    for r in range(C):
+        for b in range(len(ctx)):
+            shard, _ = oracle.decode_shard_map(ctx[b], C)
+            rows, _, _, _, _, tok0, step, _ = plan.pairs[r * len(ctx) + b]
+            assert [tok0 + i * step for i in range(rows)] == [p for p in range(ctx[b]) if shard[p] == r]
+
+
+def test_decode_plan_ex_validation(cp):
+    with pytest.raises(cp.CpError):
+        cp.cp_decode_plan_ex(4, [10], layout=2)
+    for s_q in (0, 65):
+        with pytest.raises(cp.CpError):
+            cp.cp_decode_plan_ex(4, [100], s_q=s_q)
+    with pytest.raises(cp.CpError):  # a request shorter than its query rows
+        cp.cp_decode_plan_ex(4, [10, 2], s_q=3)
+    plan = cp.cp_decode_plan_ex(4, [10, 3], s_q=3, n_workers=5)
+    assert plan.query_rows == 3 and plan.layout == 0

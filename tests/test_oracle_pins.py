@@ -500,3 +500,92 @@ def test_designated_window_empty_main_cache():
     wo, wl = oracle.decode_attention(q, kw, vw, 0.5)
     assert np.allclose(po[1], wo) and np.allclose(pl[1], wl)
     assert np.isneginf(pl[0]).all() and np.isneginf(pl[2]).all() and not po[0].any()
+
+
+# ------------------------------------------------------------------ contiguous DCP and query rows
+
+
+def test_contiguous_map_dcp_example():
+    """vLLM DCP post §4: a 200K-token request on four GPUs, each holding one
+    50K range of positions (0-50K on GPU 0, 50K-100K on GPU 1, ...)."""
+    shard, row = oracle.decode_shard_map_contiguous(200_000, 4)
+    for r in range(4):
+        lo, hi = 50_000 * r, 50_000 * (r + 1)
+        assert shard[lo] == r and row[lo] == 0
+        assert shard[hi - 1] == r and row[hi - 1] == 49_999
+    assert np.bincount(shard).tolist() == [50_000] * 4
+
+
+def test_contiguous_map_remainder_and_partition():
+    """Reading: the first L mod C chunks hold one token more; every token is
+    stored once and each shard's rows are 0, 1, ... in token order."""
+    shard, row = oracle.decode_shard_map_contiguous(10, 4)
+    assert shard == [0, 0, 0, 1, 1, 1, 2, 2, 3, 3]
+    assert row == [0, 1, 2, 0, 1, 2, 0, 1, 0, 1]
+    for L, C in [(0, 3), (1, 4), (7, 8), (129, 8), (1000, 7)]:
+        shard, row = oracle.decode_shard_map_contiguous(L, C)
+        counts = np.bincount(shard, minlength=C) if L else np.zeros(C, int)
+        assert counts.max() - counts.min() <= 1
+        assert all(shard[p] <= shard[p + 1] for p in range(L - 1))
+        for r in range(C):
+            assert [row[p] for p in range(L) if shard[p] == r] == list(range(counts[r]))
+
+
+def _rows_case(L=11, s_q=3, H=4, D=16, seed=5):
+    g = np.random.default_rng(seed)
+    q_all = g.standard_normal((L, H, D))
+    k = g.standard_normal((L, 1, D))
+    v = g.standard_normal((L, 1, D))
+    return q_all, k, v
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+def test_query_rows_match_causal_sdpa(contiguous):
+    """The s_q query rows of a decode step are the request's last s_q
+    positions: merged over the shards they equal the last s_q rows of
+    torch's causal scaled_dot_product_attention over the whole request."""
+    L, s_q, H, D = 11, 3, 4, 16
+    q_all, k, v = _rows_case(L, s_q, H, D)
+    scale = 0.37
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q_all).permute(1, 0, 2), torch.from_numpy(k[:, 0]).expand(H, L, D),
+        torch.from_numpy(v[:, 0]).expand(H, L, D), is_causal=True, scale=scale).permute(1, 0, 2).numpy()
+    for C in (1, 3, 4, 16):
+        po, pl = oracle.query_rows_partials(q_all[L - s_q:], k, v, C, scale, contiguous=contiguous)
+        o, lse = oracle.lse_merge(po, pl)
+        assert np.allclose(o, ref[L - s_q:], atol=1e-12)
+        # LSE: logsumexp of the row's causal scores, from torch
+        s = torch.einsum("qhd,kd->qhk", torch.from_numpy(q_all[L - s_q:]), torch.from_numpy(k[:, 0])) * scale
+        mask = torch.arange(L)[None, :] <= torch.arange(L - s_q, L)[:, None]
+        want = torch.logsumexp(s.masked_fill(~mask[:, None, :], -math.inf), dim=-1).numpy()
+        assert np.allclose(lse, want, atol=1e-12)
+
+
+def test_query_rows_one_row_is_decode():
+    L, H, D = 9, 2, 8
+    q_all, k, v = _rows_case(L, 1, H, D, seed=9)
+    po, pl = oracle.query_rows_partials(q_all[-1:], k, v, 4, 0.5)
+    so, sl = oracle.decode_shard_partials(q_all[-1], k, v, 4, 0.5)
+    assert np.allclose(po[:, 0], so) and np.allclose(pl[:, 0], sl)
+
+
+def test_query_rows_pin_catches_off_by_one(monkeypatch):
+    """A row that stops one token early (or reads one late) fails the SDPA pin."""
+    L, s_q, H, D = 11, 3, 4, 16
+    q_all, k, v = _rows_case(L, s_q, H, D)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q_all).permute(1, 0, 2), torch.from_numpy(k[:, 0]).expand(H, L, D),
+        torch.from_numpy(v[:, 0]).expand(H, L, D), is_causal=True, scale=0.37).permute(1, 0, 2).numpy()
+    real = oracle.decode_attention
+    for shift in (-1, 1):
+        def shifted(q, kc, vc, sm, keys=None, _s=shift):
+            keys = np.asarray(keys)
+            if len(keys):
+                top = keys.max() + _s
+                keys = np.arange(0, min(top, kc.shape[0] - 1) + 1)
+            return real(q, kc, vc, sm, keys=keys)
+        monkeypatch.setattr(oracle.cpattn_oracle, "decode_attention", shifted)
+        po, pl = oracle.query_rows_partials(q_all[L - s_q:], k, v, 1, 0.37)
+        o, _ = oracle.lse_merge(po, pl)
+        monkeypatch.setattr(oracle.cpattn_oracle, "decode_attention", real)
+        assert not np.allclose(o, ref[L - s_q:], atol=1e-6)
