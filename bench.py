@@ -290,7 +290,12 @@ def run_ours(args, world, rank, local):
     if do_dec:
         data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev,
                                    bf16=not fp8, fp8=fp8)
-        dplan = cp.cp_decode_plan(m["C"], ctx, device=dev)
+        layout = cp.CP_DCP_CONTIGUOUS if args.decode_layout == "contiguous" else cp.CP_DCP_ROUND_ROBIN
+        s_q = args.decode_rows
+        if s_q < 1 or m["H"] % s_q:
+            raise SystemExit(f"--decode-rows must divide {m['H']}")
+        Hr = m["H"] // s_q  # heads per query row: the s_q rows fill the kernels' 64 columns
+        dplan = cp.cp_decode_plan_ex(m["C"], ctx, layout=layout, s_q=s_q, device=dev)
         kv, kv_scale = (data["kv_fp8"], data["kv_scale"]) if fp8 else (data["kv_bf16"], None)
         pages = None
         if args.decode_paged:
@@ -310,13 +315,16 @@ def run_ours(args, world, rank, local):
         del kv, kv_scale, data["kv_fp8" if fp8 else "kv_bf16"]
         if fp8:
             del data["kv_scale"]
-        dq = data["q"]
         B = len(ctx)
-        o_part = torch.empty((m["C"], B, m["H"], m["Dv"]), dtype=torch.float32, device=dev)
-        lse_part = torch.empty((m["C"], B, m["H"]), dtype=torch.float32, device=dev)
-        o_dec = torch.empty((B, m["H"], m["Dv"]), dtype=torch.bfloat16, device=dev)
-        lse_dec = torch.empty((B, m["H"]), dtype=torch.float32, device=dev)
-        ws_bytes = cp.cp_decode_workspace_size(dplan, m["H"], m["Dv"])
+        dq = data["q"].reshape(B, s_q, Hr, m["Dqk"]) if s_q > 1 else data["q"]
+        lead = (B, s_q) if s_q > 1 else (B,)
+        o_part = torch.empty((m["C"], *lead, Hr, m["Dv"]), dtype=torch.float32, device=dev)
+        lse_part = torch.empty((m["C"], *lead, Hr), dtype=torch.float32, device=dev)
+        o_mrg = o_part.view(m["C"], B * s_q, Hr, m["Dv"])
+        lse_mrg = lse_part.view(m["C"], B * s_q, Hr)
+        o_dec = torch.empty((B * s_q, Hr, m["Dv"]), dtype=torch.bfloat16, device=dev)
+        lse_dec = torch.empty((B * s_q, Hr), dtype=torch.float32, device=dev)
+        ws_bytes = cp.cp_decode_workspace_size(dplan, Hr, m["Dv"])
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         n_dec_kernels = 2 + (1 if dplan.n_split > 0 else 0)  # decode (+ split merge) + LSE merge
     torch.cuda.synchronize(dev)
@@ -333,7 +341,7 @@ def run_ours(args, world, rank, local):
             cp.cp_prefill_attn(plan, q, k, v, scale, out=o, lse=lse)
         e2.record(stream)
         if do_dec:
-            dp = cp.cp_decode_plan(m["C"], ctx, device=dev)
+            dp = cp.cp_decode_plan_ex(m["C"], ctx, layout=layout, s_q=s_q, device=dev)
             if pages is not None:
                 cp.cp_decode_attn_paged(dp, pages, cp.CP_DECODE_MLA, dq, shards, scale_pool=scales,
                                         sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
@@ -342,7 +350,7 @@ def run_ours(args, world, rank, local):
                                   sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
         e3.record(stream)
         if do_dec:
-            cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
+            cp.cp_lse_merge(o_mrg, lse_mrg, out=o_dec, lse=lse_dec)
         e4.record(stream)
 
     for _ in range(args.warmup):
@@ -429,11 +437,14 @@ def run_ours(args, world, rank, local):
                "kv": args.decode_kv,
                "cache": (f"paged, {args.decode_paged}-row pages placed at random"
                          if args.decode_paged else "one contiguous buffer per shard"),
+               "layout": args.decode_layout,
+               "query_rows": args.decode_rows,
                "ms_decode": dec_avg, "ms_merge": statistics.mean(mrg_ms),
                "merge_share": statistics.mean(mrg_ms) / (dec_avg + statistics.mean(mrg_ms)),
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
                             "frac": dec_ach / hbm,
-                            "traffic": (None if args.decode_paged else
+                            "traffic": (None if args.decode_paged or args.decode_rows > 1
+                                        or args.decode_layout != "round_robin" else
                                         profiled_traffic("decode_" + args.decode_kv, sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
@@ -489,6 +500,10 @@ def main():
     ap.add_argument("--decode-paged", type=int, default=0, metavar="PAGE_ROWS",
                     help="decode from a paged pool with pages of this many rows (multiple of 64), "
                          "placed at random; 0 = one contiguous buffer per shard")
+    ap.add_argument("--decode-layout", choices=["round_robin", "contiguous"], default="round_robin",
+                    help="decode token shards: token p on shard p mod C, or C contiguous chunks")
+    ap.add_argument("--decode-rows", type=int, default=1, metavar="S_Q",
+                    help="query rows per request (MTP); the 64 heads split into S_Q rows of 64/S_Q")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()
