@@ -47,15 +47,15 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "b7e2d65e16aa3b45f81ef50e7b206f806cb4ada6", "bytes": 2.376624e9 + 0.273960e9},
+                "sha1": "44fff9fda4e68d8f406c141795af9500b6584e56", "bytes": 2.377489e9 + 0.276153e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "6877ca2dd8c43b740d8df26608437b85500dc60f",
-                   "bytes_per_token": (0.637617e9 + 0.011065e9) / (8 * 131072)},
+                   "sha1": "19e3b1c25c898b463eeaa8898be05f8b86692f62",
+                   "bytes_per_token": (0.629337e9 + 0.010362e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "2899e683da4b57101d20237f8e1458e96cfa6227",
-                    "bytes_per_token": (1.209231e9 + 0.011313e9) / (8 * 131072)},
+                    "sha1": "b2abd418aceb16519afd17a0e263cc8231d5f9a6",
+                    "bytes_per_token": (1.209227e9 + 0.011821e9) / (8 * 131072)},
 }
 
 
