@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     CP_BF16,
     CP_DCP_CONTIGUOUS,
     CP_DCP_ROUND_ROBIN,
+    CP_DCP_SELECTED,
     CP_DECODE_GQA,
     CP_DECODE_MLA,
     CP_FP8_E4M3,
@@ -41,6 +42,12 @@ from ._binding import (  # noqa: F401
     cp_plan_size,
     cp_prefill_attn,
     cp_shard_plan,
+    cp_sparse_decode_attn,
+    cp_sparse_gather,
+    cp_sparse_plan,
+    cp_sparse_topk,
+    cp_sparse_workspace_size,
     lib,
     lib_path,
+    sparse_slot_rows,
 )

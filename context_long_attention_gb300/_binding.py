@@ -15,7 +15,7 @@ lib_path = os.path.join(_HERE, "_lib", "libcpattn.so")
 CP_ZIGZAG, CP_INTERLEAVE = 0, 1
 CP_BF16, CP_FP32, CP_FP8_E4M3 = 0, 1, 2
 CP_DECODE_GQA, CP_DECODE_MLA = 0, 1
-CP_DCP_ROUND_ROBIN, CP_DCP_CONTIGUOUS = 0, 1
+CP_DCP_ROUND_ROBIN, CP_DCP_CONTIGUOUS, CP_DCP_SELECTED = 0, 1, 2
 _STATUS = {0: "CP_OK", -1: "CP_ERR_INVALID_ARG", -2: "CP_ERR_UNSUPPORTED", -3: "CP_ERR_CUDA",
            -4: "CP_ERR_DEVICE_TIMEOUT", -5: "CP_ERR_WORKSPACE"}
 MAX_SHARDS = 64
@@ -63,6 +63,13 @@ _SIGS = {
                                     _vp]),
     "cp_decode_attn_paged": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                                   _i, _i, _i, _f, _vp, _vp, _vp, _sz, _vp]),
+    "cp_sparse_workspace_size": (_i, [_vp, _i, _szp]),
+    "cp_sparse_topk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp]),
+    "cp_sparse_gather": (_i, [_vp, _vp, _i, _vp, _sz, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
+    "cp_sparse_plan_size": (_i, [_i, _i, _i, _i, _szp, _szp]),
+    "cp_sparse_plan": (_i, [_i, _i, _i, _i, _vp, _sz, _vp, _sz, _vp]),
+    "cp_sparse_decode_attn": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
+                                   _vp, _vp, _vp, _sz, _vp]),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
 for _name, (_res, _args) in _SIGS.items():
@@ -479,3 +486,108 @@ def cp_lse_fold(o, lse, o_add, lse_add):
 
 def cp_device_error_check(device=None):
     _check(lib.cp_device_error_check(_stream(device)))
+
+
+# ---------------------------------------------------------------- sparse decode
+
+def cp_sparse_workspace_size(plan: DecodePlan, k: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib.cp_sparse_workspace_size(_np_ptr(plan.host), k, ctypes.byref(b)))
+    return b.value
+
+
+def cp_sparse_topk(plan: DecodePlan, shard_scores, k: int, sel_ids=None, sel_count=None, ws=None):
+    """Exact sharded top-k: shard_scores[r] fp32 [rows_r] (the plan's rows).
+    Returns (sel_ids [B, k] int32 ascending, -1 padded; sel_count [B]; ws),
+    ws holding the candidates for cp_sparse_gather."""
+    dev = next(t.device for t in shard_scores if t is not None)
+    _need_cuda(*[t for t in shard_scores if t is not None])
+    B = plan.R
+    if sel_ids is None:
+        sel_ids = torch.empty((B, k), dtype=torch.int32, device=dev)
+    if sel_count is None:
+        sel_count = torch.empty((B,), dtype=torch.int32, device=dev)
+    need = cp_sparse_workspace_size(plan, k)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib.cp_sparse_topk(_np_ptr(plan.host), _ptr(plan.dev), _ptr_array(shard_scores), k,
+                              _ptr(sel_ids), _ptr(sel_count), _ptr(ws), ws.numel(), _stream(dev)))
+    return sel_ids, sel_count, ws
+
+
+def sparse_slot_rows(k: int) -> int:
+    """Rows per (shard, request) slot of a selection buffer: k rounded up to 128."""
+    return (k + 127) // 128 * 128
+
+
+def cp_sparse_gather(plan: DecodePlan, k: int, ws, shard_kv, shard_scale=None, sel_kv=None,
+                     sel_scale=None, pair_count=None):
+    """Packs each owner's selected rows (after cp_sparse_topk with the same
+    plan, k, ws) into selection buffers [B kp, ...] (kp = sparse_slot_rows(k));
+    returns
+    (sel_kv list, sel_scale list or None, pair_count [C * B])."""
+    sk = [t.view(torch.uint8) if t is not None and t.dtype == torch.float8_e4m3fn else t
+          for t in shard_kv]
+    ref = next(t for t in sk if t is not None)
+    _need_cuda(*[t for t in sk if t is not None])
+    C, B = plan.C, plan.R
+    kp = sparse_slot_rows(k)
+    if sel_kv is None:
+        sel_kv = [torch.empty((B * kp, *ref.shape[1:]), dtype=ref.dtype, device=ref.device)
+                  for _ in range(C)]
+    if shard_scale is not None and sel_scale is None:
+        sel_scale = [torch.empty((B * kp,), dtype=torch.float32, device=ref.device) for _ in range(C)]
+    if pair_count is None:
+        pair_count = torch.empty((C * B,), dtype=torch.int32, device=ref.device)
+    row_elems = int(np.prod(ref.shape[1:]))
+    _check(lib.cp_sparse_gather(_np_ptr(plan.host), _ptr(plan.dev), k, _ptr(ws), ws.numel(),
+                                _dtype_code(ref), _ptr_array(sk),
+                                _ptr_array(shard_scale) if shard_scale is not None else None,
+                                row_elems, _ptr_array(sel_kv),
+                                _ptr_array(sel_scale) if sel_scale is not None else None,
+                                _ptr(pair_count), _stream(ref.device)))
+    return sel_kv, sel_scale, pair_count
+
+
+def cp_sparse_plan(C: int, B: int, k: int, n_workers: int = 0, device=None) -> DecodePlan:
+    """The decode plan over selection buffers with room for k rows per pair."""
+    hb, db = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib.cp_sparse_plan_size(C, B, k, n_workers, ctypes.byref(hb), ctypes.byref(db)))
+    host = np.zeros(hb.value // 4, dtype=np.int32)
+    dev = None
+    if device is not None:
+        dev = torch.empty(db.value // 4, dtype=torch.int32, device=device)
+    _check(lib.cp_sparse_plan(C, B, k, n_workers, _np_ptr(host), hb.value, _ptr(dev), db.value,
+                              _stream(dev.device) if dev is not None else None))
+    return DecodePlan(host, dev)
+
+
+def cp_sparse_decode_attn(plan: DecodePlan, pair_count, mode: int, q, sel_k, sel_v=None,
+                          sel_scale=None, sm_scale=None, o_part=None, lse_part=None, ws=None):
+    """cp_decode_attn over the selection buffers (plan from cp_sparse_plan)."""
+    B, H, Dqk = q.shape
+    sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in sel_k]
+    _need_cuda(q, pair_count, *sk)
+    kv_dtype = _dtype_code(sk[0])
+    if mode == CP_DECODE_MLA:
+        Hkv, Dv = 1, 512
+    else:
+        Hkv, Dv = sk[0].shape[1], Dqk
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(Dqk)
+    C = plan.C
+    if o_part is None:
+        o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((C, B, H), dtype=torch.float32, device=q.device)
+    need = cp_decode_workspace_size(plan, H, Dv)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.cp_sparse_decode_attn(_np_ptr(plan.host), _ptr(plan.dev), _ptr(pair_count), mode,
+                                     kv_dtype, _ptr(q), _ptr_array(sk),
+                                     _ptr_array(sel_v) if sel_v is not None else None,
+                                     _ptr_array(sel_scale) if sel_scale is not None else None,
+                                     H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part), _ptr(lse_part),
+                                     _ptr(ws), ws_bytes, _stream(q.device)))
+    return o_part, lse_part

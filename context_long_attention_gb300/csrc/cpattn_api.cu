@@ -244,7 +244,7 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
   if (B < 1) return fail(CP_ERR_INVALID_ARG, "B=%d must be >= 1", B);
   if (!ctx_len) return fail(CP_ERR_INVALID_ARG, "ctx_len is NULL");
   if (n_workers < 0) return fail(CP_ERR_INVALID_ARG, "n_workers=%d < 0", n_workers);
-  if (layout != CP_DCP_ROUND_ROBIN && layout != CP_DCP_CONTIGUOUS)
+  if (layout != CP_DCP_ROUND_ROBIN && layout != CP_DCP_CONTIGUOUS && layout != CP_DCP_SELECTED)
     return fail(CP_ERR_INVALID_ARG, "layout=%d is not a cp_dcp_layout", layout);
   if (s_q < 1 || s_q > 64) return fail(CP_ERR_INVALID_ARG, "s_q=%d outside [1, 64]", s_q);
   long long total = 0;
@@ -272,10 +272,14 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
         rows = L > r ? (L - r + C - 1) / C : 0;
         tok0 = r;
         step = C;
-      } else {  // one chunk; the first L mod C chunks one token longer
+      } else if (layout == CP_DCP_CONTIGUOUS) {  // one chunk; the first L mod C one token longer
         const int q = L / C, m = L % C;
         rows = q + (r < m ? 1 : 0);
         tok0 = r * q + std::min(r, m);
+        step = 1;
+      } else {  // selection buffer: room for L rows per pair, the count known on the device
+        rows = L;
+        tok0 = 0;
         step = 1;
       }
       cp_pair_desc& d = pair[r * B + b];
@@ -503,7 +507,7 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
                      cp_dtype kv_dtype, const void* q, const ShardPtrs& K, const ShardPtrs& V,
                      const ScalePtrs& S, const long long* shard_rows, const RowMap& rm, int Hq,
                      int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
-                     void* ws, size_t ws_bytes, void* stream) {
+                     void* ws, size_t ws_bytes, void* stream, const int32_t* pair_count = nullptr) {
   const int Hc = Hq * plan_s_q(h);  // query rows x heads: the kernels' head columns
   size_t need = (size_t)h.n_parts * Hc * (Dv + 1) * sizeof(float);
   if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
@@ -515,11 +519,11 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   cudaError_t e =
       mla && kv_dtype == CP_FP8_E4M3
           ? launch_decode_mla_fp8((const int32_t*)dev_plan, h, q, K, S, shard_rows, rm, Hq, sm_scale,
-                                  o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+                                  o_part, lse_part, ws_o, ws_lse, pair_count, wait_limit_ns(), s)
       : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, q, K, shard_rows, rm, Hq, sm_scale,
-                                   o_part, lse_part, ws_o, ws_lse, wait_limit_ns(), s)
+                                   o_part, lse_part, ws_o, ws_lse, pair_count, wait_limit_ns(), s)
             : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk,
-                                 Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, s);
+                                 Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, pair_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
   if (h.n_split) {
     e = launch_decode_fixup((const int32_t*)dev_plan, h, Hc, Dv, ws_o, ws_lse, o_part, lse_part, s);
@@ -630,6 +634,7 @@ cp_status cp_decode_plan_size(int C, int B, const int32_t* ctx_len, int n_worker
 cp_status cp_decode_plan_ex_size(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
                                  int n_workers, size_t* host_bytes, size_t* dev_bytes) {
   if (!host_bytes || !dev_bytes) return fail(CP_ERR_INVALID_ARG, "size outputs are NULL");
+  if (layout == CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "selection plans come from cp_sparse_plan");
   DecodeBuild b;
   cp_status st = build_decode_plan(C, B, ctx_len, (int)layout, s_q, n_workers, &b);
   if (st != CP_OK) return st;
@@ -640,6 +645,7 @@ cp_status cp_decode_plan_ex_size(int C, int B, const int32_t* ctx_len, cp_dcp_la
 cp_status cp_decode_plan_ex(int C, int B, const int32_t* ctx_len, cp_dcp_layout layout, int s_q,
                             int n_workers, void* host_plan, size_t host_bytes, void* dev_plan,
                             size_t dev_bytes, void* stream) {
+  if (layout == CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "selection plans come from cp_sparse_plan");
   DecodeBuild b;
   cp_status st = build_decode_plan(C, B, ctx_len, (int)layout, s_q, n_workers, &b);
   if (st != CP_OK) return st;
@@ -841,6 +847,193 @@ cp_status cp_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o
   cudaError_t e = launch_lse_fold(N, H, Dv, o, lse, o_add, lse_add, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "fold kernel");
   return ok();
+}
+
+// ---------------------------------------------------------------- sparse decode
+
+namespace {
+constexpr int kMaxTopK = 4096;
+
+struct TopkWs {
+  uint64_t* cand_keys;  // [C * B][k]
+  uint64_t* thresh;     // [B]
+  int32_t* cand_n;      // [C * B]
+};
+size_t topk_ws_bytes(const cp_plan_header& h, int k) {
+  const size_t P = (size_t)h.C * h.R;
+  return P * k * 8 + (size_t)h.R * 8 + ((P * 4 + 15) / 16) * 16;
+}
+TopkWs topk_ws(const cp_plan_header& h, int k, void* ws) {
+  TopkWs w;
+  const size_t P = (size_t)h.C * h.R;
+  w.cand_keys = static_cast<uint64_t*>(ws);
+  w.thresh = w.cand_keys + P * k;
+  w.cand_n = reinterpret_cast<int32_t*>(w.thresh + h.R);
+  return w;
+}
+cp_status check_topk_args(const cp_plan_header& h, int k) {
+  if (k < 1 || k > kMaxTopK) return fail(CP_ERR_INVALID_ARG, "k=%d outside [1, %d]", k, kMaxTopK);
+  if (h.layout == CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "top-k runs on a cache plan, not a selection plan");
+  if (plan_s_q(h) != 1) return fail(CP_ERR_UNSUPPORTED, "sparse decode takes one query row per request");
+  return ok();
+}
+}  // namespace
+
+cp_status cp_sparse_plan_size(int C, int B, int k, int n_workers, size_t* host_bytes,
+                              size_t* dev_bytes) {
+  if (!host_bytes || !dev_bytes) return fail(CP_ERR_INVALID_ARG, "size outputs are NULL");
+  if (k < 1 || k > kMaxTopK) return fail(CP_ERR_INVALID_ARG, "k=%d outside [1, %d]", k, kMaxTopK);
+  if (B < 1) return fail(CP_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+  std::vector<int32_t> cap(B, (k + kDecodeTileRows - 1) / kDecodeTileRows * kDecodeTileRows);
+  DecodeBuild b;
+  cp_status st = build_decode_plan(C, B, cap.data(), CP_DCP_SELECTED, 1, n_workers, &b);
+  if (st != CP_OK) return st;
+  *host_bytes = *dev_bytes = b.words.size() * 4;
+  return ok();
+}
+
+cp_status cp_sparse_plan(int C, int B, int k, int n_workers, void* host_plan, size_t host_bytes,
+                         void* dev_plan, size_t dev_bytes, void* stream) {
+  if (k < 1 || k > kMaxTopK) return fail(CP_ERR_INVALID_ARG, "k=%d outside [1, %d]", k, kMaxTopK);
+  if (B < 1) return fail(CP_ERR_INVALID_ARG, "B=%d must be >= 1", B);
+  std::vector<int32_t> cap(B, (k + kDecodeTileRows - 1) / kDecodeTileRows * kDecodeTileRows);
+  DecodeBuild b;
+  cp_status st = build_decode_plan(C, B, cap.data(), CP_DCP_SELECTED, 1, n_workers, &b);
+  if (st != CP_OK) return st;
+  st = copy_plan(b.words, host_plan, host_bytes, dev_plan, dev_bytes, b.words.size() * 4,
+                 (cudaStream_t)stream);
+  return st == CP_OK ? ok() : st;
+}
+
+cp_status cp_sparse_workspace_size(const void* host_plan, int k, size_t* bytes) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (!bytes) return fail(CP_ERR_INVALID_ARG, "bytes is NULL");
+  st = check_topk_args(h, k);
+  if (st != CP_OK) return st;
+  *bytes = topk_ws_bytes(h, k);
+  return ok();
+}
+
+cp_status cp_sparse_topk(const void* host_plan, const void* dev_plan, const float* const* shard_scores,
+                         int k, int32_t* sel_ids, int32_t* sel_count, void* ws, size_t ws_bytes,
+                         void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  st = check_topk_args(h, k);
+  if (st != CP_OK) return st;
+  if (!dev_plan || !shard_scores || !sel_ids || !sel_count || !ws)
+    return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (!aligned16(ws) || !aligned16(dev_plan)) return fail(CP_ERR_INVALID_ARG, "ws/dev_plan not 16-byte aligned");
+  if (ws_bytes < topk_ws_bytes(h, k))
+    return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, topk_ws_bytes(h, k));
+  ScorePtrs sc;
+  memset(&sc, 0, sizeof(sc));
+  const int32_t* W = (const int32_t*)host_plan;
+  for (int r = 0; r < h.C; ++r) {
+    sc.p[r] = shard_scores[r];
+    if (pair_rows_of_shard(h, W, r) > 0 && !shard_scores[r])
+      return fail(CP_ERR_INVALID_ARG, "shard_scores[%d] is NULL", r);
+  }
+  const TopkWs w = topk_ws(h, k, ws);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_topk_local((const int32_t*)dev_plan, h, sc, k, w.cand_keys, w.cand_n, s);
+  if (e != cudaSuccess) return cuda_fail(e, "local top-k kernel");
+  e = launch_topk_merge(h, k, w.cand_keys, w.cand_n, w.thresh, sel_ids, sel_count, s);
+  if (e != cudaSuccess) return cuda_fail(e, "top-k merge kernel");
+  return ok();
+}
+
+cp_status cp_sparse_gather(const void* host_plan, const void* dev_plan, int k, const void* ws,
+                           size_t ws_bytes, cp_dtype dtype, const void* const* shard_kv,
+                           const float* const* shard_scale, int row_elems, void* const* sel_kv,
+                           float* const* sel_scale, int32_t* pair_count, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  st = check_topk_args(h, k);
+  if (st != CP_OK) return st;
+  if (!dev_plan || !ws || !shard_kv || !sel_kv || !pair_count)
+    return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (ws_bytes < topk_ws_bytes(h, k))
+    return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, topk_ws_bytes(h, k));
+  if (dtype != CP_BF16 && dtype != CP_FP32 && dtype != CP_FP8_E4M3) return fail(CP_ERR_INVALID_ARG, "bad dtype");
+  if (row_elems < 1) return fail(CP_ERR_INVALID_ARG, "row_elems=%d < 1", row_elems);
+  const size_t rb = (size_t)row_elems * elem_size(dtype);
+  if (rb % 16) return fail(CP_ERR_UNSUPPORTED, "row bytes %zu not a multiple of 16", rb);
+  if ((shard_scale == nullptr) != (sel_scale == nullptr))
+    return fail(CP_ERR_INVALID_ARG, "shard_scale and sel_scale must both be given or both NULL");
+  ShardPtrs src;
+  ScalePtrs ssc;
+  MutShardPtrs dst;
+  MutScalePtrs dsc;
+  memset(&src, 0, sizeof(src));
+  memset(&ssc, 0, sizeof(ssc));
+  memset(&dst, 0, sizeof(dst));
+  memset(&dsc, 0, sizeof(dsc));
+  const int32_t* W = (const int32_t*)host_plan;
+  for (int r = 0; r < h.C; ++r) {
+    const bool used = pair_rows_of_shard(h, W, r) > 0;
+    src.p[r] = shard_kv[r];
+    dst.p[r] = sel_kv[r];
+    if (used && (!shard_kv[r] || !aligned16(shard_kv[r]))) return fail(CP_ERR_INVALID_ARG, "shard_kv[%d] NULL or misaligned", r);
+    if (!sel_kv[r] || !aligned16(sel_kv[r])) return fail(CP_ERR_INVALID_ARG, "sel_kv[%d] NULL or misaligned", r);
+    if (shard_scale) {
+      ssc.p[r] = shard_scale[r];
+      dsc.p[r] = sel_scale[r];
+      if ((used && !shard_scale[r]) || !sel_scale[r]) return fail(CP_ERR_INVALID_ARG, "scale pointer %d is NULL", r);
+    }
+  }
+  const TopkWs w = topk_ws(h, k, const_cast<void*>(ws));
+  cudaError_t e = launch_sparse_gather((const int32_t*)dev_plan, h, k, w.cand_keys, w.cand_n, w.thresh,
+                                       src, ssc, (int)rb, dst, dsc, shard_scale != nullptr, pair_count,
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse gather kernel");
+  return ok();
+}
+
+cp_status cp_sparse_decode_attn(const void* host_plan, const void* dev_plan, const int32_t* pair_count,
+                                cp_decode_mode mode, cp_dtype kv_dtype, const void* q,
+                                const void* const* sel_k, const void* const* sel_v,
+                                const float* const* sel_scale, int Hq, int Hkv, int Dqk, int Dv,
+                                float sm_scale, float* o_part, float* lse_part, void* ws,
+                                size_t ws_bytes, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (h.layout != CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "needs a selection plan (cp_sparse_plan)");
+  if (!dev_plan || !q || !sel_k || !o_part || !lse_part || !pair_count)
+    return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o_part) || !aligned16(lse_part))
+    return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
+  st = check_decode_shapes(mode, kv_dtype, sel_v != nullptr, sel_scale != nullptr, Hq, Hkv, Dqk, Dv,
+                           sm_scale, 1);
+  if (st != CP_OK) return st;
+  ShardPtrs K, V;
+  ScalePtrs S;
+  memset(&K, 0, sizeof(K));
+  memset(&V, 0, sizeof(V));
+  memset(&S, 0, sizeof(S));
+  long long shard_rows[CP_MAX_SHARDS] = {0};
+  for (int r = 0; r < h.C; ++r) {
+    shard_rows[r] = pair_rows_of_shard(h, (const int32_t*)host_plan, r);
+    K.p[r] = sel_k[r];
+    if (!sel_k[r] || !aligned16(sel_k[r])) return fail(CP_ERR_INVALID_ARG, "sel_k[%d] NULL or misaligned", r);
+    if (sel_v) {
+      V.p[r] = sel_v[r];
+      if (!sel_v[r] || !aligned16(sel_v[r])) return fail(CP_ERR_INVALID_ARG, "sel_v[%d] NULL or misaligned", r);
+    }
+    if (sel_scale) {
+      S.p[r] = sel_scale[r];
+      if (!sel_scale[r]) return fail(CP_ERR_INVALID_ARG, "sel_scale[%d] is NULL", r);
+    }
+  }
+  RowMap rm;
+  memset(&rm, 0, sizeof(rm));
+  return run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv,
+                    sm_scale, o_part, lse_part, ws, ws_bytes, stream, pair_count);
 }
 
 }  // extern "C"

@@ -81,6 +81,7 @@ struct Params {
   float* lse_part;
   float* ws_o;
   float* ws_lse;
+  const int32_t* pair_count;  // rows in use per pair (a selection buffer), or nullptr
   unsigned* status;
   unsigned long long wait_ns;
 };
@@ -173,7 +174,9 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   Item it;
   it.r = wd.pair / p.B;
   it.b = wd.pair % p.B;
-  it.nrows = wd.row_end - wd.row_begin;
+  const int row_end = p.pair_count ? min(wd.row_end, max(wd.row_begin, __ldg(p.pair_count + wd.pair)))
+                                    : wd.row_end;
+  it.nrows = row_end - wd.row_begin;
   it.ntiles = (it.nrows + kRows - 1) / kRows;
   it.row0 = (long long)pd.row_off + wd.row_begin;
   it.pair = wd.pair;
@@ -707,8 +710,10 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
                                   const ShardPtrs& k, const ScalePtrs& sc,
                                   const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
-                                  unsigned long long wait_ns, cudaStream_t s) {
+                                  const int32_t* pair_count, unsigned long long wait_ns,
+                                  cudaStream_t s) {
   Params p;
+  p.pair_count = pair_count;
   p.plan = dev_plan;
   p.B = h.R;
   p.off_pair = h.off_rank;

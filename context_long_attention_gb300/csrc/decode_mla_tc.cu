@@ -68,6 +68,7 @@ struct Params {
   float* lse_part;
   float* ws_o;
   float* ws_lse;
+  const int32_t* pair_count;  // rows in use per pair (a selection buffer), or nullptr
   unsigned* status;
   unsigned long long wait_ns;
 };
@@ -160,7 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const cp_work_desc wd = work[wi];
     const int r = wd.pair / p.B, b = wd.pair % p.B;
     const cp_pair_desc pd = pairs[wd.pair];
-    const int nrows = wd.row_end - wd.row_begin;
+    const int row_end = p.pair_count ? min(wd.row_end, max(wd.row_begin, __ldg(p.pair_count + wd.pair)))
+                                      : wd.row_end;
+    const int nrows = row_end - wd.row_begin;
     const int ntiles = (nrows + kRows - 1) / kRows;
     const long long row0 = (long long)pd.row_off + wd.row_begin;  // first shard row
     float* out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
@@ -451,8 +454,10 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
                                  const void* q, const ShardPtrs& k,
                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
-                                 unsigned long long wait_ns, cudaStream_t s) {
+                                 const int32_t* pair_count, unsigned long long wait_ns,
+                                 cudaStream_t s) {
   Params p;
+  p.pair_count = pair_count;
   p.plan = dev_plan;
   p.B = h.R;
   p.off_pair = h.off_rank;

@@ -30,6 +30,7 @@ struct ShardPtrs {
 struct ScalePtrs {
   const float* p[CP_MAX_SHARDS];
 };
+using ScorePtrs = ScalePtrs;  // per-shard fp32 arrays of token scores
 struct MutShardPtrs {
   void* p[CP_MAX_SHARDS];
 };
@@ -105,14 +106,16 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
                                   const ShardPtrs& k, const ScalePtrs& sc,
                                   const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
-                                  unsigned long long wait_ns, cudaStream_t s);
+                                  const int32_t* pair_count, unsigned long long wait_ns,
+                                  cudaStream_t s);
 
 // ---- tensor-core MLA decode over a bf16 cache (decode_mla_tc.cu)
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,
                                  const void* q, const ShardPtrs& k,
                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
-                                 unsigned long long wait_ns, cudaStream_t s);
+                                 const int32_t* pair_count, unsigned long long wait_ns,
+                                 cudaStream_t s);
 unsigned long long wait_limit_ns();
 
 // ---- CUDA-core attention (simt_attn.cu)
@@ -125,6 +128,22 @@ cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
                                const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,
                                int Hkv, int Dqk,
                                int Dv, float sm_scale, float* o_part, float* lse_part,
-                               float* ws_o, float* ws_lse, cudaStream_t s);
+                               float* ws_o, float* ws_lse, const int32_t* pair_count,
+                               cudaStream_t s);
+
+// ---- sparse decode: exact sharded top-k and the owners' gather (sparse_kernels.cu)
+// Decode kernels given a pair_count (device, one per (shard, request) pair)
+// read only the first pair_count[pair] rows of each pair.
+cudaError_t launch_topk_local(const int32_t* dev_plan, const cp_plan_header& h, const ScorePtrs& scores,
+                              int k, uint64_t* cand_keys, int32_t* cand_n, cudaStream_t s);
+cudaError_t launch_topk_merge(const cp_plan_header& h, int k, const uint64_t* cand_keys,
+                              const int32_t* cand_n, uint64_t* thresh, int32_t* sel_ids,
+                              int32_t* sel_count, cudaStream_t s);
+cudaError_t launch_sparse_gather(const int32_t* dev_plan, const cp_plan_header& h, int k,
+                                 const uint64_t* cand_keys, const int32_t* cand_n,
+                                 const uint64_t* thresh, const ShardPtrs& src,
+                                 const ScalePtrs& src_scale, int row_bytes, const MutShardPtrs& dst,
+                                 const MutScalePtrs& dst_scale, bool has_scale, int32_t* pair_count,
+                                 cudaStream_t s);
 
 }  // namespace cpattn

@@ -95,7 +95,7 @@ template <typename T, int ND>
 __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                                        int off_worker, int off_work, const T* __restrict__ q,
                                        ShardPtrs kp, ShardPtrs vp, RowMap rm, int Hq, int Hkv,
-                                       int s_q, float sm_scale,
+                                       int s_q, float sm_scale, const int32_t* __restrict__ pair_count,
                                        float* __restrict__ o_part, float* __restrict__ lse_part,
                                        float* __restrict__ ws_o, float* __restrict__ ws_lse) {
   constexpr int D = ND * 32;
@@ -120,7 +120,7 @@ __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, 
     // rows hold tokens tok0 + i tok_step in increasing order, so a prefix.
     const int lim = pd.ctx_len - s_q + qi;
     const int n_valid = lim < pd.tok0 ? 0 : min(pd.rows, (lim - pd.tok0) / pd.tok_step + 1);
-    const int row_end = min(wd.row_end, n_valid);
+    const int row_end = min(min(wd.row_end, n_valid), pair_count ? pair_count[wd.pair] : wd.row_end);
     const T* kb = static_cast<const T*>(kp.p[r]);
     const T* vb = static_cast<const T*>(vp.p[r]);
     RowState<ND> st;
@@ -169,13 +169,13 @@ cudaError_t decode_gqa_t(const int32_t* plan, const cp_plan_header& h, const voi
                          const ShardPtrs& k, const ShardPtrs& v, const RowMap& rm, int Hq, int Hkv,
                          float sm_scale,
                          float* o_part, float* lse_part, float* ws_o, float* ws_lse,
-                         cudaStream_t s) {
+                         const int32_t* pair_count, cudaStream_t s) {
   const int warps = 4;
   const int s_q = plan_s_q(h);
   dim3 grid(h.n_tiles, (Hq * s_q + warps - 1) / warps);
   decode_gqa_simt_kernel<T, ND><<<grid, warps * 32, 0, s>>>(
       plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, rm, Hq, Hkv,
-      s_q, sm_scale, o_part, lse_part, ws_o, ws_lse);
+      s_q, sm_scale, pair_count, o_part, lse_part, ws_o, ws_lse);
   return cudaGetLastError();
 }
 
@@ -206,16 +206,17 @@ cudaError_t launch_decode_simt(const int32_t* plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
                                const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,
                                int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
-                               float* ws_o, float* ws_lse, cudaStream_t s) {
+                               float* ws_o, float* ws_lse, const int32_t* pair_count,
+                               cudaStream_t s) {
   (void)sc;
   (void)Dv;
 #define CP_GQA_CASE(ND)                                                                         \
   case ND:                                                                                      \
     return kv_dtype == CP_BF16                                                                  \
                ? decode_gqa_t<__nv_bfloat16, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale,       \
-                                                 o_part, lse_part, ws_o, ws_lse, s)             \
+                                                 o_part, lse_part, ws_o, ws_lse, pair_count, s) \
                : decode_gqa_t<float, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale, o_part,       \
-                                         lse_part, ws_o, ws_lse, s);
+                                         lse_part, ws_o, ws_lse, pair_count, s);
   switch (Dqk / 32) {
     CP_GQA_CASE(1)
     CP_GQA_CASE(2)

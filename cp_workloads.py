@@ -38,7 +38,8 @@ import torch
 
 E4M3_MAX = 448.0
 
-SEEDS = {"tiny": 1001, "zigzag": 1002, "interleave": 1003, "mla": 1004, "mla_mixed": 1005}
+SEEDS = {"tiny": 1001, "zigzag": 1002, "interleave": 1003, "mla": 1004, "mla_mixed": 1005,
+         "index": 1006}
 
 WORKLOADS = {
     "tiny": dict(kind="prefill+decode", strategy="zigzag", new_len=[256], prefix_len=[0], C=4,
@@ -174,6 +175,16 @@ def mla_decode_inputs(ctx, H=64, Dqk=576, seed=0, device="cpu", q_std=1.0, kv_st
         out["kv_fp8"] = codes
         out["kv_scale"] = scale
     return out
+
+
+def index_scores(ctx, seed=SEEDS["index"], device="cpu", ties=False):
+    """Relevance scores of every cached token [sum(ctx)] fp32, token order,
+    requests back to back: N(0, 1), or with ``ties`` rounded to multiples of
+    1/2 (few distinct values, many equal scores).  They stand in for the
+    output of a sparse-attention index scan, whose weights are not here."""
+    g = _gen(device, seed)
+    s = torch.randn((sum(int(c) for c in ctx),), generator=g, device=device, dtype=torch.float32)
+    return torch.round(s * 2) / 2 if ties else s
 
 
 def tiny_inputs(device="cpu", seed=SEEDS["tiny"]):

@@ -67,7 +67,8 @@ typedef enum { CP_DECODE_GQA = 0, CP_DECODE_MLA = 1 } cp_decode_mode;
 /* Which decode shard holds token p of a request of L cached tokens. */
 typedef enum {
   CP_DCP_ROUND_ROBIN = 0, /* shard p mod C, row p / C ([CTX] §3.1; [V4] §5) */
-  CP_DCP_CONTIGUOUS = 1   /* C consecutive chunks, the first L mod C one token longer ([DCP] §4) */
+  CP_DCP_CONTIGUOUS = 1,  /* C consecutive chunks, the first L mod C one token longer ([DCP] §4) */
+  CP_DCP_SELECTED = 2     /* selection buffers of a sparse decode (cp_sparse_plan only) */
 } cp_dcp_layout;
 
 /* ---------------------------------------------------------------------------
@@ -333,6 +334,68 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
                          const void* const* shard_v, const float* const* shard_scale, int Hq,
                          int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
                          void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Sparse decode with an exact sharded top-k ("DeepSeek-V4 Attention
+ * Inference Systems" §5.2; [CTX] §4.1, the index split with the cache).
+ *
+ * Each shard holds the relevance scores of the tokens it stores (the output
+ * of its local index scan; the scoring function belongs to the model and is
+ * an input here) and the steps run as the pages list them:
+ *   cp_sparse_topk    every (shard, request) pair keeps its k best tokens,
+ *                     then the at most C k candidates of a request give the
+ *                     exact global top-k (the union of the local top-k lists
+ *                     contains it, so nothing is approximated);
+ *   cp_sparse_gather  every owner packs the cache rows of the selected tokens
+ *                     it stores into its selection buffer (route to owners);
+ *   cp_sparse_decode_attn  every owner attends to its selected rows; the
+ *                     partials merge exactly with cp_lse_merge.
+ * Order: higher score first; equal scores by lower token index (the pages
+ * ask only for deterministic ties).  Scores must not be NaN.
+ *
+ * cp_sparse_topk: host_plan/dev_plan = the cache's decode plan (any layout,
+ *   one query row); shard_scores[r] fp32 [rows_r] device, shard r's scores in
+ *   the plan's row order; k in [1, 4096].  Writes sel_ids [B][k] int32 (the
+ *   selected token indices of request b in increasing order, -1 past the
+ *   count) and sel_count [B] = min(k, L_b).  ws: cp_sparse_workspace_size()
+ *   bytes, 16-byte aligned; it keeps the candidates for cp_sparse_gather.
+ * cp_sparse_gather: after cp_sparse_topk with the same plan, k and ws.
+ *   shard_kv[r] [rows_r, row_elems] (and shard_scale[r] fp32 [rows_r] or
+ *   NULL) as packed by cp_kv_shard_pack; sel_kv[r] [B kp, row_elems] (and
+ *   sel_scale[r] [B kp]), kp = CP_SPARSE_SLOT_ROWS(k), receive the selected
+ *   rows of request b at rows b kp .. b kp + pair_count[r B + b] - 1, in
+ *   token order, and zeros up to the next multiple of 128 rows (the decode
+ *   reads whole 128-row tiles; a row past the count enters with weight 0 and
+ *   must hold finite values); pair_count [C B] int32 device.  Call once per
+ *   array (K and V for GQA).
+ * cp_sparse_plan: the decode plan over those selection buffers (room for kp
+ *   rows per pair; the rows in use are pair_count's, read on the device).
+ * cp_sparse_decode_attn: cp_decode_attn over the selection buffers with
+ *   that plan and pair_count; same shapes and outputs (o_part [C, B, H, Dv],
+ *   lse_part [C, B, H]); ws: cp_decode_workspace_size(sparse plan).
+ * Errors: CP_ERR_INVALID_ARG for k outside [1, 4096], a selection plan given
+ *   to top-k or a cache plan to the sparse attention, NULL or misaligned
+ *   pointers; CP_ERR_UNSUPPORTED for a plan with s_q > 1; CP_ERR_WORKSPACE.
+ * ------------------------------------------------------------------------- */
+#define CP_SPARSE_SLOT_ROWS(k) ((((k) + 127) / 128) * 128)
+cp_status cp_sparse_workspace_size(const void* host_plan, int k, size_t* bytes);
+cp_status cp_sparse_topk(const void* host_plan, const void* dev_plan, const float* const* shard_scores,
+                         int k, int32_t* sel_ids, int32_t* sel_count, void* ws, size_t ws_bytes,
+                         void* stream);
+cp_status cp_sparse_gather(const void* host_plan, const void* dev_plan, int k, const void* ws,
+                           size_t ws_bytes, cp_dtype dtype, const void* const* shard_kv,
+                           const float* const* shard_scale, int row_elems, void* const* sel_kv,
+                           float* const* sel_scale, int32_t* pair_count, void* stream);
+cp_status cp_sparse_plan_size(int C, int B, int k, int n_workers, size_t* host_bytes,
+                              size_t* dev_bytes);
+cp_status cp_sparse_plan(int C, int B, int k, int n_workers, void* host_plan, size_t host_bytes,
+                         void* dev_plan, size_t dev_bytes, void* stream);
+cp_status cp_sparse_decode_attn(const void* host_plan, const void* dev_plan, const int32_t* pair_count,
+                                cp_decode_mode mode, cp_dtype kv_dtype, const void* q,
+                                const void* const* sel_k, const void* const* sel_v,
+                                const float* const* sel_scale, int Hq, int Hkv, int Dqk, int Dv,
+                                float sm_scale, float* o_part, float* lse_part, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Paged token-sharded decode cache ("How GPUs Share a Long Context During LLM

@@ -481,6 +481,48 @@ def query_rows_partials(q_rows: np.ndarray, kcache: np.ndarray, vcache: np.ndarr
     return outs, lses
 
 
+def sharded_topk(scores, C: int, k: int, contiguous: bool = False):
+    """Exact global top-k from shard-local top-k lists.
+
+    [V4] §5.2, steps 2-4: each rank scores only its own tokens, keeps a local
+    top-k list of (score, token), and the at most C k candidates are merged
+    into the global top-k; the union of the local lists contains the global
+    top-k, so the merge is exact.  [CTX] §4.1 describes the same exchange of
+    best candidates when the index is split with the cache.  Order: higher
+    score first; equal scores by lower token index (reading: the pages only
+    ask for deterministic ties).
+
+    scores [L] (the index scan's output per token).  Returns the selected
+    token indices in increasing order and the C local lists.
+    """
+    L = len(scores)
+    shard, _ = (decode_shard_map_contiguous if contiguous else decode_shard_map)(L, C)
+    better = lambda p: (-float(scores[p]), p)  # noqa: E731
+    local = []
+    for r in range(C):
+        mine = [p for p in range(L) if shard[p] == r]
+        local.append(sorted(mine, key=better)[:k])
+    candidates = [p for lst in local for p in lst]
+    chosen = sorted(candidates, key=better)[:k]
+    return sorted(chosen), local
+
+
+def sparse_partials(q: np.ndarray, kcache: np.ndarray, vcache: np.ndarray, selected, C: int,
+                    sm_scale: float, contiguous: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """[V4] §5.2, steps 5-7: the selected tokens go to the shards that store
+    them and each shard attends to its own selected tokens; the partials
+    combine exactly.  Returns O [C, H, Dv], LSE [C, H]."""
+    L = kcache.shape[0]
+    shard, _ = (decode_shard_map_contiguous if contiguous else decode_shard_map)(L, C)
+    outs, lses = [], []
+    for r in range(C):
+        keys = np.asarray([p for p in selected if shard[p] == r], dtype=np.int64)
+        o, lse = decode_attention(q, kcache, vcache, sm_scale, keys=keys)
+        outs.append(o)
+        lses.append(lse)
+    return np.stack(outs), np.stack(lses)
+
+
 def designated_partials(q: np.ndarray, kmain: np.ndarray, vmain: np.ndarray, kwin: np.ndarray,
                         vwin: np.ndarray, C: int, designated: int,
                         sm_scale: float) -> tuple[np.ndarray, np.ndarray]:

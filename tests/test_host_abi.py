@@ -270,3 +270,26 @@ def test_decode_plan_ex_validation(cp):
         cp.cp_decode_plan_ex(4, [10, 2], s_q=3)
     plan = cp.cp_decode_plan_ex(4, [10, 3], s_q=3, n_workers=5)
     assert plan.query_rows == 3 and plan.layout == 0
+
+
+def test_sparse_plan_and_argument_validation(cp):
+    splan = cp.cp_sparse_plan(4, 3, 16, n_workers=5)
+    assert splan.layout == cp.CP_DCP_SELECTED
+    # every (shard, request) pair has room for kp = 128 rows at row b kp of its shard
+    for r in range(4):
+        for b in range(3):
+            rows, row_off = splan.pairs[r * 3 + b, :2]
+            assert rows == 128 and row_off == 128 * b
+    assert cp.sparse_slot_rows(512) == 512 and cp.sparse_slot_rows(513) == 640
+    for k in (0, 4097):
+        with pytest.raises(cp.CpError, match="INVALID_ARG"):
+            cp.cp_sparse_plan(4, 3, k, n_workers=5)
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):  # top-k runs on a cache plan
+        cp.cp_sparse_workspace_size(splan, 16)
+    with pytest.raises(cp.CpError, match="INVALID_ARG"):  # selection plans come from cp_sparse_plan
+        cp.cp_decode_plan_ex(4, [10], layout=cp.CP_DCP_SELECTED, n_workers=5)
+    mtp = cp.cp_decode_plan_ex(4, [10, 12], s_q=2, n_workers=5)
+    with pytest.raises(cp.CpError, match="UNSUPPORTED"):
+        cp.cp_sparse_workspace_size(mtp, 8)
+    plan = cp.cp_decode_plan_ex(4, [10, 12], n_workers=5)
+    assert cp.cp_sparse_workspace_size(plan, 8) >= 4 * 2 * 8 * 8

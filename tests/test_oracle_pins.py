@@ -589,3 +589,79 @@ def test_query_rows_pin_catches_off_by_one(monkeypatch):
         o, _ = oracle.lse_merge(po, pl)
         monkeypatch.setattr(oracle.cpattn_oracle, "decode_attention", real)
         assert not np.allclose(o, ref[L - s_q:], atol=1e-6)
+
+
+# ------------------------------------------------------------------ exact sharded top-k
+
+
+def _global_topk(scores, k):
+    """Brute force: every token ranked at once (higher score, then lower index)."""
+    return sorted(sorted(range(len(scores)), key=lambda p: (-float(scores[p]), p))[:k])
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+def test_sharded_topk_equals_global_topk(contiguous):
+    """[V4] §5.2: the union of the local top-k lists contains the global
+    top-k, so merging them is exact — against brute force, ties included."""
+    rng = np.random.default_rng(11)
+    for L, C, k in [(1, 1, 1), (20, 4, 5), (37, 8, 1), (100, 3, 17), (64, 8, 64), (50, 7, 80)]:
+        for ties in (False, True):
+            s = rng.standard_normal(L).astype(np.float32)
+            if ties:
+                s = np.round(s * 2) / 2  # few distinct values, many ties
+            got, local = oracle.sharded_topk(s, C, k, contiguous=contiguous)
+            assert got == _global_topk(s, k)
+            assert len(got) == min(k, L)
+            shard, _ = (oracle.decode_shard_map_contiguous if contiguous else oracle.decode_shard_map)(L, C)
+            for r, lst in enumerate(local):
+                assert len(lst) == min(k, shard.count(r)) and all(shard[p] == r for p in lst)
+
+
+def test_sharded_topk_tie_rule_and_all_selected():
+    s = np.zeros(30, np.float32)
+    assert oracle.sharded_topk(s, 4, 7)[0] == list(range(7))  # equal scores: lower index first
+    s = np.arange(10, dtype=np.float32)
+    assert oracle.sharded_topk(s, 3, 50)[0] == list(range(10))  # k >= L: everything
+    assert oracle.sharded_topk(s, 3, 3)[0] == [7, 8, 9]
+
+
+def test_sharded_topk_pin_catches_short_local_lists(monkeypatch):
+    """Local lists cut to k / C (a plausible shortcut) lose exactness when the
+    best tokens sit on one shard; the brute-force pin catches it."""
+    L, C, k = 64, 4, 8
+    s = np.zeros(L, np.float32)
+    s[::C] = 10 + np.arange(L // C)  # shard 0 holds every high score
+    got, _ = oracle.sharded_topk(s, C, k)
+    assert got == _global_topk(s, k)
+    # plant: each shard keeps only k // C candidates
+    orig = oracle.cpattn_oracle.sharded_topk
+
+    def planted(scores, C, k, contiguous=False):
+        shard, _ = oracle.decode_shard_map(len(scores), C)
+        better = lambda p: (-float(scores[p]), p)  # noqa: E731
+        local = [sorted([p for p in range(len(scores)) if shard[p] == r], key=better)[:k // C]
+                 for r in range(C)]
+        return sorted(sorted([p for lst in local for p in lst], key=better)[:k]), local
+    monkeypatch.setattr(oracle.cpattn_oracle, "sharded_topk", planted)
+    assert oracle.cpattn_oracle.sharded_topk(s, C, k)[0] != _global_topk(s, k)
+    monkeypatch.setattr(oracle.cpattn_oracle, "sharded_topk", orig)
+
+
+def test_sparse_partials_merge_to_attention_over_selection():
+    rng = np.random.default_rng(4)
+    L, H, D = 40, 3, 8
+    q = rng.standard_normal((H, D))
+    k = rng.standard_normal((L, 1, D))
+    v = rng.standard_normal((L, 1, D))
+    s = rng.standard_normal(L).astype(np.float32)
+    for C, kk, contiguous in [(1, 9, False), (4, 9, False), (4, 9, True), (8, 50, False)]:
+        sel, _ = oracle.sharded_topk(s, C, kk, contiguous=contiguous)
+        po, pl = oracle.sparse_partials(q, k, v, sel, C, 0.4, contiguous=contiguous)
+        o, lse = oracle.lse_merge(po, pl)
+        # against torch: softmax over the selected tokens only
+        qs = torch.from_numpy(q)
+        ks = torch.from_numpy(k[sel, 0])
+        vs = torch.from_numpy(v[sel, 0])
+        sc = qs @ ks.T * 0.4
+        assert np.allclose(o, (torch.softmax(sc, -1) @ vs).numpy(), atol=1e-12)
+        assert np.allclose(lse, torch.logsumexp(sc, -1).numpy(), atol=1e-12)
