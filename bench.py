@@ -260,6 +260,65 @@ def run_reference(args, world, rank):
 # --------------------------------------------------------------------------- GPU arm
 
 
+def sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, world, rank):
+    """Top-k over per-token relevance scores on every shard, the exact merge,
+    the owners' gather and attention over the selected rows, and the LSE merge,
+    each stage timed with CUDA events; inputs resident in HBM."""
+    if args.decode_paged or args.decode_rows > 1 or args.decode_layout != "round_robin":
+        raise SystemExit("--sparse-k runs on the round-robin, one-row, per-shard cache")
+    k, C, B, L = args.sparse_k, m["C"], len(ctx), ctx[0]
+    scores = W.index_scores(ctx, seed=W.SEEDS["index"] + rank, device=dev)
+    st = scores.view(B, L // C, C)  # round robin: shard r holds tokens r, r + C, ...
+    shard_scores = [st[:, :, r].contiguous().view(-1) for r in range(C)]
+    del scores, st
+    splan = cp.cp_sparse_plan(C, B, k, device=dev)
+    sel_ids, sel_cnt, ws = cp.cp_sparse_topk(dplan, shard_scores, k)
+    selk, selsc, pc = cp.cp_sparse_gather(dplan, k, ws, shards, scales)
+    Hr, Dv = m["H"], m["Dv"]
+    o_part = torch.empty((C, B, Hr, Dv), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((C, B, Hr), dtype=torch.float32, device=dev)
+    o_dec = torch.empty((B, Hr, Dv), dtype=torch.bfloat16, device=dev)
+    lse_dec = torch.empty((B, Hr), dtype=torch.float32, device=dev)
+    dws = torch.empty(max(16, cp.cp_decode_workspace_size(splan, Hr, Dv)), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(m["Dqk"])
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(e):
+        e[0].record(stream)
+        cp.cp_sparse_topk(dplan, shard_scores, k, sel_ids, sel_cnt, ws)
+        e[1].record(stream)
+        cp.cp_sparse_gather(dplan, k, ws, shards, scales, selk, selsc, pc)
+        e[2].record(stream)
+        cp.cp_sparse_decode_attn(splan, pc, cp.CP_DECODE_MLA, dq, selk, sel_scale=selsc,
+                                 sm_scale=scale, o_part=o_part, lse_part=lse_part, ws=dws)
+        e[3].record(stream)
+        cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
+        e[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step([ev() for _ in range(5)])
+    torch.cuda.synchronize(dev)
+    cp.cp_device_error_check(dev)
+    recs = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        step(recs[i])
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    cp.cp_device_error_check(dev)
+    stage = [[r[i].elapsed_time(r[i + 1]) for r in recs] for i in range(4)]
+    total = max_over_ranks(sum(sum(x) for x in stage), world)
+    row = 580 if fp8 else 1152
+    alg = 4 * sum(ctx) + B * k * row + B * Hr * 576 * 2 + B * Hr * 512 * 2
+    return {"k": k, "workload": f"{B} x {L} tokens, C={C}, top-{k} of per-token fp32 scores, "
+                                f"MLA {'FP8' if fp8 else 'bf16'} rows",
+            "ms": {"topk": statistics.mean(stage[0]), "gather": statistics.mean(stage[1]),
+                   "decode": statistics.mean(stage[2]), "merge": statistics.mean(stage[3])},
+            "algorithmic_bytes_per_step": alg,
+            "value": whole_job_rate(alg * args.steps, total, world) / 1e9, "unit": "GB/s",
+            "note": "scores read once + selected rows once + Q + O over the time of all four stages"}
+
+
 def run_ours(args, world, rank, local):
     import context_long_attention_gb300 as cp
 
@@ -418,6 +477,11 @@ def run_ours(args, world, rank, local):
                "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
                "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4}
 
+    # ---- sparse decode with an exact sharded top-k (timed on its own)
+    sparse = None
+    if do_dec and args.sparse_k:
+        sparse = sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, world, rank)
+
     if rank != 0:
         return
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -475,6 +539,7 @@ def run_ours(args, world, rank, local):
             "parallelism": "virtual CP=8 on each GPU; replicas across GPUs",
         },
         "decode": dec,
+        "sparse_decode": sparse,
         "ms_breakdown": {"plan": statistics.mean(plan_ms), "prefill": statistics.mean(pre_ms),
                          "decode": statistics.mean(dec_ms), "merge": statistics.mean(mrg_ms)},
         "roofline": roof,
@@ -504,6 +569,8 @@ def main():
                     help="decode token shards: token p on shard p mod C, or C contiguous chunks")
     ap.add_argument("--decode-rows", type=int, default=1, metavar="S_Q",
                     help="query rows per request (MTP); the 64 heads split into S_Q rows of 64/S_Q")
+    ap.add_argument("--sparse-k", type=int, default=0, metavar="K",
+                    help="also time sparse decode over the exact sharded top-K of per-token scores")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()

@@ -937,9 +937,11 @@ cp_status cp_sparse_topk(const void* host_plan, const void* dev_plan, const floa
     if (pair_rows_of_shard(h, W, r) > 0 && !shard_scores[r])
       return fail(CP_ERR_INVALID_ARG, "shard_scores[%d] is NULL", r);
   }
+  int max_rows = 0;
+  for (int i = 0; i < h.C * h.R; ++i) max_rows = std::max(max_rows, W[h.off_rank + kPairWords * i]);
   const TopkWs w = topk_ws(h, k, ws);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_topk_local((const int32_t*)dev_plan, h, sc, k, w.cand_keys, w.cand_n, s);
+  cudaError_t e = launch_topk_local((const int32_t*)dev_plan, h, sc, k, max_rows, w.cand_keys, w.cand_n, s);
   if (e != cudaSuccess) return cuda_fail(e, "local top-k kernel");
   e = launch_topk_merge(h, k, w.cand_keys, w.cand_n, w.thresh, sel_ids, sel_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "top-k merge kernel");

@@ -23,7 +23,8 @@
 namespace cpattn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: the select's loops are latency-bound
+constexpr int kMaxTopK = 4096;  // largest k (the API rejects more)
 constexpr unsigned kFull = 0xffffffffu;
 
 // float -> uint32 that increases with the float (NaN excluded; -0 ranks as +0).
@@ -41,128 +42,196 @@ __device__ __forceinline__ int key_token(uint64_t key) {
   return (int)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
 }
 
-// The k-th largest (k >= 1) of n distinct keys get(0..n-1), n >= k, by radix
-// select from the top byte down.  All threads of the block call it.
-template <typename Get>
-__device__ uint64_t kth_largest(int n, int k, Get get, uint32_t* hist, uint32_t* pick) {
-  uint64_t prefix = 0, mask = 0;
-  int want = k;  // rank still sought among the keys matching the prefix
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const uint64_t key = get(i);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // lane l counts bins 255 - 8l .. 248 - 8l (from the top); a scan over
-      // the lanes finds the bin holding the wanted rank
-      const int lane = threadIdx.x;
-      uint32_t c[8], sum = 0;
+constexpr int kWarps = kThreads / 32;
+constexpr int kSmallKeys = 2048;  // keys the select finishes on in shared memory (a power of two)
+constexpr int kStageScores = 32768;  // a pair's scores staged in shared memory up to this many
+constexpr int kStageKeys = 16384;    // a request's candidates staged in shared memory up to this many
+
+// Ordered compaction: calls emit(i, j) for every i in [0, n) with pred(i), j
+// counting those before i; returns their number.  Each warp takes one
+// contiguous segment of [0, n) in steps of 32 (coalesced, conflict-free in
+// shared memory): a counting pass, one scan of the warps' totals, a writing
+// pass.  All threads of the block call it; warp_cnt is kWarps ints.
+template <typename Pred, typename Emit>
+__device__ int block_compact(int n, Pred pred, Emit emit, int* warp_cnt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (n + kWarps - 1) / kWarps;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  int cnt = 0;
+  for (int b = s0; b < s1; b += 32) cnt += __popc(__ballot_sync(kFull, b + lane < s1 && pred(b + lane)));
+  if (lane == 0) warp_cnt[warp] = cnt;
+  __syncthreads();
+  int at = 0, tot = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - 8 * lane - j];
-        sum += c[j];
-      }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t v = __shfl_up_sync(kFull, incl, d);
-        if (lane >= d) incl += v;
-      }
-      const uint32_t excl = incl - sum;
-      if (excl < (uint32_t)want && (uint32_t)want <= incl) {
-        uint32_t above = excl;
-        int bin = 255 - 8 * lane;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (above + c[j] >= (uint32_t)want) {
-            bin = 255 - 8 * lane - j;
-            break;
-          }
-          above += c[j];
-        }
-        pick[0] = (uint32_t)bin;
-        pick[1] = above;  // keys with this prefix in higher bins
-      }
-    }
-    __syncthreads();
-    prefix |= (uint64_t)pick[0] << shift;
-    mask |= (uint64_t)255u << shift;
-    want -= (int)pick[1];
-    __syncthreads();
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = warp_cnt[w];
+    at += w < warp ? c : 0;
+    tot += c;
   }
-  return prefix;
+  for (int b = s0; b < s1; b += 32) {
+    const bool f = b + lane < s1 && pred(b + lane);
+    const unsigned bal = __ballot_sync(kFull, f);
+    if (f) emit(b + lane, at + __popc(bal & ((1u << lane) - 1u)));
+    at += __popc(bal);
+  }
+  __syncthreads();
+  return tot;
 }
 
-// Exclusive prefix sum over the block of one int per thread (256 threads).
-__device__ int block_exclusive_sum(int v, int* warp_sums, int* total) {
+// Unordered collection of the i in [0, n) with pred(i) into out[]: one shared
+// counter, one atomic per warp and step.  Returns the number (all threads).
+template <typename Pred, typename Get>
+__device__ int block_collect(int n, Pred pred, Get value, uint64_t* out, int* counter) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) *counter = 0;
+  __syncthreads();
+  for (int b = 0; b < n; b += blockDim.x) {
+    const int i = b + threadIdx.x;
+    const bool f = i < n && pred(i);
+    const unsigned bal = __ballot_sync(kFull, f);
+    int base = 0;
+    if (lane == 0 && bal) base = atomicAdd(counter, __popc(bal));
+    base = __shfl_sync(kFull, base, 0);
+    if (f) out[base + __popc(bal & ((1u << lane) - 1u))] = value(i);
+  }
+  __syncthreads();
+  return *counter;
+}
+
+// Bytes of the merge's token list in shared memory, padded to 16 so that the
+// 64-bit keys staged after it stay aligned.
+__host__ __device__ __forceinline__ size_t ids_bytes(int kpow2) {
+  return ((size_t)kpow2 * sizeof(int32_t) + 15) & ~(size_t)15;
+}
+
+constexpr int kTopBins = 4096;  // the first pass splits on the key's top 12 bits
+
+// Shared scratch of the radix select.
+struct __align__(16) SelectSmem {
+  uint32_t hist[kTopBins];
+  uint32_t pick[4];
+  int small_n;
+  int warp_cnt[kWarps];
+  uint64_t small[kSmallKeys];
+};
+
+// Finds, among the NB bins of hist taken from the top, the one that holds
+// rank `want` (1-based): pick = {bin, keys in higher bins, keys in it}.  Each
+// thread owns NB / blockDim consecutive bins (one, or none, when NB is
+// smaller than the block); one block-wide scan.
+template <int NB>
+__device__ void pick_bin(const uint32_t* hist, int want, uint32_t* pick, int* warp_cnt) {
+  constexpr int PER = NB >= kThreads ? NB / kThreads : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  const int top = NB - 1 - PER * (int)threadIdx.x;  // this thread's highest bin (< 0: none)
+  uint32_t c[PER], sum = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    c[j] = top - j >= 0 ? hist[top - j] : 0u;
+    sum += c[j];
+  }
+  uint32_t incl = sum;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    const int t = __shfl_up_sync(kFull, incl, d);
-    if (lane >= d) incl += t;
+    const uint32_t v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
   }
-  if (lane == 31) warp_sums[warp] = incl;
+  if (lane == 31) warp_cnt[warp] = (int)incl;
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < kThreads / 32 ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int t = __shfl_up_sync(kFull, w, d);
-      if (lane >= d) w += t;
+  uint32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += (uint32_t)warp_cnt[w];
+  const uint32_t excl = before + incl - sum;
+  if (excl < (uint32_t)want && (uint32_t)want <= excl + sum) {
+    uint32_t above = excl;
+    int j = 0;
+    for (; j < PER - 1 && above + c[j] < (uint32_t)want; ++j) above += c[j];
+    pick[0] = (uint32_t)(top - j);
+    pick[1] = above;
+    pick[2] = c[j];
+  }
+  __syncthreads();
+}
+
+// The k-th largest (k >= 1) of n distinct keys get(0..n-1), n >= k.  A first
+// pass over the keys' top 12 bits finds the bin holding rank k; 8-bit passes
+// then fix the lower bits, over all n keys until the keys still in play fit
+// in shared memory (kSmallKeys; they are then collected once) and over those
+// from there on.  All threads of the block call it.
+template <typename Get>
+__device__ uint64_t kth_largest(int n, int k, Get get, SelectSmem& sm) {
+  for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&sm.hist[get(i) >> 52], 1u);
+  __syncthreads();
+  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
+  uint64_t prefix = (uint64_t)sm.pick[0] << 52, mask = 0xFFFull << 52;
+  int want = k - (int)sm.pick[1];
+  int in_bin = (int)sm.pick[2];
+  int m = -1;  // keys collected in sm.small, once they fit
+  for (int shift = 44;; shift = shift >= 8 ? shift - 8 : 0) {
+    if (m < 0 && in_bin <= kSmallKeys)
+      m = block_collect(n, [&](int i) { return (get(i) & mask) == prefix; }, get, sm.small,
+                        &sm.small_n);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
+    __syncthreads();
+    const int cnt = m < 0 ? n : m;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      const uint64_t key = m < 0 ? get(i) : sm.small[i];
+      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], 1u);
     }
-    if (lane < kThreads / 32) warp_sums[lane] = w;  // inclusive over warps
-    if (lane == kThreads / 32 - 1) *total = w;
+    __syncthreads();
+    pick_bin<256>(sm.hist, want, sm.pick, sm.warp_cnt);
+    prefix = (prefix & ~(255ull << shift)) | ((uint64_t)sm.pick[0] << shift);
+    mask |= 255ull << shift;
+    want -= (int)sm.pick[1];
+    in_bin = (int)sm.pick[2];
+    if (shift == 0) return prefix;  // all 64 bits fixed
   }
-  __syncthreads();
-  const int before = warp == 0 ? 0 : warp_sums[warp - 1];
-  const int r = before + incl - v;
-  __syncthreads();
-  return r;
 }
 
 // Local top-k of every (shard, request) pair: candidate keys in token order.
 __global__ void __launch_bounds__(kThreads)
     topk_local_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
-                      ScorePtrs scores, int k, uint64_t* __restrict__ cand_keys,
+                      ScorePtrs scores, int k, int stage_cap, uint64_t* __restrict__ cand_keys,
                       int32_t* __restrict__ cand_n) {
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t pick[2];
-  __shared__ int warp_sums[kThreads / 32];
-  __shared__ int total;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
   const int pair = blockIdx.x;
   const cp_pair_desc pd = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[pair];
   const int r = pair / B;
   const int n = pd.rows;
   const float* sc = scores.p[r] + pd.row_off;
-  auto get = [&](int i) { return token_key(__ldg(sc + i), pd.tok0 + i * pd.tok_step); };
-  const uint64_t thresh = n > k ? kth_largest(n, k, get, hist, pick) : 0ull;
-  // ordered compaction: thread t takes rows [t per, (t + 1) per)
-  const int per = (n + kThreads - 1) / kThreads;
-  const int i0 = min(n, threadIdx.x * per), i1 = min(n, i0 + per);
-  int mine = 0;
-  for (int i = i0; i < i1; ++i) mine += get(i) >= thresh;
-  int at = block_exclusive_sum(mine, warp_sums, &total);
-  uint64_t* out = cand_keys + (long long)pair * k;
-  for (int i = i0; i < i1; ++i) {
-    const uint64_t key = get(i);
-    if (key >= thresh) out[at++] = key;
+  // Every pass reads the pair's scores: stage them in shared memory once,
+  // eight independent loads in flight per thread (the passes would otherwise
+  // wait out an L2 round trip per element).
+  float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem));
+  const bool st = n <= stage_cap;
+  if (st) {
+#pragma unroll 8
+    for (int i = threadIdx.x; i < n; i += blockDim.x) staged[i] = __ldg(sc + i);
+    __syncthreads();
   }
-  if (threadIdx.x == 0) cand_n[pair] = total;
+  auto get = [&](int i) {
+    return token_key(st ? staged[i] : __ldg(sc + i), pd.tok0 + i * pd.tok_step);
+  };
+  const uint64_t thresh = n > k ? kth_largest(n, k, get, sm) : 0ull;
+  // the candidates in token order
+  uint64_t* out = cand_keys + (long long)pair * k;
+  const int got = block_compact(
+      n, [&](int i) { return get(i) >= thresh; }, [&](int i, int j) { out[j] = get(i); },
+      sm.warp_cnt);
+  if (threadIdx.x == 0) cand_n[pair] = got;
 }
 
 // Merge of one request's candidates: the global k-th key (the selection
 // threshold) and the selected tokens in increasing order.
 __global__ void __launch_bounds__(kThreads)
     topk_merge_kernel(int C, int B, int k, int kpow2, const uint64_t* __restrict__ cand_keys,
-                      const int32_t* __restrict__ cand_n, uint64_t* __restrict__ thresh,
+                      const int32_t* __restrict__ cand_n, int stage_cap, uint64_t* __restrict__ thresh,
                       int32_t* __restrict__ sel_ids, int32_t* __restrict__ sel_count) {
-  extern __shared__ int32_t ids[];  // kpow2 entries
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t pick[2];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
+  int32_t* ids = reinterpret_cast<int32_t*>(smem_raw + sizeof(SelectSmem));  // kpow2 entries
   __shared__ int start[CP_MAX_SHARDS + 1];
   __shared__ int n_sel;
   const int b = blockIdx.x;
@@ -177,18 +246,31 @@ __global__ void __launch_bounds__(kThreads)
   }
   __syncthreads();
   const int N = start[C];
-  auto get = [&](int i) {
+  auto get_global = [&](int i) {
     int r = 0;
     while (start[r + 1] <= i) ++r;
     return cand_keys[(long long)(r * B + b) * k + (i - start[r])];
   };
-  const uint64_t t = N > k ? kth_largest(N, k, get, hist, pick) : 0ull;
+  // stage the candidates in shared memory when they fit (see topk_local_kernel)
+  uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + ids_bytes(kpow2));
+  const bool st = N <= stage_cap;
+  if (st) {
+    for (int r = 0; r < C; ++r) {
+      const uint64_t* src = cand_keys + (long long)(r * B + b) * k;
+      const int n_r = start[r + 1] - start[r];
+#pragma unroll 8
+      for (int i = threadIdx.x; i < n_r; i += blockDim.x) staged[start[r] + i] = src[i];
+    }
+    __syncthreads();
+  }
+  auto get = [&](int i) { return st ? staged[i] : get_global(i); };
+  const uint64_t t = N > k ? kth_largest(N, k, get, sm) : 0ull;
   for (int i = threadIdx.x; i < kpow2; i += blockDim.x) ids[i] = 0x7FFFFFFF;
   __syncthreads();
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    const uint64_t key = get(i);
-    if (key >= t) ids[atomicAdd(&n_sel, 1)] = key_token(key);
-  }
+  const int got = block_compact(
+      N, [&](int i) { return get(i) >= t; }, [&](int i, int j) { ids[j] = key_token(get(i)); },
+      sm.warp_cnt);
+  if (threadIdx.x == 0) n_sel = got;
   __syncthreads();
   // bitonic sort of the selected token indices, ascending
   for (int size = 2; size <= kpow2; size <<= 1)
@@ -226,58 +308,50 @@ __global__ void __launch_bounds__(kThreads)
                          const uint64_t* __restrict__ thresh, ShardPtrs src, ScalePtrs src_scale,
                          int row_vec, MutShardPtrs dst, MutScalePtrs dst_scale, int has_scale,
                          int32_t* __restrict__ pair_count) {
-  __shared__ int warp_sums[kThreads / 32];
-  __shared__ int total;
-  __shared__ int rows[1024];  // source rows of this pair's selected tokens (chunk)
+  __shared__ int warp_cnt[kWarps];
+  __shared__ int rows[kMaxTopK];  // source rows of this pair's selected tokens, in token order
   const int pair = blockIdx.x;
   const int r = pair / B, b = pair % B;
   const cp_pair_desc pd = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[pair];
   const int n = cand_n[pair];
   const uint64_t t = thresh[b];
   const uint64_t* keys = cand_keys + (long long)pair * k;
+  const int count = block_compact(
+      n, [&](int i) { return keys[i] >= t; },
+      [&](int i, int j) { rows[j] = (key_token(keys[i]) - pd.tok0) / pd.tok_step; }, warp_cnt);
+  // one warp per row: 16-byte copies
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int base = 0;  // selected rows written so far
-  for (int c0 = 0; c0 < n; c0 += 1024) {
-    const int cn = min(1024, n - c0);
-    const int per = (cn + kThreads - 1) / kThreads;
-    const int i0 = min(cn, threadIdx.x * per), i1 = min(cn, i0 + per);
-    int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += keys[c0 + i] >= t;
-    int at = block_exclusive_sum(mine, warp_sums, &total);
-    for (int i = i0; i < i1; ++i) {
-      const uint64_t key = keys[c0 + i];
-      if (key >= t) rows[at++] = (key_token(key) - pd.tok0) / pd.tok_step;
-    }
-    __syncthreads();
-    const int got = total;
-    // one warp per row: 16-byte copies
-    for (int j = warp; j < got; j += kThreads / 32) {
-      const long long srow = (long long)pd.row_off + rows[j];
-      const long long drow = (long long)b * kp + base + j;
-      const uint4* s = static_cast<const uint4*>(src.p[r]) + srow * row_vec;
-      uint4* d = static_cast<uint4*>(dst.p[r]) + drow * row_vec;
-      for (int c = lane; c < row_vec; c += 32) d[c] = s[c];
-      if (has_scale && lane == 0) dst_scale.p[r][drow] = src_scale.p[r][srow];
-    }
-    base += got;
-    __syncthreads();
-  }
-  const int pad_end = min(kp, (base + kDecodeTileRows - 1) / kDecodeTileRows * kDecodeTileRows);
-  for (int j = base + warp; j < pad_end; j += kThreads / 32) {
+  for (int j = warp; j < count; j += kWarps) {
+    const long long srow = (long long)pd.row_off + rows[j];
     const long long drow = (long long)b * kp + j;
-    uint4* d = static_cast<uint4*>(dst.p[r]) + drow * row_vec;
-    for (int c = lane; c < row_vec; c += 32) d[c] = make_uint4(0, 0, 0, 0);
+    const uint4* sp = static_cast<const uint4*>(src.p[r]) + srow * row_vec;
+    uint4* dp = static_cast<uint4*>(dst.p[r]) + drow * row_vec;
+    for (int c = lane; c < row_vec; c += 32) dp[c] = sp[c];
+    if (has_scale && lane == 0) dst_scale.p[r][drow] = src_scale.p[r][srow];
+  }
+  const int pad_end = min(kp, (count + kDecodeTileRows - 1) / kDecodeTileRows * kDecodeTileRows);
+  for (int j = count + warp; j < pad_end; j += kWarps) {
+    const long long drow = (long long)b * kp + j;
+    uint4* dp = static_cast<uint4*>(dst.p[r]) + drow * row_vec;
+    for (int c = lane; c < row_vec; c += 32) dp[c] = make_uint4(0, 0, 0, 0);
     if (has_scale && lane == 0) dst_scale.p[r][drow] = 0.f;
   }
-  if (threadIdx.x == 0) pair_count[pair] = base;
+  if (threadIdx.x == 0) pair_count[pair] = count;
 }
 
 }  // namespace
 
 cudaError_t launch_topk_local(const int32_t* dev_plan, const cp_plan_header& h, const ScorePtrs& scores,
-                              int k, uint64_t* cand_keys, int32_t* cand_n, cudaStream_t s) {
+                              int k, int max_pair_rows, uint64_t* cand_keys, int32_t* cand_n,
+                              cudaStream_t s) {
   const int pairs = h.C * h.R;
-  topk_local_kernel<<<pairs, kThreads, 0, s>>>(dev_plan, h.R, h.off_rank, scores, k, cand_keys, cand_n);
+  // room to stage the longest pair's scores, up to kStageScores (longer pairs read from L2)
+  const int cap = max_pair_rows < kStageScores ? max_pair_rows : kStageScores;
+  const int smem = (int)sizeof(SelectSmem) + cap * (int)sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(topk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  topk_local_kernel<<<pairs, kThreads, smem, s>>>(dev_plan, h.R, h.off_rank, scores, k, cap, cand_keys,
+                                                  cand_n);
   return cudaGetLastError();
 }
 
@@ -286,13 +360,12 @@ cudaError_t launch_topk_merge(const cp_plan_header& h, int k, const uint64_t* ca
                               int32_t* sel_count, cudaStream_t s) {
   int kpow2 = 1;
   while (kpow2 < k) kpow2 <<= 1;
-  const size_t smem = (size_t)kpow2 * sizeof(int32_t);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  topk_merge_kernel<<<h.R, kThreads, smem, s>>>(h.C, h.R, k, kpow2, cand_keys, cand_n, thresh,
+  const int cap = h.C * k < kStageKeys ? h.C * k : kStageKeys;
+  const size_t smem = sizeof(SelectSmem) + ids_bytes(kpow2) + (size_t)cap * sizeof(uint64_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<h.R, kThreads, smem, s>>>(h.C, h.R, k, kpow2, cand_keys, cand_n, cap, thresh,
                                                  sel_ids, sel_count);
   return cudaGetLastError();
 }
