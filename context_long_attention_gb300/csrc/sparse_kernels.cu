@@ -157,11 +157,12 @@ __device__ void pick_bin(const uint32_t* hist, int want, uint32_t* pick, int* wa
 // then fix the lower bits, over all n keys until the keys still in play fit
 // in shared memory (kSmallKeys; they are then collected once) and over those
 // from there on.  All threads of the block call it.
-template <typename Get>
-__device__ uint64_t kth_largest(int n, int k, Get get, SelectSmem& sm) {
+template <typename Get, typename Top>
+__device__ uint64_t kth_largest(int n, int k, Get get, Top top12, SelectSmem& sm) {
+  // top12(i) == get(i) >> 52, possibly cheaper
   for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&sm.hist[get(i) >> 52], 1u);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&sm.hist[top12(i)], 1u);
   __syncthreads();
   pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
   uint64_t prefix = (uint64_t)sm.pick[0] << 52, mask = 0xFFFull << 52;
@@ -169,9 +170,13 @@ __device__ uint64_t kth_largest(int n, int k, Get get, SelectSmem& sm) {
   int in_bin = (int)sm.pick[2];
   int m = -1;  // keys collected in sm.small, once they fit
   for (int shift = 44;; shift = shift >= 8 ? shift - 8 : 0) {
-    if (m < 0 && in_bin <= kSmallKeys)
-      m = block_collect(n, [&](int i) { return (get(i) & mask) == prefix; }, get, sm.small,
-                        &sm.small_n);
+    if (m < 0 && in_bin <= kSmallKeys) {
+      const uint32_t bin12 = (uint32_t)(prefix >> 52);
+      m = shift == 44 ? block_collect(n, [&](int i) { return top12(i) == bin12; }, get, sm.small,
+                                      &sm.small_n)
+                      : block_collect(n, [&](int i) { return (get(i) & mask) == prefix; }, get,
+                                      sm.small, &sm.small_n);
+    }
     for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
     __syncthreads();
     const int cnt = m < 0 ? n : m;
@@ -211,15 +216,18 @@ __global__ void __launch_bounds__(kThreads)
     for (int i = threadIdx.x; i < n; i += blockDim.x) staged[i] = __ldg(sc + i);
     __syncthreads();
   }
-  auto get = [&](int i) {
-    return token_key(st ? staged[i] : __ldg(sc + i), pd.tok0 + i * pd.tok_step);
+  auto score = [&](int i) { return st ? staged[i] : __ldg(sc + i); };
+  auto get = [&](int i) { return token_key(score(i), pd.tok0 + i * pd.tok_step); };
+  auto top12 = [&](int i) { return ordered_bits(score(i)) >> 20; };
+  const uint64_t thresh = n > k ? kth_largest(n, k, get, top12, sm) : 0ull;
+  // the candidates in token order (the comparison split into two 32-bit halves)
+  const uint32_t th_hi = (uint32_t)(thresh >> 32), th_lo = (uint32_t)thresh;
+  auto keep = [&](int i) {
+    const uint32_t hi = ordered_bits(score(i));
+    return hi > th_hi || (hi == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
   };
-  const uint64_t thresh = n > k ? kth_largest(n, k, get, sm) : 0ull;
-  // the candidates in token order
   uint64_t* out = cand_keys + (long long)pair * k;
-  const int got = block_compact(
-      n, [&](int i) { return get(i) >= thresh; }, [&](int i, int j) { out[j] = get(i); },
-      sm.warp_cnt);
+  const int got = block_compact(n, keep, [&](int i, int j) { out[j] = get(i); }, sm.warp_cnt);
   if (threadIdx.x == 0) cand_n[pair] = got;
 }
 
@@ -264,7 +272,8 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
   }
   auto get = [&](int i) { return st ? staged[i] : get_global(i); };
-  const uint64_t t = N > k ? kth_largest(N, k, get, sm) : 0ull;
+  const uint64_t t = N > k ? kth_largest(N, k, get, [&](int i) { return (uint32_t)(get(i) >> 52); }, sm)
+                           : 0ull;
   for (int i = threadIdx.x; i < kpow2; i += blockDim.x) ids[i] = 0x7FFFFFFF;
   __syncthreads();
   const int got = block_compact(
@@ -319,16 +328,19 @@ __global__ void __launch_bounds__(kThreads)
   const int count = block_compact(
       n, [&](int i) { return keys[i] >= t; },
       [&](int i, int j) { rows[j] = (key_token(keys[i]) - pd.tok0) / pd.tok_step; }, warp_cnt);
-  // one warp per row: 16-byte copies
+  // 16-byte pieces of all the selected rows, spread over the block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int j = warp; j < count; j += kWarps) {
-    const long long srow = (long long)pd.row_off + rows[j];
-    const long long drow = (long long)b * kp + j;
-    const uint4* sp = static_cast<const uint4*>(src.p[r]) + srow * row_vec;
-    uint4* dp = static_cast<uint4*>(dst.p[r]) + drow * row_vec;
-    for (int c = lane; c < row_vec; c += 32) dp[c] = sp[c];
-    if (has_scale && lane == 0) dst_scale.p[r][drow] = src_scale.p[r][srow];
+  const uint4* sbase = static_cast<const uint4*>(src.p[r]);
+  uint4* dbase = static_cast<uint4*>(dst.p[r]) + (long long)b * kp * row_vec;
+  const int pieces = count * row_vec;
+#pragma unroll 4
+  for (int c = threadIdx.x; c < pieces; c += blockDim.x) {
+    const int j = c / row_vec, q = c - j * row_vec;
+    dbase[c] = __ldg(sbase + ((long long)pd.row_off + rows[j]) * row_vec + q);
   }
+  if (has_scale)
+    for (int j = threadIdx.x; j < count; j += blockDim.x)
+      dst_scale.p[r][(long long)b * kp + j] = src_scale.p[r][(long long)pd.row_off + rows[j]];
   const int pad_end = min(kp, (count + kDecodeTileRows - 1) / kDecodeTileRows * kDecodeTileRows);
   for (int j = count + warp; j < pad_end; j += kWarps) {
     const long long drow = (long long)b * kp + j;
