@@ -160,3 +160,39 @@ def test_paged_contiguous_query_rows_match_unpaged(cp):
                                        sm_scale=1.0 / math.sqrt(576))
     cp.cp_device_error_check()
     assert torch.equal(o_p.reshape(o_ref.shape), o_ref) and torch.equal(l_p.reshape(l_ref.shape), l_ref)
+
+
+def test_mla_query_rows_full_size_sampled(cp):
+    """64 requests x 131,072 tokens, 2 query rows of 32 heads, FP8, C = 8:
+    sampled requests and rows against the oracle."""
+    B, L, s_q, H, C = 64, 131072, 2, 32, 8
+    ctx = [L] * B
+    data = W.mla_decode_inputs(ctx, H=s_q * H, seed=55, device=DEV, bf16=False)
+    _, o_part, lse_part, o, lse = run_mla(cp, data, ctx, C, s_q, H, True, False)
+    scale = 1.0 / math.sqrt(576)
+    qn = np64(data["q"]).reshape(B, s_q, H, 576)
+    for b in (0, 41):
+        lat = oracle.e4m3_decode(data["kv_fp8"][b * L:(b + 1) * L].cpu().numpy())
+        K, V = oracle.mla_cache_to_kv(lat, data["kv_scale"][b * L:(b + 1) * L].double().cpu().numpy())
+        for i in range(s_q):
+            fo, fl = oracle.decode_attention(qn[b, i], K[:L - s_q + i + 1], V[:L - s_q + i + 1], scale)
+            check_o(o[b, i], fo, what=f"full-size MTP b{b} row{i}", **TOL_FP8)
+            check_lse(lse[b, i], fl)
+
+
+def test_gqa_paged_query_rows_match_unpaged(cp):
+    """GQA with 3 query rows over a paged pool: bit-identical to the per-shard buffers."""
+    ctx = [3, 130, 900]
+    B, Hq, Hkv, D, C, s_q = len(ctx), 8, 2, 64, 4, 3
+    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=66, device=DEV, std=0.3)
+    plan = cp.cp_decode_plan_ex(C, ctx, s_q=s_q, n_workers=5, device=DEV)
+    qq = q.reshape(B, s_q, Hq, D)
+    sk, _ = cp.cp_kv_shard_pack(plan, k)
+    sv, _ = cp.cp_kv_shard_pack(plan, v)
+    o_ref, l_ref = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, qq, sk, sv, sm_scale=0.125)
+    pages = make_pages(cp, plan, 64, seed=6)
+    kp, _ = cp.cp_kv_shard_pack_paged(plan, pages, k)
+    vp, _ = cp.cp_kv_shard_pack_paged(plan, pages, v)
+    o_p, l_p = cp.cp_decode_attn_paged(plan, pages, cp.CP_DECODE_GQA, qq, kp, vp, sm_scale=0.125)
+    cp.cp_device_error_check()
+    assert torch.equal(o_p, o_ref) and torch.equal(l_p, l_ref)

@@ -168,3 +168,34 @@ def test_sparse_decode(cp, kind, contiguous):
         fo, fl = oracle.decode_attention(qn, K, V, scale, keys=np.asarray(want[b], dtype=np.int64))
         check_o(o[b], fo, what=f"{kind} merged b{b}", **tol)
         check_lse(lse[b], fl)
+
+
+def test_sparse_decode_full_size_sampled(cp):
+    """64 x 131,072 tokens, C = 8, k = 2048, FP8: sampled requests' merged
+    sparse attention against the oracle over the oracle's selection."""
+    B, L, C, k = 64, 131072, 8, 2048
+    ctx = [L] * B
+    plan = cp.cp_decode_plan_ex(C, ctx, device=DEV)
+    scores = W.index_scores(ctx, seed=77, device=DEV)
+    st = scores.view(B, L // C, C)
+    shards_s = [st[:, :, r].contiguous().view(-1) for r in range(C)]
+    sel, cnt, ws = cp.cp_sparse_topk(plan, shards_s, k)
+    data = W.mla_decode_inputs(ctx, H=64, seed=78, device=DEV, bf16=False)
+    sh, sc = cp.cp_kv_shard_pack(plan, data["kv_fp8"], data["kv_scale"])
+    selk, selsc, pc = cp.cp_sparse_gather(plan, k, ws, sh, sc)
+    splan = cp.cp_sparse_plan(C, B, k, device=DEV)
+    scale = 1.0 / math.sqrt(576)
+    o_part, lse_part = cp.cp_sparse_decode_attn(splan, pc, cp.CP_DECODE_MLA, data["q"], selk,
+                                                sel_scale=selsc, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    s = scores.cpu().numpy()
+    for b in (3, 60):
+        sb = s[b * L:(b + 1) * L]
+        want = sorted(np.lexsort((np.arange(L), -sb.astype(np.float64)))[:k].tolist())
+        assert sel[b].tolist() == want
+        lat = oracle.e4m3_decode(data["kv_fp8"][b * L:(b + 1) * L].cpu().numpy())
+        K, V = oracle.mla_cache_to_kv(lat, data["kv_scale"][b * L:(b + 1) * L].double().cpu().numpy())
+        fo, fl = oracle.decode_attention(np64(data["q"][b]), K, V, scale, keys=np.asarray(want))
+        check_o(o[b], fo, what=f"full-size sparse b{b}", **TOL_FP8)
+        check_lse(lse[b], fl)
