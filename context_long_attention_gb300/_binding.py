@@ -591,3 +591,25 @@ def cp_sparse_decode_attn(plan: DecodePlan, pair_count, mode: int, q, sel_k, sel
                                      H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part), _ptr(lse_part),
                                      _ptr(ws), ws_bytes, _stream(q.device)))
     return o_part, lse_part
+
+
+# ---------------------------------------------------------------- NVTX ranges
+# With CPATTN_NVTX=1 every public entry point runs inside an NVTX range of
+# its own name, so a timeline profiler shows the path's steps (plan, prefill,
+# pack, decode, merge, ...) on the host and the launch rows they issue.
+if os.environ.get("CPATTN_NVTX") == "1":
+    import functools
+
+    def _ranged(fn):
+        @functools.wraps(fn)
+        def wrapper(*args, **kwargs):
+            torch.cuda.nvtx.range_push(fn.__name__)
+            try:
+                return fn(*args, **kwargs)
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return wrapper
+
+    for _n, _f in list(globals().items()):
+        if _n.startswith("cp_") and callable(_f):
+            globals()[_n] = _ranged(_f)
