@@ -293,7 +293,11 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
       off += rows;
     }
   }
-  for (int i = 0; i < P; ++i) tile_start[i + 1] = tile_start[i] + (pair[i].rows + TR - 1) / TR;
+  // The schedule walks the pairs request by request (shards 0..C-1 of
+  // request 0, then of request 1, ...), so that consecutive items of a worker
+  // share a request and the MLA kernels keep its query in shared memory.
+  auto walk = [&](int s) { return (s % C) * B + s / C; };  // walk position -> pair index
+  for (int i = 0; i < P; ++i) tile_start[i + 1] = tile_start[i] + (pair[walk(i)].rows + TR - 1) / TR;
   const long long NT = tile_start[P];
 
   // Balanced contiguous ranges of tiles per worker, cut at pair boundaries.
@@ -306,9 +310,9 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
       while (tile_start[p + 1] <= t) ++p;
       const long long pend = std::min(t1, tile_start[p + 1]);
       cp_work_desc wd;
-      wd.pair = p;
+      wd.pair = walk(p);
       wd.row_begin = (int)((t - tile_start[p]) * TR);
-      wd.row_end = (int)std::min<long long>(pair[p].rows, (pend - tile_start[p]) * TR);
+      wd.row_end = (int)std::min<long long>(pair[walk(p)].rows, (pend - tile_start[p]) * TR);
       wd.part = -1;
       per_worker[wkr].push_back(wd);
       t = pend;

@@ -378,16 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       bool ok = true;
-      int g = 0, nq = 0;  // tiles and non-empty items so far
+      int g = 0, nq = 0;  // tiles and query loads so far
+      int q_b = -1;       // request whose query the operand holds
       for (int wi = w0; wi < w1 && ok; ++wi) {
         const Item it = read_item(p, wi);
         if (it.ntiles == 0) continue;
-        // the item's query is in place (written after every earlier product completed)
-        if (!wait_all(smem_u32(&bar_q), nq & 1)) {
-          if (lane == 0) report_timeout(p.status, 2, &abort_flag);
-          break;
+        // a new request's query is in place (written after every earlier product completed)
+        if (it.b != q_b) {
+          if (!wait_all(smem_u32(&bar_q), nq & 1)) {
+            if (lane == 0) report_timeout(p.status, 2, &abort_flag);
+            break;
+          }
+          ++nq;
+          q_b = it.b;
         }
-        ++nq;
         int done = 0;  // chunk groups of QK^T(g) already issued
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
           for (; done < 5; ++done) {
@@ -448,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sPlo = smem + kPloOff;
     bool ok = true;
     int g = 0;
+    int q_b = -1, eq = 0;  // request whose query the operand holds, its scale exponent
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, wi);
       if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
@@ -457,52 +462,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // ---- [Q_hi | Q_lo] of request b: x = q 2^eq with max |x| in [128, 256).
       // Every product of the previous item has completed (its epilogue waited
-      // for the last P.V), so the operand can be overwritten.
-      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
-      constexpr int kPieces = kDqk / 8;  // 16-byte pieces per head
-      uint32_t qmax = 0;                 // largest |q| as bf16 magnitude bits
-      for (int i = tid; i < p.H * kPieces; i += kSoftmax) {
-        const uint4 v = __ldg(qsrc + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-      }
-      qmax = __reduce_max_sync(0xffffffffu, qmax);
-      if (lane == 0) sRed1[warp] = qmax;
-      named_bar_sync(1, kSoftmax);
-#pragma unroll
-      for (int w = 0; w < 8; ++w) qmax = max(qmax, sRed1[w]);
-      const int eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
-      const float qs = pow2i(eq);
-      for (int i = tid; i < kHeads * kPieces; i += kSoftmax) {
-        const int h = i / kPieces, d0 = (i % kPieces) * 8;
-        uint2 hw = make_uint2(0, 0), lw = make_uint2(0, 0);
-        if (h < p.H) {
+      // for the last P.V), so the operand can be overwritten; an item of the
+      // same request as the previous one keeps it.
+      const bool new_q = it.b != q_b;
+      if (new_q) {
+        q_b = it.b;
+        const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
+        constexpr int kPieces = kDqk / 8;  // 16-byte pieces per head
+        uint32_t qmax = 0;                 // largest |q| as bf16 magnitude bits
+        for (int i = tid; i < p.H * kPieces; i += kSoftmax) {
           const uint4 v = __ldg(qsrc + i);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t hs[4], ls[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
-                         hs[e], ls[e]);
-          hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
-          lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+          for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
         }
-        int oh, ol;
-        if (d0 < 4 * 128) {
-          const int base = (d0 >> 7) * kChunkBytes;
-          oh = base + sw128(h, d0 & 127);
-          ol = base + sw128(kHeads + h, d0 & 127);
-        } else {
-          oh = kRopeOff + sw64(h, d0 - 512);
-          ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+        qmax = __reduce_max_sync(0xffffffffu, qmax);
+        if (lane == 0) sRed1[warp] = qmax;
+        named_bar_sync(1, kSoftmax);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) qmax = max(qmax, sRed1[w]);
+        eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
+        const float qs = pow2i(eq);
+        for (int i = tid; i < kHeads * kPieces; i += kSoftmax) {
+          const int h = i / kPieces, d0 = (i % kPieces) * 8;
+          uint2 hw = make_uint2(0, 0), lw = make_uint2(0, 0);
+          if (h < p.H) {
+            const uint4 v = __ldg(qsrc + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t hs[4], ls[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
+                           hs[e], ls[e]);
+            hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
+            lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+          }
+          int oh, ol;
+          if (d0 < 4 * 128) {
+            const int base = (d0 >> 7) * kChunkBytes;
+            oh = base + sw128(h, d0 & 127);
+            ol = base + sw128(kHeads + h, d0 & 127);
+          } else {
+            oh = kRopeOff + sw64(h, d0 - 512);
+            ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+          }
+          *reinterpret_cast<uint2*>(sQ + oh) = hw;
+          *reinterpret_cast<uint2*>(sQ + ol) = lw;
         }
-        *reinterpret_cast<uint2*>(sQ + oh) = hw;
-        *reinterpret_cast<uint2*>(sQ + ol) = lw;
       }
       if (tid < kHeads) sM[tid] = 0.f;  // set from the item's first tile
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bar_q));
+      if (new_q) {
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bar_q));  // the issuer's first QK^T orders the reset too
+      } else {
+        named_bar_sync(1, kSoftmax);    // the reset before any reader
+      }
 
       const float* srow = p.sc.p[it.r] + it.row0;
       const float cq = p.scale_log2 * pow2i(-eq);

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // to wait for is that of the tile's index g over all items of this CTA.
   int g0 = 0;
   bool ok = true;
+  int q_b = -1;  // request whose query sQ holds
 
   for (int wi = w0; wi < w1 && ok; ++wi) {
     const cp_work_desc wd = work[wi];
@@ -178,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- the query of request b -> sQ (K-major, 128-byte swizzle); heads >= H are zero.
     // The previous item's MMAs have completed: its softmax waited for its last P.V.
-    for (int i = threadIdx.x; i < kHeads * (kDqk / 8); i += kThreads) {
+    // An item of the same request as the previous one keeps it.
+    for (int i = threadIdx.x; b != q_b && i < kHeads * (kDqk / 8); i += kThreads) {
       const int h = i / (kDqk / 8), piece = i % (kDqk / 8);
       const int c = piece >> 3, cc = piece & 7;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -186,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         v = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.H + h) * kDqk) + piece);
       *reinterpret_cast<uint4*>(sQ + c * kQChunkBytes + h * 128 + ((cc ^ (h & 7)) << 4)) = v;
     }
+    q_b = b;
     if (threadIdx.x < kHeads) sM[threadIdx.x] = 0.f;  // set from the first tile's maxima
     fence_proxy_async_smem();
     __syncthreads();
