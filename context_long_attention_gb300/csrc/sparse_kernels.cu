@@ -112,6 +112,7 @@ struct __align__(16) SelectSmem {
   uint32_t pick[4];
   int small_n;
   int warp_cnt[kWarps];
+  int seg_cnt[kWarps];
   uint64_t small[kSmallKeys];
 };
 
@@ -194,6 +195,145 @@ __device__ uint64_t kth_largest(int n, int k, Get get, Top top12, SelectSmem& sm
   }
 }
 
+// Sorts a[0, m) (m <= kSmallKeys) in decreasing order, padding to a power
+// of two with zeros (every key is > 0).
+__device__ void sort_desc_small(uint64_t* a, int m) {
+  int mp = 1;
+  while (mp < m) mp <<= 1;
+  for (int i = m + threadIdx.x; i < mp; i += blockDim.x) a[i] = 0;
+  __syncthreads();
+  for (int size = 2; size <= mp; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < mp; i += blockDim.x) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool down = (i & size) == 0;
+          const uint64_t x = a[i], y = a[j];
+          if ((x < y) == down) {
+            a[i] = y;
+            a[j] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+}
+
+// The want-th largest (1-based) of a[0, m), m <= blockDim: a bitonic sort
+// with one key per thread, through shuffles for strides below 32 and through
+// a (reused) for the larger ones, so that only those stages meet a barrier.
+__device__ uint64_t kth_of_small(uint64_t* a, int m, int want) {
+  const int t = threadIdx.x;
+  int mp = 32;
+  while (mp < m) mp <<= 1;
+  uint64_t v = t < m ? a[t] : 0ull;  // keys are > 0: the padding sorts last
+  __syncthreads();
+  for (int size = 2; size <= mp; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      uint64_t o;
+      if (stride >= 32) {
+        a[t] = v;
+        __syncthreads();
+        o = a[t ^ stride];
+        __syncthreads();
+      } else {
+        o = __shfl_xor_sync(kFull, v, stride);
+      }
+      const bool desc = (t & size) == 0, lower = (t & stride) == 0;
+      v = desc == lower ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  a[t] = v;
+  __syncthreads();
+  return a[want - 1];
+}
+
+// The staged path of a pair's local top-k: stages the scores with a
+// histogram of their top 12 bits, finds the bin holding rank k, collects that
+// bin (at most kSmallKeys keys) while counting, per warp segment, the keys
+// above it, sorts the bin for the k-th key, and writes the candidates in
+// token order: three passes over the scores.  Returns false (scores staged,
+// nothing written) when the bin is larger (many equal scores).
+template <typename Get, typename Top>
+__device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, Get get, Top top12,
+                                  uint64_t* out, SelectSmem& sm, const cp_pair_desc& pd,
+                                  int32_t* n_out) {
+  for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
+  __syncthreads();
+#pragma unroll 8
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const float f = __ldg(sc + i);
+    staged[i] = f;
+    atomicAdd(&sm.hist[ordered_bits(f) >> 20], 1u);
+  }
+  __syncthreads();
+  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
+  const uint32_t bin = sm.pick[0];
+  const int want = k - (int)sm.pick[1];
+  if ((int)sm.pick[2] > kSmallKeys) return false;
+  // warp w classifies keys [w seg, (w + 1) seg) in steps of 32
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (n + kWarps * 32 - 1) / (kWarps * 32) * 32;
+  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+  if (threadIdx.x == 0) sm.small_n = 0;
+  __syncthreads();
+  int above = 0;
+#pragma unroll 4
+  for (int b = s0; b < s1; b += 32) {
+    const int i = b + lane;
+    const uint32_t t = i < s1 ? top12(i) : 0u;
+    above += __popc(__ballot_sync(kFull, i < s1 && t > bin));
+    const bool in = i < s1 && t == bin;
+    const unsigned bal = __ballot_sync(kFull, in);
+    if (bal) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sm.small_n, __popc(bal));
+      base = __shfl_sync(kFull, base, 0);
+      if (in) sm.small[base + __popc(bal & ((1u << lane) - 1u))] = get(i);
+    }
+  }
+  if (lane == 0) sm.seg_cnt[warp] = above;
+  __syncthreads();
+  const int m = sm.small_n;
+  // the bin's keys that make it, counted into their warps' segments
+  uint64_t thresh;
+  if (m <= kThreads) {
+    const uint64_t mine = threadIdx.x < m ? sm.small[threadIdx.x] : 0ull;
+    thresh = kth_of_small(sm.small, m, want);
+    if (mine >= thresh && threadIdx.x < m)
+      atomicAdd(&sm.seg_cnt[((key_token(mine) - pd.tok0) / pd.tok_step) / seg], 1);
+  } else {
+    sort_desc_small(sm.small, m);
+    thresh = sm.small[want - 1];
+    for (int j = threadIdx.x; j < m; j += blockDim.x) {
+      const uint64_t key = sm.small[j];
+      if (key >= thresh) atomicAdd(&sm.seg_cnt[((key_token(key) - pd.tok0) / pd.tok_step) / seg], 1);
+    }
+  }
+  __syncthreads();
+  int at = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = sm.seg_cnt[w];
+    at += w < warp ? c : 0;
+    tot += c;
+  }
+  const uint32_t th_hi = (uint32_t)(thresh >> 32), th_lo = (uint32_t)thresh;
+#pragma unroll 4
+  for (int b = s0; b < s1; b += 32) {
+    const int i = b + lane;
+    bool keep = false;
+    if (i < s1) {
+      const uint32_t hi = ordered_bits(staged[i]);
+      keep = hi > th_hi || (hi == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
+    }
+    const unsigned bal = __ballot_sync(kFull, keep);
+    if (keep) out[at + __popc(bal & ((1u << lane) - 1u))] = get(i);
+    at += __popc(bal);
+  }
+  if (threadIdx.x == 0) *n_out = tot;
+  return true;
+}
+
 // Local top-k of every (shard, request) pair: candidate keys in token order.
 __global__ void __launch_bounds__(kThreads)
     topk_local_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
@@ -210,15 +350,12 @@ __global__ void __launch_bounds__(kThreads)
   // eight independent loads in flight per thread (the passes would otherwise
   // wait out an L2 round trip per element).
   float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem));
-  const bool st = n <= stage_cap;
-  if (st) {
-#pragma unroll 8
-    for (int i = threadIdx.x; i < n; i += blockDim.x) staged[i] = __ldg(sc + i);
-    __syncthreads();
-  }
+  const bool st = n <= stage_cap && n > k;  // staged by the fast path below
   auto score = [&](int i) { return st ? staged[i] : __ldg(sc + i); };
   auto get = [&](int i) { return token_key(score(i), pd.tok0 + i * pd.tok_step); };
   auto top12 = [&](int i) { return ordered_bits(score(i)) >> 20; };
+  uint64_t* out = cand_keys + (long long)pair * k;
+  if (st && n > k && local_topk_staged(n, k, sc, staged, get, top12, out, sm, pd, cand_n + pair)) return;
   const uint64_t thresh = n > k ? kth_largest(n, k, get, top12, sm) : 0ull;
   // the candidates in token order (the comparison split into two 32-bit halves)
   const uint32_t th_hi = (uint32_t)(thresh >> 32), th_lo = (uint32_t)thresh;
@@ -226,7 +363,6 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t hi = ordered_bits(score(i));
     return hi > th_hi || (hi == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
   };
-  uint64_t* out = cand_keys + (long long)pair * k;
   const int got = block_compact(n, keep, [&](int i, int j) { out[j] = get(i); }, sm.warp_cnt);
   if (threadIdx.x == 0) cand_n[pair] = got;
 }
