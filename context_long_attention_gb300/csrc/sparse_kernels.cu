@@ -399,17 +399,37 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + ids_bytes(kpow2));
   const bool st = N <= stage_cap;
   if (st) {
+    // stage the candidates with a histogram of their top 12 bits
+    for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
+    __syncthreads();
     for (int r = 0; r < C; ++r) {
       const uint64_t* src = cand_keys + (long long)(r * B + b) * k;
       const int n_r = start[r + 1] - start[r];
 #pragma unroll 8
-      for (int i = threadIdx.x; i < n_r; i += blockDim.x) staged[start[r] + i] = src[i];
+      for (int i = threadIdx.x; i < n_r; i += blockDim.x) {
+        const uint64_t key = src[i];
+        staged[start[r] + i] = key;
+        atomicAdd(&sm.hist[key >> 52], 1u);
+      }
     }
     __syncthreads();
   }
   auto get = [&](int i) { return st ? staged[i] : get_global(i); };
-  const uint64_t t = N > k ? kth_largest(N, k, get, [&](int i) { return (uint32_t)(get(i) >> 52); }, sm)
-                           : 0ull;
+  auto top12 = [&](int i) { return (uint32_t)(get(i) >> 52); };
+  uint64_t t = 0;
+  bool found = N <= k;  // then every candidate is selected (t = 0)
+  if (!found && st) {
+    // the bin of rank k, collected and sorted when it is small (else the general path)
+    pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
+    const uint32_t bin = sm.pick[0];
+    const int want = k - (int)sm.pick[1];
+    if ((int)sm.pick[2] <= kThreads) {
+      const int m = block_collect(N, [&](int i) { return top12(i) == bin; }, get, sm.small, &sm.small_n);
+      t = kth_of_small(sm.small, m, want);
+      found = true;
+    }
+  }
+  if (!found) t = kth_largest(N, k, get, top12, sm);
   for (int i = threadIdx.x; i < kpow2; i += blockDim.x) ids[i] = 0x7FFFFFFF;
   __syncthreads();
   const int got = block_compact(
