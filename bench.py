@@ -47,15 +47,15 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "44fff9fda4e68d8f406c141795af9500b6584e56", "bytes": 2.378338e9 + 0.275882e9},
+                "sha1": "44fff9fda4e68d8f406c141795af9500b6584e56", "bytes": 2.375181e9 + 0.276237e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "e2acaaa88f153538137e1944d7088eb4a7a5ab0c",
-                   "bytes_per_token": (0.630276e9 + 0.010276e9) / (8 * 131072)},
+                   "sha1": "4513d4372c0b3a837ddf6aca7ff7daa9852cc938",
+                   "bytes_per_token": (0.623363e9 + 0.010096e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "ee1837fb969a68e1033b7c4607e721cd91d58de2",
-                    "bytes_per_token": (1.209276e9 + 0.011507e9) / (8 * 131072)},
+                    "sha1": "b171657466e437a5d9757d567876a1272ea0019a",
+                    "bytes_per_token": (1.208762e9 + 0.011218e9) / (8 * 131072)},
 }
 
 
