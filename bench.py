@@ -86,6 +86,24 @@ WORKLOAD = ("zigzag prefill: 1 request, 32768 new tokens + 4096-token cached pre
             "D 128, bf16, CP=8 virtual shards; plus MLA decode: 64 x 131072 ctx, 64 heads, 576/512 "
             "FP8-E4M3 latent, DCP=8, LSE merge")
 
+PREFILL_WORKLOADS = {
+    "zigzag": "zigzag prefill: 1 request, 32768 new tokens + 4096-token cached prefix, GQA 32q/8kv, "
+              "D 128, bf16, CP=8 virtual shards",
+    "interleave": "interleave prefill: 16 ragged requests (bimodal log-uniform lengths, 2^20 tokens "
+                  "in all), GQA 64q/8kv, D 128, bf16, CP=8 virtual shards",
+}
+DECODE_WORKLOADS = {
+    "uniform": "MLA decode: 64 x 131072 ctx, 64 heads, 576/512 latent, DCP=8, LSE merge",
+    "mixed": "MLA decode: 128 requests, bimodal log-uniform ctx 1k..1M (2.4e7 tokens), 64 heads, "
+             "576/512 latent, DCP=8, LSE merge",
+}
+
+
+def workload_name(args):
+    if args.prefill_workload == "zigzag" and args.decode_workload == "uniform":
+        return WORKLOAD
+    return PREFILL_WORKLOADS[args.prefill_workload] + "; plus " + DECODE_WORKLOADS[args.decode_workload]
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -328,26 +346,38 @@ def run_ours(args, world, rank, local):
     do_pre = args.only in ("all", "prefill")
     do_dec = args.only in ("all", "decode")
 
-    # ---- prefill inputs (zigzag)
-    z = W.WORKLOADS["zigzag"]
-    nl, pl, C, Hq, Hkv, D = z["new_len"], z["prefix_len"], z["C"], z["Hq"], z["Hkv"], z["D"]
+    # ---- prefill inputs (zigzag: one long request; interleave: the ragged batch)
+    zz = args.prefill_workload == "zigzag"
+    z = W.WORKLOADS[args.prefill_workload]
+    if zz:
+        nl, pl, strategy = z["new_len"], z["prefix_len"], cp.CP_ZIGZAG
+    else:
+        nl = W.interleave_lengths()
+        pl, strategy = [0] * len(nl), cp.CP_INTERLEAVE
+    C, Hq, Hkv, D = z["C"], z["Hq"], z["Hkv"], z["D"]
     scale = 1.0 / math.sqrt(D)
     p_flops, _ = prefill_flops(nl, pl, Hq, D)
     if do_pre:
-        q, k, v = W.prefill_inputs(nl, pl, Hq, Hkv, D, "bf16", seed=W.SEEDS["zigzag"] + rank,
+        q, k, v = W.prefill_inputs(nl, pl, Hq, Hkv, D, "bf16", seed=W.SEEDS[args.prefill_workload] + rank,
                                    device=dev)
         o = torch.empty_like(q)
         lse = torch.empty((q.shape[0], Hq), dtype=torch.float32, device=dev)
 
     # ---- decode inputs (MLA, FP8 cache, packed into token shards once)
-    m = W.WORKLOADS["mla"]
-    ctx = [m["ctx"]] * (args.decode_batch or m["B"])
+    uniform = args.decode_workload == "uniform"
+    m = W.WORKLOADS["mla" if uniform else "mla_mixed"]
+    if uniform:
+        ctx = [m["ctx"]] * (args.decode_batch or m["B"])
+    else:
+        ctx = W.mixed_context_lengths()
+        ctx = ctx[:args.decode_batch] if args.decode_batch else ctx
     fp8 = args.decode_kv == "fp8"
     d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
     dscale = 1.0 / math.sqrt(m["Dqk"])
     n_dec_kernels = 0
     if do_dec:
-        data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla"] + rank, device=dev,
+        data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla" if uniform else "mla_mixed"] + rank,
+                                   device=dev,
                                    bf16=not fp8, fp8=fp8)
         layout = cp.CP_DCP_CONTIGUOUS if args.decode_layout == "contiguous" else cp.CP_DCP_ROUND_ROBIN
         s_q = args.decode_rows
@@ -394,7 +424,7 @@ def run_ours(args, world, rank, local):
         e0, e1, e2, e3, e4 = rec
         e0.record(stream)
         if do_pre:
-            plan = cp.cp_shard_plan(cp.CP_ZIGZAG, C, nl, pl, device=dev)
+            plan = cp.cp_shard_plan(strategy, C, nl, pl, device=dev)
         e1.record(stream)
         if do_pre:
             cp.cp_prefill_attn(plan, q, k, v, scale, out=o, lse=lse)
@@ -448,7 +478,7 @@ def run_ours(args, world, rank, local):
     # copies run on two copy streams, double-buffered, so step i + 1's inputs
     # upload and step i - 1's outputs download while step i computes.
     e2e = None
-    if do_pre:
+    if do_pre and zz:
         qh = q.cpu().pin_memory()
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
@@ -521,7 +551,7 @@ def run_ours(args, world, rank, local):
         pre_avg = statistics.mean(pre_ms)
         achieved = p_flops / (pre_avg / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": profiled_traffic("prefill"),
+                "frac": achieved / peak, "traffic": profiled_traffic("prefill") if zz else None,
                 "peak_kind": peak_kind + " burst",
                 "kernel": "prefill_tc_kernel<128>"}
     if do_dec:
@@ -538,7 +568,7 @@ def run_ours(args, world, rank, local):
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
                             "frac": dec_ach / hbm,
                             "traffic": (None if args.decode_paged or args.decode_rows > 1
-                                        or args.decode_layout != "round_robin" else
+                                        or args.decode_layout != "round_robin" or not uniform else
                                         profiled_traffic("decode_" + args.decode_kv, sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
@@ -561,11 +591,12 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": WORKLOAD,
+            "workload": workload_name(args),
             "timed": args.only,
             "prefill_flops_per_step": p_flops,
             "decode_bytes_per_step": d_bytes,
-            "l2": "inputs larger than L2 (K/V 151 MB, Q 268 MB, FP8 cache 4.9 GB); no flush",
+            "l2": ("inputs larger than L2 (K/V 151 MB, Q 268 MB, FP8 cache 4.9 GB); no flush"
+                   if zz and uniform else "inputs larger than L2; no flush"),
             "parallelism": "virtual CP=8 on each GPU; replicas across GPUs",
         },
         "decode": dec,
@@ -601,6 +632,11 @@ def main():
                     help="query rows per request (MTP); the 64 heads split into S_Q rows of 64/S_Q")
     ap.add_argument("--sparse-k", type=int, default=0, metavar="K",
                     help="also time sparse decode over the exact sharded top-K of per-token scores")
+    ap.add_argument("--prefill-workload", choices=list(PREFILL_WORKLOADS), default="zigzag",
+                    help="zigzag: one 32k request after a 4k prefix (the default line); interleave: "
+                         "16 ragged requests, 2^20 tokens (about 1.3 s per step)")
+    ap.add_argument("--decode-workload", choices=list(DECODE_WORKLOADS), default="uniform",
+                    help="uniform: 64 x 131072 (the default line); mixed: 128 requests, 1k..1M")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()

@@ -300,11 +300,33 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
   for (int i = 0; i < P; ++i) tile_start[i + 1] = tile_start[i] + (pair[walk(i)].rows + TR - 1) / TR;
   const long long NT = tile_start[P];
 
-  // Balanced contiguous ranges of tiles per worker, cut at pair boundaries.
+  // Worker ranges balance a cost: every tile, plus kDecodeItemCost tiles for
+  // each nonempty pair (a work item's fixed work: its query, the first tile's
+  // fill, the epilogue and the partial's write), so that many short pairs do
+  // not pile up on one worker.  A cut that falls in a pair's fixed cost moves
+  // to the pair's start; one inside its tiles splits the pair there.
+  std::vector<long long> cost_start(P + 1, 0);
+  for (int i = 0; i < P; ++i) {
+    const long long nt = tile_start[i + 1] - tile_start[i];
+    cost_start[i + 1] = cost_start[i] + (nt > 0 ? kDecodeItemCost + nt : 0);
+  }
+  const long long total_cost = cost_start[P];
+  std::vector<long long> cut(G + 1, NT);  // worker w: tiles [cut[w], cut[w + 1])
+  {
+    int i = 0;
+    for (int wkr = 0; wkr < G; ++wkr) {
+      const long long x = total_cost * wkr / G;
+      while (i < P && cost_start[i + 1] <= x) ++i;
+      if (i == P) break;
+      cut[wkr] = tile_start[i] + std::max(0LL, x - cost_start[i] - kDecodeItemCost);
+    }
+  }
+
+  // Contiguous tile ranges per worker, cut at pair boundaries into items.
   std::vector<std::vector<cp_work_desc>> per_worker(G);
   int p = 0;
   for (int wkr = 0; wkr < G; ++wkr) {
-    const long long t0 = NT * wkr / G, t1 = NT * (wkr + 1) / G;
+    const long long t0 = cut[wkr], t1 = cut[wkr + 1];
     long long t = t0;
     while (t < t1) {
       while (tile_start[p + 1] <= t) ++p;

@@ -468,13 +468,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (new_q) {
         q_b = it.b;
         const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
-        constexpr int kPieces = kDqk / 8;  // 16-byte pieces per head
-        uint32_t qmax = 0;                 // largest |q| as bf16 magnitude bits
-        for (int i = tid; i < p.H * kPieces; i += kSoftmax) {
-          const uint4 v = __ldg(qsrc + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        constexpr int kPieces = kDqk / 8;                   // 16-byte pieces per head
+        constexpr int kPer = kHeads * kPieces / kSoftmax;   // pieces per thread
+        static_assert(kHeads * kPieces % kSoftmax == 0, "query pieces split evenly");
+        constexpr int kBatch = 6;  // pieces in flight at once per thread
+        static_assert(kPer % kBatch == 0, "whole batches of pieces");
+        // a batch of this thread's pieces (heads past H are zero)
+        auto load_batch = [&](int k0, uint4* qv) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+          for (int k = 0; k < kBatch; ++k) {
+            const int i = tid + (k0 + k) * kSoftmax;
+            qv[k] = i < p.H * kPieces ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
+          }
+        };
+        uint32_t qmax = 0;  // largest |q| as bf16 magnitude bits
+#pragma unroll 1
+        for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+          uint4 qv[kBatch];
+          load_batch(k0, qv);
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
+          }
         }
         qmax = __reduce_max_sync(0xffffffffu, qmax);
         if (lane == 0) sRed1[warp] = qmax;
@@ -483,31 +500,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < 8; ++w) qmax = max(qmax, sRed1[w]);
         eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
         const float qs = pow2i(eq);
-        for (int i = tid; i < kHeads * kPieces; i += kSoftmax) {
-          const int h = i / kPieces, d0 = (i % kPieces) * 8;
-          uint2 hw = make_uint2(0, 0), lw = make_uint2(0, 0);
-          if (h < p.H) {
-            const uint4 v = __ldg(qsrc + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll 1
+        for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+          uint4 qv[kBatch];
+          load_batch(k0, qv);
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            const int i = tid + (k0 + k) * kSoftmax;
+            const int h = i / kPieces, d0 = (i % kPieces) * 8;
+            const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
             uint32_t hs[4], ls[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
                            hs[e], ls[e]);
-            hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
-            lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+            const uint2 hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
+            const uint2 lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+            int oh, ol;
+            if (d0 < 4 * 128) {
+              const int base = (d0 >> 7) * kChunkBytes;
+              oh = base + sw128(h, d0 & 127);
+              ol = base + sw128(kHeads + h, d0 & 127);
+            } else {
+              oh = kRopeOff + sw64(h, d0 - 512);
+              ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+            }
+            *reinterpret_cast<uint2*>(sQ + oh) = hw;
+            *reinterpret_cast<uint2*>(sQ + ol) = lw;
           }
-          int oh, ol;
-          if (d0 < 4 * 128) {
-            const int base = (d0 >> 7) * kChunkBytes;
-            oh = base + sw128(h, d0 & 127);
-            ol = base + sw128(kHeads + h, d0 & 127);
-          } else {
-            oh = kRopeOff + sw64(h, d0 - 512);
-            ol = kRopeOff + sw64(kHeads + h, d0 - 512);
-          }
-          *reinterpret_cast<uint2*>(sQ + oh) = hw;
-          *reinterpret_cast<uint2*>(sQ + ol) = lw;
         }
       }
       if (tid < kHeads) sM[tid] = 0.f;  // set from the item's first tile

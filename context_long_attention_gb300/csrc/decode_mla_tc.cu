@@ -111,8 +111,50 @@ __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, 
 // overwritten by P^T once S^T is computed.
 __device__ __forceinline__ int group_chunks(int q) { return q < 4 ? 2 : 1; }
 
+// The fields of one work item that every role reads.
+struct Item {
+  int pair, r, b, part, row_begin, nrows, ntiles;
+  long long row0;  // first shard row
+  cp_pair_desc pd;
+};
+
+__device__ __forceinline__ Item read_item(const Params& p, const cp_pair_desc* pairs,
+                                          const cp_work_desc* work, int wi) {
+  const cp_work_desc wd = work[wi];
+  Item it;
+  it.pair = wd.pair;
+  it.r = wd.pair / p.B;
+  it.b = wd.pair % p.B;
+  it.part = wd.part;
+  it.pd = pairs[wd.pair];
+  const int row_end = p.pair_count ? min(wd.row_end, max(wd.row_begin, __ldg(p.pair_count + wd.pair)))
+                                   : wd.row_end;
+  it.row_begin = wd.row_begin;
+  it.nrows = row_end - wd.row_begin;
+  it.ntiles = (it.nrows + kRows - 1) / kRows;
+  it.row0 = (long long)it.pd.row_off + wd.row_begin;
+  return it;
+}
+
+// Where an item's partial goes: its pair's row of the partials, or, for one
+// part of a pair split between CTAs, a workspace row merged afterwards.
+__device__ __forceinline__ float* out_rows(const Params& p, const Item& it) {
+  return it.part < 0 ? p.o_part + (long long)it.pair * p.H * kDv : p.ws_o + (long long)it.part * p.H * kDv;
+}
+__device__ __forceinline__ float* out_lse(const Params& p, const Item& it) {
+  return it.part < 0 ? p.lse_part + (long long)it.pair * p.H : p.ws_lse + (long long)it.part * p.H;
+}
+
+// Warp roles run their loops over all work items of the CTA without meeting
+// at item boundaries: the TMA warp fills the next item's first tile as soon
+// as the previous tile's P.V releases the buffer, and loads a new request's
+// query (one TMA box per 64-dim chunk; heads past H read as zeros) once the
+// previous QK^T has completed.  Every barrier completes once per tile (bar_q
+// once per query load), so the parity to wait for is that of the tile's index
+// g over all items of this CTA.
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_mla_tc_kernel(const __grid_constant__ ShardMaps maps, const Params p) {
+    decode_mla_tc_kernel(const __grid_constant__ ShardMaps maps, const __grid_constant__ CUtensorMap qmap,
+                         const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -122,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // fill[q]: chunk group q of the tile holds the current tile.
   // mb[q]: the P.V product of M-block q (dims of group q) has completed; mb[3]
   //        also means the whole P.V (and every read of P^T) has completed.
-  __shared__ __align__(8) uint64_t bar_fill[5], bar_mb[4], bar_s, bar_drain;
+  // q: sQ holds the query of the item's request.
+  __shared__ __align__(8) uint64_t bar_fill[5], bar_mb[4], bar_s, bar_q, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;
@@ -137,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_fill[q]), 1);
     for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bar_mb[q]), 1);
     mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_q), 1);
     mbar_init(smem_u32(&bar_drain), 1);
     abort_flag = 0;
     zero_flag = 0;
@@ -152,118 +196,125 @@ __global__ void __launch_bounds__(kThreads, 1)
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work);
   const int w0 = p.plan[p.off_worker + blockIdx.x], w1 = p.plan[p.off_worker + blockIdx.x + 1];
-  // Every barrier completes exactly once per tile, so the parity of the phase
-  // to wait for is that of the tile's index g over all items of this CTA.
-  int g0 = 0;
   bool ok = true;
-  int q_b = -1;  // request whose query sQ holds
 
-  for (int wi = w0; wi < w1 && ok; ++wi) {
-    const cp_work_desc wd = work[wi];
-    const int r = wd.pair / p.B, b = wd.pair % p.B;
-    const cp_pair_desc pd = pairs[wd.pair];
-    const int row_end = p.pair_count ? min(wd.row_end, max(wd.row_begin, __ldg(p.pair_count + wd.pair)))
-                                      : wd.row_end;
-    const int nrows = row_end - wd.row_begin;
-    const int ntiles = (nrows + kRows - 1) / kRows;
-    const long long row0 = (long long)pd.row_off + wd.row_begin;  // first shard row
-    float* out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
-                               : p.ws_o + (long long)wd.part * p.H * kDv;
-    float* out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
-                               : p.ws_lse + (long long)wd.part * p.H;
-    if (ntiles == 0) {  // empty shard: O = 0, LSE = -inf
-      for (int i = threadIdx.x; i < p.H * kDv; i += kThreads) out_o[i] = 0.f;
-      for (int i = threadIdx.x; i < p.H; i += kThreads) out_l[i] = -INFINITY;
-      continue;
-    }
-
-    // ---- the query of request b -> sQ (K-major, 128-byte swizzle); heads >= H are zero.
-    // The previous item's MMAs have completed: its softmax waited for its last P.V.
-    // An item of the same request as the previous one keeps it.
-    for (int i = threadIdx.x; b != q_b && i < kHeads * (kDqk / 8); i += kThreads) {
-      const int h = i / (kDqk / 8), piece = i % (kDqk / 8);
-      const int c = piece >> 3, cc = piece & 7;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (h < p.H)
-        v = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.H + h) * kDqk) + piece);
-      *reinterpret_cast<uint4*>(sQ + c * kQChunkBytes + h * 128 + ((cc ^ (h & 7)) << 4)) = v;
-    }
-    q_b = b;
-    if (threadIdx.x < kHeads) sM[threadIdx.x] = 0.f;  // set from the first tile's maxima
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    if (warp >= 4) {
-      // ------------------------------------------------------------ tile fill (TMA, warp 4;
-      // the warp runs the loop, one elected lane issues the copies)
-      if (warp == 4) {
-        int issued_tiles = 0;  // tiles whose copies were issued (for the drain)
-        for (int j = 0; j < ntiles && ok; ++j) {
-          const int g = g0 + j;
-          // paged: the pool rows of the tile's two 64-row halves (each inside one page);
-          // past the pair's rows the coordinate is past the pool and the copy reads zeros
-          long long yh[2] = {0, 0};
-          if (p.rm.table) {
-            for (int hh = 0; hh < 2; ++hh) {
-              const int i0 = wd.row_begin + j * kRows + 64 * hh;
-              yh[hh] = i0 < pd.rows ? map_row(p.rm, wd.pair, 0, i0) : p.rm.pool_rows;
-            }
+  if (warp == 4) {
+    // ------------------------------------------------------------ tile fill (TMA; the
+    // warp runs the loop, one elected lane issues the copies)
+    int g = 0;             // tiles of this CTA so far
+    int q_b = -1, nq = 0;  // request whose query was loaded last, query loads issued
+    int last_fill[5] = {-1, -1, -1, -1, -1};  // tile of each group's last issued fill
+    for (int wi = w0; wi < w1 && ok; ++wi) {
+      const Item it = read_item(p, pairs, work, wi);
+      if (it.ntiles == 0) continue;
+      const bool new_q = it.b != q_b;
+      q_b = it.b;
+      for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
+        // paged: the pool rows of the tile's two 64-row halves (each inside one page);
+        // past the pair's rows the coordinate is past the pool and the copy reads zeros
+        long long yh[2] = {0, 0};
+        if (p.rm.table) {
+          for (int hh = 0; hh < 2; ++hh) {
+            const int i0 = it.row_begin + j * kRows + 64 * hh;
+            yh[hh] = i0 < it.pd.rows ? map_row(p.rm, it.pair, 0, i0) : p.rm.pool_rows;
           }
+        }
 #pragma unroll
-          for (int q = 0; q < 5; ++q) {
-            // group q is free once the previous tile's P.V M-block q (or, for the
-            // rope group that holds P^T, the whole P.V) has read it
-            if (ok && j > 0 &&
-                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]), (g - 1) & 1,
-                                                   p.wait_ns, &abort_flag))) {
-              if (lane == 0) report_timeout(p.status, 1, &abort_flag);
-              ok = false;
-            }
-            if (!ok) continue;
-            const uint32_t full = smem_u32(&bar_fill[q]);
+        for (int q = 0; q < 5; ++q) {
+          // group q is free once the previous tile's P.V M-block q (or, for the
+          // rope group that holds P^T, the whole P.V) has read it
+          if (g > 0 &&
+              !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[q < 4 ? q : 3]), (g - 1) & 1,
+                                                 p.wait_ns, &abort_flag))) {
+            if (lane == 0) report_timeout(p.status, 1, &abort_flag);
+            ok = false;
+            break;
+          }
+          if (j == 0 && q == 0 && new_q) {
+            // P.V block 0 of the previous tile follows its QK^T, the last read of sQ
             if (elect_one()) {
-              mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
-              for (int cc = 0; cc < group_chunks(q); ++cc) {
-                const int c = 2 * q + cc;
-                if (!p.rm.table) {
-                  tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[r], c * 64,
-                              (int)(row0 + (long long)j * kRows), full);
-                } else {
-                  for (int hh = 0; hh < 2; ++hh)
-                    tma_load_2d(smem_u32(sTile + c * kChunkBytes + hh * 64 * 128), &maps.m[0],
-                                c * 64, (int)yh[hh], full);
-                }
-              }
+              mbar_expect_tx(smem_u32(&bar_q), kQBytes);
+              for (int c = 0; c < kChunks; ++c)
+                tma_load_3d(smem_u32(sQ + c * kQChunkBytes), &qmap, c * 64, 0, it.b, smem_u32(&bar_q));
             }
             __syncwarp();
+            ++nq;
           }
-          if (!ok) break;
-          issued_tiles = j + 1;
-        }
-        if (!ok && issued_tiles > 0) {
-          // never leave with a copy in flight: the last issued tile's groups
-          for (int q = 0; q < 5; ++q)
-            mbar_wait(smem_u32(&bar_fill[q]), (g0 + issued_tiles - 1) & 1, 1000000000ull, &zero_flag);
+          const uint32_t full = smem_u32(&bar_fill[q]);
+          if (elect_one()) {
+            mbar_expect_tx(full, group_chunks(q) * kChunkBytes);
+            for (int cc = 0; cc < group_chunks(q); ++cc) {
+              const int c = 2 * q + cc;
+              if (!p.rm.table) {
+                tma_load_2d(smem_u32(sTile + c * kChunkBytes), &maps.m[it.r], c * 64,
+                            (int)(it.row0 + (long long)j * kRows), full);
+              } else {
+                for (int hh = 0; hh < 2; ++hh)
+                  tma_load_2d(smem_u32(sTile + c * kChunkBytes + hh * 64 * 128), &maps.m[0],
+                              c * 64, (int)yh[hh], full);
+              }
+            }
+          }
           __syncwarp();
+          last_fill[q] = g;
         }
       }
-    } else {
-      // ------------------------------------------------------------ softmax (warps 0-3)
-      const int t = threadIdx.x;  // tile row = TMEM lane
-      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
-      const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
-      const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
-      // Warp 0 issues the products warp-wide (one elected lane); descriptors are
-      // built once and an MMA adds its byte offset / 16 to the address field.
-      const uint64_t dK = smem_desc(tile, 16, 1024), dQ = smem_desc(qb, 16, 1024);
-      const uint64_t dV = smem_desc(tile, kChunkBytes, 1024), dP = smem_desc(pb, 16, 1024);
+    }
+    if (!ok) {
+      // never leave with a copy in flight: each group's last fill and the last query load
+      for (int q = 0; q < 5; ++q)
+        if (last_fill[q] >= 0)
+          mbar_wait(smem_u32(&bar_fill[q]), last_fill[q] & 1, 1000000000ull, &zero_flag);
+      if (nq > 0) mbar_wait(smem_u32(&bar_q), (nq - 1) & 1, 1000000000ull, &zero_flag);
+      __syncwarp();
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax (warps 0-3)
+    const int t = threadIdx.x;  // tile row = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t idS = idesc_bf16_f32(kRows, kHeads, 0, 0);
+    const uint32_t idPV = idesc_bf16_f32(kRows, kHeads, 1, 1);
+    const uint32_t tile = smem_u32(sTile), qb = smem_u32(sQ), pb = smem_u32(sP);
+    // Warp 0 issues the products warp-wide (one elected lane); descriptors are
+    // built once and an MMA adds its byte offset / 16 to the address field.
+    const uint64_t dK = smem_desc(tile, 16, 1024), dQ = smem_desc(qb, 16, 1024);
+    const uint64_t dV = smem_desc(tile, kChunkBytes, 1024), dP = smem_desc(pb, 16, 1024);
+    int g0 = 0;
+    int q_b = -1, nq = 0;  // request whose query sQ holds, query loads so far
+    for (int wi = w0; wi < w1 && ok; ++wi) {
+      const Item it = read_item(p, pairs, work, wi);
+      if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
+        float* out_o = out_rows(p, it);
+        float* out_l = out_lse(p, it);
+        for (int i = t; i < p.H * kDv; i += 128) out_o[i] = 0.f;
+        for (int i = t; i < p.H; i += 128) out_l[i] = -INFINITY;
+        continue;
+      }
+      // a new request: warp 0 waits for its query before the first QK^T
+      bool q_ok = true;
+      if (it.b != q_b) {
+        if (warp == 0)
+          q_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag));
+        ++nq;
+      }
+      q_b = it.b;
+      // the running max restarts from the first tile's maxima; every read of
+      // the previous item's maxima came before its epilogue's barrier
+      if (t < kHeads) sM[t] = 0.f;
+      named_bar_sync(1, 128);
+      // token of tile row t of tile j: tok_t + j * tok_j; a cache row is masked
+      // for the columns of query rows below tok - lim
+      const int tok_j = kRows * it.pd.tok_step;
+      const int tok_t = it.pd.tok0 + (it.row_begin + t) * it.pd.tok_step;
+      const int lim = it.pd.ctx_len - p.s_q;
+      const int nrows = it.nrows, ntiles = it.ntiles;
       float l[kHeads];
 #pragma unroll
       for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
       for (int j = 0; j < ntiles; ++j) {
         const int g = g0 + j;
-        bool issued = true;
+        bool issued = q_ok;
+        q_ok = true;
         if (warp == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
           for (int q = 0; q < 5 && issued; ++q) {
             issued = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns,
@@ -287,8 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Several query rows (s_q > 1): row qi of the request reads tokens up
         // to L - s_q + qi, so this cache row is masked for the columns of the
         // query rows qi < tok - (L - s_q), columns [0, mcols).
-        const int tok = pd.tok0 + (wd.row_begin + j * kRows + t) * pd.tok_step;
-        const int mcols = min(kHeads, max(0, tok - (pd.ctx_len - p.s_q)) * p.Hrow);
+        const int tok = tok_t + j * tok_j;
+        const int mcols = min(kHeads, max(0, tok - lim) * p.Hrow);
         const float cj = p.scale_log2;  // scores in log2 units
         // The four softmax warps leave together: a warp that gave up still
         // meets the others at the named barrier of this vote.
@@ -401,12 +452,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
+        const cp_work_desc wd = work[wi];
+        float* out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
+                                   : p.ws_o + (long long)wd.part * p.H * kDv;
+        float* out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
+                                   : p.ws_lse + (long long)wd.part * p.H;
 #pragma unroll
         for (int h = 0; h < kHeads; ++h) {
           float v = l[h];
 #pragma unroll
           for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
           if (lane == 0) sL[warp][h] = v;
+        }
+        named_bar_sync(1, 128);
+        // one reciprocal per head (sAlpha is free until the next item's first
+        // tile): a division per element made the epilogue cost more than a tile
+        if (t < kHeads) {
+          const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
+          sAlpha[t] = tot > 0.f ? 1.f / tot : 0.f;
+          if (t < p.H) out_l[t] = tot > 0.f ? (sM[t] + lg2(tot)) * kLn2 : -INFINITY;
         }
         named_bar_sync(1, 128);
 #pragma unroll 1
@@ -419,25 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
               const int hh = 32 * half + h;
-              if (hh < p.H) {
-                const float tot = sL[0][hh] + sL[1][hh] + sL[2][hh] + sL[3][hh];
-                out_o[(long long)hh * kDv + 128 * mb + t] = tot > 0.f ? __uint_as_float(a[h]) / tot : 0.f;
-              }
+              if (hh < p.H) out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * sAlpha[hh];
             }
           }
         }
-        if (t < p.H) {
-          const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
-          out_l[t] = tot > 0.f ? (sM[t] + lg2(tot)) * kLn2 : -INFINITY;
-        }
       }
+
+      g0 += ntiles;
+      // the four softmax warps decide together whether to go on
+      if (bar_red_or(1, 128, !ok || abort_flag != 0)) ok = false;
     }
-    g0 += ntiles;
-    // every role learns whether one gave up; shared state is free for the next item
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    ok = ok && !abort_flag;
   }
   // Never free TMEM under a running MMA.
   if (warp == 0) {
@@ -498,10 +553,19 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
         return cudaErrorInvalidValue;
     }
   }
+  // the queries [B][H][576]: one box per 64-dim chunk of a request's 64 columns
+  // (columns past H fall outside the map and read as zeros)
+  CUtensorMap qmap;
+  {
+    const uint64_t dims[3] = {(uint64_t)kDqk, (uint64_t)p.H, (uint64_t)h.R};
+    const uint64_t strides[2] = {(uint64_t)kDqk * 2, (uint64_t)p.H * kDqk * 2};
+    const uint32_t box[3] = {64, (uint32_t)kHeads, 1};
+    if (!encode_tensor_map_bf16(&qmap, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   auto kern = decode_mla_tc_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<h.n_tiles, kThreads, kSmem, s>>>(local, p);
+  kern<<<h.n_tiles, kThreads, kSmem, s>>>(local, qmap, p);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ constexpr int kPairWords = (int)(sizeof(cp_pair_desc) / 4);
 constexpr int kWorkWords = (int)(sizeof(cp_work_desc) / 4);
 constexpr int kPrefillTileRows = 256;  // queries per prefill tile (two 128-row MMA tiles)
 constexpr int kDecodeTileRows = 128;   // KV rows per decode scheduling tile (MMA M)
+constexpr long long kDecodeItemCost = 2;  // a work item's fixed work, in tiles, for the schedule
 
 // Query rows per request of a decode plan (plans without the field have one).
 inline int plan_s_q(const cp_plan_header& h) { return h.s_q > 0 ? h.s_q : 1; }

@@ -239,10 +239,11 @@ cp_status cp_prefill_attn(const void* host_plan, const void* dev_plan, int rank,
  * Token p of request b lives on shard p mod C at row p / C ([CTX] §3.1
  * "Storing each token once": gpu = slot % C, row = slot // C; [V4] §5
  * owner(j) = j mod P).  Shard r holds rows_{r,b} = ceil((L_b - r)/C) rows of
- * request b, requests back to back (row_off).  The work of all (r, b) pairs
- * is cut into contiguous row ranges balanced over `n_workers` CTAs
- * (0 = twice the SM count of the current device); a pair split over several
- * workers gets workspace slots that cp_decode_attn merges exactly.
+ * request b, requests back to back (row_off).  The work of all (r, b) pairs,
+ * walked request by request, is cut into contiguous row ranges over
+ * `n_workers` CTAs (0 = the SM count of the current device), balanced in
+ * 128-row tiles plus a fixed two-tile cost per work item; a pair split over
+ * several workers gets workspace slots that cp_decode_attn merges exactly.
  *
  * Arguments: C in [1, CP_MAX_SHARDS]; B >= 1; ctx_len[B] >= 0 host array.
  * ------------------------------------------------------------------------- */

@@ -165,14 +165,20 @@ def test_decode_plan_matches_shard_map_and_covers_rows(cp, ctx, C, G):
         else:
             first = int(pairs[i][4])
             assert sorted(ps) == list(range(first, first + len(ps)))
-    # balance: each worker holds floor or ceil of NT/G tiles
-    tiles = [0] * G
+    # balance: a worker's cost (its tiles plus ITEM_COST per nonempty item) is
+    # within ITEM_COST + 1 of an even share of the total
+    ITEM_COST = 2
+    tiles, cost = [0] * G, [0] * G
     wo = plan.worker_off
     for w in range(G):
         for pair, rb, re_, part in plan.work[wo[w]:wo[w + 1]]:
-            tiles[w] += (re_ - rb + 127) // 128
+            nt = (re_ - rb + 127) // 128
+            tiles[w] += nt
+            cost[w] += nt + (ITEM_COST if nt else 0)
     NT = sum((int(p[0]) + 127) // 128 for p in pairs)
-    assert sum(tiles) == NT and max(tiles) - min(tiles) <= 1
+    total = NT + ITEM_COST * sum(1 for p in pairs if p[0] > 0)
+    assert sum(tiles) == NT
+    assert max(abs(c - total / G) for c in cost) <= ITEM_COST + 1
 
 
 def test_argument_validation(cp):
