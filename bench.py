@@ -544,7 +544,11 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # the tensor peak: the burst figure, or the sustained one (under the power
+    # cap) when the timed prefill work lasts more than a second
+    sustained = do_pre and sum(pre_ms) > 1000.0
+    peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = float(peaks.get(peak_key, FALLBACK_PEAKS[peak_key]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     roof = dec = None
     if do_pre:
@@ -552,7 +556,7 @@ def run_ours(args, world, rank, local):
         achieved = p_flops / (pre_avg / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": profiled_traffic("prefill") if zz else None,
-                "peak_kind": peak_kind + " burst",
+                "peak_kind": peak_kind + (" sustained" if sustained else " burst"),
                 "kernel": "prefill_tc_kernel<128>"}
     if do_dec:
         dec_avg = statistics.mean(dec_ms)

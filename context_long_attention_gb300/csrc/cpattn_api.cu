@@ -542,14 +542,20 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   float* ws_lse = ws_o ? ws_o + (size_t)h.n_parts * Hc * Dv : nullptr;
   cudaStream_t s = (cudaStream_t)stream;
   const bool mla = mode == CP_DECODE_MLA;
-  cudaError_t e =
-      mla && kv_dtype == CP_FP8_E4M3
-          ? launch_decode_mla_fp8((const int32_t*)dev_plan, h, q, K, S, shard_rows, rm, Hq, sm_scale,
-                                  o_part, lse_part, ws_o, ws_lse, pair_count, wait_limit_ns(), s)
-      : mla ? launch_decode_mla_tc((const int32_t*)dev_plan, h, q, K, shard_rows, rm, Hq, sm_scale,
-                                   o_part, lse_part, ws_o, ws_lse, pair_count, wait_limit_ns(), s)
-            : launch_decode_simt((const int32_t*)dev_plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk,
-                                 Dv, sm_scale, o_part, lse_part, ws_o, ws_lse, pair_count, s);
+  const int32_t* plan = (const int32_t*)dev_plan;
+  cudaError_t e;
+  if (mla && kv_dtype == CP_FP8_E4M3)
+    e = launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, o_part, lse_part, ws_o, ws_lse,
+                              pair_count, wait_limit_ns(), s);
+  else if (mla)
+    e = launch_decode_mla_tc(plan, h, q, K, shard_rows, rm, Hq, sm_scale, o_part, lse_part, ws_o, ws_lse,
+                             pair_count, wait_limit_ns(), s);
+  else if (gqa_tc_supported(kv_dtype, Hq, Hkv, Dqk, Dv, plan_s_q(h)))
+    e = launch_decode_gqa_tc(plan, h, q, K, V, shard_rows, rm, Hq, Hkv, sm_scale, o_part, lse_part, ws_o,
+                             ws_lse, pair_count, wait_limit_ns(), s);
+  else  // fp32 caches, head dim 64, more query columns per kv head: CUDA cores
+    e = launch_decode_simt(plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk, Dv, sm_scale, o_part, lse_part,
+                           ws_o, ws_lse, pair_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
   if (h.n_split) {
     e = launch_decode_fixup((const int32_t*)dev_plan, h, Hc, Dv, ws_o, ws_lse, o_part, lse_part, s);

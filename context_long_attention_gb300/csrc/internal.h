@@ -23,7 +23,12 @@ inline int plan_s_q(const cp_plan_header& h) { return h.s_q > 0 ? h.s_q : 1; }
 // Device status word layout (written by kernels, read by cp_device_error_check).
 //   [0] non-zero once any bounded wait gave up
 //   [1] kernel id   [2] wait site   [3] block index
-enum KernelId : unsigned { kKernPrefillTc = 1, kKernDecodeMlaTc = 2, kKernDecodeMlaFp8 = 3 };
+enum KernelId : unsigned {
+  kKernPrefillTc = 1,
+  kKernDecodeMlaTc = 2,
+  kKernDecodeMlaFp8 = 3,
+  kKernDecodeGqaTc = 4
+};
 
 struct ShardPtrs {
   const void* p[CP_MAX_SHARDS];
@@ -91,7 +96,7 @@ cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
                               const void* v, int Hq, int Hkv, int D, float sm_scale, void* o,
                               float* lse, bool stall_test, cudaStream_t s);
 
-// bf16 tensor map with a 128-byte swizzle (rank 2 or 3; strides in bytes for
+// bf16 tensor map with a 128-byte swizzle (rank 2 to 4; strides in bytes for
 // dims 1..rank-1).  False if the driver entry point is missing or rejects it.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides, const uint32_t* box);
@@ -124,6 +129,14 @@ cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h
                                 int row_begin, int n_rows, bool bf16, const void* q,
                                 const void* k, const void* v, int Hq, int Hkv, int D,
                                 float sm_scale, void* o, float* lse, cudaStream_t s);
+// The tensor-core GQA decode takes a bf16 cache with head dim 128 and at most
+// 64 query columns per kv head (G s_q), Hkv of them padded to 16/32/64 <= 256.
+bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s_q);
+cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
+                                 const ShardPtrs& k, const ShardPtrs& v, const long long* shard_rows,
+                                 const RowMap& rm, int Hq, int Hkv, float sm_scale, float* o_part,
+                                 float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
+                                 unsigned long long wait_ns, cudaStream_t s);
 cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
                                const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,

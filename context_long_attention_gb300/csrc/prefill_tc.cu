@@ -525,9 +525,9 @@ cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params&
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                             const uint64_t* strides, const uint32_t* box) {
   EncodeTiledFn enc = encode_fn();
-  if (!enc || rank < 2 || rank > 3) return false;
-  cuuint64_t d[3], st[2];
-  cuuint32_t b[3], es[3] = {1, 1, 1};
+  if (!enc || rank < 2 || rank > 4) return false;
+  cuuint64_t d[4], st[3];
+  cuuint32_t b[4], es[4] = {1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];

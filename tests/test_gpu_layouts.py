@@ -113,13 +113,12 @@ def test_mla_query_rows_tiny_requests(cp):
             check_mla(data, ctx, C, s_q, H, fp8, contiguous, o_part, lse_part, o, lse)
 
 
-@pytest.mark.parametrize("contiguous", [False, True])
-@pytest.mark.parametrize("s_q", [1, 3])
-def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
-    ctx = [s_q, 40, 300, 4100]
-    B, Hq, Hkv, D, C = len(ctx), 8, 2, 128, 4
-    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=60 + s_q, device=DEV, std=0.3)
-    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=5, device=DEV)
+def gqa_rows_case(cp, ctx, Hq, Hkv, s_q, contiguous, seed, C=4, n_workers=5, D=128):
+    """GQA decode with s_q query rows per request: every shard's partials and
+    the merged rows against the oracle."""
+    B = len(ctx)
+    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=seed, device=DEV, std=0.3)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=n_workers, device=DEV)
     qq = q.reshape(B, s_q, Hq, D) if s_q > 1 else q
     sk, _ = cp.cp_kv_shard_pack(plan, k)
     sv, _ = cp.cp_kv_shard_pack(plan, v)
@@ -144,6 +143,41 @@ def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
             fo, fl = oracle.decode_attention(qn[b, i], K[:L - s_q + i + 1], V[:L - s_q + i + 1], scale)
             check_o(o[b, i], fo, what=f"GQA merged b{b} row{i}", **TOL_BF16)
             check_lse(lse[b, i], fl)
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("s_q", [1, 3])
+def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
+    gqa_rows_case(cp, [s_q, 40, 300, 4100], 8, 2, s_q, contiguous, seed=60 + s_q)
+
+
+@pytest.mark.parametrize("Hq,Hkv,s_q", [(32, 4, 3), (32, 4, 6), (32, 16, 1), (64, 8, 1), (64, 8, 2), (8, 8, 1)])
+def test_gqa_column_widths(cp, Hq, Hkv, s_q):
+    """The tensor-core GQA decode pads a kv head's G s_q query columns to 16,
+    32 or 64: each width, 16 kv heads, G = 1, ragged tiles and split pairs."""
+    ctx = [s_q, 129, 1000, 2600] + ([0] if s_q == 1 else [])
+    gqa_rows_case(cp, ctx, Hq, Hkv, s_q, False, seed=Hq + 3 * Hkv + s_q, n_workers=7)
+
+
+def test_gqa_full_size_sampled(cp):
+    """16 requests x 131,072 tokens, 32 q / 8 kv heads, head dim 128, C = 8:
+    sampled requests against the oracle (whole context)."""
+    B, L, Hq, Hkv, D, C = 16, 131072, 32, 8, 128, 8
+    ctx = [L] * B
+    q, k, v = W.gqa_decode_inputs(B, ctx, Hq, Hkv, D, "bf16", seed=71, device=DEV)
+    plan = cp.cp_decode_plan(C, ctx, device=DEV)
+    sk, _ = cp.cp_kv_shard_pack(plan, k)
+    sv, _ = cp.cp_kv_shard_pack(plan, v)
+    scale = 1.0 / math.sqrt(D)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, sk, sv, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    qn = np64(q)
+    for b in (0, 11):
+        K, V = np64(k[b * L:(b + 1) * L]), np64(v[b * L:(b + 1) * L])
+        fo, fl = oracle.decode_attention(qn[b], K, V, scale)
+        check_o(o[b], fo, what=f"full-size GQA b{b}", **TOL_BF16)
+        check_lse(lse[b], fl)
 
 
 def test_paged_contiguous_query_rows_match_unpaged(cp):
