@@ -551,9 +551,9 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
     e = launch_decode_mla_tc(plan, h, q, K, shard_rows, rm, Hq, sm_scale, o_part, lse_part, ws_o, ws_lse,
                              pair_count, wait_limit_ns(), s);
   else if (gqa_tc_supported(kv_dtype, Hq, Hkv, Dqk, Dv, plan_s_q(h)))
-    e = launch_decode_gqa_tc(plan, h, q, K, V, shard_rows, rm, Hq, Hkv, sm_scale, o_part, lse_part, ws_o,
+    e = launch_decode_gqa_tc(plan, h, q, K, V, shard_rows, rm, Hq, Hkv, Dqk, sm_scale, o_part, lse_part, ws_o,
                              ws_lse, pair_count, wait_limit_ns(), s);
-  else  // fp32 caches, head dim 64, more query columns per kv head: CUDA cores
+  else  // fp32 caches, other head dims, more query columns per kv head: CUDA cores
     e = launch_decode_simt(plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk, Dv, sm_scale, o_part, lse_part,
                            ws_o, ws_lse, pair_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");

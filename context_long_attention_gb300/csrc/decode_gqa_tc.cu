@@ -1,5 +1,5 @@
-// GQA split-KV decode over a bf16 cache (head dim 128) on the tcgen05 tensor
-// cores.
+// GQA split-KV decode over a bf16 cache (head dim 64 or 128) on the tcgen05
+// tensor cores.
 //
 // One decode step of every request against the rows a virtual shard stores
 // ("How GPUs Share a Long Context During LLM Inference" §3.1-3.4): query head
@@ -12,15 +12,16 @@
 // for each of the s_q query rows, form the unit's n = qi G + i columns
 // (padded to NP = 16, 32 or 64), and the products are transposed so that the
 // MMA M dimension is 128 KV rows:
-//   S^T [128 rows x NP]  = K_g tile [128 x 128 dims] . Q_g^T          (K = 128)
+//   S^T [128 rows x NP]  = K_g tile [128 x D dims] . Q_g^T            (K = D)
 //   O^T [128 dims x NP] += V_g tile^T [128 dims x 128 rows] . P^T     (K = 128)
-// K_g and V_g tiles come by TMA (a 3-d map over [rows][Hkv][128], one box per
+// (at D = 64 the upper 64 dims of V^T are a zero block).
+// K_g and V_g tiles come by TMA (a 3-d map over [rows][Hkv][D], one box per
 // 64-dim chunk); the request's query, all kv heads, by TMA into one operand
 // per kv head; P goes through shared memory as a K-major operand.
 //
 // Warp roles (256 threads): warps 0-3 softmax (thread = KV row of the tile =
 // TMEM lane; in the epilogue a dim row of O^T), warp 4 TMA, warp 5 MMA issue
-// (one elected lane, the loop run warp-wide).  Two K/V stages; two S^T
+// (one elected lane, the loop run warp-wide).  Two or four K/V stages; two S^T
 // buffers in TMEM so the issuer runs the next tile's QK^T ahead of this
 // tile's P.V.  The running max of a column moves only when a score passes it
 // by more than 2^8 (one block-wide vote per tile), which keeps every
@@ -38,11 +39,7 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;                      // KV rows per tile (MMA M)
-constexpr int kD = 128;                         // head dim
 constexpr int kChunkBytes = kRows * 128;        // 64 dims of a tile: 16 KB
-constexpr int kTileBytes = 2 * kChunkBytes;     // K or V tile of one kv head: 32 KB
-constexpr int kStageBytes = 2 * kTileBytes;     // K and V: 64 KB
-constexpr int kStages = 2;
 constexpr int kMaxQCols = 256;                  // Hkv x NP, the query operands of all kv heads
 constexpr int kThreads = 256;
 constexpr int kSoftmax = 128;
@@ -51,10 +48,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int NP>
-constexpr int smem_bytes() {
-  return kStages * kStageBytes + kMaxQCols * 256 + NP * 256 + 1024;
-}
+// Shared-memory geometry for head dim D (64 or 128): a row is D / 64 chunks of
+// 64 dims (128 B, 128-byte swizzle); a stage holds the K and V tiles of one kv
+// head (64 KB at D = 128, 32 KB at D = 64, which takes four stages).  At D = 64
+// the P.V A operand V^T still spans M = 128: its second 64-dim chunk is a
+// zero block.
+template <int D>
+struct Geo {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTileBytes = kChunks * kChunkBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kQBytes = kMaxQCols * 128 * kChunks;  // query operands of all kv heads
+  static constexpr int kZeroBytes = D == 64 ? kChunkBytes : 0;
+  template <int NP>
+  static constexpr int smem() {
+    return kStages * kStageBytes + kQBytes + NP * 256 + kZeroBytes + 1024;
+  }
+};
 
 struct Params {
   const int32_t* plan;
@@ -73,7 +84,7 @@ struct Params {
   unsigned long long wait_ns;
 };
 
-// Tensor maps of the shards' K and V caches ([rows, Hkv, 128], box 64 dims x
+// Tensor maps of the shards' K and V caches ([rows, Hkv, D], box 64 dims x
 // 1 head x 128 rows, 128-byte swizzle); a paged cache has one map of each pool
 // with 64-row boxes.
 struct KVMaps {
@@ -136,8 +147,8 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
 
 // Where an item's partial goes: its pair's row of the partials, or, for one
 // part of a pair split between CTAs, a workspace row merged afterwards.
-__device__ __forceinline__ float* out_rows(const Params& p, const Item& it) {
-  return it.part < 0 ? p.o_part + (long long)it.pair * p.Hc * kD : p.ws_o + (long long)it.part * p.Hc * kD;
+__device__ __forceinline__ float* out_rows(const Params& p, const Item& it, int D) {
+  return it.part < 0 ? p.o_part + (long long)it.pair * p.Hc * D : p.ws_o + (long long)it.part * p.Hc * D;
 }
 __device__ __forceinline__ float* out_lse(const Params& p, const Item& it) {
   return it.part < 0 ? p.lse_part + (long long)it.pair * p.Hc : p.ws_lse + (long long)it.part * p.Hc;
@@ -165,16 +176,20 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t addr, uint32_t (&a)[NP]) {
 // all units of this CTA in the order every role walks them, and each barrier
 // completes once per tile (bar_s[b] once per two, bar_q once per query
 // load), so the parity to wait for follows from g.
-template <int NP>
+template <int NP, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_gqa_tc_kernel(const __grid_constant__ KVMaps maps, const __grid_constant__ CUtensorMap qmap,
                          const Params p) {
+  using Gm = Geo<D>;
+  constexpr int kStages = Gm::kStages, kStageBytes = Gm::kStageBytes, kTileBytes = Gm::kTileBytes;
+  constexpr int kChunks = Gm::kChunks;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sStage = smem;                          // [stage][K: 2 chunks | V: 2 chunks]
-  uint8_t* sQ = smem + kStages * kStageBytes;      // [Hkv][2 chunks][NP rows x 128 B]
-  uint8_t* sP = sQ + kMaxQCols * 256;              // [2 chunks of 64 rows][NP rows x 128 B]
+  uint8_t* sStage = smem;                          // [stage][K: kChunks chunks | V: kChunks chunks]
+  uint8_t* sQ = smem + kStages * kStageBytes;      // [Hkv][kChunks][NP rows x 128 B]
+  uint8_t* sP = sQ + Gm::kQBytes;                  // [2 chunks of 64 rows][NP rows x 128 B]
+  uint8_t* sZero = sP + NP * 256;                  // D = 64: the zero half of V^T
   // full[s]: stage s holds its tile; empty[s]: the tile's products have read it.
   // s[b]: S^T buffer b holds the scores; p: the four softmax warps wrote P;
   // pv: the tile's P.V has completed; q: sQ holds the request's query.
@@ -207,9 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init_fence();
   }
   if (threadIdx.x < NP) sCol[threadIdx.x] = (threadIdx.x / p.G) * p.Hq + threadIdx.x % p.G;
-  // Rows of a kv head's query operand past its G s_q columns stay zero.
-  for (int i = threadIdx.x; i < kMaxQCols * 256 / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  // Rows of a kv head's query operand past its G s_q columns stay zero, and so
+  // does the zero block.
+  for (int i = threadIdx.x; i < Gm::kQBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = threadIdx.x; i < Gm::kZeroBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sZero)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 256);
   tc_fence_before();
@@ -250,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             if (elect_one()) {
-              mbar_expect_tx(smem_u32(&bar_q), p.Hkv * 2 * ncols * 128);
+              mbar_expect_tx(smem_u32(&bar_q), p.Hkv * kChunks * ncols * 128);
               for (int h2 = 0; h2 < p.Hkv; ++h2)
-                for (int c = 0; c < 2; ++c)
-                  tma_load_4d(smem_u32(sQ + (h2 * 2 + c) * NP * 128), &qmap, c * 64, 0, h2, it.b * p.s_q,
+                for (int c = 0; c < kChunks; ++c)
+                  tma_load_4d(smem_u32(sQ + (h2 * kChunks + c) * NP * 128), &qmap, c * 64, 0, h2, it.b * p.s_q,
                               smem_u32(&bar_q));
             }
             __syncwarp();
@@ -265,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(full, kStageBytes);
             if (!p.rm.table) {
               const int y = (int)(it.row0 + (long long)j * kRows);
-              for (int c = 0; c < 2; ++c) {
+              for (int c = 0; c < kChunks; ++c) {
                 tma_load_3d(smem_u32(st + c * kChunkBytes), &maps.k[it.r], c * 64, kh, y, full);
                 tma_load_3d(smem_u32(st + kTileBytes + c * kChunkBytes), &maps.v[it.r], c * 64, kh, y, full);
               }
@@ -275,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int hh = 0; hh < 2; ++hh) {
                 const int i0 = it.row_begin + j * kRows + 64 * hh;
                 const int y = (int)(i0 < it.pd.rows ? map_row(p.rm, it.pair, 0, i0) : p.rm.pool_rows);
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
                   tma_load_3d(smem_u32(st + c * kChunkBytes + hh * 64 * 128), &maps.k[0], c * 64, kh, y, full);
                   tma_load_3d(smem_u32(st + kTileBytes + c * kChunkBytes + hh * 64 * 128), &maps.v[0], c * 64,
                               kh, y, full);
@@ -301,10 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S^T(g) first, then P.V of tile g - 1 once its P is written
     const uint32_t idS = idesc_bf16_f32(kRows, NP, 0, 0);
     const uint32_t idPV = idesc_bf16_f32(kRows, NP, 1, 0);
-    const uint32_t st0 = smem_u32(sStage);
-    // K tile K-major; V^T MN-major (its two 64-dim chunks kChunkBytes apart);
-    // Q_g and P K-major (64-element chunks NP x 128 B apart)
-    const uint64_t dK = smem_desc(st0, 16, 1024), dV = smem_desc(st0 + kTileBytes, kChunkBytes, 1024);
+    const uint32_t st0 = smem_u32(sStage), zero = smem_u32(sZero);
+    // K tile K-major; V^T MN-major (its two 64-dim chunks along M kChunkBytes
+    // apart, or the V chunk and the zero block at D = 64); Q_g and P K-major
+    // (64-element chunks NP x 128 B apart)
+    const uint64_t dK = smem_desc(st0, 16, 1024);
     const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024), dP = smem_desc(smem_u32(sP), 16, 1024);
     bool ok = true;
     int g = 0, q_b = -1, nq = 0;
@@ -314,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p), gp & 1, p.wait_ns, &abort_flag))) return false;
       tc_fence_after();
       if (elect_one()) {
-        const uint64_t v = dV + ((uint32_t)(sp * kStageBytes) >> 4);
+        const uint32_t vaddr = st0 + sp * kStageBytes + kTileBytes;
+        const uint64_t v = smem_desc(vaddr, D == 128 ? kChunkBytes : zero - vaddr, 1024);
 #pragma unroll
         for (int kk = 0; kk < kRows / 16; ++kk)
           mma_ss(tmem + 2 * NP, v + ((kk * 2048) >> 4), dP + (((kk >> 2) * NP * 128 + (kk & 3) * 32) >> 4), idPV,
@@ -348,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the P.V of tile g - 2 waited for
           if (elect_one()) {
             const uint64_t k = dK + ((uint32_t)(s * kStageBytes) >> 4);
-            const uint64_t qd = dQ + ((uint32_t)(kh * 2 * NP * 128) >> 4);
+            const uint64_t qd = dQ + ((uint32_t)(kh * kChunks * NP * 128) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
               const uint32_t qoff = (kk >> 2) * NP * 128 + (kk & 3) * 32;
               mma_ss(tmem + NP * (g & 1), k + (off >> 4), qd + (qoff >> 4), idS, kk > 0);
@@ -389,9 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, wi);
       if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
-        float* out_o = out_rows(p, it);
+        float* out_o = out_rows(p, it, D);
         float* out_l = out_lse(p, it);
-        for (int i = t; i < p.Hc * kD; i += kSoftmax) out_o[i] = 0.f;
+        for (int i = t; i < p.Hc * D; i += kSoftmax) out_o[i] = 0.f;
         for (int i = t; i < p.Hc; i += kSoftmax) out_l[i] = -INFINITY;
         continue;
       }
@@ -510,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kSoftmax);
         // unit column n is output column (n / G) Hq + kh G + n % G
-        float* out_o = out_rows(p, it);
+        float* out_o = out_rows(p, it, D);
         if (t < NP) {
           const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
           sAlpha[t] = tot > 0.f ? 1.f / tot : 0.f;
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int n = 0; n < NP; ++n)
-            if (n < ncols) out_o[(long long)(sCol[n] + kh * p.G) * kD + t] = __uint_as_float(o[n]) * sAlpha[n];
+            if (n < ncols && t < D) out_o[(long long)(sCol[n] + kh * p.G) * D + t] = __uint_as_float(o[n]) * sAlpha[n];
         }
         tc_fence_before();
         // the four softmax warps decide together whether to go on
@@ -537,13 +556,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, 256);
 }
 
-template <int NP>
+template <int NP, int D>
 cudaError_t launch_np(const KVMaps& maps, const CUtensorMap& qmap, const Params& p, int grid, cudaStream_t s) {
-  auto kern = decode_gqa_tc_kernel<NP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NP>());
+  auto kern = decode_gqa_tc_kernel<NP, D>;
+  constexpr int smem = Geo<D>::template smem<NP>();
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem_bytes<NP>(), s>>>(maps, qmap, p);
+  kern<<<grid, kThreads, smem, s>>>(maps, qmap, p);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const KVMaps& maps, const CUtensorMap& qmap, const Params& p, int np, int grid,
+                     cudaStream_t s) {
+  switch (np) {
+    case 16:
+      return launch_np<16, D>(maps, qmap, p, grid, s);
+    case 32:
+      return launch_np<32, D>(maps, qmap, p, grid, s);
+    default:
+      return launch_np<64, D>(maps, qmap, p, grid, s);
+  }
 }
 
 // Columns of a unit padded to the MMA N: 16, 32 or 64.
@@ -552,14 +585,14 @@ int padded_cols(int ncols) { return ncols <= 16 ? 16 : ncols <= 32 ? 32 : 64; }
 }  // namespace
 
 bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s_q) {
-  if (kv_dtype != CP_BF16 || Dqk != kD || Dv != kD || Hkv < 1 || Hq % Hkv) return false;
+  if (kv_dtype != CP_BF16 || (Dqk != 64 && Dqk != 128) || Dv != Dqk || Hkv < 1 || Hq % Hkv) return false;
   const int ncols = (Hq / Hkv) * s_q;
   return ncols <= 64 && Hkv * padded_cols(ncols) <= kMaxQCols;
 }
 
 cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                  const ShardPtrs& k, const ShardPtrs& v, const long long* shard_rows,
-                                 const RowMap& rm, int Hq, int Hkv, float sm_scale, float* o_part,
+                                 const RowMap& rm, int Hq, int Hkv, int D, float sm_scale, float* o_part,
                                  float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
                                  unsigned long long wait_ns, cudaStream_t s) {
   Params p;
@@ -585,9 +618,9 @@ cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.wait_ns = wait_ns;
   KVMaps maps;
   memset(&maps, 0, sizeof(maps));
-  const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)Hkv * kD * 2};
+  const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2};
   if (rm.table) {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)Hkv, (uint64_t)rm.pool_rows};
+    const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)rm.pool_rows};
     const uint32_t box[3] = {64, 1, 64};
     if (!encode_tensor_map_bf16(&maps.k[0], k.p[0], 3, dims, strides, box) ||
         !encode_tensor_map_bf16(&maps.v[0], v.p[0], 3, dims, strides, box))
@@ -595,30 +628,24 @@ cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& 
   } else {
     for (int r = 0; r < h.C; ++r) {
       if (shard_rows[r] == 0) continue;
-      const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)Hkv, (uint64_t)shard_rows[r]};
+      const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)shard_rows[r]};
       const uint32_t box[3] = {64, 1, (uint32_t)kRows};
       if (!encode_tensor_map_bf16(&maps.k[r], k.p[r], 3, dims, strides, box) ||
           !encode_tensor_map_bf16(&maps.v[r], v.p[r], 3, dims, strides, box))
         return cudaErrorInvalidValue;
     }
   }
-  // the queries [B s_q][Hkv][G][128]: one box per (kv head, 64-dim chunk) holds
+  // the queries [B s_q][Hkv][G][D]: one box per (kv head, 64-dim chunk) holds
   // the kv head's G heads of every query row of a request, rows n = qi G + i
   CUtensorMap qmap;
   {
-    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)p.G, (uint64_t)Hkv, (uint64_t)h.R * p.s_q};
-    const uint64_t qstrides[3] = {(uint64_t)kD * 2, (uint64_t)p.G * kD * 2, (uint64_t)Hq * kD * 2};
+    const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)Hkv, (uint64_t)h.R * p.s_q};
+    const uint64_t qstrides[3] = {(uint64_t)D * 2, (uint64_t)p.G * D * 2, (uint64_t)Hq * D * 2};
     const uint32_t box[4] = {64, (uint32_t)p.G, 1, (uint32_t)p.s_q};
     if (!encode_tensor_map_bf16(&qmap, q, 4, dims, qstrides, box)) return cudaErrorInvalidValue;
   }
-  switch (padded_cols(p.G * p.s_q)) {
-    case 16:
-      return launch_np<16>(maps, qmap, p, h.n_tiles, s);
-    case 32:
-      return launch_np<32>(maps, qmap, p, h.n_tiles, s);
-    default:
-      return launch_np<64>(maps, qmap, p, h.n_tiles, s);
-  }
+  const int np = padded_cols(p.G * p.s_q);
+  return D == 64 ? launch_d<64>(maps, qmap, p, np, h.n_tiles, s) : launch_d<128>(maps, qmap, p, np, h.n_tiles, s);
 }
 
 }  // namespace cpattn

@@ -129,12 +129,12 @@ cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h
                                 int row_begin, int n_rows, bool bf16, const void* q,
                                 const void* k, const void* v, int Hq, int Hkv, int D,
                                 float sm_scale, void* o, float* lse, cudaStream_t s);
-// The tensor-core GQA decode takes a bf16 cache with head dim 128 and at most
+// The tensor-core GQA decode takes a bf16 cache with head dim 64 or 128 and at most
 // 64 query columns per kv head (G s_q), Hkv of them padded to 16/32/64 <= 256.
 bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s_q);
 cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                  const ShardPtrs& k, const ShardPtrs& v, const long long* shard_rows,
-                                 const RowMap& rm, int Hq, int Hkv, float sm_scale, float* o_part,
+                                 const RowMap& rm, int Hq, int Hkv, int D, float sm_scale, float* o_part,
                                  float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
                                  unsigned long long wait_ns, cudaStream_t s);
 cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,

@@ -151,12 +151,15 @@ def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
     gqa_rows_case(cp, [s_q, 40, 300, 4100], 8, 2, s_q, contiguous, seed=60 + s_q)
 
 
-@pytest.mark.parametrize("Hq,Hkv,s_q", [(32, 4, 3), (32, 4, 6), (32, 16, 1), (64, 8, 1), (64, 8, 2), (8, 8, 1)])
-def test_gqa_column_widths(cp, Hq, Hkv, s_q):
+@pytest.mark.parametrize("Hq,Hkv,s_q,D", [(32, 4, 3, 128), (32, 4, 6, 128), (32, 16, 1, 128), (64, 8, 1, 128),
+                                          (64, 8, 2, 128), (8, 8, 1, 128), (8, 2, 1, 64), (32, 4, 3, 64),
+                                          (32, 4, 6, 64), (32, 8, 1, 64)])
+def test_gqa_column_widths(cp, Hq, Hkv, s_q, D):
     """The tensor-core GQA decode pads a kv head's G s_q query columns to 16,
-    32 or 64: each width, 16 kv heads, G = 1, ragged tiles and split pairs."""
+    32 or 64: each width at head dim 128 and 64, 16 kv heads, G = 1, ragged
+    tiles and split pairs."""
     ctx = [s_q, 129, 1000, 2600] + ([0] if s_q == 1 else [])
-    gqa_rows_case(cp, ctx, Hq, Hkv, s_q, False, seed=Hq + 3 * Hkv + s_q, n_workers=7)
+    gqa_rows_case(cp, ctx, Hq, Hkv, s_q, False, seed=Hq + 3 * Hkv + s_q + D, n_workers=7, D=D)
 
 
 def test_gqa_full_size_sampled(cp):
