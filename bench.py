@@ -42,20 +42,24 @@ import cp_workloads as W  # noqa: E402
 # DRAM bytes (read + write) per launch from the ncu captures summarised in
 # profiles/; a figure is reported only while the kernel sources it was
 # measured on are unchanged (SHA-1 of the kernel file and the shared PTX
-# header).  The decode captures ran 8 of the 64 requests; their traffic scales
-# with the tokens read.
+# header).  The MLA decode captures ran 8 of the 64 requests and the GQA one 4
+# of 16; their traffic scales with the tokens read.
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "44fff9fda4e68d8f406c141795af9500b6584e56", "bytes": 2.375181e9 + 0.276237e9},
+                "sha1": "cd52c03055d6f55bbce6d7072775ce1cf39f3c2b", "bytes": 2.375940e9 + 0.275704e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "4513d4372c0b3a837ddf6aca7ff7daa9852cc938",
-                   "bytes_per_token": (0.623363e9 + 0.010096e9) / (8 * 131072)},
+                   "sha1": "e69f16b9bcd03fec5060f8f9c972a030945a4345",
+                   "bytes_per_token": (0.623427e9 + 0.009787e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "b171657466e437a5d9757d567876a1272ea0019a",
-                    "bytes_per_token": (1.208762e9 + 0.011218e9) / (8 * 131072)},
+                    "sha1": "43f9c87bbf81615d7476207c07c0e84fa83f7011",
+                    "bytes_per_token": (1.208719e9 + 0.011262e9) / (8 * 131072)},
+    "decode_gqa": {"src": ["context_long_attention_gb300/csrc/decode_gqa_tc.cu",
+                           "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                   "sha1": "01bfeb42674b1a1b19689a00b2cc65f966caf252",
+                   "bytes_per_token": (2.147622e9 + 0.006300e9) / (4 * 131072)},
 }
 
 
@@ -96,6 +100,7 @@ DECODE_WORKLOADS = {
     "uniform": "MLA decode: 64 x 131072 ctx, 64 heads, 576/512 latent, DCP=8, LSE merge",
     "mixed": "MLA decode: 128 requests, bimodal log-uniform ctx 1k..1M (2.4e7 tokens), 64 heads, "
              "576/512 latent, DCP=8, LSE merge",
+    "gqa": "GQA decode: 16 x 131072 ctx, 32 q / 8 kv heads, head dim 128, bf16 cache, DCP=8, LSE merge",
 }
 
 
@@ -121,6 +126,13 @@ def prefill_flops(new_len, prefix_len, Hq, D):
     for n, p in zip(new_len, prefix_len):
         pairs += n * p + n * (n + 1) // 2
     return 4 * D * Hq * pairs, pairs
+
+
+def gqa_decode_bytes(ctx, Hq, Hkv, D):
+    """K and V rows read once (2 Hkv D bf16 per token), the bf16 query and
+    the bf16 merged output."""
+    B = len(ctx)
+    return sum(ctx) * 2 * Hkv * D * 2 + 2 * B * Hq * D * 2
 
 
 def decode_bytes(ctx, H, fp8=True):
@@ -363,19 +375,41 @@ def run_ours(args, world, rank, local):
         o = torch.empty_like(q)
         lse = torch.empty((q.shape[0], Hq), dtype=torch.float32, device=dev)
 
-    # ---- decode inputs (MLA, FP8 cache, packed into token shards once)
-    uniform = args.decode_workload == "uniform"
-    m = W.WORKLOADS["mla" if uniform else "mla_mixed"]
-    if uniform:
-        ctx = [m["ctx"]] * (args.decode_batch or m["B"])
-    else:
+    # ---- decode inputs (MLA latent cache, FP8 or bf16, or a GQA bf16 cache),
+    # packed into token shards once
+    dw = args.decode_workload
+    gqa = dw == "gqa"
+    uniform = dw == "uniform"
+    m = W.WORKLOADS[{"uniform": "mla", "mixed": "mla_mixed", "gqa": "gqa_decode"}[dw]]
+    if dw == "mixed":
         ctx = W.mixed_context_lengths()
         ctx = ctx[:args.decode_batch] if args.decode_batch else ctx
-    fp8 = args.decode_kv == "fp8"
-    d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
-    dscale = 1.0 / math.sqrt(m["Dqk"])
+    else:
+        ctx = [m["ctx"]] * (args.decode_batch or m["B"])
+    fp8 = args.decode_kv == "fp8" and not gqa
+    if gqa:
+        if args.decode_paged or args.decode_rows > 1 or args.sparse_k:
+            raise SystemExit("--decode-workload gqa times the one-row decode from per-shard buffers")
+        d_bytes = gqa_decode_bytes(ctx, m["Hq"], m["Hkv"], m["D"])
+        dscale = 1.0 / math.sqrt(m["D"])
+    else:
+        d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
+        dscale = 1.0 / math.sqrt(m["Dqk"])
     n_dec_kernels = 0
-    if do_dec:
+    vshards = None
+    if do_dec and gqa:
+        Hr, Dv, s_q, pages, scales = m["Hq"], m["D"], 1, None, None
+        layout = cp.CP_DCP_CONTIGUOUS if args.decode_layout == "contiguous" else cp.CP_DCP_ROUND_ROBIN
+        B = len(ctx)
+        dq, kc, vc = W.gqa_decode_inputs(B, ctx, Hr, m["Hkv"], Dv, "bf16", seed=W.SEEDS["gqa_decode"] + rank,
+                                         device=dev)
+        dplan = cp.cp_decode_plan_ex(m["C"], ctx, layout=layout, s_q=1, device=dev)
+        shards, _ = cp.cp_kv_shard_pack(dplan, kc)
+        vshards, _ = cp.cp_kv_shard_pack(dplan, vc)
+        del kc, vc
+        lead = (B,)
+    elif do_dec:
+        Dv = m["Dv"]
         data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS["mla" if uniform else "mla_mixed"] + rank,
                                    device=dev,
                                    bf16=not fp8, fp8=fp8)
@@ -407,13 +441,14 @@ def run_ours(args, world, rank, local):
         B = len(ctx)
         dq = data["q"].reshape(B, s_q, Hr, m["Dqk"]) if s_q > 1 else data["q"]
         lead = (B, s_q) if s_q > 1 else (B,)
-        o_part = torch.empty((m["C"], *lead, Hr, m["Dv"]), dtype=torch.float32, device=dev)
+    if do_dec:
+        o_part = torch.empty((m["C"], *lead, Hr, Dv), dtype=torch.float32, device=dev)
         lse_part = torch.empty((m["C"], *lead, Hr), dtype=torch.float32, device=dev)
-        o_mrg = o_part.view(m["C"], B * s_q, Hr, m["Dv"])
+        o_mrg = o_part.view(m["C"], B * s_q, Hr, Dv)
         lse_mrg = lse_part.view(m["C"], B * s_q, Hr)
-        o_dec = torch.empty((B * s_q, Hr, m["Dv"]), dtype=torch.bfloat16, device=dev)
+        o_dec = torch.empty((B * s_q, Hr, Dv), dtype=torch.bfloat16, device=dev)
         lse_dec = torch.empty((B * s_q, Hr), dtype=torch.float32, device=dev)
-        ws_bytes = cp.cp_decode_workspace_size(dplan, Hr, m["Dv"])
+        ws_bytes = cp.cp_decode_workspace_size(dplan, Hr, Dv)
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         n_dec_kernels = 2 + (1 if dplan.n_split > 0 else 0)  # decode (+ split merge) + LSE merge
     torch.cuda.synchronize(dev)
@@ -434,6 +469,9 @@ def run_ours(args, world, rank, local):
             if pages is not None:
                 cp.cp_decode_attn_paged(dp, pages, cp.CP_DECODE_MLA, dq, shards, scale_pool=scales,
                                         sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
+            elif gqa:
+                cp.cp_decode_attn(dp, cp.CP_DECODE_GQA, dq, shards, vshards, sm_scale=dscale,
+                                  o_part=o_part, lse_part=lse_part, ws=ws)
             else:
                 cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
                                   sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
@@ -562,7 +600,8 @@ def run_ours(args, world, rank, local):
         dec_avg = statistics.mean(dec_ms)
         dec_ach = d_bytes / (dec_avg / 1e3) / 1e9
         dec = {"metric": "decode KV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
-               "kv": args.decode_kv,
+               "kv": "bf16" if gqa else args.decode_kv,
+               "mode": "gqa" if gqa else "mla",
                "cache": (f"paged, {args.decode_paged}-row pages placed at random"
                          if args.decode_paged else "one contiguous buffer per shard"),
                "layout": args.decode_layout,
@@ -572,8 +611,9 @@ def run_ours(args, world, rank, local):
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
                             "frac": dec_ach / hbm,
                             "traffic": (None if args.decode_paged or args.decode_rows > 1
-                                        or args.decode_layout != "round_robin" or not uniform else
-                                        profiled_traffic("decode_" + args.decode_kv, sum(ctx))),
+                                        or args.decode_layout != "round_robin" or not (uniform or gqa) else
+                                        profiled_traffic("decode_" + ("gqa" if gqa else args.decode_kv),
+                                                         sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
     if not args.no_cpu:
@@ -640,7 +680,8 @@ def main():
                     help="zigzag: one 32k request after a 4k prefix (the default line); interleave: "
                          "16 ragged requests, 2^20 tokens (about 1.3 s per step)")
     ap.add_argument("--decode-workload", choices=list(DECODE_WORKLOADS), default="uniform",
-                    help="uniform: 64 x 131072 (the default line); mixed: 128 requests, 1k..1M")
+                    help="uniform: MLA 64 x 131072 (the default line); mixed: MLA 128 requests, "
+                         "1k..1M; gqa: GQA 16 x 131072, 32 q / 8 kv heads, head dim 128")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()

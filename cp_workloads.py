@@ -24,6 +24,9 @@ Workloads (lengths in tokens; "1M" is 2**20):
                   8 token-interleaved shards.
 * ``mla_mixed``   128 requests, bimodal context lengths (18% log-uniform
                   1k..8k, 29% 8k..64k, 53% 64k..1M), FP8 cache, 8 shards.
+* ``gqa_decode``  16 requests x 131,072 cached tokens, GQA 32 q / 8 kv
+                  heads, head dim 128, bf16 ~N(0,1)/sqrt(128), 8
+                  token-interleaved shards.
 
 The long-context agentic traces the pages measure on are not available here;
 these length mixes stand in for them.
@@ -39,7 +42,7 @@ import torch
 E4M3_MAX = 448.0
 
 SEEDS = {"tiny": 1001, "zigzag": 1002, "interleave": 1003, "mla": 1004, "mla_mixed": 1005,
-         "index": 1006}
+         "index": 1006, "gqa_decode": 1007}
 
 WORKLOADS = {
     "tiny": dict(kind="prefill+decode", strategy="zigzag", new_len=[256], prefix_len=[0], C=4,
@@ -50,6 +53,7 @@ WORKLOADS = {
                        Hq=64, Hkv=8, D=128, dtype="bf16", R=16),
     "mla": dict(kind="decode", B=64, ctx=131072, H=64, Dqk=576, Dv=512, C=8),
     "mla_mixed": dict(kind="decode", B=128, ctx=None, H=64, Dqk=576, Dv=512, C=8, kv="fp8"),
+    "gqa_decode": dict(kind="decode", B=16, ctx=131072, Hq=32, Hkv=8, D=128, C=8, kv="bf16"),
 }
 
 
