@@ -261,6 +261,21 @@ def oracle_prefill_sample(rows_per_call=64, seed=0, budget_s=15.0):
     return done_flops / dt / 1e12, dt, done_rows, cores
 
 
+def oracle_decode_sample():
+    """The fp64 oracle on one request of the MLA FP8 decode workload (131,072
+    tokens, 64 heads): E4M3 decode of the cache, then attention over all of
+    it.  Returns (decode KV GB/s, seconds, cores)."""
+    import oracle
+    m = W.WORKLOADS["mla"]
+    d = W.mla_decode_inputs([m["ctx"]], H=m["H"], seed=W.SEEDS["mla"], device="cpu", bf16=False)
+    t0 = time.perf_counter()
+    lat = oracle.e4m3_decode(d["kv_fp8"].numpy())
+    K, V = oracle.mla_cache_to_kv(lat, d["kv_scale"].double().numpy())
+    oracle.decode_attention(d["q"][0].double().numpy(), K, V, 1.0 / math.sqrt(m["Dqk"]))
+    dt = time.perf_counter() - t0
+    return decode_bytes([m["ctx"]], m["H"], fp8=True) / dt / 1e9, dt, len(os.sched_getaffinity(0))
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -621,6 +636,12 @@ def run_ours(args, world, rank, local):
         cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{cpu_rows} query rows x 32 heads of rank 0's late zigzag block, "
                          f"fp64 numpy, {cpu_s:.1f} s"}
+        if do_dec and uniform and fp8:
+            dec_gbs_cpu, dec_s, _ = oracle_decode_sample()
+            cpu["decode"] = {"value": dec_gbs_cpu, "unit": "GB/s",
+                             "sample": f"1 of the {len(ctx)} requests (131,072 FP8 tokens, 64 heads), fp64 "
+                                       f"numpy, {dec_s:.1f} s; the whole batch extrapolates to "
+                                       f"{dec_s * len(ctx):.0f} s"}
     line = {
         "metric": "prefill causal-attn TFLOP/s",
         "value": value,
