@@ -155,6 +155,25 @@ def test_prefill_edge_cases(cp):
     prefill_vs_oracle(cp, cp.CP_INTERLEAVE, [1], [0], 8, 2, 2, 128, "fp32", seed=5)
 
 
+@pytest.mark.parametrize("strategy", [0, 1])
+def test_prefill_maximum_shards(cp, strategy):
+    # C = 64, the shard limit: 128 zigzag blocks, most of a few tokens, some empty
+    prefill_vs_oracle(cp, strategy, [300, 2000, 40], [0, 64, 7], 64, 8, 2, 128, "bf16", seed=21 + strategy)
+
+
+@pytest.mark.parametrize("kind", ["fp8", "bf16", "gqa"])
+def test_decode_maximum_shards(cp, kind):
+    """C = 64, the shard limit: requests shorter than C leave shards empty."""
+    ctx, C = [1, 63, 100, 5000], 64
+    if kind == "gqa":
+        q, k, v = W.gqa_decode_inputs(len(ctx), ctx, 16, 4, 128, "bf16", seed=22, device=DEV, std=0.3)
+        gqa_decode_case(cp, q, k, v, ctx, C, 1.0 / math.sqrt(128), 9)
+    else:
+        fp8 = kind == "fp8"
+        data = W.mla_decode_inputs(ctx, H=64, seed=23, device=DEV, fp8=fp8, bf16=not fp8)
+        mla_decode_case(cp, data, C, fp8, 9)
+
+
 def sample_rows(plan, per_rank=48, seed=0):
     """Each segment's first and last row, plus random rows, per rank."""
     rng = np.random.default_rng(seed)

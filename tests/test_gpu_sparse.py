@@ -45,7 +45,7 @@ def oracle_selection(scores, ctx, C, k, contiguous):
 
 @pytest.mark.parametrize("contiguous", [False, True])
 @pytest.mark.parametrize("ties", [False, True])
-@pytest.mark.parametrize("C,k", [(1, 7), (4, 1), (8, 64), (8, 512), (3, 2048)])
+@pytest.mark.parametrize("C,k", [(1, 7), (4, 1), (8, 64), (8, 512), (3, 2048), (4, 4096)])
 def test_topk_bit_exact(cp, contiguous, ties, C, k):
     ctx = [0, 1, 5, 300, 4100, 20000]
     scores = W.index_scores(ctx, seed=C * 100 + k, device=DEV, ties=ties)
