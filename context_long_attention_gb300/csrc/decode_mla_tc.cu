@@ -58,7 +58,6 @@ constexpr float kRescaleLog2 = 8.0f;
 struct Params {
   const int32_t* plan;
   int B, off_pair, off_worker, off_work;
-  const __nv_bfloat16* q;
   ShardPtrs k;
   RowMap rm;  // paged cache: 64-row boxes of a pool, rows through the page table
   int H;             // columns = s_q query rows x Hrow heads (<= 64)
@@ -521,7 +520,6 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.off_pair = h.off_rank;
   p.off_worker = h.off_req;
   p.off_work = h.off_seg;
-  p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = k;
   p.rm = rm;
   p.s_q = plan_s_q(h);
