@@ -311,6 +311,8 @@ def sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, wo
     each stage timed with CUDA events; inputs resident in HBM."""
     if args.decode_paged or args.decode_rows > 1 or args.decode_layout != "round_robin":
         raise SystemExit("--sparse-k runs on the round-robin, one-row, per-shard cache")
+    if args.decode_workload != "uniform" or ctx[0] % m["C"]:
+        raise SystemExit("--sparse-k runs on the uniform MLA workload with contexts a multiple of C")
     k, C, B, L = args.sparse_k, m["C"], len(ctx), ctx[0]
     scores = W.index_scores(ctx, seed=W.SEEDS["index"] + rank, device=dev)
     st = scores.view(B, L // C, C)  # round robin: shard r holds tokens r, r + C, ...
@@ -400,7 +402,7 @@ def run_ours(args, world, rank, local):
         ctx = W.mixed_context_lengths()
         ctx = ctx[:args.decode_batch] if args.decode_batch else ctx
     else:
-        ctx = [m["ctx"]] * (args.decode_batch or m["B"])
+        ctx = [args.decode_ctx or m["ctx"]] * (args.decode_batch or m["B"])
     fp8 = args.decode_kv == "fp8" and not gqa
     if gqa:
         if args.decode_paged or args.decode_rows > 1 or args.sparse_k:
@@ -703,6 +705,8 @@ def main():
     ap.add_argument("--decode-workload", choices=list(DECODE_WORKLOADS), default="uniform",
                     help="uniform: MLA 64 x 131072 (the default line); mixed: MLA 128 requests, "
                          "1k..1M; gqa: GQA 16 x 131072, 32 q / 8 kv heads, head dim 128")
+    ap.add_argument("--decode-ctx", type=int, default=0, metavar="L",
+                    help="cached tokens per request for the uniform and gqa decode workloads (0: 131072)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
     args = ap.parse_args()
