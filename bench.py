@@ -232,33 +232,55 @@ def max_over_ranks(x, world):
 # --------------------------------------------------------------------------- CPU oracle
 
 
-def oracle_prefill_sample(rows_per_call=64, seed=0, budget_s=15.0):
-    """The fp64 oracle on a bounded sample of the zigzag prefill workload:
-    rows of rank 0's late block (the longest extents) for all heads.
-    Returns (TFLOP/s, seconds, rows, cores)."""
+def oracle_prefill_sample(workload="zigzag", rows_per_call=64, seed=0, budget_s=15.0):
+    """The fp64 oracle on a bounded sample of a prefill workload, all heads:
+    rows of rank 0's late zigzag block (the longest extents), or late rows of
+    the interleave batch's longest request (its K/V and the sampled query rows
+    drawn at that shape: a timing sample, not the GPU run's values).  Returns
+    a dict: TFLOP/s, seconds, rows, cores, (query, key) pairs per second and
+    the whole workload's time extrapolated from the sample."""
     import oracle
-    z = W.WORKLOADS["zigzag"]
-    q, k, v = W.prefill_inputs(z["new_len"], z["prefix_len"], z["Hq"], z["Hkv"], z["D"], "bf16",
-                               seed=W.SEEDS["zigzag"], device="cpu")
-    plan = oracle.zigzag_plan(z["new_len"], z["prefix_len"], z["C"])
-    n_late = len(plan["order"][0]) // 2
+    z = W.WORKLOADS[workload]
+    Hq, Hkv, D, C = z["Hq"], z["Hkv"], z["D"], z["C"]
     rng = np.random.default_rng(seed)
-    L = z["new_len"][0] + z["prefix_len"][0]
-    k64 = k.double().numpy()
-    v64 = v.double().numpy()
-    done_flops = 0
+    if workload == "zigzag":
+        nl, pl = z["new_len"], z["prefix_len"]
+        q, k, v = W.prefill_inputs(nl, pl, Hq, Hkv, D, "bf16", seed=W.SEEDS["zigzag"], device="cpu")
+        plan = oracle.zigzag_plan(nl, pl, C)
+        n_late = len(plan["order"][0]) // 2
+        L = nl[0] + pl[0]
+        qd = q.double().numpy()
+
+        def draw():
+            li = n_late + rng.choice(n_late, size=rows_per_call, replace=False)
+            return qd[np.asarray(plan["order"][0])[li]], np.asarray(plan["pos"][0])[li]
+    else:
+        nl = W.interleave_lengths()
+        pl = [0] * len(nl)
+        L = max(nl)
+        g = torch.Generator().manual_seed(W.SEEDS[workload])
+        sd = 1.0 / math.sqrt(D)
+        k = (torch.randn((L, Hkv, D), generator=g) * sd).to(torch.bfloat16)
+        v = (torch.randn((L, Hkv, D), generator=g) * sd).to(torch.bfloat16)
+
+        def draw():
+            qr = (torch.randn((rows_per_call, Hq, D), generator=g) * sd).to(torch.bfloat16)
+            return qr.double().numpy(), rng.integers(L // 2, L, size=rows_per_call)
+    k64 = k.double().numpy()[:L]
+    v64 = v.double().numpy()[:L]
+    done_pairs = 0
     done_rows = 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < budget_s and done_rows < 64 * rows_per_call:
-        li = n_late + rng.choice(n_late, size=rows_per_call, replace=False)
-        f = np.asarray(plan["order"][0])[li]
-        pos = np.asarray(plan["pos"][0])[li]
-        oracle.causal_rows(q[f].double().numpy(), k64[:L], v64[:L], pos, 1.0 / math.sqrt(z["D"]))
-        done_flops += 4 * z["D"] * z["Hq"] * int((pos + 1).sum())
+        qr, pos = draw()
+        oracle.causal_rows(qr, k64, v64, pos, 1.0 / math.sqrt(D))
+        done_pairs += int((pos + 1).sum())
         done_rows += rows_per_call
     dt = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0))
-    return done_flops / dt / 1e12, dt, done_rows, cores
+    flops, pairs = prefill_flops(nl, pl, Hq, D)
+    rate = 4 * D * Hq * done_pairs / dt
+    return {"tflops": rate / 1e12, "seconds": dt, "rows": done_rows, "cores": len(os.sched_getaffinity(0)),
+            "pairs_per_s": Hq * done_pairs / dt, "full_s": flops / rate}
 
 
 def oracle_decode_sample():
@@ -281,7 +303,8 @@ def run_reference(args, world, rank):
         return
     steps = []
     for i in range(args.warmup + args.steps):
-        tf, dt, rows, cores = oracle_prefill_sample(rows_per_call=16, seed=i, budget_s=2.0)
+        o = oracle_prefill_sample(rows_per_call=16, seed=i, budget_s=2.0)
+        tf, dt, rows, cores = o["tflops"], o["seconds"], o["rows"], o["cores"]
         if i >= args.warmup:
             steps.append((tf, dt, rows))
     value = statistics.median(s[0] for s in steps)
@@ -634,10 +657,12 @@ def run_ours(args, world, rank, local):
                             "peak_kind": peak_kind}}
     cpu = None
     if not args.no_cpu:
-        cpu_tf, cpu_s, cpu_rows, cores = oracle_prefill_sample(rows_per_call=32, budget_s=12.0)
-        cpu = {"value": cpu_tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{cpu_rows} query rows x 32 heads of rank 0's late zigzag block, "
-                         f"fp64 numpy, {cpu_s:.1f} s"}
+        o_s = oracle_prefill_sample(args.prefill_workload, rows_per_call=32, budget_s=12.0)
+        where = ("rank 0's late zigzag block" if zz else "late rows of the interleave batch's longest request")
+        cpu = {"value": o_s["tflops"], "unit": "TFLOP/s", "cores": o_s["cores"], "kind": "oracle",
+               "sample": f"{o_s['rows']} query rows x {Hq} heads of {where}, fp64 numpy, "
+                         f"{o_s['seconds']:.1f} s; {o_s['pairs_per_s']:.3g} (query, key) head pairs/s; "
+                         f"the whole prefill extrapolates to {o_s['full_s']:.0f} s (extrapolated)"}
         if do_dec and uniform and fp8:
             dec_gbs_cpu, dec_s, _ = oracle_decode_sample()
             cpu["decode"] = {"value": dec_gbs_cpu, "unit": "GB/s",
