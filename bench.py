@@ -599,6 +599,22 @@ def run_ours(args, world, rank, local):
                     downloaded[i].record(down)
             stream.wait_event(downloaded[n - 1])
 
+        # the copies' own rates, one upload and one download timed alone
+        ca, cb, cc = ev(), ev(), ev()
+        ca.record(up)
+        with torch.cuda.stream(up):
+            for d_, h_ in zip(dq[0], (qh, kh, vh)):
+                d_.copy_(h_, non_blocking=True)
+        cb.record(up)
+        with torch.cuda.stream(up):
+            oh[0].copy_(do[0][0], non_blocking=True)
+            lh[0].copy_(do[0][1], non_blocking=True)
+        cc.record(up)
+        torch.cuda.synchronize(dev)
+        h2d_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
+        d2h_bytes = o.numel() * 2 + lse.numel() * 4
+        h2d_gbs = h2d_bytes / (ca.elapsed_time(cb) / 1e3) / 1e9
+        d2h_gbs = d2h_bytes / (cb.elapsed_time(cc) / 1e3) / 1e9
         run_e2e(3)
         torch.cuda.synchronize(dev)
         barrier(world)
@@ -609,8 +625,9 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(a.elapsed_time(b), world)
         e2e = {"value": whole_job_rate(p_flops * n_e2e, e2e_ms, world) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 2 + v.numel() * 2,
-               "d2h_bytes_per_step": o.numel() * 2 + lse.numel() * 4,
+               "h2d_bytes_per_step": h2d_bytes,
+               "d2h_bytes_per_step": d2h_bytes,
+               "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
                "steps": n_e2e,
                "note": "pinned host buffers; uploads and downloads on two copy streams overlap "
                        "the neighbouring steps' compute (double-buffered)"}
