@@ -17,7 +17,9 @@
 // (at D = 64 the upper 64 dims of V^T are a zero block).
 // K_g and V_g tiles come by TMA (a 3-d map over [rows][Hkv][D], one box per
 // 64-dim chunk); the request's query, all kv heads, by TMA into one operand
-// per kv head; P goes through shared memory as a K-major operand.
+// per kv head (when those do not fit in 64 KB, as with many kv heads of one
+// query head each, one kv head's operand, loaded at each unit); P goes
+// through shared memory as a K-major operand.
 //
 // Warp roles (256 threads): warps 0-3 softmax (thread = KV row of the tile =
 // TMEM lane; in the epilogue a dim row of O^T), warp 4 TMA, warp 5 MMA issue
@@ -74,6 +76,7 @@ struct Params {
   int Hq, Hkv, G;    // query heads, kv heads, query heads per kv head
   int s_q;           // query rows per request
   int Hc;            // output columns per request: s_q x Hq
+  int q_per_unit;    // the operands of all kv heads do not fit: sQ holds one, loaded per unit
   float scale_log2;  // sm_scale * log2(e)
   float* o_part;
   float* lse_part;
@@ -258,20 +261,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (kh == 0 && j == 0 && new_q) {
-            // the previous tile's QK^T, the last read of sQ, has completed
-            if (g > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[(g - 1) & 1]), ((g - 1) >> 1) & 1,
-                                                            p.wait_ns, &abort_flag))) {
+          if (j == 0 && (p.q_per_unit || (kh == 0 && new_q))) {
+            // the previous tile's QK^T, the last read of sQ, has completed: for
+            // g >= 2 the P.V of tile g - 2, issued after it, has (that phase of
+            // its stage's barrier follows one this warp has already seen); for
+            // g = 1 the first QK^T's own barrier, whose first phase it is
+            const bool freed =
+                g == 0 ||
+                __all_sync(0xffffffffu,
+                           g == 1 ? mbar_wait(smem_u32(&bar_s[0]), 0, p.wait_ns, &abort_flag)
+                                  : mbar_wait(smem_u32(&bar_empty[(g - 2) % kStages]), ((g - 2) / kStages) & 1,
+                                              p.wait_ns, &abort_flag));
+            if (!freed) {
               if (lane == 0) report_timeout(p.status, 2, &abort_flag);
               ok = false;
               break;
             }
             if (elect_one()) {
-              mbar_expect_tx(smem_u32(&bar_q), p.Hkv * kChunks * ncols * 128);
-              for (int h2 = 0; h2 < p.Hkv; ++h2)
+              // every kv head's operand at its slot, or this unit's kv head at slot 0
+              const int h0 = p.q_per_unit ? kh : 0, h1 = p.q_per_unit ? kh + 1 : p.Hkv;
+              mbar_expect_tx(smem_u32(&bar_q), (h1 - h0) * kChunks * ncols * 128);
+              for (int h2 = h0; h2 < h1; ++h2)
                 for (int c = 0; c < kChunks; ++c)
-                  tma_load_4d(smem_u32(sQ + (h2 * kChunks + c) * NP * 128), &qmap, c * 64, 0, h2, it.b * p.s_q,
-                              smem_u32(&bar_q));
+                  tma_load_4d(smem_u32(sQ + ((h2 - h0) * kChunks + c) * NP * 128), &qmap, c * 64, 0, h2,
+                              it.b * p.s_q, smem_u32(&bar_q));
             }
             __syncwarp();
             ++nq;
@@ -353,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < it.ntiles; ++j, ++g) {
           const int s = g % kStages, use = g / kStages;
           bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_full[s]), use & 1, p.wait_ns, &abort_flag));
-          if (got && kh == 0 && j == 0 && new_q) {
+          if (got && j == 0 && (p.q_per_unit || (kh == 0 && new_q))) {
             got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag));
             ++nq;
           }
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the P.V of tile g - 2 waited for
           if (elect_one()) {
             const uint64_t k = dK + ((uint32_t)(s * kStageBytes) >> 4);
-            const uint64_t qd = dQ + ((uint32_t)(kh * kChunks * NP * 128) >> 4);
+            const uint64_t qd = dQ + ((uint32_t)((p.q_per_unit ? 0 : kh) * kChunks * NP * 128) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
@@ -587,7 +600,7 @@ int padded_cols(int ncols) { return ncols <= 16 ? 16 : ncols <= 32 ? 32 : 64; }
 bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s_q) {
   if (kv_dtype != CP_BF16 || (Dqk != 64 && Dqk != 128) || Dv != Dqk || Hkv < 1 || Hq % Hkv) return false;
   const int ncols = (Hq / Hkv) * s_q;
-  return ncols <= 64 && Hkv * padded_cols(ncols) <= kMaxQCols;
+  return ncols <= 64;
 }
 
 cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
@@ -607,6 +620,7 @@ cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.G = Hq / Hkv;
   p.s_q = plan_s_q(h);
   p.Hc = Hq * p.s_q;
+  p.q_per_unit = Hkv * padded_cols(p.G * p.s_q) > kMaxQCols ? 1 : 0;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
   p.lse_part = lse_part;

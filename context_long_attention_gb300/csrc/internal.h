@@ -130,7 +130,7 @@ cudaError_t launch_prefill_simt(const int32_t* dev_plan, const cp_plan_header& h
                                 const void* k, const void* v, int Hq, int Hkv, int D,
                                 float sm_scale, void* o, float* lse, cudaStream_t s);
 // The tensor-core GQA decode takes a bf16 cache with head dim 64 or 128 and at most
-// 64 query columns per kv head (G s_q), Hkv of them padded to 16/32/64 <= 256.
+// 64 query columns per kv head (G s_q).
 bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s_q);
 cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                  const ShardPtrs& k, const ShardPtrs& v, const long long* shard_rows,

@@ -325,11 +325,11 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  * mode CP_DECODE_GQA: q [B, Hq, D] and shard_k[r], shard_v[r]
  *   [rows_r, Hkv, D], all of kv_dtype CP_BF16 or CP_FP32; Dqk = Dv = D,
  *   D % 32 == 0, D <= 256; shard_scale must be NULL.  A bf16 cache with
- *   D = 64 or 128, at most 64 query columns per kv head ((Hq/Hkv) s_q) and
- *   Hkv times those columns padded to 16, 32 or 64 at most 256 runs on the
- *   tensor cores (the kv head's query heads share each K/V tile); other
- *   shapes run on the CUDA cores.  The results agree within the bf16
- *   tolerance either way.
+ *   D = 64 or 128 and at most 64 query columns per kv head ((Hq/Hkv) s_q)
+ *   runs on the tensor cores (the kv head's query heads share each K/V
+ *   tile; Hq = Hkv, plain multi-head attention, included); other shapes run
+ *   on the CUDA cores.  The results agree within the bf16 tolerance either
+ *   way.
  * o_part [C, B, H, Dv] fp32 and lse_part [C, B, H] fp32 (normalised partial
  *   outputs; an empty shard gives O = 0, LSE = -inf).
  * ws: workspace of cp_decode_workspace_size() bytes (NULL if that is 0).

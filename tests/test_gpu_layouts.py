@@ -153,11 +153,13 @@ def test_gqa_layout_and_query_rows(cp, contiguous, s_q):
 
 @pytest.mark.parametrize("Hq,Hkv,s_q,D", [(32, 4, 3, 128), (32, 4, 6, 128), (32, 16, 1, 128), (64, 8, 1, 128),
                                           (64, 8, 2, 128), (8, 8, 1, 128), (8, 2, 1, 64), (32, 4, 3, 64),
-                                          (32, 4, 6, 64), (32, 8, 1, 64)])
+                                          (32, 4, 6, 64), (32, 8, 1, 64), (32, 32, 1, 128), (32, 32, 3, 128),
+                                          (64, 32, 1, 64)])
 def test_gqa_column_widths(cp, Hq, Hkv, s_q, D):
     """The tensor-core GQA decode pads a kv head's G s_q query columns to 16,
     32 or 64: each width at head dim 128 and 64, 16 kv heads, G = 1, ragged
-    tiles and split pairs."""
+    tiles and split pairs; 32 kv heads (multi-head attention among them),
+    whose query operands load one kv head at a time."""
     ctx = [s_q, 129, 1000, 2600] + ([0] if s_q == 1 else [])
     gqa_rows_case(cp, ctx, Hq, Hkv, s_q, False, seed=Hq + 3 * Hkv + s_q + D, n_workers=7, D=D)
 
