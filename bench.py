@@ -58,8 +58,8 @@ PROFILED_TRAFFIC = {
                     "bytes_per_token": (1.208703e9 + 0.010866e9) / (8 * 131072)},
     "decode_gqa": {"src": ["context_long_attention_gb300/csrc/decode_gqa_tc.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "01bfeb42674b1a1b19689a00b2cc65f966caf252",
-                   "bytes_per_token": (2.147665e9 + 0.006333e9) / (4 * 131072)},
+                   "sha1": "a1131f3db55523681afdfcae50d089c7c5e93ac5",
+                   "bytes_per_token": (2.147699e9 + 0.006343e9) / (4 * 131072)},
 }
 
 
@@ -618,16 +618,20 @@ def run_ours(args, world, rank, local):
         run_e2e(3)
         torch.cuda.synchronize(dev)
         barrier(world)
+        e2e_clocks = ClockSampler(dev.index if dev.index is not None else 0)
+        e2e_clocks.start()
         a, b = ev(), ev()
         a.record(stream)
         run_e2e(n_e2e)
         b.record(stream)
         torch.cuda.synchronize(dev)
+        e2e_clock_info = e2e_clocks.stop()
         e2e_ms = max_over_ranks(a.elapsed_time(b), world)
         e2e = {"value": whole_job_rate(p_flops * n_e2e, e2e_ms, world) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_bytes,
                "d2h_bytes_per_step": d2h_bytes,
                "copy_gbs": {"h2d": h2d_gbs, "d2h": d2h_gbs},
+               "clocks": e2e_clock_info,
                "steps": n_e2e,
                "note": "pinned host buffers; uploads and downloads on two copy streams overlap "
                        "the neighbouring steps' compute (double-buffered)"}
