@@ -226,6 +226,42 @@ def test_causal_rows_vs_torch_sdpa(Hq, Hkv, D, n, pre):
     np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("strategy", ["zigzag", "interleave"])
+@pytest.mark.parametrize("C", [1, 3, 4])
+def test_prefill_reference_rank_order_vs_sdpa(strategy, C):
+    """prefill_reference's rows, rank by rank in local order, against torch
+    SDPA over each whole request (its prefix included): local row i of rank r
+    is flattened new token f = order[r][i], whose request and position follow
+    from the request lengths alone."""
+    rng = np.random.default_rng(C * 7 + len(strategy))
+    nl, pl = [37, 20, 1], [5, 0, 3]
+    Hq, Hkv, D = 4, 2, 8
+    T = sum(nl)
+    q = rng.standard_normal((T, Hq, D))
+    k = rng.standard_normal((sum(nl) + sum(pl), Hkv, D))
+    v = rng.standard_normal((sum(nl) + sum(pl), Hkv, D))
+    scale = 1 / math.sqrt(D)
+    plan = oracle.zigzag_plan(nl, pl, C) if strategy == "zigzag" else oracle.interleave_plan_np(nl, pl, C)
+    ref = oracle.prefill_reference(plan, nl, pl, q, k, v, scale)
+    # whole-request SDPA, indexed by flattened new token
+    want_o, want_l = np.zeros((T, Hq, D)), np.zeros((T, Hq))
+    f0, kv0 = 0, 0
+    for n, p_ in zip(nl, pl):
+        pos = np.arange(p_, p_ + n)
+        o_, l_ = sdpa_causal_ref(q[f0:f0 + n], k[kv0:kv0 + p_ + n], v[kv0:kv0 + p_ + n], pos, scale)
+        want_o[f0:f0 + n], want_l[f0:f0 + n] = o_, l_
+        f0 += n
+        kv0 += p_ + n
+    seen = []
+    for r in range(C):
+        local, o, lse = ref[r]
+        f = np.asarray(plan["order"][r], dtype=np.int64)[local]
+        np.testing.assert_allclose(o, want_o[f], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, want_l[f], rtol=1e-12, atol=1e-12)
+        seen.extend(f.tolist())
+    assert sorted(seen) == list(range(T))
+
+
 def test_causal_rows_brute_force_python():
     """Pure-Python probability table on a tiny case (no numpy algebra)."""
     rng = np.random.default_rng(7)
