@@ -399,7 +399,9 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
                    sm_scale=None, o_part=None, lse_part=None, ws=None):
     """Per-shard partial decode attention.  MLA: q [B, H, 576] bf16,
     shard_k[r] [rows_r, 576] bf16 or fp8 codes (+ shard_scale[r]).
-    GQA: q [B, Hq, D], shard_k[r]/shard_v[r] [rows_r, Hkv, D].
+    GQA: q [B, Hq, D], shard_k[r]/shard_v[r] [rows_r, Hkv, D] bf16 or fp32 (q
+    of the same type), or E4M3 codes with shard_scale[r] [rows_r] fp32, one
+    scale per token for its K and V rows (q bf16).
     Returns (o_part [C, B, H, Dv] fp32, lse_part [C, B, H] fp32).  With an
     MTP plan (s_q > 1) q is [B, s_q, H, Dqk] and the outputs [C, B, s_q, ...]."""
     lead, H, Dqk = _decode_shapes(plan, q)
@@ -410,6 +412,9 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
         Hkv, Dv = 1, 512
     else:
         Hkv, Dv = sk[0].shape[1], Dqk
+        want_q = torch.float32 if kv_dtype == CP_FP32 else torch.bfloat16
+        if q.dtype != want_q:
+            raise TypeError(f"GQA decode over this cache takes a {want_q} query, got {q.dtype}")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(Dqk)
     C = plan.C
@@ -442,6 +447,9 @@ def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None
         Hkv, Dv = 1, 512
     else:
         Hkv, Dv = sk[0].shape[1], Dqk
+        want_q = torch.float32 if kv_dtype == CP_FP32 else torch.bfloat16
+        if q.dtype != want_q:
+            raise TypeError(f"GQA decode over this cache takes a {want_q} query, got {q.dtype}")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(Dqk)
     C = plan.C

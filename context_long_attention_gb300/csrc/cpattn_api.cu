@@ -521,8 +521,11 @@ cp_status check_decode_shapes(cp_decode_mode mode, cp_dtype kv_dtype, bool has_v
   } else {
     if (Dqk != Dv || Dqk % 32 || Dqk < 32 || Dqk > 256) return fail(CP_ERR_UNSUPPORTED, "GQA needs Dqk == Dv, a multiple of 32 up to 256");
     if (Hq < 1 || Hkv < 1 || Hq % Hkv) return fail(CP_ERR_INVALID_ARG, "Hq=%d must be a multiple of Hkv=%d", Hq, Hkv);
-    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP32) return fail(CP_ERR_UNSUPPORTED, "GQA cache must be bf16 or fp32");
-    if (!has_v || has_scale) return fail(CP_ERR_INVALID_ARG, "GQA needs shard_v and no shard_scale");
+    if (kv_dtype != CP_BF16 && kv_dtype != CP_FP32 && kv_dtype != CP_FP8_E4M3)
+      return fail(CP_ERR_UNSUPPORTED, "GQA cache must be bf16, fp32 or fp8");
+    if (!has_v) return fail(CP_ERR_INVALID_ARG, "GQA needs shard_v");
+    if ((kv_dtype == CP_FP8_E4M3) != has_scale)
+      return fail(CP_ERR_INVALID_ARG, "shard_scale is required for fp8 and only for fp8");
   }
   return ok();
 }

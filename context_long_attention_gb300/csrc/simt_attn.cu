@@ -7,6 +7,7 @@
 // One warp owns one (query row, head); lane l holds dims l, l+32, ... so that
 // every key/value row is read with coalesced loads.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 
@@ -17,6 +18,9 @@ __device__ __forceinline__ float ld_elem(const float* p, long long i) { return p
 __device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, long long i) {
   return __bfloat162float(p[i]);
 }
+// E4M3 codes (the caller's scale applies separately), converted by CUDA's own
+// fp8 type
+__device__ __forceinline__ float ld_elem(const __nv_fp8_e4m3* p, long long i) { return float(p[i]); }
 __device__ __forceinline__ void st_elem(float* p, long long i, float x) { p[i] = x; }
 __device__ __forceinline__ void st_elem(__nv_bfloat16* p, long long i, float x) {
   p[i] = __float2bfloat16_rn(x);
@@ -88,13 +92,14 @@ __global__ void prefill_simt_kernel(const int32_t* __restrict__ plan, int off_re
 // ------------------------------------------------------------------ decode
 
 // GQA split-KV decode: a warp owns one (query head, work item) and walks the
-// item's shard rows; ND dims per lane (D / 32).  It is HBM-bound at a few
-// FLOP per byte (Hq/Hkv heads reuse each K/V row), so it runs on the CUDA
-// cores with coalesced loads.
-template <typename T, int ND>
+// item's shard rows; ND dims per lane (D / 32).  The shapes the tensor-core
+// GQA kernel does not take land here: fp32 caches, E4M3 caches (codes with one
+// fp32 scale per token for its K and V rows: k = code_k scale, v = code_v
+// scale), other head dims.  TQ is the query's type, T the cache's.
+template <typename TQ, typename T, int ND>
 __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
-                                       int off_worker, int off_work, const T* __restrict__ q,
-                                       ShardPtrs kp, ShardPtrs vp, RowMap rm, int Hq, int Hkv,
+                                       int off_worker, int off_work, const TQ* __restrict__ q,
+                                       ShardPtrs kp, ShardPtrs vp, ScalePtrs sc, RowMap rm, int Hq, int Hkv,
                                        int s_q, float sm_scale, const int32_t* __restrict__ pair_count,
                                        float* __restrict__ o_part, float* __restrict__ lse_part,
                                        float* __restrict__ ws_o, float* __restrict__ ws_lse) {
@@ -123,16 +128,19 @@ __global__ void decode_gqa_simt_kernel(const int32_t* __restrict__ plan, int B, 
     const int row_end = min(min(wd.row_end, n_valid), pair_count ? pair_count[wd.pair] : wd.row_end);
     const T* kb = static_cast<const T*>(kp.p[r]);
     const T* vb = static_cast<const T*>(vp.p[r]);
+    const float* scr = sc.p[r];  // per-row scales of an E4M3 cache, else nullptr
     RowState<ND> st;
     for (int row = wd.row_begin; row < row_end; ++row) {
-      const long long kr = (map_row(rm, wd.pair, pd.row_off, row) * Hkv + g) * D + lane;
+      const long long cr = map_row(rm, wd.pair, pd.row_off, row);
+      const long long kr = (cr * Hkv + g) * D + lane;
+      const float rs = scr ? __ldg(scr + cr) : 1.f;
       float part = 0.f, vv[ND];
 #pragma unroll
       for (int e = 0; e < ND; ++e) {
         part += qv[e] * ld_elem(kb, kr + 32 * e);
-        vv[e] = ld_elem(vb, kr + 32 * e);
+        vv[e] = ld_elem(vb, kr + 32 * e) * rs;
       }
-      st.add(sm_scale * warp_sum(part), vv);
+      st.add(sm_scale * rs * warp_sum(part), vv);
     }
     float* ob;
     float* lb;
@@ -164,17 +172,17 @@ cudaError_t prefill_simt_t(const int32_t* plan, const cp_plan_header& h, int ran
   return cudaGetLastError();
 }
 
-template <typename T, int ND>
+template <typename TQ, typename T, int ND>
 cudaError_t decode_gqa_t(const int32_t* plan, const cp_plan_header& h, const void* q,
-                         const ShardPtrs& k, const ShardPtrs& v, const RowMap& rm, int Hq, int Hkv,
-                         float sm_scale,
+                         const ShardPtrs& k, const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm,
+                         int Hq, int Hkv, float sm_scale,
                          float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                          const int32_t* pair_count, cudaStream_t s) {
   const int warps = 4;
   const int s_q = plan_s_q(h);
   dim3 grid(h.n_tiles, (Hq * s_q + warps - 1) / warps);
-  decode_gqa_simt_kernel<T, ND><<<grid, warps * 32, 0, s>>>(
-      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const T*>(q), k, v, rm, Hq, Hkv,
+  decode_gqa_simt_kernel<TQ, T, ND><<<grid, warps * 32, 0, s>>>(
+      plan, h.R, h.off_rank, h.off_req, h.off_seg, static_cast<const TQ*>(q), k, v, sc, rm, Hq, Hkv,
       s_q, sm_scale, pair_count, o_part, lse_part, ws_o, ws_lse);
   return cudaGetLastError();
 }
@@ -208,15 +216,21 @@ cudaError_t launch_decode_simt(const int32_t* plan, const cp_plan_header& h,
                                int Hkv, int Dqk, int Dv, float sm_scale, float* o_part, float* lse_part,
                                float* ws_o, float* ws_lse, const int32_t* pair_count,
                                cudaStream_t s) {
-  (void)sc;
   (void)Dv;
-#define CP_GQA_CASE(ND)                                                                         \
-  case ND:                                                                                      \
-    return kv_dtype == CP_BF16                                                                  \
-               ? decode_gqa_t<__nv_bfloat16, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale,       \
-                                                 o_part, lse_part, ws_o, ws_lse, pair_count, s) \
-               : decode_gqa_t<float, ND>(plan, h, q, k, v, rm, Hq, Hkv, sm_scale, o_part,       \
-                                         lse_part, ws_o, ws_lse, pair_count, s);
+  ScalePtrs none;
+  for (int r = 0; r < CP_MAX_SHARDS; ++r) none.p[r] = nullptr;
+#define CP_GQA_CASE(ND)                                                                              \
+  case ND:                                                                                           \
+    return kv_dtype == CP_BF16                                                                       \
+               ? decode_gqa_t<__nv_bfloat16, __nv_bfloat16, ND>(plan, h, q, k, v, none, rm, Hq, Hkv, \
+                                                                sm_scale, o_part, lse_part, ws_o,    \
+                                                                ws_lse, pair_count, s)               \
+           : kv_dtype == CP_FP8_E4M3                                                                 \
+               ? decode_gqa_t<__nv_bfloat16, __nv_fp8_e4m3, ND>(plan, h, q, k, v, sc, rm, Hq, Hkv,   \
+                                                                sm_scale, o_part, lse_part, ws_o,    \
+                                                                ws_lse, pair_count, s)               \
+               : decode_gqa_t<float, float, ND>(plan, h, q, k, v, none, rm, Hq, Hkv, sm_scale,      \
+                                                o_part, lse_part, ws_o, ws_lse, pair_count, s);
   switch (Dqk / 32) {
     CP_GQA_CASE(1)
     CP_GQA_CASE(2)

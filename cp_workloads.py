@@ -140,6 +140,19 @@ def gqa_decode_inputs(B, ctx, Hq, Hkv, D, dtype="fp32", seed=0, device="cpu", st
     return q, k, v
 
 
+def gqa_decode_inputs_fp8(B, ctx, Hq, Hkv, D, seed=0, device="cpu", std=None):
+    """GQA decode inputs with an FP8 cache: Q [B, Hq, D] bf16, K and V codes
+    [sum(ctx), Hkv, D] (uint8 E4M3) and one fp32 scale per token for both of
+    its rows (amax over the token's K and V values / 448).  The codes quantise
+    the bf16 K and V of gqa_decode_inputs with the same seed."""
+    q, k, v = gqa_decode_inputs(B, ctx, Hq, Hkv, D, "bf16", seed=seed, device=device, std=std)
+    T = k.shape[0]
+    codes, scale = quantize_e4m3_per_token(torch.cat([k.reshape(T, -1), v.reshape(T, -1)], dim=1))
+    kc = codes[:, :Hkv * D].reshape(T, Hkv, D).contiguous()
+    vc = codes[:, Hkv * D:].reshape(T, Hkv, D).contiguous()
+    return q, kc, vc, scale
+
+
 def quantize_e4m3_per_token(x: torch.Tensor):
     """FP8-E4M3 codes and one fp32 scale per row: scale = amax/448 (1 for an
     all-zero row), code = round-to-nearest-even(x / scale).  Done once, at

@@ -323,8 +323,11 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  *   query and the softmax weights enter those products as pairs of E4M3
  *   numbers whose sum keeps 8 significant bits (see the kernel's notes).
  * mode CP_DECODE_GQA: q [B, Hq, D] and shard_k[r], shard_v[r]
- *   [rows_r, Hkv, D], all of kv_dtype CP_BF16 or CP_FP32; Dqk = Dv = D,
- *   D % 32 == 0, D <= 256; shard_scale must be NULL.  A bf16 cache with
+ *   [rows_r, Hkv, D], all of kv_dtype CP_BF16 or CP_FP32 (shard_scale NULL),
+ *   or shard_k/shard_v E4M3 codes (CP_FP8_E4M3, q bf16) with
+ *   shard_scale[r] [rows_r] fp32, one scale per token for both its K and V
+ *   rows (k = code x scale, v = code x scale); Dqk = Dv = D, D % 32 == 0,
+ *   D <= 256.  An FP8 cache runs on the CUDA cores.  A bf16 cache with
  *   D = 64 or 128 and at most 64 query columns per kv head ((Hq/Hkv) s_q)
  *   runs on the tensor cores (the kv head's query heads share each K/V
  *   tile; Hq = Hkv, plain multi-head attention, included); other shapes run

@@ -282,6 +282,35 @@ def test_decode_gqa_bf16_ragged(cp):
     gqa_decode_case(cp, q, k, v, ctx, 8, 1.0 / math.sqrt(128), 6)
 
 
+@pytest.mark.parametrize("ctx,C,Hq,Hkv,D,nw", [([0, 2, 300, 4100], 4, 16, 4, 128, 6),
+                                                ([1, 700, 2049], 8, 8, 2, 64, 0)])
+def test_decode_gqa_fp8(cp, ctx, C, Hq, Hkv, D, nw):
+    """GQA over an E4M3 cache: codes with one scale per token for its K and
+    V rows; every shard's partial and the merge against the oracle."""
+    q, kc, vc, sc = W.gqa_decode_inputs_fp8(len(ctx), ctx, Hq, Hkv, D, seed=C + D, device=DEV, std=0.3)
+    plan = cp.cp_decode_plan(C, ctx, n_workers=nw, device=DEV)
+    sk, ss = cp.cp_kv_shard_pack(plan, kc, sc)
+    sv, _ = cp.cp_kv_shard_pack(plan, vc)
+    scale = 1.0 / math.sqrt(D)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, sk, sv, shard_scale=ss, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    s64 = sc.double().cpu().numpy()[:, None, None]
+    kn = oracle.e4m3_decode(kc.cpu().numpy()) * s64
+    vn = oracle.e4m3_decode(vc.cpu().numpy()) * s64
+    qn = np64(q)
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    for b, L in enumerate(ctx):
+        kb, vb = kn[base[b]:base[b] + L], vn[base[b]:base[b] + L]
+        po, pl = oracle.decode_shard_partials(qn[b], kb, vb, C, scale)
+        for r in range(C):
+            check_o(o_part[r, b], po[r], what=f"partial r{r} b{b}", **TOL_FP8)
+            check_lse(lse_part[r, b], pl[r])
+        fo, fl = oracle.decode_attention(qn[b], kb, vb, scale)
+        check_o(o[b], fo, what=f"merged b{b}", **TOL_FP8)
+        check_lse(lse[b], fl)
+
+
 def mla_decode_case(cp, data, C, fp8, n_workers, check_reqs=None, H=64):
     ctx = data["ctx"]
     scale = 1.0 / math.sqrt(576)
