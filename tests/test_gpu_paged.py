@@ -139,3 +139,24 @@ def test_paged_decode_gqa(cp):
         for r in range(C):
             check_o(o_part[r, b], po[r], what=f"paged GQA partial r{r} b{b}", **TOL_BF16)
             check_lse(lse_part[r, b], pl[r])
+
+
+def test_paged_decode_gqa_fp8(cp):
+    """GQA over an E4M3 pool: scales read through the page table, partials
+    bit-identical to the per-shard buffers (whose parity the FP8 GQA test
+    checks against the oracle)."""
+    ctx = [0, 5, 300, 2100]
+    C, Hq, Hkv, D = 4, 8, 2, 128
+    q, kc, vc, sc = W.gqa_decode_inputs_fp8(len(ctx), ctx, Hq, Hkv, D, seed=63, device=DEV, std=0.3)
+    scale = 1.0 / math.sqrt(D)
+    plan = cp.cp_decode_plan(C, ctx, n_workers=5, device=DEV)
+    pages = make_pages(cp, plan, 64, seed=64)
+    kpool, spool = cp.cp_kv_shard_pack_paged(plan, pages, kc, sc)
+    vpool, _ = cp.cp_kv_shard_pack_paged(plan, pages, vc)
+    o_p, l_p = cp.cp_decode_attn_paged(plan, pages, cp.CP_DECODE_GQA, q, kpool, vpool, scale_pool=spool,
+                                       sm_scale=scale)
+    ks, ss = cp.cp_kv_shard_pack(plan, kc, sc)
+    vs, _ = cp.cp_kv_shard_pack(plan, vc)
+    o_c, l_c = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, ks, vs, shard_scale=ss, sm_scale=scale)
+    cp.cp_device_error_check()
+    assert torch.equal(o_p, o_c) and torch.equal(l_p, l_c), "paged differs from contiguous"
