@@ -100,7 +100,7 @@ DECODE_WORKLOADS = {
     "uniform": "MLA decode: 64 x 131072 ctx, 64 heads, 576/512 latent, DCP=8, LSE merge",
     "mixed": "MLA decode: 128 requests, bimodal log-uniform ctx 1k..1M (2.4e7 tokens), 64 heads, "
              "576/512 latent, DCP=8, LSE merge",
-    "gqa": "GQA decode: 16 x 131072 ctx, 32 q / 8 kv heads, head dim 128, bf16 cache, DCP=8, LSE merge",
+    "gqa": "GQA decode: 16 x 131072 ctx, 32 q / 8 kv heads, head dim 128, bf16 (or E4M3) cache, DCP=8, LSE merge",
 }
 
 
@@ -128,11 +128,12 @@ def prefill_flops(new_len, prefix_len, Hq, D):
     return 4 * D * Hq * pairs, pairs
 
 
-def gqa_decode_bytes(ctx, Hq, Hkv, D):
-    """K and V rows read once (2 Hkv D bf16 per token), the bf16 query and
-    the bf16 merged output."""
+def gqa_decode_bytes(ctx, Hq, Hkv, D, fp8=False):
+    """K and V rows read once (2 Hkv D values per token: bf16, or E4M3 codes
+    plus one 4-byte scale), the bf16 query and the bf16 merged output."""
     B = len(ctx)
-    return sum(ctx) * 2 * Hkv * D * 2 + 2 * B * Hq * D * 2
+    per_tok = 2 * Hkv * D + 4 if fp8 else 2 * Hkv * D * 2
+    return sum(ctx) * per_tok + 2 * B * Hq * D * 2
 
 
 def decode_bytes(ctx, H, fp8=True):
@@ -426,11 +427,12 @@ def run_ours(args, world, rank, local):
         ctx = ctx[:args.decode_batch] if args.decode_batch else ctx
     else:
         ctx = [args.decode_ctx or m["ctx"]] * (args.decode_batch or m["B"])
-    fp8 = args.decode_kv == "fp8" and not gqa
+    kv_kind = args.decode_kv or ("bf16" if gqa else "fp8")  # MLA defaults to FP8, GQA to bf16
+    fp8 = kv_kind == "fp8"
     if gqa:
         if args.decode_paged or args.decode_rows > 1 or args.sparse_k:
             raise SystemExit("--decode-workload gqa times the one-row decode from per-shard buffers")
-        d_bytes = gqa_decode_bytes(ctx, m["Hq"], m["Hkv"], m["D"])
+        d_bytes = gqa_decode_bytes(ctx, m["Hq"], m["Hkv"], m["D"], fp8=fp8)
         dscale = 1.0 / math.sqrt(m["D"])
     else:
         d_bytes = decode_bytes(ctx, m["H"], fp8=fp8)
@@ -441,10 +443,15 @@ def run_ours(args, world, rank, local):
         Hr, Dv, s_q, pages, scales = m["Hq"], m["D"], 1, None, None
         layout = cp.CP_DCP_CONTIGUOUS if args.decode_layout == "contiguous" else cp.CP_DCP_ROUND_ROBIN
         B = len(ctx)
-        dq, kc, vc = W.gqa_decode_inputs(B, ctx, Hr, m["Hkv"], Dv, "bf16", seed=W.SEEDS["gqa_decode"] + rank,
-                                         device=dev)
+        if fp8:
+            dq, kc, vc, kvs = W.gqa_decode_inputs_fp8(B, ctx, Hr, m["Hkv"], Dv, seed=W.SEEDS["gqa_decode"] + rank,
+                                                      device=dev)
+        else:
+            dq, kc, vc = W.gqa_decode_inputs(B, ctx, Hr, m["Hkv"], Dv, "bf16",
+                                             seed=W.SEEDS["gqa_decode"] + rank, device=dev)
+            kvs = None
         dplan = cp.cp_decode_plan_ex(m["C"], ctx, layout=layout, s_q=1, device=dev)
-        shards, _ = cp.cp_kv_shard_pack(dplan, kc)
+        shards, scales = cp.cp_kv_shard_pack(dplan, kc, kvs)
         vshards, _ = cp.cp_kv_shard_pack(dplan, vc)
         del kc, vc
         lead = (B,)
@@ -510,8 +517,8 @@ def run_ours(args, world, rank, local):
                 cp.cp_decode_attn_paged(dp, pages, cp.CP_DECODE_MLA, dq, shards, scale_pool=scales,
                                         sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
             elif gqa:
-                cp.cp_decode_attn(dp, cp.CP_DECODE_GQA, dq, shards, vshards, sm_scale=dscale,
-                                  o_part=o_part, lse_part=lse_part, ws=ws)
+                cp.cp_decode_attn(dp, cp.CP_DECODE_GQA, dq, shards, vshards, shard_scale=scales,
+                                  sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
             else:
                 cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
                                   sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
@@ -661,7 +668,7 @@ def run_ours(args, world, rank, local):
         dec_avg = statistics.mean(dec_ms)
         dec_ach = d_bytes / (dec_avg / 1e3) / 1e9
         dec = {"metric": "decode KV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
-               "kv": "bf16" if gqa else args.decode_kv,
+               "kv": kv_kind,
                "mode": "gqa" if gqa else "mla",
                "cache": (f"paged, {args.decode_paged}-row pages placed at random"
                          if args.decode_paged else "one contiguous buffer per shard"),
@@ -672,8 +679,9 @@ def run_ours(args, world, rank, local):
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
                             "frac": dec_ach / hbm,
                             "traffic": (None if args.decode_paged or args.decode_rows > 1
-                                        or args.decode_layout != "round_robin" or not (uniform or gqa) else
-                                        profiled_traffic("decode_" + ("gqa" if gqa else args.decode_kv),
+                                        or args.decode_layout != "round_robin" or not (uniform or gqa)
+                                        or (gqa and fp8) else
+                                        profiled_traffic("decode_" + ("gqa" if gqa else kv_kind),
                                                          sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
@@ -734,8 +742,8 @@ def main():
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="time one half of the step (for profiler captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
-    ap.add_argument("--decode-kv", choices=["fp8", "bf16"], default="fp8",
-                    help="decode cache type (the MLA workload has both)")
+    ap.add_argument("--decode-kv", choices=["fp8", "bf16"], default=None,
+                    help="decode cache type (default: fp8 for the MLA workloads, bf16 for gqa)")
     ap.add_argument("--decode-paged", type=int, default=0, metavar="PAGE_ROWS",
                     help="decode from a paged pool with pages of this many rows (multiple of 64), "
                          "placed at random; 0 = one contiguous buffer per shard")

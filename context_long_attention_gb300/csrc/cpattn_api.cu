@@ -553,6 +553,9 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   else if (mla)
     e = launch_decode_mla_tc(plan, h, q, K, shard_rows, rm, Hq, sm_scale, o_part, lse_part, ws_o, ws_lse,
                              pair_count, wait_limit_ns(), s);
+  else if (kv_dtype == CP_FP8_E4M3 && gqa_f8_supported(Hq, Hkv, Dqk, Dv, plan_s_q(h), rm.table != nullptr))
+    e = launch_decode_gqa_f8(plan, h, q, K, V, S, shard_rows, Hq, Hkv, sm_scale, o_part, lse_part, ws_o, ws_lse,
+                             pair_count, wait_limit_ns(), s);
   else if (gqa_tc_supported(kv_dtype, Hq, Hkv, Dqk, Dv, plan_s_q(h)))
     e = launch_decode_gqa_tc(plan, h, q, K, V, shard_rows, rm, Hq, Hkv, Dqk, sm_scale, o_part, lse_part, ws_o,
                              ws_lse, pair_count, wait_limit_ns(), s);

@@ -27,7 +27,8 @@ enum KernelId : unsigned {
   kKernPrefillTc = 1,
   kKernDecodeMlaTc = 2,
   kKernDecodeMlaFp8 = 3,
-  kKernDecodeGqaTc = 4
+  kKernDecodeGqaTc = 4,
+  kKernDecodeGqaF8 = 5
 };
 
 struct ShardPtrs {
@@ -103,6 +104,9 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const ui
 
 // [rows, cols] byte tensor (row stride row_bytes), box [box_rows, box_cols],
 // 128-byte swizzle if swizzle_128 else 64-byte.
+// 3-d byte tensor (strides in bytes for dims 1..2), 128-byte swizzle.
+bool encode_tensor_map_u8_3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides,
+                             const uint32_t* box);
 bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                              uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
                              bool swizzle_128);
@@ -135,6 +139,15 @@ bool gqa_tc_supported(cp_dtype kv_dtype, int Hq, int Hkv, int Dqk, int Dv, int s
 cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                  const ShardPtrs& k, const ShardPtrs& v, const long long* shard_rows,
                                  const RowMap& rm, int Hq, int Hkv, int D, float sm_scale, float* o_part,
+                                 float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
+                                 unsigned long long wait_ns, cudaStream_t s);
+// The tensor-core GQA decode over an E4M3 cache (codes expanded to f16 in
+// shared memory): head dim 128, at most 32 query columns per kv head, per-shard
+// buffers (not a paged pool).
+bool gqa_f8_supported(int Hq, int Hkv, int Dqk, int Dv, int s_q, bool paged);
+cudaError_t launch_decode_gqa_f8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
+                                 const ShardPtrs& k, const ShardPtrs& v, const ScalePtrs& sc,
+                                 const long long* shard_rows, int Hq, int Hkv, float sm_scale, float* o_part,
                                  float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
                                  unsigned long long wait_ns, cudaStream_t s);
 cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,

@@ -538,6 +538,17 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const ui
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tensor_map_u8_3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides,
+                             const uint32_t* box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]}, st[2] = {strides[0], strides[1]};
+  const cuuint32_t b[3] = {box[0], box[1], box[2]}, es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, st, b, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                              uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
                              bool swizzle_128) {

@@ -327,7 +327,10 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  *   or shard_k/shard_v E4M3 codes (CP_FP8_E4M3, q bf16) with
  *   shard_scale[r] [rows_r] fp32, one scale per token for both its K and V
  *   rows (k = code x scale, v = code x scale); Dqk = Dv = D, D % 32 == 0,
- *   D <= 256.  An FP8 cache runs on the CUDA cores.  A bf16 cache with
+ *   D <= 256.  An FP8 cache with D = 128, at most 32 query columns per kv
+ *   head and per-shard buffers runs on the tensor cores (the codes expanded
+ *   to f16 in shared memory); other FP8 shapes, and a paged FP8 pool, on the
+ *   CUDA cores.  A bf16 cache with
  *   D = 64 or 128 and at most 64 query columns per kv head ((Hq/Hkv) s_q)
  *   runs on the tensor cores (the kv head's query heads share each K/V
  *   tile; Hq = Hkv, plain multi-head attention, included); other shapes run

@@ -142,9 +142,9 @@ def test_paged_decode_gqa(cp):
 
 
 def test_paged_decode_gqa_fp8(cp):
-    """GQA over an E4M3 pool: scales read through the page table, partials
-    bit-identical to the per-shard buffers (whose parity the FP8 GQA test
-    checks against the oracle)."""
+    """GQA over an E4M3 pool: scales read through the page table; the paged
+    partials against the oracle, and within the FP8 bound of the per-shard
+    ones (which take the tensor-core kernel)."""
     ctx = [0, 5, 300, 2100]
     C, Hq, Hkv, D = 4, 8, 2, 128
     q, kc, vc, sc = W.gqa_decode_inputs_fp8(len(ctx), ctx, Hq, Hkv, D, seed=63, device=DEV, std=0.3)
@@ -159,4 +159,14 @@ def test_paged_decode_gqa_fp8(cp):
     vs, _ = cp.cp_kv_shard_pack(plan, vc)
     o_c, l_c = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, ks, vs, shard_scale=ss, sm_scale=scale)
     cp.cp_device_error_check()
-    assert torch.equal(o_p, o_c) and torch.equal(l_p, l_c), "paged differs from contiguous"
+    assert (o_p - o_c).abs().max().item() <= 6e-2
+    s64 = sc.double().cpu().numpy()[:, None, None]
+    kn = oracle.e4m3_decode(kc.cpu().numpy()) * s64
+    vn = oracle.e4m3_decode(vc.cpu().numpy()) * s64
+    qn = np64(q)
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    for b, L in enumerate(ctx):
+        po, pl = oracle.decode_shard_partials(qn[b], kn[base[b]:base[b] + L], vn[base[b]:base[b] + L], C, scale)
+        for r in range(C):
+            check_o(o_p[r, b], po[r], what=f"paged FP8 GQA partial r{r} b{b}", **TOL_FP8)
+            check_lse(l_p[r, b], pl[r])

@@ -283,7 +283,10 @@ def test_decode_gqa_bf16_ragged(cp):
 
 
 @pytest.mark.parametrize("ctx,C,Hq,Hkv,D,nw", [([0, 2, 300, 4100], 4, 16, 4, 128, 6),
-                                                ([1, 700, 2049], 8, 8, 2, 64, 0)])
+                                                ([1, 700, 2049], 8, 8, 2, 64, 0),
+                                                ([3, 129, 5000], 8, 32, 1, 128, 7),
+                                                ([0, 640, 3000], 4, 32, 2, 128, 0),
+                                                ([257, 1000], 4, 64, 1, 128, 5)])
 def test_decode_gqa_fp8(cp, ctx, C, Hq, Hkv, D, nw):
     """GQA over an E4M3 cache: codes with one scale per token for its K and
     V rows; every shard's partial and the merge against the oracle."""
