@@ -9,7 +9,7 @@
 // its K and V rows (k = code x scale, v = code x scale).
 //
 // Every E4M3 value is exactly an f16 value, so the codes are expanded to f16
-// in shared memory by four converter warps and the products run as kind::f16
+// in shared memory by six converter warps and the products run as kind::f16
 // with f16 operands:
 //   S^T [128 rows x NP]  = K_codes_g [128 x 128] . (Q_g 2^e)^T, scaled per row
 //                           by scale_row 2^-e in the softmax,
@@ -19,11 +19,11 @@
 // puts its largest magnitude in [2^13, 2^14), so its bf16 values are exact in
 // f16.
 //
-// Warp roles (320 threads): warps 0-3 softmax (thread = KV row of the tile =
+// Warp roles (384 threads): warps 0-3 softmax (thread = KV row of the tile =
 // TMEM lane; in the epilogue a dim row of O^T), warp 4 TMA (codes into two
 // staging slots), warp 5 MMA issue (one elected lane, the loop run
-// warp-wide), warps 6-9 expand the codes into two f16 stages and convert each
-// unit's query; two S^T buffers in TMEM.
+// warp-wide), warps 6-11 expand the codes into two f16 stages and convert
+// each unit's query; two S^T buffers in TMEM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -45,9 +45,11 @@ constexpr int kChunkBytes = kRows * 128;    // 64 dims of an f16 tile: 16 KB
 constexpr int kTileBytes = 2 * kChunkBytes; // f16 K or V tile: 32 KB
 constexpr int kStageBytes = 2 * kTileBytes; // f16 K and V: 64 KB
 constexpr int kSlots = 2, kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kSoftmax = 128;
-constexpr int kConv = 128;  // converter threads (warps 6-9, one per SM sub-partition)
+constexpr int kConvWarps = 6;
+constexpr int kConv = kConvWarps * 32;  // converter threads (warps 6-11: three SM sub-partitions hold
+                                        // three warps, the register cap of 168 a thread either way)
 constexpr int kWarpTma = 4, kWarpMma = 5, kWarpConv0 = 6;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int sRed[4][NP];   // cross-warp column maxima
   __shared__ float sL[4][NP];   // cross-warp column sums
   __shared__ int sCol[NP];      // output column of unit column n for kv head 0
-  __shared__ uint32_t sQmax[4]; // the converter warps' largest |q| (bf16 magnitude bits)
+  __shared__ uint32_t sQmax[kConvWarps];  // the converter warps' largest |q| (bf16 magnitude bits)
   __shared__ int sQe[4];        // unit u's query exponent e, at u % 4
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else if (warp >= kWarpConv0) {
-    // ------------------------------------------------------------ converters (warps 6-9):
+    // ------------------------------------------------------------ converters (warps 6-11):
     // each unit's query to f16 x 2^e, each tile's codes to f16
     const int ct = threadIdx.x - kWarpConv0 * 32;  // 0 .. kConv - 1
     bool ok = true;
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mx = __reduce_max_sync(0xffffffffu, mx);
               if (lane == 0) sQmax[warp - kWarpConv0] = mx;
               named_bar_sync(2, kConv);
-              mx = max(max(sQmax[0], sQmax[1]), max(sQmax[2], sQmax[3]));
+              for (int w2 = 0; w2 < kConvWarps; ++w2) mx = max(mx, sQmax[w2]);
               // 2^e puts the largest |q| in [2^13, 2^14); e kept where 2^e and 2^-e are normal
               const int ex = (int)((mx >> 7) & 0xFF) - 127;
               const int e = mx == 0 ? 0 : max(-126, min(126, 13 - ex));
