@@ -632,20 +632,22 @@ cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.wait_ns = wait_ns;
   KVMaps maps;
   memset(&maps, 0, sizeof(maps));
+  // a kv head's slice of a row is 2 D bytes: at D = 64 a 128-byte slice, whose
+  // neighbours (the other kv heads) are read in later units, so L2 fetches stay 128 bytes
   const uint64_t strides[2] = {(uint64_t)D * 2, (uint64_t)Hkv * D * 2};
   if (rm.table) {
     const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)rm.pool_rows};
     const uint32_t box[3] = {64, 1, 64};
-    if (!encode_tensor_map_bf16(&maps.k[0], k.p[0], 3, dims, strides, box) ||
-        !encode_tensor_map_bf16(&maps.v[0], v.p[0], 3, dims, strides, box))
+    if (!encode_tensor_map_bf16(&maps.k[0], k.p[0], 3, dims, strides, box, D == 128) ||
+        !encode_tensor_map_bf16(&maps.v[0], v.p[0], 3, dims, strides, box, D == 128))
       return cudaErrorInvalidValue;
   } else {
     for (int r = 0; r < h.C; ++r) {
       if (shard_rows[r] == 0) continue;
       const uint64_t dims[3] = {(uint64_t)D, (uint64_t)Hkv, (uint64_t)shard_rows[r]};
       const uint32_t box[3] = {64, 1, (uint32_t)kRows};
-      if (!encode_tensor_map_bf16(&maps.k[r], k.p[r], 3, dims, strides, box) ||
-          !encode_tensor_map_bf16(&maps.v[r], v.p[r], 3, dims, strides, box))
+      if (!encode_tensor_map_bf16(&maps.k[r], k.p[r], 3, dims, strides, box, D == 128) ||
+          !encode_tensor_map_bf16(&maps.v[r], v.p[r], 3, dims, strides, box, D == 128))
         return cudaErrorInvalidValue;
     }
   }

@@ -99,12 +99,16 @@ cudaError_t launch_prefill_tc(const int32_t* dev_plan, const int32_t* host_plan,
 
 // bf16 tensor map with a 128-byte swizzle (rank 2 to 4; strides in bytes for
 // dims 1..rank-1).  False if the driver entry point is missing or rejects it.
+// promote_256: L2 fetches widened to 256 bytes (the box rows are 256 bytes or
+// neighbouring boxes are read together); else 128 bytes (a box row is a
+// 128-byte slice whose neighbours are read much later).
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides, const uint32_t* box);
+                            const uint64_t* strides, const uint32_t* box, bool promote_256 = true);
 
 // [rows, cols] byte tensor (row stride row_bytes), box [box_rows, box_cols],
 // 128-byte swizzle if swizzle_128 else 64-byte.
-// 3-d byte tensor (strides in bytes for dims 1..2), 128-byte swizzle.
+// 3-d byte tensor (strides in bytes for dims 1..2), 128-byte swizzle, L2
+// fetches of 128 bytes (a box row is one kv head's 128-byte slice of a row).
 bool encode_tensor_map_u8_3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides,
                              const uint32_t* box);
 bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,

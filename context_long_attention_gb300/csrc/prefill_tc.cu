@@ -523,7 +523,7 @@ cudaError_t launch_d(const CUtensorMap& km, const CUtensorMap& vm, const Params&
 }  // namespace
 
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-                            const uint64_t* strides, const uint32_t* box) {
+                            const uint64_t* strides, const uint32_t* box, bool promote_256) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || rank < 2 || rank > 4) return false;
   cuuint64_t d[4], st[3];
@@ -535,7 +535,8 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const ui
   for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, st, b, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             promote_256 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_tensor_map_u8_3d(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides,
@@ -545,7 +546,7 @@ bool encode_tensor_map_u8_3d(CUtensorMap* m, const void* base, const uint64_t* d
   const cuuint64_t d[3] = {dims[0], dims[1], dims[2]}, st[2] = {strides[0], strides[1]};
   const cuuint32_t b[3] = {box[0], box[1], box[2]}, es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, st, b, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
