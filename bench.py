@@ -47,19 +47,23 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "cd52c03055d6f55bbce6d7072775ce1cf39f3c2b", "bytes": 2.376776e9 + 0.276023e9},
+                "sha1": "df3c47221f9a4778217bee17d5d95d14f5eea68b", "bytes": 2.373758e9 + 0.275600e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "e69f16b9bcd03fec5060f8f9c972a030945a4345",
-                   "bytes_per_token": (0.624172e9 + 0.010335e9) / (8 * 131072)},
+                   "sha1": "6861272f9604b5957ab957f1a61cbad8e4a08a2b",
+                   "bytes_per_token": (0.623026e9 + 0.010095e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "0a9bd16be333ff8f6a95e2a27bd68654912905d5",
-                    "bytes_per_token": (1.208703e9 + 0.010866e9) / (8 * 131072)},
+                    "sha1": "04100416602e6fe976f64f3844df844162af152b",
+                    "bytes_per_token": (1.208702e9 + 0.011389e9) / (8 * 131072)},
     "decode_gqa": {"src": ["context_long_attention_gb300/csrc/decode_gqa_tc.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "a1131f3db55523681afdfcae50d089c7c5e93ac5",
-                   "bytes_per_token": (2.147699e9 + 0.006343e9) / (4 * 131072)},
+                   "sha1": "5c78af98b68dea241bf2ff79d760ad98160a7703",
+                   "bytes_per_token": (2.147962e9 + 0.006286e9) / (4 * 131072)},
+    "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
+                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                    "sha1": "e616155ef8e891b9d763749b709609c8249e70ec",
+                    "bytes_per_token": (1.077085e9 + 0.006480e9) / (4 * 131072)},
 }
 
 
@@ -680,9 +684,9 @@ def run_ours(args, world, rank, local):
                             "frac": dec_ach / hbm,
                             "traffic": (None if args.decode_paged or args.decode_rows > 1
                                         or args.decode_layout != "round_robin" or not (uniform or gqa)
-                                        or (gqa and fp8) else
-                                        profiled_traffic("decode_" + ("gqa" if gqa else kv_kind),
-                                                         sum(ctx))),
+                                        else profiled_traffic(("decode_gqa" + ("8" if fp8 else ""))
+                                                              if gqa else "decode_" + kv_kind,
+                                                              sum(ctx))),
                             "peak_kind": peak_kind}}
     cpu = None
     if not args.no_cpu:
