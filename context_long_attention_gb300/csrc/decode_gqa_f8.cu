@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // units behind the converters (a unit's query load waits for the P.V of the
   // tile two before it, which waits for that tile's softmax), so one barrier
   // for it would let its phase run two ahead of the wait.
-  __shared__ __align__(8) uint64_t bar_code[kSlots], bar_codefree[kSlots], bar_full[kStages],
+  __shared__ __align__(8) uint64_t bar_code[kSlots], bar_codefree[kSlots], bar_fullK[kStages], bar_fullV[kStages],
       bar_empty[kStages], bar_s[2], bar_p, bar_pv, bar_q, bar_qf, bar_qe[4], bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -227,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bar_codefree[s]), kConv);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), kConv);
+      mbar_init(smem_u32(&bar_fullK[s]), kConv);
+      mbar_init(smem_u32(&bar_fullV[s]), kConv);
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
     mbar_init(smem_u32(&bar_s[0]), 1);
@@ -364,29 +365,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // ---- codes of slot s -> f16 stage st (K then V)
+          // ---- codes of slot s -> f16 stage st: K, announced on its own so that
+          // QK^T and the softmax overlap the conversion of V
           const uint8_t* src = sSlot + s * kSlotBytes;
           uint8_t* dst = sStage + st * kStageBytes;
+#pragma unroll 1
+          for (int tsr = 0; tsr < 2; ++tsr) {
 #pragma unroll 4
-          for (int i = ct; i < 2 * kRows * 8; i += kConv) {
-            const int tsr = i >> 10, r = (i >> 3) & (kRows - 1), u = i & 7;  // tensor, row, 16-code unit
-            const uint4 v = *reinterpret_cast<const uint4*>(src + tsr * kCodeBytes + r * 128 + ((u ^ (r & 7)) << 4));
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[8];
+            for (int i = ct; i < kRows * 8; i += kConv) {
+              const int r = i >> 3, u = i & 7;  // row, 16-code unit
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(src + tsr * kCodeBytes + r * 128 + ((u ^ (r & 7)) << 4));
+              const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+              uint32_t h[8];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              h[2 * e] = e4m3x2_to_f16x2_hw<0>(wd[e]);
-              h[2 * e + 1] = e4m3x2_to_f16x2_hw<2>(wd[e]);
+              for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_to_f16x2_hw<0>(wd[e]);
+                h[2 * e + 1] = e4m3x2_to_f16x2_hw<2>(wd[e]);
+              }
+              // dims 16u .. 16u + 15: chunk u / 4, 16-byte units 2 (u % 4) and 2 (u % 4) + 1
+              uint8_t* rowp = dst + tsr * kTileBytes + (u >> 2) * kChunkBytes + r * 128;
+              const int w0u = 2 * (u & 3);
+              *reinterpret_cast<uint4*>(rowp + ((w0u ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(rowp + (((w0u + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
             }
-            // dims 16u .. 16u + 15: chunk u / 4, 16-byte units 2 (u % 4) and 2 (u % 4) + 1
-            uint8_t* rowp = dst + tsr * kTileBytes + (u >> 2) * kChunkBytes + r * 128;
-            const int w0u = 2 * (u & 3);
-            *reinterpret_cast<uint4*>(rowp + ((w0u ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(rowp + (((w0u + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            fence_proxy_async_smem();
+            if (tsr == 0) mbar_arrive(smem_u32(&bar_fullK[st]));
           }
-          fence_proxy_async_smem();
           mbar_arrive(smem_u32(&bar_codefree[s]));
-          mbar_arrive(smem_u32(&bar_full[st]));
+          mbar_arrive(smem_u32(&bar_fullV[st]));
         }
       }
     }
@@ -409,6 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int prev_j = -1, prev_s = 0;  // tile index in its unit and stage of the tile whose P.V is pending
     auto pv = [&](int gp, int jp, int sp) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p), gp & 1, p.wait_ns, &abort_flag))) return false;
+      // every earlier phase of this stage's V barrier was waited for here
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fullV[sp]), (gp / kStages) & 1, p.wait_ns,
+                                             &abort_flag)))
+        return false;
       tc_fence_after();
       if (elect_one()) {
         const uint64_t v = dV + ((uint32_t)(sp * kStageBytes) >> 4);
@@ -427,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kh = 0; kh < p.Hkv && it.ntiles > 0 && ok; ++kh, ++nu) {
         for (int j = 0; j < it.ntiles; ++j, ++g) {
           const int s = g % kStages;
-          bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_full[s]), (g / kStages) & 1, p.wait_ns,
+          bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fullK[s]), (g / kStages) & 1, p.wait_ns,
                                                        &abort_flag));
           if (got && j == 0)
             got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_qf), nu & 1, p.wait_ns, &abort_flag));
