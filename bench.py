@@ -62,8 +62,8 @@ PROFILED_TRAFFIC = {
                    "bytes_per_token": (2.147962e9 + 0.006286e9) / (4 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "e616155ef8e891b9d763749b709609c8249e70ec",
-                    "bytes_per_token": (1.077085e9 + 0.006480e9) / (4 * 131072)},
+                    "sha1": "c77af04969f83e602ccf338767b0de680d3bfdee",
+                    "bytes_per_token": (1.077104e9 + 0.006117e9) / (4 * 131072)},
 }
 
 
