@@ -60,12 +60,20 @@ struct Geo {
   static constexpr int kChunks = D / 64;
   static constexpr int kTileBytes = kChunks * kChunkBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = D == 64 ? 4 : 2;
-  static constexpr int kQBytes = kMaxQCols * 128 * kChunks;  // query operands of all kv heads
+  // at D = 128 a third 64 KB stage takes the room of the query operands of
+  // all kv heads: the query slot holds one unit's operand, loaded per unit
+  // (at 64 columns the three stages and the kernel's static arrays would pass
+  // the 227 KB a block may hold: two stages there)
+  template <int NP>
+  __host__ __device__ static constexpr int stages() {
+    return D == 64 ? 4 : (NP == 64 ? 2 : 3);
+  }
+  static constexpr bool kQPerUnit = D == 128;
+  static constexpr int kQBytes = (kQPerUnit ? 64 : kMaxQCols) * 128 * kChunks;
   static constexpr int kZeroBytes = D == 64 ? kChunkBytes : 0;
   template <int NP>
   static constexpr int smem() {
-    return kStages * kStageBytes + kQBytes + NP * 256 + kZeroBytes + 1024;
+    return stages<NP>() * kStageBytes + kQBytes + NP * 256 + kZeroBytes + 1024;
   }
 };
 
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_gqa_tc_kernel(const __grid_constant__ KVMaps maps, const __grid_constant__ CUtensorMap qmap,
                          const Params p) {
   using Gm = Geo<D>;
-  constexpr int kStages = Gm::kStages, kStageBytes = Gm::kStageBytes, kTileBytes = Gm::kTileBytes;
+  constexpr int kStages = Gm::template stages<NP>(), kStageBytes = Gm::kStageBytes, kTileBytes = Gm::kTileBytes;
   constexpr int kChunks = Gm::kChunks;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -620,7 +628,7 @@ cudaError_t launch_decode_gqa_tc(const int32_t* dev_plan, const cp_plan_header& 
   p.G = Hq / Hkv;
   p.s_q = plan_s_q(h);
   p.Hc = Hq * p.s_q;
-  p.q_per_unit = Hkv * padded_cols(p.G * p.s_q) > kMaxQCols ? 1 : 0;
+  p.q_per_unit = (D == 128 || Hkv * padded_cols(p.G * p.s_q) > kMaxQCols) ? 1 : 0;
   p.scale_log2 = sm_scale * kLog2e;
   p.o_part = o_part;
   p.lse_part = lse_part;
