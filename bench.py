@@ -58,8 +58,8 @@ PROFILED_TRAFFIC = {
                     "bytes_per_token": (1.208702e9 + 0.011389e9) / (8 * 131072)},
     "decode_gqa": {"src": ["context_long_attention_gb300/csrc/decode_gqa_tc.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "5c78af98b68dea241bf2ff79d760ad98160a7703",
-                   "bytes_per_token": (2.147962e9 + 0.006286e9) / (4 * 131072)},
+                   "sha1": "66afd4cc6ca2416d3262e0e21695f9dcf534f72c",
+                   "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "c77af04969f83e602ccf338767b0de680d3bfdee",
