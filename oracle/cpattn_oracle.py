@@ -20,7 +20,7 @@ definitions.  Sources, cited by page title and section:
 * [GLM]  vLLM blog "GLM-5.3 Part 2: PCP, DCP and Hybrid HiSparse on 16 H200",
          footnote 1 (MLA: QK over 576 dims, PV over 512)
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * zigzag remainder: the first ``n mod 2C`` blocks (in block order) get one
   extra token ([SGL] "early blocks receive the remainder");
