@@ -36,6 +36,11 @@ class CpError(RuntimeError):
 
 if not os.path.exists(lib_path):
     raise ImportError(f"{lib_path} is missing: build it with __graft_entry__.build()")
+if os.path.isdir(os.path.join(_HERE, "csrc")):
+    from . import _build
+    if _build.is_stale():
+        raise ImportError(f"{lib_path} was built from other sources than the ones in "
+                          f"{os.path.join(_HERE, 'csrc')}: rebuild it with __graft_entry__.build()")
 lib = ctypes.CDLL(lib_path)
 
 _vp, _i, _sz, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
@@ -59,6 +64,7 @@ _SIGS = {
     "cp_lse_fold": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "cp_decode_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
                                     _vp, _vp]),
+    "cp_noalloc_scratch_bytes": (_sz, []),
     "cp_kv_shard_pack_paged": (_i, [_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i,
                                     _vp]),
     "cp_decode_attn_paged": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
@@ -71,11 +77,11 @@ _SIGS = {
     "cp_sparse_decode_attn": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
                                    _vp, _vp, _vp, _sz, _vp]),
 }
-NOALLOC_SCRATCH_BYTES = 16 << 20
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
     _fn.restype = _res
     _fn.argtypes = _args
+NOALLOC_SCRATCH_BYTES = int(lib.cp_noalloc_scratch_bytes())
 
 
 def _check(status: int):
@@ -457,11 +463,12 @@ def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None
         o_part = torch.empty((C, *lead, H, Dv), dtype=torch.float32, device=q.device)
     if lse_part is None:
         lse_part = torch.empty((C, *lead, H), dtype=torch.float32, device=q.device)
-    _check(lib.cp_decode_attn_noalloc(
-        _np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q), _ptr_array(sk),
-        _ptr_array(shard_v) if shard_v is not None else None,
-        _ptr_array(shard_scale) if shard_scale is not None else None, H, Hkv, Dqk, Dv,
-        float(sm_scale), _ptr(o_part), _ptr(lse_part), _stream(q.device)))
+    with torch.cuda.device(q.device):  # the library uses the current device's array
+        _check(lib.cp_decode_attn_noalloc(
+            _np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q), _ptr_array(sk),
+            _ptr_array(shard_v) if shard_v is not None else None,
+            _ptr_array(shard_scale) if shard_scale is not None else None, H, Hkv, Dqk, Dv,
+            float(sm_scale), _ptr(o_part), _ptr(lse_part), _stream(q.device)))
     return o_part, lse_part
 
 

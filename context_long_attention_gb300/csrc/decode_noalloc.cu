@@ -2,9 +2,8 @@
 // library-owned device array instead of a caller-provided workspace.
 //
 // Who needs it: callers that cannot allocate device memory at the point of
-// the call — code running inside a CUDA-graph capture that must not grow the
-// memory pool, real-time serving loops with a fixed memory budget, and
-// plugins called through a C interface that gives them no allocator.  They
+// the call — real-time serving loops held to a fixed memory budget, and
+// plugins reached through a C interface that gives them no allocator.  They
 // pass inputs and outputs only; the partial results of KV ranges that the
 // schedule splits across CTAs go to a static __device__ array.
 //
@@ -18,9 +17,12 @@
 // them on one stream.
 //
 // Host code cannot pass the symbol itself to a kernel (in host code it names a
-// host-side stand-in).  The device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made on
-// it; make that first call before any stream capture begins.
+// host-side stand-in).  The device address comes from cudaGetSymbolAddress
+// with the query's device current.  It is looked up again on every call made
+// while the stream is not capturing (so a context torn down and re-created,
+// e.g. after cudaDeviceReset, never leaves a stale address behind); a call on
+// a capturing stream uses the address cached by the last such lookup on that
+// device, so the first call on a device must come before any stream capture.
 #include <mutex>
 
 #include "internal.h"
@@ -32,18 +34,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[CP_NOALLOC_SCRA
 std::mutex g_scratch_mu;
 void* g_scratch_ptr[256] = {nullptr};
 
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+cudaError_t scratch_address(int dev, cudaStream_t stream, void** out) {
   if (dev < 0 || dev >= 256) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     if (!p) return cudaErrorInvalidSymbol;
     g_scratch_ptr[dev] = p;
+  } else if (!g_scratch_ptr[dev]) {
+    return cudaErrorStreamCaptureUnsupported;  // no earlier call on this device
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;
@@ -67,13 +71,38 @@ extern "C" cp_status cp_decode_attn_noalloc(const void* host_plan, const void* d
         "cp_decode_attn_noalloc: this plan needs %zu bytes of scratch, more than the fixed "
         "%zu-byte array; call cp_decode_attn with a workspace, or plan with fewer workers",
         need, (size_t)CP_NOALLOC_SCRATCH_BYTES);
+  // The array used is the current device's: q must live on that device.
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return cpattn::report_error(CP_ERR_CUDA, "cp_decode_attn_noalloc: cudaGetDevice failed: %s",
+                                cudaGetErrorString(e));
+  if (q) {
+    cudaPointerAttributes attr;
+    e = cudaPointerGetAttributes(&attr, q);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return cpattn::report_error(CP_ERR_INVALID_ARG,
+                                  "cp_decode_attn_noalloc: q is not a device pointer");
+    }
+    if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+      return cpattn::report_error(
+          CP_ERR_INVALID_ARG,
+          "cp_decode_attn_noalloc: q lives on device %d but device %d is current; make q's "
+          "device current before the call",
+          attr.device, dev);
+  }
   void* scratch = nullptr;
-  cudaError_t e = scratch_address(&scratch);
+  e = scratch_address(dev, static_cast<cudaStream_t>(stream), &scratch);
   if (e != cudaSuccess)
     return cpattn::report_error(CP_ERR_CUDA,
-                                "cp_decode_attn_noalloc: looking up the scratch array failed: %s",
+                                "cp_decode_attn_noalloc: looking up the scratch array failed "
+                                "(the first call on a device must not be on a capturing "
+                                "stream): %s",
                                 cudaGetErrorString(e));
   return cp_decode_attn(host_plan, dev_plan, mode, kv_dtype, q, shard_k, shard_v, shard_scale, Hq,
                         Hkv, Dqk, Dv, sm_scale, o_part, lse_part, scratch,
                         (size_t)CP_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+extern "C" size_t cp_noalloc_scratch_bytes(void) { return (size_t)CP_NOALLOC_SCRATCH_BYTES; }

@@ -480,10 +480,9 @@ cp_status cp_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o
  * cp_decode_attn_noalloc — cp_decode_attn for callers that cannot allocate.
  *
  * The pages have no counterpart: this is an interface convenience.  Some
- * callers cannot allocate device memory where they call the decode: code
- * inside a CUDA-graph capture that must not grow the memory pool, serving
- * loops with a fixed memory budget, plugins reached through a C interface
- * without an allocator.  This entry point takes the same arguments as
+ * callers cannot allocate device memory where they call the decode: serving
+ * loops held to a fixed memory budget, and plugins reached through a C
+ * interface that gives them no allocator.  This entry point takes the same arguments as
  * cp_decode_attn minus the workspace, and keeps the split-KV partial results
  * in a library-owned static device array of CP_NOALLOC_SCRATCH_BYTES.
  *
@@ -496,11 +495,18 @@ cp_status cp_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o
  *   contents; nothing in it needs to start at zero (each slot is fully written
  *   before it is read within one call).  Calls that overlap on the GPU race
  *   on the array: serialise them on one stream.
- * - Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, that device current); make that first call before
- *   any stream capture begins.
+ * - Device: the array used is the current device's; q must live on the
+ *   current device, else CP_ERR_INVALID_ARG.
+ * - Set-up: every call on a stream that is not capturing looks up the array's
+ *   device address (cudaGetSymbolAddress, the current device) and caches it
+ *   per device, so a context torn down and re-created (cudaDeviceReset) never
+ *   leaves a stale address; a call on a capturing stream uses that cache, so
+ *   the first call on a device must come before any stream capture begins
+ *   (else CP_ERR_CUDA).
  * ------------------------------------------------------------------------- */
 #define CP_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per device */
+/* The array's size in bytes (CP_NOALLOC_SCRATCH_BYTES of the built library). */
+size_t cp_noalloc_scratch_bytes(void);
 cp_status cp_decode_attn_noalloc(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
                                  cp_dtype kv_dtype, const void* q, const void* const* shard_k,
                                  const void* const* shard_v, const float* const* shard_scale,

@@ -37,6 +37,14 @@ def test_library_exports_every_declared_symbol(cp):
     assert cp.lib.cp_version() == 1
 
 
+def test_noalloc_scratch_size_matches_header(cp):
+    with open(os.path.join(ROOT, "include", "cpattn.h")) as f:
+        m = re.search(r"#define CP_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", f.read())
+    assert m, "CP_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert cp.lib.cp_noalloc_scratch_bytes() == int(m.group(1)) << int(m.group(2))
+    assert cp._binding.NOALLOC_SCRATCH_BYTES == cp.lib.cp_noalloc_scratch_bytes()
+
+
 def expand_segments(plan):
     """(f, pos, req) of every rank-major row, from the host segment table."""
     T = plan.T
