@@ -37,6 +37,32 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+def source_digest() -> str:
+    """SHA-1 of everything the library is built from: the kernel sources and
+    headers, the public header and the compiler flags.  build() stores it
+    beside the library; a library whose stored digest differs is stale."""
+    import hashlib
+    h = hashlib.sha1(" ".join(ARCH + NVCC_FLAGS[:-4]).encode())
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cuh", ".h"))]
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
+    for path in sorted(files):
+        h.update(os.path.relpath(path, ROOT).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+STAMP = LIB + ".srcsha1"
+
+
+def is_stale() -> bool:
+    """True if the library is missing or was built from other sources."""
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
+        return True
+    with open(STAMP) as f:
+        return f.read().strip() != source_digest()
+
+
 def _compile(src: str) -> tuple[str, str]:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
@@ -51,6 +77,7 @@ def _compile(src: str) -> tuple[str, str]:
 def build(verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
+    digest = source_digest()
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         results = list(ex.map(_compile, srcs))
@@ -66,6 +93,8 @@ def build(verbose: bool = False) -> str:
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(digest + "\n")
     return LIB
 
 
