@@ -288,19 +288,38 @@ def oracle_prefill_sample(workload="zigzag", rows_per_call=64, seed=0, budget_s=
             "pairs_per_s": Hq * done_pairs / dt, "full_s": flops / rate}
 
 
-def oracle_decode_sample():
-    """The fp64 oracle on one request of the MLA FP8 decode workload (131,072
-    tokens, 64 heads): E4M3 decode of the cache, then attention over all of
-    it.  Returns (decode KV GB/s, seconds, cores)."""
+def oracle_decode_sample(ctx=None, workload="mla", fp8=True):
+    """The fp64 oracle on one request of an MLA decode workload (64 heads):
+    E4M3 decode of the cache (FP8) or its bf16 values, then attention over all
+    of it.  Returns (decode KV GB/s, seconds, cores)."""
     import oracle
-    m = W.WORKLOADS["mla"]
-    d = W.mla_decode_inputs([m["ctx"]], H=m["H"], seed=W.SEEDS["mla"], device="cpu", bf16=False)
+    m = W.WORKLOADS[workload]
+    ctx = ctx or m["ctx"]
+    d = W.mla_decode_inputs([ctx], H=m["H"], seed=W.SEEDS[workload], device="cpu", bf16=not fp8, fp8=fp8)
     t0 = time.perf_counter()
-    lat = oracle.e4m3_decode(d["kv_fp8"].numpy())
-    K, V = oracle.mla_cache_to_kv(lat, d["kv_scale"].double().numpy())
+    if fp8:
+        lat = oracle.e4m3_decode(d["kv_fp8"].numpy())
+        K, V = oracle.mla_cache_to_kv(lat, d["kv_scale"].double().numpy())
+    else:
+        K, V = oracle.mla_cache_to_kv(d["kv_bf16"].double().numpy(), None)
     oracle.decode_attention(d["q"][0].double().numpy(), K, V, 1.0 / math.sqrt(m["Dqk"]))
     dt = time.perf_counter() - t0
-    return decode_bytes([m["ctx"]], m["H"], fp8=True) / dt / 1e9, dt, len(os.sched_getaffinity(0))
+    return decode_bytes([ctx], m["H"], fp8=fp8) / dt / 1e9, dt, len(os.sched_getaffinity(0))
+
+
+def oracle_tiny():
+    """The fp64 oracle on the whole tiny workload: the zigzag prefill of all 4
+    shards and the 257-token decode.  Returns (seconds, cores)."""
+    import oracle
+    w = W.WORKLOADS["tiny"]
+    t = W.tiny_inputs(device="cpu")
+    f64 = lambda x: x.double().numpy()  # noqa: E731
+    scale = 1.0 / math.sqrt(w["D"])
+    t0 = time.perf_counter()
+    plan = oracle.zigzag_plan(w["new_len"], w["prefix_len"], w["C"])
+    oracle.prefill_reference(plan, w["new_len"], w["prefix_len"], f64(t["q"]), f64(t["k"]), f64(t["v"]), scale)
+    oracle.decode_attention(f64(t["dec_q"][0]), f64(t["dec_k"]), f64(t["dec_v"]), scale)
+    return time.perf_counter() - t0, len(os.sched_getaffinity(0))
 
 
 def run_reference(args, world, rank):
@@ -394,7 +413,289 @@ def sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, wo
             "note": "scores read once + selected rows once + Q + O over the time of all four stages"}
 
 
+def time_region(dev, stream, world, step, steps, warmup):
+    """W untimed steps, then K steps, each bracketed by CUDA events on the
+    launch stream, between a barrier and a synchronize on both sides; clocks
+    sampled by nvidia-smi meanwhile.  Returns (per-step records, clocks)."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(warmup):
+        step(None)
+    torch.cuda.synchronize(dev)
+    recs = [None] * steps
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for i in range(steps):
+        recs[i] = step(ev)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return recs, clocks.stop()
+
+
+def leg_prefill_interleave(cp, args, dev, stream, world, rank, peaks, peak_kind):
+    """The ragged interleave prefill (16 requests, 2^20 tokens, 64 q / 8 kv
+    heads): shard plan + prefill per step, against the sustained tensor peak
+    (one launch lasts over a second)."""
+    z = W.WORKLOADS["interleave"]
+    nl = W.interleave_lengths()
+    pl = [0] * len(nl)
+    Hq, Hkv, D, C = z["Hq"], z["Hkv"], z["D"], z["C"]
+    q, k, v = W.prefill_inputs(nl, pl, Hq, Hkv, D, "bf16", seed=W.SEEDS["interleave"] + rank, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], Hq), dtype=torch.float32, device=dev)
+    flops, _ = prefill_flops(nl, pl, Hq, D)
+    scale = 1.0 / math.sqrt(D)
+
+    def step(ev):
+        e = [ev() for _ in range(3)] if ev else None
+        if e:
+            e[0].record(stream)
+        plan = cp.cp_shard_plan(cp.CP_INTERLEAVE, C, nl, pl, device=dev)
+        if e:
+            e[1].record(stream)
+        cp.cp_prefill_attn(plan, q, k, v, scale, out=o, lse=lse)
+        if e:
+            e[2].record(stream)
+        return e
+
+    steps = max(1, min(args.steps, args.leg_steps_long))
+    recs, clk = time_region(dev, stream, world, step, steps, max(3, min(args.warmup, 3)))
+    cp.cp_device_error_check(dev)
+    plan_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    pre_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    total = max_over_ranks(sum(plan_ms) + sum(pre_ms), world)
+    ach = flops / (statistics.mean(pre_ms) / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    out = {"workload": PREFILL_WORKLOADS["interleave"], "lengths": {"requests": len(nl), "tokens": sum(nl),
+                                                                  "median": int(statistics.median(nl))},
+           "metric": "prefill causal-attn TFLOP/s", "unit": "TFLOP/s",
+           "value": whole_job_rate(flops * steps, total, world) / 1e12,
+           "steps": steps, "ms_plan": statistics.mean(plan_ms), "ms_prefill": statistics.mean(pre_ms),
+           "flops_per_step": flops, "gpu_launches": 2 * steps,
+           "roofline": {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                        "frac": ach / peak, "traffic": None,
+                        "peak_kind": peak_kind + " sustained", "kernel": "prefill_tc_kernel<128>"},
+           "clocks": clk}
+    if not args.no_cpu and rank == 0:
+        o_s = oracle_prefill_sample("interleave", rows_per_call=32, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = {
+            "value": o_s["tflops"], "unit": "TFLOP/s", "cores": o_s["cores"], "kind": "oracle",
+            "sample": f"{o_s['rows']} query rows x {Hq} heads, late rows of the longest request, fp64 "
+                      f"numpy, {o_s['seconds']:.1f} s; the whole prefill extrapolates to "
+                      f"{o_s['full_s']:.0f} s (extrapolated)"}
+    return out
+
+
+def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, fp8):
+    """MLA decode of one of the decode workloads (plan + split-KV decode + LSE
+    merge per step) from per-shard buffers packed once before timing."""
+    m = W.WORKLOADS[workload]
+    ctx = W.mixed_context_lengths() if workload == "mla_mixed" else [m["ctx"]] * m["B"]
+    data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS[workload] + rank, device=dev,
+                               bf16=not fp8, fp8=fp8)
+    plan = cp.cp_decode_plan(m["C"], ctx, device=dev)
+    if fp8:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_fp8"], data["kv_scale"])
+        del data["kv_fp8"], data["kv_scale"]
+    else:
+        shards, scales = cp.cp_kv_shard_pack(plan, data["kv_bf16"])
+        del data["kv_bf16"]
+    torch.cuda.empty_cache()
+    dq = data["q"]
+    B, H, Dv, C = len(ctx), m["H"], m["Dv"], m["C"]
+    o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((C, B, H), dtype=torch.float32, device=dev)
+    o_dec = torch.empty((B, H, Dv), dtype=torch.bfloat16, device=dev)
+    lse_dec = torch.empty((B, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, cp.cp_decode_workspace_size(plan, H, Dv)), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(m["Dqk"])
+    nbytes = decode_bytes(ctx, H, fp8=fp8)
+
+    def step(ev):
+        e = [ev() for _ in range(3)] if ev else None
+        if e:
+            e[0].record(stream)
+        dp = cp.cp_decode_plan(C, ctx, device=dev)
+        cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales, sm_scale=scale,
+                          o_part=o_part, lse_part=lse_part, ws=ws)
+        if e:
+            e[1].record(stream)
+        cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
+        if e:
+            e[2].record(stream)
+        return e
+
+    steps = max(1, min(args.steps, args.leg_steps))
+    recs, clk = time_region(dev, stream, world, step, steps, max(3, args.warmup))
+    cp.cp_device_error_check(dev)
+    dec_ms = [r[0].elapsed_time(r[1]) for r in recs]
+    mrg_ms = [r[1].elapsed_time(r[2]) for r in recs]
+    total = max_over_ranks(sum(dec_ms) + sum(mrg_ms), world)
+    ach = nbytes / (statistics.mean(dec_ms) / 1e3) / 1e9
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    n_k = 2 + (1 if plan.n_split > 0 else 0)
+    out = {"workload": (DECODE_WORKLOADS["mixed"] if workload == "mla_mixed" else DECODE_WORKLOADS["uniform"]),
+           "kv": "fp8" if fp8 else "bf16", "metric": "decode KV HBM GB/s", "unit": "GB/s",
+           "context": {"requests": B, "tokens": sum(ctx), "median": int(statistics.median(ctx)),
+                       "min": min(ctx), "max": max(ctx)},
+           "value": whole_job_rate(nbytes * steps, total, world) / 1e9, "steps": steps,
+           "ms_decode": statistics.mean(dec_ms), "ms_merge": statistics.mean(mrg_ms),
+           "merge_share": statistics.mean(mrg_ms) / (statistics.mean(dec_ms) + statistics.mean(mrg_ms)),
+           "bytes_per_step": nbytes, "gpu_launches": n_k * steps,
+           "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                        "traffic": (profiled_traffic("decode_fp8" if fp8 else "decode_bf16", sum(ctx))
+                                    if workload == "mla" else None),
+                        "peak_kind": peak_kind,
+                        "kernel": "decode_mla_fp8_kernel" if fp8 else "decode_mla_tc_kernel"},
+           "clocks": clk}
+    del shards, scales, o_part, lse_part, o_dec, lse_dec, ws, data
+    torch.cuda.empty_cache()
+    if not args.no_cpu and rank == 0:
+        one = sorted(ctx)[len(ctx) // 2]  # the median request
+        gbs, sec, cores = oracle_decode_sample(one, workload, fp8)
+        out["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                               "sample": f"1 request of {one} {'FP8' if fp8 else 'bf16'} tokens (the "
+                                         f"batch's median), 64 heads, fp64 numpy, {sec:.1f} s; the "
+                                         f"whole batch extrapolates to {sec * sum(ctx) / one:.0f} s "
+                                         "(extrapolated)"}
+    return out
+
+
+def leg_tiny(cp, args, dev, stream, world, rank):
+    """The tiny workload as one step: zigzag plan + fp32 prefill over 4
+    shards, decode plan + GQA decode of the 257-token cache over 4
+    token-interleaved shards (packed before timing) + LSE merge."""
+    w = W.WORKLOADS["tiny"]
+    t = W.tiny_inputs(device=dev)
+    scale = 1.0 / math.sqrt(w["D"])
+    dplan = cp.cp_decode_plan(w["C"], t["ctx"], device=dev)
+    sk, _ = cp.cp_kv_shard_pack(dplan, t["dec_k"])
+    sv, _ = cp.cp_kv_shard_pack(dplan, t["dec_v"])
+    pflops, _ = prefill_flops(w["new_len"], w["prefix_len"], w["Hq"], w["D"])
+    dbytes = 2 * w["decode_ctx"] * w["Hkv"] * w["D"] * 4 + 2 * w["Hq"] * w["D"] * 4
+
+    def step(ev):
+        e = [ev() for _ in range(3)] if ev else None
+        if e:
+            e[0].record(stream)
+        plan = cp.cp_shard_plan(cp.CP_ZIGZAG, w["C"], w["new_len"], w["prefix_len"], device=dev)
+        cp.cp_prefill_attn(plan, t["q"], t["k"], t["v"], scale)
+        if e:
+            e[1].record(stream)
+        dp = cp.cp_decode_plan(w["C"], t["ctx"], device=dev)
+        op, lp = cp.cp_decode_attn(dp, cp.CP_DECODE_GQA, t["dec_q"], sk, sv, sm_scale=scale)
+        cp.cp_lse_merge(op, lp, out_dtype=torch.float32)
+        if e:
+            e[2].record(stream)
+        return e
+
+    steps = max(1, min(args.steps, 50))
+    recs, clk = time_region(dev, stream, world, step, steps, max(3, args.warmup))
+    cp.cp_device_error_check(dev)
+    pre = [r[0].elapsed_time(r[1]) for r in recs]
+    dec = [r[1].elapsed_time(r[2]) for r in recs]
+    total = max_over_ranks(sum(pre) + sum(dec), world)
+    out = {"workload": "tiny: 256-token fp32 prompt, GQA 8q/2kv, D 64, zigzag CP=4; decode of the "
+                       "257-token cache over 4 token-interleaved shards + LSE merge",
+           "metric": "ms per step (prefill + decode)", "unit": "ms", "higher_is_better": False,
+           "value": total / steps, "steps": steps,
+           "ms_prefill": statistics.mean(pre), "ms_decode": statistics.mean(dec),
+           "prefill_tflops": pflops / (statistics.mean(pre) / 1e3) / 1e12,
+           "decode_gbs": dbytes / (statistics.mean(dec) / 1e3) / 1e9,
+           "gpu_launches": 5 * steps, "clocks": clk,
+           "note": "launch-bound: 2.7e8 FLOP and 0.26 MB per step; no roofline is meaningful at this size"}
+    if not args.no_cpu and rank == 0:
+        sec, cores = oracle_tiny()
+        out["cpu_baseline"] = {"value": sec * 1e3, "unit": "ms", "cores": cores, "kind": "oracle",
+                               "sample": "the whole tiny workload (prefill of all 4 shards + the decode), "
+                                         "fp64 numpy"}
+    return out
+
+
+def decode_e2e(cp, args, dev, stream, world, ctx, m, dq, shards, scales, dscale, d_bytes):
+    """The decode step end to end through the binding with host buffers:
+    every step uploads the decode query from pinned host memory, builds the
+    decode plan on the host and copies it up, runs the decode and the LSE
+    merge, and reads the merged O and LSE back into pinned host memory.  The
+    copies run on two copy streams with double-buffered device buffers, so
+    step i + 1's upload and step i - 1's download overlap step i."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    B, H, Dv, C = len(ctx), m["H"], m["Dv"], m["C"]
+    qh = dq.cpu().pin_memory()
+    dqs = [torch.empty_like(dq) for _ in range(2)]
+    o_part = torch.empty((C, B, H, Dv), dtype=torch.float32, device=dev)
+    lse_part = torch.empty((C, B, H), dtype=torch.float32, device=dev)
+    outs = [(torch.empty((B, H, Dv), dtype=torch.bfloat16, device=dev),
+             torch.empty((B, H), dtype=torch.float32, device=dev)) for _ in range(2)]
+    hosts = [(torch.empty((B, H, Dv), dtype=torch.bfloat16).pin_memory(),
+              torch.empty((B, H), dtype=torch.float32).pin_memory()) for _ in range(2)]
+    probe = cp.cp_decode_plan(C, ctx, device=dev)
+    ws = torch.empty(max(16, cp.cp_decode_workspace_size(probe, H, Dv)), dtype=torch.uint8, device=dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def run(n):
+        uploaded = [ev() for _ in range(n)]
+        computed = [ev() for _ in range(n)]
+        downloaded = [ev() for _ in range(n)]
+
+        def upload(i):
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(computed[i - 2])
+                dqs[i % 2].copy_(qh, non_blocking=True)
+                uploaded[i].record(up)
+
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(uploaded[i])
+            if i >= 2:
+                stream.wait_event(downloaded[i - 2])
+            dp = cp.cp_decode_plan(C, ctx, device=dev)
+            cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dqs[i % 2], shards, shard_scale=scales,
+                              sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
+            od, ld = outs[i % 2]
+            cp.cp_lse_merge(o_part, lse_part, out=od, lse=ld)
+            computed[i].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[i])
+                hosts[i % 2][0].copy_(od, non_blocking=True)
+                hosts[i % 2][1].copy_(ld, non_blocking=True)
+                downloaded[i].record(down)
+        stream.wait_event(downloaded[n - 1])
+
+    run(3)
+    torch.cuda.synchronize(dev)
+    n = args.steps + 2
+    barrier(world)
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    clk.start()
+    a, b = ev(), ev()
+    a.record(stream)
+    run(n)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    info = clk.stop()
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    h2d = dq.numel() * dq.element_size() + probe.dev.numel() * 4
+    d2h = B * H * Dv * 2 + B * H * 4
+    return {"value": whole_job_rate(d_bytes * n, ms, world) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "clocks": info,
+            "note": "query uploaded from pinned host memory and the plan built on the host and copied "
+                    "up every step; merged O and LSE read back to pinned host memory; copies on two "
+                    "copy streams overlap the neighbouring steps (double-buffered); the KV cache "
+                    "stays resident"}
+
+
 def run_ours(args, world, rank, local):
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.ensure_built()  # rebuilds a library older than its sources
+    barrier(world)
     import context_long_attention_gb300 as cp
 
     dev = torch.device("cuda", local if world > 1 else 0)
@@ -573,8 +874,8 @@ def run_ours(args, world, rank, local):
         vh = v.cpu().pin_memory()
         oh = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
         lh = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
-        dq = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
-        do = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+        dev_in = [(torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)) for _ in range(2)]
+        dev_out = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
         up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         n_e2e = args.steps + 2
 
@@ -587,7 +888,7 @@ def run_ours(args, world, rank, local):
                 with torch.cuda.stream(up):
                     if i >= 2:
                         up.wait_event(computed[i - 2])  # buffer i % 2 is free again
-                    for d_, h_ in zip(dq[i % 2], (qh, kh, vh)):
+                    for d_, h_ in zip(dev_in[i % 2], (qh, kh, vh)):
                         d_.copy_(h_, non_blocking=True)
                     uploaded[i].record(up)
 
@@ -598,8 +899,8 @@ def run_ours(args, world, rank, local):
                 stream.wait_event(uploaded[i])
                 if i >= 2:
                     stream.wait_event(downloaded[i - 2])  # outputs i % 2 read back
-                qd, kd, vd = dq[i % 2]
-                od, ld = do[i % 2]
+                qd, kd, vd = dev_in[i % 2]
+                od, ld = dev_out[i % 2]
                 plan = cp.cp_shard_plan(cp.CP_ZIGZAG, C, nl, pl, device=dev)
                 cp.cp_prefill_attn(plan, qd, kd, vd, scale, out=od, lse=ld)
                 computed[i].record(stream)
@@ -614,12 +915,12 @@ def run_ours(args, world, rank, local):
         ca, cb, cc = ev(), ev(), ev()
         ca.record(up)
         with torch.cuda.stream(up):
-            for d_, h_ in zip(dq[0], (qh, kh, vh)):
+            for d_, h_ in zip(dev_in[0], (qh, kh, vh)):
                 d_.copy_(h_, non_blocking=True)
         cb.record(up)
         with torch.cuda.stream(up):
-            oh[0].copy_(do[0][0], non_blocking=True)
-            lh[0].copy_(do[0][1], non_blocking=True)
+            oh[0].copy_(dev_out[0][0], non_blocking=True)
+            lh[0].copy_(dev_out[0][1], non_blocking=True)
         cc.record(up)
         torch.cuda.synchronize(dev)
         h2d_bytes = q.numel() * 2 + k.numel() * 2 + v.numel() * 2
@@ -651,6 +952,28 @@ def run_ours(args, world, rank, local):
     sparse = None
     if do_dec and args.sparse_k:
         sparse = sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, world, rank)
+
+    # ---- the decode half end to end through the binding with host buffers
+    dec_e2e = None
+    default_decode = (do_dec and uniform and fp8 and not args.decode_paged and args.decode_rows == 1
+                      and args.decode_layout == "round_robin" and not args.decode_ctx
+                      and not args.decode_batch)
+    if default_decode:
+        dec_e2e = decode_e2e(cp, args, dev, stream, world, ctx, m, dq, shards, scales, dscale, d_bytes)
+
+    # ---- the other workloads, each timed on its own (the default line only)
+    legs = None
+    if args.legs and args.only == "all" and zz and default_decode and not args.sparse_k:
+        del q, k, v, o, lse, shards, scales, o_part, lse_part, o_mrg, lse_mrg, o_dec, lse_dec, ws, dq
+        if e2e is not None:
+            del qh, kh, vh, oh, lh, dev_in, dev_out
+        torch.cuda.empty_cache()
+        legs = {"tiny": leg_tiny(cp, args, dev, stream, world, rank),
+                "decode_bf16": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, "mla", False),
+                "decode_mixed": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind,
+                                           "mla_mixed", True),
+                "prefill_interleave": leg_prefill_interleave(cp, args, dev, stream, world, rank, peaks,
+                                                             peak_kind)}
 
     if rank != 0:
         return
@@ -688,6 +1011,8 @@ def run_ours(args, world, rank, local):
                                                               if gqa else "decode_" + kv_kind,
                                                               sum(ctx))),
                             "peak_kind": peak_kind}}
+        if dec_e2e is not None:
+            dec["e2e"] = dec_e2e
     cpu = None
     if not args.no_cpu:
         o_s = oracle_prefill_sample(args.prefill_workload, rows_per_call=32, budget_s=12.0)
@@ -733,6 +1058,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": args.steps * ((2 if do_pre else 0) + n_dec_kernels),
         "clocks": clock_info,
+        "legs": legs,
     }
     print(json.dumps(line), flush=True)
 
@@ -767,6 +1093,14 @@ def main():
                     help="cached tokens per request for the uniform and gqa decode workloads (0: 131072)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="requests in the decode batch (0: the workload's 64); for profiler captures")
+    ap.add_argument("--no-legs", dest="legs", action="store_false",
+                    help="skip the other workloads' legs of the default line (tiny, bf16 and mixed "
+                         "MLA decode, interleave prefill)")
+    ap.add_argument("--leg-steps", type=int, default=20, help="timed steps of the decode legs (at most --steps)")
+    ap.add_argument("--leg-steps-long", type=int, default=3,
+                    help="timed steps of the interleave prefill leg (1.3 s each; at most --steps)")
+    ap.add_argument("--cpu-budget", type=float, default=8.0,
+                    help="seconds of oracle time for each leg's CPU baseline sample")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
