@@ -26,13 +26,17 @@
 // V_codes^T is the tile's first four 128-dim chunks read as an MN-major
 // operand; P_hi^T goes over the tile's rope chunk once S^T is computed.
 //
-// Roles (320 threads): warps 0-7 softmax (thread = KV row of the tile = TMEM
+// Roles (352 threads): warps 0-7 softmax (thread = KV row of the tile = TMEM
 // lane, warps w and w + 4 taking heads 0-31 and 32-63 of the same rows; in
-// the epilogue, a dim row of O^T); warp 8 TMA producer; warp 9 MMA issuer and
-// TMEM owner.  Two tile stages in shared memory, each refilled chunk by chunk
-// as P.V's M-blocks release it, and two S^T buffers in TMEM let the next
-// tile's QK^T run while this tile's softmax works.  The issuer puts QK^T
-// first: P.V goes one M-block at a time, so a late tile waits for one block.
+// the epilogue, a dim row of O^T); warp 8 TMA producer; warp 9 P.V issuer and
+// TMEM owner; warp 10 QK^T issuer.  Issuing a tcgen05.mma holds the issuing
+// thread about as long as the product runs, so a single issuer serialises the
+// two streams behind its own waits: with one per stream the tensor pipe runs
+// the next tile's QK^T groups, which arrive chunk by chunk, while this tile's
+// P.V waits for its weights.  Two tile stages in shared memory, each refilled
+// chunk by chunk as P.V's M-blocks release it, and two S^T buffers in TMEM
+// (each released by the softmax once it has loaded the scores) let the next
+// tile's QK^T run while this tile's softmax works.
 // TMEM: S^T buffer b at columns [128 b, 128 b + 128); O^T M-block mb at
 // [256 + 64 mb, 320 + 64 mb).
 #include <cuda_bf16.h>
@@ -58,9 +62,9 @@ constexpr int kStageBytes = kRopeOff + kRows * 64; // 73,728 B
 constexpr int kQOff = 2 * kStageBytes;             // [Q_hi | Q_lo]: 128 operand rows x 576 B
 constexpr int kPloOff = kQOff + kStageBytes;       // P_lo^T: 128 rows x 64 heads
 constexpr int kSmem = kPloOff + kRows * 64 + 1024;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmax = 256;  // warps 0-7: a row's 64 heads in two halves of 32
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kWarpTma = 8, kWarpPv = 9, kWarpQk = 10;
 constexpr int kPrefetchAhead = 2;  // tiles between the L2 prefetch and the shared-memory copy
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -93,6 +97,25 @@ struct CodeMaps {
   CUtensorMap body[CP_MAX_SHARDS];
   CUtensorMap rope[CP_MAX_SHARDS];
 };
+
+// D[tmem] (+)= A . B with 8-bit operands, A read from shared memory into the
+// tensor core's A collector buffer and kept there for the next product
+// (fill), or taken from that buffer, which the next product may not use
+// again (lastuse).  Consecutive products with the same A read it once.
+__device__ __forceinline__ void mma_f8_fill_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4.collector::a::fill [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_f8_reuse_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4.collector::a::lastuse [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -205,8 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   //   P_lo^T buffer.
   // bar_s[b]: S^T buffer b holds its tile's products.  bar_p: this tile's
   // P^T is written.  bar_q: the work item's query is in shared memory.
-  __shared__ __align__(8) uint64_t bar_full[2][5], bar_done[2][4], bar_s[2];
-  __shared__ __align__(8) uint64_t bar_p, bar_q, bar_drain;
+  __shared__ __align__(8) uint64_t bar_full[2][5], bar_done[2][4], bar_s[2], bar_sfree[2];
+  __shared__ __align__(8) uint64_t bar_p, bar_q, bar_drain, bar_drain_qk;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
@@ -221,15 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 5; ++q) mbar_init(smem_u32(&bar_full[s][q]), 1);
       for (int mb = 0; mb < 4; ++mb) mbar_init(smem_u32(&bar_done[s][mb]), 1);
       mbar_init(smem_u32(&bar_s[s]), 1);
+      mbar_init(smem_u32(&bar_sfree[s]), kSoftmax);
     }
     mbar_init(smem_u32(&bar_p), kSoftmax);
     mbar_init(smem_u32(&bar_q), kSoftmax);
     mbar_init(smem_u32(&bar_drain), 1);
+    mbar_init(smem_u32(&bar_drain_qk), 1);
     abort_flag = 0;
     zero_flag = 0;
     mbar_init_fence();
   }
-  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 512);
+  if (warp == kWarpPv) tmem_alloc(smem_u32(&tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -307,75 +332,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < last_n[s]; ++q)
           mbar_wait(smem_u32(&bar_full[s][q]), (last_g[s] >> 1) & 1, 1000000000ull, &zero_flag);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop, so that descriptors and loop state stay
-    // warp-uniform; one elected lane (lane 0, the same one every time, which
-    // also commits) issues the products.  Barrier results are made uniform by
-    // a vote before they steer the loop.
+  } else if (warp == kWarpQk) {
+    // ------------------------------------------------------------ QK^T issuer
+    // Issuing a tcgen05.mma holds the issuing thread for about as long as the
+    // product runs, so one thread cannot run ahead of the tensor pipe: QK^T and
+    // P.V each have an issuing warp, and the pipe interleaves the two streams
+    // (the next tile's QK^T groups, which arrive chunk by chunk, fill the pipe
+    // while this tile's P.V waits for its weights).  The whole warp runs the
+    // loop so that descriptors and loop state stay warp-uniform; one elected
+    // lane issues and commits.
     {
-      constexpr unsigned kAll = 0xffffffffu;
       const uint32_t idQK = idesc_e4m3_f32(kRows, 2 * kHeads, 0, 0);
-      const uint32_t idPV = idesc_e4m3_f32(kRows, kHeads, 1, 1);
       // Descriptors are built once; an MMA adds its byte offset / 16 to the
       // start-address field (shared addresses stay below 2^18, so it never carries).
       const uint32_t st0 = sbase, st1 = sbase + kStageBytes;
       const uint64_t dK[2] = {smem_desc(st0, 16, 1024, 2), smem_desc(st1, 16, 1024, 2)};
       const uint64_t dKr[2] = {smem_desc(st0 + kRopeOff, 16, 512, 4),
                                smem_desc(st1 + kRopeOff, 16, 512, 4)};
-      const uint64_t dV[2] = {smem_desc(st0, kChunkBytes, 1024, 2),
-                              smem_desc(st1, kChunkBytes, 1024, 2)};
       const uint64_t dQ = smem_desc(sbase + kQOff, 16, 1024, 2);
       const uint64_t dQr = smem_desc(sbase + kQOff + kRopeOff, 16, 512, 4);
-      const uint64_t dPlo = smem_desc(sbase + kPloOff, 16, 512, 4);
-      auto full_bar = [&](int gq, int q) { return smem_u32(&bar_full[gq & 1][q]); };
       auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        return __all_sync(kAll, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
-      };
-      auto test_any = [&](uint32_t bar, uint32_t parity) {
-        return __any_sync(kAll, mbar_test(bar, parity));
-      };
-      // S^T(gq) += K_codes . [Q_hi | Q_lo]^T over chunk group q
-      auto qk_group = [&](int gq, int q) {
-        const int s = gq & 1;
-        const uint32_t d = tmem + 128 * s;
-        tc_fence_after();
-        if (q < 4) {
-          const uint64_t a = (s ? dK[1] : dK[0]) + (uint64_t)((q * kChunkBytes) >> 4);
-          const uint64_t b = dQ + (uint64_t)((q * kChunkBytes) >> 4);
-          if (elect_one()) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ss_f8(d, a + 2 * ks, b + 2 * ks, idQK, (q | ks) != 0 ? 1u : 0u);
-          }
-        } else {
-          const uint64_t a = s ? dKr[1] : dKr[0];
-          if (elect_one()) {
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) mma_ss_f8(d, a + 2 * ks, dQr + 2 * ks, idQK, 1u);
-            mma_commit(smem_u32(&bar_s[s]));
-          }
-        }
-        __syncwarp();
-      };
-      // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T); each block's commit
-      // releases its chunk of the stage (block 3's also the rope chunk and
-      // P_lo^T's buffer).
-      auto pv_block = [&](int gp, int mb, bool first) {
-        const int s = gp & 1;
-        const uint64_t av = (s ? dV[1] : dV[0]) + (uint64_t)((mb * kChunkBytes) >> 4);
-        const uint64_t bh = s ? dKr[1] : dKr[0];  // P_hi^T over the rope chunk
-        const uint32_t d = tmem + 256 + 64 * mb;
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kRows / 32; ++kk) {
-            const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
-            mma_ss_f8(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || !first) ? 1u : 0u);
-            mma_ss_f8(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
-          }
-          mma_commit(smem_u32(&bar_done[s][mb]));
-        }
-        __syncwarp();
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
       };
       bool ok = true;
       int g = 0, nq = 0;  // tiles and query loads so far
@@ -392,51 +369,93 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nq;
           q_b = it.b;
         }
-        int done = 0;  // chunk groups of QK^T(g) already issued
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
-          for (; done < 5; ++done) {
-            if (!wait_all(full_bar(g, done), (g >> 1) & 1)) {
+          const int s = g & 1;
+          const uint32_t d = tmem + 128 * s;
+          // S^T buffer s is free once the softmax has loaded tile g - 2's scores
+          if (g >= 2 && !wait_all(smem_u32(&bar_sfree[s]), ((g >> 1) & 1) ^ 1)) {
+            if (lane == 0) report_timeout(p.status, 9, &abort_flag);
+            ok = false;
+            break;
+          }
+          // S^T(g) = K_codes . [Q_hi | Q_lo]^T, chunk group by chunk group as the codes land
+          for (int q = 0; q < 5; ++q) {
+            if (!wait_all(smem_u32(&bar_full[s][q]), (g >> 1) & 1)) {
               if (lane == 0) report_timeout(p.status, 3, &abort_flag);
               ok = false;
               break;
             }
-            qk_group(g, done);
+            tc_fence_after();
+            if (q < 4) {
+              const uint64_t a = (s ? dK[1] : dK[0]) + (uint64_t)((q * kChunkBytes) >> 4);
+              const uint64_t b = dQ + (uint64_t)((q * kChunkBytes) >> 4);
+              if (elect_one()) {
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                  mma_ss_f8(d, a + 2 * ks, b + 2 * ks, idQK, (q | ks) != 0 ? 1u : 0u);
+              }
+            } else {
+              const uint64_t a = s ? dKr[1] : dKr[0];
+              if (elect_one()) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) mma_ss_f8(d, a + 2 * ks, dQr + 2 * ks, idQK, 1u);
+                mma_commit(smem_u32(&bar_s[s]));
+              }
+            }
+            __syncwarp();
           }
-          if (!ok) break;
-          // Next tile's QK^T groups go first, as their codes land (its S^T buffer
-          // was read before P(g - 1) arrived); P.V(g) M-block by M-block once P(g)
-          // is written, so a late QK^T waits behind one block at most.
-          const bool more = j + 1 < it.ntiles;
-          int next = 0, mb = 0;
-          bool p_ready = false;
-          const uint64_t t0 = global_timer_ns();
-          for (uint32_t spin = 1; mb < 4; ++spin) {
-            if (more && next < 5 && test_any(full_bar(g + 1, next), ((g + 1) >> 1) & 1)) {
-              qk_group(g + 1, next++);
-              continue;
-            }
-            if (!p_ready && test_any(smem_u32(&bar_p), g & 1)) {
-              p_ready = true;
-              tc_fence_after();
-            }
-            if (p_ready) {
-              pv_block(g, mb, j == 0);
-              ++mb;
-              continue;
-            }
-            if ((spin & 255u) == 0 &&
-                __any_sync(kAll, abort_flag || global_timer_ns() - t0 > p.wait_ns))
-              break;
-          }
-          if (mb < 4) {
+        }
+      }
+      // Never free TMEM under a running MMA.
+      if (elect_one()) mma_commit(smem_u32(&bar_drain_qk));
+      __syncwarp();
+      mbar_wait(smem_u32(&bar_drain_qk), 0, 1000000000ull, &zero_flag);
+    }
+  } else if (warp == kWarpPv) {
+    // ------------------------------------------------------------ P.V issuer and TMEM owner
+    // O^T[M-block mb] (+)= V_codes^T . (P_hi^T + P_lo^T): the hi and lo
+    // products of a K-step read the same A (a 128-dim x 32-row block of
+    // V_codes^T), which the second one takes from the tensor core's A
+    // collector buffer instead of shared memory.  Each block's commit releases
+    // its chunk of the stage (block 3's also the rope chunk and P_lo^T's buffer).
+    {
+      const uint32_t idPV = idesc_e4m3_f32(kRows, kHeads, 1, 1);
+      const uint32_t st0 = sbase, st1 = sbase + kStageBytes;
+      const uint64_t dPhi[2] = {smem_desc(st0 + kRopeOff, 16, 512, 4),  // P_hi^T over the rope chunk
+                                smem_desc(st1 + kRopeOff, 16, 512, 4)};
+      const uint64_t dV[2] = {smem_desc(st0, kChunkBytes, 1024, 2),
+                              smem_desc(st1, kChunkBytes, 1024, 2)};
+      const uint64_t dPlo = smem_desc(sbase + kPloOff, 16, 512, 4);
+      bool ok = true;
+      int g = 0;
+      for (int wi = w0; wi < w1 && ok; ++wi) {
+        const Item it = read_item(p, wi);
+        for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
+          const int s = g & 1;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p), g & 1, p.wait_ns, &abort_flag))) {
             if (lane == 0) report_timeout(p.status, 4, &abort_flag);
             ok = false;
             break;
           }
-          done = next;
+          tc_fence_after();
+#pragma unroll 1
+          for (int mb = 0; mb < 4; ++mb) {
+            const uint64_t av = (s ? dV[1] : dV[0]) + (uint64_t)((mb * kChunkBytes) >> 4);
+            const uint64_t bh = s ? dPhi[1] : dPhi[0];
+            const uint32_t d = tmem + 256 + 64 * mb;
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kRows / 32; ++kk) {
+                const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
+                mma_f8_fill_a(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || j > 0) ? 1u : 0u);
+                mma_f8_reuse_a(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
+              }
+              mma_commit(smem_u32(&bar_done[s][mb]));
+            }
+            __syncwarp();
+          }
         }
       }
-      // Never free TMEM under a running MMA.
       if (elect_one()) mma_commit(smem_u32(&bar_drain));
       __syncwarp();
       mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
@@ -588,6 +607,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // the scores are in registers: the QK^T issuer may refill this S^T buffer
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_sfree[b]));
         // Block-wide vote: the item's first tile, a score past its running max by
         // more than 2^3, or a token scale that would take a weight to 2^8 or more.
         const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
@@ -735,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+  if (warp == kWarpPv) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
