@@ -50,8 +50,8 @@ PROFILED_TRAFFIC = {
                 "sha1": "df3c47221f9a4778217bee17d5d95d14f5eea68b", "bytes": 2.373758e9 + 0.275600e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "6861272f9604b5957ab957f1a61cbad8e4a08a2b",
-                   "bytes_per_token": (0.623026e9 + 0.010095e9) / (8 * 131072)},
+                   "sha1": "8a956f900500e87b6853cccde1bb8bbb3839ab88",
+                   "bytes_per_token": (0.610018e9 + 0.009791e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "04100416602e6fe976f64f3844df844162af152b",

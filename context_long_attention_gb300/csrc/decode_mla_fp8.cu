@@ -62,10 +62,13 @@ constexpr int kStageBytes = kRopeOff + kRows * 64; // 73,728 B
 constexpr int kQOff = 2 * kStageBytes;             // [Q_hi | Q_lo]: 128 operand rows x 576 B
 constexpr int kPloOff = kQOff + kStageBytes;       // P_lo^T: 128 rows x 64 heads
 constexpr int kSmem = kPloOff + kRows * 64 + 1024;
-constexpr int kThreads = 352;
-constexpr int kSoftmax = 256;  // warps 0-7: a row's 64 heads in two halves of 32
-constexpr int kWarpTma = 8, kWarpPv = 9, kWarpQk = 10;
-constexpr int kPrefetchAhead = 2;  // tiles between the L2 prefetch and the shared-memory copy
+constexpr int kSoftmaxWarps = 8;  // a row's 64 heads in two groups of 32
+constexpr int kSoftmax = 32 * kSoftmaxWarps;
+constexpr int kHpw = kHeads / (kSoftmaxWarps / 4);  // heads per softmax warp
+static_assert(kHpw % 16 == 0, "a softmax warp takes whole 16-head TMEM loads");
+constexpr int kWarpTma = kSoftmaxWarps, kWarpPv = kSoftmaxWarps + 1, kWarpQk = kSoftmaxWarps + 2;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
+constexpr int kPrefetchAhead = 1;  // tiles between the L2 prefetch and the shared-memory copy
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 3.0f;  // the running max moves when a score passes it by > 2^3
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float sM[kHeads];  // running max per head (log2 units)
   __shared__ float sDelta[kHeads];            // its last move; in the epilogue 1 / column sum
   __shared__ int sRed[4][kHeads];             // per row-quarter column maxima, then column sums
-  __shared__ uint32_t sRed1[8];               // per-warp max of |q| or of the token scales
+  __shared__ uint32_t sRed1[kSoftmaxWarps];   // per-warp max of |q| or of the token scales
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -461,11 +464,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
+    // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;          // TMEM lane quarter: tile rows [32 quarter, +32)
-    const int hb = (warp >> 2) * 32;       // this warp's heads [hb, hb + 32)
+    const int hb = (warp >> 2) * kHpw;     // this warp's heads [hb, hb + kHpw)
     const int t = quarter * 32 + lane;     // tile row = TMEM lane; in the epilogue a dim row
-    const int tid = threadIdx.x;           // 0 .. 255
+    const int tid = threadIdx.x;           // 0 .. kSoftmax - 1
     const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* sQ = smem + kQOff;
     uint8_t* sPlo = smem + kPloOff;
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kPieces = kDqk / 8;                   // 16-byte pieces per head
         constexpr int kPer = kHeads * kPieces / kSoftmax;   // pieces per thread
         static_assert(kHeads * kPieces % kSoftmax == 0, "query pieces split evenly");
-        constexpr int kBatch = 6;  // pieces in flight at once per thread
+        constexpr int kBatch = kPer % 6 == 0 ? 6 : 3;  // pieces in flight at once per thread
         static_assert(kPer % kBatch == 0, "whole batches of pieces");
         // a batch of this thread's pieces (heads past H are zero)
         auto load_batch = [&](int k0, uint4* qv) {
@@ -516,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) sRed1[warp] = qmax;
         named_bar_sync(1, kSoftmax);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) qmax = max(qmax, sRed1[w]);
+        for (int w = 0; w < kSoftmaxWarps; ++w) qmax = max(qmax, sRed1[w]);
         eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
         const float qs = pow2i(eq);
 #pragma unroll 1
@@ -560,9 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* srow = p.sc.p[it.r] + it.row0;
       const float cq = p.scale_log2 * pow2i(-eq);
       int gs = 0;  // weights carry scale_row 2^gs (set on the item's first tile, only decreases)
-      float l[32];
+      float l[kHpw];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) l[h] = 0.f;
+      for (int h = 0; h < kHpw; ++h) l[h] = 0.f;
       for (int j = 0; j < it.ntiles; ++j, ++g) {
         const int row = j * kRows + t;
         const bool valid = row < it.nrows;
@@ -575,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : p.rm.table ? __ldg(p.sc.p[0] + map_row(p.rm, it.pair, 0, it.row_begin + row))
                                 : __ldg(srow + row);
         const int b = g & 1;
-        // The eight warps leave together: one that gave up meets the others at this vote.
+        // The softmax warps leave together: one that gave up meets the others at this vote.
         const bool got = __all_sync(
             0xffffffffu, mbar_wait(smem_u32(&bar_s[b]), (g >> 1) & 1, p.wait_ns, &abort_flag));
         if (bar_red_or(1, kSoftmax, !got)) {
@@ -586,22 +589,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // u = score - running max (log2 units); rows past the item read nothing
         const float c = scale * cq;
-        float u[32];
+        float u[kHpw];
         float over = -INFINITY;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {  // 16 heads at a time keeps registers low
-          uint32_t a[16], z[16];
-          tmem_ld16(lane_addr + 128 * b + hb + 16 * half, a);
-          tmem_ld16(lane_addr + 128 * b + kHeads + hb + 16 * half, z);
+        {  // one wait for all of the row's scores (the loads are slow while P.V runs)
+          static_assert(kHpw == 32, "the score load takes 32 heads");
+          uint32_t a[32], z[32];
+          tmem_ld32(lane_addr + 128 * b + hb, a);
+          tmem_ld32(lane_addr + 128 * b + kHeads + hb, z);
           tmem_ld_wait();
 #pragma unroll
-          for (int h4 = 0; h4 < 4; ++h4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 16 * half + 4 * h4]);
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 4 * h4]);
             const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int h = 16 * half + 4 * h4 + e;
-              u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[4 * h4 + e]) + __uint_as_float(z[4 * h4 + e]), c, -mm[e])
+              const int h = 4 * h4 + e;
+              u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[h]) + __uint_as_float(z[h]), c, -mm[e])
                            : -INFINITY;
               over = fmaxf(over, u[h]);
             }
@@ -615,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
         if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2 || big)) {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
+          for (int h = 0; h < kHpw; ++h) {
             const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
             if (lane == 0) sRed[quarter][hb + h] = m;
           }
@@ -624,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1, kSoftmax);
           uint32_t smb = 0;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) smb = max(smb, sRed1[w]);
+          for (int w = 0; w < kSoftmaxWarps; ++w) smb = max(smb, sRed1[w]);
           const float smax = __uint_as_float(smb);
           const int gs_new = j == 0 ? scale_exponent(smax, kWeightTop, 0)
                                     : min(gs, scale_exponent(smax, kWeightTop, gs));
@@ -640,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1, kSoftmax);
           const float gf = pow2i(max(gs_new - gs, -126));
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
+          for (int h = 0; h < kHpw; ++h) {
             const float dl = sDelta[hb + h];
             u[h] -= dl;
             l[h] *= ex2(-dl);
@@ -657,8 +660,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             // column h of O^T becomes O^T 2^-delta_h 2^(gs_new - gs)
 #pragma unroll 1
-            for (int c = 0; c < 2 * (kDv / 128); ++c) {
-              const int mb = c >> 1, h0 = 16 * (c & 1);
+            for (int c = 0; c < (kHpw / 16) * (kDv / 128); ++c) {
+              const int mb = c / (kHpw / 16), h0 = 16 * (c % (kHpw / 16));
               uint32_t a[16];
               tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
               tmem_ld_wait();
@@ -671,11 +674,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           gs = gs_new;
         }
-        // P^T row t, heads [hb, hb + 32): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
+        // P^T row t, heads [hb, hb + kHpw): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
         const float gr = scale * pow2i(gs);
-        uint32_t hw[8], lw[8];
+        uint32_t hw[kHpw / 4], lw[kHpw / 4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kHpw / 4; ++k) {
           float pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -702,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rope chunk of this tile's stage (QK^T(g) has read it)
         uint8_t* phi = smem + b * kStageBytes + kRopeOff;
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < kHpw / 16; ++k) {
           *reinterpret_cast<uint4*>(phi + sw64(t, hb + 16 * k)) =
               make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
           *reinterpret_cast<uint4*>(sPlo + sw64(t, hb + 16 * k)) =
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
+      for (int h = 0; h < kHpw; ++h) {
         float v = l[h];
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -739,13 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1, kSoftmax);
       const float og = pow2i(-gs);
 #pragma unroll 1
-      for (int mb = 0; mb < kDv / 128; ++mb) {
-        uint32_t a[32];
-        tmem_ld32(lane_addr + 256 + 64 * mb + hb, a);
+      for (int c = 0; c < (kHpw / 16) * (kDv / 128); ++c) {
+        const int mb = c / (kHpw / 16), h0 = 16 * (c % (kHpw / 16));
+        uint32_t a[16];
+        tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
         tmem_ld_wait();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          const int hh = hb + h;
+        for (int h = 0; h < 16; ++h) {
+          const int hh = hb + h0 + h;
           if (hh < p.H)
             it.out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * og * sDelta[hh];
         }
