@@ -1,5 +1,5 @@
-// GQA split-KV decode over an FP8-E4M3 cache (head dim 128) on the tcgen05
-// tensor cores.
+// GQA split-KV decode over an FP8-E4M3 cache (head dim 128) on FP8 tensor-core
+// products.
 //
 // The same computation as the bf16 GQA kernel ("How GPUs Share a Long
 // Context During LLM Inference" §3.1-3.4): per work item (a row range of one
@@ -8,22 +8,35 @@
 // (§3.3).  The cache holds E4M3 codes with one fp32 scale per token for both
 // its K and V rows (k = code x scale, v = code x scale).
 //
-// Every E4M3 value is exactly an f16 value, so the codes are expanded to f16
-// in shared memory by six converter warps and the products run as kind::f16
-// with f16 operands:
-//   S^T [128 rows x NP]  = K_codes_g [128 x 128] . (Q_g 2^e)^T, scaled per row
-//                           by scale_row 2^-e in the softmax,
-//   O^T [128 dims x NP] += V_codes_g^T . (P scale_row)^T,
-// the running sum counting the unscaled weights, so O = sum p v / sum p.
-// The query of a unit (request, kv head) is scaled by a power of two 2^e that
-// puts its largest magnitude in [2^13, 2^14), so its bf16 values are exact in
-// f16.
+// The codes go from HBM to shared memory by TMA as stored and feed
+// kind::f8f6f4 products directly, as in the FP8 MLA decode: the bf16 query and
+// the softmax weights are carried as pairs hi + lo of E4M3 numbers (hi = x
+// rounded to E4M3, lo = the remainder rounded to E4M3; 8 significant bits for
+// |x| >= 2^-2, absolute error <= 2^-10 below):
+//   query:   x = q 2^e_q, e_q per unit so that max |x| is in [128, 256)
+//   weights: x = 2^(s - M_n) scale_row 2^gs, gs per unit so that
+//            scale_row 2^gs < 32; the running max of a column moves when a
+//            score passes it by more than 2^3, so x < 256
+// The products, transposed so that M = 128 KV rows, with the unit's
+// n = qi G + i query columns padded to NP (16 or 32):
+//   S^T [128 rows x 2 NP] = K_codes_g [128 x 128] . [Q_hi | Q_lo]^T
+//     score(row, n) = (S^T[row][n] + S^T[row][NP + n]) scale_row 2^-e_q
+//   O^T [128 dims x NP]  += V_codes_g^T [128 x 128 rows] . (P_hi^T + P_lo^T)
+// The hi and lo products of a K-step share A (a 128-dim x 32-row block of
+// V_codes^T), which the second takes from the tensor core's A collector.
 //
-// Warp roles (384 threads): warps 0-3 softmax (thread = KV row of the tile =
-// TMEM lane; in the epilogue a dim row of O^T), warp 4 TMA (codes into two
-// staging slots), warp 5 MMA issue (one elected lane, the loop run
-// warp-wide), warps 6-11 expand the codes into two f16 stages and convert
-// each unit's query; two S^T buffers in TMEM.
+// Warp roles (352 threads): warps 0-7 softmax in two streams, warps 0-3 the
+// tiles with even g and warps 4-7 those with odd g (thread = KV row of the
+// tile = TMEM lane; in a unit's epilogue a dim row of O^T); warp 8 TMA (the K
+// and V codes of a tile into one of six 32 KB slots); warp 9 QK^T issue;
+// warp 10 P.V issue and TMEM owner.  Issuing a tcgen05.mma holds the issuing
+// thread about as long as the product runs, so each product stream has its
+// own issuing warp (one elected lane, the loop run warp-wide) and the tensor
+// pipe interleaves them.  A softmax stream has its own S^T buffer, P buffer,
+// O^T accumulator and running max, sum and weight exponent: loading a tile's
+// scores from TMEM takes ~900 clk while products run, and one stream's loads
+// overlap the other's exponentials.  The unit's epilogue merges the two
+// streams' (O, max, sum) exactly, as the LSE merge would.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -40,34 +53,40 @@ using namespace tc;
 constexpr int kRows = 128;                  // KV rows per tile (MMA M)
 constexpr int kD = 128;                     // head dim
 constexpr int kCodeBytes = kRows * kD;      // E4M3 K or V tile of one kv head: 16 KB
-constexpr int kSlotBytes = 2 * kCodeBytes;  // a staging slot: K and V codes, 32 KB
-constexpr int kChunkBytes = kRows * 128;    // 64 dims of an f16 tile: 16 KB
-constexpr int kTileBytes = 2 * kChunkBytes; // f16 K or V tile: 32 KB
-constexpr int kStageBytes = 2 * kTileBytes; // f16 K and V: 64 KB
-constexpr int kSlots = 2, kStages = 2;
-constexpr int kThreads = 384;
-constexpr int kSoftmax = 128;
-constexpr int kConvWarps = 6;
-constexpr int kConv = kConvWarps * 32;  // converter threads (warps 6-11: three SM sub-partitions hold
-                                        // three warps, the register cap of 168 a thread either way)
-constexpr int kWarpTma = 4, kWarpMma = 5, kWarpConv0 = 6;
+constexpr int kSlotBytes = 2 * kCodeBytes;  // a slot: the tile's K and V codes
+constexpr int kSlots = 6;
+constexpr int kSoftmaxWarps = 8;  // two streams (even and odd tiles) of four TMEM lane quarters
+constexpr int kSoftmax = 32 * kSoftmaxWarps;
+constexpr int kWarpTma = kSoftmaxWarps, kWarpQk = kSoftmaxWarps + 1, kWarpPv = kSoftmaxWarps + 2;
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleLog2 = 3.0f;  // the running max moves when a score passes it by > 2^3
+constexpr int kWeightTop = 5;         // scale_row 2^gs < 2^5, so a weight 2^(s - M) scale_row 2^gs < 2^8
+constexpr int kTmemCols = 256;
 
+// Shared memory: the slots, the unit's query operand [Q_hi | Q_lo] (2 NP rows
+// x 128 B, K-major, 128-byte swizzle), two P buffers [P_hi | P_lo] (each NP
+// rows x 128 B, K-major: row n holds column n's weights of the tile's 128 KV
+// rows).
 template <int NP>
-constexpr int smem_bytes() {
-  return kSlots * kSlotBytes + kStages * kStageBytes + NP * 256 /* Q */ + NP * 256 /* P */ + 1024;
-}
+struct Geo {
+  static constexpr int kQOff = kSlots * kSlotBytes;
+  static constexpr int kQBytes = 2 * NP * 128;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kPBytes = 2 * NP * 128;  // one buffer: hi then lo
+  static constexpr int kSmem = kPOff + 2 * kPBytes + 1024;
+};
 
 struct Params {
   const int32_t* plan;
   int B, off_pair, off_worker, off_work;
-  int Hq, Hkv, G;    // query heads, kv heads, query heads per kv head
-  int s_q;           // query rows per request
-  int Hc;            // output columns per request: s_q x Hq
-  float scale_log2;  // sm_scale * log2(e)
-  ScalePtrs sc;      // per-row scales of each shard
+  const __nv_bfloat16* q;  // [B][s_q][Hq][128]
+  int Hq, Hkv, G;          // query heads, kv heads, query heads per kv head
+  int s_q;                 // query rows per request
+  int Hc;                  // output columns per request: s_q x Hq
+  float scale_log2;        // sm_scale * log2(e)
+  ScalePtrs sc;            // per-row scales of each shard
   float* o_part;
   float* lse_part;
   float* ws_o;
@@ -101,7 +120,51 @@ __device__ __forceinline__ int ordered(float f) {
 __device__ __forceinline__ float unordered(int b) {
   return __int_as_float(b >= 0 ? b : b ^ 0x7FFFFFFF);
 }
-__device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
+// 2^e for integer e in [-126, 127], exactly.
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+// Byte offset of (row, byte) in a 128-byte-swizzled [rows][128 B] block.
+__device__ __forceinline__ int sw128(int row, int byte) {
+  return row * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15);
+}
+// D[tmem] (+)= A . B with 8-bit operands, A read from shared memory into the
+// tensor core's A collector buffer and kept for the next product (fill), or
+// taken from that buffer, which the next product may not use again (lastuse).
+__device__ __forceinline__ void mma_f8_fill_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4.collector::a::fill [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_f8_reuse_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4.collector::a::lastuse [%0], %1, %2, %3, p;\n}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+// Two values -> E4M3 pairs (hi, lo) with hi + lo ~ (x0, x1); byte 0 holds x0's code.
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint16_t a, b, h, l;
+  uint32_t xh, back, rem;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(a) : "f"(x0));
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(b) : "f"(x1));
+  asm("mov.b32 %0, {%1, %2};" : "=r"(xh) : "h"(a), "h"(b));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(h) : "r"(xh));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(h));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rem) : "r"(xh), "r"(back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(rem));
+  hi = h;
+  lo = l;
+}
+// Exponent that maps the largest |x| of a set into [2^(top-1), 2^top).
+__device__ __forceinline__ int scale_exponent(float maxabs, int top, int fallback) {
+  if (!(maxabs > 0.f)) return fallback;
+  const int E = (__float_as_int(maxabs) >> 23) & 0xFF;
+  const int e = E == 0 ? -126 : E - 126;
+  return max(-120, min(120, top - e));
+}
+__device__ void report_timeout(unsigned* status, unsigned site, volatile int* abort) {
   *abort = 1;
   if (atomicCAS(status, 0u, 1u) == 0u) {
     status[1] = kKernDecodeGqaF8;
@@ -110,29 +173,6 @@ __device__ __forceinline__ void report_timeout(unsigned* status, unsigned site, 
     __threadfence();
   }
 }
-// Two E4M3 codes of a word (bytes `lo` and `lo + 1`) to f16x2 holding the
-// codes' values x 2^-8, exactly: an E4M3 code's sign, 4 exponent bits and 3
-// mantissa bits, moved to the f16 sign, the low 4 exponent bits and the top 3
-// mantissa bits, read as f16 with bias 15 instead of 7, give its value x 2^-8,
-// subnormals included (both formats scale their subnormals the same way).
-// Integer ALU work only: the 16-bit conversion instructions, issued at this
-// rate, slow the tensor pipe.  Codes must be finite (0x7F, 0xFF are NaN).
-template <int lo>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t word) {
-  const uint32_t t = __byte_perm(word, 0u, lo == 0 ? 0x1404u : 0x3424u);  // codes into bytes 1 and 3
-  return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
-}
-// Two E4M3 codes of a word (bytes `lo` and `lo + 1`) to f16x2 by the hardware
-// conversion: the codes' values exactly.  Fewer instructions than the integer
-// form, and the converter warps are issue-bound, so this is the one used.
-template <int lo>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_hw(uint32_t word) {
-  uint32_t r;
-  const uint32_t two = lo == 0 ? (word & 0xFFFFu) : (word >> 16);
-  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}" : "=r"(r) : "r"(two));
-  return r;
-}
-constexpr float kCodeScale = 1.f;  // the f16 tiles hold the codes' values x 1 / kCodeScale
 
 // The fields of one work item that every role reads.
 struct Item {
@@ -140,7 +180,6 @@ struct Item {
   long long row0;  // first shard row
   cp_pair_desc pd;
 };
-
 __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   const cp_pair_desc* pairs = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair);
   const cp_work_desc* work = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work);
@@ -159,7 +198,6 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   it.row0 = (long long)it.pd.row_off + wd.row_begin;
   return it;
 }
-
 __device__ __forceinline__ float* out_rows(const Params& p, const Item& it) {
   return it.part < 0 ? p.o_part + (long long)it.pair * p.Hc * kD : p.ws_o + (long long)it.part * p.Hc * kD;
 }
@@ -167,325 +205,228 @@ __device__ __forceinline__ float* out_lse(const Params& p, const Item& it) {
   return it.part < 0 ? p.lse_part + (long long)it.pair * p.Hc : p.ws_lse + (long long)it.part * p.Hc;
 }
 
-template <int NP>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&a)[NP]) {
-  if constexpr (NP == 16) {
-    tmem_ld16(addr, a);
-  } else {
-    tmem_ld32(addr, a);
-  }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
 }
-template <int NP>
-__device__ __forceinline__ void tmem_st_cols(uint32_t addr, uint32_t (&a)[NP]) {
-#pragma unroll
-  for (int c = 0; c < NP / 16; ++c) tmem_st16(addr + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&a[16 * c]));
-}
-
-// A unit (work item, kv head) covers the item's tiles; g counts tiles over
-// all units of this CTA in the order every role walks them; each barrier
-// completes once per tile (per slot or stage use; bar_s[b] once per two
-// tiles; bar_q and bar_qf once per unit), so the parity to wait for follows
-// from g.
+// A unit (work item, kv head) covers the item's tiles; g counts tiles over all
+// units of this CTA in the order every role walks them, so the parity of
+// each barrier's wait follows from g (slot barriers complete once per use of
+// their slot, S^T and P buffer barriers once per use of their buffer, bar_q
+// once per unit).
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_gqa_f8_kernel(const __grid_constant__ CodeMaps maps, const __grid_constant__ CUtensorMap qmap,
-                         const Params p) {
+    decode_gqa_f8_kernel(const __grid_constant__ CodeMaps maps, const Params p) {
+  using Gm = Geo<NP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sSlot = smem;                            // [slot][K codes 16 KB | V codes 16 KB]
-  uint8_t* sStage = smem + kSlots * kSlotBytes;     // [stage][K f16: 2 chunks | V f16: 2 chunks]
-  uint8_t* sQ = sStage + kStages * kStageBytes;     // [2 chunks][NP rows x 128 B]: the unit's query
-  uint8_t* sP = sQ + NP * 256;                      // [2 chunks of 64 rows][NP rows x 128 B]
-  // code[s]: slot s holds its tile's codes; codefree[s]: the converters read them.
-  // full[s]: f16 stage s holds its tile; empty[s]: the tile's products read it.
-  // s[b]: S^T buffer b holds the scores; p: the four softmax warps wrote P;
-  // pv: the tile's P.V has completed; q: the unit's bf16 query landed in sQ;
-  // qf: the converters rewrote it as f16 (x 2^e), for the issuer; qe[u % 4]:
-  // unit u's exponent is in sQe[u % 4], for the softmax, which may be two
-  // units behind the converters (a unit's query load waits for the P.V of the
-  // tile two before it, which waits for that tile's softmax), so one barrier
-  // for it would let its phase run two ahead of the wait.
-  __shared__ __align__(8) uint64_t bar_code[kSlots], bar_codefree[kSlots], bar_fullK[kStages], bar_fullV[kStages],
-      bar_empty[kStages], bar_s[2], bar_p, bar_pv, bar_q, bar_qf, bar_qe[4], bar_drain;
+  uint8_t* sQ = smem + Gm::kQOff;
+  uint8_t* sP = smem + Gm::kPOff;
+  // full[s]: slot s holds its tile's codes; empty[s]: the P.V of the slot's
+  // tile has completed (and with it the QK^T before it), so the slot, the P
+  // buffer of that tile and O^T's earlier columns are free.
+  // s[b]: S^T buffer b holds its tile's scores; sfree[b]: the softmax loaded them.
+  // p[b]: P buffer b holds its tile's weights.  q: the unit's query operand is written.
+  __shared__ __align__(8) uint64_t bar_full[kSlots], bar_empty[kSlots], bar_s[2], bar_sfree[2], bar_p[2];
+  __shared__ __align__(8) uint64_t bar_q, bar_drain_qk, bar_drain_pv;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ volatile int zero_flag;
-  __shared__ float sM[NP];      // running max per column (log2 units)
-  __shared__ float sAlpha[NP];  // rescale of a moved max; in the epilogue 1 / column sum
-  __shared__ float sDelta[NP];
-  __shared__ int sRed[4][NP];   // cross-warp column maxima
-  __shared__ float sL[4][NP];   // cross-warp column sums
-  __shared__ int sCol[NP];      // output column of unit column n for kv head 0
-  __shared__ uint32_t sQmax[kConvWarps];  // the converter warps' largest |q| (bf16 magnitude bits)
-  __shared__ int sQe[4];        // unit u's query exponent e, at u % 4
+  __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
+  __shared__ float sM[2][NP];       // each stream's running max per column (log2 units)
+  __shared__ float sDelta[2][NP];   // its last move
+  __shared__ int sRed[2][4][NP];    // each stream's cross-warp column maxima, then column sums
+  __shared__ uint32_t sRed1[2][4];  // each stream's per-warp max of the token scales
+  __shared__ uint32_t sQmax[kSoftmaxWarps];  // per-warp max of |q|
+  __shared__ float sCoef[2][NP];    // epilogue: each stream's factor to the common max, / sum
+  __shared__ int sGs[2];            // epilogue: each stream's weight exponent
+  __shared__ int sCol[NP];       // output column of unit column n for kv head 0
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(smem_u32(&bar_code[s]), 1);
-      mbar_init(smem_u32(&bar_codefree[s]), kConv);
-    }
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_fullK[s]), kConv);
-      mbar_init(smem_u32(&bar_fullV[s]), kConv);
+      mbar_init(smem_u32(&bar_full[s]), 1);
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bar_s[0]), 1);
-    mbar_init(smem_u32(&bar_s[1]), 1);
-    mbar_init(smem_u32(&bar_p), 4);
-    mbar_init(smem_u32(&bar_pv), 1);
-    mbar_init(smem_u32(&bar_q), 1);
-    mbar_init(smem_u32(&bar_qf), kConv);
-    for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&bar_qe[i]), kConv);
-    mbar_init(smem_u32(&bar_drain), 1);
+    for (int b = 0; b < 2; ++b) {  // buffer b serves the tiles of stream b
+      mbar_init(smem_u32(&bar_s[b]), 1);
+      mbar_init(smem_u32(&bar_sfree[b]), kSoftmax / 2);
+      mbar_init(smem_u32(&bar_p[b]), kSoftmax / 2);
+    }
+    mbar_init(smem_u32(&bar_q), kSoftmax);
+    mbar_init(smem_u32(&bar_drain_qk), 1);
+    mbar_init(smem_u32(&bar_drain_pv), 1);
     abort_flag = 0;
     zero_flag = 0;
     mbar_init_fence();
   }
   if (threadIdx.x < NP) sCol[threadIdx.x] = (threadIdx.x / p.G) * p.Hq + threadIdx.x % p.G;
-  // rows of the query operand past the unit's G s_q columns stay zero
-  for (int i = threadIdx.x; i < NP * 256 / 16; i += kThreads) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  // query operand rows past the unit's columns stay zero
+  for (int i = threadIdx.x; i < Gm::kQBytes / 16; i += kThreads) reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
-  if (warp == kWarpMma) tmem_alloc(smem_u32(&tmem_slot), 128);
+  if (warp == kWarpPv) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // TMEM: S^T buffer b: cols [NP b, NP b + NP); O^T: [2 NP, 3 NP)
+  // TMEM: S^T buffer b at columns [2 NP b, 2 NP b + 2 NP) (hi products, then
+  // lo); stream b's O^T at [4 NP + NP b, 5 NP + NP b)
   const uint32_t tmem = tmem_slot;
+  const uint32_t tmem_o = tmem + 4 * NP;
   const int w0 = p.plan[p.off_worker + blockIdx.x], w1 = p.plan[p.off_worker + blockIdx.x + 1];
   const int ncols = p.G * p.s_q;  // columns of a unit in use
+  const uint32_t sbase = smem_u32(smem);
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: codes into the slots
     bool ok = true;
     int g = 0;
-    int last[kSlots] = {-1, -1};  // tile of each slot's last fill
+    int last[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) last[s] = -1;
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, wi);
       for (int kh = 0; kh < p.Hkv && it.ntiles > 0 && ok; ++kh) {
         for (int j = 0; j < it.ntiles; ++j, ++g) {
           const int s = g % kSlots, use = g / kSlots;
-          if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_codefree[s]), (use - 1) & 1,
+          // the slot's previous tile (g - kSlots) must have gone through its P.V
+          if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[s]), (use - 1) & 1,
                                                             p.wait_ns, &abort_flag))) {
             if (lane == 0) report_timeout(p.status, 1, &abort_flag);
             ok = false;
             break;
           }
-          const uint32_t full = smem_u32(&bar_code[s]);
+          const uint32_t full = smem_u32(&bar_full[s]);
           if (elect_one()) {
             mbar_expect_tx(full, kSlotBytes);
             const int y = (int)(it.row0 + (long long)j * kRows);
-            tma_load_3d(smem_u32(sSlot + s * kSlotBytes), &maps.k[it.r], 0, kh, y, full);
-            tma_load_3d(smem_u32(sSlot + s * kSlotBytes + kCodeBytes), &maps.v[it.r], 0, kh, y, full);
+            tma_load_3d(sbase + s * kSlotBytes, &maps.k[it.r], 0, kh, y, full);
+            tma_load_3d(sbase + s * kSlotBytes + kCodeBytes, &maps.v[it.r], 0, kh, y, full);
           }
           __syncwarp();
           last[s] = g;
         }
       }
     }
-    if (!ok) {
-      // never leave with a copy in flight
-      for (int s = 0; s < kSlots; ++s)
-        if (last[s] >= 0) mbar_wait(smem_u32(&bar_code[s]), (last[s] / kSlots) & 1, 1000000000ull, &zero_flag);
-      __syncwarp();
-    }
-  } else if (warp >= kWarpConv0) {
-    // ------------------------------------------------------------ converters (warps 6-11):
-    // each unit's query to f16 x 2^e, each tile's codes to f16
-    const int ct = threadIdx.x - kWarpConv0 * 32;  // 0 .. kConv - 1
+    // Never leave with a copy in flight.
+    for (int s = 0; s < kSlots; ++s)
+      if (last[s] >= 0) mbar_wait(smem_u32(&bar_full[s]), (last[s] / kSlots) & 1, 1000000000ull, &zero_flag);
+    __syncwarp();
+  } else if (warp == kWarpQk) {
+    // ------------------------------------------------------------ QK^T issue
+    const uint32_t idQK = idesc_e4m3_f32(kRows, 2 * NP, 0, 0);
+    // K codes and the query operand K-major, 128-byte swizzle; a K-step of 32
+    // dims is 32 bytes of a row, 2 in the descriptor's start-address field
+    const uint64_t dK = smem_desc(sbase, 16, 1024, 2);
+    const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024, 2);
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
+    };
     bool ok = true;
-    int g = 0, nu = 0;  // tiles and units so far
-    int q_pending = -1; // parity of a query load that may still be in flight
+    int g = 0, nu = 0;
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, wi);
       for (int kh = 0; kh < p.Hkv && it.ntiles > 0 && ok; ++kh, ++nu) {
+        // the unit's query operand is in place (written after every product of
+        // the previous unit completed)
+        if (!wait_all(smem_u32(&bar_q), nu & 1)) {
+          if (lane == 0) report_timeout(p.status, 2, &abort_flag);
+          ok = false;
+          break;
+        }
         for (int j = 0; j < it.ntiles; ++j, ++g) {
-          const int s = g % kSlots, st = g % kStages;
-          // f16 stage st is free once the P.V of tile g - 2 has completed; that
-          // P.V was issued after the QK^T of tile g - 1, so sQ is free too (for
-          // g = 1: the first QK^T's own barrier, whose first phase it is)
-          bool got = true;
-          if (g >= 2)
-            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[st]), ((g - 2) / kStages) & 1,
-                                                    p.wait_ns, &abort_flag));
-          else if (g == 1 && j == 0)
-            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[0]), 0, p.wait_ns, &abort_flag));
-          if (got && j == 0) {
-            // ---- the unit's query: bf16 by TMA, then f16 x 2^e in place
-            q_pending = nu & 1;
-            if (ct == 0) {
-              mbar_expect_tx(smem_u32(&bar_q), 2 * ncols * 128);
-              for (int c = 0; c < 2; ++c)
-                tma_load_4d(smem_u32(sQ + c * NP * 128), &qmap, c * 64, 0, kh, it.b * p.s_q, smem_u32(&bar_q));
-            }
-            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q), nu & 1, p.wait_ns, &abort_flag));
-            if (got) {
-              q_pending = -1;
-              uint32_t mx = 0;  // largest |q| as bf16 magnitude bits
-              for (int i = ct; i < 2 * ncols * 8; i += kConv) {
-                const int c = i / (ncols * 8), n = (i / 8) % ncols, w = i % 8;
-                const uint4 v = *reinterpret_cast<const uint4*>(sQ + c * NP * 128 + n * 128 + w * 16);
-                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) mx = max(mx, max(wd[e] & 0x7FFFu, (wd[e] >> 16) & 0x7FFFu));
-              }
-              mx = __reduce_max_sync(0xffffffffu, mx);
-              if (lane == 0) sQmax[warp - kWarpConv0] = mx;
-              named_bar_sync(2, kConv);
-              for (int w2 = 0; w2 < kConvWarps; ++w2) mx = max(mx, sQmax[w2]);
-              // 2^e puts the largest |q| in [2^13, 2^14); e kept where 2^e and 2^-e are normal
-              const int ex = (int)((mx >> 7) & 0xFF) - 127;
-              const int e = mx == 0 ? 0 : max(-126, min(126, 13 - ex));
-              const float sc = __int_as_float((e + 127) << 23);
-              for (int i = ct; i < 2 * ncols * 8; i += kConv) {
-                const int c = i / (ncols * 8), n = (i / 8) % ncols, w = i % 8;
-                uint4* ptr = reinterpret_cast<uint4*>(sQ + c * NP * 128 + n * 128 + w * 16);
-                const uint4 v = *ptr;
-                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-                uint32_t o[4];
-#pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                  const __half2 h = __floats2half2_rn(__uint_as_float(wd[e2] << 16) * sc,
-                                                      __uint_as_float(wd[e2] & 0xFFFF0000u) * sc);
-                  o[e2] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-                *ptr = make_uint4(o[0], o[1], o[2], o[3]);
-              }
-              if (ct == 0) sQe[nu & 3] = e;
-              fence_proxy_async_smem();
-              mbar_arrive(smem_u32(&bar_qf));
-              mbar_arrive(smem_u32(&bar_qe[nu & 3]));
-            }
-          }
-          got = got && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_code[s]), (g / kSlots) & 1, p.wait_ns,
-                                                         &abort_flag));
-          if (!got) {
-            if (lane == 0) report_timeout(p.status, 2, &abort_flag);
+          const int s = g % kSlots, b = g & 1;
+          // S^T buffer b is free once the softmax has loaded tile g - 2's scores
+          if (g >= 2 && !wait_all(smem_u32(&bar_sfree[b]), ((g >> 1) & 1) ^ 1)) {
+            if (lane == 0) report_timeout(p.status, 9, &abort_flag);
             ok = false;
             break;
           }
-          // ---- codes of slot s -> f16 stage st: K, announced on its own so that
-          // QK^T and the softmax overlap the conversion of V
-          const uint8_t* src = sSlot + s * kSlotBytes;
-          uint8_t* dst = sStage + st * kStageBytes;
-#pragma unroll 1
-          for (int tsr = 0; tsr < 2; ++tsr) {
-#pragma unroll 4
-            for (int i = ct; i < kRows * 8; i += kConv) {
-              const int r = i >> 3, u = i & 7;  // row, 16-code unit
-              const uint4 v =
-                  *reinterpret_cast<const uint4*>(src + tsr * kCodeBytes + r * 128 + ((u ^ (r & 7)) << 4));
-              const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
-              uint32_t h[8];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                h[2 * e] = e4m3x2_to_f16x2_hw<0>(wd[e]);
-                h[2 * e + 1] = e4m3x2_to_f16x2_hw<2>(wd[e]);
-              }
-              // dims 16u .. 16u + 15: chunk u / 4, 16-byte units 2 (u % 4) and 2 (u % 4) + 1
-              uint8_t* rowp = dst + tsr * kTileBytes + (u >> 2) * kChunkBytes + r * 128;
-              const int w0u = 2 * (u & 3);
-              *reinterpret_cast<uint4*>(rowp + ((w0u ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-              *reinterpret_cast<uint4*>(rowp + (((w0u + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
-            }
-            fence_proxy_async_smem();
-            if (tsr == 0) mbar_arrive(smem_u32(&bar_fullK[st]));
-          }
-          mbar_arrive(smem_u32(&bar_codefree[s]));
-          mbar_arrive(smem_u32(&bar_fullV[st]));
-        }
-      }
-    }
-    if (!ok && q_pending >= 0) {
-      // never leave with the query copy in flight
-      mbar_wait(smem_u32(&bar_q), q_pending, 1000000000ull, &zero_flag);
-      __syncwarp();
-    }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA issue: per tile g,
-    // S^T(g) first, then P.V of tile g - 1 once its P is written
-    const uint32_t idS = idesc_f16_f32(kRows, NP, 0, 0);
-    const uint32_t idPV = idesc_f16_f32(kRows, NP, 1, 0);
-    const uint32_t st0 = smem_u32(sStage);
-    // K tile K-major; V^T MN-major (its two 64-dim chunks kChunkBytes apart); Q and P K-major
-    const uint64_t dK = smem_desc(st0, 16, 1024), dV = smem_desc(st0 + kTileBytes, kChunkBytes, 1024);
-    const uint64_t dQ = smem_desc(smem_u32(sQ), 16, 1024), dP = smem_desc(smem_u32(sP), 16, 1024);
-    bool ok = true;
-    int g = 0, nu = 0;
-    int prev_j = -1, prev_s = 0;  // tile index in its unit and stage of the tile whose P.V is pending
-    auto pv = [&](int gp, int jp, int sp) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p), gp & 1, p.wait_ns, &abort_flag))) return false;
-      // every earlier phase of this stage's V barrier was waited for here
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fullV[sp]), (gp / kStages) & 1, p.wait_ns,
-                                             &abort_flag)))
-        return false;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t v = dV + ((uint32_t)(sp * kStageBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kRows / 16; ++kk)
-          mma_ss(tmem + 2 * NP, v + ((kk * 2048) >> 4), dP + (((kk >> 2) * NP * 128 + (kk & 3) * 32) >> 4), idPV,
-                 (jp > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bar_empty[sp]));
-        mma_commit(smem_u32(&bar_pv));
-      }
-      __syncwarp();
-      return true;
-    };
-    for (int wi = w0; wi < w1 && ok; ++wi) {
-      const Item it = read_item(p, wi);
-      for (int kh = 0; kh < p.Hkv && it.ntiles > 0 && ok; ++kh, ++nu) {
-        for (int j = 0; j < it.ntiles; ++j, ++g) {
-          const int s = g % kStages;
-          bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fullK[s]), (g / kStages) & 1, p.wait_ns,
-                                                       &abort_flag));
-          if (got && j == 0)
-            got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_qf), nu & 1, p.wait_ns, &abort_flag));
-          if (!got) {
+          if (!wait_all(smem_u32(&bar_full[s]), (g / kSlots) & 1)) {
             if (lane == 0) report_timeout(p.status, 3, &abort_flag);
             ok = false;
             break;
           }
           tc_fence_after();
-          // S^T buffer g & 1 was last read by the softmax of tile g - 2, whose P
-          // the P.V of tile g - 2 waited for
           if (elect_one()) {
-            const uint64_t k = dK + ((uint32_t)(s * kStageBytes) >> 4);
+            const uint64_t a = dK + (uint64_t)((s * kSlotBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-              const uint32_t qoff = (kk >> 2) * NP * 128 + (kk & 3) * 32;
-              mma_ss(tmem + NP * (g & 1), k + (off >> 4), dQ + (qoff >> 4), idS, kk > 0);
-            }
-            mma_commit(smem_u32(&bar_s[g & 1]));
+            for (int ks = 0; ks < kD / 32; ++ks)
+              mma_ss_f8(tmem + 2 * NP * b, a + 2 * ks, dQ + 2 * ks, idQK, ks > 0 ? 1u : 0u);
+            mma_commit(smem_u32(&bar_s[b]));
           }
           __syncwarp();
-          if (prev_j >= 0 && !pv(g - 1, prev_j, prev_s)) {
+        }
+      }
+    }
+    // Never free TMEM under a running MMA.
+    if (elect_one()) mma_commit(smem_u32(&bar_drain_qk));
+    __syncwarp();
+    mbar_wait(smem_u32(&bar_drain_qk), 0, 1000000000ull, &zero_flag);
+  } else if (warp == kWarpPv) {
+    // ------------------------------------------------------------ P.V issue, TMEM owner
+    const uint32_t idPV = idesc_e4m3_f32(kRows, NP, 1, 0);
+    // V^T: the V codes read MN-major (M = 128 dims of a 128-byte row; a K-step
+    // of 32 rows is 4 KB); P_hi / P_lo K-major like the query operand
+    const uint64_t dV = smem_desc(sbase + kCodeBytes, kCodeBytes, 1024, 2);
+    const uint64_t dP = smem_desc(smem_u32(sP), 16, 1024, 2);
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
+    };
+    bool ok = true;
+    int g = 0;
+    for (int wi = w0; wi < w1 && ok; ++wi) {
+      const Item it = read_item(p, wi);
+      for (int kh = 0; kh < p.Hkv && it.ntiles > 0 && ok; ++kh) {
+        for (int j = 0; j < it.ntiles; ++j, ++g) {
+          const int s = g % kSlots, b = g & 1;
+          if (!wait_all(smem_u32(&bar_p[b]), (g >> 1) & 1) ||
+              !wait_all(smem_u32(&bar_full[s]), (g / kSlots) & 1)) {
             if (lane == 0) report_timeout(p.status, 4, &abort_flag);
             ok = false;
             break;
           }
-          prev_j = j;
-          prev_s = s;
+          tc_fence_after();
+          if (elect_one()) {
+            const uint64_t av = dV + (uint64_t)((s * kSlotBytes) >> 4);
+            const uint64_t bh = dP + (uint64_t)((b * Gm::kPBytes) >> 4);
+            const uint64_t bl = bh + (uint64_t)((NP * 128) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kRows / 32; ++kk) {
+              const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
+              // stream b's accumulator; its first tile of the unit (j < 2) starts it
+              mma_f8_fill_a(tmem_o + NP * b, a, bh + 2 * kk, idPV, (j >= 2 || kk > 0) ? 1u : 0u);
+              mma_f8_reuse_a(tmem_o + NP * b, a, bl + 2 * kk, idPV, 1u);
+            }
+            mma_commit(smem_u32(&bar_empty[s]));
+          }
+          __syncwarp();
         }
       }
     }
-    if (ok && prev_j >= 0 && !pv(g - 1, prev_j, prev_s)) {
-      if (lane == 0) report_timeout(p.status, 4, &abort_flag);
-    }
-    // never free TMEM under a running MMA
-    if (elect_one()) mma_commit(smem_u32(&bar_drain));
+    if (elect_one()) mma_commit(smem_u32(&bar_drain_pv));
     __syncwarp();
-    mbar_wait(smem_u32(&bar_drain), 0, 1000000000ull, &zero_flag);
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int t = threadIdx.x;  // tile row = TMEM lane; in the epilogue a dim row of O^T
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    // P row n is K-major: KV row t sits in chunk t / 64, 16-byte unit (t % 64) / 8
-    // (swizzled with n % 8), halfword t % 8
-    uint8_t* prow = sP + (t >> 6) * NP * 128 + (t & 7) * 2;
-    const int punit = (t & 63) >> 3;
+    mbar_wait(smem_u32(&bar_drain_pv), 0, 1000000000ull, &zero_flag);
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    // Two streams: warps 0-3 take the unit's tiles with even g, warps 4-7 those
+    // with odd g.  Each stream has its own S^T buffer, P buffer, O^T
+    // accumulator and running max and sum, so one stream's score loads (slow
+    // while products run) overlap the other's exponentials; a unit's epilogue
+    // merges the two streams' (O, max, sum) exactly.
+    const int st = warp >> 2;           // stream: tiles g with g % 2 == st
+    const int quarter = warp & 3;       // TMEM lane quarter: tile rows [32 quarter, +32)
+    const int t = quarter * 32 + lane;  // tile row = TMEM lane; in the epilogue a dim row of O^T
+    const int tid = threadIdx.x;        // 0 .. kSoftmax - 1
+    const int sid = tid & 127;          // thread within the stream
+    const int bar_st = 1 + st;          // the stream's named barrier (128 threads)
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t o_addr = lane_addr + 4 * NP + NP * st;  // this stream's O^T
+    auto pv_done = [&](int gg) {  // the P.V of tile gg has completed
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[gg % kSlots]), (gg / kSlots) & 1,
+                                               p.wait_ns, &abort_flag));
+    };
     bool ok = true;
     int g = 0, nu = 0;
     for (int wi = w0; wi < w1 && ok; ++wi) {
@@ -493,170 +434,282 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
         float* out_o = out_rows(p, it);
         float* out_l = out_lse(p, it);
-        for (int i = t; i < p.Hc * kD; i += kSoftmax) out_o[i] = 0.f;
-        for (int i = t; i < p.Hc; i += kSoftmax) out_l[i] = -INFINITY;
+        for (int i = tid; i < p.Hc * kD; i += kSoftmax) out_o[i] = 0.f;
+        for (int i = tid; i < p.Hc; i += kSoftmax) out_l[i] = -INFINITY;
         continue;
       }
-      // token of tile row t of tile j: tok_t + j * tok_j; a cache row is masked
+      // token of tile row t of tile j: tok_t + j tok_j; a cache row is masked
       // for the columns of query rows below tok - lim
       const int tok_j = kRows * it.pd.tok_step;
       const int tok_t = it.pd.tok0 + (it.row_begin + t) * it.pd.tok_step;
       const int lim = it.pd.ctx_len - p.s_q;
       const float* srow = p.sc.p[it.r] + it.row0;  // the item's per-row scales
       for (int kh = 0; kh < p.Hkv && ok; ++kh, ++nu) {
-        // the unit's query exponent: scores in log2 units are S x scale_row x 2^-e x scale_log2
-        const bool qok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_qe[nu & 3]), (nu >> 2) & 1, p.wait_ns,
-                                                           &abort_flag));
-        if (bar_red_or(1, kSoftmax, !qok)) {
-          if (!qok) report_timeout(p.status, 8, &abort_flag);
-          ok = false;
-          break;
+        const int g0 = g;  // the unit's first tile
+        // ---- the unit's [Q_hi | Q_lo]: x = q 2^eq with max |x| in [128, 256).
+        // Every product of the previous unit has completed (its epilogue
+        // waited for both streams' last P.V), so the operand can be overwritten.
+        constexpr int kPieces = kD / 8;  // 16-byte pieces per query column
+        constexpr int kPer = NP * kPieces / kSoftmax;
+        uint4 qv[kPer];
+        uint32_t qmax = 0;  // largest |q| as bf16 magnitude bits
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = tid + k * kSoftmax, n = i / kPieces, d0 = (i % kPieces) * 8;
+          qv[k] = make_uint4(0, 0, 0, 0);
+          if (n < ncols) {
+            const int qi = n / p.G, hh = kh * p.G + n % p.G;
+            qv[k] = __ldg(reinterpret_cast<const uint4*>(
+                p.q + (((long long)it.b * p.s_q + qi) * p.Hq + hh) * kD + d0));
+          }
+          const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
         }
-        const float cj = p.scale_log2 * kCodeScale * __int_as_float((127 - sQe[nu & 3]) << 23);
-        // the running max restarts from the unit's first tile; every read of the
-        // previous unit's maxima came before its epilogue's barriers
-        if (t < NP) sM[t] = 0.f;
-        named_bar_sync(1, kSoftmax);
+        qmax = __reduce_max_sync(0xffffffffu, qmax);
+        if (lane == 0) sQmax[warp] = qmax;
+        if (sid < NP) sM[st][sid] = 0.f;  // each stream's running max restarts with the unit
+        named_bar_sync(3, kSoftmax);
+#pragma unroll
+        for (int w = 0; w < kSoftmaxWarps; ++w) qmax = max(qmax, sQmax[w]);
+        const int eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
+        const float qs = pow2i(eq);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+          const int i = tid + k * kSoftmax, n = i / kPieces, d0 = (i % kPieces) * 8;
+          if (n < ncols) {
+            const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+            uint32_t hs[4], ls[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs, hs[e],
+                           ls[e]);
+            *reinterpret_cast<uint2*>(sQ + sw128(n, d0)) = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
+            *reinterpret_cast<uint2*>(sQ + sw128(NP + n, d0)) =
+                make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&bar_q));
+        named_bar_sync(3, kSoftmax);  // sQmax read before its next write
+
+        // ---- this stream's tiles of the unit
+        const float cq = p.scale_log2 * pow2i(-eq);
+        int gs = 0;  // weights carry scale_row 2^gs (set on the stream's first tile, only decreases)
         float l[NP];
 #pragma unroll
         for (int n = 0; n < NP; ++n) l[n] = 0.f;
-        for (int j = 0; j < it.ntiles; ++j, ++g) {
+        const int j0 = (st ^ g0) & 1;  // the stream's first tile in the unit
+        bool failed = false;
+        for (int j = j0; j < it.ntiles; j += 2) {
+          const int gg = g0 + j, b = st;
+          const bool first = j < 2;
           const bool valid = j * kRows + t < it.nrows;
           const float rs = valid ? __ldg(srow + j * kRows + t) : 0.f;
           // several query rows (s_q > 1): row qi reads tokens up to L - s_q + qi,
           // so this cache row is masked for columns n = qi G + i with qi < tok - lim
           const int mcols = min(NP, max(0, tok_t + j * tok_j - lim) * p.G);
-          const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[g & 1]), (g >> 1) & 1, p.wait_ns,
+          // The stream's warps leave together: one that gave up meets the others at this vote.
+          const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[b]), (gg >> 1) & 1, p.wait_ns,
                                                              &abort_flag));
-          if (bar_red_or(1, kSoftmax, !got)) {
+          if (bar_red_or(bar_st, 128, !got)) {
             if (!got) report_timeout(p.status, 5, &abort_flag);
-            ok = false;
+            failed = true;
             break;
           }
           tc_fence_after();
           // u = score - running max (log2 units); masked rows and columns read nothing
+          const float c = rs * cq;
           float u[NP];
           float over = -INFINITY;
-          {
-            uint32_t a[NP];
-            tmem_ld_cols<NP>(lane_addr + NP * (g & 1), a);
+#pragma unroll
+          for (int h0 = 0; h0 < NP; h0 += 16) {  // 16 columns at a time keeps registers low
+            uint32_t a[16], z[16];
+            tmem_ld16(lane_addr + 2 * NP * b + h0, a);
+            tmem_ld16(lane_addr + 2 * NP * b + NP + h0, z);
             tmem_ld_wait();
 #pragma unroll
-            for (int n = 0; n < NP; ++n) {
-              u[n] = valid && n >= mcols ? fmaf(__uint_as_float(a[n]), cj * rs, -sM[n]) : -INFINITY;
-              over = fmaxf(over, u[n]);
+            for (int n = 0; n < 16; ++n) {
+              const int col = h0 + n;
+              u[col] = valid && col >= mcols && col < ncols
+                           ? fmaf(__uint_as_float(a[n]) + __uint_as_float(z[n]), c, -sM[st][col])
+                           : -INFINITY;
+              over = fmaxf(over, u[col]);
             }
           }
-          // the previous tile's P.V has completed: P is free and O^T holds it
-          const bool freed = g == 0 || __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g - 1) & 1,
-                                                                          p.wait_ns, &abort_flag));
-          if (bar_red_or(1, kSoftmax, !freed)) {
-            if (!freed) report_timeout(p.status, 7, &abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // block-wide vote: does any score pass its running max by more than 2^8?
-          if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2)) {
+          // the scores are in registers: the QK^T issuer may refill this S^T buffer
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_sfree[b]));
+          // Stream-wide vote: the stream's first tile, a score past its running max by
+          // more than 2^3, or a token scale that would take a weight to 2^8 or more.
+          const bool big = valid && rs * pow2i(gs) >= (float)(1 << kWeightTop);
+          if (bar_red_or(bar_st, 128, first || over > kRescaleLog2 || big)) {
 #pragma unroll
             for (int n = 0; n < NP; ++n) {
               const int m = __reduce_max_sync(0xffffffffu, ordered(u[n]));
-              if (lane == 0) sRed[warp][n] = m;
+              if (lane == 0) sRed[st][quarter][n] = m;
             }
-            named_bar_sync(1, kSoftmax);
-            if (t < NP) {
-              const float cm = fmaxf(fmaxf(unordered(sRed[0][t]), unordered(sRed[1][t])),
-                                     fmaxf(unordered(sRed[2][t]), unordered(sRed[3][t])));
-              // the first tile sets the max; later the max moves when it grew by
-              // more than 2^8, earlier sums and O^T shrinking by 2^-delta (a column
-              // with no unmasked row in the unit's first tile has none at all:
-              // rows go up in token order; it keeps max 0 and weight 0)
-              const float delta = j == 0 ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
-              sAlpha[t] = j == 0 ? 0.f : ex2(-delta);
-              sDelta[t] = delta;
-              sM[t] += delta;
+            const uint32_t smx = __reduce_max_sync(0xffffffffu, __float_as_uint(rs));
+            if (lane == 0) sRed1[st][quarter] = smx;
+            named_bar_sync(bar_st, 128);
+            const float smax = __uint_as_float(max(max(sRed1[st][0], sRed1[st][1]), max(sRed1[st][2], sRed1[st][3])));
+            const int gs_new = first ? scale_exponent(smax, kWeightTop, 0)
+                                     : min(gs, scale_exponent(smax, kWeightTop, gs));
+            if (sid < NP) {
+              const float cm = fmaxf(fmaxf(unordered(sRed[st][0][sid]), unordered(sRed[st][1][sid])),
+                                     fmaxf(unordered(sRed[st][2][sid]), unordered(sRed[st][3][sid])));
+              // the first tile sets the max; later it moves when it grew by more
+              // than 2^3 (a column with no unmasked row in the stream's first tile
+              // has none later: rows go up in token order; it keeps max 0, weight 0)
+              const float delta = first ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
+              sDelta[st][sid] = delta;
+              sM[st][sid] += delta;
             }
-            named_bar_sync(1, kSoftmax);
+            named_bar_sync(bar_st, 128);
+            const float gf = pow2i(max(gs_new - gs, -126));
 #pragma unroll
             for (int n = 0; n < NP; ++n) {
-              l[n] *= sAlpha[n];
-              u[n] -= sDelta[n];
+              const float dl = sDelta[st][n];
+              u[n] -= dl;
+              l[n] *= ex2(-dl);
             }
-            if (j > 0) {
-              uint32_t o[NP];
-              tmem_ld_cols<NP>(lane_addr + 2 * NP, o);
-              tmem_ld_wait();
+            if (!first) {
+              // O^T holds the stream's earlier tiles: once its last P.V has landed, scale its columns
+              const bool landed = pv_done(gg - 2);
+              if (bar_red_or(bar_st, 128, !landed)) {
+                if (!landed) report_timeout(p.status, 6, &abort_flag);
+                failed = true;
+                break;
+              }
+              tc_fence_after();
 #pragma unroll
-              for (int n = 0; n < NP; ++n) o[n] = __float_as_uint(__uint_as_float(o[n]) * sAlpha[n]);
-              tmem_st_cols<NP>(lane_addr + 2 * NP, o);
+              for (int h0 = 0; h0 < NP; h0 += 16) {
+                uint32_t o[16];
+                tmem_ld16(o_addr + h0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int n = 0; n < 16; ++n)
+                  o[n] = __float_as_uint(__uint_as_float(o[n]) * (ex2(-sDelta[st][h0 + n]) * gf));
+                tmem_st16(o_addr + h0, o);
+              }
               tmem_st_wait();
             }
+            gs = gs_new;
+            named_bar_sync(bar_st, 128);  // sRed, sRed1 and sDelta read before their next writes
           }
-          // P[n][t] = 2^u x scale_row (f16): the value rows' scale; l counts 2^u
+          // P row t: p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
+          const float gr = rs * pow2i(gs);
+          uint32_t hw[NP / 2], lw[NP / 2];
 #pragma unroll
-          for (int n = 0; n < NP; ++n) {
-            const float pn = ex2(u[n]);
-            l[n] += pn;
-            *reinterpret_cast<__half*>(prow + n * 128 + ((punit ^ (n & 7)) << 4)) = __float2half_rn(pn * rs);
+          for (int k = 0; k < NP / 2; ++k) {
+            const float p0 = ex2(u[2 * k]), p1 = ex2(u[2 * k + 1]);
+            l[2 * k] += p0;
+            l[2 * k + 1] += p1;
+            split_e4m3x2(p0 * gr, p1 * gr, hw[k], lw[k]);
+          }
+          // P buffer b was read by the P.V of the stream's previous tile
+          if (!first) {
+            const bool freed = pv_done(gg - 2);
+            if (bar_red_or(bar_st, 128, !freed)) {
+              if (!freed) report_timeout(p.status, 7, &abort_flag);
+              failed = true;
+              break;
+            }
+          }
+          // K-major: row n of P_hi / P_lo holds column n's weights; this thread's KV row is byte t
+          uint8_t* ph = sP + b * Gm::kPBytes;
+#pragma unroll
+          for (int k = 0; k < NP / 2; ++k) {
+            ph[sw128(2 * k, t)] = (uint8_t)(hw[k] & 0xFF);
+            ph[sw128(2 * k + 1, t)] = (uint8_t)(hw[k] >> 8);
+            ph[NP * 128 + sw128(2 * k, t)] = (uint8_t)(lw[k] & 0xFF);
+            ph[NP * 128 + sw128(2 * k + 1, t)] = (uint8_t)(lw[k] >> 8);
           }
           fence_proxy_async_smem();
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bar_p));
+          mbar_arrive(smem_u32(&bar_p[b]));
         }
-        if (!ok) break;
-        // ---- epilogue of the unit: column sums of l, O^T / l, LSE
-        const bool landed =
-            __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_pv), (g - 1) & 1, p.wait_ns, &abort_flag));
-        if (bar_red_or(1, kSoftmax, !landed)) {
-          if (!landed) report_timeout(p.status, 6, &abort_flag);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        g = g0 + it.ntiles;
+        // ---- epilogue of the unit: both streams' column maxima and sums, the
+        // two O^T accumulators scaled to the common max, / sum, LSE
 #pragma unroll
         for (int n = 0; n < NP; ++n) {
           float v = l[n];
 #pragma unroll
           for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-          if (lane == 0) sL[warp][n] = v;
+          if (lane == 0) sRed[st][quarter][n] = __float_as_int(v);
         }
-        named_bar_sync(1, kSoftmax);
-        // unit column n is output column (n / G) Hq + kh G + n % G
-        float* out_o = out_rows(p, it);
-        if (t < NP) {
-          const float tot = sL[0][t] + sL[1][t] + sL[2][t] + sL[3][t];
-          sAlpha[t] = tot > 0.f ? kCodeScale / tot : 0.f;
-          if (t < ncols) out_lse(p, it)[sCol[t] + kh * p.G] = tot > 0.f ? (sM[t] + lg2(tot)) * kLn2 : -INFINITY;
+        if (sid == 0) sGs[st] = gs;
+        // both streams' last P.V have landed (the stream that gave up skips the wait)
+        const bool aborted = __any_sync(0xffffffffu, abort_flag != 0);
+        const bool landed = failed || aborted || ((it.ntiles < 2 || pv_done(g - 2)) && pv_done(g - 1));
+        if (bar_red_or(3, kSoftmax, failed || !landed || aborted)) {
+          if (!landed) report_timeout(p.status, 8, &abort_flag);
+          ok = false;
+          break;
         }
-        named_bar_sync(1, kSoftmax);
+        tc_fence_after();
+        if (tid < NP) {
+          const float l0 = __int_as_float(sRed[0][0][tid]) + __int_as_float(sRed[0][1][tid]) +
+                           __int_as_float(sRed[0][2][tid]) + __int_as_float(sRed[0][3][tid]);
+          const float l1 = __int_as_float(sRed[1][0][tid]) + __int_as_float(sRed[1][1][tid]) +
+                           __int_as_float(sRed[1][2][tid]) + __int_as_float(sRed[1][3][tid]);
+          // a stream with no weight in the column (or no tile in the unit) adds nothing
+          const float m0 = l0 > 0.f ? sM[0][tid] : -INFINITY, m1 = l1 > 0.f ? sM[1][tid] : -INFINITY;
+          const float m = fmaxf(m0, m1);
+          const float c0 = l0 > 0.f ? ex2(m0 - m) : 0.f, c1 = l1 > 0.f ? ex2(m1 - m) : 0.f;
+          const float tot = l0 * c0 + l1 * c1;
+          const float inv = tot > 0.f ? 1.f / tot : 0.f;
+          sCoef[0][tid] = c0 * inv * pow2i(-sGs[0]);
+          sCoef[1][tid] = c1 * inv * pow2i(-sGs[1]);
+          if (tid < ncols) out_lse(p, it)[sCol[tid] + kh * p.G] = tot > 0.f ? (m + lg2(tot)) * kLn2 : -INFINITY;
+        }
+        named_bar_sync(3, kSoftmax);
         {
-          uint32_t o[NP];
-          tmem_ld_cols<NP>(lane_addr + 2 * NP, o);
+          // warp (st, quarter): dim rows of the quarter, columns [st NP / 2, st NP / 2 + NP / 2)
+          constexpr int NC = NP / 2;
+          const int cb = st * NC;
+          uint32_t o0[NC], o1[NC];
+          if constexpr (NC == 8) {
+            tmem_ld8(lane_addr + 4 * NP + cb, o0);
+            tmem_ld8(lane_addr + 5 * NP + cb, o1);
+          } else {
+            tmem_ld16(lane_addr + 4 * NP + cb, o0);
+            tmem_ld16(lane_addr + 5 * NP + cb, o1);
+          }
           tmem_ld_wait();
+          float* out_o = out_rows(p, it);
 #pragma unroll
-          for (int n = 0; n < NP; ++n)
-            if (n < ncols) out_o[(long long)(sCol[n] + kh * p.G) * kD + t] = __uint_as_float(o[n]) * sAlpha[n];
+          for (int n = 0; n < NC; ++n) {
+            const int col = cb + n;
+            if (col < ncols) {
+              // a stream without weight in the column may hold an earlier unit's values: select, not scale
+              const float c0 = sCoef[0][col], c1 = sCoef[1][col];
+              const float v = (c0 != 0.f ? __uint_as_float(o0[n]) * c0 : 0.f) +
+                              (c1 != 0.f ? __uint_as_float(o1[n]) * c1 : 0.f);
+              out_o[(long long)(sCol[col] + kh * p.G) * kD + t] = v;
+            }
+          }
         }
         tc_fence_before();
-        // the four softmax warps decide together whether to go on
-        if (bar_red_or(1, kSoftmax, abort_flag != 0)) ok = false;
+        // the softmax warps decide together whether to go on; shared state is
+        // free for the next unit
+        if (bar_red_or(3, kSoftmax, abort_flag != 0)) ok = false;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 128);
+  if (warp == kWarpPv) tmem_dealloc(tmem, kTmemCols);
 }
 
-
 template <int NP>
-cudaError_t launch_np(const CodeMaps& maps, const CUtensorMap& qmap, const Params& p, int grid, cudaStream_t s) {
+cudaError_t launch_np(const CodeMaps& maps, const Params& p, int grid, cudaStream_t s) {
   auto kern = decode_gqa_f8_kernel<NP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<NP>());
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<NP>::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem_bytes<NP>(), s>>>(maps, qmap, p);
+  kern<<<grid, kThreads, Geo<NP>::kSmem, s>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -677,6 +730,7 @@ cudaError_t launch_decode_gqa_f8(const int32_t* dev_plan, const cp_plan_header& 
   p.off_pair = h.off_rank;
   p.off_worker = h.off_req;
   p.off_work = h.off_seg;
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
@@ -703,16 +757,7 @@ cudaError_t launch_decode_gqa_f8(const int32_t* dev_plan, const cp_plan_header& 
         !encode_tensor_map_u8_3d(&maps.v[r], v.p[r], dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  // the bf16 queries [B s_q][Hkv][G][128]: one box per 64-dim chunk holds one
-  // kv head's G heads of every query row of a request, rows n = qi G + i
-  CUtensorMap qmap;
-  {
-    const uint64_t dims[4] = {(uint64_t)kD, (uint64_t)p.G, (uint64_t)Hkv, (uint64_t)h.R * p.s_q};
-    const uint64_t qstrides[3] = {(uint64_t)kD * 2, (uint64_t)p.G * kD * 2, (uint64_t)Hq * kD * 2};
-    const uint32_t box[4] = {64, (uint32_t)p.G, 1, (uint32_t)p.s_q};
-    if (!encode_tensor_map_bf16(&qmap, q, 4, dims, qstrides, box)) return cudaErrorInvalidValue;
-  }
-  return p.G * p.s_q <= 16 ? launch_np<16>(maps, qmap, p, h.n_tiles, s) : launch_np<32>(maps, qmap, p, h.n_tiles, s);
+  return p.G * p.s_q <= 16 ? launch_np<16>(maps, p, h.n_tiles, s) : launch_np<32>(maps, p, h.n_tiles, s);
 }
 
 }  // namespace cpattn

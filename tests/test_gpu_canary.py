@@ -91,24 +91,32 @@ def test_decode_pack_merge_guards(cp, fp8):
         check_guards(b_, k_, what)
 
 
-@pytest.mark.parametrize("D,s_q", [(128, 1), (64, 1), (128, 3)])
-def test_gqa_decode_guards(cp, D, s_q):
-    """The GQA decode (the tensor-core kernel for these shapes) writes only its
-    partials, their LSE and its workspace; split pairs use the workspace."""
+@pytest.mark.parametrize("D,s_q,kv", [(128, 1, "bf16"), (64, 1, "bf16"), (128, 3, "bf16"), (128, 1, "fp8"),
+                                       (128, 3, "fp8")])
+def test_gqa_decode_guards(cp, D, s_q, kv):
+    """The GQA decode (the tensor-core kernels for these shapes, bf16 and FP8
+    caches) writes only its partials, their LSE and its workspace; split
+    pairs use the workspace."""
     ctx, C, Hq, Hkv = [s_q, 300, 1000], 4, 8, 2
     B = len(ctx)
-    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=5 + D + s_q, device=DEV, std=0.3)
     plan = cp.cp_decode_plan_ex(C, ctx, s_q=s_q, n_workers=7, device=DEV)
-    sk, _ = cp.cp_kv_shard_pack(plan, k)
-    sv, _ = cp.cp_kv_shard_pack(plan, v)
+    ss = None
+    if kv == "fp8":
+        q, kc, vc, sc = W.gqa_decode_inputs_fp8(B, ctx, Hq * s_q, Hkv, D, seed=15 + s_q, device=DEV, std=0.3)
+        sk, ss = cp.cp_kv_shard_pack(plan, kc, sc)
+        sv, _ = cp.cp_kv_shard_pack(plan, vc)
+    else:
+        q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=5 + D + s_q, device=DEV, std=0.3)
+        sk, _ = cp.cp_kv_shard_pack(plan, k)
+        sv, _ = cp.cp_kv_shard_pack(plan, v)
     lead = (B, s_q) if s_q > 1 else (B,)
     qq = q.reshape(B, s_q, Hq, D) if s_q > 1 else q
     o_part, opb, opk = guarded((C, *lead, Hq, D), torch.float32, 60)
     lse_part, lpb, lpk = guarded((C, *lead, Hq), torch.float32, 61)
     ws_bytes = cp.cp_decode_workspace_size(plan, Hq, D)
     ws, wsb, wsk = guarded((max(ws_bytes, 16),), torch.uint8, 62)
-    cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, qq, sk, sv, sm_scale=1.0 / math.sqrt(D), o_part=o_part,
-                      lse_part=lse_part, ws=ws)
+    cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, qq, sk, sv, shard_scale=ss, sm_scale=1.0 / math.sqrt(D),
+                      o_part=o_part, lse_part=lse_part, ws=ws)
     cp.cp_device_error_check()
     for (b_, k_), what in [((opb, opk), "o_part"), ((lpb, lpk), "lse_part"), ((wsb, wsk), "workspace")]:
         check_guards(b_, k_, what)

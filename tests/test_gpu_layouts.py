@@ -235,3 +235,72 @@ def test_gqa_paged_query_rows_match_unpaged(cp):
     o_p, l_p = cp.cp_decode_attn_paged(plan, pages, cp.CP_DECODE_GQA, qq, kp, vp, sm_scale=0.125)
     cp.cp_device_error_check()
     assert torch.equal(o_p, o_ref) and torch.equal(l_p, l_ref)
+
+
+def gqa_fp8_rows_case(cp, ctx, Hq, Hkv, s_q, contiguous, seed, C=4, n_workers=5):
+    """GQA over an E4M3 cache (one scale per token for its K and V rows) with
+    s_q query rows per request: every shard's partials and the merged rows
+    against the oracle (codes decoded bit by bit, times the scale)."""
+    B, D = len(ctx), 128
+    q, kc, vc, sc = W.gqa_decode_inputs_fp8(B, ctx, Hq * s_q, Hkv, D, seed=seed, device=DEV, std=0.3)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=n_workers, device=DEV)
+    qq = q.reshape(B, s_q, Hq, D) if s_q > 1 else q
+    sk, ss = cp.cp_kv_shard_pack(plan, kc, sc)
+    sv, _ = cp.cp_kv_shard_pack(plan, vc)
+    scale = 1.0 / math.sqrt(D)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, qq, sk, sv, shard_scale=ss, sm_scale=scale)
+    o_part = o_part.reshape(C, B, s_q, Hq, D)
+    lse_part = lse_part.reshape(C, B, s_q, Hq)
+    o, lse = cp.cp_lse_merge(o_part.reshape(C, B * s_q, Hq, D), lse_part.reshape(C, B * s_q, Hq),
+                             out_dtype=torch.float32)
+    o, lse = o.reshape(B, s_q, Hq, D), lse.reshape(B, s_q, Hq)
+    cp.cp_device_error_check()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    s64 = sc.double().cpu().numpy()[:, None, None]
+    kn = oracle.e4m3_decode(kc.cpu().numpy()) * s64
+    vn = oracle.e4m3_decode(vc.cpu().numpy()) * s64
+    qn = np64(q).reshape(B, s_q, Hq, D)
+    for b, L in enumerate(ctx):
+        K, V = kn[base[b]:base[b] + L], vn[base[b]:base[b] + L]
+        po, pl = oracle.query_rows_partials(qn[b], K, V, C, scale, contiguous=contiguous)
+        for r in range(C):
+            for i in range(s_q):
+                check_o(o_part[r, b, i], po[r, i], what=f"FP8 GQA partial r{r} b{b} row{i}", **TOL_FP8)
+                check_lse(lse_part[r, b, i], pl[r, i])
+        for i in range(s_q):
+            fo, fl = oracle.decode_attention(qn[b, i], K[:L - s_q + i + 1], V[:L - s_q + i + 1], scale)
+            check_o(o[b, i], fo, what=f"FP8 GQA merged b{b} row{i}", **TOL_FP8)
+            check_lse(lse[b, i], fl)
+
+
+@pytest.mark.parametrize("Hq,Hkv,s_q,contiguous", [(8, 2, 2, False), (8, 2, 3, True), (16, 4, 2, True),
+                                                   (32, 8, 1, False), (16, 16, 1, False), (32, 1, 1, True)])
+def test_gqa_fp8_query_rows_and_widths(cp, Hq, Hkv, s_q, contiguous):
+    """The FP8 tensor-core GQA decode pads a kv head's G s_q query columns to
+    16 or 32: several query rows, both shard layouts, one query head per kv
+    head, one kv head for 32 query heads, ragged tiles and split pairs."""
+    ctx = [s_q, 129, 1000, 2600] + ([0] if s_q == 1 else [])
+    gqa_fp8_rows_case(cp, ctx, Hq, Hkv, s_q, contiguous, seed=300 + Hq + Hkv + s_q, n_workers=7)
+
+
+def test_gqa_fp8_full_size_sampled(cp):
+    """16 requests x 131,072 tokens over an E4M3 cache, 32 q / 8 kv heads,
+    head dim 128, C = 8 (the benchmark's GQA workload): one sampled request,
+    whole context, against the oracle."""
+    B, L, Hq, Hkv, D, C = 16, 131072, 32, 8, 128, 8
+    ctx = [L] * B
+    q, kc, vc, sc = W.gqa_decode_inputs_fp8(B, ctx, Hq, Hkv, D, seed=72, device=DEV)
+    plan = cp.cp_decode_plan(C, ctx, device=DEV)
+    sk, ss = cp.cp_kv_shard_pack(plan, kc, sc)
+    sv, _ = cp.cp_kv_shard_pack(plan, vc)
+    scale = 1.0 / math.sqrt(D)
+    o_part, lse_part = cp.cp_decode_attn(plan, cp.CP_DECODE_GQA, q, sk, sv, shard_scale=ss, sm_scale=scale)
+    o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
+    cp.cp_device_error_check()
+    b = 9
+    s64 = sc[b * L:(b + 1) * L].double().cpu().numpy()[:, None, None]
+    K = oracle.e4m3_decode(kc[b * L:(b + 1) * L].cpu().numpy()) * s64
+    V = oracle.e4m3_decode(vc[b * L:(b + 1) * L].cpu().numpy()) * s64
+    fo, fl = oracle.decode_attention(np64(q)[b], K, V, scale)
+    check_o(o[b], fo, what=f"full-size FP8 GQA b{b}", **TOL_FP8)
+    check_lse(lse[b], fl)
