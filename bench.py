@@ -62,8 +62,8 @@ PROFILED_TRAFFIC = {
                    "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "c77af04969f83e602ccf338767b0de680d3bfdee",
-                    "bytes_per_token": (1.077104e9 + 0.006117e9) / (4 * 131072)},
+                    "sha1": "c19956b2693cf34223e556901c4c0d1891584060",
+                    "bytes_per_token": (1.078127e9 + 0.006134e9) / (4 * 131072)},
 }
 
 
