@@ -559,7 +559,10 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   else if (gqa_tc_supported(kv_dtype, Hq, Hkv, Dqk, Dv, plan_s_q(h)))
     e = launch_decode_gqa_tc(plan, h, q, K, V, shard_rows, rm, Hq, Hkv, Dqk, sm_scale, o_part, lse_part, ws_o,
                              ws_lse, pair_count, wait_limit_ns(), s);
-  else  // fp32 caches, other head dims, more query columns per kv head: CUDA cores
+  else if (kv_dtype == CP_FP32 && gqa_tf32_supported(Hq, Hkv, Dqk, Dv, plan_s_q(h), rm.table != nullptr))
+    e = launch_decode_gqa_tf32(plan, h, q, K, V, Hq, Hkv, Dqk, sm_scale, o_part, lse_part, ws_o, ws_lse,
+                               pair_count, s);
+  else  // paged fp32 or FP8 pools, other head dims, more query columns per kv head: CUDA cores
     e = launch_decode_simt(plan, h, kv_dtype, q, K, V, S, rm, Hq, Hkv, Dqk, Dv, sm_scale, o_part, lse_part,
                            ws_o, ws_lse, pair_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
@@ -651,7 +654,9 @@ cp_status cp_prefill_attn(const void* host_plan, const void* dev_plan, int rank,
     const char* stall = getenv("CPATTN_TEST_STALL");
     e = launch_prefill_tc((const int32_t*)dev_plan, W, h, rank, q, k, v, Hq, Hkv, D, sm_scale, o,
                           lse, stall && stall[0] == '1', s);
-  } else {
+  } else if (prefill_tf32_supported(D)) {
+    e = launch_prefill_tf32((const int32_t*)dev_plan, W, h, rank, q, k, v, Hq, Hkv, D, sm_scale, o, lse, s);
+  } else {  // fp32 at head dims 32 and 96: CUDA cores
     e = launch_prefill_simt((const int32_t*)dev_plan, h, rank, row_begin, n_rows, false, q, k, v,
                             Hq, Hkv, D, sm_scale, o, lse, s);
   }

@@ -28,7 +28,8 @@ enum KernelId : unsigned {
   kKernDecodeMlaTc = 2,
   kKernDecodeMlaFp8 = 3,
   kKernDecodeGqaTc = 4,
-  kKernDecodeGqaF8 = 5
+  kKernDecodeGqaF8 = 5,
+  kKernTf32 = 6
 };
 
 struct ShardPtrs {
@@ -154,6 +155,18 @@ cudaError_t launch_decode_gqa_f8(const int32_t* dev_plan, const cp_plan_header& 
                                  const long long* shard_rows, int Hq, int Hkv, float sm_scale, float* o_part,
                                  float* lse_part, float* ws_o, float* ws_lse, const int32_t* pair_count,
                                  unsigned long long wait_ns, cudaStream_t s);
+// ---- fp32 inputs on the tensor cores, kind::tf32 (tf32_attn.cu): the prefill
+// at head dim 64 or 128; the GQA decode over per-shard fp32 buffers at head
+// dim 64 or 128 with at most 64 query columns per kv head (G s_q).
+bool prefill_tf32_supported(int D);
+cudaError_t launch_prefill_tf32(const int32_t* dev_plan, const int32_t* host_plan, const cp_plan_header& h,
+                                int rank, const void* q, const void* k, const void* v, int Hq, int Hkv, int D,
+                                float sm_scale, void* o, float* lse, cudaStream_t s);
+bool gqa_tf32_supported(int Hq, int Hkv, int Dqk, int Dv, int s_q, bool paged);
+cudaError_t launch_decode_gqa_tf32(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
+                                   const ShardPtrs& k, const ShardPtrs& v, int Hq, int Hkv, int D, float sm_scale,
+                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
+                                   const int32_t* pair_count, cudaStream_t s);
 cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
                                cp_dtype kv_dtype, const void* q, const ShardPtrs& k,
                                const ShardPtrs& v, const ScalePtrs& sc, const RowMap& rm, int Hq,

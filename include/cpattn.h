@@ -225,9 +225,12 @@ cp_status cp_shard_plan(cp_strategy strategy, int C, int R, const int32_t* new_l
  * o   [rows, Hq, D] same dtype as q; rows = T (rank = -1, rank-major order)
  *                   or rank r's count (rank = r, its local order)
  * lse [rows, Hq]    fp32
- * dtype: CP_BF16 (tensor-core path, D in {64, 128}) or CP_FP32 (CUDA-core
- *   path, D <= 128, D % 32 == 0).  Hq % Hkv == 0.  host_plan and dev_plan
- *   come from cp_shard_plan (the host part is read for the launch shape).
+ * dtype: CP_BF16 (tensor cores, bf16 products; D in {64, 128}) or CP_FP32
+ *   (D <= 128, D % 32 == 0): at D = 64 or 128 on the tensor cores as tf32
+ *   products (fp32 values read with a 10-bit mantissa, fp32 accumulation),
+ *   at D = 32 or 96 on the CUDA cores.  Hq % Hkv == 0.  host_plan and
+ *   dev_plan come from cp_shard_plan (the host part is read for the launch
+ *   shape).
  * ------------------------------------------------------------------------- */
 cp_status cp_prefill_attn(const void* host_plan, const void* dev_plan, int rank, cp_dtype dtype,
                           const void* q, const void* k, const void* v, int Hq, int Hkv, int D,
@@ -327,15 +330,17 @@ cp_status cp_kv_shard_pack(const void* host_plan, const void* dev_plan, cp_dtype
  *   or shard_k/shard_v E4M3 codes (CP_FP8_E4M3, q bf16) with
  *   shard_scale[r] [rows_r] fp32, one scale per token for both its K and V
  *   rows (k = code x scale, v = code x scale); Dqk = Dv = D, D % 32 == 0,
- *   D <= 256.  An FP8 cache with D = 128, at most 32 query columns per kv
- *   head and per-shard buffers runs on the tensor cores (the codes expanded
- *   to f16 in shared memory); other FP8 shapes, and a paged FP8 pool, on the
- *   CUDA cores.  A bf16 cache with
- *   D = 64 or 128 and at most 64 query columns per kv head ((Hq/Hkv) s_q)
- *   runs on the tensor cores (the kv head's query heads share each K/V
- *   tile; Hq = Hkv, plain multi-head attention, included); other shapes run
- *   on the CUDA cores.  The results agree within the bf16 tolerance either
- *   way.
+ *   D <= 256.  Which kernel runs (the results agree within the bf16
+ *   tolerance either way; Hq = Hkv, plain multi-head attention, included):
+ *   - FP8 cache, D = 128, at most 32 query columns per kv head
+ *     ((Hq/Hkv) s_q), per-shard buffers: tensor cores, FP8 products on the
+ *     codes as stored (query and weights as E4M3 hi + lo pairs);
+ *   - bf16 cache, D = 64 or 128, at most 64 query columns per kv head, per
+ *     shard or paged: tensor cores, bf16 products;
+ *   - fp32 cache, D = 64 or 128, at most 64 query columns per kv head,
+ *     per-shard buffers: tensor cores, tf32 products;
+ *   - every other shape (other head dims, more query columns per kv head, a
+ *     paged FP8 or fp32 pool): CUDA cores.
  * o_part [C, B, H, Dv] fp32 and lse_part [C, B, H] fp32 (normalised partial
  *   outputs; an empty shard gives O = 0, LSE = -inf).
  * ws: workspace of cp_decode_workspace_size() bytes (NULL if that is 0).

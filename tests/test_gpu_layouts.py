@@ -113,11 +113,11 @@ def test_mla_query_rows_tiny_requests(cp):
             check_mla(data, ctx, C, s_q, H, fp8, contiguous, o_part, lse_part, o, lse)
 
 
-def gqa_rows_case(cp, ctx, Hq, Hkv, s_q, contiguous, seed, C=4, n_workers=5, D=128):
+def gqa_rows_case(cp, ctx, Hq, Hkv, s_q, contiguous, seed, C=4, n_workers=5, D=128, dtype="bf16"):
     """GQA decode with s_q query rows per request: every shard's partials and
     the merged rows against the oracle."""
     B = len(ctx)
-    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, "bf16", seed=seed, device=DEV, std=0.3)
+    q, k, v = W.gqa_decode_inputs(B, ctx, Hq * s_q, Hkv, D, dtype, seed=seed, device=DEV, std=0.3)
     plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), s_q=s_q, n_workers=n_workers, device=DEV)
     qq = q.reshape(B, s_q, Hq, D) if s_q > 1 else q
     sk, _ = cp.cp_kv_shard_pack(plan, k)
@@ -162,6 +162,15 @@ def test_gqa_column_widths(cp, Hq, Hkv, s_q, D):
     whose query operands load one kv head at a time."""
     ctx = [s_q, 129, 1000, 2600] + ([0] if s_q == 1 else [])
     gqa_rows_case(cp, ctx, Hq, Hkv, s_q, False, seed=Hq + 3 * Hkv + s_q + D, n_workers=7, D=D)
+
+
+@pytest.mark.parametrize("Hq,Hkv,s_q,D,contiguous", [(8, 2, 2, 64, False), (8, 2, 3, 128, True),
+                                                     (16, 1, 4, 64, False)])
+def test_gqa_fp32_query_rows(cp, Hq, Hkv, s_q, D, contiguous):
+    """fp32 caches on the tf32 GQA decode with several query rows (up to 64
+    columns per kv head) and both shard layouts."""
+    gqa_rows_case(cp, [s_q, 129, 1000, 2600], Hq, Hkv, s_q, contiguous, seed=400 + Hq + s_q + D,
+                  n_workers=7, D=D, dtype="fp32")
 
 
 def test_gqa_full_size_sampled(cp):

@@ -136,6 +136,20 @@ def test_prefill_tiny_fp32(cp):
 
 @pytest.mark.parametrize("strategy", [0, 1])
 @pytest.mark.parametrize("D", [64, 128])
+def test_prefill_fp32_ragged_batch(cp, strategy, D):
+    """fp32 inputs on the tf32 tensor-core prefill: ragged requests with and
+    without a cached prefix, several 128-query M tiles and 128-key tiles,
+    every rank's call alone; held to the bf16 bound."""
+    prefill_vs_oracle(cp, strategy, [300, 1000, 77, 5], [0, 500, 13, 0], 4, 8, 2, D, "fp32",
+                      seed=21 + D + strategy, check_ranks=True)
+
+
+def test_prefill_fp32_sharp_scores(cp):
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, [700, 333], [129, 0], 8, 16, 4, 64, "fp32", seed=98, std=0.35)
+
+
+@pytest.mark.parametrize("strategy", [0, 1])
+@pytest.mark.parametrize("D", [64, 128])
 def test_prefill_bf16_ragged_batch(cp, strategy, D):
     prefill_vs_oracle(cp, strategy, [300, 1000, 77, 5], [0, 500, 13, 0], 4, 8, 2, D, "bf16",
                       seed=7 + D + strategy, check_ranks=True)
@@ -274,6 +288,16 @@ def test_decode_gqa_tiny(cp):
     for nw in (0, 3, 64):
         gqa_decode_case(cp, t["dec_q"], t["dec_k"], t["dec_v"], t["ctx"], w["C"],
                         1.0 / math.sqrt(w["D"]), nw)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,nw", [(16, 4, 128, 6), (8, 2, 64, 0), (32, 1, 64, 7), (64, 1, 128, 5)])
+def test_decode_gqa_fp32(cp, Hq, Hkv, D, nw):
+    """fp32 caches on the tf32 tensor-core GQA decode: ragged requests, empty
+    shards, split pairs, 4 to 64 query columns per kv head; every shard's
+    partial and the merge; held to the bf16 bound."""
+    ctx = [0, 2, 300, 2100]
+    q, k, v = W.gqa_decode_inputs(len(ctx), ctx, Hq, Hkv, D, "fp32", seed=Hq + D, device=DEV, std=0.3)
+    gqa_decode_case(cp, q, k, v, ctx, 8, 1.0 / math.sqrt(D), nw)
 
 
 def test_decode_gqa_bf16_ragged(cp):
