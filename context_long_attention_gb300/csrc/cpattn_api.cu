@@ -900,18 +900,20 @@ constexpr int kMaxTopK = 4096;
 struct TopkWs {
   uint64_t* cand_keys;  // [C * B][k]
   uint64_t* thresh;     // [B]
+  uint64_t* range;      // [C * B]
   int32_t* cand_n;      // [C * B]
 };
 size_t topk_ws_bytes(const cp_plan_header& h, int k) {
   const size_t P = (size_t)h.C * h.R;
-  return P * k * 8 + (size_t)h.R * 8 + ((P * 4 + 15) / 16) * 16;
+  return P * k * 8 + (size_t)h.R * 8 + P * 8 + ((P * 4 + 15) / 16) * 16;
 }
 TopkWs topk_ws(const cp_plan_header& h, int k, void* ws) {
   TopkWs w;
   const size_t P = (size_t)h.C * h.R;
   w.cand_keys = static_cast<uint64_t*>(ws);
   w.thresh = w.cand_keys + P * k;
-  w.cand_n = reinterpret_cast<int32_t*>(w.thresh + h.R);
+  w.range = w.thresh + h.R;
+  w.cand_n = reinterpret_cast<int32_t*>(w.range + P);
   return w;
 }
 cp_status check_topk_args(const cp_plan_header& h, int k) {
@@ -984,9 +986,11 @@ cp_status cp_sparse_topk(const void* host_plan, const void* dev_plan, const floa
   for (int i = 0; i < h.C * h.R; ++i) max_rows = std::max(max_rows, W[h.off_rank + kPairWords * i]);
   const TopkWs w = topk_ws(h, k, ws);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_topk_local((const int32_t*)dev_plan, h, sc, k, max_rows, w.cand_keys, w.cand_n, s);
+  cudaError_t e =
+      launch_topk_local((const int32_t*)dev_plan, h, sc, k, max_rows, w.cand_keys, w.cand_n, w.range, s);
   if (e != cudaSuccess) return cuda_fail(e, "local top-k kernel");
-  e = launch_topk_merge(h, k, w.cand_keys, w.cand_n, w.thresh, sel_ids, sel_count, s);
+  e = launch_topk_merge((const int32_t*)dev_plan, h, k, w.cand_keys, w.cand_n, w.range, w.thresh, sel_ids,
+                        sel_count, s);
   if (e != cudaSuccess) return cuda_fail(e, "top-k merge kernel");
   return ok();
 }

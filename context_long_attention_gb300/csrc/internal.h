@@ -178,11 +178,12 @@ cudaError_t launch_decode_simt(const int32_t* dev_plan, const cp_plan_header& h,
 // ---- sparse decode: exact sharded top-k and the owners' gather (sparse_kernels.cu)
 // Decode kernels given a pair_count (device, one per (shard, request) pair)
 // read only the first pair_count[pair] rows of each pair.
+// range [C * B]: each pair's score range for the merge (hi << 32 | lo, ordered scores).
 cudaError_t launch_topk_local(const int32_t* dev_plan, const cp_plan_header& h, const ScorePtrs& scores,
-                              int k, int max_pair_rows, uint64_t* cand_keys, int32_t* cand_n,
+                              int k, int max_pair_rows, uint64_t* cand_keys, int32_t* cand_n, uint64_t* range,
                               cudaStream_t s);
-cudaError_t launch_topk_merge(const cp_plan_header& h, int k, const uint64_t* cand_keys,
-                              const int32_t* cand_n, uint64_t* thresh, int32_t* sel_ids,
+cudaError_t launch_topk_merge(const int32_t* dev_plan, const cp_plan_header& h, int k, const uint64_t* cand_keys,
+                              const int32_t* cand_n, const uint64_t* range, uint64_t* thresh, int32_t* sel_ids,
                               int32_t* sel_count, cudaStream_t s);
 cudaError_t launch_sparse_gather(const int32_t* dev_plan, const cp_plan_header& h, int k,
                                  const uint64_t* cand_keys, const int32_t* cand_n,

@@ -98,11 +98,33 @@ __device__ int block_collect(int n, Pred pred, Get value, uint64_t* out, int* co
   return *counter;
 }
 
-// Bytes of the merge's token list in shared memory, padded to 16 so that the
-// 64-bit keys staged after it stay aligned.
-__host__ __device__ __forceinline__ size_t ids_bytes(int kpow2) {
-  return ((size_t)kpow2 * sizeof(int32_t) + 15) & ~(size_t)15;
+// Exclusive scan of one count per thread across the block: returns the sum
+// of the counts of the threads before this one, *total the sum of all.  All
+// threads call it; warp_cnt (kWarps ints) must be free on entry, and stays in
+// use until the block's next barrier.
+__device__ int block_excl_scan(int c, int* warp_cnt, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_cnt[warp] = incl;
+  __syncthreads();
+  int at = incl - c, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int v = warp_cnt[w];
+    at += w < warp ? v : 0;
+    tot += v;
+  }
+  *total = tot;
+  return at;
 }
+
+// A shared-memory region's bytes rounded up to 16, so that what follows stays aligned.
+__host__ __device__ __forceinline__ size_t pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
 
 constexpr int kTopBins = 4096;  // the first pass splits on the key's top 12 bits
 
@@ -110,18 +132,29 @@ constexpr int kTopBins = 4096;  // the first pass splits on the key's top 12 bit
 struct __align__(16) SelectSmem {
   uint32_t hist[kTopBins];
   uint32_t pick[4];
+  uint32_t top_bin;  // highest non-empty bin of a first-pass histogram
+  uint32_t umax;
   int small_n;
+  int few_n;
+  int ids_n;
   int warp_cnt[kWarps];
-  int seg_cnt[kWarps];
   uint64_t small[kSmallKeys];
+  uint64_t few[32];
+  uint64_t result;
 };
 
+// Bit words of a staged pair's scores: one bit per score, the scores shifted
+// by up to 3 places and covered in groups of 128.
+constexpr int kStageWords = (kStageScores + 3 + 127) / 128 * 4;
+
 // Finds, among the NB bins of hist taken from the top, the one that holds
-// rank `want` (1-based): pick = {bin, keys in higher bins, keys in it}.  Each
+// rank `want` (1-based): pick = {bin, keys in higher bins, keys in it}, and
+// (top_bin given) the highest bin holding a key.  Each
 // thread owns NB / blockDim consecutive bins (one, or none, when NB is
 // smaller than the block); one block-wide scan.
 template <int NB>
-__device__ void pick_bin(const uint32_t* hist, int want, uint32_t* pick, int* warp_cnt) {
+__device__ void pick_bin(const uint32_t* hist, int want, uint32_t* pick, int* warp_cnt,
+                         uint32_t* top_bin = nullptr) {
   constexpr int PER = NB >= kThreads ? NB / kThreads : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int top = NB - 1 - PER * (int)threadIdx.x;  // this thread's highest bin (< 0: none)
@@ -143,12 +176,27 @@ __device__ void pick_bin(const uint32_t* hist, int want, uint32_t* pick, int* wa
   for (int w = 0; w < warp; ++w) before += (uint32_t)warp_cnt[w];
   const uint32_t excl = before + incl - sum;
   if (excl < (uint32_t)want && (uint32_t)want <= excl + sum) {
-    uint32_t above = excl;
-    int j = 0;
-    for (; j < PER - 1 && above + c[j] < (uint32_t)want; ++j) above += c[j];
-    pick[0] = (uint32_t)(top - j);
+    uint32_t above = excl, in_bin = 0;
+    int jsel = -1;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      if (jsel < 0 && (j == PER - 1 || above + c[j] >= (uint32_t)want)) {
+        jsel = j;
+        in_bin = c[j];
+      } else if (jsel < 0) {
+        above += c[j];
+      }
+    }
+    pick[0] = (uint32_t)(top - jsel);
     pick[1] = above;
-    pick[2] = c[j];
+    pick[2] = in_bin;
+  }
+  if (top_bin && excl == 0 && sum > 0) {  // the first thread from the top with a key
+    int jt = -1;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (jt < 0 && c[j] > 0) jt = j;
+    *top_bin = (uint32_t)(top - jt);
   }
   __syncthreads();
 }
@@ -165,7 +213,7 @@ __device__ uint64_t kth_largest(int n, int k, Get get, Top top12, SelectSmem& sm
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += blockDim.x) atomicAdd(&sm.hist[top12(i)], 1u);
   __syncthreads();
-  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
+  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt, &sm.top_bin);
   uint64_t prefix = (uint64_t)sm.pick[0] << 52, mask = 0xFFFull << 52;
   int want = k - (int)sm.pick[1];
   int in_bin = (int)sm.pick[2];
@@ -195,150 +243,171 @@ __device__ uint64_t kth_largest(int n, int k, Get get, Top top12, SelectSmem& sm
   }
 }
 
-// Sorts a[0, m) (m <= kSmallKeys) in decreasing order, padding to a power
-// of two with zeros (every key is > 0).
-__device__ void sort_desc_small(uint64_t* a, int m) {
-  int mp = 1;
-  while (mp < m) mp <<= 1;
-  for (int i = m + threadIdx.x; i < mp; i += blockDim.x) a[i] = 0;
+// The want-th largest (1 <= want <= m) of m distinct keys a[0, m), m <=
+// kSmallKeys, that agree on the bits `mask` selects (= prefix): 8-bit radix
+// passes from bit sh down narrow the keys still in play to at most 32, which
+// one warp sorts with shuffles.  All threads of the block call it.
+__device__ uint64_t kth_refine(const uint64_t* a, int m, int want, uint64_t prefix, uint64_t mask, int sh,
+                               SelectSmem& sm) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) sm.few_n = 0;
   __syncthreads();
-  for (int size = 2; size <= mp; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < mp; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool down = (i & size) == 0;
-          const uint64_t x = a[i], y = a[j];
-          if ((x < y) == down) {
-            a[i] = y;
-            a[j] = x;
-          }
-        }
-      }
-      __syncthreads();
+  for (int in_play = m; in_play > 32; sh = sh >= 8 ? sh - 8 : 0) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < m; i += blockDim.x) {
+      const uint64_t key = a[i];
+      if ((key & mask) == prefix) atomicAdd(&sm.hist[(key >> sh) & 255u], 1u);
     }
-}
-
-// The want-th largest (1-based) of a[0, m), m <= blockDim: a bitonic sort
-// with one key per thread, through shuffles for strides below 32 and through
-// a (reused) for the larger ones, so that only those stages meet a barrier.
-__device__ uint64_t kth_of_small(uint64_t* a, int m, int want) {
-  const int t = threadIdx.x;
-  int mp = 32;
-  while (mp < m) mp <<= 1;
-  uint64_t v = t < m ? a[t] : 0ull;  // keys are > 0: the padding sorts last
-  __syncthreads();
-  for (int size = 2; size <= mp; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      uint64_t o;
-      if (stride >= 32) {
-        a[t] = v;
-        __syncthreads();
-        o = a[t ^ stride];
-        __syncthreads();
-      } else {
-        o = __shfl_xor_sync(kFull, v, stride);
-      }
-      const bool desc = (t & size) == 0, lower = (t & stride) == 0;
-      v = desc == lower ? (v > o ? v : o) : (v < o ? v : o);
-    }
-  a[t] = v;
-  __syncthreads();
-  return a[want - 1];
-}
-
-// The staged path of a pair's local top-k: stages the scores with a
-// histogram of their top 12 bits, finds the bin holding rank k, collects that
-// bin (at most kSmallKeys keys) while counting, per warp segment, the keys
-// above it, sorts the bin for the k-th key, and writes the candidates in
-// token order: three passes over the scores.  Returns false (scores staged,
-// nothing written) when the bin is larger (many equal scores).
-template <typename Get, typename Top>
-__device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, Get get, Top top12,
-                                  uint64_t* out, SelectSmem& sm, const cp_pair_desc& pd,
-                                  int32_t* n_out) {
-  for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
-  __syncthreads();
-#pragma unroll 8
-  for (int i = threadIdx.x; i < n; i += blockDim.x) {
-    const float f = __ldg(sc + i);
-    staged[i] = f;
-    atomicAdd(&sm.hist[ordered_bits(f) >> 20], 1u);
+    __syncthreads();
+    pick_bin<256>(sm.hist, want, sm.pick, sm.warp_cnt);
+    prefix = (prefix & ~(255ull << sh)) | ((uint64_t)sm.pick[0] << sh);
+    mask |= 255ull << sh;
+    want -= (int)sm.pick[1];
+    in_play = (int)sm.pick[2];
+    if (sh == 0) break;  // all 64 bits fixed (one key)
+  }
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const uint64_t key = a[i];
+    if ((key & mask) == prefix) sm.few[atomicAdd(&sm.few_n, 1)] = key;
   }
   __syncthreads();
-  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
+  if (threadIdx.x < 32) {
+    // bitonic sort of the <= 32 keys in play, decreasing (the padding, 0, sorts last)
+    uint64_t v = lane < sm.few_n ? sm.few[lane] : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint64_t o = __shfl_xor_sync(kFull, v, stride);
+        const bool desc = (lane & size) == 0, lower = (lane & stride) == 0;
+        v = desc == lower ? (v > o ? v : o) : (v < o ? v : o);
+      }
+    if (lane == want - 1) sm.result = v;
+  }
+  __syncthreads();
+  return sm.result;
+}
+
+// The staged path of a pair's local top-k (k < n <= the staging room).
+// Score i is kept at stg[i] = staged[i + pad], pad in [0, 3] chosen so that
+// the source's 16-byte groups land on 16-byte groups of shared memory; the
+// passes work in that shifted index j = i + pad, four scores a thread.
+//   pass 1  stage the scores with a histogram of their top 12 bits; the bin
+//           holding rank k is found from it;
+//   pass 2  one bit per score for those in higher bins, and the bin's keys
+//           collected; the bin's want-th key is the threshold, and the bin's
+//           keys at or above it get their bits too;
+//   pass 3  the marked scores' keys written in token order (a scan of the
+//           bit words' counts gives each thread its place).
+// Returns false (scores staged, nothing written) when the bin holds more than
+// kSmallKeys keys (many equal scores).
+__device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, uint32_t* bits, uint64_t* out,
+                                  SelectSmem& sm, const cp_pair_desc& pd, int32_t* n_out, uint64_t* range_out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int head = (int)((16u - ((uint32_t)(uintptr_t)sc & 15u)) & 15u) >> 2;  // scores before a 16-byte boundary
+  const int pad = (4 - head) & 3;
+  float* stg = staged + pad;
+  for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
+  if (threadIdx.x == 0) sm.small_n = 0;
+  __syncthreads();
+  const int h = min(head, n);
+  const int nv = (n - h) >> 2;
+  const float4* src4 = reinterpret_cast<const float4*>(sc + h);
+  float4* dst4 = reinterpret_cast<float4*>(stg + h);  // pad + h is a multiple of 4 whenever nv > 0
+#pragma unroll 8
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const float4 f = __ldg(src4 + v);
+    dst4[v] = f;
+    atomicAdd(&sm.hist[ordered_bits(f.x) >> 20], 1u);
+    atomicAdd(&sm.hist[ordered_bits(f.y) >> 20], 1u);
+    atomicAdd(&sm.hist[ordered_bits(f.z) >> 20], 1u);
+    atomicAdd(&sm.hist[ordered_bits(f.w) >> 20], 1u);
+  }
+  {  // the scalars before and after the groups of four (at most 3 each)
+    const int rest = h + 4 * nv;
+    int i = -1;
+    if ((int)threadIdx.x < h) i = threadIdx.x;
+    else if ((int)threadIdx.x - h < n - rest) i = rest + (int)threadIdx.x - h;
+    if (i >= 0) {
+      const float f = __ldg(sc + i);
+      stg[i] = f;
+      atomicAdd(&sm.hist[ordered_bits(f) >> 20], 1u);
+    }
+  }
+  __syncthreads();
+  pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt, &sm.top_bin);
   const uint32_t bin = sm.pick[0];
   const int want = k - (int)sm.pick[1];
   if ((int)sm.pick[2] > kSmallKeys) return false;
-  // warp w classifies keys [w seg, (w + 1) seg) in steps of 32
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = (n + kWarps * 32 - 1) / (kWarps * 32) * 32;
-  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-  if (threadIdx.x == 0) sm.small_n = 0;
-  __syncthreads();
-  int above = 0;
-#pragma unroll 4
-  for (int b = s0; b < s1; b += 32) {
-    const int i = b + lane;
-    const uint32_t t = i < s1 ? top12(i) : 0u;
-    above += __popc(__ballot_sync(kFull, i < s1 && t > bin));
-    const bool in = i < s1 && t == bin;
-    const unsigned bal = __ballot_sync(kFull, in);
-    if (bal) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&sm.small_n, __popc(bal));
-      base = __shfl_sync(kFull, base, 0);
-      if (in) sm.small[base + __popc(bal & ((1u << lane) - 1u))] = get(i);
+  const int J = pad + n, Q = (J + 127) >> 7;  // groups of 128 shifted indices
+  const float4* s4 = reinterpret_cast<const float4*>(staged);
+  for (int q = warp; q < Q; q += kWarps) {
+    const float4 f = s4[32 * q + lane];
+    const float fv[4] = {f.x, f.y, f.z, f.w};
+    const int j0 = 128 * q + 4 * lane;
+    uint32_t nib = 0, in_bin = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      const bool valid = j >= pad && j < J;
+      const uint32_t t = ordered_bits(fv[e]) >> 20;
+      if (valid && t > bin) nib |= 1u << e;
+      if (valid && t == bin) in_bin |= 1u << e;
     }
+    if (in_bin) {
+      const int tok = pd.tok0 + (j0 - pad) * pd.tok_step;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (in_bin & (1u << e)) sm.small[atomicAdd(&sm.small_n, 1)] = token_key(fv[e], tok + e * pd.tok_step);
+    }
+    // lanes 8w .. 8w + 7 hold the 32 bits of word 4q + w
+    uint32_t word = nib << (4 * (lane & 7));
+    word |= __shfl_xor_sync(kFull, word, 1);
+    word |= __shfl_xor_sync(kFull, word, 2);
+    word |= __shfl_xor_sync(kFull, word, 4);
+    if ((lane & 7) == 0) bits[4 * q + (lane >> 3)] = word;
   }
-  if (lane == 0) sm.seg_cnt[warp] = above;
   __syncthreads();
   const int m = sm.small_n;
-  // the bin's keys that make it, counted into their warps' segments
-  uint64_t thresh;
-  if (m <= kThreads) {
-    const uint64_t mine = threadIdx.x < m ? sm.small[threadIdx.x] : 0ull;
-    thresh = kth_of_small(sm.small, m, want);
-    if (mine >= thresh && threadIdx.x < m)
-      atomicAdd(&sm.seg_cnt[((key_token(mine) - pd.tok0) / pd.tok_step) / seg], 1);
-  } else {
-    sort_desc_small(sm.small, m);
-    thresh = sm.small[want - 1];
-    for (int j = threadIdx.x; j < m; j += blockDim.x) {
-      const uint64_t key = sm.small[j];
-      if (key >= thresh) atomicAdd(&sm.seg_cnt[((key_token(key) - pd.tok0) / pd.tok_step) / seg], 1);
+  const uint64_t thresh = kth_refine(sm.small, m, want, (uint64_t)bin << 52, 0xFFFull << 52, 44, sm);
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const uint64_t key = sm.small[i];
+    if (key >= thresh) {
+      const int j = (key_token(key) - pd.tok0) / pd.tok_step + pad;
+      atomicOr(&bits[j >> 5], 1u << (j & 31));
     }
   }
   __syncthreads();
-  int at = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int c = sm.seg_cnt[w];
-    at += w < warp ? c : 0;
-    tot += c;
-  }
-  const uint32_t th_hi = (uint32_t)(thresh >> 32), th_lo = (uint32_t)thresh;
-#pragma unroll 4
-  for (int b = s0; b < s1; b += 32) {
-    const int i = b + lane;
-    bool keep = false;
-    if (i < s1) {
-      const uint32_t hi = ordered_bits(staged[i]);
-      keep = hi > th_hi || (hi == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
+  // pass 3: thread t takes words [t per, (t + 1) per)
+  const int W = 4 * Q;
+  const int per = (W + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int w0 = min(W, (int)threadIdx.x * per), w1 = min(W, w0 + per);
+  int c = 0;
+  for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
+  int tot;
+  int at = block_excl_scan(c, sm.warp_cnt, &tot);
+  for (int w = w0; w < w1; ++w) {
+    for (uint32_t word = bits[w]; word; word &= word - 1u) {
+      const int j = 32 * w + __ffs(word) - 1;
+      out[at++] = token_key(staged[j], pd.tok0 + (j - pad) * pd.tok_step);
     }
-    const unsigned bal = __ballot_sync(kFull, keep);
-    if (keep) out[at + __popc(bal & ((1u << lane) - 1u))] = get(i);
-    at += __popc(bal);
   }
-  if (threadIdx.x == 0) *n_out = tot;
+  if (threadIdx.x == 0) {
+    *n_out = tot;
+    *range_out = (uint64_t)((sm.top_bin << 20) | 0xFFFFFu) << 32 | (uint32_t)(thresh >> 32);
+  }
   return true;
 }
 
-// Local top-k of every (shard, request) pair: candidate keys in token order.
+// Local top-k of every (shard, request) pair: candidate keys in token order,
+// and the pair's score range for the merge: range = hi << 32 | lo, hi at or
+// above every candidate's ordered score, lo the ordered score of the k-th key
+// when the pair had more than k rows (else 0, no bound).
 __global__ void __launch_bounds__(kThreads)
     topk_local_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                       ScorePtrs scores, int k, int stage_cap, uint64_t* __restrict__ cand_keys,
-                      int32_t* __restrict__ cand_n) {
+                      int32_t* __restrict__ cand_n, uint64_t* __restrict__ range) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
   const int pair = blockIdx.x;
@@ -349,112 +418,230 @@ __global__ void __launch_bounds__(kThreads)
   // Every pass reads the pair's scores: stage them in shared memory once,
   // eight independent loads in flight per thread (the passes would otherwise
   // wait out an L2 round trip per element).
-  float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem));
+  uint32_t* bits = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelectSmem));
+  float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem) + kStageWords * sizeof(uint32_t));
   const bool st = n <= stage_cap && n > k;  // staged by the fast path below
-  auto score = [&](int i) { return st ? staged[i] : __ldg(sc + i); };
+  const int pad = (4 - ((int)((16u - ((uint32_t)(uintptr_t)sc & 15u)) & 15u) >> 2)) & 3;
+  auto score = [&](int i) { return st ? staged[pad + i] : __ldg(sc + i); };
   auto get = [&](int i) { return token_key(score(i), pd.tok0 + i * pd.tok_step); };
   auto top12 = [&](int i) { return ordered_bits(score(i)) >> 20; };
   uint64_t* out = cand_keys + (long long)pair * k;
-  if (st && n > k && local_topk_staged(n, k, sc, staged, get, top12, out, sm, pd, cand_n + pair)) return;
-  const uint64_t thresh = n > k ? kth_largest(n, k, get, top12, sm) : 0ull;
+  if (st && local_topk_staged(n, k, sc, staged, bits, out, sm, pd, cand_n + pair, range + pair)) return;
+  uint64_t thresh = 0;
+  uint32_t hi;
+  if (n > k) {
+    thresh = kth_largest(n, k, get, top12, sm);
+    hi = (sm.top_bin << 20) | 0xFFFFFu;
+  } else {  // every row is a candidate: the largest ordered score
+    if (threadIdx.x == 0) sm.umax = 0;
+    __syncthreads();
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = max(m, ordered_bits(score(i)));
+    m = __reduce_max_sync(kFull, m);
+    if ((threadIdx.x & 31) == 0) atomicMax(&sm.umax, m);
+    __syncthreads();
+    hi = sm.umax;
+  }
   // the candidates in token order (the comparison split into two 32-bit halves)
   const uint32_t th_hi = (uint32_t)(thresh >> 32), th_lo = (uint32_t)thresh;
   auto keep = [&](int i) {
-    const uint32_t hi = ordered_bits(score(i));
-    return hi > th_hi || (hi == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
+    const uint32_t u = ordered_bits(score(i));
+    return u > th_hi || (u == th_hi && 0xFFFFFFFFu - (uint32_t)(pd.tok0 + i * pd.tok_step) >= th_lo);
   };
   const int got = block_compact(n, keep, [&](int i, int j) { out[j] = get(i); }, sm.warp_cnt);
-  if (threadIdx.x == 0) cand_n[pair] = got;
+  if (threadIdx.x == 0) {
+    cand_n[pair] = got;
+    range[pair] = (uint64_t)hi << 32 | th_hi;
+  }
 }
 
 // Merge of one request's candidates: the global k-th key (the selection
 // threshold) and the selected tokens in increasing order.
+//
+// The threshold.  A shard that had more than k rows sent k candidates, all at
+// or above its k-th key, so the global k-th key is at least the largest of
+// those shards' k-th keys; lo, its ordered score, bounds the keys in play from
+// below, and hi, the largest of the shards' upper bounds, from above.  The
+// first histogram cuts [lo, hi] into kTopBins equal slices (a shift of u - lo)
+// as the candidates are staged, so that the bin holding rank k is narrow even
+// when the candidates share their top bits.  A second pass collects the
+// tokens of the bins above it and the keys of that bin, whose want-th key
+// (kth_refine) is the threshold.  A bin of more than kSmallKeys keys (many
+// equal scores) goes to the general radix select instead.
+// The order.  The selected tokens are set as bits of a bitmap over token
+// indices (kSortTokens of them at a time, in the histogram's words), whose
+// scan gives every token its place: no sort.
+constexpr int kSortTokens = kTopBins * 32;
+
 __global__ void __launch_bounds__(kThreads)
-    topk_merge_kernel(int C, int B, int k, int kpow2, const uint64_t* __restrict__ cand_keys,
-                      const int32_t* __restrict__ cand_n, int stage_cap, uint64_t* __restrict__ thresh,
+    topk_merge_kernel(const int32_t* __restrict__ plan, int off_pair, int C, int B, int k,
+                      const uint64_t* __restrict__ cand_keys, const int32_t* __restrict__ cand_n,
+                      const uint64_t* __restrict__ range, int stage_cap, uint64_t* __restrict__ thresh,
                       int32_t* __restrict__ sel_ids, int32_t* __restrict__ sel_count) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
-  int32_t* ids = reinterpret_cast<int32_t*>(smem_raw + sizeof(SelectSmem));  // kpow2 entries
-  __shared__ int start[CP_MAX_SHARDS + 1];
-  __shared__ int n_sel;
+  int32_t* ids = reinterpret_cast<int32_t*>(smem_raw + sizeof(SelectSmem));  // selected tokens, any order
+  uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + pad16((size_t)k * 4));
+  __shared__ int start[CP_MAX_SHARDS + 1];  // shard r's candidates: [start[r], start[r + 1])
+  __shared__ uint32_t lo_s, hi_s;
   const int b = blockIdx.x;
-  if (threadIdx.x == 0) {
-    int s = 0;
-    for (int r = 0; r < C; ++r) {
-      start[r] = s;
-      s += cand_n[r * B + b];
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {  // warp 0: the shards' counts (a scan) and ranges, two shards a lane
+    int n0 = 0, n1 = 0;
+    uint64_t g0 = 0, g1 = 0;
+    if (lane < C) {
+      n0 = cand_n[lane * B + b];
+      g0 = range[lane * B + b];
     }
-    start[C] = s;
-    n_sel = 0;
+    if (lane + 32 < C) {
+      n1 = cand_n[(lane + 32) * B + b];
+      g1 = range[(lane + 32) * B + b];
+    }
+    int i0 = n0, i1 = n1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v0 = __shfl_up_sync(kFull, i0, d), v1 = __shfl_up_sync(kFull, i1, d);
+      if (lane >= d) {
+        i0 += v0;
+        i1 += v1;
+      }
+    }
+    const int tot0 = __shfl_sync(kFull, i0, 31);
+    if (lane < C) start[lane] = i0 - n0;
+    if (lane + 32 < C) start[lane + 32] = tot0 + i1 - n1;
+    if (lane == 31) start[C] = tot0 + i1;
+    // hi: the largest bound; lo: the largest k-th key (0: no bound from that shard)
+    const uint32_t hi = __reduce_max_sync(kFull, max(n0 ? (uint32_t)(g0 >> 32) : 0u, n1 ? (uint32_t)(g1 >> 32) : 0u));
+    const uint32_t lo = __reduce_max_sync(kFull, max(n0 ? (uint32_t)g0 : 0u, n1 ? (uint32_t)g1 : 0u));
+    if (lane == 0) {
+      lo_s = lo;  // 0 when no shard bounds it: every candidate in play
+      hi_s = max(hi, lo);
+      sm.ids_n = 0;
+    }
   }
+  for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
   __syncthreads();
   const int N = start[C];
+  const uint32_t lo = lo_s;
+  const int sh = max(0, 32 - __clz(hi_s - lo) - 12);  // (hi - lo) >> sh < kTopBins
+  auto bin_of = [&](uint32_t u) { return min((u - lo) >> sh, (uint32_t)kTopBins - 1u); };
+  const bool st = N <= stage_cap;
+  const bool select = N > k;  // else every candidate is selected (threshold 0)
+  // pass 1: stage the candidates (when they fit), counting those in play;
+  // entry idx of the flattened [C][k] lists is row i = idx - r k of shard
+  // r = idx / k (a float estimate, corrected: no divide, no branch)
+  {
+    const float inv_k = 1.0f / (float)k;
+#pragma unroll 8
+    for (int idx = threadIdx.x; idx < C * k; idx += blockDim.x) {
+      int r = (int)((float)idx * inv_k);
+      r -= r * k > idx ? 1 : 0;
+      r += (r + 1) * k <= idx ? 1 : 0;
+      const int i = idx - r * k;
+      const uint64_t key = cand_keys[(long long)(r * B + b) * k + i];  // past the count: unused
+      if (i < start[r + 1] - start[r]) {
+        if (st) staged[start[r] + i] = key;
+        const uint32_t u = (uint32_t)(key >> 32);
+        if (select && u >= lo) atomicAdd(&sm.hist[bin_of(u)], 1u);
+      }
+    }
+  }
+  __syncthreads();
   auto get_global = [&](int i) {
     int r = 0;
     while (start[r + 1] <= i) ++r;
     return cand_keys[(long long)(r * B + b) * k + (i - start[r])];
   };
-  // stage the candidates in shared memory when they fit (see topk_local_kernel)
-  uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + ids_bytes(kpow2));
-  const bool st = N <= stage_cap;
-  if (st) {
-    // stage the candidates with a histogram of their top 12 bits
-    for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
-    __syncthreads();
-    for (int r = 0; r < C; ++r) {
-      const uint64_t* src = cand_keys + (long long)(r * B + b) * k;
-      const int n_r = start[r + 1] - start[r];
-#pragma unroll 8
-      for (int i = threadIdx.x; i < n_r; i += blockDim.x) {
-        const uint64_t key = src[i];
-        staged[start[r] + i] = key;
-        atomicAdd(&sm.hist[key >> 52], 1u);
-      }
-    }
-    __syncthreads();
-  }
   auto get = [&](int i) { return st ? staged[i] : get_global(i); };
-  auto top12 = [&](int i) { return (uint32_t)(get(i) >> 52); };
+  // append tokens to ids (one shared counter update per warp and step)
+  auto append = [&](bool f, int token) {
+    const unsigned bal = __ballot_sync(kFull, f);
+    if (!bal) return;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sm.ids_n, __popc(bal));
+    base = __shfl_sync(kFull, base, 0);
+    if (f) ids[base + __popc(bal & ((1u << lane) - 1u))] = token;
+  };
+  const int n_pad = (N + 31) & ~31;  // whole warps in the passes that append
   uint64_t t = 0;
-  bool found = N <= k;  // then every candidate is selected (t = 0)
-  if (!found && st) {
-    // the bin of rank k, collected and sorted when it is small (else the general path)
+  bool done = false;
+  if (select) {
     pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
     const uint32_t bin = sm.pick[0];
     const int want = k - (int)sm.pick[1];
-    if ((int)sm.pick[2] <= kThreads) {
-      const int m = block_collect(N, [&](int i) { return top12(i) == bin; }, get, sm.small, &sm.small_n);
-      t = kth_of_small(sm.small, m, want);
-      found = true;
-    }
-  }
-  if (!found) t = kth_largest(N, k, get, top12, sm);
-  for (int i = threadIdx.x; i < kpow2; i += blockDim.x) ids[i] = 0x7FFFFFFF;
-  __syncthreads();
-  const int got = block_compact(
-      N, [&](int i) { return get(i) >= t; }, [&](int i, int j) { ids[j] = key_token(get(i)); },
-      sm.warp_cnt);
-  if (threadIdx.x == 0) n_sel = got;
-  __syncthreads();
-  // bitonic sort of the selected token indices, ascending
-  for (int size = 2; size <= kpow2; size <<= 1)
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < kpow2; i += blockDim.x) {
-        const int j = i ^ stride;
-        if (j > i) {
-          const bool up = (i & size) == 0;
-          const int a = ids[i], c = ids[j];
-          if ((a > c) == up) {
-            ids[i] = c;
-            ids[j] = a;
+    if ((int)sm.pick[2] <= kSmallKeys) {
+      // pass 2: tokens of the higher bins to ids, keys of the bin to small
+      if (threadIdx.x == 0) sm.small_n = 0;
+      __syncthreads();
+      auto pass2 = [&](auto key_at) {
+        for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+          uint64_t key = 0;
+          uint32_t bi = 0;
+          bool in_play = false;
+          if (i < N) {
+            key = key_at(i);
+            const uint32_t u = (uint32_t)(key >> 32);
+            in_play = u >= lo;
+            bi = bin_of(u);
+          }
+          append(in_play && bi > bin, key_token(key));
+          const bool mine = in_play && bi == bin;
+          const unsigned bal = __ballot_sync(kFull, mine);
+          if (bal) {
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sm.small_n, __popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            if (mine) sm.small[base + __popc(bal & ((1u << lane) - 1u))] = key;
           }
         }
-      }
+      };
+      if (st) pass2([&](int i) { return staged[i]; });
+      else pass2(get_global);
       __syncthreads();
+      const int m = sm.small_n;
+      t = kth_refine(sm.small, m, want, 0ull, 0ull, 56, sm);
+      for (int i = threadIdx.x; i < ((m + 31) & ~31); i += blockDim.x) {
+        const uint64_t key = i < m ? sm.small[i] : 0ull;
+        append(i < m && key >= t, key_token(key));
+      }
+      done = true;
+    } else {
+      t = kth_largest(N, k, get, [&](int i) { return (uint32_t)(get(i) >> 52); }, sm);
     }
-  const int cnt = n_sel;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) sel_ids[(long long)b * k + i] = i < cnt ? ids[i] : -1;
+  }
+  if (!done)  // every key at or above t
+    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
+      const uint64_t key = i < N ? get(i) : 0ull;
+      append(i < N && key >= t, key_token(key));
+    }
+  __syncthreads();
+  const int cnt = sm.ids_n;
+  // the selected tokens in increasing order, kSortTokens token indices at a time
+  const int L = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[b].ctx_len;  // tokens are < L
+  uint32_t* bmp = sm.hist;
+  int32_t* out = sel_ids + (long long)b * k;
+  int placed = 0;
+  for (int t0 = 0; t0 < L && placed < cnt; t0 += kSortTokens) {
+    const int words = (min(L - t0, kSortTokens) + 31) >> 5;
+    for (int w = threadIdx.x; w < words; w += blockDim.x) bmp[w] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
+      const int tok = ids[j] - t0;
+      if (tok >= 0 && tok < kSortTokens) atomicOr(&bmp[tok >> 5], 1u << (tok & 31));
+    }
+    __syncthreads();
+    const int per = (words + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int w0 = min(words, (int)threadIdx.x * per), w1 = min(words, w0 + per);
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(bmp[w]);
+    int tot;
+    int at = placed + block_excl_scan(c, sm.warp_cnt, &tot);
+    for (int w = w0; w < w1; ++w)
+      for (uint32_t word = bmp[w]; word; word &= word - 1u) out[at++] = t0 + 32 * w + __ffs(word) - 1;
+    placed += tot;
+    __syncthreads();
+  }
+  for (int i = cnt + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
   if (threadIdx.x == 0) {
     sel_count[b] = cnt;
     thresh[b] = t;
@@ -510,31 +697,30 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_topk_local(const int32_t* dev_plan, const cp_plan_header& h, const ScorePtrs& scores,
-                              int k, int max_pair_rows, uint64_t* cand_keys, int32_t* cand_n,
+                              int k, int max_pair_rows, uint64_t* cand_keys, int32_t* cand_n, uint64_t* range,
                               cudaStream_t s) {
   const int pairs = h.C * h.R;
   // room to stage the longest pair's scores, up to kStageScores (longer pairs read from L2)
   const int cap = max_pair_rows < kStageScores ? max_pair_rows : kStageScores;
-  const int smem = (int)sizeof(SelectSmem) + cap * (int)sizeof(float);
+  const int smem = (int)sizeof(SelectSmem) + kStageWords * (int)sizeof(uint32_t) +
+                   (cap + 3 + 127) / 128 * 128 * (int)sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(topk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   topk_local_kernel<<<pairs, kThreads, smem, s>>>(dev_plan, h.R, h.off_rank, scores, k, cap, cand_keys,
-                                                  cand_n);
+                                                  cand_n, range);
   return cudaGetLastError();
 }
 
-cudaError_t launch_topk_merge(const cp_plan_header& h, int k, const uint64_t* cand_keys,
-                              const int32_t* cand_n, uint64_t* thresh, int32_t* sel_ids,
+cudaError_t launch_topk_merge(const int32_t* dev_plan, const cp_plan_header& h, int k, const uint64_t* cand_keys,
+                              const int32_t* cand_n, const uint64_t* range, uint64_t* thresh, int32_t* sel_ids,
                               int32_t* sel_count, cudaStream_t s) {
-  int kpow2 = 1;
-  while (kpow2 < k) kpow2 <<= 1;
   const int cap = h.C * k < kStageKeys ? h.C * k : kStageKeys;
-  const size_t smem = sizeof(SelectSmem) + ids_bytes(kpow2) + (size_t)cap * sizeof(uint64_t);
+  const size_t smem = sizeof(SelectSmem) + pad16((size_t)k * 4) + (size_t)cap * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<h.R, kThreads, smem, s>>>(h.C, h.R, k, kpow2, cand_keys, cand_n, cap, thresh,
-                                                 sel_ids, sel_count);
+  topk_merge_kernel<<<h.R, kThreads, smem, s>>>(dev_plan, h.off_rank, h.C, h.R, k, cand_keys, cand_n, range,
+                                                 cap, thresh, sel_ids, sel_count);
   return cudaGetLastError();
 }
 

@@ -25,13 +25,11 @@ def shard_scores(scores, ctx, C, plan, contiguous):
     """Each shard's scores in its row order, placed by the oracle's map."""
     s = scores.cpu().numpy()
     base = np.concatenate([[0], np.cumsum(ctx)])
+    maps = [np.asarray(token_map(L, C, contiguous)[0], dtype=np.int64) for L in ctx]
     out = []
     for r in range(C):
-        rows = []
-        for b, L in enumerate(ctx):
-            shard, _ = token_map(L, C, contiguous)
-            rows += [base[b] + p for p in range(L) if shard[p] == r]
-        out.append(torch.from_numpy(s[np.asarray(rows, dtype=np.int64)].copy()).to(DEV))
+        rows = np.concatenate([base[b] + np.nonzero(m == r)[0] for b, m in enumerate(maps)]).astype(np.int64)
+        out.append(torch.from_numpy(s[rows].copy()).to(DEV))
         assert out[-1].shape[0] == sum(int(plan.pairs[r * len(ctx) + b, 0]) for b in range(len(ctx)))
     return out
 
@@ -63,6 +61,29 @@ def test_topk_bit_exact(cp, contiguous, ties, C, k):
         if L <= 4100:  # brute force over the whole request
             sb = s[base[b]:base[b] + L]
             assert want[b] == sorted(sorted(range(L), key=lambda p: (-float(sb[p]), p))[:k])
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("C,k", [(1, 100), (2, 3000), (8, 4096)])
+def test_topk_unstaged(cp, contiguous, ties, C, k):
+    """Pairs longer than the 32,768 scores a block stages, requests whose C k
+    candidates pass the 16,384 the merge stages, and a context past the
+    131,072 token indices the merge orders at a time: the same exact selection."""
+    ctx = [200003, 70001, 40000, 33]
+    scores = W.index_scores(ctx, seed=C * 7 + k, device=DEV, ties=ties)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), device=DEV)
+    sel, cnt, _ = cp.cp_sparse_topk(plan, shard_scores(scores, ctx, C, plan, contiguous), k)
+    cp.cp_device_error_check()
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    s = scores.cpu().numpy()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    for b, L in enumerate(ctx):
+        sb = s[base[b]:base[b] + L]
+        order = np.lexsort((np.arange(L), -sb.astype(np.float64)))
+        assert cnt[b] == min(k, L)
+        assert sel[b, :cnt[b]].tolist() == sorted(order[:k].tolist()), f"request {b}"
+        assert np.all(sel[b, cnt[b]:] == -1)
 
 
 def test_topk_full_size_sampled(cp):
