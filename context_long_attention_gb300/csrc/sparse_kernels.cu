@@ -34,6 +34,14 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The least float f with ordered_bits(f) >= v: codes up to -inf's (those
+// below it belong to no number) give -inf, codes above +inf's give NaN, which
+// no comparison passes.
+__device__ __forceinline__ float from_ordered(uint32_t v) {
+  if (v <= 0x007FFFFFu) return -INFINITY;
+  return __uint_as_float((v & 0x80000000u) ? (v & 0x7FFFFFFFu) : ~v);
+}
+
 __device__ __forceinline__ uint64_t token_key(float score, int token) {
   return ((uint64_t)ordered_bits(score) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)token);
 }
@@ -123,9 +131,6 @@ __device__ int block_excl_scan(int c, int* warp_cnt, int* total) {
   return at;
 }
 
-// A shared-memory region's bytes rounded up to 16, so that what follows stays aligned.
-__host__ __device__ __forceinline__ size_t pad16(size_t bytes) { return (bytes + 15) & ~(size_t)15; }
-
 constexpr int kTopBins = 4096;  // the first pass splits on the key's top 12 bits
 
 // Shared scratch of the radix select.
@@ -144,7 +149,8 @@ struct __align__(16) SelectSmem {
 };
 
 // Bit words of a staged pair's scores: one bit per score, the scores shifted
-// by up to 3 places and covered in groups of 128.
+// by up to 3 places and covered in groups of 128 (two such arrays: the
+// scores above the rank-k bin, and those in it).
 constexpr int kStageWords = (kStageScores + 3 + 127) / 128 * 4;
 
 // Finds, among the NB bins of hist taken from the top, the one that holds
@@ -292,12 +298,15 @@ __device__ uint64_t kth_refine(const uint64_t* a, int m, int want, uint64_t pref
 // The staged path of a pair's local top-k (k < n <= the staging room).
 // Score i is kept at stg[i] = staged[i + pad], pad in [0, 3] chosen so that
 // the source's 16-byte groups land on 16-byte groups of shared memory; the
-// passes work in that shifted index j = i + pad, four scores a thread.
+// passes work in that shifted index j = i + pad, four scores a thread, over
+// whole groups of 128 (the places before pad and past pad + n hold NaN, which
+// no comparison passes).
 //   pass 1  stage the scores with a histogram of their top 12 bits; the bin
 //           holding rank k is found from it;
-//   pass 2  one bit per score for those in higher bins, and the bin's keys
-//           collected; the bin's want-th key is the threshold, and the bin's
-//           keys at or above it get their bits too;
+//   pass 2  one bit per score above the bin and one per score in it (float
+//           comparisons against the bin's bounds); the bin's keys are
+//           collected from their bits, its want-th key is the threshold, and
+//           the bin's keys at or above it join the first bits;
 //   pass 3  the marked scores' keys written in token order (a scan of the
 //           bit words' counts gives each thread its place).
 // Returns false (scores staged, nothing written) when the bin holds more than
@@ -307,9 +316,12 @@ __device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int head = (int)((16u - ((uint32_t)(uintptr_t)sc & 15u)) & 15u) >> 2;  // scores before a 16-byte boundary
   const int pad = (4 - head) & 3;
+  const int J = pad + n, Q = (J + 127) >> 7;  // groups of 128 shifted indices
+  uint32_t* in_bits = bits + kStageWords;
   float* stg = staged + pad;
   for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
-  if (threadIdx.x == 0) sm.small_n = 0;
+  for (int j = threadIdx.x; j < pad; j += blockDim.x) staged[j] = __uint_as_float(0x7FFFFFFFu);
+  for (int j = J + threadIdx.x; j < 128 * Q; j += blockDim.x) staged[j] = __uint_as_float(0x7FFFFFFFu);
   __syncthreads();
   const int h = min(head, n);
   const int nv = (n - h) >> 2;
@@ -340,33 +352,46 @@ __device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, 
   const uint32_t bin = sm.pick[0];
   const int want = k - (int)sm.pick[1];
   if ((int)sm.pick[2] > kSmallKeys) return false;
-  const int J = pad + n, Q = (J + 127) >> 7;  // groups of 128 shifted indices
+  // the bin's scores are [f_lo, f_hi) (f_hi NaN for the top bin: nothing above it)
+  const float f_lo = from_ordered(bin << 20);
+  const float f_hi = bin + 1 < (uint32_t)kTopBins ? from_ordered((bin + 1) << 20) : __uint_as_float(0x7FFFFFFFu);
   const float4* s4 = reinterpret_cast<const float4*>(staged);
   for (int q = warp; q < Q; q += kWarps) {
     const float4 f = s4[32 * q + lane];
-    const float fv[4] = {f.x, f.y, f.z, f.w};
-    const int j0 = 128 * q + 4 * lane;
-    uint32_t nib = 0, in_bin = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j0 + e;
-      const bool valid = j >= pad && j < J;
-      const uint32_t t = ordered_bits(fv[e]) >> 20;
-      if (valid && t > bin) nib |= 1u << e;
-      if (valid && t == bin) in_bin |= 1u << e;
-    }
-    if (in_bin) {
-      const int tok = pd.tok0 + (j0 - pad) * pd.tok_step;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (in_bin & (1u << e)) sm.small[atomicAdd(&sm.small_n, 1)] = token_key(fv[e], tok + e * pd.tok_step);
-    }
+    const uint32_t up = (f.x >= f_hi ? 1u : 0u) | (f.y >= f_hi ? 2u : 0u) | (f.z >= f_hi ? 4u : 0u) |
+                        (f.w >= f_hi ? 8u : 0u);
+    const uint32_t at_least = (f.x >= f_lo ? 1u : 0u) | (f.y >= f_lo ? 2u : 0u) | (f.z >= f_lo ? 4u : 0u) |
+                              (f.w >= f_lo ? 8u : 0u);
     // lanes 8w .. 8w + 7 hold the 32 bits of word 4q + w
-    uint32_t word = nib << (4 * (lane & 7));
-    word |= __shfl_xor_sync(kFull, word, 1);
-    word |= __shfl_xor_sync(kFull, word, 2);
-    word |= __shfl_xor_sync(kFull, word, 4);
-    if ((lane & 7) == 0) bits[4 * q + (lane >> 3)] = word;
+    const int sh4 = 4 * (lane & 7);
+    uint32_t wa = up << sh4, wb = (at_least & ~up) << sh4;
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+      wa |= __shfl_xor_sync(kFull, wa, d);
+      wb |= __shfl_xor_sync(kFull, wb, d);
+    }
+    if ((lane & 7) == 0) {
+      bits[4 * q + (lane >> 3)] = wa;
+      in_bits[4 * q + (lane >> 3)] = wb;
+    }
+  }
+  __syncthreads();
+  // the bin's keys, collected in index order from their bits (thread t takes words [t per, (t + 1) per))
+  const int W = 4 * Q;
+  const int per = (W + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int w0 = min(W, (int)threadIdx.x * per), w1 = min(W, w0 + per);
+  {
+    int c = 0;
+    for (int w = w0; w < w1; ++w) c += __popc(in_bits[w]);
+    int m_all;
+    int at = block_excl_scan(c, sm.warp_cnt, &m_all);
+    for (int w = w0; w < w1; ++w)
+      for (uint32_t word = in_bits[w]; word; word &= word - 1u) {
+        const int j = 32 * w + __ffs(word) - 1;
+        if (at < kSmallKeys) sm.small[at] = token_key(staged[j], pd.tok0 + (j - pad) * pd.tok_step);
+        ++at;
+      }
+    if (threadIdx.x == 0) sm.small_n = min(m_all, kSmallKeys);  // m_all is the bin's count, at most kSmallKeys
   }
   __syncthreads();
   const int m = sm.small_n;
@@ -379,10 +404,7 @@ __device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, 
     }
   }
   __syncthreads();
-  // pass 3: thread t takes words [t per, (t + 1) per)
-  const int W = 4 * Q;
-  const int per = (W + (int)blockDim.x - 1) / (int)blockDim.x;
-  const int w0 = min(W, (int)threadIdx.x * per), w1 = min(W, w0 + per);
+  // pass 3
   int c = 0;
   for (int w = w0; w < w1; ++w) c += __popc(bits[w]);
   int tot;
@@ -390,11 +412,12 @@ __device__ bool local_topk_staged(int n, int k, const float* sc, float* staged, 
   for (int w = w0; w < w1; ++w) {
     for (uint32_t word = bits[w]; word; word &= word - 1u) {
       const int j = 32 * w + __ffs(word) - 1;
-      out[at++] = token_key(staged[j], pd.tok0 + (j - pad) * pd.tok_step);
+      if (at < k) out[at] = token_key(staged[j], pd.tok0 + (j - pad) * pd.tok_step);
+      ++at;
     }
   }
   if (threadIdx.x == 0) {
-    *n_out = tot;
+    *n_out = min(tot, k);  // tot is k: the keys above the bin and the bin's want best
     *range_out = (uint64_t)((sm.top_bin << 20) | 0xFFFFFu) << 32 | (uint32_t)(thresh >> 32);
   }
   return true;
@@ -419,7 +442,7 @@ __global__ void __launch_bounds__(kThreads)
   // eight independent loads in flight per thread (the passes would otherwise
   // wait out an L2 round trip per element).
   uint32_t* bits = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelectSmem));
-  float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem) + kStageWords * sizeof(uint32_t));
+  float* staged = reinterpret_cast<float*>(smem_raw + sizeof(SelectSmem) + 2 * kStageWords * sizeof(uint32_t));
   const bool st = n <= stage_cap && n > k;  // staged by the fast path below
   const int pad = (4 - ((int)((16u - ((uint32_t)(uintptr_t)sc & 15u)) & 15u) >> 2)) & 3;
   auto score = [&](int i) { return st ? staged[pad + i] : __ldg(sc + i); };
@@ -464,14 +487,16 @@ __global__ void __launch_bounds__(kThreads)
 // below, and hi, the largest of the shards' upper bounds, from above.  The
 // first histogram cuts [lo, hi] into kTopBins equal slices (a shift of u - lo)
 // as the candidates are staged, so that the bin holding rank k is narrow even
-// when the candidates share their top bits.  A second pass collects the
-// tokens of the bins above it and the keys of that bin, whose want-th key
-// (kth_refine) is the threshold.  A bin of more than kSmallKeys keys (many
-// equal scores) goes to the general radix select instead.
+// when the candidates share their top bits.  A second pass marks the
+// candidates of the bins above it (one bit each) and collects the keys of that
+// bin, whose want-th key (kth_refine) is the threshold.  A bin of more than
+// kSmallKeys keys (many equal scores) goes to the general radix select, and
+// the marks are then the keys at or above its result.
 // The order.  The selected tokens are set as bits of a bitmap over token
 // indices (kSortTokens of them at a time, in the histogram's words), whose
 // scan gives every token its place: no sort.
 constexpr int kSortTokens = kTopBins * 32;
+constexpr int kMergeBatch = 16;  // candidate loads a thread keeps in flight
 
 __global__ void __launch_bounds__(kThreads)
     topk_merge_kernel(const int32_t* __restrict__ plan, int off_pair, int C, int B, int k,
@@ -480,12 +505,35 @@ __global__ void __launch_bounds__(kThreads)
                       int32_t* __restrict__ sel_ids, int32_t* __restrict__ sel_count) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelectSmem& sm = *reinterpret_cast<SelectSmem*>(smem_raw);
-  int32_t* ids = reinterpret_cast<int32_t*>(smem_raw + sizeof(SelectSmem));  // selected tokens, any order
-  uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + pad16((size_t)k * 4));
+  // marks of the selected candidates (one bit each): their own words when
+  // the candidates are staged, else the unused staging room
+  uint32_t* marks_st = reinterpret_cast<uint32_t*>(smem_raw + sizeof(SelectSmem));
+  uint64_t* staged = reinterpret_cast<uint64_t*>(smem_raw + sizeof(SelectSmem) + kStageKeys / 8);
   __shared__ int start[CP_MAX_SHARDS + 1];  // shard r's candidates: [start[r], start[r + 1])
   __shared__ uint32_t lo_s, hi_s;
   const int b = blockIdx.x;
   const int lane = threadIdx.x & 31;
+  const int total = C * k;
+  // entry idx of the flattened [C][k] lists is row idx - r k of shard r =
+  // idx / k (a float estimate, corrected: no divide, no branch); entries past
+  // a shard's count lie in the workspace too and are loaded but not used
+  const float inv_k = 1.0f / (float)k;
+  auto shard_of = [&](int idx) {
+    int r = (int)((float)idx * inv_k);
+    r -= r * k > idx ? 1 : 0;
+    r += (r + 1) * k <= idx ? 1 : 0;
+    return r;
+  };
+  auto load_batch = [&](int base, uint64_t (&kv)[kMergeBatch]) {
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int idx = base + u * (int)blockDim.x + (int)threadIdx.x;
+      const int r = shard_of(idx);
+      kv[u] = idx < total ? __ldg(cand_keys + (long long)(r * B + b) * k + (idx - r * k)) : 0ull;
+    }
+  };
+  uint64_t kv[kMergeBatch];
+  load_batch(0, kv);  // in flight while warp 0 reads the shards' counts
   if (threadIdx.x < 32) {  // warp 0: the shards' counts (a scan) and ranges, two shards a lane
     int n0 = 0, n1 = 0;
     uint64_t g0 = 0, g1 = 0;
@@ -516,7 +564,7 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) {
       lo_s = lo;  // 0 when no shard bounds it: every candidate in play
       hi_s = max(hi, lo);
-      sm.ids_n = 0;
+      sm.small_n = 0;
     }
   }
   for (int i = threadIdx.x; i < kTopBins; i += blockDim.x) sm.hist[i] = 0;
@@ -527,22 +575,20 @@ __global__ void __launch_bounds__(kThreads)
   auto bin_of = [&](uint32_t u) { return min((u - lo) >> sh, (uint32_t)kTopBins - 1u); };
   const bool st = N <= stage_cap;
   const bool select = N > k;  // else every candidate is selected (threshold 0)
-  // pass 1: stage the candidates (when they fit), counting those in play;
-  // entry idx of the flattened [C][k] lists is row i = idx - r k of shard
-  // r = idx / k (a float estimate, corrected: no divide, no branch)
-  {
-    const float inv_k = 1.0f / (float)k;
-#pragma unroll 8
-    for (int idx = threadIdx.x; idx < C * k; idx += blockDim.x) {
-      int r = (int)((float)idx * inv_k);
-      r -= r * k > idx ? 1 : 0;
-      r += (r + 1) * k <= idx ? 1 : 0;
-      const int i = idx - r * k;
-      const uint64_t key = cand_keys[(long long)(r * B + b) * k + i];  // past the count: unused
-      if (i < start[r + 1] - start[r]) {
-        if (st) staged[start[r] + i] = key;
-        const uint32_t u = (uint32_t)(key >> 32);
-        if (select && u >= lo) atomicAdd(&sm.hist[bin_of(u)], 1u);
+  // pass 1: stage the candidates (when they fit), counting those in play
+  for (int base = 0; base < total; base += kMergeBatch * (int)blockDim.x) {
+    if (base > 0) load_batch(base, kv);
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int idx = base + u * (int)blockDim.x + (int)threadIdx.x;
+      if (idx < total) {
+        const int r = shard_of(idx);
+        const int i = idx - r * k;
+        if (i < start[r + 1] - start[r]) {
+          if (st) staged[start[r] + i] = kv[u];
+          const uint32_t u32 = (uint32_t)(kv[u] >> 32);
+          if (select && u32 >= lo) atomicAdd(&sm.hist[bin_of(u32)], 1u);
+        }
       }
     }
   }
@@ -553,82 +599,66 @@ __global__ void __launch_bounds__(kThreads)
     return cand_keys[(long long)(r * B + b) * k + (i - start[r])];
   };
   auto get = [&](int i) { return st ? staged[i] : get_global(i); };
-  // append tokens to ids (one shared counter update per warp and step)
-  auto append = [&](bool f, int token) {
-    const unsigned bal = __ballot_sync(kFull, f);
-    if (!bal) return;
-    int base = 0;
-    if (lane == 0) base = atomicAdd(&sm.ids_n, __popc(bal));
-    base = __shfl_sync(kFull, base, 0);
-    if (f) ids[base + __popc(bal & ((1u << lane) - 1u))] = token;
+  uint32_t* marks = st ? marks_st : reinterpret_cast<uint32_t*>(staged);
+  const int n_words = (N + 31) >> 5;
+  // marks of whole warps of 32 candidates: mark(i, key) says whether key (candidate i) is selected
+  auto mark_pass = [&](auto key_at, auto mark) {
+    for (int i = threadIdx.x; i < 32 * n_words; i += blockDim.x) {
+      const uint64_t key = i < N ? key_at(i) : 0ull;
+      const unsigned bal = __ballot_sync(kFull, i < N && mark(i, key));
+      if (lane == 0) marks[i >> 5] = bal;
+    }
   };
-  const int n_pad = (N + 31) & ~31;  // whole warps in the passes that append
   uint64_t t = 0;
+  int m = 0;  // the rank-k bin's keys in sm.small (selected when >= t)
   bool done = false;
   if (select) {
     pick_bin<kTopBins>(sm.hist, k, sm.pick, sm.warp_cnt);
     const uint32_t bin = sm.pick[0];
     const int want = k - (int)sm.pick[1];
     if ((int)sm.pick[2] <= kSmallKeys) {
-      // pass 2: tokens of the higher bins to ids, keys of the bin to small
-      if (threadIdx.x == 0) sm.small_n = 0;
-      __syncthreads();
-      auto pass2 = [&](auto key_at) {
-        for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-          uint64_t key = 0;
-          uint32_t bi = 0;
-          bool in_play = false;
-          if (i < N) {
-            key = key_at(i);
-            const uint32_t u = (uint32_t)(key >> 32);
-            in_play = u >= lo;
-            bi = bin_of(u);
-          }
-          append(in_play && bi > bin, key_token(key));
-          const bool mine = in_play && bi == bin;
-          const unsigned bal = __ballot_sync(kFull, mine);
-          if (bal) {
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&sm.small_n, __popc(bal));
-            base = __shfl_sync(kFull, base, 0);
-            if (mine) sm.small[base + __popc(bal & ((1u << lane) - 1u))] = key;
-          }
-        }
+      // pass 2: marks for the bins above, the bin's keys to small
+      auto above = [&](int, uint64_t key) {
+        const uint32_t u = (uint32_t)(key >> 32);
+        if (u < lo) return false;
+        const uint32_t bi = bin_of(u);
+        if (bi == bin) sm.small[atomicAdd(&sm.small_n, 1)] = key;  // a few keys
+        return bi > bin;
       };
-      if (st) pass2([&](int i) { return staged[i]; });
-      else pass2(get_global);
+      if (st) mark_pass([&](int i) { return staged[i]; }, above);
+      else mark_pass(get_global, above);
       __syncthreads();
-      const int m = sm.small_n;
+      m = sm.small_n;
       t = kth_refine(sm.small, m, want, 0ull, 0ull, 56, sm);
-      for (int i = threadIdx.x; i < ((m + 31) & ~31); i += blockDim.x) {
-        const uint64_t key = i < m ? sm.small[i] : 0ull;
-        append(i < m && key >= t, key_token(key));
-      }
       done = true;
     } else {
       t = kth_largest(N, k, get, [&](int i) { return (uint32_t)(get(i) >> 52); }, sm);
     }
   }
-  if (!done)  // every key at or above t
-    for (int i = threadIdx.x; i < n_pad; i += blockDim.x) {
-      const uint64_t key = i < N ? get(i) : 0ull;
-      append(i < N && key >= t, key_token(key));
-    }
+  if (!done) {  // every key at or above t
+    __syncthreads();  // marks may alias the staging room the select just read
+    auto at_least = [&](int, uint64_t key) { return key >= t; };
+    if (st) mark_pass([&](int i) { return staged[i]; }, at_least);
+    else mark_pass(get_global, at_least);
+  }
   __syncthreads();
-  const int cnt = sm.ids_n;
   // the selected tokens in increasing order, kSortTokens token indices at a time
   const int L = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[b].ctx_len;  // tokens are < L
   uint32_t* bmp = sm.hist;
   int32_t* out = sel_ids + (long long)b * k;
   int placed = 0;
-  for (int t0 = 0; t0 < L && placed < cnt; t0 += kSortTokens) {
+  for (int t0 = 0; t0 < L; t0 += kSortTokens) {
     const int words = (min(L - t0, kSortTokens) + 31) >> 5;
     for (int w = threadIdx.x; w < words; w += blockDim.x) bmp[w] = 0;
     __syncthreads();
-    for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
-      const int tok = ids[j] - t0;
+    auto set = [&](int tok) {
+      tok -= t0;
       if (tok >= 0 && tok < kSortTokens) atomicOr(&bmp[tok >> 5], 1u << (tok & 31));
-    }
+    };
+    for (int w = threadIdx.x; w < n_words; w += blockDim.x)
+      for (uint32_t word = marks[w]; word; word &= word - 1u) set(key_token(get(32 * w + __ffs(word) - 1)));
+    for (int j = threadIdx.x; j < m; j += blockDim.x)
+      if (sm.small[j] >= t) set(key_token(sm.small[j]));
     __syncthreads();
     const int per = (words + (int)blockDim.x - 1) / (int)blockDim.x;
     const int w0 = min(words, (int)threadIdx.x * per), w1 = min(words, w0 + per);
@@ -637,10 +667,14 @@ __global__ void __launch_bounds__(kThreads)
     int tot;
     int at = placed + block_excl_scan(c, sm.warp_cnt, &tot);
     for (int w = w0; w < w1; ++w)
-      for (uint32_t word = bmp[w]; word; word &= word - 1u) out[at++] = t0 + 32 * w + __ffs(word) - 1;
+      for (uint32_t word = bmp[w]; word; word &= word - 1u) {
+        if (at < k) out[at] = t0 + 32 * w + __ffs(word) - 1;
+        ++at;
+      }
     placed += tot;
     __syncthreads();
   }
+  const int cnt = min(placed, k);  // k when the request has more than k candidates, else all of them
   for (int i = cnt + threadIdx.x; i < k; i += blockDim.x) out[i] = -1;
   if (threadIdx.x == 0) {
     sel_count[b] = cnt;
@@ -702,7 +736,7 @@ cudaError_t launch_topk_local(const int32_t* dev_plan, const cp_plan_header& h, 
   const int pairs = h.C * h.R;
   // room to stage the longest pair's scores, up to kStageScores (longer pairs read from L2)
   const int cap = max_pair_rows < kStageScores ? max_pair_rows : kStageScores;
-  const int smem = (int)sizeof(SelectSmem) + kStageWords * (int)sizeof(uint32_t) +
+  const int smem = (int)sizeof(SelectSmem) + 2 * kStageWords * (int)sizeof(uint32_t) +
                    (cap + 3 + 127) / 128 * 128 * (int)sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(topk_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -715,7 +749,9 @@ cudaError_t launch_topk_merge(const int32_t* dev_plan, const cp_plan_header& h, 
                               const int32_t* cand_n, const uint64_t* range, uint64_t* thresh, int32_t* sel_ids,
                               int32_t* sel_count, cudaStream_t s) {
   const int cap = h.C * k < kStageKeys ? h.C * k : kStageKeys;
-  const size_t smem = sizeof(SelectSmem) + pad16((size_t)k * 4) + (size_t)cap * sizeof(uint64_t);
+  // the staging room doubles as the marks when the candidates do not fit
+  // (C k / 32 words <= kStageKeys * 2 words since C k <= 64 x 4096)
+  const size_t smem = sizeof(SelectSmem) + kStageKeys / 8 + (size_t)kStageKeys * sizeof(uint64_t);
   cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
