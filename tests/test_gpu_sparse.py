@@ -86,6 +86,37 @@ def test_topk_unstaged(cp, contiguous, ties, C, k):
         assert np.all(sel[b, cnt[b]:] == -1)
 
 
+@pytest.mark.parametrize("contiguous", [False, True])
+def test_topk_infinite_scores(cp, contiguous):
+    """Masked tokens scored -inf (most of some requests, so the k-th key is
+    -inf) and a few +inf: the order still counts them as numbers."""
+    ctx = [9000, 30000, 5000]
+    C, k = 4, 2048
+    scores = W.index_scores(ctx, seed=99, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    u = torch.rand(sum(ctx), generator=g)
+    s = scores.cpu()
+    base = 0
+    for L, masked in zip(ctx, (0.9, 0.5, 0.7)):
+        s[base:base + L][u[base:base + L] < masked] = -math.inf
+        s[base:base + L][u[base:base + L] > 0.999] = math.inf
+        base += L
+    scores = s.to(DEV)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), device=DEV)
+    sel, cnt, _ = cp.cp_sparse_topk(plan, shard_scores(scores, ctx, C, plan, contiguous), k)
+    cp.cp_device_error_check()
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    want = oracle_selection(scores, ctx, C, k, contiguous)
+    sn = scores.cpu().numpy()
+    off = np.concatenate([[0], np.cumsum(ctx)])
+    for b, L in enumerate(ctx):
+        sb = sn[off[b]:off[b] + L]
+        order = np.lexsort((np.arange(L), -sb.astype(np.float64)))
+        assert want[b] == sorted(order[:k].tolist())
+        assert cnt[b] == min(k, L)
+        assert sel[b, :cnt[b]].tolist() == want[b], f"request {b}"
+
+
 def test_topk_full_size_sampled(cp):
     """64 requests x 131,072 tokens, C = 8, k = 2048: sampled requests exact."""
     ctx = [131072] * 64
