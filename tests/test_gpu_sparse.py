@@ -87,6 +87,27 @@ def test_topk_unstaged(cp, contiguous, ties, C, k):
 
 
 @pytest.mark.parametrize("contiguous", [False, True])
+@pytest.mark.parametrize("k", [1, 100, 700])
+def test_topk_sixty_four_shards(cp, contiguous, k):
+    """C = 64, the largest: the merge reads two shards' counts per lane."""
+    ctx = [20000, 64, 0, 5001]
+    C = 64
+    scores = W.index_scores(ctx, seed=640 + k, device=DEV)
+    plan = cp.cp_decode_plan_ex(C, ctx, layout=int(contiguous), device=DEV)
+    sel, cnt, _ = cp.cp_sparse_topk(plan, shard_scores(scores, ctx, C, plan, contiguous), k)
+    cp.cp_device_error_check()
+    sel, cnt = sel.cpu().numpy(), cnt.cpu().numpy()
+    s = scores.cpu().numpy()
+    base = np.concatenate([[0], np.cumsum(ctx)])
+    for b, L in enumerate(ctx):
+        sb = s[base[b]:base[b] + L]
+        order = np.lexsort((np.arange(L), -sb.astype(np.float64)))
+        assert cnt[b] == min(k, L)
+        assert sel[b, :cnt[b]].tolist() == sorted(order[:k].tolist()), f"request {b}"
+        assert np.all(sel[b, cnt[b]:] == -1)
+
+
+@pytest.mark.parametrize("contiguous", [False, True])
 def test_topk_infinite_scores(cp, contiguous):
     """Masked tokens scored -inf (most of some requests, so the k-th key is
     -inf) and a few +inf: the order still counts them as numbers."""
