@@ -15,7 +15,8 @@
 // (a deterministic tie rule).  Both are one 64-bit key,
 //   key = ordered(score) << 32 | (2^32 - 1 - token),
 // so "the k best" is "the k largest keys" and every key is distinct; the
-// k-th largest key is found by an 8-pass radix select (8 bits a pass).
+// k-th largest key is found by a radix select: a 4,096-bin first pass, then
+// 8-bit passes over the keys of the bin that holds rank k.
 #include <cuda_runtime.h>
 
 #include "internal.h"
