@@ -23,7 +23,8 @@ HEADER_WORDS = 24
 SEG_WORDS, PAIR_WORDS, WORK_WORDS = 12, 8, 4
 HEADER_FIELDS = ["magic", "kind", "C", "R", "T", "KV", "n_seg", "n_tiles", "off_rank", "off_req",
                  "off_seg", "off_tiles", "off_rtile", "off_idx", "off_qpos", "off_qreq",
-                 "host_words", "dev_words", "n_parts", "tile_rows", "n_split", "layout", "s_q"]
+                 "host_words", "dev_words", "n_parts", "tile_rows", "n_split", "layout", "s_q",
+                 "off_run"]
 SEG_FIELDS = ["rank", "req", "block", "which", "local_start", "count", "first_f", "stride",
               "q_start", "first_pos", "kv_len", "kv_base"]
 
@@ -200,6 +201,24 @@ class DecodePlan(_Plan):
     @property
     def split_pairs(self):
         return self.words(self.off_rtile, self.n_split)
+
+    @property
+    def run_out(self):
+        """Per work item, for the merged-output decode: -1 the run goes on to
+        the worker's next item; -2 the last item of a run holding its whole
+        request; k >= 0 the last item of a partial run, written to part slot
+        k; -3 an empty pair's item."""
+        return self.words(self.off_run + 2, self.n_seg)
+
+    @property
+    def merge_list(self):
+        """[m, 3]: (request, first part slot, parts) of the requests merged from parts."""
+        n = int(self.words(self.off_run + 1, 1)[0])
+        return self.words(self.off_run + 2 + self.n_seg, 3 * n).reshape(n, 3)
+
+    @property
+    def n_merge_parts(self):
+        return int(self.words(self.off_run, 1)[0])
 
     def shard_rows(self):
         p = self.pairs

@@ -368,6 +368,54 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
     if (pair[wd.pair].n_parts > 1) wd.part = pair[wd.pair].first_part + next[wd.pair]++;
 
   const int n_work = (int)work.size();
+
+  // Runs for the merged-output decode: within a worker, the consecutive items
+  // (of nonempty pairs) of one request.  A run that holds all of its request's
+  // nonempty items writes the request's result; the others write parts, which
+  // a merge combines.  A request's parts are consecutive slots, in worker order.
+  std::vector<int32_t> run_out(n_work, -3);  // -3: an empty pair's item (nothing to do)
+  std::vector<int> req_items(B, 0), req_parts(B, 0), run_req, run_last, run_n;
+  for (const cp_work_desc& wd : work)
+    if (pair[wd.pair].rows > 0) req_items[wd.pair % B]++;
+  for (int wkr = 0; wkr < G; ++wkr) {
+    int cur = -1;  // this worker's open run
+    for (int i = worker_off[wkr]; i < worker_off[wkr + 1]; ++i) {
+      if (pair[work[i].pair].rows == 0) continue;
+      const int b = work[i].pair % B;
+      if (cur >= 0 && run_req[cur] == b) {
+        run_out[run_last[cur]] = -1;  // the run goes on to item i
+        run_last[cur] = i;
+        run_n[cur]++;
+      } else {
+        cur = (int)run_req.size();
+        run_req.push_back(b);
+        run_last.push_back(i);
+        run_n.push_back(1);
+      }
+      run_out[i] = -2;  // provisionally the last item of a complete run
+    }
+  }
+  for (size_t k = 0; k < run_req.size(); ++k)
+    if (run_n[k] < req_items[run_req[k]]) req_parts[run_req[k]]++;
+  std::vector<int> req_first(B, 0), req_next(B, 0);
+  std::vector<int32_t> merge_list;  // {request, first part slot, parts}
+  int n_mparts = 0;
+  for (int b = 0; b < B; ++b) {
+    req_first[b] = n_mparts;
+    n_mparts += req_parts[b];
+    if (req_parts[b] > 0 || req_items[b] == 0) {  // parts to merge, or no rows at all (O = 0, LSE = -inf)
+      merge_list.push_back(b);
+      merge_list.push_back(req_first[b]);
+      merge_list.push_back(req_parts[b]);
+    }
+  }
+  for (size_t k = 0; k < run_req.size(); ++k)
+    if (run_n[k] < req_items[run_req[k]]) {
+      const int b = run_req[k];
+      run_out[run_last[k]] = req_first[b] + req_next[b]++;
+    }
+  const int n_mlist = (int)merge_list.size() / 3;
+
   cp_plan_header h;
   memset(&h, 0, sizeof(h));
   h.magic = CP_PLAN_MAGIC;
@@ -393,11 +441,17 @@ cp_status build_decode_plan(int C, int B, const int32_t* ctx_len, int layout, in
   w = align4(w + 2 * B);
   h.off_rtile = w;
   w = align4(w + (int)split.size());
+  h.off_run = w;
+  w = align4(w + 2 + n_work + 3 * n_mlist);
   h.host_words = w;
   h.dev_words = w;
   out->words.assign(w, 0);
   int32_t* W = out->words.data();
   memcpy(W, &h, sizeof(h));
+  W[h.off_run] = n_mparts;
+  W[h.off_run + 1] = n_mlist;
+  if (n_work) memcpy(W + h.off_run + 2, run_out.data(), 4 * n_work);
+  if (n_mlist) memcpy(W + h.off_run + 2 + n_work, merge_list.data(), 4 * merge_list.size());
   memcpy(W + h.off_rank, pair.data(), sizeof(cp_pair_desc) * P);
   memcpy(W + h.off_req, worker_off.data(), 4 * (G + 1));
   if (n_work) memcpy(W + h.off_seg, work.data(), sizeof(cp_work_desc) * n_work);

@@ -102,7 +102,7 @@ typedef struct {
   int32_t n_split;    /* decode: pairs covered by more than one work item */
   int32_t layout;     /* decode: cp_dcp_layout of the token shards */
   int32_t s_q;        /* decode: query rows per request (1, or more for MTP) */
-  int32_t reserved;
+  int32_t off_run;    /* decode: the merged-output run table (cp_decode_attn_merged) */
 } cp_plan_header;
 /* Decode plans reuse the table offsets: off_tiles -> int32 [R][2]
  * {ctx_len, first token of the request in the token-ordered cache};
