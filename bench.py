@@ -60,6 +60,9 @@ PROFILED_TRAFFIC = {
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                    "sha1": "66afd4cc6ca2416d3262e0e21695f9dcf534f72c",
                    "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
+    "decode_fp8_merged": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
+                                  "context_long_attention_gb300/csrc/tc_ptx.cuh"],
+                          "sha1": None, "bytes_per_token": None},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "c19956b2693cf34223e556901c4c0d1891584060",
@@ -489,9 +492,10 @@ def leg_prefill_interleave(cp, args, dev, stream, world, rank, peaks, peak_kind)
     return out
 
 
-def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, fp8):
+def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, fp8, merged=False):
     """MLA decode of one of the decode workloads (plan + split-KV decode + LSE
-    merge per step) from per-shard buffers packed once before timing."""
+    merge per step, or with merged: plan + cp_decode_attn_merged) from
+    per-shard buffers packed once before timing."""
     m = W.WORKLOADS[workload]
     ctx = W.mixed_context_lengths() if workload == "mla_mixed" else [m["ctx"]] * m["B"]
     data = W.mla_decode_inputs(ctx, H=m["H"], seed=W.SEEDS[workload] + rank, device=dev,
@@ -511,6 +515,9 @@ def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, f
     o_dec = torch.empty((B, H, Dv), dtype=torch.bfloat16, device=dev)
     lse_dec = torch.empty((B, H), dtype=torch.float32, device=dev)
     ws = torch.empty(max(16, cp.cp_decode_workspace_size(plan, H, Dv)), dtype=torch.uint8, device=dev)
+    kv_code = cp.CP_FP8_E4M3 if fp8 else cp.CP_BF16
+    ws_m = (torch.empty(max(16, cp.cp_decode_merged_workspace_size(plan, cp.CP_DECODE_MLA, kv_code, H, Dv)),
+                        dtype=torch.uint8, device=dev) if merged else None)
     scale = 1.0 / math.sqrt(m["Dqk"])
     nbytes = decode_bytes(ctx, H, fp8=fp8)
 
@@ -519,11 +526,16 @@ def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, f
         if e:
             e[0].record(stream)
         dp = cp.cp_decode_plan(C, ctx, device=dev)
-        cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales, sm_scale=scale,
-                          o_part=o_part, lse_part=lse_part, ws=ws)
+        if merged:
+            cp.cp_decode_attn_merged(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales, sm_scale=scale,
+                                     o=o_dec, lse=lse_dec, ws=ws_m)
+        else:
+            cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales, sm_scale=scale,
+                              o_part=o_part, lse_part=lse_part, ws=ws)
         if e:
             e[1].record(stream)
-        cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
+        if not merged:
+            cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
         if e:
             e[2].record(stream)
         return e
@@ -536,8 +548,14 @@ def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, f
     total = max_over_ranks(sum(dec_ms) + sum(mrg_ms), world)
     ach = nbytes / (statistics.mean(dec_ms) / 1e3) / 1e9
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    n_k = 2 + (1 if plan.n_split > 0 else 0)
+    if merged:  # decode (+ the runs' parts merge, when a request is cut by a worker boundary)
+        n_k = 1 + (1 if len(plan.merge_list) else 0) if fp8 else 2 + (1 if plan.n_split > 0 else 0)
+    else:
+        n_k = 2 + (1 if plan.n_split > 0 else 0)
+    traffic_key = ("decode_fp8_merged" if merged else "decode_fp8") if fp8 else "decode_bf16"
     out = {"workload": (DECODE_WORKLOADS["mixed"] if workload == "mla_mixed" else DECODE_WORKLOADS["uniform"]),
+           "api": ("cp_decode_attn_merged (ms_decode: decode and merge in one call)" if merged
+                   else "cp_decode_attn + cp_lse_merge"),
            "kv": "fp8" if fp8 else "bf16", "metric": "decode KV HBM GB/s", "unit": "GB/s",
            "context": {"requests": B, "tokens": sum(ctx), "median": int(statistics.median(ctx)),
                        "min": min(ctx), "max": max(ctx)},
@@ -546,14 +564,14 @@ def leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, workload, f
            "merge_share": statistics.mean(mrg_ms) / (statistics.mean(dec_ms) + statistics.mean(mrg_ms)),
            "bytes_per_step": nbytes, "gpu_launches": n_k * steps,
            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                        "traffic": (profiled_traffic("decode_fp8" if fp8 else "decode_bf16", sum(ctx))
-                                    if workload == "mla" else None),
+                        "traffic": (profiled_traffic(traffic_key, sum(ctx))
+                                    if workload == "mla" and (fp8 or not merged) else None),
                         "peak_kind": peak_kind,
                         "kernel": "decode_mla_fp8_kernel" if fp8 else "decode_mla_tc_kernel"},
            "clocks": clk}
-    del shards, scales, o_part, lse_part, o_dec, lse_dec, ws, data
+    del shards, scales, o_part, lse_part, o_dec, lse_dec, ws, ws_m, data
     torch.cuda.empty_cache()
-    if not args.no_cpu and rank == 0:
+    if not args.no_cpu and rank == 0 and not merged:  # the merged legs run the same workloads
         one = sorted(ctx)[len(ctx) // 2]  # the median request
         gbs, sec, cores = oracle_decode_sample(one, workload, fp8)
         out["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
@@ -803,6 +821,16 @@ def run_ours(args, world, rank, local):
         ws_bytes = cp.cp_decode_workspace_size(dplan, Hr, Dv)
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         n_dec_kernels = 2 + (1 if dplan.n_split > 0 else 0)  # decode (+ split merge) + LSE merge
+        if args.decode_merged:
+            if args.decode_paged:
+                raise SystemExit("--decode-merged takes per-shard buffers, not a paged pool")
+            mode_code = cp.CP_DECODE_GQA if gqa else cp.CP_DECODE_MLA
+            kv_code = cp.CP_FP8_E4M3 if fp8 else (cp.CP_FP32 if shards[0].dtype == torch.float32 else cp.CP_BF16)
+            ws_m = torch.empty(max(16, cp.cp_decode_merged_workspace_size(dplan, mode_code, kv_code, Hr, Dv)),
+                               dtype=torch.uint8, device=dev)
+            merged_native = fp8 and not gqa
+            # decode (+ the runs' merge), or decode (+ split merge) + LSE merge
+            n_dec_kernels = (1 + (1 if len(dplan.merge_list) else 0)) if merged_native else n_dec_kernels
     torch.cuda.synchronize(dev)
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -818,7 +846,11 @@ def run_ours(args, world, rank, local):
         e2.record(stream)
         if do_dec:
             dp = cp.cp_decode_plan_ex(m["C"], ctx, layout=layout, s_q=s_q, device=dev)
-            if pages is not None:
+            if args.decode_merged:
+                cp.cp_decode_attn_merged(dp, cp.CP_DECODE_GQA if gqa else cp.CP_DECODE_MLA, dq, shards,
+                                         vshards if gqa else None, shard_scale=scales, sm_scale=dscale,
+                                         o=o_dec.view(*lead, Hr, Dv), lse=lse_dec.view(*lead, Hr), ws=ws_m)
+            elif pages is not None:
                 cp.cp_decode_attn_paged(dp, pages, cp.CP_DECODE_MLA, dq, shards, scale_pool=scales,
                                         sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
             elif gqa:
@@ -828,7 +860,7 @@ def run_ours(args, world, rank, local):
                 cp.cp_decode_attn(dp, cp.CP_DECODE_MLA, dq, shards, shard_scale=scales,
                                   sm_scale=dscale, o_part=o_part, lse_part=lse_part, ws=ws)
         e3.record(stream)
-        if do_dec:
+        if do_dec and not args.decode_merged:
             cp.cp_lse_merge(o_mrg, lse_mrg, out=o_dec, lse=lse_dec)
         e4.record(stream)
 
@@ -957,7 +989,7 @@ def run_ours(args, world, rank, local):
     dec_e2e = None
     default_decode = (do_dec and uniform and fp8 and not args.decode_paged and args.decode_rows == 1
                       and args.decode_layout == "round_robin" and not args.decode_ctx
-                      and not args.decode_batch)
+                      and not args.decode_batch and not args.decode_merged)
     if default_decode:
         dec_e2e = decode_e2e(cp, args, dev, stream, world, ctx, m, dq, shards, scales, dscale, d_bytes)
 
@@ -972,6 +1004,10 @@ def run_ours(args, world, rank, local):
                 "decode_bf16": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, "mla", False),
                 "decode_mixed": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind,
                                            "mla_mixed", True),
+                "decode_merged": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind, "mla", True,
+                                            merged=True),
+                "decode_mixed_merged": leg_decode(cp, args, dev, stream, world, rank, peaks, peak_kind,
+                                                  "mla_mixed", True, merged=True),
                 "prefill_interleave": leg_prefill_interleave(cp, args, dev, stream, world, rank, peaks,
                                                              peak_kind)}
 
@@ -1001,6 +1037,8 @@ def run_ours(args, world, rank, local):
                          if args.decode_paged else "one contiguous buffer per shard"),
                "layout": args.decode_layout,
                "query_rows": args.decode_rows,
+               "api": ("cp_decode_attn_merged (ms_decode: decode and merge)" if args.decode_merged
+                       else "cp_decode_attn + cp_lse_merge"),
                "ms_decode": dec_avg, "ms_merge": statistics.mean(mrg_ms),
                "merge_share": statistics.mean(mrg_ms) / (dec_avg + statistics.mean(mrg_ms)),
                "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": hbm, "unit": "GB/s",
@@ -1081,6 +1119,8 @@ def main():
                     help="decode token shards: token p on shard p mod C, or C contiguous chunks")
     ap.add_argument("--decode-rows", type=int, default=1, metavar="S_Q",
                     help="query rows per request (MTP); the 64 heads split into S_Q rows of 64/S_Q")
+    ap.add_argument("--decode-merged", action="store_true",
+                    help="time the decode through cp_decode_attn_merged (decode and merge in one call)")
     ap.add_argument("--sparse-k", type=int, default=0, metavar="K",
                     help="also time sparse decode over the exact sharded top-K of per-token scores")
     ap.add_argument("--prefill-workload", choices=list(PREFILL_WORKLOADS), default="zigzag",

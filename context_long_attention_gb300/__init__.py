@@ -29,10 +29,12 @@ from ._binding import (  # noqa: F401
     PageTable,
     PrefillPlan,
     cp_decode_attn,
+    cp_decode_attn_merged,
     cp_decode_attn_noalloc,
     cp_decode_attn_paged,
     cp_decode_plan,
     cp_decode_plan_ex,
+    cp_decode_merged_workspace_size,
     cp_decode_workspace_size,
     cp_device_error_check,
     cp_kv_shard_pack,

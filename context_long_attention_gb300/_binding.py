@@ -61,6 +61,9 @@ _SIGS = {
     "cp_decode_workspace_size": (_i, [_vp, _i, _i, _szp]),
     "cp_decode_attn": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp,
                             _vp, _sz, _vp]),
+    "cp_decode_merged_workspace_size": (_i, [_vp, _i, _i, _i, _i, _szp]),
+    "cp_decode_attn_merged": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _i,
+                                   _vp, _vp, _sz, _vp]),
     "cp_lse_merge": (_i, [_i, _i, _i, _i, _vp, _vp, _vp, _i, _vp, _vp]),
     "cp_lse_fold": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "cp_decode_attn_noalloc": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
@@ -457,6 +460,48 @@ def cp_decode_attn(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_
                               H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part), _ptr(lse_part),
                               _ptr(ws), ws_bytes, _stream(q.device)))
     return o_part, lse_part
+
+
+def cp_decode_merged_workspace_size(plan: DecodePlan, mode: int, kv_dtype: int, H: int, Dv: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib.cp_decode_merged_workspace_size(_np_ptr(plan.host), mode, kv_dtype, H, Dv, ctypes.byref(b)))
+    return b.value
+
+
+def cp_decode_attn_merged(plan: DecodePlan, mode: int, q, shard_k, shard_v=None, shard_scale=None,
+                          sm_scale=None, out_dtype=torch.bfloat16, o=None, lse=None, ws=None):
+    """cp_decode_attn and the LSE merge of its partials in one call: returns
+    (o [B, H, Dv] out_dtype, lse [B, H] fp32); with an MTP plan (s_q > 1)
+    q is [B, s_q, H, Dqk] and the outputs [B, s_q, ...].  MLA over an FP8
+    cache accumulates each worker's items of one request together and writes
+    partials only for requests cut by a worker boundary."""
+    lead, H, Dqk = _decode_shapes(plan, q)
+    _need_cuda(q, *[t for t in shard_k if t is not None], o, lse)
+    sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in shard_k]
+    kv_dtype = _dtype_code(sk[0]) if sk else CP_BF16
+    if mode == CP_DECODE_MLA:
+        Hkv, Dv = 1, 512
+    else:
+        Hkv, Dv = sk[0].shape[1], Dqk
+        want_q = torch.float32 if kv_dtype == CP_FP32 else torch.bfloat16
+        if q.dtype != want_q:
+            raise TypeError(f"GQA decode over this cache takes a {want_q} query, got {q.dtype}")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(Dqk)
+    if o is None:
+        o = torch.empty((*lead, H, Dv), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((*lead, H), dtype=torch.float32, device=q.device)
+    need = cp_decode_merged_workspace_size(plan, mode, kv_dtype, H, Dv)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.cp_decode_attn_merged(_np_ptr(plan.host), _ptr(plan.dev), mode, kv_dtype, _ptr(q),
+                                     _ptr_array(sk), _ptr_array(shard_v) if shard_v is not None else None,
+                                     _ptr_array(shard_scale) if shard_scale is not None else None,
+                                     H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o), _dtype_code(o), _ptr(lse),
+                                     _ptr(ws), ws_bytes, _stream(q.device)))
+    return o, lse
 
 
 def cp_decode_attn_noalloc(plan: DecodePlan, mode: int, q, shard_k, shard_v=None,

@@ -850,6 +850,97 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
                     sm_scale, o_part, lse_part, ws, ws_bytes, stream);
 }
 
+cp_status cp_decode_merged_workspace_size(const void* host_plan, cp_decode_mode mode, cp_dtype kv_dtype, int H,
+                                          int Dv, size_t* bytes) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (!bytes || H < 1 || Dv < 1) return fail(CP_ERR_INVALID_ARG, "bad arguments");
+  if (h.off_run <= 0) return fail(CP_ERR_INVALID_ARG, "the plan has no run table");
+  const size_t Hc = (size_t)H * plan_s_q(h);
+  const int32_t* W = (const int32_t*)host_plan;
+  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3)
+    *bytes = (size_t)W[h.off_run] * Hc * (Dv + 1) * sizeof(float);
+  else  // the per-shard partials, then the split-KV scratch
+    *bytes = ((size_t)h.C * h.R * Hc * (Dv + 1) * sizeof(float) + 15) / 16 * 16 +
+             (size_t)h.n_parts * Hc * (Dv + 1) * sizeof(float);
+  return ok();
+}
+
+cp_status cp_decode_attn_merged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                                cp_dtype kv_dtype, const void* q, const void* const* shard_k,
+                                const void* const* shard_v, const float* const* shard_scale, int Hq, int Hkv,
+                                int Dqk, int Dv, float sm_scale, void* o, cp_dtype o_dtype, float* lse, void* ws,
+                                size_t ws_bytes, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (!dev_plan || !q || !shard_k || !o || !lse) return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o) || !aligned16(lse))
+    return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
+  if (o_dtype != CP_BF16 && o_dtype != CP_FP32) return fail(CP_ERR_INVALID_ARG, "o_dtype must be bf16 or fp32");
+  if (h.off_run <= 0) return fail(CP_ERR_INVALID_ARG, "the plan has no run table");
+  if (h.layout == CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "a selection plan goes to cp_sparse_decode_attn");
+  st = check_decode_shapes(mode, kv_dtype, shard_v != nullptr, shard_scale != nullptr, Hq, Hkv, Dqk, Dv, sm_scale,
+                           plan_s_q(h));
+  if (st != CP_OK) return st;
+  size_t need = 0;
+  st = cp_decode_merged_workspace_size(host_plan, mode, kv_dtype, Hq, Dv, &need);
+  if (st != CP_OK) return st;
+  if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (need && !aligned16(ws)) return fail(CP_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  ShardPtrs K, V;
+  ScalePtrs S;
+  memset(&K, 0, sizeof(K));
+  memset(&V, 0, sizeof(V));
+  memset(&S, 0, sizeof(S));
+  const int32_t* W = (const int32_t*)host_plan;
+  long long shard_rows[CP_MAX_SHARDS] = {0};
+  for (int r = 0; r < h.C; ++r) {
+    const long long rows_r = pair_rows_of_shard(h, W, r);
+    shard_rows[r] = rows_r;
+    K.p[r] = shard_k[r];
+    if (rows_r > 0 && (!shard_k[r] || !aligned16(shard_k[r]))) return fail(CP_ERR_INVALID_ARG, "shard_k[%d] NULL or misaligned", r);
+    if (shard_v) {
+      V.p[r] = shard_v[r];
+      if (rows_r > 0 && (!shard_v[r] || !aligned16(shard_v[r]))) return fail(CP_ERR_INVALID_ARG, "shard_v[%d] NULL or misaligned", r);
+    }
+    if (shard_scale) {
+      S.p[r] = shard_scale[r];
+      if (rows_r > 0 && !shard_scale[r]) return fail(CP_ERR_INVALID_ARG, "shard_scale[%d] is NULL", r);
+    }
+  }
+  RowMap rm;
+  memset(&rm, 0, sizeof(rm));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Hc = Hq * plan_s_q(h);
+  const bool bf16 = o_dtype == CP_BF16;
+  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3) {
+    // runs accumulate in the kernel; only the runs cut by a worker boundary leave parts
+    const int n_mparts = W[h.off_run], n_list = W[h.off_run + 1];
+    float* ws_o = (float*)ws;
+    float* ws_lse = ws_o ? ws_o + (size_t)n_mparts * Hc * Dv : nullptr;
+    const int32_t* plan = (const int32_t*)dev_plan;
+    const MergedOut mo = {plan + h.off_run + 2, o, bf16, lse};
+    cudaError_t e = launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, nullptr, nullptr, ws_o,
+                                          ws_lse, nullptr, wait_limit_ns(), s, &mo);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    e = launch_merge_runs(plan, h, n_list, Hc, Dv, ws_o, ws_lse, o, bf16, lse, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge of the runs' parts");
+    return ok();
+  }
+  // other caches: the per-shard partials in the workspace, then their merge
+  float* o_part = (float*)ws;
+  float* lse_part = o_part + (size_t)h.C * h.R * Hc * Dv;
+  const size_t part_bytes = ((size_t)h.C * h.R * Hc * (Dv + 1) * sizeof(float) + 15) / 16 * 16;
+  st = run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv, sm_scale, o_part,
+                  lse_part, (uint8_t*)ws + part_bytes, ws_bytes - part_bytes, stream);
+  if (st != CP_OK) return st;
+  const cudaError_t e = launch_lse_merge(h.C, h.R, Hc, Dv, o_part, lse_part, o, bf16, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "LSE merge kernel");
+  return ok();
+}
+
 cp_status cp_decode_attn_paged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
                                cp_dtype kv_dtype, const void* q, const void* k_pool,
                                const void* v_pool, const float* scale_pool,

@@ -89,6 +89,14 @@ struct Params {
   float* ws_o;
   float* ws_lse;
   const int32_t* pair_count;  // rows in use per pair (a selection buffer), or nullptr
+  // Merged output: run_out is the plan's run table (nullptr: one partial per
+  // work item).  A worker's consecutive items of one request accumulate as
+  // one run; a run holding its whole request writes the result to o_fin /
+  // lse_fin, any other run a part to ws_o / ws_lse at its slot.
+  const int32_t* run_out;
+  void* o_fin;     // [B][H][512], bf16 (o_fin_bf16) or fp32
+  int o_fin_bf16;
+  float* lse_fin;  // [B][H]
   unsigned* status;
   unsigned long long wait_ns;
 };
@@ -191,8 +199,11 @@ struct Item {
   int pair, row_begin, pair_rows;  // the pair, the item's first row in it, the pair's rows
   int tok0, tok_step, ctx_len;     // token of the pair's row i = tok0 + i tok_step; L
   long long row0;  // first shard row (contiguous caches)
-  float* out_o;
+  void* out_o;     // where the item's run writes O: fp32, or bf16 when out_bf16
   float* out_l;
+  bool out_bf16;
+  bool run_end;    // the item ends its run (always, without the run table)
+  bool skip;       // an empty pair's item in a merged decode: nothing to do
 };
 __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   const cp_work_desc wd = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work)[wi];
@@ -211,10 +222,27 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   it.tok0 = pd.tok0;
   it.tok_step = pd.tok_step;
   it.ctx_len = pd.ctx_len;
-  it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
-                         : p.ws_o + (long long)wd.part * p.H * kDv;
-  it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
-                         : p.ws_lse + (long long)wd.part * p.H;
+  it.out_bf16 = false;
+  it.run_end = true;
+  it.skip = false;
+  if (!p.run_out) {
+    it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
+                           : p.ws_o + (long long)wd.part * p.H * kDv;
+    it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
+                           : p.ws_lse + (long long)wd.part * p.H;
+    return it;
+  }
+  const int ro = p.run_out[wi];
+  it.skip = ro == -3;
+  it.run_end = ro >= 0 || ro == -2;
+  if (ro >= 0) {  // a part
+    it.out_o = p.ws_o + (long long)ro * p.H * kDv;
+    it.out_l = p.ws_lse + (long long)ro * p.H;
+  } else {  // the request's result (read only when ro == -2)
+    it.out_bf16 = p.o_fin_bf16 != 0;
+    it.out_o = static_cast<uint8_t*>(p.o_fin) + (long long)it.b * p.H * kDv * (it.out_bf16 ? 2 : 4);
+    it.out_l = p.lse_fin + (long long)it.b * p.H;
+  }
   return it;
 }
 
@@ -240,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float sDelta[kHeads];            // its last move; in the epilogue 1 / column sum
   __shared__ int sRed[4][kHeads];             // per row-quarter column maxima, then column sums
   __shared__ uint32_t sRed1[kSoftmaxWarps];   // per-warp max of |q| or of the token scales
+  __shared__ int sInit[kHeads];               // head h has had an unmasked row in the current run
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -431,10 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dPlo = smem_desc(sbase + kPloOff, 16, 512, 4);
       bool ok = true;
       int g = 0;
+      int run_tiles = 0;  // tiles of the current run issued so far (O^T accumulates after the first)
       for (int wi = w0; wi < w1 && ok; ++wi) {
         const Item it = read_item(p, wi);
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
           const int s = g & 1;
+          const bool acc = run_tiles > 0;
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p), g & 1, p.wait_ns, &abort_flag))) {
             if (lane == 0) report_timeout(p.status, 4, &abort_flag);
             ok = false;
@@ -450,14 +481,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < kRows / 32; ++kk) {
                 const uint64_t a = av + (uint64_t)((kk * 4096) >> 4);
-                mma_f8_fill_a(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || j > 0) ? 1u : 0u);
+                mma_f8_fill_a(d, a, bh + (uint64_t)((kk * 2048) >> 4), idPV, (kk > 0 || acc) ? 1u : 0u);
                 mma_f8_reuse_a(d, a, dPlo + (uint64_t)((kk * 2048) >> 4), idPV, 1u);
               }
               mma_commit(smem_u32(&bar_done[s][mb]));
             }
             __syncwarp();
           }
+          ++run_tiles;
         }
+        if (it.run_end) run_tiles = 0;
       }
       if (elect_one()) mma_commit(smem_u32(&bar_drain));
       __syncwarp();
@@ -475,247 +508,279 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int g = 0;
     int q_b = -1, eq = 0;  // request whose query the operand holds, its scale exponent
+    // the run's state: tiles so far, the weights' scale exponent (set on the
+    // run's first tile, only decreases), this row's sums per head
+    int run_tiles = 0, gs = 0;
+    float l[kHpw];
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, wi);
-      if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
-        for (int i = tid; i < p.H * kDv; i += kSoftmax) it.out_o[i] = 0.f;
-        for (int i = tid; i < p.H; i += kSoftmax) it.out_l[i] = -INFINITY;
-        continue;
-      }
-      // ---- [Q_hi | Q_lo] of request b: x = q 2^eq with max |x| in [128, 256).
-      // Every product of the previous item has completed (its epilogue waited
-      // for the last P.V), so the operand can be overwritten; an item of the
-      // same request as the previous one keeps it.
-      const bool new_q = it.b != q_b;
-      if (new_q) {
-        q_b = it.b;
-        const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
-        constexpr int kPieces = kDqk / 8;                   // 16-byte pieces per head
-        constexpr int kPer = kHeads * kPieces / kSoftmax;   // pieces per thread
-        static_assert(kHeads * kPieces % kSoftmax == 0, "query pieces split evenly");
-        constexpr int kBatch = kPer % 6 == 0 ? 6 : 3;  // pieces in flight at once per thread
-        static_assert(kPer % kBatch == 0, "whole batches of pieces");
-        // a batch of this thread's pieces (heads past H are zero)
-        auto load_batch = [&](int k0, uint4* qv) {
-#pragma unroll
-          for (int k = 0; k < kBatch; ++k) {
-            const int i = tid + (k0 + k) * kSoftmax;
-            qv[k] = i < p.H * kPieces ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
-          }
-        };
-        uint32_t qmax = 0;  // largest |q| as bf16 magnitude bits
-#pragma unroll 1
-        for (int k0 = 0; k0 < kPer; k0 += kBatch) {
-          uint4 qv[kBatch];
-          load_batch(k0, qv);
-#pragma unroll
-          for (int k = 0; k < kBatch; ++k) {
-            const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
-          }
-        }
-        qmax = __reduce_max_sync(0xffffffffu, qmax);
-        if (lane == 0) sRed1[warp] = qmax;
-        named_bar_sync(1, kSoftmax);
-#pragma unroll
-        for (int w = 0; w < kSoftmaxWarps; ++w) qmax = max(qmax, sRed1[w]);
-        eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
-        const float qs = pow2i(eq);
-#pragma unroll 1
-        for (int k0 = 0; k0 < kPer; k0 += kBatch) {
-          uint4 qv[kBatch];
-          load_batch(k0, qv);
-#pragma unroll
-          for (int k = 0; k < kBatch; ++k) {
-            const int i = tid + (k0 + k) * kSoftmax;
-            const int h = i / kPieces, d0 = (i % kPieces) * 8;
-            const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-            uint32_t hs[4], ls[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
-                           hs[e], ls[e]);
-            const uint2 hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
-            const uint2 lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
-            int oh, ol;
-            if (d0 < 4 * 128) {
-              const int base = (d0 >> 7) * kChunkBytes;
-              oh = base + sw128(h, d0 & 127);
-              ol = base + sw128(kHeads + h, d0 & 127);
-            } else {
-              oh = kRopeOff + sw64(h, d0 - 512);
-              ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+      if (it.skip) continue;
+      // the run's result or part: O in fp32, or bf16 for a bf16 result
+      void* const out_o = it.out_o;
+      const bool out_bf16 = it.out_bf16;
+      auto put_o = [out_o, out_bf16](long long i, float v) {
+        if (out_bf16) static_cast<__nv_bfloat16*>(out_o)[i] = __float2bfloat16_rn(v);
+        else static_cast<float*>(out_o)[i] = v;
+      };
+      if (it.ntiles > 0) {
+        // ---- [Q_hi | Q_lo] of request b: x = q 2^eq with max |x| in [128, 256).
+        // Every product of the previous item has completed (its epilogue waited
+        // for the last P.V), so the operand can be overwritten; an item of the
+        // same request as the previous one keeps it.
+        const bool new_q = it.b != q_b;
+        if (new_q) {
+          q_b = it.b;
+          const uint4* qsrc = reinterpret_cast<const uint4*>(p.q + (long long)it.b * p.H * kDqk);
+          constexpr int kPieces = kDqk / 8;                   // 16-byte pieces per head
+          constexpr int kPer = kHeads * kPieces / kSoftmax;   // pieces per thread
+          static_assert(kHeads * kPieces % kSoftmax == 0, "query pieces split evenly");
+          constexpr int kBatch = kPer % 6 == 0 ? 6 : 3;  // pieces in flight at once per thread
+          static_assert(kPer % kBatch == 0, "whole batches of pieces");
+          // a batch of this thread's pieces (heads past H are zero)
+          auto load_batch = [&](int k0, uint4* qv) {
+  #pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = tid + (k0 + k) * kSoftmax;
+              qv[k] = i < p.H * kPieces ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
             }
-            *reinterpret_cast<uint2*>(sQ + oh) = hw;
-            *reinterpret_cast<uint2*>(sQ + ol) = lw;
-          }
-        }
-      }
-      if (tid < kHeads) sM[tid] = 0.f;  // set from the item's first tile
-      if (new_q) {
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&bar_q));  // the issuer's first QK^T orders the reset too
-      } else {
-        named_bar_sync(1, kSoftmax);    // the reset before any reader
-      }
-
-      const float* srow = p.sc.p[it.r] + it.row0;
-      const float cq = p.scale_log2 * pow2i(-eq);
-      int gs = 0;  // weights carry scale_row 2^gs (set on the item's first tile, only decreases)
-      float l[kHpw];
-#pragma unroll
-      for (int h = 0; h < kHpw; ++h) l[h] = 0.f;
-      for (int j = 0; j < it.ntiles; ++j, ++g) {
-        const int row = j * kRows + t;
-        const bool valid = row < it.nrows;
-        // Several query rows (s_q > 1): query row qi reads tokens up to
-        // L - s_q + qi, so this cache row is masked for columns [0, mcols).
-        const int tok = it.tok0 + (it.row_begin + row) * it.tok_step;
-        const int mcols = min(kHeads, max(0, tok - (it.ctx_len - p.s_q)) * p.Hrow);
-        const float scale =
-            !valid ? 0.f
-                   : p.rm.table ? __ldg(p.sc.p[0] + map_row(p.rm, it.pair, 0, it.row_begin + row))
-                                : __ldg(srow + row);
-        const int b = g & 1;
-        // The softmax warps leave together: one that gave up meets the others at this vote.
-        const bool got = __all_sync(
-            0xffffffffu, mbar_wait(smem_u32(&bar_s[b]), (g >> 1) & 1, p.wait_ns, &abort_flag));
-        if (bar_red_or(1, kSoftmax, !got)) {
-          if (!got) report_timeout(p.status, 5, &abort_flag);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // u = score - running max (log2 units); rows past the item read nothing
-        const float c = scale * cq;
-        float u[kHpw];
-        float over = -INFINITY;
-        {  // one wait for all of the row's scores (the loads are slow while P.V runs)
-          static_assert(kHpw == 32, "the score load takes 32 heads");
-          uint32_t a[32], z[32];
-          tmem_ld32(lane_addr + 128 * b + hb, a);
-          tmem_ld32(lane_addr + 128 * b + kHeads + hb, z);
-          tmem_ld_wait();
-#pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 4 * h4]);
-            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int h = 4 * h4 + e;
-              u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[h]) + __uint_as_float(z[h]), c, -mm[e])
-                           : -INFINITY;
-              over = fmaxf(over, u[h]);
+          };
+          uint32_t qmax = 0;  // largest |q| as bf16 magnitude bits
+  #pragma unroll 1
+          for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+            uint4 qv[kBatch];
+            load_batch(k0, qv);
+  #pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
             }
           }
-        }
-        // the scores are in registers: the QK^T issuer may refill this S^T buffer
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_sfree[b]));
-        // Block-wide vote: the item's first tile, a score past its running max by
-        // more than 2^3, or a token scale that would take a weight to 2^8 or more.
-        const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
-        if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2 || big)) {
-#pragma unroll
-          for (int h = 0; h < kHpw; ++h) {
-            const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
-            if (lane == 0) sRed[quarter][hb + h] = m;
-          }
-          const uint32_t smx = __reduce_max_sync(0xffffffffu, __float_as_uint(scale));
-          if (lane == 0) sRed1[warp] = smx;
+          qmax = __reduce_max_sync(0xffffffffu, qmax);
+          if (lane == 0) sRed1[warp] = qmax;
           named_bar_sync(1, kSoftmax);
-          uint32_t smb = 0;
-#pragma unroll
-          for (int w = 0; w < kSoftmaxWarps; ++w) smb = max(smb, sRed1[w]);
-          const float smax = __uint_as_float(smb);
-          const int gs_new = j == 0 ? scale_exponent(smax, kWeightTop, 0)
-                                    : min(gs, scale_exponent(smax, kWeightTop, gs));
+  #pragma unroll
+          for (int w = 0; w < kSoftmaxWarps; ++w) qmax = max(qmax, sRed1[w]);
+          eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
+          const float qs = pow2i(eq);
+  #pragma unroll 1
+          for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+            uint4 qv[kBatch];
+            load_batch(k0, qv);
+  #pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int i = tid + (k0 + k) * kSoftmax;
+              const int h = i / kPieces, d0 = (i % kPieces) * 8;
+              const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
+              uint32_t hs[4], ls[4];
+  #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
+                             hs[e], ls[e]);
+              const uint2 hw = make_uint2(hs[0] | (hs[1] << 16), hs[2] | (hs[3] << 16));
+              const uint2 lw = make_uint2(ls[0] | (ls[1] << 16), ls[2] | (ls[3] << 16));
+              int oh, ol;
+              if (d0 < 4 * 128) {
+                const int base = (d0 >> 7) * kChunkBytes;
+                oh = base + sw128(h, d0 & 127);
+                ol = base + sw128(kHeads + h, d0 & 127);
+              } else {
+                oh = kRopeOff + sw64(h, d0 - 512);
+                ol = kRopeOff + sw64(kHeads + h, d0 - 512);
+              }
+              *reinterpret_cast<uint2*>(sQ + oh) = hw;
+              *reinterpret_cast<uint2*>(sQ + ol) = lw;
+            }
+          }
+        }
+        if (run_tiles == 0) {  // a new run: maxima set from its first tile
           if (tid < kHeads) {
-            const float cm = fmaxf(fmaxf(unordered(sRed[0][tid]), unordered(sRed[1][tid])),
-                                   fmaxf(unordered(sRed[2][tid]), unordered(sRed[3][tid])));
-            // (a column with no unmasked row in the item's first tile has none
-            // in the item: rows go up in token order; it keeps max 0, weight 0)
-            const float delta = j == 0 ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
-            sDelta[tid] = delta;
-            sM[tid] += delta;
+            sM[tid] = 0.f;
+            sInit[tid] = 0;
           }
-          named_bar_sync(1, kSoftmax);
-          const float gf = pow2i(max(gs_new - gs, -126));
-#pragma unroll
-          for (int h = 0; h < kHpw; ++h) {
-            const float dl = sDelta[hb + h];
-            u[h] -= dl;
-            l[h] *= ex2(-dl);
-          }
-          if (j > 0) {
-            // O^T holds the earlier tiles: once the last P.V has landed, scale its columns
-            const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1,
-                                                                  p.wait_ns, &abort_flag));
-            if (bar_red_or(1, kSoftmax, !landed)) {
-              if (!landed) report_timeout(p.status, 6, &abort_flag);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            // column h of O^T becomes O^T 2^-delta_h 2^(gs_new - gs)
-#pragma unroll 1
-            for (int c = 0; c < (kHpw / 16) * (kDv / 128); ++c) {
-              const int mb = c / (kHpw / 16), h0 = 16 * (c % (kHpw / 16));
-              uint32_t a[16];
-              tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 16; ++e)
-                a[e] = __float_as_uint(__uint_as_float(a[e]) * (ex2(-sDelta[hb + h0 + e]) * gf));
-              tmem_st16(lane_addr + 256 + 64 * mb + hb + h0, a);
-            }
-            tmem_st_wait();
-          }
-          gs = gs_new;
+          gs = 0;
+  #pragma unroll
+          for (int h = 0; h < kHpw; ++h) l[h] = 0.f;
         }
-        // P^T row t, heads [hb, hb + kHpw): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
-        const float gr = scale * pow2i(gs);
-        uint32_t hw[kHpw / 4], lw[kHpw / 4];
-#pragma unroll
-        for (int k = 0; k < kHpw / 4; ++k) {
-          float pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pk[e] = ex2(u[4 * k + e]);
-            l[4 * k + e] += pk[e];
-          }
-          uint32_t h0, l0, h1, l1;
-          split_e4m3x2(pk[0] * gr, pk[1] * gr, h0, l0);
-          split_e4m3x2(pk[2] * gr, pk[3] * gr, h1, l1);
-          hw[k] = h0 | (h1 << 16);
-          lw[k] = l0 | (l1 << 16);
+        if (new_q) {
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&bar_q));  // the issuer's first QK^T orders the reset too
+        } else {
+          named_bar_sync(1, kSoftmax);    // the reset before any reader
         }
-        // P_lo^T has one buffer: the previous tile's P.V must have read it
-        if (g > 0) {
-          const bool freed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1,
-                                                               p.wait_ns, &abort_flag));
-          if (bar_red_or(1, kSoftmax, !freed)) {
-            if (!freed) report_timeout(p.status, 7, &abort_flag);
+
+        const float* srow = p.sc.p[it.r] + it.row0;
+        const float cq = p.scale_log2 * pow2i(-eq);
+        for (int j = 0; j < it.ntiles; ++j, ++g) {
+          const int row = j * kRows + t;
+          const bool valid = row < it.nrows;
+          // Several query rows (s_q > 1): query row qi reads tokens up to
+          // L - s_q + qi, so this cache row is masked for columns [0, mcols).
+          const int tok = it.tok0 + (it.row_begin + row) * it.tok_step;
+          const int mcols = min(kHeads, max(0, tok - (it.ctx_len - p.s_q)) * p.Hrow);
+          const float scale =
+              !valid ? 0.f
+                     : p.rm.table ? __ldg(p.sc.p[0] + map_row(p.rm, it.pair, 0, it.row_begin + row))
+                                  : __ldg(srow + row);
+          const int b = g & 1;
+          // The softmax warps leave together: one that gave up meets the others at this vote.
+          const bool got = __all_sync(
+              0xffffffffu, mbar_wait(smem_u32(&bar_s[b]), (g >> 1) & 1, p.wait_ns, &abort_flag));
+          if (bar_red_or(1, kSoftmax, !got)) {
+            if (!got) report_timeout(p.status, 5, &abort_flag);
             ok = false;
             break;
           }
+          tc_fence_after();
+          // u = score - running max (log2 units); rows past the item read nothing
+          const float c = scale * cq;
+          float u[kHpw];
+          float over = -INFINITY;
+          {  // one wait for all of the row's scores (the loads are slow while P.V runs)
+            static_assert(kHpw == 32, "the score load takes 32 heads");
+            uint32_t a[32], z[32];
+            tmem_ld32(lane_addr + 128 * b + hb, a);
+            tmem_ld32(lane_addr + 128 * b + kHeads + hb, z);
+            tmem_ld_wait();
+  #pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 4 * h4]);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int h = 4 * h4 + e;
+                u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[h]) + __uint_as_float(z[h]), c, -mm[e])
+                             : -INFINITY;
+                over = fmaxf(over, u[h]);
+              }
+            }
+          }
+          // the scores are in registers: the QK^T issuer may refill this S^T buffer
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_sfree[b]));
+          // Block-wide vote: the item's first tile, a score past its running max by
+          // more than 2^3, or a token scale that would take a weight to 2^8 or more.
+          const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
+          if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2 || big)) {
+  #pragma unroll
+            for (int h = 0; h < kHpw; ++h) {
+              const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
+              if (lane == 0) sRed[quarter][hb + h] = m;
+            }
+            const uint32_t smx = __reduce_max_sync(0xffffffffu, __float_as_uint(scale));
+            if (lane == 0) sRed1[warp] = smx;
+            named_bar_sync(1, kSoftmax);
+            uint32_t smb = 0;
+  #pragma unroll
+            for (int w = 0; w < kSoftmaxWarps; ++w) smb = max(smb, sRed1[w]);
+            const float smax = __uint_as_float(smb);
+            const int gs_new = run_tiles == 0 ? scale_exponent(smax, kWeightTop, 0)
+                                              : min(gs, scale_exponent(smax, kWeightTop, gs));
+            if (tid < kHeads) {
+              const float cm = fmaxf(fmaxf(unordered(sRed[0][tid]), unordered(sRed[1][tid])),
+                                     fmaxf(unordered(sRed[2][tid]), unordered(sRed[3][tid])));
+              // A column takes its max from its first unmasked rows; until then it
+              // keeps max 0 and weight 0.  Within an item rows go up in token
+              // order, so a column masked in an item's first tile stays masked in
+              // the item; a later item of the run (another shard) may unmask it,
+              // and its first tile always votes.
+              float delta;
+              if (!sInit[tid]) {
+                delta = cm == -INFINITY ? 0.f : cm;
+                if (cm != -INFINITY) sInit[tid] = 1;
+              } else {
+                delta = cm > kRescaleLog2 ? cm : 0.f;
+              }
+              sDelta[tid] = delta;
+              sM[tid] += delta;
+            }
+            named_bar_sync(1, kSoftmax);
+            const float gf = pow2i(max(gs_new - gs, -126));
+  #pragma unroll
+            for (int h = 0; h < kHpw; ++h) {
+              const float dl = sDelta[hb + h];
+              u[h] -= dl;
+              l[h] *= ex2(-dl);
+            }
+            if (run_tiles > 0) {
+              // O^T holds the run's earlier tiles: once the last P.V has landed, scale its columns
+              const bool landed = __all_sync(
+                  0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1, p.wait_ns,
+                                         &abort_flag));
+              if (bar_red_or(1, kSoftmax, !landed)) {
+                if (!landed) report_timeout(p.status, 6, &abort_flag);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // column h of O^T becomes O^T 2^-delta_h 2^(gs_new - gs)
+  #pragma unroll 1
+              for (int c = 0; c < (kHpw / 16) * (kDv / 128); ++c) {
+                const int mb = c / (kHpw / 16), h0 = 16 * (c % (kHpw / 16));
+                uint32_t a[16];
+                tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  a[e] = __float_as_uint(__uint_as_float(a[e]) * (ex2(-sDelta[hb + h0 + e]) * gf));
+                tmem_st16(lane_addr + 256 + 64 * mb + hb + h0, a);
+              }
+              tmem_st_wait();
+            }
+            gs = gs_new;
+          }
+          // P^T row t, heads [hb, hb + kHpw): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
+          const float gr = scale * pow2i(gs);
+          uint32_t hw[kHpw / 4], lw[kHpw / 4];
+  #pragma unroll
+          for (int k = 0; k < kHpw / 4; ++k) {
+            float pk[4];
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pk[e] = ex2(u[4 * k + e]);
+              l[4 * k + e] += pk[e];
+            }
+            uint32_t h0, l0, h1, l1;
+            split_e4m3x2(pk[0] * gr, pk[1] * gr, h0, l0);
+            split_e4m3x2(pk[2] * gr, pk[3] * gr, h1, l1);
+            hw[k] = h0 | (h1 << 16);
+            lw[k] = l0 | (l1 << 16);
+          }
+          // P_lo^T has one buffer: the previous tile's P.V must have read it
+          if (g > 0) {
+            const bool freed = __all_sync(
+                0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1, p.wait_ns,
+                                       &abort_flag));
+            if (bar_red_or(1, kSoftmax, !freed)) {
+              if (!freed) report_timeout(p.status, 7, &abort_flag);
+              ok = false;
+              break;
+            }
+          }
+          // MN-major operands [128 rows][64 heads], 64-byte swizzle; P_hi^T over the
+          // rope chunk of this tile's stage (QK^T(g) has read it)
+          uint8_t* phi = smem + b * kStageBytes + kRopeOff;
+  #pragma unroll
+          for (int k = 0; k < kHpw / 16; ++k) {
+            *reinterpret_cast<uint4*>(phi + sw64(t, hb + 16 * k)) =
+                make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
+            *reinterpret_cast<uint4*>(sPlo + sw64(t, hb + 16 * k)) =
+                make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bar_p));
+          ++run_tiles;
         }
-        // MN-major operands [128 rows][64 heads], 64-byte swizzle; P_hi^T over the
-        // rope chunk of this tile's stage (QK^T(g) has read it)
-        uint8_t* phi = smem + b * kStageBytes + kRopeOff;
-#pragma unroll
-        for (int k = 0; k < kHpw / 16; ++k) {
-          *reinterpret_cast<uint4*>(phi + sw64(t, hb + 16 * k)) =
-              make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
-          *reinterpret_cast<uint4*>(sPlo + sw64(t, hb + 16 * k)) =
-              make_uint4(lw[4 * k], lw[4 * k + 1], lw[4 * k + 2], lw[4 * k + 3]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bar_p));
+        if (!ok) break;
       }
-      if (!ok) break;
+      if (!it.run_end) continue;
+      if (run_tiles == 0) {  // no rows in the run (an empty shard): O = 0, LSE = -inf
+        for (int i = tid; i < p.H * kDv; i += kSoftmax) put_o(i, 0.f);
+        for (int i = tid; i < p.H; i += kSoftmax) it.out_l[i] = -INFINITY;
+        continue;
+      }
+      run_tiles = 0;
       // ---- epilogue: column sums of l, O^T 2^-gs / l, LSE
       const bool landed = __all_sync(
           0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1, p.wait_ns, &abort_flag));
@@ -750,8 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
           const int hh = hb + h0 + h;
-          if (hh < p.H)
-            it.out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * og * sDelta[hh];
+          if (hh < p.H) put_o((long long)hh * kDv + 128 * mb + t, __uint_as_float(a[h]) * og * sDelta[hh]);
         }
       }
       tc_fence_before();
@@ -771,9 +835,13 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
                                   const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                   const int32_t* pair_count, unsigned long long wait_ns,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const MergedOut* mo) {
   Params p;
   p.pair_count = pair_count;
+  p.run_out = mo ? mo->run_out : nullptr;
+  p.o_fin = mo ? mo->o : nullptr;
+  p.o_fin_bf16 = mo && mo->o_bf16 ? 1 : 0;
+  p.lse_fin = mo ? mo->lse : nullptr;
   p.plan = dev_plan;
   p.B = h.R;
   p.off_pair = h.off_rank;

@@ -88,6 +88,11 @@ cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
                              cudaStream_t s);
 cudaError_t launch_lse_fold(int N, int H, int Dv, float* o, float* lse, const float* o_add,
                             const float* lse_add, cudaStream_t s);
+// The merged decode's requests whose result comes from parts (the plan's
+// merge list, n_list entries {request, first slot, parts}).
+cudaError_t launch_merge_runs(const int32_t* dev_plan, const cp_plan_header& h, int n_list, int H, int Dv,
+                              const float* ws_o, const float* ws_lse, void* o, bool o_bf16, float* lse,
+                              cudaStream_t s);
 cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h, int H, int Dv,
                                 const float* ws_o, const float* ws_lse, float* o_part,
                                 float* lse_part, cudaStream_t s);
@@ -116,13 +121,25 @@ bool encode_tensor_map_u8_2d(CUtensorMap* m, const void* base, uint64_t cols, ui
                              uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
                              bool swizzle_128);
 
+// The merged-output decode's destinations: the plan's run table (device),
+// the requests' results O [B][H][Dv] (bf16 or fp32) and LSE [B][H]; parts go
+// to the workspace slots ws_o / ws_lse.
+struct MergedOut {
+  const int32_t* run_out;
+  void* o;
+  bool o_bf16;
+  float* lse;
+};
+
 // ---- MLA decode over an FP8 cache on FP8 tensor-core products (decode_mla_fp8.cu)
+// With mo, a worker's consecutive items of one request accumulate as one run
+// (per-item partials otherwise).
 cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header& h, const void* q,
                                   const ShardPtrs& k, const ScalePtrs& sc,
                                   const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                   float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                   const int32_t* pair_count, unsigned long long wait_ns,
-                                  cudaStream_t s);
+                                  cudaStream_t s, const MergedOut* mo = nullptr);
 
 // ---- tensor-core MLA decode over a bf16 cache (decode_mla_tc.cu)
 cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& h,

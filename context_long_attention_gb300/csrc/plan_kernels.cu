@@ -80,20 +80,24 @@ __global__ void page_tail_zero_kernel(const int32_t* __restrict__ plan, int off_
   }
 }
 
-// Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride.
+// Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride
+// (any P: a warp takes the parts 32 at a time, lane u holding part p0 + u's
+// weight; the sums take the parts in order).
 __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, long long ostride,
                                           const float* __restrict__ l, long long lstride, int Dv,
                                           float* out_f32, __nv_bfloat16* out_bf16, float* out_lse) {
   const int lane = threadIdx.x & 31;
-  float l0 = lane < P ? l[lane * lstride] : -INFINITY;
-  float l1 = lane + 32 < P ? l[(lane + 32) * lstride] : -INFINITY;
-  float g = fmaxf(l0, l1);
+  float g = -INFINITY;
+  for (int p = lane; p < P; p += 32) g = fmaxf(g, l[p * lstride]);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, d));
   const bool any = g != -INFINITY;
-  const float w0 = (any && l0 != -INFINITY) ? expf(l0 - g) : 0.f;
-  const float w1 = (any && l1 != -INFINITY) ? expf(l1 - g) : 0.f;
-  float z = w0 + w1;
+  auto weight = [&](int p) {  // part p's weight exp(LSE_p - max), 0 for an empty part or p >= P
+    const float lp = p < P ? l[p * lstride] : -INFINITY;
+    return (any && lp != -INFINITY) ? expf(lp - g) : 0.f;
+  };
+  float z = 0.f;
+  for (int p0 = 0; p0 < P; p0 += 32) z += weight(p0 + lane);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
   const float inv = any ? 1.f / z : 0.f;
@@ -103,14 +107,18 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
     const int c = c0 + lane;
     const bool active = c < Dv / 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p = 0; p < P; ++p) {
-      const float w = __shfl_sync(0xffffffffu, p < 32 ? w0 : w1, p & 31);
-      if (active && w != 0.f) {
-        const float4 x = reinterpret_cast<const float4*>(o + p * ostride)[c];
-        acc.x += w * x.x;
-        acc.y += w * x.y;
-        acc.z += w * x.z;
-        acc.w += w * x.w;
+    for (int p0 = 0; p0 < P; p0 += 32) {
+      const float wl = weight(p0 + lane);
+      const int np = min(32, P - p0);
+      for (int u = 0; u < np; ++u) {
+        const float w = __shfl_sync(0xffffffffu, wl, u);
+        if (active && w != 0.f) {
+          const float4 x = reinterpret_cast<const float4*>(o + (long long)(p0 + u) * ostride)[c];
+          acc.x += w * x.x;
+          acc.y += w * x.y;
+          acc.z += w * x.z;
+          acc.w += w * x.w;
+        }
       }
     }
     acc.x *= inv;
@@ -165,6 +173,23 @@ __global__ void lse_fold_kernel(long long NH, int Dv, float* __restrict__ o, flo
   for (int c = lane; c < Dv; c += 32) od[c] = a0 * od[c] + a1 * oa[c];
   __syncwarp();
   if (lane == 0) lse[i] = lg;
+}
+
+// Requests of a merged decode whose result comes from parts: one warp per
+// (listed request, head) combines the request's parts [first, first + n)
+// (n = 0, a request with no rows: O = 0, LSE = -inf).
+__global__ void merge_runs_kernel(const int32_t* __restrict__ list, int n_list, int H, int Dv,
+                                  const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
+                                  void* __restrict__ o, int o_bf16, float* __restrict__ lse) {
+  const long long i = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (i >= (long long)n_list * H) return;
+  const int m = (int)(i / H), h = (int)(i % H);
+  const int b = list[3 * m], first = list[3 * m + 1], n = list[3 * m + 2];
+  const long long ob = (long long)b * H + h;
+  float* of = o_bf16 ? nullptr : static_cast<float*>(o) + ob * Dv;
+  __nv_bfloat16* obf = o_bf16 ? static_cast<__nv_bfloat16*>(o) + ob * Dv : nullptr;
+  merge_row(n, ws_o + ((long long)first * H + h) * Dv, (long long)H * Dv, ws_lse + (long long)first * H + h, H,
+            Dv, of, obf, lse + ob);
 }
 
 __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
@@ -224,6 +249,19 @@ cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
   const long long blocks = (NH + warps - 1) / warps;
   lse_merge_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(P, NH, Dv, o_part, lse_part, o,
                                                            o_bf16 ? 1 : 0, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_runs(const int32_t* dev_plan, const cp_plan_header& h, int n_list, int H, int Dv,
+                              const float* ws_o, const float* ws_lse, void* o, bool o_bf16, float* lse,
+                              cudaStream_t s) {
+  if (n_list == 0) return cudaSuccess;
+  const long long warps_needed = (long long)n_list * H;
+  const int warps = 8;
+  const long long blocks = (warps_needed + warps - 1) / warps;
+  const int32_t* list = dev_plan + h.off_run + 2 + h.n_seg;
+  merge_runs_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(list, n_list, H, Dv, ws_o, ws_lse, o, o_bf16 ? 1 : 0,
+                                                           lse);
   return cudaGetLastError();
 }
 

@@ -353,6 +353,41 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
                          void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * cp_decode_attn_merged — cp_decode_attn followed by cp_lse_merge over the C
+ * partials, in one call: o [B, H, Dv] (o_dtype CP_BF16 or CP_FP32) and
+ * lse [B, H] fp32 (natural log), the attention over each request's whole
+ * cache ([CTX] §3.3; [V4] §5).  Arguments as for cp_decode_attn.
+ *
+ * With an MLA FP8 cache (per-shard buffers) the partials never leave the
+ * GPU's tensor memory where they need not: the plan's run table (the header's
+ * off_run, built with every decode plan) groups each worker's consecutive
+ * work items of one request into a run, and the run accumulates all of them
+ * (the shards' partial softmax combines exactly across them, as in the
+ * merge).  A run holding all of its request's rows writes the result; the
+ * runs of a request cut by a worker boundary write fp32 parts, which a merge
+ * combines.  Short requests, whose C shards fit in one worker, then cost no
+ * partial at all.  Other caches run cp_decode_attn into the workspace and
+ * merge there.
+ *
+ * Run table at off_run (int32): n_parts, n_list, then run_out[n_work] (per
+ * work item: -1 the run goes on to the worker's next item, -2 the last item
+ * of a run holding its whole request, k >= 0 the last item of a run that is
+ * one of its request's parts, written to part slot k, -3 an empty pair's
+ * item), then n_list entries {request, first part slot, parts} (a request's
+ * parts are consecutive slots; a request with no rows is listed with none
+ * and gets O = 0, LSE = -inf).
+ * ws: cp_decode_merged_workspace_size() bytes (NULL if 0).  Errors as for
+ * cp_decode_attn; CP_ERR_INVALID_ARG also for a selection plan.
+ * ------------------------------------------------------------------------- */
+cp_status cp_decode_merged_workspace_size(const void* host_plan, cp_decode_mode mode, cp_dtype kv_dtype,
+                                          int H, int Dv, size_t* bytes);
+cp_status cp_decode_attn_merged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
+                                cp_dtype kv_dtype, const void* q, const void* const* shard_k,
+                                const void* const* shard_v, const float* const* shard_scale, int Hq,
+                                int Hkv, int Dqk, int Dv, float sm_scale, void* o, cp_dtype o_dtype,
+                                float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Sparse decode with an exact sharded top-k ("DeepSeek-V4 Attention
  * Inference Systems" §5.2; [CTX] §4.1, the index split with the cache).
  *
