@@ -50,8 +50,8 @@ PROFILED_TRAFFIC = {
                 "sha1": "df3c47221f9a4778217bee17d5d95d14f5eea68b", "bytes": 2.373758e9 + 0.275600e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "8a956f900500e87b6853cccde1bb8bbb3839ab88",
-                   "bytes_per_token": (0.610018e9 + 0.009791e9) / (8 * 131072)},
+                   "sha1": "b364057a3d6f0353e3589c08c0396c74cfa38f44",
+                   "bytes_per_token": (0.611841e9 + 0.009328e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "04100416602e6fe976f64f3844df844162af152b",
@@ -62,7 +62,8 @@ PROFILED_TRAFFIC = {
                    "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
     "decode_fp8_merged": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                                   "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                          "sha1": None, "bytes_per_token": None},
+                          "sha1": "b364057a3d6f0353e3589c08c0396c74cfa38f44",
+                          "bytes_per_token": (0.609454e9 + 0.000456e9) / (8 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "c19956b2693cf34223e556901c4c0d1891584060",

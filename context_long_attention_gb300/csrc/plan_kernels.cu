@@ -110,14 +110,27 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
     for (int p0 = 0; p0 < P; p0 += 32) {
       const float wl = weight(p0 + lane);
       const int np = min(32, P - p0);
-      for (int u = 0; u < np; ++u) {
-        const float w = __shfl_sync(0xffffffffu, wl, u);
-        if (active && w != 0.f) {
-          const float4 x = reinterpret_cast<const float4*>(o + (long long)(p0 + u) * ostride)[c];
-          acc.x += w * x.x;
-          acc.y += w * x.y;
-          acc.z += w * x.z;
-          acc.w += w * x.w;
+      // kBatch parts' loads in flight before they are summed (in order)
+      constexpr int kBatch = 8;
+      for (int u0 = 0; u0 < np; u0 += kBatch) {
+        float w[kBatch];
+        float4 x[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          w[k] = __shfl_sync(0xffffffffu, wl, (u0 + k) & 31);
+          const bool use = active && u0 + k < np && w[k] != 0.f;
+          x[k] = use ? reinterpret_cast<const float4*>(o + (long long)(p0 + u0 + k) * ostride)[c]
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!use) w[k] = 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (w[k] != 0.f) {
+            acc.x += w[k] * x[k].x;
+            acc.y += w[k] * x[k].y;
+            acc.z += w[k] * x[k].z;
+            acc.w += w[k] * x[k].w;
+          }
         }
       }
     }
