@@ -17,7 +17,7 @@
 // |x| >= 2^-2 and an absolute error <= 2^-10 below that:
 //   query:   x = q 2^e_q, with e_q per request so that max |x| is in [128, 256)
 //   weights: x = 2^(s - M_h) scale_row 2^g, with M_h the running max of head h
-//            and g per work item so that scale_row 2^g < 32; the running max
+//            and g per run of work items so that scale_row 2^g < 32; the running max
 //            moves when a score passes it by more than 2^3, so x < 256
 // The products (transposed so that M = 128 KV rows):
 //   S^T [128 rows x 128] = K_codes [128 x 576] . [Q_hi | Q_lo]^T   (N = 128)
@@ -268,7 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float sDelta[kHeads];            // its last move; in the epilogue 1 / column sum
   __shared__ int sRed[4][kHeads];             // per row-quarter column maxima, then column sums
   __shared__ uint32_t sRed1[kSoftmaxWarps];   // per-warp max of |q| or of the token scales
-  __shared__ int sInit[kHeads];               // head h has had an unmasked row in the current run
+  __shared__ uint32_t sInit[kHeads / 32];     // bit h: head h has had an unmasked row in the current run
+  __shared__ int sMoved;                      // a vote moved some running max
+  // (static shared memory has 2 KB beside the 225 KB of operands: keep these small)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -538,42 +540,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           static_assert(kPer % kBatch == 0, "whole batches of pieces");
           // a batch of this thread's pieces (heads past H are zero)
           auto load_batch = [&](int k0, uint4* qv) {
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < kBatch; ++k) {
               const int i = tid + (k0 + k) * kSoftmax;
               qv[k] = i < p.H * kPieces ? __ldg(qsrc + i) : make_uint4(0, 0, 0, 0);
             }
           };
           uint32_t qmax = 0;  // largest |q| as bf16 magnitude bits
-  #pragma unroll 1
+#pragma unroll 1
           for (int k0 = 0; k0 < kPer; k0 += kBatch) {
             uint4 qv[kBatch];
             load_batch(k0, qv);
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < kBatch; ++k) {
               const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) qmax = max(qmax, max(w[e] & 0x7FFFu, (w[e] >> 16) & 0x7FFFu));
             }
           }
           qmax = __reduce_max_sync(0xffffffffu, qmax);
           if (lane == 0) sRed1[warp] = qmax;
           named_bar_sync(1, kSoftmax);
-  #pragma unroll
+#pragma unroll
           for (int w = 0; w < kSoftmaxWarps; ++w) qmax = max(qmax, sRed1[w]);
           eq = scale_exponent(__uint_as_float(qmax << 16), 8, 0);
           const float qs = pow2i(eq);
-  #pragma unroll 1
+#pragma unroll 1
           for (int k0 = 0; k0 < kPer; k0 += kBatch) {
             uint4 qv[kBatch];
             load_batch(k0, qv);
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < kBatch; ++k) {
               const int i = tid + (k0 + k) * kSoftmax;
               const int h = i / kPieces, d0 = (i % kPieces) * 8;
               const uint32_t w[4] = {qv[k].x, qv[k].y, qv[k].z, qv[k].w};
               uint32_t hs[4], ls[4];
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e)
                 split_e4m3x2(__uint_as_float(w[e] << 16) * qs, __uint_as_float(w[e] & 0xFFFF0000u) * qs,
                              hs[e], ls[e]);
@@ -594,12 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (run_tiles == 0) {  // a new run: maxima set from its first tile
-          if (tid < kHeads) {
-            sM[tid] = 0.f;
-            sInit[tid] = 0;
-          }
+          if (tid < kHeads) sM[tid] = 0.f;
+          if (tid < kHeads / 32) sInit[tid] = 0u;
           gs = 0;
-  #pragma unroll
+#pragma unroll
           for (int h = 0; h < kHpw; ++h) l[h] = 0.f;
         }
         if (new_q) {
@@ -642,11 +642,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(lane_addr + 128 * b + hb, a);
             tmem_ld32(lane_addr + 128 * b + kHeads + hb, z);
             tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
             for (int h4 = 0; h4 < 8; ++h4) {
               const float4 m4 = *reinterpret_cast<const float4*>(&sM[hb + 4 * h4]);
               const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int h = 4 * h4 + e;
                 u[h] = valid && hb + h >= mcols ? fmaf(__uint_as_float(a[h]) + __uint_as_float(z[h]), c, -mm[e])
@@ -661,8 +661,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Block-wide vote: the item's first tile, a score past its running max by
           // more than 2^3, or a token scale that would take a weight to 2^8 or more.
           const bool big = valid && scale * pow2i(gs) >= (float)(1 << kWeightTop);
-          if (bar_red_or(1, kSoftmax, j == 0 || over > kRescaleLog2 || big)) {
-  #pragma unroll
+          // A run's first tile sets the maxima.  A later item's first tile votes
+          // only with several query rows, when heads masked so far may meet
+          // their first rows (with one row every head is set on the run's
+          // first tile).
+          const bool first = j == 0 && (run_tiles == 0 || p.s_q > 1);
+          if (bar_red_or(1, kSoftmax, first || over > kRescaleLog2 || big)) {
+            if (tid == 0) sMoved = 0;
+#pragma unroll
             for (int h = 0; h < kHpw; ++h) {
               const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
               if (lane == 0) sRed[quarter][hb + h] = m;
@@ -671,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) sRed1[warp] = smx;
             named_bar_sync(1, kSoftmax);
             uint32_t smb = 0;
-  #pragma unroll
+#pragma unroll
             for (int w = 0; w < kSoftmaxWarps; ++w) smb = max(smb, sRed1[w]);
             const float smax = __uint_as_float(smb);
             const int gs_new = run_tiles == 0 ? scale_exponent(smax, kWeightTop, 0)
@@ -685,24 +691,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the item; a later item of the run (another shard) may unmask it,
               // and its first tile always votes.
               float delta;
-              if (!sInit[tid]) {
+              if (!((sInit[tid >> 5] >> (tid & 31)) & 1u)) {
                 delta = cm == -INFINITY ? 0.f : cm;
-                if (cm != -INFINITY) sInit[tid] = 1;
+                if (cm != -INFINITY) atomicOr(&sInit[tid >> 5], 1u << (tid & 31));
               } else {
                 delta = cm > kRescaleLog2 ? cm : 0.f;
               }
               sDelta[tid] = delta;
+            if (delta != 0.f) sMoved = 1;
               sM[tid] += delta;
             }
             named_bar_sync(1, kSoftmax);
             const float gf = pow2i(max(gs_new - gs, -126));
-  #pragma unroll
+#pragma unroll
             for (int h = 0; h < kHpw; ++h) {
               const float dl = sDelta[hb + h];
               u[h] -= dl;
               l[h] *= ex2(-dl);
             }
-            if (run_tiles > 0) {
+            if (run_tiles > 0 && (sMoved || gs_new != gs)) {
               // O^T holds the run's earlier tiles: once the last P.V has landed, scale its columns
               const bool landed = __all_sync(
                   0xffffffffu, mbar_wait(smem_u32(&bar_done[(g - 1) & 1][3]), ((g - 1) >> 1) & 1, p.wait_ns,
@@ -714,13 +721,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tc_fence_after();
               // column h of O^T becomes O^T 2^-delta_h 2^(gs_new - gs)
-  #pragma unroll 1
+#pragma unroll 1
               for (int c = 0; c < (kHpw / 16) * (kDv / 128); ++c) {
                 const int mb = c / (kHpw / 16), h0 = 16 * (c % (kHpw / 16));
                 uint32_t a[16];
                 tmem_ld16(lane_addr + 256 + 64 * mb + hb + h0, a);
                 tmem_ld_wait();
-  #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 16; ++e)
                   a[e] = __float_as_uint(__uint_as_float(a[e]) * (ex2(-sDelta[hb + h0 + e]) * gf));
                 tmem_st16(lane_addr + 256 + 64 * mb + hb + h0, a);
@@ -732,10 +739,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P^T row t, heads [hb, hb + kHpw): p = 2^u, weight x = p scale_row 2^gs as E4M3 hi + lo
           const float gr = scale * pow2i(gs);
           uint32_t hw[kHpw / 4], lw[kHpw / 4];
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < kHpw / 4; ++k) {
             float pk[4];
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < 4; ++e) {
               pk[e] = ex2(u[4 * k + e]);
               l[4 * k + e] += pk[e];
@@ -760,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // MN-major operands [128 rows][64 heads], 64-byte swizzle; P_hi^T over the
           // rope chunk of this tile's stage (QK^T(g) has read it)
           uint8_t* phi = smem + b * kStageBytes + kRopeOff;
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < kHpw / 16; ++k) {
             *reinterpret_cast<uint4*>(phi + sw64(t, hb + 16 * k)) =
                 make_uint4(hw[4 * k], hw[4 * k + 1], hw[4 * k + 2], hw[4 * k + 3]);
