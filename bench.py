@@ -50,8 +50,8 @@ PROFILED_TRAFFIC = {
                 "sha1": "df3c47221f9a4778217bee17d5d95d14f5eea68b", "bytes": 2.373758e9 + 0.275600e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "b364057a3d6f0353e3589c08c0396c74cfa38f44",
-                   "bytes_per_token": (0.611841e9 + 0.009328e9) / (8 * 131072)},
+                   "sha1": "7501f84c4ada68b34b362adafb9d101b145321ff",
+                   "bytes_per_token": (0.611987e9 + 0.009694e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "04100416602e6fe976f64f3844df844162af152b",
@@ -62,8 +62,8 @@ PROFILED_TRAFFIC = {
                    "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
     "decode_fp8_merged": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                                   "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                          "sha1": "b364057a3d6f0353e3589c08c0396c74cfa38f44",
-                          "bytes_per_token": (0.609454e9 + 0.000456e9) / (8 * 131072)},
+                          "sha1": "7501f84c4ada68b34b362adafb9d101b145321ff",
+                          "bytes_per_token": (0.609247e9 + 0.003282e9) / (8 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "c19956b2693cf34223e556901c4c0d1891584060",
@@ -378,6 +378,10 @@ def sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, wo
     o_dec = torch.empty((B, Hr, Dv), dtype=torch.bfloat16, device=dev)
     lse_dec = torch.empty((B, Hr), dtype=torch.float32, device=dev)
     dws = torch.empty(max(16, cp.cp_decode_workspace_size(splan, Hr, Dv)), dtype=torch.uint8, device=dev)
+    mws = torch.empty(max(16, cp.cp_decode_merged_workspace_size(
+        splan, cp.CP_DECODE_MLA, cp.CP_FP8_E4M3 if fp8 else cp.CP_BF16, Hr, Dv)), dtype=torch.uint8, device=dev)
+    o_one = torch.empty_like(o_dec)
+    lse_one = torch.empty_like(lse_dec)
     scale = 1.0 / math.sqrt(m["Dqk"])
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
@@ -392,29 +396,37 @@ def sparse_leg(cp, args, dev, stream, ctx, m, fp8, dplan, shards, scales, dq, wo
         e[3].record(stream)
         cp.cp_lse_merge(o_part, lse_part, out=o_dec, lse=lse_dec)
         e[4].record(stream)
+        # the attention and the merge in one call, over the same selection
+        cp.cp_sparse_decode_attn_merged(splan, pc, cp.CP_DECODE_MLA, dq, selk, sel_scale=selsc, sm_scale=scale,
+                                        o=o_one, lse=lse_one, ws=mws)
+        e[5].record(stream)
 
     for _ in range(max(3, args.warmup)):
-        step([ev() for _ in range(5)])
+        step([ev() for _ in range(6)])
     torch.cuda.synchronize(dev)
     cp.cp_device_error_check(dev)
-    recs = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    recs = [[ev() for _ in range(6)] for _ in range(args.steps)]
     barrier(world)
     for i in range(args.steps):
         step(recs[i])
     torch.cuda.synchronize(dev)
     barrier(world)
     cp.cp_device_error_check(dev)
-    stage = [[r[i].elapsed_time(r[i + 1]) for r in recs] for i in range(4)]
-    total = max_over_ranks(sum(sum(x) for x in stage), world)
+    stage = [[r[i].elapsed_time(r[i + 1]) for r in recs] for i in range(5)]
+    total = max_over_ranks(sum(sum(x) for x in stage[:4]), world)
+    total_one = max_over_ranks(sum(stage[0]) + sum(stage[1]) + sum(stage[4]), world)
     row = 580 if fp8 else 1152
     alg = 4 * sum(ctx) + B * k * row + B * Hr * 576 * 2 + B * Hr * 512 * 2
     return {"k": k, "workload": f"{B} x {L} tokens, C={C}, top-{k} of per-token fp32 scores, "
                                 f"MLA {'FP8' if fp8 else 'bf16'} rows",
             "ms": {"topk": statistics.mean(stage[0]), "gather": statistics.mean(stage[1]),
-                   "decode": statistics.mean(stage[2]), "merge": statistics.mean(stage[3])},
+                   "decode": statistics.mean(stage[2]), "merge": statistics.mean(stage[3]),
+                   "decode_and_merge_one_call": statistics.mean(stage[4])},
+            "value_one_call": whole_job_rate(alg * args.steps, total_one, world) / 1e9,
             "algorithmic_bytes_per_step": alg,
             "value": whole_job_rate(alg * args.steps, total, world) / 1e9, "unit": "GB/s",
-            "note": "scores read once + selected rows once + Q + O over the time of all four stages"}
+            "note": "scores read once + selected rows once + Q + O over the time of all four stages; "
+                    "value_one_call: top-k + gather + cp_sparse_decode_attn_merged"}
 
 
 def time_region(dev, stream, world, step, steps, warmup):

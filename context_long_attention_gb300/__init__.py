@@ -45,6 +45,7 @@ from ._binding import (  # noqa: F401
     cp_prefill_attn,
     cp_shard_plan,
     cp_sparse_decode_attn,
+    cp_sparse_decode_attn_merged,
     cp_sparse_gather,
     cp_sparse_plan,
     cp_sparse_topk,

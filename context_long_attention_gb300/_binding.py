@@ -80,6 +80,8 @@ _SIGS = {
     "cp_sparse_plan": (_i, [_i, _i, _i, _i, _vp, _sz, _vp, _sz, _vp]),
     "cp_sparse_decode_attn": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
                                    _vp, _vp, _vp, _sz, _vp]),
+    "cp_sparse_decode_attn_merged": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f,
+                                          _vp, _i, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -670,6 +672,38 @@ def cp_sparse_decode_attn(plan: DecodePlan, pair_count, mode: int, q, sel_k, sel
                                      H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o_part), _ptr(lse_part),
                                      _ptr(ws), ws_bytes, _stream(q.device)))
     return o_part, lse_part
+
+
+def cp_sparse_decode_attn_merged(plan: DecodePlan, pair_count, mode: int, q, sel_k, sel_v=None,
+                                 sel_scale=None, sm_scale=None, out_dtype=torch.bfloat16, o=None, lse=None,
+                                 ws=None):
+    """cp_sparse_decode_attn and the LSE merge of its partials in one call:
+    returns (o [B, H, Dv] out_dtype, lse [B, H] fp32)."""
+    B, H, Dqk = q.shape
+    sk = [t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t for t in sel_k]
+    _need_cuda(q, pair_count, *sk, o, lse)
+    kv_dtype = _dtype_code(sk[0])
+    if mode == CP_DECODE_MLA:
+        Hkv, Dv = 1, 512
+    else:
+        Hkv, Dv = sk[0].shape[1], Dqk
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(Dqk)
+    if o is None:
+        o = torch.empty((B, H, Dv), dtype=out_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    need = cp_decode_merged_workspace_size(plan, mode, kv_dtype, H, Dv)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.cp_sparse_decode_attn_merged(_np_ptr(plan.host), _ptr(plan.dev), _ptr(pair_count), mode,
+                                            kv_dtype, _ptr(q), _ptr_array(sk),
+                                            _ptr_array(sel_v) if sel_v is not None else None,
+                                            _ptr_array(sel_scale) if sel_scale is not None else None,
+                                            H, Hkv, Dqk, Dv, float(sm_scale), _ptr(o), _dtype_code(o), _ptr(lse),
+                                            _ptr(ws), ws_bytes, _stream(q.device)))
+    return o, lse
 
 
 # ---------------------------------------------------------------- NVTX ranges

@@ -627,6 +627,48 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   return ok();
 }
 
+// The decode and the merge of its partials into o / lse: over an MLA FP8
+// cache a worker's items of one request accumulate as one run (the plan's run
+// table) and only runs cut by a worker boundary leave parts; other caches
+// write the per-shard partials into the workspace and merge them there.
+cp_status run_decode_merged(const cp_plan_header& h, const int32_t* W, const void* dev_plan, cp_decode_mode mode,
+                            cp_dtype kv_dtype, const void* q, const ShardPtrs& K, const ShardPtrs& V,
+                            const ScalePtrs& S, const long long* shard_rows, int Hq, int Hkv, int Dqk, int Dv,
+                            float sm_scale, void* o, cp_dtype o_dtype, float* lse, void* ws, size_t ws_bytes,
+                            void* stream, const int32_t* pair_count) {
+  RowMap rm;
+  memset(&rm, 0, sizeof(rm));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Hc = Hq * plan_s_q(h);
+  const bool bf16 = o_dtype == CP_BF16;
+  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3) {
+    // runs accumulate in the kernel; only the runs cut by a worker boundary leave parts
+    const int n_mparts = W[h.off_run], n_list = W[h.off_run + 1];
+    float* ws_o = (float*)ws;
+    float* ws_lse = ws_o ? ws_o + (size_t)n_mparts * Hc * Dv : nullptr;
+    const int32_t* plan = (const int32_t*)dev_plan;
+    const MergedOut mo = {plan + h.off_run + 2, o, bf16, lse};
+    cudaError_t e = launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, nullptr, nullptr, ws_o,
+                                          ws_lse, pair_count, wait_limit_ns(), s, &mo);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    e = launch_merge_runs(plan, h, n_list, Hc, Dv, ws_o, ws_lse, o, bf16, lse, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge of the runs' parts");
+    return ok();
+  }
+  // other caches: the per-shard partials in the workspace, then their merge
+  float* o_part = (float*)ws;
+  float* lse_part = o_part + (size_t)h.C * h.R * Hc * Dv;
+  const size_t part_bytes = ((size_t)h.C * h.R * Hc * (Dv + 1) * sizeof(float) + 15) / 16 * 16;
+  const cp_status st = run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv,
+                                  sm_scale, o_part, lse_part, (uint8_t*)ws + part_bytes, ws_bytes - part_bytes,
+                                  stream, pair_count);
+  if (st != CP_OK) return st;
+  const cudaError_t e = launch_lse_merge(h.C, h.R, Hc, Dv, o_part, lse_part, o, bf16, lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "LSE merge kernel");
+  return ok();
+}
+
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -910,35 +952,8 @@ cp_status cp_decode_attn_merged(const void* host_plan, const void* dev_plan, cp_
       if (rows_r > 0 && !shard_scale[r]) return fail(CP_ERR_INVALID_ARG, "shard_scale[%d] is NULL", r);
     }
   }
-  RowMap rm;
-  memset(&rm, 0, sizeof(rm));
-  cudaStream_t s = (cudaStream_t)stream;
-  const int Hc = Hq * plan_s_q(h);
-  const bool bf16 = o_dtype == CP_BF16;
-  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3) {
-    // runs accumulate in the kernel; only the runs cut by a worker boundary leave parts
-    const int n_mparts = W[h.off_run], n_list = W[h.off_run + 1];
-    float* ws_o = (float*)ws;
-    float* ws_lse = ws_o ? ws_o + (size_t)n_mparts * Hc * Dv : nullptr;
-    const int32_t* plan = (const int32_t*)dev_plan;
-    const MergedOut mo = {plan + h.off_run + 2, o, bf16, lse};
-    cudaError_t e = launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, nullptr, nullptr, ws_o,
-                                          ws_lse, nullptr, wait_limit_ns(), s, &mo);
-    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-    e = launch_merge_runs(plan, h, n_list, Hc, Dv, ws_o, ws_lse, o, bf16, lse, s);
-    if (e != cudaSuccess) return cuda_fail(e, "merge of the runs' parts");
-    return ok();
-  }
-  // other caches: the per-shard partials in the workspace, then their merge
-  float* o_part = (float*)ws;
-  float* lse_part = o_part + (size_t)h.C * h.R * Hc * Dv;
-  const size_t part_bytes = ((size_t)h.C * h.R * Hc * (Dv + 1) * sizeof(float) + 15) / 16 * 16;
-  st = run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv, sm_scale, o_part,
-                  lse_part, (uint8_t*)ws + part_bytes, ws_bytes - part_bytes, stream);
-  if (st != CP_OK) return st;
-  const cudaError_t e = launch_lse_merge(h.C, h.R, Hc, Dv, o_part, lse_part, o, bf16, lse, s);
-  if (e != cudaSuccess) return cuda_fail(e, "LSE merge kernel");
-  return ok();
+  return run_decode_merged(h, (const int32_t*)host_plan, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, Hq,
+                           Hkv, Dqk, Dv, sm_scale, o, o_dtype, lse, ws, ws_bytes, stream, nullptr);
 }
 
 cp_status cp_decode_attn_paged(const void* host_plan, const void* dev_plan, cp_decode_mode mode,
@@ -1228,6 +1243,52 @@ cp_status cp_sparse_decode_attn(const void* host_plan, const void* dev_plan, con
   memset(&rm, 0, sizeof(rm));
   return run_decode(h, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, rm, Hq, Hkv, Dqk, Dv,
                     sm_scale, o_part, lse_part, ws, ws_bytes, stream, pair_count);
+}
+
+cp_status cp_sparse_decode_attn_merged(const void* host_plan, const void* dev_plan, const int32_t* pair_count,
+                                       cp_decode_mode mode, cp_dtype kv_dtype, const void* q,
+                                       const void* const* sel_k, const void* const* sel_v,
+                                       const float* const* sel_scale, int Hq, int Hkv, int Dqk, int Dv,
+                                       float sm_scale, void* o, cp_dtype o_dtype, float* lse, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  cp_plan_header h;
+  cp_status st = read_header(host_plan, 2, &h);
+  if (st != CP_OK) return st;
+  if (h.layout != CP_DCP_SELECTED) return fail(CP_ERR_INVALID_ARG, "needs a selection plan (cp_sparse_plan)");
+  if (!dev_plan || !q || !sel_k || !o || !lse || !pair_count)
+    return fail(CP_ERR_INVALID_ARG, "a pointer argument is NULL");
+  if (!aligned16(dev_plan) || !aligned16(q) || !aligned16(o) || !aligned16(lse))
+    return fail(CP_ERR_INVALID_ARG, "a device pointer is not 16-byte aligned");
+  if (o_dtype != CP_BF16 && o_dtype != CP_FP32) return fail(CP_ERR_INVALID_ARG, "o_dtype must be bf16 or fp32");
+  if (h.off_run <= 0) return fail(CP_ERR_INVALID_ARG, "the plan has no run table");
+  st = check_decode_shapes(mode, kv_dtype, sel_v != nullptr, sel_scale != nullptr, Hq, Hkv, Dqk, Dv, sm_scale, 1);
+  if (st != CP_OK) return st;
+  size_t need = 0;
+  st = cp_decode_merged_workspace_size(host_plan, mode, kv_dtype, Hq, Dv, &need);
+  if (st != CP_OK) return st;
+  if (ws_bytes < need || (need && !ws)) return fail(CP_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (need && !aligned16(ws)) return fail(CP_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+  ShardPtrs K, V;
+  ScalePtrs S;
+  memset(&K, 0, sizeof(K));
+  memset(&V, 0, sizeof(V));
+  memset(&S, 0, sizeof(S));
+  long long shard_rows[CP_MAX_SHARDS] = {0};
+  for (int r = 0; r < h.C; ++r) {
+    shard_rows[r] = pair_rows_of_shard(h, (const int32_t*)host_plan, r);
+    K.p[r] = sel_k[r];
+    if (!sel_k[r] || !aligned16(sel_k[r])) return fail(CP_ERR_INVALID_ARG, "sel_k[%d] NULL or misaligned", r);
+    if (sel_v) {
+      V.p[r] = sel_v[r];
+      if (!sel_v[r] || !aligned16(sel_v[r])) return fail(CP_ERR_INVALID_ARG, "sel_v[%d] NULL or misaligned", r);
+    }
+    if (sel_scale) {
+      S.p[r] = sel_scale[r];
+      if (!sel_scale[r]) return fail(CP_ERR_INVALID_ARG, "sel_scale[%d] is NULL", r);
+    }
+  }
+  return run_decode_merged(h, (const int32_t*)host_plan, dev_plan, mode, kv_dtype, q, K, V, S, shard_rows, Hq,
+                           Hkv, Dqk, Dv, sm_scale, o, o_dtype, lse, ws, ws_bytes, stream, pair_count);
 }
 
 }  // extern "C"

@@ -448,6 +448,17 @@ cp_status cp_sparse_decode_attn(const void* host_plan, const void* dev_plan, con
                                 const float* const* sel_scale, int Hq, int Hkv, int Dqk, int Dv,
                                 float sm_scale, float* o_part, float* lse_part, void* ws,
                                 size_t ws_bytes, void* stream);
+/* cp_sparse_decode_attn_merged: cp_sparse_decode_attn and cp_lse_merge of
+ * its partials in one call, as cp_decode_attn_merged: o [B, H, Dv] (o_dtype
+ * CP_BF16 or CP_FP32), lse [B, H]; ws: cp_decode_merged_workspace_size(the
+ * sparse plan) bytes.  Over FP8 MLA selections the owners' items of one
+ * request combine in tensor memory. */
+cp_status cp_sparse_decode_attn_merged(const void* host_plan, const void* dev_plan, const int32_t* pair_count,
+                                       cp_decode_mode mode, cp_dtype kv_dtype, const void* q,
+                                       const void* const* sel_k, const void* const* sel_v,
+                                       const float* const* sel_scale, int Hq, int Hkv, int Dqk, int Dv,
+                                       float sm_scale, void* o, cp_dtype o_dtype, float* lse, void* ws,
+                                       size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Paged token-sharded decode cache ("How GPUs Share a Long Context During LLM

@@ -173,6 +173,8 @@ def run_sparse(cp, kind, ctx, C, k, contiguous, seed):
         assert torch.equal(pc, pc2)
         o_part, lse_part = cp.cp_sparse_decode_attn(splan, pc, cp.CP_DECODE_GQA, q, selk, selv,
                                                     sm_scale=1.0 / math.sqrt(128))
+        merged = cp.cp_sparse_decode_attn_merged(splan, pc, cp.CP_DECODE_GQA, q, selk, selv,
+                                                 sm_scale=1.0 / math.sqrt(128), out_dtype=torch.float32)
         data = {"q": q, "k": kc, "v": vc}
         shards, selb = sk, selk
     else:
@@ -183,8 +185,11 @@ def run_sparse(cp, kind, ctx, C, k, contiguous, seed):
         selb, selsc, pc = cp.cp_sparse_gather(plan, k, ws, shards, shsc)
         o_part, lse_part = cp.cp_sparse_decode_attn(splan, pc, cp.CP_DECODE_MLA, data["q"], selb,
                                                     sel_scale=selsc, sm_scale=1.0 / math.sqrt(576))
+        merged = cp.cp_sparse_decode_attn_merged(splan, pc, cp.CP_DECODE_MLA, data["q"], selb, sel_scale=selsc,
+                                                 sm_scale=1.0 / math.sqrt(576), out_dtype=torch.float32)
     o, lse = cp.cp_lse_merge(o_part, lse_part, out_dtype=torch.float32)
     cp.cp_device_error_check()
+    data["merged"] = merged  # cp_sparse_decode_attn_merged's (O, LSE)
     return plan, scores, sel, cnt, pc, shards, selb, data, o_part, lse_part, o, lse
 
 
@@ -241,6 +246,11 @@ def test_sparse_decode(cp, kind, contiguous):
         fo, fl = oracle.decode_attention(qn, K, V, scale, keys=np.asarray(want[b], dtype=np.int64))
         check_o(o[b], fo, what=f"{kind} merged b{b}", **tol)
         check_lse(lse[b], fl)
+        om, lm = data["merged"]  # decode and merge in one call
+        check_o(om[b], fo, what=f"{kind} one-call merged b{b}", **tol)
+        check_lse(lm[b], fl)
+    if kind != "fp8":  # the same kernels as decode + merge: the same bits
+        assert torch.equal(data["merged"][0], o) and torch.equal(data["merged"][1], lse)
 
 
 def test_sparse_decode_full_size_sampled(cp):
