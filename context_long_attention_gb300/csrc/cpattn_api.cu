@@ -627,10 +627,10 @@ cp_status run_decode(const cp_plan_header& h, const void* dev_plan, cp_decode_mo
   return ok();
 }
 
-// The decode and the merge of its partials into o / lse: over an MLA FP8
-// cache a worker's items of one request accumulate as one run (the plan's run
-// table) and only runs cut by a worker boundary leave parts; other caches
-// write the per-shard partials into the workspace and merge them there.
+// The decode and the merge of its partials into o / lse: over an MLA cache
+// (FP8 or bf16) a worker's items of one request accumulate as one run (the
+// plan's run table) and only runs cut by a worker boundary leave parts; GQA
+// caches write the per-shard partials into the workspace and merge them there.
 cp_status run_decode_merged(const cp_plan_header& h, const int32_t* W, const void* dev_plan, cp_decode_mode mode,
                             cp_dtype kv_dtype, const void* q, const ShardPtrs& K, const ShardPtrs& V,
                             const ScalePtrs& S, const long long* shard_rows, int Hq, int Hkv, int Dqk, int Dv,
@@ -641,15 +641,18 @@ cp_status run_decode_merged(const cp_plan_header& h, const int32_t* W, const voi
   cudaStream_t s = (cudaStream_t)stream;
   const int Hc = Hq * plan_s_q(h);
   const bool bf16 = o_dtype == CP_BF16;
-  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3) {
+  if (mode == CP_DECODE_MLA) {
     // runs accumulate in the kernel; only the runs cut by a worker boundary leave parts
     const int n_mparts = W[h.off_run], n_list = W[h.off_run + 1];
     float* ws_o = (float*)ws;
     float* ws_lse = ws_o ? ws_o + (size_t)n_mparts * Hc * Dv : nullptr;
     const int32_t* plan = (const int32_t*)dev_plan;
     const MergedOut mo = {plan + h.off_run + 2, o, bf16, lse};
-    cudaError_t e = launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, nullptr, nullptr, ws_o,
-                                          ws_lse, pair_count, wait_limit_ns(), s, &mo);
+    cudaError_t e = kv_dtype == CP_FP8_E4M3
+                        ? launch_decode_mla_fp8(plan, h, q, K, S, shard_rows, rm, Hq, sm_scale, nullptr, nullptr,
+                                                ws_o, ws_lse, pair_count, wait_limit_ns(), s, &mo)
+                        : launch_decode_mla_tc(plan, h, q, K, shard_rows, rm, Hq, sm_scale, nullptr, nullptr, ws_o,
+                                               ws_lse, pair_count, wait_limit_ns(), s, &mo);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     e = launch_merge_runs(plan, h, n_list, Hc, Dv, ws_o, ws_lse, o, bf16, lse, s);
     if (e != cudaSuccess) return cuda_fail(e, "merge of the runs' parts");
@@ -901,7 +904,7 @@ cp_status cp_decode_merged_workspace_size(const void* host_plan, cp_decode_mode 
   if (h.off_run <= 0) return fail(CP_ERR_INVALID_ARG, "the plan has no run table");
   const size_t Hc = (size_t)H * plan_s_q(h);
   const int32_t* W = (const int32_t*)host_plan;
-  if (mode == CP_DECODE_MLA && kv_dtype == CP_FP8_E4M3)
+  if (mode == CP_DECODE_MLA)  // the runs' parts
     *bytes = (size_t)W[h.off_run] * Hc * (Dv + 1) * sizeof(float);
   else  // the per-shard partials, then the split-KV scratch
     *bytes = ((size_t)h.C * h.R * Hc * (Dv + 1) * sizeof(float) + 15) / 16 * 16 +

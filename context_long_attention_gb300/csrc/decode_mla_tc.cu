@@ -68,6 +68,12 @@ struct Params {
   float* ws_o;
   float* ws_lse;
   const int32_t* pair_count;  // rows in use per pair (a selection buffer), or nullptr
+  // Merged output (as in the FP8 MLA decode): run_out is the plan's run table,
+  // nullptr for one partial per work item.
+  const int32_t* run_out;
+  void* o_fin;     // [B][H][512], bf16 (o_fin_bf16) or fp32
+  int o_fin_bf16;
+  float* lse_fin;  // [B][H]
   unsigned* status;
   unsigned long long wait_ns;
 };
@@ -144,6 +150,35 @@ __device__ __forceinline__ float* out_lse(const Params& p, const Item& it) {
   return it.part < 0 ? p.lse_part + (long long)it.pair * p.H : p.ws_lse + (long long)it.part * p.H;
 }
 
+// Where a run ending at item it writes: the item's partial (no run table),
+// a part slot, or the request's result (bf16 or fp32).
+struct RunOut {
+  float* f;
+  __nv_bfloat16* b;  // non-null: a bf16 result
+  float* l;
+  __device__ __forceinline__ void put(long long i, float v) const {
+    if (b) b[i] = __float2bfloat16_rn(v);
+    else f[i] = v;
+  }
+};
+template <bool kRuns>
+__device__ __forceinline__ RunOut run_out_of(const Params& p, const Item& it, int ro) {
+  RunOut o;
+  o.b = nullptr;
+  if (!kRuns) {
+    o.f = out_rows(p, it);
+    o.l = out_lse(p, it);
+  } else if (ro >= 0) {
+    o.f = p.ws_o + (long long)ro * p.H * kDv;
+    o.l = p.ws_lse + (long long)ro * p.H;
+  } else {
+    o.f = static_cast<float*>(p.o_fin) + (long long)it.b * p.H * kDv;
+    if (p.o_fin_bf16) o.b = static_cast<__nv_bfloat16*>(p.o_fin) + (long long)it.b * p.H * kDv;
+    o.l = p.lse_fin + (long long)it.b * p.H;
+  }
+  return o;
+}
+
 // Warp roles run their loops over all work items of the CTA without meeting
 // at item boundaries: the TMA warp fills the next item's first tile as soon
 // as the previous tile's P.V releases the buffer, and loads a new request's
@@ -151,6 +186,10 @@ __device__ __forceinline__ float* out_lse(const Params& p, const Item& it) {
 // previous QK^T has completed.  Every barrier completes once per tile (bar_q
 // once per query load), so the parity to wait for is that of the tile's index
 // g over all items of this CTA.
+// kRuns: the launch has a run table (a merged decode).  The split decode's
+// instance folds every run branch away, so the per-item path keeps its
+// registers.
+template <bool kRuns>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mla_tc_kernel(const __grid_constant__ ShardMaps maps, const __grid_constant__ CUtensorMap qmap,
                          const Params p) {
@@ -173,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ float sDelta[kHeads];
   __shared__ int sRed[4][kHeads];  // cross-warp column maxima
   __shared__ float sL[4][kHeads];  // cross-warp column sums
+  __shared__ uint32_t sInit[kHeads / 32];  // bit h: head h has had an unmasked row in the current run
+  __shared__ int sMoved;                   // a vote moved some running max
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -280,170 +321,227 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dV = smem_desc(tile, kChunkBytes, 1024), dP = smem_desc(pb, 16, 1024);
     int g0 = 0;
     int q_b = -1, nq = 0;  // request whose query sQ holds, query loads so far
+    // the run (a worker's consecutive items of one request, or one item
+    // without the run table): its tiles so far; this row's sums per head live
+    // in registers within an item and in TMEM columns [320, 384) between the
+    // items of a run (kept in registers across items they spilled)
+    int run_tiles = 0;
+    const uint32_t l_addr = lane_addr + 320;
+    auto l_save = [&](const float (&l)[kHeads]) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t a[32];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) a[h] = __float_as_uint(l[32 * h2 + h]);
+        tmem_st32(l_addr + 32 * h2, a);
+      }
+      tmem_st_wait();
+    };
+    auto l_load = [&](float (&l)[kHeads]) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t a[32];
+        tmem_ld32(l_addr + 32 * h2, a);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) l[32 * h2 + h] = __uint_as_float(a[h]);
+      }
+    };
     for (int wi = w0; wi < w1 && ok; ++wi) {
       const Item it = read_item(p, pairs, work, wi);
-      if (it.ntiles == 0) {  // empty shard: O = 0, LSE = -inf
-        float* out_o = out_rows(p, it);
-        float* out_l = out_lse(p, it);
-        for (int i = t; i < p.H * kDv; i += 128) out_o[i] = 0.f;
-        for (int i = t; i < p.H; i += 128) out_l[i] = -INFINITY;
-        continue;
-      }
-      // a new request: warp 0 waits for its query before the first QK^T
-      bool q_ok = true;
-      if (it.b != q_b) {
-        if (warp == 0)
-          q_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag));
-        ++nq;
-      }
-      q_b = it.b;
-      // the running max restarts from the first tile's maxima; every read of
-      // the previous item's maxima came before its epilogue's barrier
-      if (t < kHeads) sM[t] = 0.f;
-      named_bar_sync(1, 128);
-      // token of tile row t of tile j: tok_t + j * tok_j; a cache row is masked
-      // for the columns of query rows below tok - lim
-      const int tok_j = kRows * it.pd.tok_step;
-      const int tok_t = it.pd.tok0 + (it.row_begin + t) * it.pd.tok_step;
-      const int lim = it.pd.ctx_len - p.s_q;
-      const int nrows = it.nrows, ntiles = it.ntiles;
       float l[kHeads];
+      // where the item's run writes: the per-item partial, a part slot, or the result
+      const int ro = kRuns ? p.run_out[wi] : -2;
+      if (!kRuns) run_tiles = 0;
+      if (ro == -3) continue;  // an empty pair's item of a merged decode
+      const bool run_end = !kRuns || ro != -1;
+      if (it.ntiles == 0) {
+        if (!run_end) continue;
+        if (run_tiles == 0) {  // no rows in the run (an empty shard): O = 0, LSE = -inf
+          const RunOut out = run_out_of<kRuns>(p, it, ro);
+          for (int i = t; i < p.H * kDv; i += 128) out.put(i, 0.f);
+          for (int i = t; i < p.H; i += 128) out.l[i] = -INFINITY;
+          continue;
+        }
+      }
+      if (it.ntiles > 0) {
+        // a new request: warp 0 waits for its query before the first QK^T
+        bool q_ok = true;
+        if (it.b != q_b) {
+          if (warp == 0)
+            q_ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_q), nq & 1, p.wait_ns, &abort_flag));
+          ++nq;
+        }
+        q_b = it.b;
+        // a run's running max starts from its first tile's maxima; every read of
+        // the previous run's maxima came before its epilogue's barrier
+        if (run_tiles == 0) {
+          if (t < kHeads) sM[t] = 0.f;
+          if (t < kHeads / 32) sInit[t] = 0u;
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
-      for (int j = 0; j < ntiles; ++j) {
-        const int g = g0 + j;
-        bool issued = q_ok;
-        q_ok = true;
-        if (warp == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
-          for (int q = 0; q < 5 && issued; ++q) {
-            issued = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns,
-                                                       &abort_flag));
-            if (!issued) break;
+          for (int h = 0; h < kHeads; ++h) l[h] = 0.f;
+        } else {
+          l_load(l);  // the run's sums so far
+        }
+        named_bar_sync(1, 128);
+        // token of tile row t of tile j: tok_t + j * tok_j; a cache row is masked
+        // for the columns of query rows below tok - lim
+        const int tok_j = kRows * it.pd.tok_step;
+        const int tok_t = it.pd.tok0 + (it.row_begin + t) * it.pd.tok_step;
+        const int lim = it.pd.ctx_len - p.s_q;
+        const int nrows = it.nrows, ntiles = it.ntiles;
+        for (int j = 0; j < ntiles; ++j) {
+          const int g = g0 + j;
+          bool issued = q_ok;
+          q_ok = true;
+          if (warp == 0) {  // S^T = K_tile Q^T, chunk group by chunk group as they fill
+            for (int q = 0; q < 5 && issued; ++q) {
+              issued = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_fill[q]), g & 1, p.wait_ns,
+                                                         &abort_flag));
+              if (!issued) break;
+              tc_fence_after();
+              if (elect_one()) {
+                for (int ks = 0; ks < 4 * group_chunks(q); ++ks) {
+                  const int kk = 8 * q + ks;
+                  const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
+                  const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
+                  mma_ss(tmem, dK + (off >> 4), dQ + (qoff >> 4), idS, kk > 0);
+                }
+              }
+              __syncwarp();
+            }
+            if (issued && elect_one()) mma_commit(smem_u32(&bar_s));
+            __syncwarp();
+          }
+          const bool valid = j * kRows + t < nrows;
+          // Several query rows (s_q > 1): row qi of the request reads tokens up
+          // to L - s_q + qi, so this cache row is masked for the columns of the
+          // query rows qi < tok - (L - s_q), columns [0, mcols).
+          const int tok = tok_t + j * tok_j;
+          const int mcols = min(kHeads, max(0, tok - lim) * p.Hrow);
+          const float cj = p.scale_log2;  // scores in log2 units
+          // The four softmax warps leave together: a warp that gave up still
+          // meets the others at the named barrier of this vote.
+          const bool got = __all_sync(
+              0xffffffffu, issued && mbar_wait(smem_u32(&bar_s), g & 1, p.wait_ns, &abort_flag));
+          if (bar_red_or(1, 128, !got)) {
+            if (!got) report_timeout(p.status, 6, &abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // u = score - running max (log2 units); invalid rows read nothing
+          float u[kHeads];
+          float over = -INFINITY;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t a[32];
+            tmem_ld32(lane_addr + 32 * half, a);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              const int hh = 32 * half + h;
+              u[hh] = valid && hh >= mcols ? fmaf(__uint_as_float(a[h]), cj, -sM[hh]) : -INFINITY;
+              over = fmaxf(over, u[hh]);
+            }
+          }
+          // Block-wide vote: does any score pass its running max by more than 2^8?
+          // A run's first tile sets the maxima; a later item's first tile votes
+          // only with several query rows (heads masked so far may meet their first rows).
+          const bool first = j == 0 && (run_tiles == 0 || p.s_q > 1);
+          if (bar_red_or(1, 128, first || over > kRescaleLog2)) {
+            if (t == 0) sMoved = 0;
+            // column maxima of this tile (relative to the old running max)
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) {
+              const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
+              if (lane == 0) sRed[warp][h] = m;
+            }
+            named_bar_sync(1, 128);
+            if (t < kHeads) {
+              const float cm = fmaxf(fmaxf(unordered(sRed[0][t]), unordered(sRed[1][t])),
+                                     fmaxf(unordered(sRed[2][t]), unordered(sRed[3][t])));
+              // move the running max to a column's first unmasked maxima, or when it
+              // grew by more than 2^8; earlier sums and O^T shrink by 2^-delta.  A
+              // column masked so far keeps max 0 and weight 0: within an item rows
+              // go up in token order, and a later item of the run (another shard)
+              // that unmasks it votes on its first tile.
+              float delta;
+              if (!((sInit[t >> 5] >> (t & 31)) & 1u)) {
+                delta = cm == -INFINITY ? 0.f : cm;
+                if (cm != -INFINITY) atomicOr(&sInit[t >> 5], 1u << (t & 31));
+              } else {
+                delta = cm > kRescaleLog2 ? cm : 0.f;
+              }
+              if (delta != 0.f) sMoved = 1;
+              sAlpha[t] = run_tiles == 0 ? 0.f : ex2(-delta);
+              sDelta[t] = delta;
+              sM[t] += delta;
+            }
+            named_bar_sync(1, 128);
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) {
+              l[h] *= sAlpha[h];
+              u[h] -= sDelta[h];
+            }
+            if (run_tiles > 0 && sMoved) {  // O^T holds the run's earlier tiles (their P.V completed before this S)
+              // 16 columns at a time: u and l stay in registers meanwhile
+#pragma unroll 1
+              for (int c = 0; c < 4 * kHeads / 16; ++c) {
+                uint32_t a[16];
+                tmem_ld16(lane_addr + 64 + 16 * c, a);
+                tmem_ld_wait();
+                const float* al = sAlpha + ((16 * c) & (kHeads - 1));
+#pragma unroll
+                for (int h = 0; h < 16; ++h) a[h] = __float_as_uint(__uint_as_float(a[h]) * al[h]);
+                tmem_st16(lane_addr + 64 + 16 * c, a);
+              }
+              tmem_st_wait();
+            }
+          }
+          // P^T row t: p = 2^u.
+          // MN-major B operand: row t = 64 heads x 2 B = one 128-byte swizzled row.
+          uint8_t* prow = sP + t * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int h = 8 * c + 2 * e;
+              const float p0 = ex2(u[h]), p1 = ex2(u[h + 1]);
+              l[h] += p0;
+              l[h + 1] += p1;
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          named_bar_sync(1, 128);  // every row of P^T is written
+          if (warp == 0) {         // O^T += V_tile^T P^T, one M-block (128 dims) at a time
             tc_fence_after();
             if (elect_one()) {
-              for (int ks = 0; ks < 4 * group_chunks(q); ++ks) {
-                const int kk = 8 * q + ks;
-                const uint32_t off = (kk >> 2) * kChunkBytes + (kk & 3) * 32;
-                const uint32_t qoff = (kk >> 2) * kQChunkBytes + (kk & 3) * 32;
-                mma_ss(tmem, dK + (off >> 4), dQ + (qoff >> 4), idS, kk > 0);
+#pragma unroll
+              for (int mb = 0; mb < kDv / 128; ++mb) {
+#pragma unroll
+                for (int kk = 0; kk < kRows / 16; ++kk)
+                  mma_ss(tmem + 64 + 64 * mb, dV + ((2 * mb * kChunkBytes + kk * 2048) >> 4),
+                         dP + ((kk * 2048) >> 4), idPV, (run_tiles > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_u32(&bar_mb[mb]));
               }
             }
             __syncwarp();
           }
-          if (issued && elect_one()) mma_commit(smem_u32(&bar_s));
-          __syncwarp();
-        }
-        const bool valid = j * kRows + t < nrows;
-        // Several query rows (s_q > 1): row qi of the request reads tokens up
-        // to L - s_q + qi, so this cache row is masked for the columns of the
-        // query rows qi < tok - (L - s_q), columns [0, mcols).
-        const int tok = tok_t + j * tok_j;
-        const int mcols = min(kHeads, max(0, tok - lim) * p.Hrow);
-        const float cj = p.scale_log2;  // scores in log2 units
-        // The four softmax warps leave together: a warp that gave up still
-        // meets the others at the named barrier of this vote.
-        const bool got = __all_sync(
-            0xffffffffu, issued && mbar_wait(smem_u32(&bar_s), g & 1, p.wait_ns, &abort_flag));
-        if (bar_red_or(1, 128, !got)) {
-          if (!got) report_timeout(p.status, 6, &abort_flag);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // u = score - running max (log2 units); invalid rows read nothing
-        float u[kHeads];
-        float over = -INFINITY;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t a[32];
-          tmem_ld32(lane_addr + 32 * half, a);
-          tmem_ld_wait();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const int hh = 32 * half + h;
-            u[hh] = valid && hh >= mcols ? fmaf(__uint_as_float(a[h]), cj, -sM[hh]) : -INFINITY;
-            over = fmaxf(over, u[hh]);
-          }
-        }
-        // Block-wide vote: does any score pass its running max by more than 2^8?
-        if (bar_red_or(1, 128, j == 0 || over > kRescaleLog2)) {
-          // column maxima of this tile (relative to the old running max)
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h) {
-            const int m = __reduce_max_sync(0xffffffffu, ordered(u[h]));
-            if (lane == 0) sRed[warp][h] = m;
-          }
-          named_bar_sync(1, 128);
-          if (t < kHeads) {
-            const float cm = fmaxf(fmaxf(unordered(sRed[0][t]), unordered(sRed[1][t])),
-                                   fmaxf(unordered(sRed[2][t]), unordered(sRed[3][t])));
-            // move the running max to this tile's max on the first tile, or when it
-            // grew by more than 2^8; earlier sums and O^T shrink by 2^-delta
-            // (a column with no unmasked row in the item's first tile has none in
-            // the item: rows go up in token order; it keeps max 0 and weight 0)
-            const float delta = j == 0 ? (cm == -INFINITY ? 0.f : cm) : (cm > kRescaleLog2 ? cm : 0.f);
-            sAlpha[t] = j == 0 ? 0.f : ex2(-delta);
-            sDelta[t] = delta;
-            sM[t] += delta;
-          }
-          named_bar_sync(1, 128);
-#pragma unroll
-          for (int h = 0; h < kHeads; ++h) {
-            l[h] *= sAlpha[h];
-            u[h] -= sDelta[h];
-          }
-          if (j > 0) {  // O^T holds earlier tiles (their P.V completed before this S)
-            // 16 columns at a time: u and l stay in registers meanwhile
-#pragma unroll 1
-            for (int c = 0; c < 4 * kHeads / 16; ++c) {
-              uint32_t a[16];
-              tmem_ld16(lane_addr + 64 + 16 * c, a);
-              tmem_ld_wait();
-              const float* al = sAlpha + ((16 * c) & (kHeads - 1));
-#pragma unroll
-              for (int h = 0; h < 16; ++h) a[h] = __float_as_uint(__uint_as_float(a[h]) * al[h]);
-              tmem_st16(lane_addr + 64 + 16 * c, a);
-            }
-            tmem_st_wait();
-          }
-        }
-        // P^T row t: p = 2^u.
-        // MN-major B operand: row t = 64 heads x 2 B = one 128-byte swizzled row.
-        uint8_t* prow = sP + t * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int h = 8 * c + 2 * e;
-            const float p0 = ex2(u[h]), p1 = ex2(u[h + 1]);
-            l[h] += p0;
-            l[h + 1] += p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(prow + ((c ^ (t & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(1, 128);  // every row of P^T is written
-        if (warp == 0) {         // O^T += V_tile^T P^T, one M-block (128 dims) at a time
-          tc_fence_after();
-          if (elect_one()) {
-#pragma unroll
-            for (int mb = 0; mb < kDv / 128; ++mb) {
-#pragma unroll
-              for (int kk = 0; kk < kRows / 16; ++kk)
-                mma_ss(tmem + 64 + 64 * mb, dV + ((2 * mb * kChunkBytes + kk * 2048) >> 4),
-                       dP + ((kk * 2048) >> 4), idPV, (j > 0 || kk > 0) ? 1u : 0u);
-              mma_commit(smem_u32(&bar_mb[mb]));
-            }
-          }
-          __syncwarp();
+          ++run_tiles;
         }
       }
-      // ---- epilogue: column sums of l, O^T / l, LSE
+      if (!run_end && run_tiles > 0) l_save(l);  // the run goes on to the next item
+      // ---- epilogue at a run's end: column sums of l, O^T / l, LSE
+      if (run_end && run_tiles > 0) {
+      if (it.ntiles == 0) l_load(l);  // an item with no rows ends the run
+      run_tiles = 0;
       const bool landed =
-          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[3]), (g0 + ntiles - 1) & 1,
+          ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_mb[3]), (g0 + it.ntiles - 1) & 1,
                                                   p.wait_ns, &abort_flag));
       if (bar_red_or(1, 128, !landed)) {
         if (ok && !landed) report_timeout(p.status, 7, &abort_flag);
@@ -451,11 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         tc_fence_after();
-        const cp_work_desc wd = work[wi];
-        float* out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
-                                   : p.ws_o + (long long)wd.part * p.H * kDv;
-        float* out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
-                                   : p.ws_lse + (long long)wd.part * p.H;
+        const RunOut out = run_out_of<kRuns>(p, it, ro);
+        float* const out_l = out.l;
 #pragma unroll
         for (int h = 0; h < kHeads; ++h) {
           float v = l[h];
@@ -482,13 +577,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
               const int hh = 32 * half + h;
-              if (hh < p.H) out_o[(long long)hh * kDv + 128 * mb + t] = __uint_as_float(a[h]) * sAlpha[hh];
+              if (hh < p.H) out.put((long long)hh * kDv + 128 * mb + t, __uint_as_float(a[h]) * sAlpha[hh]);
             }
           }
         }
       }
+      }
 
-      g0 += ntiles;
+      g0 += it.ntiles;
       // the four softmax warps decide together whether to go on
       if (bar_red_or(1, 128, !ok || abort_flag != 0)) ok = false;
     }
@@ -512,9 +608,13 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  const int32_t* pair_count, unsigned long long wait_ns,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, const MergedOut* mo) {
   Params p;
   p.pair_count = pair_count;
+  p.run_out = mo ? mo->run_out : nullptr;
+  p.o_fin = mo ? mo->o : nullptr;
+  p.o_fin_bf16 = mo && mo->o_bf16 ? 1 : 0;
+  p.lse_fin = mo ? mo->lse : nullptr;
   p.plan = dev_plan;
   p.B = h.R;
   p.off_pair = h.off_rank;
@@ -560,7 +660,7 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
     const uint32_t box[3] = {64, (uint32_t)kHeads, 1};
     if (!encode_tensor_map_bf16(&qmap, q, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  auto kern = decode_mla_tc_kernel;
+  auto kern = p.run_out ? decode_mla_tc_kernel<true> : decode_mla_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   kern<<<h.n_tiles, kThreads, kSmem, s>>>(local, qmap, p);

@@ -147,7 +147,7 @@ cudaError_t launch_decode_mla_tc(const int32_t* dev_plan, const cp_plan_header& 
                                  const long long* shard_rows, const RowMap& rm, int H, float sm_scale,
                                  float* o_part, float* lse_part, float* ws_o, float* ws_lse,
                                  const int32_t* pair_count, unsigned long long wait_ns,
-                                 cudaStream_t s);
+                                 cudaStream_t s, const MergedOut* mo = nullptr);
 unsigned long long wait_limit_ns();
 
 // ---- CUDA-core attention (simt_attn.cu)

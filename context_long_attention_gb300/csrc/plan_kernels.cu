@@ -7,7 +7,7 @@
 //   into the shard's buffer or, paged, into the pool row its page table gives.
 // * lse_merge_kernel / decode_fixup_kernel / lse_fold_kernel: O = sum_p w_p O_p / sum_p w_p
 //   with w_p = exp(LSE_p - max LSE) (§3.3; "DeepSeek-V4 Attention Inference
-//   Systems" §5), one warp per (row, head), 128-bit loads.
+//   Systems" §5), one warp per (row, head, 128 output dims), 128-bit loads.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -80,11 +80,14 @@ __global__ void page_tail_zero_kernel(const int32_t* __restrict__ plan, int off_
   }
 }
 
-// Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride
-// (any P: a warp takes the parts 32 at a time, lane u holding part p0 + u's
-// weight; the sums take the parts in order).
+// Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride:
+// the slice of 128 output dims that starts at dim 4 * c0 (a warp per slice, so
+// that a launch over few rows still fills the SMs), and the LSE with the first
+// slice.  Any P: a warp takes the parts 32 at a time, lane u holding part
+// p0 + u's weight; the sums take the parts in order.
+constexpr int kMergeSlice = 32;  // float4 columns of a slice
 __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, long long ostride,
-                                          const float* __restrict__ l, long long lstride, int Dv,
+                                          const float* __restrict__ l, long long lstride, int Dv, int c0,
                                           float* out_f32, __nv_bfloat16* out_bf16, float* out_lse) {
   const int lane = threadIdx.x & 31;
   float g = -INFINITY;
@@ -96,19 +99,23 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
     const float lp = p < P ? l[p * lstride] : -INFINITY;
     return (any && lp != -INFINITY) ? expf(lp - g) : 0.f;
   };
-  float z = 0.f;
-  for (int p0 = 0; p0 < P; p0 += 32) z += weight(p0 + lane);
+  // the weights of parts lane and lane + 32, once; parts past 64 (a pair cut
+  // over more than 64 workers, a request over more than 64 runs) are weighed
+  // again where they are summed
+  const float w0 = weight(lane), w1 = weight(lane + 32);
+  float z = w0 + w1;
+  for (int p0 = 64; p0 < P; p0 += 32) z += weight(p0 + lane);
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
   const float inv = any ? 1.f / z : 0.f;
   // Every lane runs every iteration (the weights travel by warp shuffles);
   // lanes past the row's end only skip their loads and stores.
-  for (int c0 = 0; c0 < Dv / 4; c0 += 32) {
+  {
     const int c = c0 + lane;
     const bool active = c < Dv / 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int p0 = 0; p0 < P; p0 += 32) {
-      const float wl = weight(p0 + lane);
+      const float wl = p0 == 0 ? w0 : p0 == 32 ? w1 : weight(p0 + lane);
       const int np = min(32, P - p0);
       // kBatch parts' loads in flight before they are summed (in order)
       constexpr int kBatch = 8;
@@ -138,10 +145,9 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
     acc.y *= inv;
     acc.z *= inv;
     acc.w *= inv;
-    if (!active) continue;
-    if (out_f32) {
+    if (active && out_f32) {
       reinterpret_cast<float4*>(out_f32)[c] = acc;
-    } else {
+    } else if (active) {
       __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
       __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
       uint2 u;
@@ -150,7 +156,7 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
       reinterpret_cast<uint2*>(out_bf16)[c] = u;
     }
   }
-  if (out_lse && lane == 0) *out_lse = any ? g + logf(z) : -INFINITY;
+  if (out_lse && c0 == 0 && lane == 0) *out_lse = any ? g + logf(z) : -INFINITY;
 }
 
 __global__ void lse_merge_kernel(int P, long long NH, int Dv, const float* __restrict__ o_part,
@@ -160,7 +166,8 @@ __global__ void lse_merge_kernel(int P, long long NH, int Dv, const float* __res
   if (i >= NH) return;
   float* of = o_bf16 ? nullptr : static_cast<float*>(o) + i * Dv;
   __nv_bfloat16* ob = o_bf16 ? static_cast<__nv_bfloat16*>(o) + i * Dv : nullptr;
-  merge_row(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, of, ob, lse ? lse + i : nullptr);
+  merge_row(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, blockIdx.y * kMergeSlice, of, ob,
+            lse ? lse + i : nullptr);
 }
 
 // (O, LSE) <- the exact combine of (O, LSE) and (O', LSE'), in place; one warp
@@ -189,7 +196,7 @@ __global__ void lse_fold_kernel(long long NH, int Dv, float* __restrict__ o, flo
 }
 
 // Requests of a merged decode whose result comes from parts: one warp per
-// (listed request, head) combines the request's parts [first, first + n)
+// (listed request, head, 128 dims) combines the request's parts [first, first + n)
 // (n = 0, a request with no rows: O = 0, LSE = -inf).
 __global__ void merge_runs_kernel(const int32_t* __restrict__ list, int n_list, int H, int Dv,
                                   const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
@@ -202,7 +209,7 @@ __global__ void merge_runs_kernel(const int32_t* __restrict__ list, int n_list, 
   float* of = o_bf16 ? nullptr : static_cast<float*>(o) + ob * Dv;
   __nv_bfloat16* obf = o_bf16 ? static_cast<__nv_bfloat16*>(o) + ob * Dv : nullptr;
   merge_row(n, ws_o + ((long long)first * H + h) * Dv, (long long)H * Dv, ws_lse + (long long)first * H + h, H,
-            Dv, of, obf, lse + ob);
+            Dv, blockIdx.y * kMergeSlice, of, obf, lse + ob);
 }
 
 __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
@@ -216,9 +223,12 @@ __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int
   const cp_pair_desc d = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[pair];
   const long long ob = (long long)pair * H + h;
   merge_row(d.n_parts, ws_o + ((long long)d.first_part * H + h) * Dv, (long long)H * Dv,
-            ws_lse + (long long)d.first_part * H + h, H, Dv, o_part + ob * Dv, nullptr,
-            lse_part + ob);
+            ws_lse + (long long)d.first_part * H + h, H, Dv, blockIdx.y * kMergeSlice, o_part + ob * Dv,
+            nullptr, lse_part + ob);
 }
+
+// the 128-dim slices of a row of Dv dims
+unsigned merge_slices(int Dv) { return (unsigned)((Dv / 4 + kMergeSlice - 1) / kMergeSlice); }
 
 }  // namespace
 
@@ -260,8 +270,8 @@ cudaError_t launch_lse_merge(int P, int N, int H, int Dv, const float* o_part,
   const long long NH = (long long)N * H;
   const int warps = 8;
   const long long blocks = (NH + warps - 1) / warps;
-  lse_merge_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(P, NH, Dv, o_part, lse_part, o,
-                                                           o_bf16 ? 1 : 0, lse);
+  const dim3 grid((unsigned)blocks, merge_slices(Dv));
+  lse_merge_kernel<<<grid, warps * 32, 0, s>>>(P, NH, Dv, o_part, lse_part, o, o_bf16 ? 1 : 0, lse);
   return cudaGetLastError();
 }
 
@@ -273,8 +283,8 @@ cudaError_t launch_merge_runs(const int32_t* dev_plan, const cp_plan_header& h, 
   const int warps = 8;
   const long long blocks = (warps_needed + warps - 1) / warps;
   const int32_t* list = dev_plan + h.off_run + 2 + h.n_seg;
-  merge_runs_kernel<<<(unsigned)blocks, warps * 32, 0, s>>>(list, n_list, H, Dv, ws_o, ws_lse, o, o_bf16 ? 1 : 0,
-                                                           lse);
+  const dim3 grid((unsigned)blocks, merge_slices(Dv));
+  merge_runs_kernel<<<grid, warps * 32, 0, s>>>(list, n_list, H, Dv, ws_o, ws_lse, o, o_bf16 ? 1 : 0, lse);
   return cudaGetLastError();
 }
 
@@ -293,7 +303,8 @@ cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h
   const long long n = (long long)h.n_split * H;
   if (n == 0) return cudaSuccess;
   const int warps = 8;
-  decode_fixup_kernel<<<(unsigned)((n + warps - 1) / warps), warps * 32, 0, s>>>(
+  const dim3 grid((unsigned)((n + warps - 1) / warps), merge_slices(Dv));
+  decode_fixup_kernel<<<grid, warps * 32, 0, s>>>(
       dev_plan, h.R, h.off_rank, h.off_rtile, h.n_split, H, Dv, ws_o, ws_lse, o_part, lse_part);
   return cudaGetLastError();
 }

@@ -358,15 +358,15 @@ cp_status cp_decode_attn(const void* host_plan, const void* dev_plan, cp_decode_
  * lse [B, H] fp32 (natural log), the attention over each request's whole
  * cache ([CTX] §3.3; [V4] §5).  Arguments as for cp_decode_attn.
  *
- * With an MLA FP8 cache (per-shard buffers) the partials never leave the
- * GPU's tensor memory where they need not: the plan's run table (the header's
+ * With an MLA cache (FP8 or bf16, per-shard buffers) the partials never
+ * leave the GPU's tensor memory where they need not: the plan's run table (the header's
  * off_run, built with every decode plan) groups each worker's consecutive
  * work items of one request into a run, and the run accumulates all of them
  * (the shards' partial softmax combines exactly across them, as in the
  * merge).  A run holding all of its request's rows writes the result; the
  * runs of a request cut by a worker boundary write fp32 parts, which a merge
  * combines.  Short requests, whose C shards fit in one worker, then cost no
- * partial at all.  Other caches run cp_decode_attn into the workspace and
+ * partial at all.  GQA caches run cp_decode_attn into the workspace and
  * merge there.
  *
  * Run table at off_run (int32): n_parts, n_list, then run_out[n_work] (per
@@ -451,8 +451,8 @@ cp_status cp_sparse_decode_attn(const void* host_plan, const void* dev_plan, con
 /* cp_sparse_decode_attn_merged: cp_sparse_decode_attn and cp_lse_merge of
  * its partials in one call, as cp_decode_attn_merged: o [B, H, Dv] (o_dtype
  * CP_BF16 or CP_FP32), lse [B, H]; ws: cp_decode_merged_workspace_size(the
- * sparse plan) bytes.  Over FP8 MLA selections the owners' items of one
- * request combine in tensor memory. */
+ * sparse plan) bytes.  Over MLA selections the owners' items of one request
+ * combine in tensor memory. */
 cp_status cp_sparse_decode_attn_merged(const void* host_plan, const void* dev_plan, const int32_t* pair_count,
                                        cp_decode_mode mode, cp_dtype kv_dtype, const void* q,
                                        const void* const* sel_k, const void* const* sel_v,

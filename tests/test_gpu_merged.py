@@ -2,11 +2,11 @@
 shard partials in one call; "How GPUs Share a Long Context During LLM
 Inference" §3.3, "DeepSeek-V4 Attention Inference Systems" §5): the merged
 (O, LSE) of every request (every query row) against the oracle's attention
-over the whole cache.  For the MLA FP8 cache a worker's consecutive items of
-one request accumulate as one run, so the cases mix short requests (whole
-runs), long ones (cut by worker boundaries into parts), empty ones and tiny
-worker counts; the other caches go through the per-shard partials and must
-match cp_decode_attn + cp_lse_merge bit for bit."""
+over the whole cache.  For the MLA caches (FP8 and bf16) a worker's
+consecutive items of one request accumulate as one run, so the cases mix
+short requests (whole runs), long ones (cut by worker boundaries into parts),
+empty ones and tiny worker counts; GQA caches go through the per-shard
+partials and must match cp_decode_attn + cp_lse_merge bit for bit."""
 
 import math
 
@@ -122,19 +122,22 @@ def test_merged_mla_fp8_full_size_sampled(cp):
     torch.cuda.empty_cache()
 
 
-def test_merged_other_caches_match_decode_then_merge(cp):
-    """bf16 MLA and bf16 GQA take the per-shard partials in the workspace:
-    the same kernels as cp_decode_attn + cp_lse_merge, the same bits."""
+@pytest.mark.parametrize("C,nw,s_q,H", [(8, 3, 1, 64), (8, 152, 1, 64), (1, 5, 1, 64), (8, 9, 3, 20),
+                                        (4, 64, 2, 32)])
+def test_merged_mla_bf16(cp, C, nw, s_q, H):
+    """The bf16 MLA kernel's runs, as the FP8 one's."""
+    ctx = [0, 1, 3, 129, 1000, 4097, 20000, 5] if s_q == 1 else [s_q, 130, 1031, 4100, 2 * 128 * 8 + 1, 6]
+    data = W.mla_decode_inputs(ctx, H=s_q * H, seed=570 + C + nw + s_q, device=DEV, fp8=False, bf16=True)
+    data["ctx"] = ctx
+    _, o, lse = merged_mla(cp, data, C, s_q, H, False, False, nw, torch.float32)
+    check_merged(data, s_q, H, False, o, lse)
+
+
+def test_merged_gqa_matches_decode_then_merge(cp):
+    """A GQA cache takes the per-shard partials in the workspace: the same
+    kernels as cp_decode_attn + cp_lse_merge, the same bits."""
     ctx = [0, 9, 300, 4100]
-    data = W.mla_decode_inputs(ctx, H=64, seed=560, device=DEV, fp8=False, bf16=True)
     plan = cp.cp_decode_plan(8, ctx, n_workers=7, device=DEV)
-    shards, _ = cp.cp_kv_shard_pack(plan, data["kv_bf16"])
-    o, lse = cp.cp_decode_attn_merged(plan, cp.CP_DECODE_MLA, data["q"], shards, sm_scale=0.04,
-                                      out_dtype=torch.float32)
-    op, lp = cp.cp_decode_attn(plan, cp.CP_DECODE_MLA, data["q"], shards, sm_scale=0.04)
-    o2, lse2 = cp.cp_lse_merge(op, lp, out_dtype=torch.float32)
-    cp.cp_device_error_check()
-    assert torch.equal(o, o2) and torch.equal(lse, lse2)
     Hq, Hkv, D = 16, 4, 128
     q, k, v = W.gqa_decode_inputs(len(ctx), ctx, Hq, Hkv, D, "bf16", seed=561, device=DEV, std=0.3)
     sk, _ = cp.cp_kv_shard_pack(plan, k)
