@@ -205,6 +205,7 @@ struct Item {
   bool run_end;    // the item ends its run (always, without the run table)
   bool skip;       // an empty pair's item in a merged decode: nothing to do
 };
+template <bool kRuns>
 __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   const cp_work_desc wd = reinterpret_cast<const cp_work_desc*>(p.plan + p.off_work)[wi];
   const cp_pair_desc pd = reinterpret_cast<const cp_pair_desc*>(p.plan + p.off_pair)[wd.pair];
@@ -225,7 +226,7 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   it.out_bf16 = false;
   it.run_end = true;
   it.skip = false;
-  if (!p.run_out) {
+  if (!kRuns) {
     it.out_o = wd.part < 0 ? p.o_part + (long long)wd.pair * p.H * kDv
                            : p.ws_o + (long long)wd.part * p.H * kDv;
     it.out_l = wd.part < 0 ? p.lse_part + (long long)wd.pair * p.H
@@ -246,6 +247,9 @@ __device__ __forceinline__ Item read_item(const Params& p, int wi) {
   return it;
 }
 
+// kRuns: the launch has a run table (a merged decode); the split decode's
+// instance folds the run branches away.
+template <bool kRuns>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_mla_fp8_kernel(const __grid_constant__ CodeMaps maps, const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -304,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0;
       for (int wi = w0; wi < w1 && ok; ++wi) {
-        const Item it = read_item(p, wi);
+        const Item it = read_item<kRuns>(p, wi);
         const uint8_t* codes = static_cast<const uint8_t*>(p.k.p[it.r]);
         // Cache row of the item's row i; past the pair's rows, a row past the
         // pool, where the copy reads zeros.
@@ -392,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, nq = 0;  // tiles and query loads so far
       int q_b = -1;       // request whose query the operand holds
       for (int wi = w0; wi < w1 && ok; ++wi) {
-        const Item it = read_item(p, wi);
+        const Item it = read_item<kRuns>(p, wi);
         if (it.ntiles == 0) continue;
         // a new request's query is in place (written after every earlier product completed)
         if (it.b != q_b) {
@@ -464,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0;
       int run_tiles = 0;  // tiles of the current run issued so far (O^T accumulates after the first)
       for (int wi = w0; wi < w1 && ok; ++wi) {
-        const Item it = read_item(p, wi);
+        const Item it = read_item<kRuns>(p, wi);
         for (int j = 0; j < it.ntiles && ok; ++j, ++g) {
           const int s = g & 1;
           const bool acc = run_tiles > 0;
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run_tiles = 0, gs = 0;
     float l[kHpw];
     for (int wi = w0; wi < w1 && ok; ++wi) {
-      const Item it = read_item(p, wi);
+      const Item it = read_item<kRuns>(p, wi);
       if (it.skip) continue;
       // the run's result or part: O in fp32, or bf16 for a bf16 result
       void* const out_o = it.out_o;
@@ -885,10 +889,10 @@ cudaError_t launch_decode_mla_fp8(const int32_t* dev_plan, const cp_plan_header&
         return cudaErrorInvalidValue;
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(decode_mla_fp8_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  auto kern = p.run_out ? decode_mla_fp8_kernel<true> : decode_mla_fp8_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  decode_mla_fp8_kernel<<<h.n_tiles, kThreads, kSmem, s>>>(maps, p);
+  kern<<<h.n_tiles, kThreads, kSmem, s>>>(maps, p);
   return cudaGetLastError();
 }
 

@@ -81,15 +81,31 @@ __global__ void page_tail_zero_kernel(const int32_t* __restrict__ plan, int off_
 }
 
 // Merge of P parts for one (row, head), parts at o + p*ostride, l + p*lstride:
-// the slice of 128 output dims that starts at dim 4 * c0 (a warp per slice, so
-// that a launch over few rows still fills the SMs), and the LSE with the first
-// slice.  Any P: a warp takes the parts 32 at a time, lane u holding part
-// p0 + u's weight; the sums take the parts in order.
+// kSlices slices of 128 output dims from dim 4 * c0 (a launch over few rows
+// gives each warp one slice, so that the warps fill the SMs), and the LSE with
+// the slice at dim 0.  Any P: a warp takes the parts 32 at a time, lane u
+// holding part p0 + u's weight; the sums take the parts in order.
+//
+// A merge is a short chain of dependent loads (LSEs, then weights, then the
+// sums) and its time is their latency, so the loads in flight per warp set
+// its speed: kBatch parts x kSlices slices at once, and the first batch goes
+// out beside the LSEs, before the weights are known (a row whose weight turns
+// out 0 is not summed; every part slot below P lies in the buffer).
 constexpr int kMergeSlice = 32;  // float4 columns of a slice
+template <int kSlices, int kBatch>
 __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, long long ostride,
                                           const float* __restrict__ l, long long lstride, int Dv, int c0,
                                           float* out_f32, __nv_bfloat16* out_bf16, float* out_lse) {
   const int lane = threadIdx.x & 31;
+  auto col = [&](int sl) { return c0 + kMergeSlice * sl + lane; };
+  auto active = [&](int sl) { return col(sl) < Dv / 4; };  // lanes past the row's end skip loads and stores
+  auto row = [&](int p, int sl) { return reinterpret_cast<const float4*>(o + (long long)p * ostride)[col(sl)]; };
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 x[kBatch][kSlices];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+    for (int sl = 0; sl < kSlices; ++sl) x[k][sl] = k < P && active(sl) ? row(k, sl) : zero;
   float g = -INFINITY;
   for (int p = lane; p < P; p += 32) g = fmaxf(g, l[p * lstride]);
 #pragma unroll
@@ -108,52 +124,56 @@ __device__ __forceinline__ void merge_row(int P, const float* __restrict__ o, lo
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) z += __shfl_xor_sync(0xffffffffu, z, d);
   const float inv = any ? 1.f / z : 0.f;
-  // Every lane runs every iteration (the weights travel by warp shuffles);
-  // lanes past the row's end only skip their loads and stores.
-  {
-    const int c = c0 + lane;
-    const bool active = c < Dv / 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p0 = 0; p0 < P; p0 += 32) {
-      const float wl = p0 == 0 ? w0 : p0 == 32 ? w1 : weight(p0 + lane);
-      const int np = min(32, P - p0);
-      // kBatch parts' loads in flight before they are summed (in order)
-      constexpr int kBatch = 8;
-      for (int u0 = 0; u0 < np; u0 += kBatch) {
-        float w[kBatch];
-        float4 x[kBatch];
+  // every lane runs every iteration (the weights travel by warp shuffles)
+  float4 acc[kSlices];
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          w[k] = __shfl_sync(0xffffffffu, wl, (u0 + k) & 31);
-          const bool use = active && u0 + k < np && w[k] != 0.f;
-          x[k] = use ? reinterpret_cast<const float4*>(o + (long long)(p0 + u0 + k) * ostride)[c]
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!use) w[k] = 0.f;
-        }
+  for (int sl = 0; sl < kSlices; ++sl) acc[sl] = zero;
+  for (int p0 = 0; p0 < P; p0 += 32) {
+    const float wl = p0 == 0 ? w0 : p0 == 32 ? w1 : weight(p0 + lane);
+    const int np = min(32, P - p0);
+    for (int u0 = 0; u0 < np; u0 += kBatch) {
+      float w[kBatch];
+      const bool loaded = p0 + u0 == 0;  // the first batch is in x already
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          if (w[k] != 0.f) {
-            acc.x += w[k] * x[k].x;
-            acc.y += w[k] * x[k].y;
-            acc.z += w[k] * x[k].z;
-            acc.w += w[k] * x[k].w;
+      for (int k = 0; k < kBatch; ++k) {
+        w[k] = __shfl_sync(0xffffffffu, wl, (u0 + k) & 31);
+        const bool use = u0 + k < np && w[k] != 0.f;
+        if (!loaded)
+#pragma unroll
+          for (int sl = 0; sl < kSlices; ++sl) x[k][sl] = use && active(sl) ? row(p0 + u0 + k, sl) : zero;
+        if (!use) w[k] = 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (w[k] != 0.f) {
+#pragma unroll
+          for (int sl = 0; sl < kSlices; ++sl) {
+            acc[sl].x += w[k] * x[k][sl].x;
+            acc[sl].y += w[k] * x[k][sl].y;
+            acc[sl].z += w[k] * x[k][sl].z;
+            acc[sl].w += w[k] * x[k][sl].w;
           }
         }
       }
     }
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
-    if (active && out_f32) {
-      reinterpret_cast<float4*>(out_f32)[c] = acc;
-    } else if (active) {
-      __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 b = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+#pragma unroll
+  for (int sl = 0; sl < kSlices; ++sl) {
+    float4 a4 = acc[sl];
+    a4.x *= inv;
+    a4.y *= inv;
+    a4.z *= inv;
+    a4.w *= inv;
+    if (!active(sl)) continue;
+    if (out_f32) {
+      reinterpret_cast<float4*>(out_f32)[col(sl)] = a4;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(a4.x, a4.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(a4.z, a4.w);
       uint2 u;
       u.x = *reinterpret_cast<unsigned*>(&a);
       u.y = *reinterpret_cast<unsigned*>(&b);
-      reinterpret_cast<uint2*>(out_bf16)[c] = u;
+      reinterpret_cast<uint2*>(out_bf16)[col(sl)] = u;
     }
   }
   if (out_lse && c0 == 0 && lane == 0) *out_lse = any ? g + logf(z) : -INFINITY;
@@ -166,7 +186,7 @@ __global__ void lse_merge_kernel(int P, long long NH, int Dv, const float* __res
   if (i >= NH) return;
   float* of = o_bf16 ? nullptr : static_cast<float*>(o) + i * Dv;
   __nv_bfloat16* ob = o_bf16 ? static_cast<__nv_bfloat16*>(o) + i * Dv : nullptr;
-  merge_row(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, blockIdx.y * kMergeSlice, of, ob,
+  merge_row<1, 8>(P, o_part + i * Dv, NH * Dv, lse_part + i, NH, Dv, blockIdx.y * kMergeSlice, of, ob,
             lse ? lse + i : nullptr);
 }
 
@@ -208,10 +228,14 @@ __global__ void merge_runs_kernel(const int32_t* __restrict__ list, int n_list, 
   const long long ob = (long long)b * H + h;
   float* of = o_bf16 ? nullptr : static_cast<float*>(o) + ob * Dv;
   __nv_bfloat16* obf = o_bf16 ? static_cast<__nv_bfloat16*>(o) + ob * Dv : nullptr;
-  merge_row(n, ws_o + ((long long)first * H + h) * Dv, (long long)H * Dv, ws_lse + (long long)first * H + h, H,
+  merge_row<1, 8>(n, ws_o + ((long long)first * H + h) * Dv, (long long)H * Dv, ws_lse + (long long)first * H + h, H,
             Dv, blockIdx.y * kMergeSlice, of, obf, lse + ob);
 }
 
+// A split pair holds few parts (2 or 3 at most worker counts): a warp takes
+// kSlices slices of its row, so that each warp has kBatch x kSlices loads in
+// flight and the launch fewer rounds of the load chain.
+template <int kSlices, int kBatch>
 __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int off_pair,
                                     int off_split, int n_split, int H, int Dv,
                                     const float* __restrict__ ws_o, const float* __restrict__ ws_lse,
@@ -222,13 +246,15 @@ __global__ void decode_fixup_kernel(const int32_t* __restrict__ plan, int B, int
   const int pair = plan[off_split + s];
   const cp_pair_desc d = reinterpret_cast<const cp_pair_desc*>(plan + off_pair)[pair];
   const long long ob = (long long)pair * H + h;
-  merge_row(d.n_parts, ws_o + ((long long)d.first_part * H + h) * Dv, (long long)H * Dv,
-            ws_lse + (long long)d.first_part * H + h, H, Dv, blockIdx.y * kMergeSlice, o_part + ob * Dv,
-            nullptr, lse_part + ob);
+  merge_row<kSlices, kBatch>(d.n_parts, ws_o + ((long long)d.first_part * H + h) * Dv, (long long)H * Dv,
+                             ws_lse + (long long)d.first_part * H + h, H, Dv, blockIdx.y * kSlices * kMergeSlice,
+                             o_part + ob * Dv, nullptr, lse_part + ob);
 }
 
-// the 128-dim slices of a row of Dv dims
-unsigned merge_slices(int Dv) { return (unsigned)((Dv / 4 + kMergeSlice - 1) / kMergeSlice); }
+// the groups of kSlices 128-dim slices of a row of Dv dims
+unsigned merge_slices(int Dv, int kSlices = 1) {
+  return (unsigned)((Dv / 4 + kSlices * kMergeSlice - 1) / (kSlices * kMergeSlice));
+}
 
 }  // namespace
 
@@ -303,9 +329,13 @@ cudaError_t launch_decode_fixup(const int32_t* dev_plan, const cp_plan_header& h
   const long long n = (long long)h.n_split * H;
   if (n == 0) return cudaSuccess;
   const int warps = 8;
-  const dim3 grid((unsigned)((n + warps - 1) / warps), merge_slices(Dv));
-  decode_fixup_kernel<<<grid, warps * 32, 0, s>>>(
-      dev_plan, h.R, h.off_rank, h.off_rtile, h.n_split, H, Dv, ws_o, ws_lse, o_part, lse_part);
+  const unsigned blocks = (unsigned)((n + warps - 1) / warps);
+  if (Dv >= 4 * 4 * kMergeSlice)  // rows of 512 dims and more: four slices per warp
+    decode_fixup_kernel<4, 4><<<dim3(blocks, merge_slices(Dv, 4)), warps * 32, 0, s>>>(
+        dev_plan, h.R, h.off_rank, h.off_rtile, h.n_split, H, Dv, ws_o, ws_lse, o_part, lse_part);
+  else
+    decode_fixup_kernel<1, 8><<<dim3(blocks, merge_slices(Dv)), warps * 32, 0, s>>>(
+        dev_plan, h.R, h.off_rank, h.off_rtile, h.n_split, H, Dv, ws_o, ws_lse, o_part, lse_part);
   return cudaGetLastError();
 }
 
