@@ -49,6 +49,7 @@ constexpr int kWarpMma = kSoftmaxWarps + 1;
 constexpr int kLaunchBoundThreads = 640;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max when it grows by > 2^8
+constexpr float kSpecSum = 64.f * 256.f;  // a half row's P sum that may hide a P above 2^8
 
 template <int D>
 struct Cfg {
@@ -216,21 +217,11 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
       const float thr = kRescaleLog2 / sl2;  // threshold in raw score units
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int j = 0; j < n_t && ok; ++j) {
-        const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns,
-                                                           &abort_flag));
-        // Both warps of these rows leave together: one that gave up meets the
-        // other at this vote.
-        if (bar_red_or(pbar, 64, !got)) {
-          if (!got) report_timeout(p.status, 1, &abort_flag);
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // This half of the S row to registers (one wait); P overwrites only
-        // these columns, so the two halves never touch each other's S.
+      // this half of the S row to registers, masked past the row's position
+      // (P overwrites only these columns, so the two halves never touch each
+      // other's S)
+      auto load_s = [&](int j, uint32_t (&sr)[64]) {
         const int kbase = j * BN + 64 * half;
-        uint32_t sr[64];
         tmem_ld32(lane_addr + colS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(lane_addr + colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
@@ -239,23 +230,63 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           for (int e = 0; e < 64; ++e)
             if (kbase + e > pos) sr[e] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+      };
+      // P = 2^(s c - m c) as bf16 pairs; returns this half's sum of P
+      auto exps = [&](const uint32_t (&sr)[64], uint32_t (&pk)[32]) -> float {
+        const float neg = -m_used * sl2;
+        float s0sum = 0.f, s1sum = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx = fmax3(mx, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
-        // The running max moves on the first tile and when a row's max grows by
-        // more than 2^8: the halves exchange maxima so both move it together.
-        if (bar_red_or(pbar, 64, j == 0 || mx > m_used + thr)) {
+        for (int e = 0; e < 32; ++e) {
+          const float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+          float u0, u1;
+          fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
+          const float p0 = ex2(u0), p1 = ex2(u1);
+          add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        return s0sum + s1sum;
+      };
+      for (int j = 0; j < n_t && ok; ++j) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns,
+                                                           &abort_flag));
+        tc_fence_after();
+        uint32_t sr[64], pk[32];
+        float part = 0.f;
+        bool slow = j == 0;
+        if (j > 0) {
+          // P with the running max as it stands, before anything is known of
+          // this tile's maxima: a half whose P sums past 64 x 2^8 holds a P
+          // above 2^8, its max passed the running max by more than 2^8 (NaN
+          // counts as that too), and the row takes the exact path below.  Else
+          // every P of the row is at most 2^14 and the running max stays.  (S
+          // of a warp that gave up is read but never used.)
+          load_s(j, sr);
+          part = exps(sr, pk);
+          slow = bar_red_or(pbar, 64, !got || !(part <= kSpecSum));
+        }
+        if (slow) {
+          // Both warps of these rows leave together: one that gave up meets
+          // the other at this vote.
+          if (bar_red_or(pbar, 64, !got)) {
+            if (!got) report_timeout(p.status, 1, &abort_flag);
+            ok = false;
+            break;
+          }
+          load_s(j, sr);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mx = fmax3(mx, __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+          // The running max is the first tile's row max, and moves when a row's
+          // max grows by more than 2^8: the halves exchange maxima so both move
+          // it together.
           const float mrow = fmaxf(mx, exchange(mx));
           if (j == 0) {
             m_used = mrow;
-          } else {
-            const bool need = mrow > m_used + thr;
-            const float alpha = need ? ex2((m_used - mrow) * sl2) : 1.f;
-            if (need) {
-              l *= alpha;
-              m_used = mrow;
-            }
+          } else if (mrow > m_used + thr) {
+            const float alpha = ex2((m_used - mrow) * sl2);
+            l *= alpha;
+            m_used = mrow;
             // rescale this half of O_t once its previous P V product has landed
             const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1,
                                                                   p.wait_ns, &abort_flag));
@@ -275,26 +306,12 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
               tmem_st16(lane_addr + colO + c * 16, r);
             }
           }
+          part = exps(sr, pk);
         }
-        // P = 2^(s c - m c) as bf16 pairs over this half's first 32 columns of S
-        const float neg = -m_used * sl2;
-        float s0sum = 0.f, s1sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t q16[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float s0 = __uint_as_float(sr[32 * c + 2 * e]);
-            const float s1 = __uint_as_float(sr[32 * c + 2 * e + 1]);
-            float u0, u1;
-            fma2(u0, u1, s0, s1, sl2, sl2, neg, neg);
-            const float p0 = ex2(u0), p1 = ex2(u1);
-            add2(s0sum, s1sum, s0sum, s1sum, p0, p1);
-            q16[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(lane_addr + colS + c * 16, q16);
-        }
-        l += s0sum + s1sum;
+        l += part;
+        // P over this half's first 32 columns of S
+        tmem_st16(lane_addr + colS, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(lane_addr + colS + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p[t]));
@@ -446,6 +463,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           ok = false;
           break;
         }
+        bool haveK = false;  // K_{j+1} waited for already (by tile 0)
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t ? nkv1 : nkv0;
           if (j >= nt) continue;
@@ -457,12 +475,17 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           tc_fence_after();
           issue_pv(t, uV, j > 0);
           if (j + 1 < nt) {
-            if (!wait_full(uK)) {
-              fail(16);
-              ok = false;
-              break;
+            // a wait costs the issue loop ~140 clk even on a completed phase,
+            // and the tensor pipe runs dry meanwhile: wait for K_{j+1} once
+            if (!haveK) {
+              if (!wait_full(uK)) {
+                fail(16);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              haveK = true;
             }
-            tc_fence_after();
             issue_s(t, uK);
           }
         }
