@@ -121,7 +121,13 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                    // two Q tiles
   uint8_t* sKV = smem + 2 * C::kQBytes;  // K/V slot ring
-  __shared__ __align__(8) uint64_t bar_full[C::kSlots], bar_empty[C::kSlots];
+  // Loads go out in units that one wait covers: unit 0 = K_0, unit k = {V_(k-1), K_k},
+  // unit nK = V_(nK-1); unit k completes bar_unit[k % kUnitBars].  A barrier
+  // comes round again for unit k + kSlots, whose slots last held K/V tiles
+  // k + 2 or later: freed by products the MMA thread issued after it waited
+  // for unit k + 2, so no phase completes before the one waited for.
+  constexpr int kUnitBars = C::kSlots;
+  __shared__ __align__(8) uint64_t bar_unit[kUnitBars], bar_empty[C::kSlots];
   __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_never, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -141,10 +147,8 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   const int nK = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
-    }
+    for (int s = 0; s < C::kSlots; ++s) mbar_init(smem_u32(&bar_empty[s]), 1);
+    for (int s = 0; s < kUnitBars; ++s) mbar_init(smem_u32(&bar_unit[s]), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 2 * BM);
       mbar_init(smem_u32(&bar_s[t]), 1);
@@ -353,32 +357,37 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     // ------------------------------------------------------------ TMA producer
     // The warp runs the loop; one elected lane issues the copies.
     {
-      int last_round[C::kSlots];
-#pragma unroll
-      for (int s = 0; s < C::kSlots; ++s) last_round[s] = -1;
-      for (int u = 0; u < 2 * nK; ++u) {
-        const int j = u >> 1, slot = u % C::kSlots, round = u / C::kSlots;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1,
-                                               p.wait_ns, &abort_flag))) {
-          if (lane == 0) report_timeout(p.status, 4, &abort_flag);
-          break;
+      int last_unit = -1;
+      bool ok = true;
+      for (int k = 0; k <= nK && nK > 0 && ok; ++k) {
+        // load u = 2j (K_j) or 2j + 1 (V_j) goes to slot u % kSlots
+        const int u0 = k == 0 ? 0 : 2 * k - 1, u1 = k == nK ? 2 * k - 1 : 2 * k;
+        for (int u = u0; u <= u1 && ok; ++u) {
+          const int slot = u % C::kSlots, round = u / C::kSlots;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1,
+                                                 p.wait_ns, &abort_flag))) {
+            if (lane == 0) report_timeout(p.status, 4, &abort_flag);
+            ok = false;
+          }
         }
-        const uint32_t full = smem_u32(&bar_full[slot]);
-        const uint32_t dst = smem_u32(sKV + slot * C::kSlotBytes);
-        const CUtensorMap* map = (u & 1) ? &vmap : &kmap;
+        if (!ok) break;
+        const uint32_t full = smem_u32(&bar_unit[k % kUnitBars]);
         if (elect_one()) {
-          mbar_expect_tx(full, C::kSlotBytes);
+          mbar_expect_tx(full, (u1 - u0 + 1) * C::kSlotBytes);
+          for (int u = u0; u <= u1; ++u) {
+            const uint32_t dst = smem_u32(sKV + (u % C::kSlots) * C::kSlotBytes);
+            const CUtensorMap* map = (u & 1) ? &vmap : &kmap;
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(dst + c * (BN * 128), map, c * 64, g, sg.kv_base + j * BN, full);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(dst + c * (BN * 128), map, c * 64, g, sg.kv_base + (u >> 1) * BN, full);
+          }
         }
         __syncwarp();
-        last_round[slot] = round;
+        last_unit = k;
       }
-      // Never leave with a copy in flight: wait for the last load of every slot.
-      for (int s = 0; s < C::kSlots; ++s)
-        if (last_round[s] >= 0)
-          mbar_wait(smem_u32(&bar_full[s]), last_round[s] & 1, 1000000000ull, &zero_flag);
+      // Never leave with a copy in flight: wait for the last unit of every barrier.
+      for (int k = max(0, last_unit - kUnitBars + 1); k <= last_unit; ++k)
+        mbar_wait(smem_u32(&bar_unit[k % kUnitBars]), (k / kUnitBars) & 1, 1000000000ull, &zero_flag);
       __syncwarp();
     }
   } else {
@@ -395,8 +404,8 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
       auto wait_all = [&](uint32_t bar, uint32_t parity) {
         return __all_sync(kAll, mbar_wait(bar, parity, p.wait_ns, &abort_flag));
       };
-      auto wait_full = [&](int u) -> bool {
-        return wait_all(smem_u32(&bar_full[u % C::kSlots]), (u / C::kSlots) & 1);
+      auto wait_unit = [&](int k) -> bool {
+        return wait_all(smem_u32(&bar_unit[k % kUnitBars]), (k / kUnitBars) & 1);
       };
       auto commit = [&](uint64_t* bar) {
         if (elect_one()) mma_commit(smem_u32(bar));
@@ -446,7 +455,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           ok = false;
         }
       if (ok && nK > 0) {
-        if (!wait_full(0)) {
+        if (!wait_unit(0)) {
           fail(12);
           ok = false;
         } else {
@@ -458,12 +467,13 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
       }
       for (int j = 0; j < nK && ok; ++j) {
         const int uV = 2 * j + 1, uK = 2 * j + 2;
-        if (!wait_full(uV)) {
+        // V_j and K_{j+1} with one wait: a wait costs the issue loop ~140 clk
+        // even on a completed phase, and the tensor pipe runs dry meanwhile
+        if (!wait_unit(j + 1)) {
           fail(13);
           ok = false;
           break;
         }
-        bool haveK = false;  // K_{j+1} waited for already (by tile 0)
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t ? nkv1 : nkv0;
           if (j >= nt) continue;
@@ -474,20 +484,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           }
           tc_fence_after();
           issue_pv(t, uV, j > 0);
-          if (j + 1 < nt) {
-            // a wait costs the issue loop ~140 clk even on a completed phase,
-            // and the tensor pipe runs dry meanwhile: wait for K_{j+1} once
-            if (!haveK) {
-              if (!wait_full(uK)) {
-                fail(16);
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              haveK = true;
-            }
-            issue_s(t, uK);
-          }
+          if (j + 1 < nt) issue_s(t, uK);
         }
         if (!ok) break;
         commit(&bar_empty[uV % C::kSlots]);
