@@ -127,7 +127,12 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   // k + 2 or later: freed by products the MMA thread issued after it waited
   // for unit k + 2, so no phase completes before the one waited for.
   constexpr int kUnitBars = C::kSlots;
-  __shared__ __align__(8) uint64_t bar_unit[kUnitBars], bar_empty[C::kSlots];
+  // Slots are freed by one commit per step: release 0 after the first S
+  // products (K_0), release j + 1 after step j's products (V_j, K_(j+1)), on
+  // bar_rel[r % kSlots].  The TMA warp waits for the release of load u -
+  // kSlots, about step u / 2 - kSlots / 2, while the MMA thread cannot pass
+  // the unit it loads: no release barrier completes twice unobserved.
+  __shared__ __align__(8) uint64_t bar_unit[kUnitBars], bar_rel[C::kSlots];
   __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_never, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -147,7 +152,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   const int nK = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kSlots; ++s) mbar_init(smem_u32(&bar_empty[s]), 1);
+    for (int s = 0; s < C::kSlots; ++s) mbar_init(smem_u32(&bar_rel[s]), 1);
     for (int s = 0; s < kUnitBars; ++s) mbar_init(smem_u32(&bar_unit[s]), 1);
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 2 * BM);
@@ -363,8 +368,9 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
         // load u = 2j (K_j) or 2j + 1 (V_j) goes to slot u % kSlots
         const int u0 = k == 0 ? 0 : 2 * k - 1, u1 = k == nK ? 2 * k - 1 : 2 * k;
         for (int u = u0; u <= u1 && ok; ++u) {
-          const int slot = u % C::kSlots, round = u / C::kSlots;
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_empty[slot]), (round & 1) ^ 1,
+          if (u < C::kSlots) continue;  // the slot's first load
+          const int r = (u - C::kSlots + 1) >> 1;  // the release of load u - kSlots
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_rel[r % C::kSlots]), (r / C::kSlots) & 1,
                                                  p.wait_ns, &abort_flag))) {
             if (lane == 0) report_timeout(p.status, 4, &abort_flag);
             ok = false;
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           tc_fence_after();
           if (nkv0 > 0) issue_s(0, 0);
           if (nkv1 > 0) issue_s(1, 0);
-          commit(&bar_empty[0]);
+          commit(&bar_rel[0]);
         }
       }
       for (int j = 0; j < nK && ok; ++j) {
@@ -487,8 +493,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           if (j + 1 < nt) issue_s(t, uK);
         }
         if (!ok) break;
-        commit(&bar_empty[uV % C::kSlots]);
-        if (j + 1 < nK) commit(&bar_empty[uK % C::kSlots]);
+        commit(&bar_rel[(j + 1) % C::kSlots]);  // frees V_j and K_(j+1)
       }
       // Never free TMEM under a running MMA: wait for everything issued.
       commit(&bar_drain);
