@@ -47,23 +47,23 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "df3c47221f9a4778217bee17d5d95d14f5eea68b", "bytes": 2.373758e9 + 0.275600e9},
+                "sha1": "6db7f57830fd80e52f2d0cd948567ed81a3311b9", "bytes": 2.307813e9 + 0.288180e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                   "sha1": "7501f84c4ada68b34b362adafb9d101b145321ff",
-                   "bytes_per_token": (0.611987e9 + 0.009694e9) / (8 * 131072)},
+                   "sha1": "c9efc8882c264cf544b88b58756f4d6698949a1b",
+                   "bytes_per_token": (0.610205e9 + 0.009656e9) / (8 * 131072)},
     "decode_bf16": {"src": ["context_long_attention_gb300/csrc/decode_mla_tc.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                    "sha1": "04100416602e6fe976f64f3844df844162af152b",
-                    "bytes_per_token": (1.208702e9 + 0.011389e9) / (8 * 131072)},
+                    "sha1": "4998f17b89e397c6fa2724adb688bda380f3b834",
+                    "bytes_per_token": (1.208675e9 + 0.010585e9) / (8 * 131072)},
     "decode_gqa": {"src": ["context_long_attention_gb300/csrc/decode_gqa_tc.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                    "sha1": "66afd4cc6ca2416d3262e0e21695f9dcf534f72c",
                    "bytes_per_token": (2.147824e9 + 0.006298e9) / (4 * 131072)},
     "decode_fp8_merged": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                                   "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                          "sha1": "7501f84c4ada68b34b362adafb9d101b145321ff",
-                          "bytes_per_token": (0.609247e9 + 0.003282e9) / (8 * 131072)},
+                          "sha1": "c9efc8882c264cf544b88b58756f4d6698949a1b",
+                          "bytes_per_token": (0.609321e9 + 0.000153e9) / (8 * 131072)},
     "decode_gqa8": {"src": ["context_long_attention_gb300/csrc/decode_gqa_f8.cu",
                             "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                     "sha1": "c19956b2693cf34223e556901c4c0d1891584060",

@@ -12,9 +12,12 @@
 //               (w / 4) % 2, columns [64 h, 64 h + 64) of S and dims
 //               [D/2 h, D/2 h + D/2) of O with h = w / 8 (four softmax warps
 //               per SM sub-partition hide each other's latency)
-//   warp 16     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring
+//   warp 16     TMA producer: K_j, V_j tiles [128 keys x D] into a slot ring,
+//               V_(j-1) and K_j as one unit under one barrier
 //   warp 17     MMA issuer (one elected lane; the warp runs the loop) and
-//               TMEM owner
+//               TMEM owner.  Each of its mbarrier waits leaves the tensor
+//               pipe idle (the pipe takes few products ahead), so a step has
+//               three: the K/V unit and the two tiles' P.
 // TMEM (512 columns): tile t holds S_t = Q_t K_j^T in columns [256t, 256t+128)
 // and its output accumulator O_t in [256t+128, 256t+128+D).  Each half of a
 // row writes its P (bf16 pairs) over the first 32 of its own 64 S columns,
@@ -22,7 +25,8 @@
 // two M tiles so that one tile's softmax overlaps the other tile's matrix
 // products.  The running max used in the exponentials only moves when a
 // row's max grows by more than 2^8 (the two halves of the row exchange their
-// maxima then, and O is rescaled); the result is exact either way because
+// maxima then, and O is rescaled); P is first computed with the max as it
+// stands and recomputed only then.  The result is exact either way because
 // O = sum_t exp(s_t - m) v_t / sum_t exp(s_t - m) holds for any m.
 #include <cuda.h>
 #include <cuda_bf16.h>
