@@ -17,7 +17,10 @@
 //   warp 17     MMA issuer (one elected lane; the warp runs the loop) and
 //               TMEM owner.  Each of its mbarrier waits leaves the tensor
 //               pipe idle (the pipe takes few products ahead), so a step has
-//               three: the K/V unit and the two tiles' P.
+//               two: the two tiles' P
+//   warp 18     relay: one more arrival on each tile's P barrier per step,
+//               once the step's K/V unit has landed, so the wait for P
+//               covers the unit; the slots are freed by a softmax thread
 // TMEM (512 columns): tile t holds S_t = Q_t K_j^T in columns [256t, 256t+128)
 // and its output accumulator O_t in [256t+128, 256t+128+D).  Each half of a
 // row writes its P (bf16 pairs) over the first 32 of its own 64 S columns,
@@ -45,11 +48,12 @@ using namespace tc;
 constexpr int BM = 128;        // query rows per M tile
 constexpr int BN = 128;        // keys per K/V tile
 constexpr int kSoftmaxWarps = 16;                 // two per row quarter of each M tile
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);  // + TMA warp + MMA warp
+constexpr int kThreads = 32 * (kSoftmaxWarps + 3);  // + TMA warp + MMA warp + relay warp
 constexpr int kWarpTma = kSoftmaxWarps;
 constexpr int kWarpMma = kSoftmaxWarps + 1;
-// Registers are capped as for five warps per SM sub-partition (warps 16, 17
-// share sub-partitions 0 and 1 with four softmax warps each).
+constexpr int kWarpRelay = kSoftmaxWarps + 2;
+// Registers are capped as for five warps per SM sub-partition (warps 16-18
+// share sub-partitions 0-2 with four softmax warps each).
 constexpr int kLaunchBoundThreads = 640;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // move the running max when it grows by > 2^8
@@ -131,11 +135,14 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   // k + 2 or later: freed by products the MMA thread issued after it waited
   // for unit k + 2, so no phase completes before the one waited for.
   constexpr int kUnitBars = C::kSlots;
-  // Slots are freed by one commit per step: release 0 after the first S
-  // products (K_0), release j + 1 after step j's products (V_j, K_(j+1)), on
-  // bar_rel[r % kSlots].  The TMA warp waits for the release of load u -
-  // kSlots, about step u / 2 - kSlots / 2, while the MMA thread cannot pass
-  // the unit it loads: no release barrier completes twice unobserved.
+  // Slots are freed once per step: release j frees V_(j-1) and K_j (release
+  // 0: K_0), on bar_rel[j % kSlots].  The last product the MMA thread issues
+  // before tile rt's S_j is that of step j - 1, so one softmax thread of tile
+  // rt (the tile that runs every step) arrives there when it sees S_j
+  // complete: the issuing thread spends no commit on it.  The TMA warp waits
+  // for the release of load u - kSlots, about step u / 2 - kSlots / 2, while
+  // the MMA thread cannot pass the unit it loads: no release barrier
+  // completes twice unobserved.
   __shared__ __align__(8) uint64_t bar_unit[kUnitBars], bar_rel[C::kSlots];
   __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_never, bar_drain;
   __shared__ uint32_t tmem_slot;
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bar_q[t]), 2 * BM);
       mbar_init(smem_u32(&bar_s[t]), 1);
-      mbar_init(smem_u32(&bar_p[t]), 2 * BM);
+      mbar_init(smem_u32(&bar_p[t]), 2 * BM + 1);  // + the relay warp
       mbar_init(smem_u32(&bar_o[t]), 1);
     }
     mbar_init(smem_u32(&bar_never), 1);
@@ -196,6 +203,8 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
     const uint32_t colS = t * 256 + 64 * half, colO = t * 256 + 128 + (D / 2) * half;
     const int rows_t = t ? rows1 : rows0;
     const bool valid = i < rows_t;
+    // the thread that frees K/V slots (bar_rel): tile 1 runs every step when it has rows
+    const bool releaser = t == (rows1 > 0 ? 1 : 0) && quarter == 0 && half == 0;
     // value of the other half of this row
     auto exchange = [&](float v) -> float {
       tmem_st1(lane_addr + t * 256 + 64 * half + 63, __float_as_uint(v));
@@ -262,6 +271,7 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
       for (int j = 0; j < n_t && ok; ++j) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_s[t]), j & 1, p.wait_ns,
                                                            &abort_flag));
+        if (got && releaser && lane == 0) mbar_arrive(smem_u32(&bar_rel[j % C::kSlots]));
         tc_fence_after();
         uint32_t sr[64], pk[32];
         float part = 0.f;
@@ -400,6 +410,28 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
         mbar_wait(smem_u32(&bar_unit[k % kUnitBars]), (k / kUnitBars) & 1, 1000000000ull, &zero_flag);
       __syncwarp();
     }
+  } else if (warp == kWarpRelay) {
+    // ------------------------------------------------------------ relay
+    // P_j of tile t completes only once V_j and K_(j+1) have landed: this warp
+    // adds one arrival per step to bar_p[t] after their unit is in and the
+    // barrier's previous phase (step j - 1) is over, so the MMA thread's wait
+    // for P_j covers the unit.  (A wait costs the issuing thread ~140 clk even
+    // on a completed phase, and the tensor pipe runs dry meanwhile.)  Phase j
+    // cannot complete before this arrival, so the wait for phase j - 1 never
+    // sees two phases pass.
+    bool ok = true;
+    for (int j = 0; j < nK && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_unit[(j + 1) % kUnitBars]),
+                                             ((j + 1) / kUnitBars) & 1, p.wait_ns, &abort_flag));
+      for (int t = 0; t < 2 && ok; ++t) {
+        if (j >= (t ? nkv1 : nkv0)) continue;
+        if (j > 0)
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_p[t]), (j - 1) & 1, p.wait_ns, &abort_flag));
+        if (ok && lane == 0) mbar_arrive(smem_u32(&bar_p[t]));
+        __syncwarp();
+      }
+      if (!ok && lane == 0) report_timeout(p.status, 17, &abort_flag);
+    }
   } else {
     // ------------------------------------------------------------ MMA issuer
     // The warp runs the loop so that descriptors stay warp-uniform; one elected
@@ -472,18 +504,12 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           tc_fence_after();
           if (nkv0 > 0) issue_s(0, 0);
           if (nkv1 > 0) issue_s(1, 0);
-          commit(&bar_rel[0]);
         }
       }
       for (int j = 0; j < nK && ok; ++j) {
         const int uV = 2 * j + 1, uK = 2 * j + 2;
-        // V_j and K_{j+1} with one wait: a wait costs the issue loop ~140 clk
-        // even on a completed phase, and the tensor pipe runs dry meanwhile
-        if (!wait_unit(j + 1)) {
-          fail(13);
-          ok = false;
-          break;
-        }
+        // V_j and K_(j+1) are in place once a tile's P_j has completed (the
+        // relay warp's arrival)
         for (int t = 0; t < 2 && ok; ++t) {
           const int nt = t ? nkv1 : nkv0;
           if (j >= nt) continue;
@@ -497,7 +523,6 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           if (j + 1 < nt) issue_s(t, uK);
         }
         if (!ok) break;
-        commit(&bar_rel[(j + 1) % C::kSlots]);  // frees V_j and K_(j+1)
       }
       // Never free TMEM under a running MMA: wait for everything issued.
       commit(&bar_drain);
