@@ -150,7 +150,12 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   __shared__ volatile int zero_flag;  // never set: drains ignore the abort flag
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile_i = blockIdx.x / p.Hq, h = blockIdx.x % p.Hq;
+  // CTAs go kv head by kv head (each head's tiles longest first, the q heads
+  // of its group side by side): the CTAs in flight then read one kv head's
+  // K/V, which the L2 holds, instead of all of them
+  const int per_g = p.n_tiles * p.group;
+  const int gi = blockIdx.x / per_g, rem = blockIdx.x - gi * per_g;
+  const int tile_i = rem / p.group, h = gi * p.group + rem % p.group;
   const cp_tile_desc td = reinterpret_cast<const cp_tile_desc*>(p.plan + p.tile_list)[tile_i];
   const cp_seg_desc sg = reinterpret_cast<const cp_seg_desc*>(p.plan + p.off_seg)[td.seg];
   const int g = h / p.group;
@@ -306,10 +311,16 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           const float mrow = fmaxf(mx, exchange(mx));
           if (j == 0) {
             m_used = mrow;
-          } else if (mrow > m_used + thr) {
-            const float alpha = ex2((m_used - mrow) * sl2);
-            l *= alpha;
-            m_used = mrow;
+          } else {
+            // Each row (lane) moves its own max; the wait and the pair's barrier
+            // below are taken by every lane of both warps (a lane whose max
+            // stays scales by 1), since the vote to be here was the pair's.
+            const bool need = mrow > m_used + thr;
+            const float alpha = need ? ex2((m_used - mrow) * sl2) : 1.f;
+            if (need) {
+              l *= alpha;
+              m_used = mrow;
+            }
             // rescale this half of O_t once its previous P V product has landed
             const bool landed = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar_o[t]), (j - 1) & 1,
                                                                   p.wait_ns, &abort_flag));

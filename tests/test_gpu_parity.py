@@ -104,8 +104,11 @@ def test_device_maps_full_size(cp):
 
 
 def prefill_vs_oracle(cp, strategy, new_len, prefix_len, C, Hq, Hkv, D, dtype, seed, rows=None,
-                      tol=TOL_BF16, std=None, check_ranks=False):
-    q, k, v = W.prefill_inputs(new_len, prefix_len, Hq, Hkv, D, dtype, seed=seed, device=DEV, std=std)
+                      tol=TOL_BF16, std=None, check_ranks=False, qkv=None):
+    if qkv is None:
+        q, k, v = W.prefill_inputs(new_len, prefix_len, Hq, Hkv, D, dtype, seed=seed, device=DEV, std=std)
+    else:
+        q, k, v = (x.to(DEV) for x in qkv)
     plan = cp.cp_shard_plan(strategy, C, new_len, prefix_len, device=DEV)
     scale = 1.0 / math.sqrt(D)
     o, lse = cp.cp_prefill_attn(plan, q, k, v, scale)
@@ -160,6 +163,33 @@ def test_prefill_bf16_sharp_scores(cp, strategy):
     # larger inputs give peaked softmax rows (scores of order 10)
     prefill_vs_oracle(cp, strategy, [700, 333], [129, 0], 8, 16, 4, 128, "bf16", seed=99,
                       std=0.35)
+
+
+def scores_along_keys(T, KV, Hq, Hkv, D, slope, seed):
+    """bf16 Q, K, V whose scores move linearly along the keys: q = 4u + noise,
+    k_j = (b0 + slope j) u + noise for a unit vector u."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(D, generator=g, dtype=torch.float64)
+    u /= u.norm()
+    b = (0.0 if slope > 0 else -slope * KV) + slope * torch.arange(KV, dtype=torch.float64)
+    q = 4.0 * u + 0.3 * torch.randn(T, Hq, D, generator=g, dtype=torch.float64)
+    k = b[:, None, None] * u + 0.3 * torch.randn(KV, Hkv, D, generator=g, dtype=torch.float64)
+    v = torch.randn(KV, Hkv, D, generator=g, dtype=torch.float64)
+    return tuple(x.to(torch.bfloat16) for x in (q, k, v))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("slope", [0.25, -0.25])
+def test_prefill_bf16_scores_along_keys(cp, D, slope):
+    """Rising scores pass the running max by far more than 2^8 on every KV
+    tile (about 11 natural units per 128 keys at head dim 128), so every tile
+    takes the softmax's exact path (maxima exchanged, O rescaled) after its
+    speculative P; falling scores keep the first tile's max, so every later
+    tile keeps its speculative P."""
+    new_len, prefix_len = [1100, 300], [60, 0]
+    qkv = scores_along_keys(1400, 1460, 4, 2, D, slope, seed=31 + D)
+    prefill_vs_oracle(cp, cp.CP_ZIGZAG, new_len, prefix_len, 4, 4, 2, D, "bf16", seed=0, qkv=qkv)
+    prefill_vs_oracle(cp, cp.CP_INTERLEAVE, new_len, prefix_len, 4, 4, 2, D, "bf16", seed=0, qkv=qkv)
 
 
 def test_prefill_edge_cases(cp):
