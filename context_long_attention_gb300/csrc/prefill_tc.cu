@@ -343,9 +343,8 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
           part = exps(sr, pk);
         }
         l += part;
-        // P over this half's first 32 columns of S
-        tmem_st16(lane_addr + colS, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(lane_addr + colS + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        // P over this half's first 32 columns of S, one store
+        tmem_st32(lane_addr + colS, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&bar_p[t]));
