@@ -47,7 +47,7 @@ import cp_workloads as W  # noqa: E402
 PROFILED_TRAFFIC = {
     "prefill": {"src": ["context_long_attention_gb300/csrc/prefill_tc.cu",
                         "context_long_attention_gb300/csrc/tc_ptx.cuh"],
-                "sha1": "f622f12f0e92de6e2da0c810572f4ed69ca27525", "bytes": 0.424714e9 + 0.244750e9},
+                "sha1": "98ac8718b240f5fd25a3280da4134f23934e585d", "bytes": 0.424714e9 + 0.244750e9},
     "decode_fp8": {"src": ["context_long_attention_gb300/csrc/decode_mla_fp8.cu",
                            "context_long_attention_gb300/csrc/tc_ptx.cuh"],
                    "sha1": "c9efc8882c264cf544b88b58756f4d6698949a1b",

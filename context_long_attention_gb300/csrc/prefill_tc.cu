@@ -132,17 +132,19 @@ __global__ void __launch_bounds__(kLaunchBoundThreads, 1)
   // Loads go out in units that one wait covers: unit 0 = K_0, unit k = {V_(k-1), K_k},
   // unit nK = V_(nK-1); unit k completes bar_unit[k % kUnitBars].  A barrier
   // comes round again for unit k + kSlots, whose slots last held K/V tiles
-  // k + 2 or later: freed by products the MMA thread issued after it waited
-  // for unit k + 2, so no phase completes before the one waited for.
+  // k + 2 or later, freed only once S_(k+2) has completed; that needs
+  // P_(k+1), which the relay warp completes after it has waited for unit k
+  // (it takes the units in order; the MMA thread waits for unit 0), so no
+  // phase completes before the one waited for.
   constexpr int kUnitBars = C::kSlots;
   // Slots are freed once per step: release j frees V_(j-1) and K_j (release
   // 0: K_0), on bar_rel[j % kSlots].  The last product the MMA thread issues
   // before tile rt's S_j is that of step j - 1, so one softmax thread of tile
   // rt (the tile that runs every step) arrives there when it sees S_j
   // complete: the issuing thread spends no commit on it.  The TMA warp waits
-  // for the release of load u - kSlots, about step u / 2 - kSlots / 2, while
-  // the MMA thread cannot pass the unit it loads: no release barrier
-  // completes twice unobserved.
+  // for release r of load u - kSlots (r about u / 2 - kSlots / 2) before it
+  // loads u, while release r + kSlots needs S_(r+kSlots) and so a unit it has
+  // not loaded yet: no release barrier completes twice unobserved.
   __shared__ __align__(8) uint64_t bar_unit[kUnitBars], bar_rel[C::kSlots];
   __shared__ __align__(8) uint64_t bar_q[2], bar_s[2], bar_p[2], bar_o[2], bar_never, bar_drain;
   __shared__ uint32_t tmem_slot;
